@@ -1,0 +1,437 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA mixer core on one GB300 (or N independent replicas).
+
+Headline workload: one KDA layer, batched decode of B=256 independent
+sequences, 96 heads x 128, FP32 recurrent state (~1.6 GB, larger than L2),
+BF16 inputs/outputs. One step = one decode token for the whole batch (one
+launch of the fused decode kernel). Beside it, the chunked prefill of one
+sequence of T=8192 tokens (same geometry) is timed and reported under
+"prefill".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kda|reference]
+
+--impl reference times the FP64 CPU oracle (the only other implementation of
+this path) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA tokens/s: decode B=256 (HBM GB/s, % peak); prefill T=8192 (% TC peak)"
+H, DH, KCONV, CHUNK = 96, 128, 4, 64
+D = H * DH
+B_DEC = 256
+T_PRE = 8192
+# algorithmic bytes per (sequence, head, token) of decode with BF16 I/O:
+# state read + write, q,k,v,z,g in, b in, out, conv history read + write
+DEC_BYTES_PER_UNIT = 2 * DH * DH * 4 + 5 * DH * 2 + 2 + DH * 2 + 2 * 3 * (KCONV - 1) * DH * 2
+# algorithmic FLOPs per (token, head) of chunked prefill at C = 64: 2 (3 d^2 + 5 C d)
+PRE_FLOP_PER_TOKEN_HEAD = 2 * (3 * DH * DH + 5 * CHUNK * DH)
+# algorithmic bytes per token of prefill with BF16 I/O: q,k,v,z,g,b in, out
+PRE_BYTES_PER_TOKEN = (5 * D + H + D) * 2
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region (read-only)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.f is None:
+            return None
+        try:
+            self.f.flush()
+            rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+            os.unlink(self.f.name)
+        except Exception:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for nm, val in zip(names, r[5:9]):
+                    if val.strip().lower() == "active":
+                        reasons.add(nm)
+            except Exception:
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def _oracle_decode_sample(n_seq: int, steps: int, seed: int = 2):
+    """Time the FP64 oracle on n_seq sequences x 96 heads for `steps` decode tokens."""
+    import numpy as np
+
+    import kda_inputs as KI
+    from oracle import oracle as O
+    O.build()
+    p = KI.make_params(H, DH, KCONV, seed)
+    S_all = KI.make_state(n_seq, H, DH, seed, std=0.05).astype(np.float64)
+    tail_all = KI.make_tail(n_seq, H, DH, KCONV, seed, bf16=True).astype(np.float64)
+    tok = KI.make_tokens(n_seq * steps, H, DH, seed, bf16=True)
+    oc = O.OracleCfg(H=H, d=DH)
+    slots = np.arange(n_seq, dtype=np.int32)
+    nt = O.max_threads()
+    times = []
+    for s in range(steps):
+        rows = slice(s * n_seq, (s + 1) * n_seq)
+        t0 = time.perf_counter()
+        O.decode_batch(oc, p, S_all, tail_all, slots, {k: v[rows] for k, v in tok.items()}, nthreads=nt)
+        times.append(time.perf_counter() - t0)
+    return times, nt
+
+
+def _oracle_prefill_sample(T: int, n_heads: int, seed: int = 3):
+    import numpy as np
+
+    import kda_inputs as KI
+    from oracle import oracle as O
+    O.build()
+    p = KI.make_params(n_heads, DH, KCONV, seed)
+    tok = KI.make_tokens(T, n_heads, DH, seed, bf16=True)
+    oc = O.OracleCfg(H=n_heads, d=DH)
+    S, tail = O.new_state(oc)
+    nt = O.max_threads()
+    t0 = time.perf_counter()
+    O.sequence(oc, p, S, tail, tok, nthreads=nt)
+    return time.perf_counter() - t0, nt
+
+
+def cpu_baseline_decode(target_s: float = 12.0):
+    """Bounded sample: n_seq sequences x 96 heads, as many decode steps as fit ~target_s."""
+    n_seq = 32
+    t1, nt = _oracle_decode_sample(n_seq, 1)
+    steps = max(1, min(20, int(target_s / max(t1[0], 1e-3))))
+    times, nt = _oracle_decode_sample(n_seq, steps)
+    tot = sum(times)
+    return {"value": n_seq * steps / tot, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+            "sample": f"FP64 oracle, {steps} decode steps x {n_seq} sequences x {H} heads x {DH} "
+                      f"(B=256 workload shape), OpenMP over (sequence, head) units"}
+
+
+def cpu_baseline_prefill():
+    """Bounded sample: 1024 tokens x 8 heads of the T=8192 prefill, scaled to 96 heads."""
+    T, nh = 1024, 8
+    t, nt = _oracle_prefill_sample(T, nh)
+    return {"value": T / (t * H / nh), "unit": "tokens/s", "cores": nt, "kind": "oracle",
+            "sample": f"FP64 oracle, sequential per token, {T} tokens x {nh} heads (scaled to {H} heads), "
+                      f"OpenMP over heads"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    n_seq = 8
+    _oracle_decode_sample(n_seq, max(1, min(args.warmup, 3)))  # warm-up (untimed)
+    times, nt = _oracle_decode_sample(n_seq, args.steps)
+    tot = sum(times)
+    val = n_seq * args.steps / tot
+    line = {"metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "decode B=256, 96 heads x 128, 1 KDA layer (each step: a sample of "
+                                   f"{n_seq} sequences)", "batch": B_DEC, "heads": H, "head_dim": DH,
+                       "io_dtype": "bf16", "state_dtype": "f64"},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+                             "sample": f"FP64 oracle, {n_seq} sequences x {H} heads per step"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ CUDA arm
+
+def _fill_state_random(K, cfg, st, n_slots, gen, dev):
+    """Fill S ~ N(0, 0.05^2) and the conv history ~ N(0, 1) (BF16) through a device blob."""
+    import torch
+    sb = H * DH * DH * 4
+    tb = 3 * (KCONV - 1) * D * 2
+    blob = torch.empty(64 + n_slots * (sb + tb), dtype=torch.uint8, device=dev)
+    hdr = K.kda_blob_header()
+    hdr.magic, hdr.version = K.KDA_BLOB_MAGIC, K.KDA_BLOB_VERSION
+    hdr.num_heads, hdr.head_dim, hdr.conv_kernel, hdr.io_dtype, hdr.n_slots = H, DH, KCONV, cfg.io_dtype, n_slots
+    hdr.state_bytes_per_slot, hdr.tail_bytes_per_slot = sb, tb
+    blob[:64].copy_(torch.frombuffer(bytearray(bytes(hdr)), dtype=torch.uint8))
+    body = blob[64:].view(n_slots, sb + tb)
+    for s in range(n_slots):
+        body[s, :sb].view(torch.float32).copy_(torch.randn(sb // 4, generator=gen, device=dev) * 0.05)
+        body[s, sb:].view(torch.bfloat16).copy_(torch.randn(tb // 2, generator=gen, device=dev).to(torch.bfloat16))
+    K.kda_state_restore(st, list(range(n_slots)), blob)
+    torch.cuda.synchronize()
+    del blob
+
+
+def _params(K, gen, dev):
+    import torch
+    conv_w = (torch.randn(3, D, KCONV, generator=gen, device=dev) * 0.5).contiguous()
+    dt_bias = torch.randn(D, generator=gen, device=dev) * math.sqrt(0.5)
+    A_log = torch.rand(H, generator=gen, device=dev) * math.log(16.0)
+    norm_w = 1.0 + torch.randn(DH, generator=gen, device=dev) * math.sqrt(0.1)
+    return K.kda_layer_params_from(conv_w, dt_bias, A_log, norm_w)
+
+
+def _inputs(rows, gen, dev, dtype):
+    import torch
+    return {n: torch.randn(rows, H if n == "b" else D, generator=gen, device=dev).to(dtype).contiguous()
+            for n in ("q", "k", "v", "z", "b", "g")}
+
+
+def run_kda(args):
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from linear_attention_mixer_gb300 import build as KB
+    KB.build()
+    import linear_attention_mixer_gb300 as K
+    peaks = _peaks()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    stream = torch.cuda.current_stream()
+
+    # ---------------- decode B=256 ----------------
+    cfg = K.kda_config(H, DH, K.KDA_BF16)
+    params = _params(K, gen, dev)
+    st = K.kda_state_alloc(cfg, B_DEC)
+    _fill_state_random(K, cfg, st, B_DEC, gen, dev)
+    ring_n = 16  # 16 distinct input sets (~0.5 GB), cycled
+    ring = [_inputs(B_DEC, gen, dev, torch.bfloat16) for _ in range(ring_n)]
+    slots = torch.arange(B_DEC, dtype=torch.int32, device=dev)
+    out = torch.empty(B_DEC, D, dtype=torch.bfloat16, device=dev)
+
+    def dec_step(i):
+        x = ring[i % ring_n]
+        K.kda_decode_token(cfg, params, st, slots, x["q"], x["k"], x["v"], x["z"], x["b"], x["g"], out, stream)
+
+    for i in range(32):  # the states are further filled by random decode steps (untimed)
+        dec_step(i)
+    for i in range(args.warmup):
+        dec_step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            dec_step(i)
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    _barrier(ws)
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    assert K.kda_state_poll_error(st) == 0
+    total_ms_max = _max_over_ranks(total_ms, ws, dev)
+    tokens = B_DEC * args.steps * ws
+    value = tokens / (total_ms_max / 1e3)
+    dec_bytes = DEC_BYTES_PER_UNIT * B_DEC * H
+    achieved = dec_bytes / (launch_ms / 1e3) / 1e9
+
+    # ---------------- e2e through the public API with host buffers ----------------
+    e2e_steps = min(args.steps, 100)
+    host = [{n: t.cpu().pin_memory() for n, t in ring[j].items()} for j in range(4)]
+    dbuf = {n: torch.empty_like(t) for n, t in ring[0].items()}
+    hout = torch.empty(B_DEC, D, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step(i):
+        hx = host[i % 4]
+        for n in dbuf:
+            dbuf[n].copy_(hx[n], non_blocking=True)
+        K.kda_decode_token(cfg, params, st, slots, dbuf["q"], dbuf["k"], dbuf["v"], dbuf["z"], dbuf["b"],
+                           dbuf["g"], out, stream)
+        hout.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    e2e_val = B_DEC * e2e_steps * ws / (e2e_ms / 1e3)
+    K.kda_state_free(st)
+    del ring, host, dbuf
+    torch.cuda.empty_cache()
+
+    # ---------------- prefill T=8192 ----------------
+    pcfg = cfg
+    pst = K.kda_state_alloc(pcfg, 1)
+    px = _inputs(T_PRE, gen, dev, torch.bfloat16)
+    pout = torch.empty(T_PRE, D, dtype=torch.bfloat16, device=dev)
+    pslots = torch.zeros(1, dtype=torch.int32, device=dev)
+    cu_h = [0, T_PRE]
+    cu = torch.tensor(cu_h, dtype=torch.int32, device=dev)
+
+    def pre_call():
+        K.kda_prefill(pcfg, params, pst, pslots, cu, cu_h, px["q"], px["k"], px["v"], px["z"], px["b"], px["g"],
+                      pout, stream)
+
+    for _ in range(3):
+        K.kda_state_reset(pst, [0], stream)
+        pre_call()
+    torch.cuda.synchronize()
+    reps = args.prefill_reps
+    pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        K.kda_state_reset(pst, [0], stream)
+        pev[i][0].record(stream)
+        pre_call()
+        pev[i][1].record(stream)
+    torch.cuda.synchronize()
+    pre_ms = statistics.median(a.elapsed_time(b) for a, b in pev)
+    assert K.kda_state_poll_error(pst) == 0
+    K.kda_state_free(pst)
+    pre_flop = PRE_FLOP_PER_TOKEN_HEAD * T_PRE * H
+    pre_bytes = PRE_BYTES_PER_TOKEN * T_PRE
+    pre_tflops = pre_flop / (pre_ms / 1e3) / 1e12
+    pre_gbs = pre_bytes / (pre_ms / 1e3) / 1e9
+
+    if rank != 0:
+        return 0
+    cpu_dec = cpu_baseline_decode() if not args.no_cpu_baseline else None
+    cpu_pre = cpu_baseline_prefill() if not args.no_cpu_baseline else None
+    src = "of measured" if peaks["source"] == "measured" else "of fallback"
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "decode B=256, 96 heads x 128, 1 KDA layer", "batch": B_DEC, "heads": H,
+                   "head_dim": DH, "io_dtype": "bf16", "state_dtype": "f32",
+                   "l2": "inputs larger than L2 (1.61 GB of state per step)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "decode_kernel<bf16>",
+                     "bytes_per_launch": dec_bytes, "launch_ms": launch_ms, "peak_note": src},
+        "cpu_baseline": cpu_dec,
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "prefill": {"workload": "prefill 1 sequence T=8192, 96 heads x 128, chunk 64, BF16 I/O",
+                    "value": T_PRE / (pre_ms / 1e3), "unit": "tokens/s", "ms": pre_ms, "reps": reps,
+                    "gpu_launches_per_call": 4,
+                    "roofline_tensor": {"bound": "tensor", "achieved": pre_tflops, "peak": peaks["bf16_tflops"],
+                                        "unit": "TFLOP/s", "frac": pre_tflops / peaks["bf16_tflops"],
+                                        "flop_per_call": pre_flop, "peak_note": src},
+                    "roofline_hbm": {"bound": "hbm", "achieved": pre_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                     "frac": pre_gbs / peaks["hbm_gbs"], "bytes_per_call": pre_bytes,
+                                     "peak_note": src},
+                    "cpu_baseline": cpu_pre},
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
+    ap.add_argument("--prefill-reps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_kda(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

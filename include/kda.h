@@ -1,0 +1,217 @@
+/*
+ * kda.h - C ABI of the KDA (Kimi Delta Attention) mixer core on GB300 (sm_103a).
+ *
+ * The library computes, for every token of every sequence and every head,
+ * the KDA per-head recurrence stated in the kimi_k3.c header comment, block
+ * "KDA per-head recurrence":
+ *
+ *   q,k,v = SiLU(ShortConv4(x))              depthwise, causal, taps oldest first
+ *   q,k   = L2-normalised (eps 1e-6 inside the sqrt), q *= d^-1/2
+ *   gk    = gmin * sigmoid(exp(A_log[h]) * (z + dt_bias)),  gmin = -5,  alpha = exp(gk)
+ *   beta  = sigmoid(b)                        one scalar per head and token
+ *   S     = (I - beta k k^T) Diag(alpha) S + beta k v^T      S[key][value], FP32
+ *   o     = S^T q                             read after the update
+ *   out   = sigmoid(g) * RMSNorm_head(o)      RMSNorm weight [d], shared by all heads
+ *
+ * The W_q/W_k/W_v/W_o/W_g/W_b and decay projections stay outside: callers pass
+ * the post-projection q, k, v, the gate pre-activation z (without dt_bias), the
+ * beta logits b and the output-gate logits g.
+ *
+ * Conventions for every entry point:
+ *  - Status codes are returned; no call exits the process or traps on the GPU.
+ *    The text of the last error of the calling thread is kda_last_error().
+ *  - Argument checks happen on the host before anything is enqueued; a call
+ *    that returns an error has enqueued nothing.
+ *  - "stream" is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Work is enqueued on it and the call returns without waiting,
+ *    except where a function says it synchronises.
+ *  - The calling thread's current CUDA device must be the one the state was
+ *    allocated on.
+ *  - All tensors are dense, row-major, with the layouts given below. The caller
+ *    owns every input, output and parameter buffer; the library owns the state.
+ *  - Device pointers must be 16-byte aligned.
+ *  - Calls that use the same kda_state must be ordered (same stream, or
+ *    synchronised by the caller); the library keeps per-state workspace.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID = 1,  /* bad argument, shape or config: nothing was enqueued */
+    KDA_ERR_OOM = 2,      /* a device or host allocation failed */
+    KDA_ERR_CUDA = 3,     /* a CUDA runtime call failed (message holds cudaGetErrorString) */
+    KDA_ERR_BLOB = 4,     /* a snapshot blob has the wrong magic, version, geometry or size */
+    KDA_ERR_TIMEOUT = 5,  /* a bounded device-side wait gave up */
+    KDA_ERR_DEVICE = 6    /* a kernel recorded a bad index (see kda_state_poll_error) */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/*
+ * Mixer geometry and constants (kimi_k3.c: config parsing of
+ * "linear_attn_config" - num_heads, head_dim, short_conv_kernel_size,
+ * gate_lower_bound; the header comment gives eps 1e-6 and the d^-1/2 q scale).
+ * The RMSNorm eps is a field (default 1e-6).
+ */
+typedef struct {
+    int32_t num_heads;       /* H >= 1 */
+    int32_t head_dim;        /* d; this build supports 128 */
+    int32_t conv_kernel;     /* K; this build supports 4 */
+    int32_t io_dtype;        /* kda_dtype of q,k,v,z,b,g, out and the conv history */
+    int32_t chunk_size;      /* prefill chunk length C; this build supports 64 */
+    float gate_lower_bound;  /* gmin, default -5 */
+    float l2_eps;            /* default 1e-6 */
+    float rms_eps;           /* default 1e-6 */
+    float q_scale;           /* default d^-1/2 */
+} kda_config_t;
+
+/*
+ * Fill *cfg with the defaults above for the given geometry.
+ * Returns KDA_ERR_INVALID (cfg untouched) for cfg == NULL, num_heads < 1,
+ * head_dim != 128 or an io_dtype that is not KDA_F32/KDA_BF16.
+ */
+kda_status kda_config(kda_config_t *cfg, int32_t num_heads, int32_t head_dim, int32_t io_dtype);
+
+/*
+ * Per-layer parameters, device pointers, FP32, caller-owned (kimi_k3.c,
+ * struct Kda: conv_q/conv_k/conv_v "[proj*4] depthwise taps, oldest first",
+ * dt "dt_bias[proj]", A from A_log "[heads]", onw "o_norm[hd]").
+ *   conv_w  [3][H*d][K]   taps for q, k, v in that order; tap 0 meets the oldest input
+ *   dt_bias [H*d]
+ *   A_log   [H]           the library takes exp(A_log) itself
+ *   norm_w  [d]           RMSNorm weight shared by all heads
+ */
+typedef struct {
+    const float *conv_w;
+    const float *dt_bias;
+    const float *A_log;
+    const float *norm_w;
+} kda_layer_params;
+
+/* Opaque recurrent state for max_slots sequences. */
+typedef struct kda_state kda_state;
+
+/*
+ * Allocate device state for max_slots sequences and zero it (synchronously)
+ * (spark_model/kimi_k3/bound.rs, TransformerLayer::alloc_state ->
+ * KdaState::new; kimi_k3.c, struct Model: kstate "[heads*hd*hd], S[k][v]" and
+ * the conv windows cwq/cwk/cwv).
+ * Per slot the library holds S [H][d][d] FP32 (row = key index) and the conv
+ * history [3][K-1][H*d] in io_dtype: the last K-1 raw q, k, v inputs, oldest
+ * first. The config is copied. *out receives the handle.
+ * Errors: KDA_ERR_INVALID (NULL args, max_slots < 1, unsupported config),
+ * KDA_ERR_OOM (cudaMalloc failed; nothing leaks), KDA_ERR_CUDA.
+ */
+kda_status kda_state_alloc(const kda_config_t *cfg, int32_t max_slots, kda_state **out);
+
+/* Free the state and its workspace (spark_model/kimi_k3/bound.rs,
+ * TransformerLayer::release_state). Synchronises the device first. NULL is a no-op. */
+kda_status kda_state_free(kda_state *st);
+
+/*
+ * Zero S and the conv history of the n listed slots (host array of slot ids).
+ * Errors: KDA_ERR_INVALID for a NULL state, n < 0, slots == NULL with n > 0,
+ * or an id outside [0, max_slots).
+ */
+kda_status kda_state_reset(kda_state *st, const int32_t *slots, int32_t n, void *stream);
+
+/* Geometry accessors. kda_state_blob_bytes returns 0 for a NULL state or n_slots < 0. */
+int32_t kda_state_max_slots(const kda_state *st);
+size_t kda_state_blob_bytes(const kda_state *st, int32_t n_slots);
+
+/*
+ * Snapshot / restore of the state of n slots (spark_model/kimi_k3/bound.rs,
+ * TransformerLayer::snapshot_aux -> a byte blob, restore_aux(blob); the
+ * "decode_rollback_unsupported" comment: a prefix snapshot and an explicit
+ * restore are the only way back).
+ * Blob = kda_blob_header (64 bytes) followed, for each listed slot in order,
+ * by S [H][d][d] FP32 then the conv history [3][K-1][H*d] in io_dtype.
+ * dst/src is host memory when *_on_device == 0, else device memory; its size
+ * must be at least kda_state_blob_bytes(st, n). Copies are stream-ordered; a
+ * host destination is complete once the stream is synchronised.
+ * Restore checks magic, version, H, d, K, io_dtype and the slot count before
+ * enqueuing any copy: a mismatch returns KDA_ERR_BLOB (for a device src the
+ * header is read back synchronously).
+ */
+typedef struct {
+    uint32_t magic;      /* KDA_BLOB_MAGIC */
+    uint32_t version;    /* KDA_BLOB_VERSION */
+    int32_t num_heads, head_dim, conv_kernel, io_dtype;
+    int32_t n_slots;
+    int32_t reserved0;
+    uint64_t state_bytes_per_slot;
+    uint64_t tail_bytes_per_slot;
+    uint8_t reserved[16];
+} kda_blob_header;
+#define KDA_BLOB_MAGIC 0x3141444Bu  /* "KDA1" little-endian */
+#define KDA_BLOB_VERSION 1u
+
+kda_status kda_state_snapshot(const kda_state *st, const int32_t *slots, int32_t n,
+                              void *dst, int32_t dst_on_device, void *stream);
+kda_status kda_state_restore(kda_state *st, const int32_t *slots, int32_t n,
+                             const void *src, int32_t src_on_device, void *stream);
+
+/*
+ * One decode token for a batch of B independent sequences (kimi_k3.c header,
+ * "KDA per-head recurrence"; kimi_k3.c K3Seq/K3Row comment: a multiplexed
+ * decode step reads each row's state from its own slot).
+ *   slots   device int32 [B]: row r advances slot slots[r]; ids must be
+ *           distinct within a call (duplicates race). An id outside
+ *           [0, max_slots) skips that row and records KDA_ERR_DEVICE in the
+ *           state's error word (read it with kda_state_poll_error).
+ *   q,k,v,z,g  device [B][H*d] io_dtype;  b device [B][H] io_dtype
+ *   out     device [B][H*d] io_dtype (must not alias an input)
+ * B == 0 is a no-op. Errors: KDA_ERR_INVALID (NULL pointer, B < 0, config
+ * different from the state's), KDA_ERR_CUDA (launch failure).
+ */
+kda_status kda_decode_token(const kda_config_t *cfg, const kda_layer_params *params, kda_state *st,
+                            const int32_t *slots, int32_t B,
+                            const void *q, const void *k, const void *v, const void *z,
+                            const void *b, const void *g, void *out, void *stream);
+
+/*
+ * Prefill N variable-length sequences packed along the token axis
+ * (kimi_k3.c: K3_CHUNK "prefill chunk size"; the per-token recurrence above
+ * evaluated in chunks of C tokens with the WY/UT rewrite, which is exact in
+ * real arithmetic). Each sequence continues from its slot's current state and
+ * conv history and leaves its final state and history in the slot; nothing
+ * crosses a sequence boundary.
+ *   slots          device int32 [N], distinct (duplicates race); a bad id is
+ *                  skipped and recorded as in kda_decode_token
+ *   cu_seqlens     device int32 [N+1]; cu_seqlens_host: the same values on the host.
+ *                  cu[0] = 0, non-decreasing; sequence i is tokens [cu[i], cu[i+1]).
+ *                  Empty sequences are allowed and leave their slot unchanged.
+ *   q,k,v,z,g      device [cu[N]][H*d] io_dtype;  b device [cu[N]][H] io_dtype
+ *   out            device [cu[N]][H*d] io_dtype
+ * The library grows a per-state device workspace as needed (cudaMalloc; this
+ * call may then synchronise). Errors: KDA_ERR_INVALID (NULL pointer, N < 0,
+ * bad cu_seqlens_host, config mismatch), KDA_ERR_OOM (workspace), KDA_ERR_CUDA.
+ */
+kda_status kda_prefill(const kda_config_t *cfg, const kda_layer_params *params, kda_state *st,
+                       const int32_t *slots, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                       int32_t N,
+                       const void *q, const void *k, const void *v, const void *z,
+                       const void *b, const void *g, void *out, void *stream);
+
+/*
+ * Synchronise the device, read and clear the state's device error word.
+ * *code receives 0 or a kda_status recorded by a kernel (KDA_ERR_DEVICE for a
+ * bad slot id). Returns KDA_OK unless the read itself failed.
+ */
+kda_status kda_state_poll_error(kda_state *st, int32_t *code);
+
+/* Message of the last failed call on this thread ("" if none). Never NULL. */
+const char *kda_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H */

@@ -1,0 +1,67 @@
+// kda_internal.cuh - shared device helpers and the state object of the KDA library.
+// Not part of the public ABI (that is include/kda.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr int kD = 128;  // head dim (dk = dv)
+constexpr int kK = 4;    // conv kernel
+constexpr int kC = 64;   // prefill chunk
+
+// The library-owned state object behind the opaque kda_state handle.
+struct State {
+    kda_config_t cfg;
+    int32_t max_slots;
+    int device;
+    float *S;         // [max_slots][H][d][d] FP32
+    void *tail;       // [max_slots][3][K-1][H*d] io dtype
+    int32_t *err;     // device error word (0 = none)
+    void *ws;         // prefill workspace
+    size_t ws_bytes;
+};
+
+// ---------------------------------------------------------------- IO types
+template <typename T> struct IO;
+template <> struct IO<float> {
+    static __device__ __forceinline__ float ld(const float *p) { return *p; }
+    static __device__ __forceinline__ void st(float *p, float x) { *p = x; }
+};
+template <> struct IO<__nv_bfloat16> {
+    static __device__ __forceinline__ float ld(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+    static __device__ __forceinline__ void st(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float siluf_(float x) { return x / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Streaming (evict-first) 16-byte accesses for data touched once per launch.
+__device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
+
+// Error word codes (device side mirror of kda_status values).
+constexpr int32_t kErrBadSlot = KDA_ERR_DEVICE;
+
+// Launchers (host), defined in kda_decode.cu / kda_prefill.cu.
+cudaError_t launch_decode(const State &st, const kda_layer_params &p, const int32_t *slots, int B,
+                          const void *q, const void *k, const void *v, const void *z, const void *b,
+                          const void *g, void *out, cudaStream_t stream);
+
+size_t prefill_workspace_bytes(const kda_config_t &cfg, int64_t total_chunks, int64_t total_T, int N);
+cudaError_t launch_prefill(const State &st, const kda_layer_params &p, const int32_t *slots,
+                           const int32_t *cu_seqlens, int N, int64_t total_T, int64_t total_chunks,
+                           const void *q, const void *k, const void *v, const void *z, const void *b,
+                           const void *g, void *out, void *ws, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,490 @@
+// kda_prefill.cu - chunked (WY / UT-transform) KDA prefill over packed
+// variable-length sequences.
+//
+// The per-token recurrence of the kimi_k3.c header comment ("KDA per-head
+// recurrence") is evaluated in chunks of C = 64 tokens. For a chunk starting
+// from state S0, with G_r the cumulative log decay (sum of gk over the chunk's
+// tokens up to r, a vector over the key dim), the exact rewrite is
+//   A[r][i] = beta_r sum_c k_r[c] k_i[c] exp(G_r[c] - G_i[c])   (i < r)
+//   W  = (I + A)^-1 Diag(beta) (K o exp(G)),  U' = (I + A)^-1 Diag(beta) V
+//   U  = U' - W S0
+//   O  = (Q o exp(G)) S0 + (P o M) U,  P[r][i] = sum_c q_r[c] k_i[c] exp(G_r[c] - G_i[c])
+//   S  = Diag(exp(G_last)) S0 + (K o exp(G_last - G))^T U
+// exp(G_r - G_i) is formed as a product of two factors that are both finite in
+// FP32: for each 16-row block with first row n, exp(G_r - G_n) (<= 1) times
+// exp(G_n - G_i) (<= 1 for i <= n, <= e^75 inside the block).
+//
+// Kernels, in stream order:
+//   chunk_table_kernel  chunk list (sequence, first token, length) from cu_seqlens
+//   prep_kernel         per (chunk, head): conv+SiLU, L2, gates, G, A, P,
+//                       the triangular solve, W, U', Q o exp(G), K o exp(G_last - G)
+//   state_kernel        per (sequence, head, 32-column block of v): the serial
+//                       pass over the chunks carrying S; writes o and the final
+//                       state, and the new conv history
+//   epilogue_kernel     gated per-head RMSNorm of o
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kBlk = 16;                  // sub-block rows for the decay reference
+constexpr int kVB = 32;                   // v columns per state_kernel CTA
+constexpr int kChunkFloats = 4 * kC * kD + kC * kC + kD;  // W, U', QG, KD, P, gC
+constexpr int kPrepSmemFloats = 4 * kC * kD + 2 * kC * kC + kD * kC + 2 * kBlk * kD + kC;
+constexpr int kStateSmemFloats = kD * kVB + 3 * kC * kD + 2 * kC * kVB + kC * kC + kD;
+
+struct ChunkEntry { int seq, t0, n, pos0; };
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t table, seq_first, chunks, obuf, total;
+};
+
+WsLayout ws_layout(int H, int64_t total_chunks, int64_t total_T, int N) {
+    WsLayout L;
+    size_t off = 0;
+    L.table = off;     off = align_up(off + sizeof(ChunkEntry) * (size_t)total_chunks, 256);
+    L.seq_first = off; off = align_up(off + sizeof(int32_t) * (size_t)(N + 1), 256);
+    L.chunks = off;    off = align_up(off + sizeof(float) * (size_t)kChunkFloats * total_chunks * H, 256);
+    L.obuf = off;      off = align_up(off + sizeof(float) * (size_t)total_T * H * kD, 256);
+    L.total = off;
+    return L;
+}
+
+// ---------------------------------------------------------------- chunk table
+// One thread builds the chunk list. The device copy of cu_seqlens is checked
+// against what the host sized the launch for (N + 1 entries, starting at 0,
+// non-decreasing, ending at total_T, at most max_chunks chunks); on a mismatch
+// the list is left empty (every sequence gets no chunk) and the error word is set.
+__global__ void chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t total_T, int64_t max_chunks,
+                                   ChunkEntry *__restrict__ table, int32_t *__restrict__ seq_first,
+                                   int32_t *__restrict__ err)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    bool ok = cu[0] == 0 && (int64_t)cu[N] == total_T;
+    int64_t count = 0;
+    for (int s = 0; s < N && ok; ++s) {
+        const int len = cu[s + 1] - cu[s];
+        if (len < 0) ok = false;
+        else count += (len + kC - 1) / kC;
+    }
+    if (count > max_chunks) ok = false;
+    if (!ok) {
+        atomicExch(err, kErrBadSlot);
+        for (int s = 0; s <= N; ++s) seq_first[s] = 0;
+        for (int64_t i = 0; i < max_chunks; ++i) table[i] = ChunkEntry{0, 0, 0, 0};
+        return;
+    }
+    int idx = 0;
+    for (int s = 0; s < N; ++s) {
+        seq_first[s] = idx;
+        const int start = cu[s], len = cu[s + 1] - cu[s];
+        for (int p = 0; p < len; p += kC) {
+            ChunkEntry e;
+            e.seq = s; e.t0 = start + p; e.n = min(kC, len - p); e.pos0 = p;
+            table[idx++] = e;
+        }
+    }
+    seq_first[N] = idx;
+    for (int64_t i = idx; i < max_chunks; ++i) table[i] = ChunkEntry{0, 0, 0, 0};
+}
+
+// ---------------------------------------------------------------- prep
+template <typename T>
+__global__ void __launch_bounds__(256, 1)
+prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
+            const float *__restrict__ A_log, const T *__restrict__ tail_all,
+            const int32_t *__restrict__ slots, int H, int max_slots,
+            const ChunkEntry *__restrict__ table,
+            const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+            const T *__restrict__ z, const T *__restrict__ bl,
+            float *__restrict__ chunks, float gmin, float l2_eps, float q_scale)
+{
+    extern __shared__ __align__(16) float sm[];
+    float *Yq = sm;                 // [C][d]   q^ after L2 and scale
+    float *Yk = Yq + kC * kD;       // [C][d]   k^
+    float *Yv = Yk + kC * kD;       // [C][d]   v
+    float *G = Yv + kC * kD;        // [C][d]   cumulative log decay
+    float *Am = G + kC * kD;        // [C][C]   A (strict lower, beta folded)
+    float *Pm = Am + kC * kC;       // [C][C]   P (inclusive lower)
+    float *KRT = Pm + kC * kC;      // [d][C]   k_i o exp(G_n - G_i), transposed
+    float *KL = KRT + kD * kC;      // [16][d]  k_r o exp(G_r - G_n)
+    float *QL = KL + kBlk * kD;     // [16][d]  q_r o exp(G_r - G_n)
+    float *sbeta = QL + kBlk * kD;  // [C]
+
+    const int chunk = blockIdx.x / H, h = blockIdx.x - (blockIdx.x / H) * H;
+    const ChunkEntry e = table[chunk];
+    if (e.n <= 0) return;  // empty entry: the chunk list was rejected
+    const int slot = slots[e.seq];
+    if (slot < 0 || slot >= max_slots) return;  // recorded by state_kernel
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = e.n;
+    const size_t D = (size_t)H * kD;
+
+    // 1. conv + SiLU. Thread (i, half): channel i, rows [32 half, 32 half + 32).
+    {
+        const int i = tid & (kD - 1), half = tid >> 7;
+        const size_t c = (size_t)h * kD + i;
+        const T *src[3] = {q, k, v};
+        float *dst[3] = {Yq, Yk, Yv};
+        const T *tl = tail_all + (size_t)slot * 3 * (kK - 1) * D + c;
+        const int r0 = 32 * half;
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {
+            const float4 wt = __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)x * D + c) * kK));
+            float hst[3] = {0.f, 0.f, 0.f};
+            if (r0 < n) {  // rows of this half exist; their history lies inside the sequence or the tail
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int pos = e.pos0 + r0 - 3 + j;  // position within the sequence
+                    hst[j] = pos >= 0 ? IO<T>::ld(src[x] + (size_t)(e.t0 + r0 - 3 + j) * D + c)
+                                      : IO<T>::ld(tl + (size_t)(x * 3 + (pos + 3)) * D);
+                }
+            }
+            for (int rr = 0; rr < 32; ++rr) {
+                const int r = r0 + rr;
+                float y = 0.f;
+                if (r < n) {
+                    const float xin = IO<T>::ld(src[x] + (size_t)(e.t0 + r) * D + c);
+                    y = siluf_(fmaf(wt.x, hst[0], fmaf(wt.y, hst[1], fmaf(wt.z, hst[2], wt.w * xin))));
+                    hst[0] = hst[1]; hst[1] = hst[2]; hst[2] = xin;
+                }
+                dst[x][r * kD + i] = y;
+            }
+        }
+        // 2. gates: gk = gmin * sigmoid(exp(A_log) (z + dt)), cumulative over rows
+        const float eA = expf(__ldg(A_log + h));
+        const float dt = __ldg(dt_bias + c);
+        float acc = 0.f;
+        for (int rr = 0; rr < 32; ++rr) {
+            const int r = r0 + rr;
+            float gk = 0.f;
+            if (r < n) gk = gmin * sigmoidf_(eA * (IO<T>::ld(z + (size_t)(e.t0 + r) * D + c) + dt));
+            acc += gk;
+            G[r * kD + i] = acc;
+        }
+    }
+    __syncthreads();
+    if (tid >= kD) {  // second half adds the first half's total
+        const int i = tid - kD;
+        const float base = G[31 * kD + i];
+        for (int r = 32; r < kC; ++r) G[r * kD + i] += base;
+    }
+    // 3. L2 norms and beta: warp w handles rows w + 8m.
+    for (int m = 0; m < kC / 8; ++m) {
+        const int r = warp + 8 * m;
+        float4 a = reinterpret_cast<float4 *>(Yq + r * kD)[lane];
+        float4 b = reinterpret_cast<float4 *>(Yk + r * kD)[lane];
+        const float sq = warp_sum(a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w);
+        const float sk = warp_sum(b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w);
+        const float rq = q_scale / sqrtf(sq + l2_eps), rk = 1.0f / sqrtf(sk + l2_eps);
+        a.x *= rq; a.y *= rq; a.z *= rq; a.w *= rq;
+        b.x *= rk; b.y *= rk; b.z *= rk; b.w *= rk;
+        reinterpret_cast<float4 *>(Yq + r * kD)[lane] = a;
+        reinterpret_cast<float4 *>(Yk + r * kD)[lane] = b;
+        if (lane == 0) sbeta[r] = r < n ? sigmoidf_(IO<T>::ld(bl + (size_t)(e.t0 + r) * H + h)) : 0.f;
+    }
+    __syncthreads();
+
+    // 4. A and P, one 16-row block at a time, reference row nR = 16 R.
+    for (int R = 0; R < kC / kBlk; ++R) {
+        const int nR = R * kBlk, m = nR + kBlk;
+        {
+            const int i = tid & (kC - 1), cg = tid >> 6;
+            if (i < m) {
+                for (int cc = 0; cc < 32; ++cc) {
+                    const int c = cg * 32 + cc;
+                    KRT[c * kC + i] = Yk[i * kD + c] * expf(G[nR * kD + c] - G[i * kD + c]);
+                }
+            }
+            for (int e2 = tid; e2 < kBlk * kD; e2 += 256) {
+                const int rr = e2 / kD, c = e2 - rr * kD;
+                const float f = expf(G[(nR + rr) * kD + c] - G[nR * kD + c]);
+                KL[e2] = Yk[(nR + rr) * kD + c] * f;
+                QL[e2] = Yq[(nR + rr) * kD + c] * f;
+            }
+        }
+        __syncthreads();
+        {
+            const int i = tid & (kC - 1), rg = tid >> 6;
+            float a[4] = {0.f, 0.f, 0.f, 0.f}, p[4] = {0.f, 0.f, 0.f, 0.f};
+            if (i < m) {
+                for (int c = 0; c < kD; ++c) {
+                    const float kr = KRT[c * kC + i];
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        a[qq] = fmaf(KL[(4 * rg + qq) * kD + c], kr, a[qq]);
+                        p[qq] = fmaf(QL[(4 * rg + qq) * kD + c], kr, p[qq]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const int r = nR + 4 * rg + qq;
+                Am[r * kC + i] = (i < r) ? sbeta[r] * a[qq] : 0.f;
+                Pm[r * kC + i] = (i <= r) ? p[qq] : 0.f;
+            }
+        }
+        __syncthreads();
+    }
+
+    float *out = chunks + (size_t)blockIdx.x * kChunkFloats;
+    float *W = out, *Up = W + kC * kD, *QG = Up + kC * kD, *KD = QG + kC * kD, *P = KD + kC * kD,
+          *GC = P + kC * kC;
+
+    // 5. Forward substitution (I + A) X = Diag(beta) B, one column per thread:
+    //    columns 0..127 of B are k o exp(G), 128..255 are v.
+    {
+        const int j = tid;
+        const bool isk = j < kD;
+        const int cj = isk ? j : j - kD;
+        float X[kC];
+#pragma unroll
+        for (int r = 0; r < kC; ++r) {
+            const float bb = isk ? Yk[r * kD + cj] * expf(G[r * kD + cj]) : Yv[r * kD + cj];
+            float x = sbeta[r] * bb;
+#pragma unroll
+            for (int i = 0; i < r; ++i) x = fmaf(-Am[r * kC + i], X[i], x);
+            X[r] = x;
+        }
+        float *dstc = isk ? W : Up;
+#pragma unroll
+        for (int r = 0; r < kC; ++r) dstc[r * kD + cj] = X[r];
+    }
+    // 6. The remaining chunk factors.
+    for (int e2 = tid; e2 < kC * kD; e2 += 256) {
+        const int r = e2 / kD, c = e2 - r * kD;
+        const float g = G[r * kD + c];
+        QG[e2] = Yq[e2] * expf(g);
+        KD[e2] = Yk[e2] * expf(G[(n - 1) * kD + c] - g);
+    }
+    for (int e2 = tid; e2 < kC * kC; e2 += 256) P[e2] = Pm[e2];
+    if (tid < kD) GC[tid] = expf(G[(n - 1) * kD + tid]);
+}
+
+// ---------------------------------------------------------------- state pass
+template <typename T>
+__global__ void __launch_bounds__(256, 1)
+state_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__restrict__ err,
+             const int32_t *__restrict__ slots, int H, int max_slots,
+             const ChunkEntry *__restrict__ table, const int32_t *__restrict__ seq_first,
+             const float *__restrict__ chunks, float *__restrict__ obuf,
+             const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v)
+{
+    extern __shared__ __align__(16) float sm[];
+    float *Ss = sm;                 // [d][32]  state columns of this block
+    float *Wc = Ss + kD * kVB;      // [C][d]
+    float *QGc = Wc + kC * kD;      // [C][d]
+    float *KDc = QGc + kC * kD;     // [C][d]
+    float *Upc = KDc + kC * kD;     // [C][32]
+    float *Uc = Upc + kC * kVB;     // [C][32]
+    float *Pc = Uc + kC * kVB;      // [C][C]
+    float *GCc = Pc + kC * kC;      // [d]
+
+    const int vb = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int slot = slots[seq];
+    if (slot < 0 || slot >= max_slots) {
+        if (tid == 0) atomicExch(err, kErrBadSlot);
+        return;
+    }
+    const size_t D = (size_t)H * kD;
+    float *Sg = S_all + ((size_t)slot * H + h) * kD * kD + vb * kVB;
+
+    const int c_first = seq_first[seq], c_last = seq_first[seq + 1];
+
+    // new conv history (the last K-1 raw inputs), written by the vb == 0 CTA;
+    // the sequence's extent comes from its (validated) chunk list
+    if (vb == 0 && tid < kD && c_last > c_first) {
+        const int start = table[c_first].t0;
+        const int len = table[c_last - 1].t0 + table[c_last - 1].n - start;
+        T *tl = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD + tid;
+        const T *src[3] = {q, k, v};
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                const int pos = len - 3 + j;
+                const T val = pos >= 0 ? src[x][(size_t)(start + pos) * D + (size_t)h * kD + tid]
+                                       : tl[(size_t)(x * 3 + (pos + 3)) * D];
+                tl[(size_t)(x * 3 + j) * D] = val;
+            }
+        }
+    }
+
+    for (int e2 = tid; e2 < kD * kVB; e2 += 256) {
+        const int c = e2 / kVB, j = e2 - c * kVB;
+        Ss[e2] = Sg[(size_t)c * kD + j];
+    }
+
+    for (int ci = c_first; ci < c_last; ++ci) {
+        const ChunkEntry e = table[ci];
+        const float *src = chunks + ((size_t)ci * H + h) * kChunkFloats;
+        __syncthreads();
+        {
+            const float4 *s4 = reinterpret_cast<const float4 *>(src);
+            float4 *w4 = reinterpret_cast<float4 *>(Wc);
+            float4 *qg4 = reinterpret_cast<float4 *>(QGc);
+            float4 *kd4 = reinterpret_cast<float4 *>(KDc);
+            for (int e2 = tid; e2 < kC * kD / 4; e2 += 256) {
+                w4[e2] = s4[e2];
+                qg4[e2] = s4[2 * kC * kD / 4 + e2];
+                kd4[e2] = s4[3 * kC * kD / 4 + e2];
+            }
+            for (int e2 = tid; e2 < kC * kVB / 4; e2 += 256) {
+                const int r = e2 / (kVB / 4), j4 = e2 - r * (kVB / 4);
+                reinterpret_cast<float4 *>(Upc)[e2] = s4[kC * kD / 4 + r * (kD / 4) + vb * (kVB / 4) + j4];
+            }
+            for (int e2 = tid; e2 < kC * kC / 4; e2 += 256)
+                reinterpret_cast<float4 *>(Pc)[e2] = s4[4 * kC * kD / 4 + e2];
+            if (tid < kD / 4)
+                reinterpret_cast<float4 *>(GCc)[tid] = s4[(4 * kC * kD + kC * kC) / 4 + tid];
+        }
+        __syncthreads();
+        // U = U' - W S and the inter-chunk part of O = (Q o exp G) S; warp w owns rows 8w..8w+7.
+        float accu[8], acco[8];
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm) { accu[mm] = 0.f; acco[mm] = 0.f; }
+        for (int c = 0; c < kD; c += 4) {
+            const float s0 = Ss[(c + 0) * kVB + lane], s1 = Ss[(c + 1) * kVB + lane];
+            const float s2 = Ss[(c + 2) * kVB + lane], s3 = Ss[(c + 3) * kVB + lane];
+#pragma unroll
+            for (int mm = 0; mm < 8; ++mm) {
+                const int r = 8 * warp + mm;
+                const float4 wv = *reinterpret_cast<const float4 *>(Wc + r * kD + c);
+                const float4 qv = *reinterpret_cast<const float4 *>(QGc + r * kD + c);
+                accu[mm] = fmaf(wv.x, s0, fmaf(wv.y, s1, fmaf(wv.z, s2, fmaf(wv.w, s3, accu[mm]))));
+                acco[mm] = fmaf(qv.x, s0, fmaf(qv.y, s1, fmaf(qv.z, s2, fmaf(qv.w, s3, acco[mm]))));
+            }
+        }
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm) {
+            const int r = 8 * warp + mm;
+            Uc[r * kVB + lane] = Upc[r * kVB + lane] - accu[mm];
+        }
+        __syncthreads();
+        // O += (P o M) U, written for the chunk's real rows
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm) {
+            const int r = 8 * warp + mm;
+            float o = acco[mm];
+            for (int i = 0; i <= r; ++i) o = fmaf(Pc[r * kC + i], Uc[i * kVB + lane], o);
+            if (r < e.n) obuf[((size_t)(e.t0 + r) * H + h) * kD + vb * kVB + lane] = o;
+        }
+        // S = Diag(gC) S + KD^T U; warp w owns state rows 16w..16w+15.
+        float accs[16];
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+            const int c = 16 * warp + cc;
+            accs[cc] = GCc[c] * Ss[c * kVB + lane];
+        }
+        for (int r = 0; r < kC; ++r) {
+            const float u = Uc[r * kVB + lane];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const float4 kd = *reinterpret_cast<const float4 *>(KDc + r * kD + 16 * warp + 4 * c4);
+                accs[4 * c4 + 0] = fmaf(kd.x, u, accs[4 * c4 + 0]);
+                accs[4 * c4 + 1] = fmaf(kd.y, u, accs[4 * c4 + 1]);
+                accs[4 * c4 + 2] = fmaf(kd.z, u, accs[4 * c4 + 2]);
+                accs[4 * c4 + 3] = fmaf(kd.w, u, accs[4 * c4 + 3]);
+            }
+        }
+        __syncthreads();  // everyone is done reading Ss for this chunk
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) Ss[(16 * warp + cc) * kVB + lane] = accs[cc];
+    }
+    __syncthreads();
+    for (int e2 = tid; e2 < kD * kVB; e2 += 256) {
+        const int c = e2 / kVB, j = e2 - c * kVB;
+        Sg[(size_t)c * kD + j] = Ss[e2];
+    }
+}
+
+// ---------------------------------------------------------------- epilogue
+template <typename T>
+__global__ void __launch_bounds__(256)
+epilogue_kernel(const float *__restrict__ obuf, const float *__restrict__ norm_w, const T *__restrict__ g,
+                T *__restrict__ out, int64_t n_rows, float rms_eps)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // (token, head) pair
+    if (row >= n_rows) return;
+    const float4 o = reinterpret_cast<const float4 *>(obuf + row * kD)[lane];
+    const float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
+    const float rinv = 1.0f / sqrtf(ss * (1.0f / kD) + rms_eps);
+    const float4 w = __ldg(reinterpret_cast<const float4 *>(norm_w) + lane);
+    const T *gp = g + row * kD + 4 * lane;
+    T *op = out + row * kD + 4 * lane;
+    IO<T>::st(op + 0, sigmoidf_(IO<T>::ld(gp + 0)) * w.x * (o.x * rinv));
+    IO<T>::st(op + 1, sigmoidf_(IO<T>::ld(gp + 1)) * w.y * (o.y * rinv));
+    IO<T>::st(op + 2, sigmoidf_(IO<T>::ld(gp + 2)) * w.z * (o.z * rinv));
+    IO<T>::st(op + 3, sigmoidf_(IO<T>::ld(gp + 3)) * w.w * (o.w * rinv));
+}
+
+template <typename T>
+cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32_t *slots,
+                         const int32_t *cu, int N, int64_t total_T, int64_t total_chunks,
+                         const void *q, const void *k, const void *v, const void *z, const void *b,
+                         const void *g, void *out, void *ws, cudaStream_t stream)
+{
+    const kda_config_t &c = st.cfg;
+    const int H = c.num_heads;
+    const WsLayout L = ws_layout(H, total_chunks, total_T, N);
+    char *base = static_cast<char *>(ws);
+    ChunkEntry *table = reinterpret_cast<ChunkEntry *>(base + L.table);
+    int32_t *seq_first = reinterpret_cast<int32_t *>(base + L.seq_first);
+    float *chunks = reinterpret_cast<float *>(base + L.chunks);
+    float *obuf = reinterpret_cast<float *>(base + L.obuf);
+
+    chunk_table_kernel<<<1, 32, 0, stream>>>(cu, N, total_T, total_chunks, table, seq_first, st.err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (total_chunks > 0) {
+        const int prep_smem = kPrepSmemFloats * (int)sizeof(float);
+        e = cudaFuncSetAttribute(prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
+        if (e != cudaSuccess) return e;
+        prep_kernel<T><<<(unsigned)(total_chunks * H), 256, prep_smem, stream>>>(
+            p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
+            (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, chunks,
+            c.gate_lower_bound, c.l2_eps, c.q_scale);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const int state_smem = kStateSmemFloats * (int)sizeof(float);
+    e = cudaFuncSetAttribute(state_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem);
+    if (e != cudaSuccess) return e;
+    state_kernel<T><<<dim3(kD / kVB, H, N), 256, state_smem, stream>>>(
+        st.S, (T *)st.tail, st.err, slots, H, st.max_slots, table, seq_first, chunks, obuf,
+        (const T *)q, (const T *)k, (const T *)v);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (total_T > 0) {
+        const int64_t rows = total_T * H;
+        epilogue_kernel<T><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(obuf, p.norm_w, (const T *)g,
+                                                                         (T *)out, rows, c.rms_eps);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(const kda_config_t &cfg, int64_t total_chunks, int64_t total_T, int N)
+{
+    return ws_layout(cfg.num_heads, total_chunks, total_T, N).total;
+}
+
+cudaError_t launch_prefill(const State &st, const kda_layer_params &p, const int32_t *slots,
+                           const int32_t *cu_seqlens, int N, int64_t total_T, int64_t total_chunks,
+                           const void *q, const void *k, const void *v, const void *z, const void *b,
+                           const void *g, void *out, void *ws, cudaStream_t stream)
+{
+    if (st.cfg.io_dtype == KDA_BF16)
+        return launch_typed<__nv_bfloat16>(st, p, slots, cu_seqlens, N, total_T, total_chunks, q, k, v, z, b,
+                                           g, out, ws, stream);
+    return launch_typed<float>(st, p, slots, cu_seqlens, N, total_T, total_chunks, q, k, v, z, b, g, out, ws,
+                               stream);
+}
+
+}  // namespace kda
