@@ -345,6 +345,31 @@ def run_kda(args):
     del ring, host, dbuf
     torch.cuda.empty_cache()
 
+    # ---------------- decode B=1 latency ----------------
+    st1 = K.kda_state_alloc(cfg, 1)
+    _fill_state_random(K, cfg, st1, 1, gen, dev)
+    x1 = [_inputs(1, gen, dev, torch.bfloat16) for _ in range(8)]
+    s1 = torch.zeros(1, dtype=torch.int32, device=dev)
+    o1 = torch.empty(1, D, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 256 MB > L2
+
+    def b1_step(i):
+        x = x1[i % 8]
+        K.kda_decode_token(cfg, params, st1, s1, x["q"], x["k"], x["v"], x["z"], x["b"], x["g"], o1, stream)
+
+    for i in range(10):
+        b1_step(i)
+    b1_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for i in range(50):
+        flush.fill_(i & 0xFF)  # evict the 6.3 MB state from L2 between steps
+        b1_ev[i][0].record(stream)
+        b1_step(i)
+        b1_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    b1_us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in b1_ev)
+    K.kda_state_free(st1)
+    del flush
+
     # ---------------- prefill T=8192 ----------------
     pcfg = cfg
     pst = K.kda_state_alloc(pcfg, 1)
@@ -399,6 +424,9 @@ def run_kda(args):
                 "steps": e2e_steps},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
+        "decode_b1": {"workload": "decode B=1, 96 heads x 128, BF16 I/O, FP32 state (L2 flushed between steps)",
+                      "latency_us": b1_us, "bytes_per_step": DEC_BYTES_PER_UNIT * H,
+                      "achieved_gbs": DEC_BYTES_PER_UNIT * H / (b1_us / 1e6) / 1e9},
         "prefill": {"workload": "prefill 1 sequence T=8192, 96 heads x 128, chunk 64, BF16 I/O",
                     "value": T_PRE / (pre_ms / 1e3), "unit": "tokens/s", "ms": pre_ms, "reps": reps,
                     "gpu_launches_per_call": 4,

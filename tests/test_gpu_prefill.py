@@ -57,6 +57,8 @@ def test_tiny_fp32_prefill_then_decode(oracle_mod):
     S, tail = oracle_mod.new_state(oc)
     ref = oracle_mod.sequence(oc, p, S, tail, tok)
     got = np.concatenate([pre] + dec)
+    print(f"tiny fp32 prefill+decode: prefill {rel_err(got[:Tp], ref[:Tp]):.2e} all {rel_err(got, ref):.2e} "
+          f"state {rel_err(Sg[0], S):.2e}")
     assert rel_err(got[:Tp], ref[:Tp]) <= TOL_F32
     assert rel_err(got, ref) <= TOL_F32
     assert rel_err(Sg[0], S) <= TOL_F32
@@ -88,6 +90,7 @@ def test_varlen_ragged_chunks_with_carried_state(oracle_mod, bf16):
         K.kda_state_free(st)
     oc = oracle_mod.OracleCfg(H=H, d=d)
     tol = TOL_BF16 if bf16 else TOL_F32
+    worst_o, worst_s = 0.0, 0.0
     for i in range(N):
         s = slots[i]
         S = S0[s].astype(np.float64)
@@ -95,9 +98,12 @@ def test_varlen_ragged_chunks_with_carried_state(oracle_mod, bf16):
         rows = slice(cu[i], cu[i + 1])
         ref = oracle_mod.sequence(oc, p, S, tail, {n: a[rows] for n, a in tok.items()})
         if lens[i]:
+            worst_o = max(worst_o, rel_err(got[rows], ref))
             assert rel_err(got[rows], ref) <= tol, (i, lens[i])
+        worst_s = max(worst_s, rel_err(Sg[s], S))
         assert rel_err(Sg[s], S) <= tol, (i, lens[i])
         assert np.array_equal(tg[s], tail.astype(np.float32)), (i, lens[i])
+    print(f"varlen ragged {'bf16' if bf16 else 'fp32'}: worst out {worst_o:.2e} worst state {worst_s:.2e}")
     for s in set(range(n_slots)) - set(slots.tolist()):
         assert np.array_equal(Sg[s], S0[s]) and np.array_equal(tg[s], T0[s])
 
@@ -189,6 +195,8 @@ def test_prefill_8192_bf16_full_size(oracle_mod):
     oc = oracle_mod.OracleCfg(H=H, d=d)
     S, tail = oracle_mod.new_state(oc)
     ref = oracle_mod.sequence(oc, p, S, tail, tok)
+    print(f"prefill T=8192 bf16: first {nchk} tokens {rel_err(got[:nchk], ref[:nchk]):.2e} "
+          f"all tokens {rel_err(got, ref):.2e} final state {rel_err(Sg[0], S):.2e}")
     assert rel_err(got[:nchk], ref[:nchk]) <= TOL_BF16
     assert rel_err(Sg[0], S) <= TOL_BF16
     assert np.array_equal(tg[0], tail.astype(np.float32))
