@@ -202,6 +202,38 @@ kda_status kda_prefill(const kda_config_t *cfg, const kda_layer_params *params, 
                        const void *b, const void *g, void *out, void *stream);
 
 /*
+ * kda_prefill_noalloc: the computation of kda_prefill for callers that must not
+ * allocate device memory. The pages have no counterpart to this entry point; it
+ * exists for callers such as serving runtimes that hand out every byte of device
+ * memory from their own arena (exact accounting, no allocation failure halfway
+ * through a request) or latency-critical loops that cannot accept the implicit
+ * device-wide synchronisation of cudaMalloc/cudaFree. It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *   S      device FP32 [max_slots][H][d][d], caller-owned (layout of a kda_state's S)
+ *   tail   device io_dtype [max_slots][3][K-1][H*d], caller-owned conv history
+ *   err    device int32 word that receives KDA_ERR_DEVICE for a bad slot id or a
+ *          cu_seqlens that disagrees with cu_seqlens_host; never cleared by the
+ *          library. NULL: a word inside the static workspace is used (and cleared
+ *          at the start of each call), and such errors are not reported.
+ *   slots .. out, stream: as for kda_prefill.
+ * Its scratch is a file-scope __device__ array of KDA_NOALLOC_WORKSPACE_BYTES
+ * (128 MiB; every GPU that loads the library holds it until the process exits).
+ * A call whose workspace need exceeds it (about 148 KB per (chunk of 64 tokens,
+ * head) plus 512 B per (token, head)) returns KDA_ERR_INVALID before enqueuing
+ * anything; split such a call. The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture. All calls on a device share the array
+ * and it keeps the previous call's contents: calls whose work overlaps on the
+ * GPU race, so order them (one stream, or events).
+ */
+#define KDA_NOALLOC_WORKSPACE_BYTES ((size_t)128 << 20)
+kda_status kda_prefill_noalloc(const kda_config_t *cfg, const kda_layer_params *params, float *S, void *tail,
+                               int32_t max_slots, int32_t *err, const int32_t *slots, const int32_t *cu_seqlens,
+                               const int32_t *cu_seqlens_host, int32_t N,
+                               const void *q, const void *k, const void *v, const void *z,
+                               const void *b, const void *g, void *out, void *stream);
+
+/*
  * Synchronise the device, read and clear the state's device error word.
  * *code receives 0 or a kda_status recorded by a kernel (KDA_ERR_DEVICE for a
  * bad slot id). Returns KDA_OK unless the read itself failed.

@@ -111,6 +111,12 @@ kda_blob_header make_header(const State *st, int32_t n)
 
 static_assert(sizeof(kda_blob_header) == 64, "blob header must be 64 bytes");
 
+namespace kda {
+// For entry points defined in other translation units.
+kda_status record_error(kda_status s, const char *msg) { return fail(s, "%s", msg); }
+bool config_ok(const kda_config_t *c) { return cfg_check(c); }
+}  // namespace kda
+
 extern "C" {
 
 const char *kda_last_error(void) { return g_err; }

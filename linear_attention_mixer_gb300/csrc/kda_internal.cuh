@@ -64,4 +64,8 @@ cudaError_t launch_prefill(const State &st, const kda_layer_params &p, const int
                            const void *q, const void *k, const void *v, const void *z, const void *b,
                            const void *g, void *out, void *ws, cudaStream_t stream);
 
+// Error text and config checks shared by every entry point (kda_api.cu).
+kda_status record_error(kda_status s, const char *msg);
+bool config_ok(const kda_config_t *c);
+
 }  // namespace kda

@@ -71,6 +71,8 @@ SIGNATURES = [
                                 _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("kda_prefill", _I32, [ctypes.POINTER(kda_config_t), ctypes.POINTER(kda_layer_params), _VP, _VP, _VP, _PI32,
                            _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    ("kda_prefill_noalloc", _I32, [ctypes.POINTER(kda_config_t), ctypes.POINTER(kda_layer_params), _VP, _VP, _I32,
+                                   _VP, _VP, _VP, _PI32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("kda_state_poll_error", _I32, [_VP, _PI32]),
     ("kda_last_error", ctypes.c_char_p, []),
 ]
@@ -219,6 +221,39 @@ def kda_prefill(cfg: kda_config_t, params: kda_layer_params, st, slots: torch.Te
                              _dev(cu_seqlens, torch.int32, "cu_seqlens"), cu_p, N,
                              _dev(q, dt, "q"), _dev(k, dt, "k"), _dev(v, dt, "v"), _dev(z, dt, "z"),
                              _dev(b, dt, "b"), _dev(g, dt, "g"), _dev(out, dt, "out"), _stream(stream)))
+
+
+def kda_prefill_noalloc(cfg: kda_config_t, params: kda_layer_params, S: torch.Tensor, tail: torch.Tensor,
+                        err, slots: torch.Tensor, cu_seqlens: torch.Tensor, cu_seqlens_host,
+                        q, k, v, z, b, g, out, stream=None) -> None:
+    """kda_prefill on caller-owned state buffers with the library's static workspace.
+
+    S: FP32 [max_slots, H, d, d]; tail: io dtype [max_slots, 3, K-1, H*d]; err: int32
+    device tensor of one element, or None.
+    """
+    dt = _torch_io_dtype(cfg)
+    H, d, Kc = cfg.num_heads, cfg.head_dim, cfg.conv_kernel
+    if S.dim() != 4 or tuple(S.shape[1:]) != (H, d, d):
+        raise ValueError(f"S must be [max_slots, {H}, {d}, {d}]")
+    max_slots = int(S.shape[0])
+    if tuple(tail.shape) != (max_slots, 3, Kc - 1, H * d):
+        raise ValueError(f"tail must be [{max_slots}, 3, {Kc - 1}, {H * d}]")
+    N = int(slots.numel())
+    cu_h, cu_p = _host_i32(cu_seqlens_host)
+    if len(cu_h) != N + 1 or cu_seqlens.numel() != N + 1:
+        raise ValueError("cu_seqlens must hold N + 1 entries")
+    T = int(cu_h[-1]) if N > 0 else 0
+    D = H * d
+    for name, t, width in (("q", q, D), ("k", k, D), ("v", v, D), ("z", z, D), ("g", g, D),
+                           ("b", b, H), ("out", out, D)):
+        if t.numel() != T * width:
+            raise ValueError(f"{name} must hold {T} x {width} elements, got {tuple(t.shape)}")
+    errp = _VP(None) if err is None else _dev(err, torch.int32, "err")
+    _check(lib().kda_prefill_noalloc(ctypes.byref(cfg), ctypes.byref(params), _dev(S, torch.float32, "S"),
+                                     _dev(tail, dt, "tail"), max_slots, errp, _dev(slots, torch.int32, "slots"),
+                                     _dev(cu_seqlens, torch.int32, "cu_seqlens"), cu_p, N,
+                                     _dev(q, dt, "q"), _dev(k, dt, "k"), _dev(v, dt, "v"), _dev(z, dt, "z"),
+                                     _dev(b, dt, "b"), _dev(g, dt, "g"), _dev(out, dt, "out"), _stream(stream)))
 
 
 def kda_state_poll_error(st) -> int:
