@@ -256,31 +256,16 @@ def _inputs(rows, gen, dev, dtype):
             for n in ("q", "k", "v", "z", "b", "g")}
 
 
-def run_kda(args):
+def _time_decode(K, args, cfg, params, gen, dev, stream, ws, local):
+    """Decode of args.batch sequences: device-resident timing, per-launch events, e2e."""
     import torch
-    ws, rank, local = _dist()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", init_method="env://")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    from linear_attention_mixer_gb300 import build as KB
-    KB.build()
-    import linear_attention_mixer_gb300 as K
-    peaks = _peaks()
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(1000 + rank)
-    stream = torch.cuda.current_stream()
-
-    # ---------------- decode B=256 ----------------
-    cfg = K.kda_config(H, DH, K.KDA_BF16)
-    params = _params(K, gen, dev)
-    st = K.kda_state_alloc(cfg, B_DEC)
-    _fill_state_random(K, cfg, st, B_DEC, gen, dev)
-    ring_n = 16  # 16 distinct input sets (~0.5 GB), cycled
-    ring = [_inputs(B_DEC, gen, dev, torch.bfloat16) for _ in range(ring_n)]
-    slots = torch.arange(B_DEC, dtype=torch.int32, device=dev)
-    out = torch.empty(B_DEC, D, dtype=torch.bfloat16, device=dev)
+    Bd = args.batch
+    st = K.kda_state_alloc(cfg, Bd)
+    _fill_state_random(K, cfg, st, Bd, gen, dev)
+    ring_n = 16  # 16 distinct input sets (~0.5 GB at B=256), cycled
+    ring = [_inputs(Bd, gen, dev, torch.bfloat16) for _ in range(ring_n)]
+    slots = torch.arange(Bd, dtype=torch.int32, device=dev)
+    out = torch.empty(Bd, D, dtype=torch.bfloat16, device=dev)
 
     def dec_step(i):
         x = ring[i % ring_n]
@@ -307,17 +292,12 @@ def run_kda(args):
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     assert K.kda_state_poll_error(st) == 0
-    total_ms_max = _max_over_ranks(total_ms, ws, dev)
-    tokens = B_DEC * args.steps * ws
-    value = tokens / (total_ms_max / 1e3)
-    dec_bytes = DEC_BYTES_PER_UNIT * B_DEC * H
-    achieved = dec_bytes / (launch_ms / 1e3) / 1e9
 
-    # ---------------- e2e through the public API with host buffers ----------------
+    # e2e through the public API: pinned host inputs copied in, result copied out, every step
     e2e_steps = min(args.steps, 100)
     host = [{n: t.cpu().pin_memory() for n, t in ring[j].items()} for j in range(4)]
     dbuf = {n: torch.empty_like(t) for n, t in ring[0].items()}
-    hout = torch.empty(B_DEC, D, dtype=torch.bfloat16).pin_memory()
+    hout = torch.empty(Bd, D, dtype=torch.bfloat16).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host[0].values())
     d2h = hout.numel() * hout.element_size()
 
@@ -339,13 +319,17 @@ def run_kda(args):
         e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws, dev)
-    e2e_val = B_DEC * e2e_steps * ws / (e2e_ms / 1e3)
+    e2e_ms = e0.elapsed_time(e1)
     K.kda_state_free(st)
     del ring, host, dbuf
     torch.cuda.empty_cache()
+    return {"total_ms": total_ms, "launch_ms": launch_ms, "clocks": clk.summary(), "e2e_ms": e2e_ms,
+            "e2e_steps": e2e_steps, "h2d": h2d, "d2h": d2h}
 
-    # ---------------- decode B=1 latency ----------------
+
+def _time_decode_b1(K, cfg, params, gen, dev, stream):
+    """Batch-1 decode latency with the L2 flushed between steps."""
+    import torch
     st1 = K.kda_state_alloc(cfg, 1)
     _fill_state_random(K, cfg, st1, 1, gen, dev)
     x1 = [_inputs(1, gen, dev, torch.bfloat16) for _ in range(8)]
@@ -369,18 +353,21 @@ def run_kda(args):
     b1_us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in b1_ev)
     K.kda_state_free(st1)
     del flush
+    return b1_us
 
-    # ---------------- prefill T=8192 ----------------
-    pcfg = cfg
-    pst = K.kda_state_alloc(pcfg, 1)
-    px = _inputs(T_PRE, gen, dev, torch.bfloat16)
-    pout = torch.empty(T_PRE, D, dtype=torch.bfloat16, device=dev)
+
+def _time_prefill(K, args, cfg, params, gen, dev, stream):
+    import torch
+    Tp = args.prefill_tokens
+    pst = K.kda_state_alloc(cfg, 1)
+    px = _inputs(Tp, gen, dev, torch.bfloat16)
+    pout = torch.empty(Tp, D, dtype=torch.bfloat16, device=dev)
     pslots = torch.zeros(1, dtype=torch.int32, device=dev)
-    cu_h = [0, T_PRE]
+    cu_h = [0, Tp]
     cu = torch.tensor(cu_h, dtype=torch.int32, device=dev)
 
     def pre_call():
-        K.kda_prefill(pcfg, params, pst, pslots, cu, cu_h, px["q"], px["k"], px["v"], px["z"], px["b"], px["g"],
+        K.kda_prefill(cfg, params, pst, pslots, cu, cu_h, px["q"], px["k"], px["v"], px["z"], px["b"], px["g"],
                       pout, stream)
 
     for _ in range(3):
@@ -398,47 +385,87 @@ def run_kda(args):
     pre_ms = statistics.median(a.elapsed_time(b) for a, b in pev)
     assert K.kda_state_poll_error(pst) == 0
     K.kda_state_free(pst)
-    pre_flop = PRE_FLOP_PER_TOKEN_HEAD * T_PRE * H
-    pre_bytes = PRE_BYTES_PER_TOKEN * T_PRE
-    pre_tflops = pre_flop / (pre_ms / 1e3) / 1e12
-    pre_gbs = pre_bytes / (pre_ms / 1e3) / 1e9
+    del px
+    torch.cuda.empty_cache()
+    return pre_ms
 
-    if rank != 0:
-        return 0
-    cpu_dec = cpu_baseline_decode() if not args.no_cpu_baseline else None
-    cpu_pre = cpu_baseline_prefill() if not args.no_cpu_baseline else None
+
+def run_kda(args):
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from linear_attention_mixer_gb300 import build as KB
+    KB.build()
+    import linear_attention_mixer_gb300 as K
+    peaks = _peaks()
     src = "of measured" if peaks["source"] == "measured" else "of fallback"
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "decode B=256, 96 heads x 128, 1 KDA layer", "batch": B_DEC, "heads": H,
-                   "head_dim": DH, "io_dtype": "bf16", "state_dtype": "f32",
-                   "l2": "inputs larger than L2 (1.61 GB of state per step)",
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "decode_kernel<bf16>",
-                     "bytes_per_launch": dec_bytes, "launch_ms": launch_ms, "peak_note": src},
-        "cpu_baseline": cpu_dec,
-        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
-        "gpu_launches": args.steps,
-        "clocks": clk.summary(),
-        "decode_b1": {"workload": "decode B=1, 96 heads x 128, BF16 I/O, FP32 state (L2 flushed between steps)",
-                      "latency_us": b1_us, "bytes_per_step": DEC_BYTES_PER_UNIT * H,
-                      "achieved_gbs": DEC_BYTES_PER_UNIT * H / (b1_us / 1e6) / 1e9},
-        "prefill": {"workload": "prefill 1 sequence T=8192, 96 heads x 128, chunk 64, BF16 I/O",
-                    "value": T_PRE / (pre_ms / 1e3), "unit": "tokens/s", "ms": pre_ms, "reps": reps,
-                    "gpu_launches_per_call": 4,
-                    "roofline_tensor": {"bound": "tensor", "achieved": pre_tflops, "peak": peaks["bf16_tflops"],
-                                        "unit": "TFLOP/s", "frac": pre_tflops / peaks["bf16_tflops"],
-                                        "flop_per_call": pre_flop, "peak_note": src},
-                    "roofline_hbm": {"bound": "hbm", "achieved": pre_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                     "frac": pre_gbs / peaks["hbm_gbs"], "bytes_per_call": pre_bytes,
-                                     "peak_note": src},
-                    "cpu_baseline": cpu_pre},
-    }
-    print(json.dumps(line), flush=True)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    stream = torch.cuda.current_stream()
+    cfg = K.kda_config(H, DH, K.KDA_BF16)
+    params = _params(K, gen, dev)
+    Bd, Tp = args.batch, args.prefill_tokens
+
+    line = {"metric": METRIC, "value": None, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"decode B={Bd}, 96 heads x 128, 1 KDA layer", "batch": Bd, "heads": H,
+                       "head_dim": DH, "io_dtype": "bf16", "state_dtype": "f32",
+                       "l2": f"inputs larger than L2 ({Bd * H * DH * DH * 4 / 1e9:.2f} GB of state per step)",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}}
+    if args.only in ("all", "decode"):
+        r = _time_decode(K, args, cfg, params, gen, dev, stream, ws, local)
+        total_ms_max = _max_over_ranks(r["total_ms"], ws, dev)
+        e2e_ms_max = _max_over_ranks(r["e2e_ms"], ws, dev)
+        dec_bytes = DEC_BYTES_PER_UNIT * Bd * H
+        achieved = dec_bytes / (r["launch_ms"] / 1e3) / 1e9
+        line.update({
+            "value": Bd * args.steps * ws / (total_ms_max / 1e3),
+            "ms_per_step": total_ms_max / args.steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": "decode_persistent_kernel<bf16,3>", "bytes_per_launch": dec_bytes,
+                         "launch_ms": r["launch_ms"], "peak_note": src},
+            "e2e": {"value": Bd * r["e2e_steps"] * ws / (e2e_ms_max / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"]},
+            "gpu_launches": args.steps,
+            "clocks": r["clocks"],
+        })
+        if args.only == "all":
+            b1_us = _time_decode_b1(K, cfg, params, gen, dev, stream)
+            line["decode_b1"] = {"workload": "decode B=1, 96 heads x 128, BF16 I/O, FP32 state "
+                                             "(L2 flushed between steps)",
+                                 "latency_us": b1_us, "bytes_per_step": DEC_BYTES_PER_UNIT * H,
+                                 "achieved_gbs": DEC_BYTES_PER_UNIT * H / (b1_us / 1e6) / 1e9}
+    if args.only in ("all", "prefill"):
+        pre_ms = _time_prefill(K, args, cfg, params, gen, dev, stream)
+        pre_flop = PRE_FLOP_PER_TOKEN_HEAD * Tp * H
+        pre_bytes = PRE_BYTES_PER_TOKEN * Tp
+        pre_tflops = pre_flop / (pre_ms / 1e3) / 1e12
+        pre_gbs = pre_bytes / (pre_ms / 1e3) / 1e9
+        line["prefill"] = {
+            "workload": f"prefill 1 sequence T={Tp}, 96 heads x 128, chunk 64, BF16 I/O",
+            "value": Tp / (pre_ms / 1e3), "unit": "tokens/s", "ms": pre_ms, "reps": args.prefill_reps,
+            "gpu_launches_per_call": 4,
+            "roofline_tensor": {"bound": "tensor", "achieved": pre_tflops, "peak": peaks["bf16_tflops"],
+                                "unit": "TFLOP/s", "frac": pre_tflops / peaks["bf16_tflops"],
+                                "flop_per_call": pre_flop, "peak_note": src},
+            "roofline_hbm": {"bound": "hbm", "achieved": pre_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": pre_gbs / peaks["hbm_gbs"], "bytes_per_call": pre_bytes, "peak_note": src}}
+        if args.only == "prefill":
+            line["value"] = Tp / (pre_ms / 1e3)
+            line["ms_per_step"] = pre_ms
+            line["gpu_launches"] = 4 * args.prefill_reps
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode()
+        if "prefill" in line:
+            line["prefill"]["cpu_baseline"] = cpu_baseline_prefill()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -453,6 +480,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
     ap.add_argument("--prefill-reps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+                    help="time one part only (small profiling runs); the JSON line keeps its keys")
+    ap.add_argument("--batch", type=int, default=B_DEC, help="decode batch (profiling runs)")
+    ap.add_argument("--prefill-tokens", type=int, default=T_PRE, help="prefill length (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
