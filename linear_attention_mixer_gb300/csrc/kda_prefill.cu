@@ -23,6 +23,7 @@
 //                       state, and the new conv history
 //   epilogue_kernel     gated per-head RMSNorm of o
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 namespace {
@@ -33,6 +34,22 @@ constexpr int kChunkFloats = 4 * kC * kD + kC * kC + kD;  // W, U', QG, KD, P, g
 constexpr int kPrepSmemFloats = 4 * kC * kD + 2 * kC * kC + kD * kC + 2 * kBlk * kD + kC;
 constexpr int kStateSmemFloats = kD * kVB + 3 * kC * kD + 2 * kC * kVB + kC * kC + kD;
 
+// Tensor-core path (BF16 I/O): per (chunk, head) the prep kernel writes one block that
+// the state kernel brings into shared memory with a single bulk copy. Operand tiles are
+// BF16 in the K-major interleaved layout of kda_tc.cuh:
+//   W   [64 r][128 k]  B operand of  S^T W^T          (N = 64,  K = 128)
+//   QG  [64 r][128 k]  B operand of  S^T QG^T         (N = 64,  K = 128)
+//   P   [64 r][64 i]   B operand of  U^T P^T          (N = 64,  K = 64)
+//   KDT [128 k][64 r]  B operand of  U^T KD           (N = 128, K = 64)
+//   U'  [64 r][128 v]  FP32, subtracted in registers
+//   gC  [128]          FP32 chunk decay exp(G_last)
+constexpr int kOffW = 0, kOffQG = 16384, kOffP = 32768, kOffKDT = 40960, kOffUp = 57344, kOffG = 90112;
+constexpr int kTcChunkBytes = 90624;
+constexpr int kTcStageBytes = kOffG;  // W..U' go to a 1024-aligned stage, gC to its own buffer
+constexpr int kStateTcSmem = 2 * kTcStageBytes + 32768 + 16384 + 2 * kD * 4 + 4 * kC * 4 + 64;
+static_assert(kStateTcSmem <= 232448, "state_tc_kernel shared memory");
+constexpr uint32_t kTcWaitLimit = 1u << 26;
+
 struct ChunkEntry { int seq, t0, n, pos0; };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -41,15 +58,36 @@ struct WsLayout {
     size_t table, seq_first, chunks, obuf, total;
 };
 
-WsLayout ws_layout(int H, int64_t total_chunks, int64_t total_T, int N) {
+// tc: BF16 tensor-core layout (no o buffer: the RMSNorm is fused into the state pass)
+WsLayout ws_layout(int H, int64_t total_chunks, int64_t total_T, int N, bool tc) {
     WsLayout L;
     size_t off = 0;
     L.table = off;     off = align_up(off + sizeof(ChunkEntry) * (size_t)total_chunks, 256);
     L.seq_first = off; off = align_up(off + sizeof(int32_t) * (size_t)(N + 1), 256);
-    L.chunks = off;    off = align_up(off + sizeof(float) * (size_t)kChunkFloats * total_chunks * H, 256);
-    L.obuf = off;      off = align_up(off + sizeof(float) * (size_t)total_T * H * kD, 256);
+    L.chunks = off;
+    off = align_up(off + (tc ? (size_t)kTcChunkBytes : sizeof(float) * (size_t)kChunkFloats) * total_chunks * H, 256);
+    L.obuf = off;
+    if (!tc) off = align_up(off + sizeof(float) * (size_t)total_T * H * kD, 256);
     L.total = off;
     return L;
+}
+
+// 16 values -> BF16 at (row, k0 .. k0+15) of a K-major interleaved tile with Kd columns (k0 % 16 == 0)
+__device__ __forceinline__ void store_row_bf16(unsigned char *tile, int row, int k0, const float *v16, int Kd)
+{
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const __nv_bfloat162 p2 = __floats2bfloat162_rn(v16[2 * i], v16[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t *>(&p2);
+    }
+    *reinterpret_cast<uint4 *>(tile + tc::kmajor_off(row, k0, Kd)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4 *>(tile + tc::kmajor_off(row, k0 + 8, Kd)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__device__ __forceinline__ void st_bf16(unsigned char *tile, uint32_t off, float x)
+{
+    *reinterpret_cast<__nv_bfloat16 *>(tile + off) = __float2bfloat16_rn(x);
 }
 
 // ---------------------------------------------------------------- chunk table
@@ -91,7 +129,8 @@ __global__ void chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_
 }
 
 // ---------------------------------------------------------------- prep
-template <typename T>
+// TC = true writes the BF16 tensor-core block (kTcChunkBytes); false the FP32 block.
+template <typename T, bool TC>
 __global__ void __launch_bounds__(256, 1)
 prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
             const float *__restrict__ A_log, const T *__restrict__ tail_all,
@@ -99,7 +138,7 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
             const ChunkEntry *__restrict__ table,
             const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
             const T *__restrict__ z, const T *__restrict__ bl,
-            float *__restrict__ chunks, float gmin, float l2_eps, float q_scale)
+            unsigned char *__restrict__ chunks, float gmin, float l2_eps, float q_scale)
 {
     extern __shared__ __align__(16) float sm[];
     float *Yq = sm;                 // [C][d]   q^ after L2 and scale
@@ -122,6 +161,32 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
     const int n = e.n;
     const size_t D = (size_t)H * kD;
 
+    // 0. (BF16 inputs) the chunk's raw q, k, v rows with their 3 rows of history, and z,
+    //    staged in shared memory with 16-byte loads; the region is reused from step 4 on.
+    constexpr int kRows = kC + 3;  // staged row j holds position j - 3 of the chunk
+    T *raw = reinterpret_cast<T *>(Am);
+    constexpr bool kStage = sizeof(T) == 2;
+    static_assert(!kStage || 4 * kRows * kD * sizeof(T) <= (2 * kC * kC + kD * kC + 2 * kBlk * kD) * sizeof(float),
+                  "raw staging must fit in the A/P/KRT/KL/QL region");
+    if constexpr (kStage) {
+        const T *srcs[4] = {q, k, v, z};
+        const T *tl0 = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD;
+        for (int e2 = tid; e2 < 4 * kRows * 16; e2 += 256) {
+            const int x = e2 / (kRows * 16), rem = e2 - x * (kRows * 16);
+            const int j = rem >> 4, vec = rem & 15;
+            const int p = j - 3;
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (p < n && !(x == 3 && p < 0)) {
+                const int pos = e.pos0 + p;  // position within the sequence
+                const T *srcp = pos >= 0 ? srcs[x] + (size_t)(e.t0 + p) * D + (size_t)h * kD
+                                         : tl0 + (size_t)(x * 3 + (pos + 3)) * D;
+                val = __ldg(reinterpret_cast<const uint4 *>(srcp) + vec);
+            }
+            reinterpret_cast<uint4 *>(raw + ((size_t)x * kRows + j) * kD)[vec] = val;
+        }
+        __syncthreads();
+    }
+
     // 1. conv + SiLU. Thread (i, half): channel i, rows [32 half, 32 half + 32).
     {
         const int i = tid & (kD - 1), half = tid >> 7;
@@ -133,24 +198,36 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 #pragma unroll
         for (int x = 0; x < 3; ++x) {
             const float4 wt = __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)x * D + c) * kK));
-            float hst[3] = {0.f, 0.f, 0.f};
-            if (r0 < n) {  // rows of this half exist; their history lies inside the sequence or the tail
+            if constexpr (kStage) {
+                const T *col = raw + (size_t)x * kRows * kD + i;
+                for (int rr = 0; rr < 32; ++rr) {
+                    const int r = r0 + rr;
+                    float y = 0.f;
+                    if (r < n)
+                        y = siluf_(fmaf(wt.x, IO<T>::ld(col + r * kD), fmaf(wt.y, IO<T>::ld(col + (r + 1) * kD),
+                                   fmaf(wt.z, IO<T>::ld(col + (r + 2) * kD), wt.w * IO<T>::ld(col + (r + 3) * kD)))));
+                    dst[x][r * kD + i] = y;
+                }
+            } else {
+                float hst[3] = {0.f, 0.f, 0.f};
+                if (r0 < n) {  // rows of this half exist; their history lies inside the sequence or the tail
 #pragma unroll
-                for (int j = 0; j < 3; ++j) {
-                    const int pos = e.pos0 + r0 - 3 + j;  // position within the sequence
-                    hst[j] = pos >= 0 ? IO<T>::ld(src[x] + (size_t)(e.t0 + r0 - 3 + j) * D + c)
-                                      : IO<T>::ld(tl + (size_t)(x * 3 + (pos + 3)) * D);
+                    for (int j = 0; j < 3; ++j) {
+                        const int pos = e.pos0 + r0 - 3 + j;  // position within the sequence
+                        hst[j] = pos >= 0 ? IO<T>::ld(src[x] + (size_t)(e.t0 + r0 - 3 + j) * D + c)
+                                          : IO<T>::ld(tl + (size_t)(x * 3 + (pos + 3)) * D);
+                    }
                 }
-            }
-            for (int rr = 0; rr < 32; ++rr) {
-                const int r = r0 + rr;
-                float y = 0.f;
-                if (r < n) {
-                    const float xin = IO<T>::ld(src[x] + (size_t)(e.t0 + r) * D + c);
-                    y = siluf_(fmaf(wt.x, hst[0], fmaf(wt.y, hst[1], fmaf(wt.z, hst[2], wt.w * xin))));
-                    hst[0] = hst[1]; hst[1] = hst[2]; hst[2] = xin;
+                for (int rr = 0; rr < 32; ++rr) {
+                    const int r = r0 + rr;
+                    float y = 0.f;
+                    if (r < n) {
+                        const float xin = IO<T>::ld(src[x] + (size_t)(e.t0 + r) * D + c);
+                        y = siluf_(fmaf(wt.x, hst[0], fmaf(wt.y, hst[1], fmaf(wt.z, hst[2], wt.w * xin))));
+                        hst[0] = hst[1]; hst[1] = hst[2]; hst[2] = xin;
+                    }
+                    dst[x][r * kD + i] = y;
                 }
-                dst[x][r * kD + i] = y;
             }
         }
         // 2. gates: gk = gmin * sigmoid(exp(A_log) (z + dt)), cumulative over rows
@@ -160,7 +237,11 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
         for (int rr = 0; rr < 32; ++rr) {
             const int r = r0 + rr;
             float gk = 0.f;
-            if (r < n) gk = gmin * sigmoidf_(eA * (IO<T>::ld(z + (size_t)(e.t0 + r) * D + c) + dt));
+            if (r < n) {
+                const float zz = kStage ? IO<T>::ld(raw + ((size_t)3 * kRows + r + 3) * kD + i)
+                                        : IO<T>::ld(z + (size_t)(e.t0 + r) * D + c);
+                gk = gmin * sigmoidf_(eA * (zz + dt));
+            }
             acc += gk;
             G[r * kD + i] = acc;
         }
@@ -229,38 +310,90 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
         __syncthreads();
     }
 
-    float *out = chunks + (size_t)blockIdx.x * kChunkFloats;
-    float *W = out, *Up = W + kC * kD, *QG = Up + kC * kD, *KD = QG + kC * kD, *P = KD + kC * kD,
-          *GC = P + kC * kC;
-
-    // 5. Forward substitution (I + A) X = Diag(beta) B, one column per thread:
-    //    columns 0..127 of B are k o exp(G), 128..255 are v.
-    {
-        const int j = tid;
-        const bool isk = j < kD;
-        const int cj = isk ? j : j - kD;
-        float X[kC];
+    if constexpr (TC) {
+        unsigned char *blk = chunks + (size_t)blockIdx.x * kTcChunkBytes;
+        // operand tiles are built in the (now free) KRT / KL / QL region, P in the A region
+        unsigned char *tW = reinterpret_cast<unsigned char *>(KRT);   // 16 KB
+        unsigned char *tQG = tW + 16384;                              // 16 KB
+        unsigned char *tKDT = reinterpret_cast<unsigned char *>(KL);  // 16 KB (KL + QL)
+        unsigned char *tP = reinterpret_cast<unsigned char *>(Am);    // 8 KB, after the solve
+        float *Up = reinterpret_cast<float *>(blk + kOffUp);
+        // 5. Forward substitution (I + A) X = Diag(beta) B, one column per thread:
+        //    columns 0..127 of B are k o exp(G) (-> W), 128..255 are v (-> U').
+        {
+            const int j = tid;
+            const bool isk = j < kD;
+            const int cj = isk ? j : j - kD;
+            float X[kC];
 #pragma unroll
-        for (int r = 0; r < kC; ++r) {
-            const float bb = isk ? Yk[r * kD + cj] * expf(G[r * kD + cj]) : Yv[r * kD + cj];
-            float x = sbeta[r] * bb;
+            for (int r = 0; r < kC; ++r) {
+                const float bb = isk ? Yk[r * kD + cj] * expf(G[r * kD + cj]) : Yv[r * kD + cj];
+                float x = sbeta[r] * bb;
 #pragma unroll
-            for (int i = 0; i < r; ++i) x = fmaf(-Am[r * kC + i], X[i], x);
-            X[r] = x;
+                for (int i = 0; i < r; ++i) x = fmaf(-Am[r * kC + i], X[i], x);
+                X[r] = x;
+            }
+            if (isk) {
+#pragma unroll
+                for (int r = 0; r < kC; ++r) st_bf16(tW, tc::kmajor_off(r, cj, kD), X[r]);
+            } else {
+#pragma unroll
+                for (int r = 0; r < kC; ++r) Up[r * kD + cj] = X[r];
+            }
         }
-        float *dstc = isk ? W : Up;
+        // 6. Q o exp(G) and (K o exp(G_last - G))^T tiles, the chunk decay
+        for (int e2 = tid; e2 < kC * kD; e2 += 256) {
+            const int r = e2 / kD, c = e2 - r * kD;
+            const float g = G[r * kD + c];
+            st_bf16(tQG, tc::kmajor_off(r, c, kD), Yq[e2] * expf(g));
+            st_bf16(tKDT, tc::kmajor_off(c, r, kC), Yk[e2] * expf(G[(n - 1) * kD + c] - g));
+        }
+        if (tid < kD) reinterpret_cast<float *>(blk + kOffG)[tid] = expf(G[(n - 1) * kD + tid]);
+        __syncthreads();  // the solve no longer reads A
+        for (int e2 = tid; e2 < kC * kC; e2 += 256) {
+            const int r = e2 / kC, i = e2 - r * kC;
+            st_bf16(tP, tc::kmajor_off(r, i, kC), Pm[e2]);
+        }
+        __syncthreads();
+        for (int o = tid * 16; o < 32768; o += 256 * 16)  // W and QG
+            *reinterpret_cast<uint4 *>(blk + kOffW + o) = *reinterpret_cast<const uint4 *>(tW + o);
+        for (int o = tid * 16; o < 8192; o += 256 * 16)
+            *reinterpret_cast<uint4 *>(blk + kOffP + o) = *reinterpret_cast<const uint4 *>(tP + o);
+        for (int o = tid * 16; o < 16384; o += 256 * 16)
+            *reinterpret_cast<uint4 *>(blk + kOffKDT + o) = *reinterpret_cast<const uint4 *>(tKDT + o);
+    } else {
+        float *out = reinterpret_cast<float *>(chunks) + (size_t)blockIdx.x * kChunkFloats;
+        float *W = out, *Up = W + kC * kD, *QG = Up + kC * kD, *KD = QG + kC * kD, *P = KD + kC * kD,
+              *GC = P + kC * kC;
+        // 5. Forward substitution (I + A) X = Diag(beta) B, one column per thread:
+        //    columns 0..127 of B are k o exp(G), 128..255 are v.
+        {
+            const int j = tid;
+            const bool isk = j < kD;
+            const int cj = isk ? j : j - kD;
+            float X[kC];
 #pragma unroll
-        for (int r = 0; r < kC; ++r) dstc[r * kD + cj] = X[r];
+            for (int r = 0; r < kC; ++r) {
+                const float bb = isk ? Yk[r * kD + cj] * expf(G[r * kD + cj]) : Yv[r * kD + cj];
+                float x = sbeta[r] * bb;
+#pragma unroll
+                for (int i = 0; i < r; ++i) x = fmaf(-Am[r * kC + i], X[i], x);
+                X[r] = x;
+            }
+            float *dstc = isk ? W : Up;
+#pragma unroll
+            for (int r = 0; r < kC; ++r) dstc[r * kD + cj] = X[r];
+        }
+        // 6. The remaining chunk factors.
+        for (int e2 = tid; e2 < kC * kD; e2 += 256) {
+            const int r = e2 / kD, c = e2 - r * kD;
+            const float g = G[r * kD + c];
+            QG[e2] = Yq[e2] * expf(g);
+            KD[e2] = Yk[e2] * expf(G[(n - 1) * kD + c] - g);
+        }
+        for (int e2 = tid; e2 < kC * kC; e2 += 256) P[e2] = Pm[e2];
+        if (tid < kD) GC[tid] = expf(G[(n - 1) * kD + tid]);
     }
-    // 6. The remaining chunk factors.
-    for (int e2 = tid; e2 < kC * kD; e2 += 256) {
-        const int r = e2 / kD, c = e2 - r * kD;
-        const float g = G[r * kD + c];
-        QG[e2] = Yq[e2] * expf(g);
-        KD[e2] = Yk[e2] * expf(G[(n - 1) * kD + c] - g);
-    }
-    for (int e2 = tid; e2 < kC * kC; e2 += 256) P[e2] = Pm[e2];
-    if (tid < kD) GC[tid] = expf(G[(n - 1) * kD + tid]);
 }
 
 // ---------------------------------------------------------------- state pass
@@ -401,6 +534,220 @@ state_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__res
     }
 }
 
+// ---------------------------------------------------------------- state pass on tensor cores
+// One CTA (128 threads) per (sequence, head). Thread v owns TMEM lane v, i.e. value index v:
+//   D1 = S^T W^T     [v][r]  TMEM columns   0.. 63
+//   D2 = S^T QG^T    [v][r]  TMEM columns  64..127, then += U^T P^T  -> O^T
+//   D3 = S^T         [v][k]  TMEM columns 128..255, FP32 state, scaled by gC and += U^T KD
+// S^T is also kept in shared memory as a BF16 A operand. Per chunk:
+//   MMA D1, D2 | scale D3 by gC | U^T = U'^T - D1 -> BF16 | MMA D2 += U^T P^T, D3 += U^T KD |
+//   O^T -> gated RMSNorm -> out | S^T operand refreshed from D3 | next chunk's block requested.
+// The chunk blocks arrive by bulk copy into two shared-memory stages. Every wait is bounded;
+// on expiry the error word gets KDA_ERR_TIMEOUT and the CTA drains and returns.
+template <typename T>
+__global__ void __launch_bounds__(128, 1)
+state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__restrict__ err,
+                const int32_t *__restrict__ slots, int H, int max_slots,
+                const ChunkEntry *__restrict__ table, const int32_t *__restrict__ seq_first,
+                const unsigned char *__restrict__ chunks,
+                const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                const T *__restrict__ g, const float *__restrict__ norm_w, T *__restrict__ out, float rms_eps)
+{
+    extern __shared__ __align__(1024) float smf[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(smf);
+    // [stage 0 | stage 1 | S^T | U^T | gC x2 | red | barriers]; operand tiles 1024-aligned
+    unsigned char *sST = sm + 2 * kTcStageBytes;           // S^T [v][k] BF16, K-major, 32 KB
+    unsigned char *sUT = sST + 32768;                      // U^T [v][r] BF16, K-major, 16 KB
+    float *sgam = reinterpret_cast<float *>(sUT + 16384);  // [2 stages][128] chunk decay
+    float *red = sgam + 2 * kD;                            // [4 warps][64 tokens]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(red + 4 * kC);  // full[0..1], mma1, mma2
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
+
+    const int h = blockIdx.x, seq = blockIdx.y;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int slot = slots[seq];
+    if (slot < 0 || slot >= max_slots) {
+        if (tid == 0) atomicExch(err, kErrBadSlot);
+        return;
+    }
+    const size_t D = (size_t)H * kD;
+    const int c_first = seq_first[seq], c_last = seq_first[seq + 1];
+    float *Sg = S_all + ((size_t)slot * H + h) * kD * kD;
+
+    if (w == 0) tc::tmem_alloc(tslot, 256);
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tb = *tslot;
+    const uint32_t lanes = (uint32_t)(32 * w) << 16;  // this warp's TMEM lane quarter
+    const uint32_t tD1 = tb + lanes, tD2 = tb + lanes + 64, tD3 = tb + lanes + 128;
+
+    auto issue = [&](int stage, int ci) {  // thread 0 only
+        const unsigned char *src = chunks + ((size_t)ci * H + h) * kTcChunkBytes;
+        mbar_arrive_expect_tx(&bar[stage], kTcChunkBytes);
+        bulk_g2s(sm + stage * kTcStageBytes, src, kTcStageBytes, &bar[stage]);
+        bulk_g2s(sgam + stage * kD, src + kOffG, kD * 4, &bar[stage]);
+    };
+
+    // initial state: column v of S -> row v of D3 (FP32) and of the BF16 operand
+    float vals[16];
+#pragma unroll 1
+    for (int kc = 0; kc < 8; ++kc) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) vals[j] = Sg[(size_t)(16 * kc + j) * kD + tid];
+        tc::tmem_st16(tD3 + 16 * kc, vals);
+        store_row_bf16(sST, tid, 16 * kc, vals, kD);
+    }
+    tc::fence_smem_to_async();
+    if (tid == 0)
+        for (int i = 0; i < 2; ++i)
+            if (c_first + i < c_last) issue(i, c_first + i);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    const float nw = __ldg(norm_w + tid);
+    constexpr uint32_t id64 = tc::idesc_bf16(128, 64), id128 = tc::idesc_bf16(128, 128);
+    uint32_t ph1 = 0, ph2 = 0;
+    bool good = true, aborted = false;
+    int it = 0;
+    for (int ci = c_first; ci < c_last; ++ci, ++it) {
+        const int st = it & 1;
+        const unsigned char *stage = sm + st * kTcStageBytes;
+        const ChunkEntry e = table[ci];
+        // this chunk's output-gate logits for column v; their latency hides behind the MMAs
+        float gl[kC];
+#pragma unroll
+        for (int r = 0; r < kC; ++r)
+            gl[r] = r < e.n ? IO<T>::ld(g + (size_t)(e.t0 + r) * D + (size_t)h * kD + tid) : 0.f;
+
+        good &= mbar_wait_bounded(&bar[st], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
+        tc::fence_after_sync();
+        if (tid == 0 && good) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                tc::mma_bf16(tb, tc::kmajor_desc(sST, kk, kD), tc::kmajor_desc(stage + kOffW, kk, kD), id64, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                tc::mma_bf16(tb + 64, tc::kmajor_desc(sST, kk, kD), tc::kmajor_desc(stage + kOffQG, kk, kD), id64,
+                             kk > 0);
+            tc::mma_commit(&bar[2]);
+        }
+        // while they run: D3 = Diag(gC) applied to S^T columns
+        const float *gam = sgam + st * kD;
+#pragma unroll 1
+        for (int kc = 0; kc < 8; ++kc) {
+            tc::tmem_ld16(tD3 + 16 * kc, vals);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) vals[j] *= gam[16 * kc + j];
+            tc::tmem_st16(tD3 + 16 * kc, vals);
+        }
+        good &= mbar_wait_bounded(&bar[2], ph1, kTcWaitLimit);
+        ph1 ^= 1u;
+        tc::fence_after_sync();
+        // U^T = U'^T - (W S)^T, as the BF16 A operand
+        const float *Up = reinterpret_cast<const float *>(stage + kOffUp);
+#pragma unroll 1
+        for (int rg = 0; rg < 4; ++rg) {
+            tc::tmem_ld16(tD1 + 16 * rg, vals);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) vals[j] = Up[(16 * rg + j) * kD + tid] - vals[j];
+            store_row_bf16(sUT, tid, 16 * rg, vals, kC);
+        }
+        tc::fence_smem_to_async();
+        tc::fence_before_sync();
+        if (__syncthreads_or(!good)) { aborted = true; break; }
+        tc::fence_after_sync();
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc::mma_bf16(tb + 64, tc::kmajor_desc(sUT, kk, kC), tc::kmajor_desc(stage + kOffP, kk, kC), id64, 1);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc::mma_bf16(tb + 128, tc::kmajor_desc(sUT, kk, kC), tc::kmajor_desc(stage + kOffKDT, kk, kC), id128,
+                             1);
+            tc::mma_commit(&bar[3]);
+        }
+        good &= mbar_wait_bounded(&bar[3], ph2, kTcWaitLimit);
+        ph2 ^= 1u;
+        tc::fence_after_sync();
+        // O^T row v (64 tokens) and the per-token sum of squares over v
+        float o[kC];
+#pragma unroll
+        for (int rg = 0; rg < 4; ++rg) tc::tmem_ld16(tD2 + 16 * rg, o + 16 * rg);
+#pragma unroll
+        for (int r = 0; r < kC; ++r) {
+            const float s2 = warp_sum(o[r] * o[r]);
+            if (lane == 0) red[w * kC + r] = s2;
+        }
+        // refresh the S^T operand from the updated FP32 state
+#pragma unroll 1
+        for (int kc = 0; kc < 8; ++kc) {
+            tc::tmem_ld16(tD3 + 16 * kc, vals);
+            store_row_bf16(sST, tid, 16 * kc, vals, kD);
+        }
+        tc::fence_smem_to_async();
+        tc::fence_before_sync();
+        if (__syncthreads_or(!good)) { aborted = true; break; }
+        tc::fence_after_sync();
+        // the stage is consumed (both MMA groups done, U' and gC read): request chunk ci + 2
+        if (tid == 0 && ci + 2 < c_last) issue(st, ci + 2);
+#pragma unroll
+        for (int r = 0; r < kC; ++r) {
+            if (r < e.n) {
+                const float ms = (red[r] + red[kC + r] + red[2 * kC + r] + red[3 * kC + r]) * (1.0f / kD);
+                const float y = sigmoidf_(gl[r]) * nw * (o[r] / sqrtf(ms + rms_eps));
+                IO<T>::st(out + (size_t)(e.t0 + r) * D + (size_t)h * kD + tid, y);
+            }
+        }
+    }
+
+    if (aborted) {
+        if (tid == 0) {
+            atomicExch(err, KDA_ERR_TIMEOUT);
+            // let this CTA's outstanding copies and MMAs finish before its memory goes away
+            for (int j = 0; j < 2; ++j) {
+                const int it2 = it + j;
+                if (c_first + it2 < c_last) mbar_wait_bounded(&bar[it2 & 1], (uint32_t)((it2 >> 1) & 1), kTcWaitLimit);
+            }
+            mbar_wait_bounded(&bar[2], ph1, kTcWaitLimit);
+            mbar_wait_bounded(&bar[3], ph2, kTcWaitLimit);
+        }
+    } else {
+        // final state back to HBM (column v of S from row v of D3)
+#pragma unroll 1
+        for (int kc = 0; kc < 8; ++kc) {
+            tc::tmem_ld16(tD3 + 16 * kc, vals);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) Sg[(size_t)(16 * kc + j) * kD + tid] = vals[j];
+        }
+        // new conv history (the last K-1 raw inputs of the sequence)
+        if (c_last > c_first) {
+            const int start = table[c_first].t0;
+            const int len = table[c_last - 1].t0 + table[c_last - 1].n - start;
+            T *tl = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD + tid;
+            const T *src[3] = {q, k, v};
+#pragma unroll
+            for (int x = 0; x < 3; ++x) {
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int pos = len - 3 + j;
+                    const T val = pos >= 0 ? src[x][(size_t)(start + pos) * D + (size_t)h * kD + tid]
+                                           : tl[(size_t)(x * 3 + (pos + 3)) * D];
+                    tl[(size_t)(x * 3 + j) * D] = val;
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (w == 0) tc::tmem_dealloc(tb, 256);
+}
+
 // ---------------------------------------------------------------- epilogue
 template <typename T>
 __global__ void __launch_bounds__(256)
@@ -428,13 +775,15 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
                          const void *q, const void *k, const void *v, const void *z, const void *b,
                          const void *g, void *out, void *ws, cudaStream_t stream)
 {
+    // BF16 I/O runs the tensor-core state pass; FP32 I/O keeps every contraction in FP32.
+    constexpr bool kTC = sizeof(T) == 2;
     const kda_config_t &c = st.cfg;
     const int H = c.num_heads;
-    const WsLayout L = ws_layout(H, total_chunks, total_T, N);
+    const WsLayout L = ws_layout(H, total_chunks, total_T, N, kTC);
     char *base = static_cast<char *>(ws);
     ChunkEntry *table = reinterpret_cast<ChunkEntry *>(base + L.table);
     int32_t *seq_first = reinterpret_cast<int32_t *>(base + L.seq_first);
-    float *chunks = reinterpret_cast<float *>(base + L.chunks);
+    unsigned char *chunks = reinterpret_cast<unsigned char *>(base + L.chunks);
     float *obuf = reinterpret_cast<float *>(base + L.obuf);
 
     chunk_table_kernel<<<1, 32, 0, stream>>>(cu, N, total_T, total_chunks, table, seq_first, st.err);
@@ -442,37 +791,46 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
     if (e != cudaSuccess) return e;
     if (total_chunks > 0) {
         const int prep_smem = kPrepSmemFloats * (int)sizeof(float);
-        e = cudaFuncSetAttribute(prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
+        e = cudaFuncSetAttribute(prep_kernel<T, kTC>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
         if (e != cudaSuccess) return e;
-        prep_kernel<T><<<(unsigned)(total_chunks * H), 256, prep_smem, stream>>>(
+        prep_kernel<T, kTC><<<(unsigned)(total_chunks * H), 256, prep_smem, stream>>>(
             p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
             (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, chunks,
             c.gate_lower_bound, c.l2_eps, c.q_scale);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const int state_smem = kStateSmemFloats * (int)sizeof(float);
-    e = cudaFuncSetAttribute(state_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem);
-    if (e != cudaSuccess) return e;
-    state_kernel<T><<<dim3(kD / kVB, H, N), 256, state_smem, stream>>>(
-        st.S, (T *)st.tail, st.err, slots, H, st.max_slots, table, seq_first, chunks, obuf,
-        (const T *)q, (const T *)k, (const T *)v);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    if (total_T > 0) {
-        const int64_t rows = total_T * H;
-        epilogue_kernel<T><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(obuf, p.norm_w, (const T *)g,
-                                                                         (T *)out, rows, c.rms_eps);
+    if constexpr (kTC) {
+        e = cudaFuncSetAttribute(state_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateTcSmem);
+        if (e != cudaSuccess) return e;
+        state_tc_kernel<T><<<dim3(H, N), 128, kStateTcSmem, stream>>>(
+            st.S, (T *)st.tail, st.err, slots, H, st.max_slots, table, seq_first, chunks,
+            (const T *)q, (const T *)k, (const T *)v, (const T *)g, p.norm_w, (T *)out, c.rms_eps);
+        return cudaGetLastError();
+    } else {
+        const int state_smem = kStateSmemFloats * (int)sizeof(float);
+        e = cudaFuncSetAttribute(state_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem);
+        if (e != cudaSuccess) return e;
+        state_kernel<T><<<dim3(kD / kVB, H, N), 256, state_smem, stream>>>(
+            st.S, (T *)st.tail, st.err, slots, H, st.max_slots, table, seq_first,
+            reinterpret_cast<const float *>(chunks), obuf, (const T *)q, (const T *)k, (const T *)v);
         e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (total_T > 0) {
+            const int64_t rows = total_T * H;
+            epilogue_kernel<T><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(obuf, p.norm_w, (const T *)g,
+                                                                             (T *)out, rows, c.rms_eps);
+            e = cudaGetLastError();
+        }
+        return e;
     }
-    return e;
 }
 
 }  // namespace
 
 size_t prefill_workspace_bytes(const kda_config_t &cfg, int64_t total_chunks, int64_t total_T, int N)
 {
-    return ws_layout(cfg.num_heads, total_chunks, total_T, N).total;
+    return ws_layout(cfg.num_heads, total_chunks, total_T, N, cfg.io_dtype == KDA_BF16).total;
 }
 
 cudaError_t launch_prefill(const State &st, const kda_layer_params &p, const int32_t *slots,
