@@ -31,7 +31,8 @@ namespace {
 constexpr int kBlk = 16;                  // sub-block rows for the decay reference
 constexpr int kVB = 32;                   // v columns per state_kernel CTA
 constexpr int kChunkFloats = 4 * kC * kD + kC * kC + kD;  // W, U', QG, KD, P, gC
-constexpr int kPrepSmemFloats = 4 * kC * kD + 2 * kC * kC + kD * kC + 2 * kBlk * kD + kC;
+constexpr int kKRS = kC + 1;  // padded row of the transposed right factor (no bank conflicts)
+constexpr int kPrepSmemFloats = 4 * kC * kD + 2 * kC * kC + kD * kKRS + 2 * kBlk * kD + kC;
 constexpr int kStateSmemFloats = kD * kVB + 3 * kC * kD + 2 * kC * kVB + kC * kC + kD;
 
 // Tensor-core path (BF16 I/O): per (chunk, head) the prep kernel writes one block that
@@ -147,8 +148,8 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
     float *G = Yv + kC * kD;        // [C][d]   cumulative log decay
     float *Am = G + kC * kD;        // [C][C]   A (strict lower, beta folded)
     float *Pm = Am + kC * kC;       // [C][C]   P (inclusive lower)
-    float *KRT = Pm + kC * kC;      // [d][C]   k_i o exp(G_n - G_i), transposed
-    float *KL = KRT + kD * kC;      // [16][d]  k_r o exp(G_r - G_n)
+    float *KRT = Pm + kC * kC;      // [d][C+1] k_i o exp(G_n - G_i), transposed, padded rows
+    float *KL = KRT + kD * kKRS;    // [16][d]  k_r o exp(G_r - G_n)
     float *QL = KL + kBlk * kD;     // [16][d]  q_r o exp(G_r - G_n)
     float *sbeta = QL + kBlk * kD;  // [C]
 
@@ -166,7 +167,7 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
     constexpr int kRows = kC + 3;  // staged row j holds position j - 3 of the chunk
     T *raw = reinterpret_cast<T *>(Am);
     constexpr bool kStage = sizeof(T) == 2;
-    static_assert(!kStage || 4 * kRows * kD * sizeof(T) <= (2 * kC * kC + kD * kC + 2 * kBlk * kD) * sizeof(float),
+    static_assert(!kStage || 4 * kRows * kD * sizeof(T) <= (2 * kC * kC + kD * kKRS + 2 * kBlk * kD) * sizeof(float),
                   "raw staging must fit in the A/P/KRT/KL/QL region");
     if constexpr (kStage) {
         const T *srcs[4] = {q, k, v, z};
@@ -272,13 +273,14 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
     for (int R = 0; R < kC / kBlk; ++R) {
         const int nR = R * kBlk, m = nR + kBlk;
         {
-            const int i = tid & (kC - 1), cg = tid >> 6;
-            if (i < m) {
-                for (int cc = 0; cc < 32; ++cc) {
-                    const int c = cg * 32 + cc;
-                    KRT[c * kC + i] = Yk[i * kD + c] * expf(G[nR * kD + c] - G[i * kD + c]);
-                }
-            }
+            // thread (c, half): consecutive threads walk consecutive c, so the row reads of
+            // Yk / G and the padded transposed writes are both free of bank conflicts
+            const int c = tid & (kD - 1), ih = tid >> 7;
+            const float gn = G[nR * kD + c];
+            for (int i = 32 * ih; i < min(m, 32 * ih + 32); ++i)
+                KRT[c * kKRS + i] = Yk[i * kD + c] * expf(gn - G[i * kD + c]);
+        }
+        {
             for (int e2 = tid; e2 < kBlk * kD; e2 += 256) {
                 const int rr = e2 / kD, c = e2 - rr * kD;
                 const float f = expf(G[(nR + rr) * kD + c] - G[nR * kD + c]);
@@ -292,7 +294,7 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
             float a[4] = {0.f, 0.f, 0.f, 0.f}, p[4] = {0.f, 0.f, 0.f, 0.f};
             if (i < m) {
                 for (int c = 0; c < kD; ++c) {
-                    const float kr = KRT[c * kC + i];
+                    const float kr = KRT[c * kKRS + i];
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) {
                         a[qq] = fmaf(KL[(4 * rg + qq) * kD + c], kr, a[qq]);
@@ -328,10 +330,19 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 #pragma unroll
             for (int r = 0; r < kC; ++r) {
                 const float bb = isk ? Yk[r * kD + cj] * expf(G[r * kD + cj]) : Yv[r * kD + cj];
-                float x = sbeta[r] * bb;
+                // four independent partial sums over i, A read 4 at a time
+                float x0 = sbeta[r] * bb, x1 = 0.f, x2 = 0.f, x3 = 0.f;
 #pragma unroll
-                for (int i = 0; i < r; ++i) x = fmaf(-Am[r * kC + i], X[i], x);
-                X[r] = x;
+                for (int i = 0; i + 4 <= r; i += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Am + r * kC + i);
+                    x0 = fmaf(-a4.x, X[i], x0);
+                    x1 = fmaf(-a4.y, X[i + 1], x1);
+                    x2 = fmaf(-a4.z, X[i + 2], x2);
+                    x3 = fmaf(-a4.w, X[i + 3], x3);
+                }
+#pragma unroll
+                for (int i = r & ~3; i < r; ++i) x0 = fmaf(-Am[r * kC + i], X[i], x0);
+                X[r] = (x0 + x1) + (x2 + x3);
             }
             if (isk) {
 #pragma unroll
@@ -375,10 +386,19 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 #pragma unroll
             for (int r = 0; r < kC; ++r) {
                 const float bb = isk ? Yk[r * kD + cj] * expf(G[r * kD + cj]) : Yv[r * kD + cj];
-                float x = sbeta[r] * bb;
+                // four independent partial sums over i, A read 4 at a time
+                float x0 = sbeta[r] * bb, x1 = 0.f, x2 = 0.f, x3 = 0.f;
 #pragma unroll
-                for (int i = 0; i < r; ++i) x = fmaf(-Am[r * kC + i], X[i], x);
-                X[r] = x;
+                for (int i = 0; i + 4 <= r; i += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Am + r * kC + i);
+                    x0 = fmaf(-a4.x, X[i], x0);
+                    x1 = fmaf(-a4.y, X[i + 1], x1);
+                    x2 = fmaf(-a4.z, X[i + 2], x2);
+                    x3 = fmaf(-a4.w, X[i + 3], x3);
+                }
+#pragma unroll
+                for (int i = r & ~3; i < r; ++i) x0 = fmaf(-Am[r * kC + i], X[i], x0);
+                X[r] = (x0 + x1) + (x2 + x3);
             }
             float *dstc = isk ? W : Up;
 #pragma unroll
@@ -535,17 +555,20 @@ state_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__res
 }
 
 // ---------------------------------------------------------------- state pass on tensor cores
-// One CTA (128 threads) per (sequence, head). Thread v owns TMEM lane v, i.e. value index v:
+// One CTA (256 threads) per (sequence, head). TMEM lane v holds value index v:
 //   D1 = S^T W^T     [v][r]  TMEM columns   0.. 63
 //   D2 = S^T QG^T    [v][r]  TMEM columns  64..127, then += U^T P^T  -> O^T
 //   D3 = S^T         [v][k]  TMEM columns 128..255, FP32 state, scaled by gC and += U^T KD
-// S^T is also kept in shared memory as a BF16 A operand. Per chunk:
-//   MMA D1, D2 | scale D3 by gC | U^T = U'^T - D1 -> BF16 | MMA D2 += U^T P^T, D3 += U^T KD |
-//   O^T -> gated RMSNorm -> out | S^T operand refreshed from D3 | next chunk's block requested.
-// The chunk blocks arrive by bulk copy into two shared-memory stages. Every wait is bounded;
-// on expiry the error word gets KDA_ERR_TIMEOUT and the CTA drains and returns.
+// Warps w and w+4 share lane quarter w%4 and split the columns in halves (grp = w/4).
+// S^T is also kept in shared memory as a BF16 A operand. Per chunk c:
+//   [MMA1(c): D1, D2 issued at the end of c-1] | scale D3 by gC | U^T = U'^T - D1 -> BF16 |
+//   MMA2(c): D2 += U^T P^T, D3 += U^T KD | O^T -> registers, sums of squares | S^T operand
+//   refreshed from D3 | chunk c+2 requested, MMA1(c+1) issued | gated RMSNorm of c written out
+// so the output epilogue of c overlaps MMA1(c+1). Chunk blocks arrive by bulk copy into two
+// shared-memory stages. Every wait is bounded; on expiry the error word gets KDA_ERR_TIMEOUT
+// and the CTA drains what it issued and returns.
 template <typename T>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
 state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__restrict__ err,
                 const int32_t *__restrict__ slots, int H, int max_slots,
                 const ChunkEntry *__restrict__ table, const int32_t *__restrict__ seq_first,
@@ -559,12 +582,14 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     unsigned char *sST = sm + 2 * kTcStageBytes;           // S^T [v][k] BF16, K-major, 32 KB
     unsigned char *sUT = sST + 32768;                      // U^T [v][r] BF16, K-major, 16 KB
     float *sgam = reinterpret_cast<float *>(sUT + 16384);  // [2 stages][128] chunk decay
-    float *red = sgam + 2 * kD;                            // [4 warps][64 tokens]
+    float *red = sgam + 2 * kD;                            // [4 lane quarters][64 tokens]
     uint64_t *bar = reinterpret_cast<uint64_t *>(red + 4 * kC);  // full[0..1], mma1, mma2
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
 
     const int h = blockIdx.x, seq = blockIdx.y;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int qtr = w & 3, grp = w >> 2;
+    const int vi = 32 * qtr + lane;  // value index = TMEM lane of this thread
     const int slot = slots[seq];
     if (slot < 0 || slot >= max_slots) {
         if (tid == 0) atomicExch(err, kErrBadSlot);
@@ -583,8 +608,10 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    const uint32_t lanes = (uint32_t)(32 * w) << 16;  // this warp's TMEM lane quarter
+    const uint32_t lanes = (uint32_t)(32 * qtr) << 16;  // this warp's TMEM lane quarter
     const uint32_t tD1 = tb + lanes, tD2 = tb + lanes + 64, tD3 = tb + lanes + 128;
+    const int k0 = 64 * grp;   // this thread's state columns k0 .. k0+63
+    const int r0 = 32 * grp;   // this thread's tokens r0 .. r0+31
 
     auto issue = [&](int stage, int ci) {  // thread 0 only
         const unsigned char *src = chunks + ((size_t)ci * H + h) * kTcChunkBytes;
@@ -592,16 +619,29 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         bulk_g2s(sm + stage * kTcStageBytes, src, kTcStageBytes, &bar[stage]);
         bulk_g2s(sgam + stage * kD, src + kOffG, kD * 4, &bar[stage]);
     };
-
-    // initial state: column v of S -> row v of D3 (FP32) and of the BF16 operand
-    float vals[16];
-#pragma unroll 1
-    for (int kc = 0; kc < 8; ++kc) {
+    constexpr uint32_t id64 = tc::idesc_bf16(128, 64), id128 = tc::idesc_bf16(128, 128);
+    auto mma1 = [&](const unsigned char *stage) {  // thread 0 only: D1 = S^T W^T, D2 = S^T QG^T
 #pragma unroll
-        for (int j = 0; j < 16; ++j) vals[j] = Sg[(size_t)(16 * kc + j) * kD + tid];
-        tc::tmem_st16(tD3 + 16 * kc, vals);
-        store_row_bf16(sST, tid, 16 * kc, vals, kD);
+        for (int kk = 0; kk < 8; ++kk)
+            tc::mma_bf16(tb, tc::kmajor_desc(sST, kk, kD), tc::kmajor_desc(stage + kOffW, kk, kD), id64, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            tc::mma_bf16(tb + 64, tc::kmajor_desc(sST, kk, kD), tc::kmajor_desc(stage + kOffQG, kk, kD), id64, kk > 0);
+        tc::mma_commit(&bar[2]);
+    };
+
+    // initial state: S[k][v] -> D3 row v (FP32) and the BF16 operand row v
+    float vals[32];
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        const int kb = k0 + 32 * half;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) vals[j] = Sg[(size_t)(kb + j) * kD + vi];
+        tc::tmem_st32(tD3 + kb, vals);
+        store_row_bf16(sST, vi, kb, vals, kD);
+        store_row_bf16(sST, vi, kb + 16, vals + 16, kD);
     }
+    tc::tmem_wait_st();
     tc::fence_smem_to_async();
     if (tid == 0)
         for (int i = 0; i < 2; ++i)
@@ -609,54 +649,53 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-
-    const float nw = __ldg(norm_w + tid);
-    constexpr uint32_t id64 = tc::idesc_bf16(128, 64), id128 = tc::idesc_bf16(128, 128);
-    uint32_t ph1 = 0, ph2 = 0;
     bool good = true, aborted = false;
+    if (tid == 0 && c_first < c_last) {
+        good &= mbar_wait_bounded(&bar[0], 0, kTcWaitLimit);
+        if (good) mma1(sm);
+    }
+
+    const float nw = __ldg(norm_w + vi);
+    uint32_t ph1 = 0, ph2 = 0;
     int it = 0;
     for (int ci = c_first; ci < c_last; ++ci, ++it) {
         const int st = it & 1;
         const unsigned char *stage = sm + st * kTcStageBytes;
         const ChunkEntry e = table[ci];
-        // this chunk's output-gate logits for column v; their latency hides behind the MMAs
-        float gl[kC];
+        // output-gate logits of this thread's tokens; their latency hides behind the MMAs
+        float gl[32];
 #pragma unroll
-        for (int r = 0; r < kC; ++r)
-            gl[r] = r < e.n ? IO<T>::ld(g + (size_t)(e.t0 + r) * D + (size_t)h * kD + tid) : 0.f;
+        for (int r = 0; r < 32; ++r)
+            gl[r] = r0 + r < e.n ? IO<T>::ld(g + (size_t)(e.t0 + r0 + r) * D + (size_t)h * kD + vi) : 0.f;
 
         good &= mbar_wait_bounded(&bar[st], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
-        tc::fence_after_sync();
-        if (tid == 0 && good) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tb, tc::kmajor_desc(sST, kk, kD), tc::kmajor_desc(stage + kOffW, kk, kD), id64, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tb + 64, tc::kmajor_desc(sST, kk, kD), tc::kmajor_desc(stage + kOffQG, kk, kD), id64,
-                             kk > 0);
-            tc::mma_commit(&bar[2]);
-        }
-        // while they run: D3 = Diag(gC) applied to S^T columns
-        const float *gam = sgam + st * kD;
+        // D3 = Diag(gC) on its columns, while MMA1 runs on D1 / D2
+        {
+            const float *gam = sgam + st * kD + k0;
+            uint32_t raw[32];
 #pragma unroll 1
-        for (int kc = 0; kc < 8; ++kc) {
-            tc::tmem_ld16(tD3 + 16 * kc, vals);
+            for (int half = 0; half < 2; ++half) {
+                tc::tmem_ld32_nowait(tD3 + k0 + 32 * half, raw);
+                tc::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) vals[j] *= gam[16 * kc + j];
-            tc::tmem_st16(tD3 + 16 * kc, vals);
+                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]) * gam[32 * half + j];
+                tc::tmem_st32(tD3 + k0 + 32 * half, vals);
+            }
+            tc::tmem_wait_st();
         }
         good &= mbar_wait_bounded(&bar[2], ph1, kTcWaitLimit);
         ph1 ^= 1u;
         tc::fence_after_sync();
-        // U^T = U'^T - (W S)^T, as the BF16 A operand
-        const float *Up = reinterpret_cast<const float *>(stage + kOffUp);
-#pragma unroll 1
-        for (int rg = 0; rg < 4; ++rg) {
-            tc::tmem_ld16(tD1 + 16 * rg, vals);
+        // U^T = U'^T - (W S)^T on this thread's tokens, as the BF16 A operand
+        {
+            const float *Up = reinterpret_cast<const float *>(stage + kOffUp);
+            uint32_t raw[32];
+            tc::tmem_ld32_nowait(tD1 + r0, raw);
+            tc::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) vals[j] = Up[(16 * rg + j) * kD + tid] - vals[j];
-            store_row_bf16(sUT, tid, 16 * rg, vals, kC);
+            for (int j = 0; j < 32; ++j) vals[j] = Up[(r0 + j) * kD + vi] - __uint_as_float(raw[j]);
+            store_row_bf16(sUT, vi, r0, vals, kC);
+            store_row_bf16(sUT, vi, r0 + 16, vals + 16, kC);
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
@@ -675,33 +714,53 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         good &= mbar_wait_bounded(&bar[3], ph2, kTcWaitLimit);
         ph2 ^= 1u;
         tc::fence_after_sync();
-        // O^T row v (64 tokens) and the per-token sum of squares over v
-        float o[kC];
+        // O^T on this thread's tokens, their partial sums of squares over this warp's 32 v
+        float o[32];
+        {
+            uint32_t raw[32];
+            tc::tmem_ld32_nowait(tD2 + r0, raw);
+            tc::tmem_wait_ld();
 #pragma unroll
-        for (int rg = 0; rg < 4; ++rg) tc::tmem_ld16(tD2 + 16 * rg, o + 16 * rg);
+            for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(raw[j]);
+        }
 #pragma unroll
-        for (int r = 0; r < kC; ++r) {
+        for (int r = 0; r < 32; ++r) {
             const float s2 = warp_sum(o[r] * o[r]);
-            if (lane == 0) red[w * kC + r] = s2;
+            if (lane == 0) red[qtr * kC + r0 + r] = s2;
         }
         // refresh the S^T operand from the updated FP32 state
+        {
+            uint32_t raw[32];
 #pragma unroll 1
-        for (int kc = 0; kc < 8; ++kc) {
-            tc::tmem_ld16(tD3 + 16 * kc, vals);
-            store_row_bf16(sST, tid, 16 * kc, vals, kD);
+            for (int half = 0; half < 2; ++half) {
+                tc::tmem_ld32_nowait(tD3 + k0 + 32 * half, raw);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
+                store_row_bf16(sST, vi, k0 + 32 * half, vals, kD);
+                store_row_bf16(sST, vi, k0 + 32 * half + 16, vals + 16, kD);
+            }
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
         if (__syncthreads_or(!good)) { aborted = true; break; }
         tc::fence_after_sync();
-        // the stage is consumed (both MMA groups done, U' and gC read): request chunk ci + 2
-        if (tid == 0 && ci + 2 < c_last) issue(st, ci + 2);
+        if (tid == 0) {
+            // the stage is consumed (both MMA groups done, U' and gC read): request chunk ci + 2,
+            // then start the next chunk's first MMAs before this chunk's epilogue
+            if (ci + 2 < c_last) issue(st, ci + 2);
+            if (ci + 1 < c_last) {
+                good &= mbar_wait_bounded(&bar[st ^ 1], (uint32_t)(((it + 1) >> 1) & 1), kTcWaitLimit);
+                if (good) mma1(sm + (st ^ 1) * kTcStageBytes);
+            }
+        }
 #pragma unroll
-        for (int r = 0; r < kC; ++r) {
-            if (r < e.n) {
-                const float ms = (red[r] + red[kC + r] + red[2 * kC + r] + red[3 * kC + r]) * (1.0f / kD);
-                const float y = sigmoidf_(gl[r]) * nw * (o[r] / sqrtf(ms + rms_eps));
-                IO<T>::st(out + (size_t)(e.t0 + r) * D + (size_t)h * kD + tid, y);
+        for (int r = 0; r < 32; ++r) {
+            if (r0 + r < e.n) {
+                const int rr = r0 + r;
+                const float ms = (red[rr] + red[kC + rr] + red[2 * kC + rr] + red[3 * kC + rr]) * (1.0f / kD);
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-gl[r]));
+                IO<T>::st(out + (size_t)(e.t0 + rr) * D + (size_t)h * kD + vi, sg * nw * (o[r] * rsqrtf(ms + rms_eps)));
             }
         }
     }
@@ -709,7 +768,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     if (aborted) {
         if (tid == 0) {
             atomicExch(err, KDA_ERR_TIMEOUT);
-            // let this CTA's outstanding copies and MMAs finish before its memory goes away
+            // let this CTA's outstanding copies and MMAs land before its memory goes away
             for (int j = 0; j < 2; ++j) {
                 const int it2 = it + j;
                 if (c_first + it2 < c_last) mbar_wait_bounded(&bar[it2 & 1], (uint32_t)((it2 >> 1) & 1), kTcWaitLimit);
@@ -718,15 +777,17 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             mbar_wait_bounded(&bar[3], ph2, kTcWaitLimit);
         }
     } else {
-        // final state back to HBM (column v of S from row v of D3)
+        // final state back to HBM: S[k][v] from D3 row v, columns of this thread's half
+        uint32_t raw[32];
 #pragma unroll 1
-        for (int kc = 0; kc < 8; ++kc) {
-            tc::tmem_ld16(tD3 + 16 * kc, vals);
+        for (int half = 0; half < 2; ++half) {
+            tc::tmem_ld32_nowait(tD3 + k0 + 32 * half, raw);
+            tc::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) Sg[(size_t)(16 * kc + j) * kD + tid] = vals[j];
+            for (int j = 0; j < 32; ++j) Sg[(size_t)(k0 + 32 * half + j) * kD + vi] = __uint_as_float(raw[j]);
         }
         // new conv history (the last K-1 raw inputs of the sequence)
-        if (c_last > c_first) {
+        if (c_last > c_first && tid < kD) {
             const int start = table[c_first].t0;
             const int len = table[c_last - 1].t0 + table[c_last - 1].n - start;
             T *tl = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD + tid;
@@ -803,7 +864,7 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
     if constexpr (kTC) {
         e = cudaFuncSetAttribute(state_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateTcSmem);
         if (e != cudaSuccess) return e;
-        state_tc_kernel<T><<<dim3(H, N), 128, kStateTcSmem, stream>>>(
+        state_tc_kernel<T><<<dim3(H, N), 256, kStateTcSmem, stream>>>(
             st.S, (T *)st.tail, st.err, slots, H, st.max_slots, table, seq_first, chunks,
             (const T *)q, (const T *)k, (const T *)v, (const T *)g, p.norm_w, (T *)out, c.rms_eps);
         return cudaGetLastError();
