@@ -416,6 +416,297 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
     }
 }
 
+// ---------------------------------------------------------------- prep on tensor cores
+// BF16 path, one CTA (256 threads) per (chunk, head). Differences from prep_kernel:
+//  * every decay factor is a running product of the per-token gates alpha_t = exp(gk_t) along
+//    the chunk (one thread per channel), not an exp of a difference of cumulative sums:
+//      exp(G_r - G_n) = prod_{t=n+1..r} alpha_t,  exp(G_r) = prod_{t<=r} alpha_t,
+//      exp(G_last - G_r) = prod_{t=r+1..last} alpha_t
+//    (all <= 1; on a block diagonal the right factor is the reciprocal of a product of at most
+//    15 gates, <= e^75, finite in FP32);
+//  * A and P come from tcgen05: for each 16-row block R an M = 128 tile whose rows 0..15 are
+//    k_r o exp(G_r - G_n) and rows 16..31 are q_r o exp(G_r - G_n) (rows 32..127 zero) times
+//    the block's right-factor tile k_i o exp(G_n - G_i) (N = 64 rows i, K = 128 channels).
+// Shared memory: FP32 [64][132] arrays (rows padded against bank conflicts) for q^, k^, v and
+// alpha, then one reused region: raw inputs -> MMA tiles -> output tiles + A.
+constexpr int kYS = kD + 4;                         // padded FP32 row
+constexpr int kPtY = 73728;                         // reused region
+constexpr int kPtOffW = 0, kPtOffQG = 16384, kPtOffKDT = 32768, kPtOffP = 49152, kPtOffA = 57344;
+constexpr int kPtOffTA = 0, kPtOffTB = 32768;       // MMA tiles (before the output tiles exist)
+constexpr int kPrepTcSmem = 4 * kC * kYS * 4 + kPtY + kC * 4 + 64;
+
+template <typename T>
+__global__ void __launch_bounds__(256, 1)
+prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
+               const float *__restrict__ A_log, const T *__restrict__ tail_all,
+               const int32_t *__restrict__ slots, int H, int max_slots,
+               const ChunkEntry *__restrict__ table,
+               const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+               const T *__restrict__ z, const T *__restrict__ bl,
+               unsigned char *__restrict__ chunks, int32_t *__restrict__ err,
+               float gmin, float l2_eps, float q_scale)
+{
+    extern __shared__ __align__(1024) float smf[];
+    float *Yq = smf;                                  // [64][132] q^
+    float *Yk = Yq + kC * kYS;                        // [64][132] k^
+    float *Yv = Yk + kC * kYS;                        // [64][132] v
+    float *AL = Yv + kC * kYS;                        // [64][132] alpha (1 beyond the chunk)
+    unsigned char *Y = reinterpret_cast<unsigned char *>(AL + kC * kYS);
+    float *sbeta = reinterpret_cast<float *>(Y + kPtY);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sbeta + kC);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 1);
+
+    const int chunk = blockIdx.x / H, h = blockIdx.x - (blockIdx.x / H) * H;
+    const ChunkEntry e = table[chunk];
+    if (e.n <= 0) return;  // empty entry: the chunk list was rejected
+    const int slot = slots[e.seq];
+    if (slot < 0 || slot >= max_slots) return;  // recorded by the state pass
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = e.n;
+    const size_t D = (size_t)H * kD;
+
+    if (warp == 0) tc::tmem_alloc(tslot, 256);
+    if (tid == 0) { mbar_init(bar, 1); fence_mbar_init(); }
+
+    // 0. raw q, k, v rows with 3 rows of history, and z, staged with asynchronous 16-byte
+    //    copies (zero-filled past the chunk); the beta logits are loaded meanwhile
+    constexpr int kRows = kC + 3;  // staged row j holds position j - 3 of the chunk
+    T *raw = reinterpret_cast<T *>(Y);
+    static_assert(4 * kRows * kD * sizeof(T) <= kPtY, "raw staging must fit in the reused region");
+    {
+        const T *srcs[4] = {q, k, v, z};
+        const T *tl0 = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD;
+        for (int e2 = tid; e2 < 4 * kRows * 16; e2 += 256) {
+            const int x = e2 / (kRows * 16), rem = e2 - x * (kRows * 16);
+            const int j = rem >> 4, vec = rem & 15;
+            const int p = j - 3;
+            const bool live = p < n && !(x == 3 && p < 0);
+            const int pos = e.pos0 + p;
+            const T *srcp = !live ? srcs[0] + (size_t)e.t0 * D + (size_t)h * kD  // any valid address
+                          : pos >= 0 ? srcs[x] + (size_t)(e.t0 + p) * D + (size_t)h * kD
+                                     : tl0 + (size_t)(x * 3 + (pos + 3)) * D;
+            cp_async16(raw + ((size_t)x * kRows + j) * kD + 8 * vec, reinterpret_cast<const uint4 *>(srcp) + vec,
+                       live ? 16u : 0u);
+        }
+    }
+    unsigned short braw = 0;
+    if (tid < kC && tid < n) braw = ld_nc_u16(bl + (size_t)(e.t0 + tid) * H + h);
+    cp_async_wait_all();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tb = *tslot;
+    if (tid < kC) sbeta[tid] = tid < n ? sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
+
+    // 1. conv + SiLU (sliding window in registers) and 2. the gates, thread (i, half)
+    {
+        const int i = tid & (kD - 1), half = tid >> 7, r0 = 32 * half;
+        const size_t c = (size_t)h * kD + i;
+        float *dst[3] = {Yq, Yk, Yv};
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {
+            const float4 wt = __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)x * D + c) * kK));
+            const T *col = raw + (size_t)x * kRows * kD + i;
+            float h0 = IO<T>::ld(col + (r0 + 0) * kD), h1 = IO<T>::ld(col + (r0 + 1) * kD),
+                  h2 = IO<T>::ld(col + (r0 + 2) * kD);
+#pragma unroll 8
+            for (int rr = 0; rr < 32; ++rr) {
+                const int r = r0 + rr;
+                const float xin = IO<T>::ld(col + (r + 3) * kD);
+                const float cv = fmaf(wt.x, h0, fmaf(wt.y, h1, fmaf(wt.z, h2, wt.w * xin)));
+                dst[x][r * kYS + i] = r < n ? __fdividef(cv, 1.0f + __expf(-cv)) : 0.f;
+                h0 = h1; h1 = h2; h2 = xin;
+            }
+        }
+        const float eA = expf(__ldg(A_log + h));
+        const float dt = __ldg(dt_bias + c);
+#pragma unroll 8
+        for (int rr = 0; rr < 32; ++rr) {
+            const int r = r0 + rr;
+            const float zz = IO<T>::ld(raw + ((size_t)3 * kRows + r + 3) * kD + i);
+            const float sg = __fdividef(1.0f, 1.0f + __expf(-eA * (zz + dt)));
+            AL[r * kYS + i] = r < n ? __expf(gmin * sg) : 1.f;
+        }
+    }
+    __syncthreads();
+    // 3. L2 norms and beta (warp w: rows w + 8m); zero the MMA tiles (raw is no longer needed)
+    for (int m = 0; m < kC / 8; ++m) {
+        const int r = warp + 8 * m;
+        float4 a = reinterpret_cast<float4 *>(Yq + r * kYS)[lane];
+        float4 b = reinterpret_cast<float4 *>(Yk + r * kYS)[lane];
+        const float sq = warp_sum(a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w);
+        const float sk = warp_sum(b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w);
+        const float rq = q_scale / sqrtf(sq + l2_eps), rk = 1.0f / sqrtf(sk + l2_eps);
+        a.x *= rq; a.y *= rq; a.z *= rq; a.w *= rq;
+        b.x *= rk; b.y *= rk; b.z *= rk; b.w *= rk;
+        reinterpret_cast<float4 *>(Yq + r * kYS)[lane] = a;
+        reinterpret_cast<float4 *>(Yk + r * kYS)[lane] = b;
+    }
+    for (int o = tid * 16; o < 49152; o += 256 * 16)
+        *reinterpret_cast<uint4 *>(Y + o) = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+
+    // 4. A and P on the tensor core, one 16-row block at a time (reference row nR = 16 R)
+    unsigned char *tA = Y + kPtOffTA, *tB = Y + kPtOffTB;
+    constexpr uint32_t id64 = tc::idesc_bf16(128, 64);
+    bool good = true;
+    for (int R = 0; R < kC / kBlk; ++R) {
+        const int nR = R * kBlk;
+        if (tid < kD) {
+            // rows nR..nR+15: left factors (tile A rows 0..31) and the diagonal-block right factors
+            const int c = tid;
+            float prod = 1.f;
+#pragma unroll 4
+            for (int rr = 0; rr < kBlk; ++rr) {
+                const int r = nR + rr;
+                if (rr > 0) prod *= AL[r * kYS + c];
+                st_bf16(tA, tc::kmajor_off(rr, c, kD), Yk[r * kYS + c] * prod);
+                st_bf16(tA, tc::kmajor_off(kBlk + rr, c, kD), Yq[r * kYS + c] * prod);
+                st_bf16(tB, tc::kmajor_off(r, c, kD), Yk[r * kYS + c] * __frcp_rn(prod));
+            }
+        } else {
+            // rows i < nR: right factors exp(G_nR - G_i) = prod_{t=i+1..nR} alpha_t
+            const int c = tid - kD;
+            float prod = 1.f;
+            for (int i = nR - 1; i >= 0; --i) {
+                prod *= AL[(i + 1) * kYS + c];
+                st_bf16(tB, tc::kmajor_off(i, c, kD), Yk[i * kYS + c] * prod);
+            }
+        }
+        tc::fence_smem_to_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                tc::mma_bf16(tb + 64 * R, tc::kmajor_desc(tA, kk, kD), tc::kmajor_desc(tB, kk, kD), id64, kk > 0);
+            tc::mma_commit(bar);
+        }
+        good &= mbar_wait_bounded(bar, (uint32_t)(R & 1), kTcWaitLimit);  // the tiles are reused
+        tc::fence_after_sync();
+    }
+    // 5. read A (lanes 0..15) and P (lanes 16..31) back: warps 0 and 4 own TMEM lanes 0..31
+    float *Am = reinterpret_cast<float *>(Y + kPtOffA);
+    unsigned char *tP = Y + kPtOffP;
+    if ((warp & 3) == 0) {
+        const int half = warp >> 2;  // warp 0: blocks 0,1; warp 4: blocks 2,3
+        uint32_t raw32[32];
+#pragma unroll 1
+        for (int Rb = 0; Rb < 2; ++Rb) {
+            const int R = 2 * half + Rb;
+#pragma unroll 1
+            for (int cb = 0; cb < 2; ++cb) {
+                tc::tmem_ld32_nowait(tb + 64 * R + 32 * cb, raw32);
+                tc::tmem_wait_ld();
+                if (lane < kBlk) {
+                    const int r = 16 * R + lane;
+                    const float bt = sbeta[r];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int i = 32 * cb + j;
+                        Am[r * kC + i] = i < r ? bt * __uint_as_float(raw32[j]) : 0.f;
+                    }
+                } else {
+                    const int r = 16 * R + lane - kBlk;
+                    float pv[16];
+#pragma unroll
+                    for (int hb = 0; hb < 2; ++hb) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int i = 32 * cb + 16 * hb + j;
+                            pv[j] = i <= r ? __uint_as_float(raw32[16 * hb + j]) : 0.f;
+                        }
+                        store_row_bf16(tP, r, 32 * cb + 16 * hb, pv, kC);
+                    }
+                }
+            }
+        }
+    }
+    if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
+    unsigned char *blk = chunks + (size_t)blockIdx.x * kTcChunkBytes;
+    // 6. Forward substitution (I + A) X = Diag(beta) B, one column per thread:
+    //    columns 0..127 of B are k o exp(G) (-> W), 128..255 are v (-> U').
+    {
+        const int j = tid;
+        const bool isk = j < kD;
+        const int cj = isk ? j : j - kD;
+        float X[kC];
+        float gp = 1.f;  // exp(G_r) of channel cj, a running product
+#pragma unroll
+        for (int r = 0; r < kC; ++r) {
+            float bb;
+            if (isk) { gp *= AL[r * kYS + cj]; bb = Yk[r * kYS + cj] * gp; }
+            else bb = Yv[r * kYS + cj];
+            float x0 = sbeta[r] * bb, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+#pragma unroll
+            for (int i = 0; i + 4 <= r; i += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Am + r * kC + i);
+                x0 = fmaf(-a4.x, X[i], x0);
+                x1 = fmaf(-a4.y, X[i + 1], x1);
+                x2 = fmaf(-a4.z, X[i + 2], x2);
+                x3 = fmaf(-a4.w, X[i + 3], x3);
+            }
+#pragma unroll
+            for (int i = r & ~3; i < r; ++i) x0 = fmaf(-Am[r * kC + i], X[i], x0);
+            X[r] = (x0 + x1) + (x2 + x3);
+        }
+        if (isk) {
+            unsigned char *tW = Y + kPtOffW;  // the MMA tiles are free now
+#pragma unroll
+            for (int r = 0; r < kC; ++r) st_bf16(tW, tc::kmajor_off(r, cj, kD), X[r]);
+        } else {
+            float *Up = reinterpret_cast<float *>(blk + kOffUp);
+#pragma unroll
+            for (int r = 0; r < kC; ++r) Up[r * kD + cj] = X[r];
+        }
+    }
+    // 7. Q o exp(G) (threads 0..127, forward products) and (K o exp(G_last - G))^T
+    //    (threads 128..255, backward products; alpha is 1 beyond the chunk), the chunk decay
+    if (tid < kD) {
+        const int c = tid;
+        unsigned char *tQG = Y + kPtOffQG;
+        float gp = 1.f;
+#pragma unroll 4
+        for (int r = 0; r < kC; ++r) {
+            gp *= AL[r * kYS + c];
+            st_bf16(tQG, tc::kmajor_off(r, c, kD), Yq[r * kYS + c] * gp);
+        }
+        reinterpret_cast<float *>(blk + kOffG)[c] = gp;  // exp(G_last): alpha = 1 past the chunk
+    } else {
+        const int c = tid - kD;
+        unsigned char *tKDT = Y + kPtOffKDT;
+        float gp = 1.f, kd[8];
+#pragma unroll 1
+        for (int rb = kC / 8 - 1; rb >= 0; --rb) {
+#pragma unroll
+            for (int t = 7; t >= 0; --t) {
+                const int r = 8 * rb + t;
+                kd[t] = Yk[r * kYS + c] * gp;
+                gp *= AL[r * kYS + c];
+            }
+            uint32_t wv[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const __nv_bfloat162 p2 = __floats2bfloat162_rn(kd[2 * t], kd[2 * t + 1]);
+                wv[t] = *reinterpret_cast<const uint32_t *>(&p2);
+            }
+            *reinterpret_cast<uint4 *>(tKDT + tc::kmajor_off(c, 8 * rb, kC)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+    }
+    __syncthreads();
+    // 8. the operand tiles to the chunk block with 16-byte stores
+    for (int o = tid * 16; o < 32768; o += 256 * 16)  // W and QG
+        *reinterpret_cast<uint4 *>(blk + kOffW + o) = *reinterpret_cast<const uint4 *>(Y + kPtOffW + o);
+    for (int o = tid * 16; o < 8192; o += 256 * 16)
+        *reinterpret_cast<uint4 *>(blk + kOffP + o) = *reinterpret_cast<const uint4 *>(Y + kPtOffP + o);
+    for (int o = tid * 16; o < 16384; o += 256 * 16)
+        *reinterpret_cast<uint4 *>(blk + kOffKDT + o) = *reinterpret_cast<const uint4 *>(Y + kPtOffKDT + o);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tb, 256);
+}
+
 // ---------------------------------------------------------------- state pass
 template <typename T>
 __global__ void __launch_bounds__(256, 1)
@@ -662,11 +953,13 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         const int st = it & 1;
         const unsigned char *stage = sm + st * kTcStageBytes;
         const ChunkEntry e = table[ci];
-        // output-gate logits of this thread's tokens; their latency hides behind the MMAs
-        float gl[32];
+        // output-gate logits of this thread's tokens, kept as raw bits until the epilogue so the
+        // loads do not block the warp; their latency hides behind the MMAs
+        static_assert(sizeof(T) == 2, "the tensor-core path reads BF16 gate logits");
+        unsigned short graw[32];
 #pragma unroll
         for (int r = 0; r < 32; ++r)
-            gl[r] = r0 + r < e.n ? IO<T>::ld(g + (size_t)(e.t0 + r0 + r) * D + (size_t)h * kD + vi) : 0.f;
+            graw[r] = ld_nc_u16(g + (size_t)(e.t0 + min(r0 + r, e.n - 1)) * D + (size_t)h * kD + vi);
 
         good &= mbar_wait_bounded(&bar[st], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
         // D3 = Diag(gC) on its columns, while MMA1 runs on D1 / D2
@@ -759,7 +1052,8 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             if (r0 + r < e.n) {
                 const int rr = r0 + r;
                 const float ms = (red[rr] + red[kC + rr] + red[2 * kC + rr] + red[3 * kC + rr]) * (1.0f / kD);
-                const float sg = __fdividef(1.0f, 1.0f + __expf(-gl[r]));
+                const float gv = __bfloat162float(__ushort_as_bfloat16(graw[r]));
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-gv));
                 IO<T>::st(out + (size_t)(e.t0 + rr) * D + (size_t)h * kD + vi, sg * nw * (o[r] * rsqrtf(ms + rms_eps)));
             }
         }
@@ -851,13 +1145,22 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (total_chunks > 0) {
-        const int prep_smem = kPrepSmemFloats * (int)sizeof(float);
-        e = cudaFuncSetAttribute(prep_kernel<T, kTC>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
-        if (e != cudaSuccess) return e;
-        prep_kernel<T, kTC><<<(unsigned)(total_chunks * H), 256, prep_smem, stream>>>(
-            p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
-            (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, chunks,
-            c.gate_lower_bound, c.l2_eps, c.q_scale);
+        if constexpr (kTC) {
+            e = cudaFuncSetAttribute(prep_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepTcSmem);
+            if (e != cudaSuccess) return e;
+            prep_tc_kernel<T><<<(unsigned)(total_chunks * H), 256, kPrepTcSmem, stream>>>(
+                p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
+                (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, chunks, st.err,
+                c.gate_lower_bound, c.l2_eps, c.q_scale);
+        } else {
+            const int prep_smem = kPrepSmemFloats * (int)sizeof(float);
+            e = cudaFuncSetAttribute(prep_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
+            if (e != cudaSuccess) return e;
+            prep_kernel<T, false><<<(unsigned)(total_chunks * H), 256, prep_smem, stream>>>(
+                p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
+                (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, chunks,
+                c.gate_lower_bound, c.l2_eps, c.q_scale);
+        }
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

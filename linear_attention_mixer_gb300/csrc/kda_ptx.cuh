@@ -80,4 +80,21 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32
         : "memory");
 }
 
+// 16-byte global -> shared copy that does not block the issuing thread; bytes_valid = 0
+// fills the 16 bytes with zeros instead of reading.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t bytes_valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes_valid)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// 16-bit read-only global load whose result is not needed until later (no conversion here).
+__device__ __forceinline__ unsigned short ld_nc_u16(const void *p)
+{
+    unsigned short v;
+    asm volatile("ld.global.nc.b16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
 }  // namespace kda
