@@ -390,6 +390,62 @@ def _time_prefill(K, args, cfg, params, gen, dev, stream):
     return pre_ms
 
 
+def _time_varlen(K, args, cfg, params, gen, dev, stream):
+    """Varlen workload: 16 sequences ~U[512, 16384] (seeded lengths), prefill all, snapshot /
+    reset / restore sequences 0-7, then 128 batched decode steps; tokens/s of both phases."""
+    import numpy as np
+    import torch
+
+    import kda_inputs as KI
+    c = KI.CONFIGS["varlen"]
+    N, steps = c["n_seq"], c["decode_steps"]
+    lens = KI.varlen_lengths(N, c["len_lo"], c["len_hi"], c["seed"])
+    cu_h = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu_h[-1])
+    x = _inputs(T, gen, dev, torch.bfloat16)
+    out = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
+    st = K.kda_state_alloc(cfg, N)
+    slots = torch.arange(N, dtype=torch.int32, device=dev)
+    cu = torch.tensor(cu_h, device=dev)
+    reps = max(1, min(3, args.prefill_reps))
+    times = []
+    for r in range(reps + 1):
+        K.kda_state_reset(st, list(range(N)), stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        K.kda_prefill(cfg, params, st, slots, cu, cu_h, x["q"], x["k"], x["v"], x["z"], x["b"], x["g"], out, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if r > 0:  # the first call grows the workspace
+            times.append(a.elapsed_time(b))
+    del x, out
+    half = list(range(N // 2))
+    blob = torch.empty(K.kda_state_blob_bytes(st, len(half)), dtype=torch.uint8, device=dev)
+    K.kda_state_snapshot(st, half, blob, stream)
+    K.kda_state_reset(st, half, stream)
+    K.kda_state_restore(st, half, blob, stream)
+    ring = [_inputs(N, gen, dev, torch.bfloat16) for _ in range(steps)]
+    o = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for s in range(steps):
+        y = ring[s]
+        K.kda_decode_token(cfg, params, st, slots, y["q"], y["k"], y["v"], y["z"], y["b"], y["g"], o, stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    dec_ms = a.elapsed_time(b)
+    assert K.kda_state_poll_error(st) == 0
+    K.kda_state_free(st)
+    del ring, blob
+    torch.cuda.empty_cache()
+    pre_ms = statistics.median(times)
+    return {"workload": f"16 sequences, lengths ~U[512,16384] (seeded), {T} tokens, 96 heads x 128, BF16 I/O; "
+                        "prefill all, snapshot/reset/restore 8, then 128 batched decode steps",
+            "total_tokens": T, "prefill_ms": pre_ms, "prefill_tokens_per_s": T / (pre_ms / 1e3),
+            "decode_ms_per_step": dec_ms / steps, "decode_tokens_per_s": N * steps / (dec_ms / 1e3)}
+
+
 def run_kda(args):
     import torch
     ws, rank, local = _dist()
@@ -460,6 +516,8 @@ def run_kda(args):
             line["value"] = Tp / (pre_ms / 1e3)
             line["ms_per_step"] = pre_ms
             line["gpu_launches"] = 4 * args.prefill_reps
+    if args.only == "all":
+        line["varlen"] = _time_varlen(K, args, cfg, params, gen, dev, stream)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode()
         if "prefill" in line:

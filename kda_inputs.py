@@ -32,11 +32,17 @@ def _rng(seed: int, stream: str, sub: int = 0) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, _STREAMS[stream], sub])))
 
 
+_BF16_HALF = np.array([0x7FFF], dtype=np.uint32)
+
+
 def bf16_round(x: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bfloat16 (ties to even); returns float32."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32)
+    u = np.array(x, dtype=np.float32, copy=True).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    u += lsb
+    u += _BF16_HALF  # finite inputs never wrap
+    u &= np.uint32(0xFFFF0000)
+    return u.view(np.float32)
 
 
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -75,6 +81,18 @@ def make_tokens(T: int, H: int, d: int, seed: int, bf16: bool, sub: int = 0) -> 
     x = _rng(seed, "b", sub).standard_normal((T, H), dtype=np.float32)
     out["b"] = bf16_round(x) if bf16 else x
     return out
+
+
+def make_tokens_torch(T: int, H: int, d: int, seed: int, sub: int = 0, device="cuda") -> dict:
+    """The same distributions drawn on a device by torch's seeded generator, rounded to
+    BF16 (nearest-even): q,k,v,z,g [T, H*d] and b [T, H] as BF16 tensors. For workloads too
+    large to draw on the host; callers copy the slices they check to the host."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed * 1_000_003 + sub)
+    D = H * d
+    return {name: torch.randn(T, H if name == "b" else D, generator=gen, device=device).to(torch.bfloat16)
+            for name in ("q", "k", "v", "z", "b", "g")}
 
 
 def make_state(n: int, H: int, d: int, seed: int, std: float = 0.05) -> np.ndarray:

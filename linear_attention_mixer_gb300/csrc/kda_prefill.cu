@@ -425,14 +425,18 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 //    (all <= 1; on a block diagonal the right factor is the reciprocal of a product of at most
 //    15 gates, <= e^75, finite in FP32);
 //  * A and P come from tcgen05: for each 16-row block R an M = 128 tile whose rows 0..15 are
-//    k_r o exp(G_r - G_n) and rows 16..31 are q_r o exp(G_r - G_n) (rows 32..127 zero) times
-//    the block's right-factor tile k_i o exp(G_n - G_i) (N = 64 rows i, K = 128 channels).
+//    k_r o exp(G_r - G_n) and rows 16..31 are q_r o exp(G_r - G_n) times the block's
+//    right-factor tile k_i o exp(G_n - G_i) (N = 64 rows i, K = 128 channels). Every factor is
+//    split into BF16 hi + lo parts (lo = x - hi): rows 32..63 of the tile hold the lo parts and
+//    a second right-factor tile holds lo, so hi*hi + lo*hi + hi*lo is accumulated (the products
+//    then carry about FP32-level error instead of BF16's 2^-9).
 // Shared memory: FP32 [64][132] arrays (rows padded against bank conflicts) for q^, k^, v and
 // alpha, then one reused region: raw inputs -> MMA tiles -> output tiles + A.
 constexpr int kYS = kD + 4;                         // padded FP32 row
 constexpr int kPtY = 73728;                         // reused region
 constexpr int kPtOffW = 0, kPtOffQG = 16384, kPtOffKDT = 32768, kPtOffP = 49152, kPtOffA = 57344;
-constexpr int kPtOffTA = 0, kPtOffTB = 32768;       // MMA tiles (before the output tiles exist)
+constexpr int kPtOffTA = 0, kPtOffTBh = 32768, kPtOffTBl = 49152;  // MMA tiles (before the output tiles)
+constexpr int kPtOffPp = 0;                         // FP32 partial of P during the read-back
 constexpr int kPrepTcSmem = 4 * kC * kYS * 4 + kPtY + kC * 4 + 64;
 
 template <typename T>
@@ -465,7 +469,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     const int n = e.n;
     const size_t D = (size_t)H * kD;
 
-    if (warp == 0) tc::tmem_alloc(tslot, 256);
+    if (warp == 0) tc::tmem_alloc(tslot, 512);
     if (tid == 0) { mbar_init(bar, 1); fence_mbar_init(); }
 
     // 0. raw q, k, v rows with 3 rows of history, and z, staged with asynchronous 16-byte
@@ -542,27 +546,35 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         reinterpret_cast<float4 *>(Yq + r * kYS)[lane] = a;
         reinterpret_cast<float4 *>(Yk + r * kYS)[lane] = b;
     }
-    for (int o = tid * 16; o < 49152; o += 256 * 16)
+    for (int o = tid * 16; o < 65536; o += 256 * 16)
         *reinterpret_cast<uint4 *>(Y + o) = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 
-    // 4. A and P on the tensor core, one 16-row block at a time (reference row nR = 16 R)
-    unsigned char *tA = Y + kPtOffTA, *tB = Y + kPtOffTB;
+    // 4. A and P on the tensor core, one 16-row block at a time (reference row nR = 16 R).
+    //    TMEM columns 128 R .. +63: tile x hi right factors; 128 R + 64 .. +63: tile x lo.
+    unsigned char *tA = Y + kPtOffTA, *tBh = Y + kPtOffTBh, *tBl = Y + kPtOffTBl;
     constexpr uint32_t id64 = tc::idesc_bf16(128, 64);
+    auto split = [](unsigned char *hi_tile, unsigned char *lo_tile, uint32_t off_hi, uint32_t off_lo, float x) {
+        const __nv_bfloat16 hb = __float2bfloat16_rn(x);
+        *reinterpret_cast<__nv_bfloat16 *>(hi_tile + off_hi) = hb;
+        *reinterpret_cast<__nv_bfloat16 *>(lo_tile + off_lo) = __float2bfloat16_rn(x - __bfloat162float(hb));
+    };
     bool good = true;
     for (int R = 0; R < kC / kBlk; ++R) {
         const int nR = R * kBlk;
         if (tid < kD) {
-            // rows nR..nR+15: left factors (tile A rows 0..31) and the diagonal-block right factors
+            // rows nR..nR+15: left factors (tile rows 0..31 hi, 32..63 lo) and the
+            // diagonal-block right factors
             const int c = tid;
             float prod = 1.f;
 #pragma unroll 4
             for (int rr = 0; rr < kBlk; ++rr) {
                 const int r = nR + rr;
                 if (rr > 0) prod *= AL[r * kYS + c];
-                st_bf16(tA, tc::kmajor_off(rr, c, kD), Yk[r * kYS + c] * prod);
-                st_bf16(tA, tc::kmajor_off(kBlk + rr, c, kD), Yq[r * kYS + c] * prod);
-                st_bf16(tB, tc::kmajor_off(r, c, kD), Yk[r * kYS + c] * __frcp_rn(prod));
+                split(tA, tA, tc::kmajor_off(rr, c, kD), tc::kmajor_off(2 * kBlk + rr, c, kD), Yk[r * kYS + c] * prod);
+                split(tA, tA, tc::kmajor_off(kBlk + rr, c, kD), tc::kmajor_off(3 * kBlk + rr, c, kD),
+                      Yq[r * kYS + c] * prod);
+                split(tBh, tBl, tc::kmajor_off(r, c, kD), tc::kmajor_off(r, c, kD), Yk[r * kYS + c] * __frcp_rn(prod));
             }
         } else {
             // rows i < nR: right factors exp(G_nR - G_i) = prod_{t=i+1..nR} alpha_t
@@ -570,7 +582,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             float prod = 1.f;
             for (int i = nR - 1; i >= 0; --i) {
                 prod *= AL[(i + 1) * kYS + c];
-                st_bf16(tB, tc::kmajor_off(i, c, kD), Yk[i * kYS + c] * prod);
+                split(tBh, tBl, tc::kmajor_off(i, c, kD), tc::kmajor_off(i, c, kD), Yk[i * kYS + c] * prod);
             }
         }
         tc::fence_smem_to_async();
@@ -580,24 +592,52 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         if (tid == 0) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tb + 64 * R, tc::kmajor_desc(tA, kk, kD), tc::kmajor_desc(tB, kk, kD), id64, kk > 0);
+                tc::mma_bf16(tb + 128 * R, tc::kmajor_desc(tA, kk, kD), tc::kmajor_desc(tBh, kk, kD), id64, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                tc::mma_bf16(tb + 128 * R + 64, tc::kmajor_desc(tA, kk, kD), tc::kmajor_desc(tBl, kk, kD), id64,
+                             kk > 0);
             tc::mma_commit(bar);
         }
         good &= mbar_wait_bounded(bar, (uint32_t)(R & 1), kTcWaitLimit);  // the tiles are reused
         tc::fence_after_sync();
     }
-    // 5. read A (lanes 0..15) and P (lanes 16..31) back: warps 0 and 4 own TMEM lanes 0..31
+    // 5. read back. Rows 32..63 of the hi accumulator (lo-left x hi-right) live in TMEM lane
+    //    quarter 1 (warps 1, 5): they land first as FP32 partials; then quarter 0 (warps 0, 4)
+    //    adds rows 0..31 of both accumulators (hi x hi, hi x lo) and writes A (FP32, beta and
+    //    mask applied) and the P tile (BF16, inclusive mask).
     float *Am = reinterpret_cast<float *>(Y + kPtOffA);
+    float *Pp = reinterpret_cast<float *>(Y + kPtOffPp);
     unsigned char *tP = Y + kPtOffP;
-    if ((warp & 3) == 0) {
-        const int half = warp >> 2;  // warp 0: blocks 0,1; warp 4: blocks 2,3
+    if ((warp & 3) == 1) {
+        const int lanes1 = 32 << 16;
         uint32_t raw32[32];
 #pragma unroll 1
         for (int Rb = 0; Rb < 2; ++Rb) {
-            const int R = 2 * half + Rb;
+            const int R = 2 * (warp >> 2) + Rb;
 #pragma unroll 1
             for (int cb = 0; cb < 2; ++cb) {
-                tc::tmem_ld32_nowait(tb + 64 * R + 32 * cb, raw32);
+                tc::tmem_ld32_nowait(tb + lanes1 + 128 * R + 32 * cb, raw32);
+                tc::tmem_wait_ld();
+                const int r = 16 * R + (lane & 15);
+                float *dstp = lane < kBlk ? Am : Pp;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dstp[r * kC + 32 * cb + j] = __uint_as_float(raw32[j]);
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if ((warp & 3) == 0) {
+        uint32_t rh[32], rl[32];
+#pragma unroll 1
+        for (int Rb = 0; Rb < 2; ++Rb) {
+            const int R = 2 * (warp >> 2) + Rb;
+#pragma unroll 1
+            for (int cb = 0; cb < 2; ++cb) {
+                tc::tmem_ld32_nowait(tb + 128 * R + 32 * cb, rh);
+                tc::tmem_ld32_nowait(tb + 128 * R + 64 + 32 * cb, rl);
                 tc::tmem_wait_ld();
                 if (lane < kBlk) {
                     const int r = 16 * R + lane;
@@ -605,7 +645,8 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int i = 32 * cb + j;
-                        Am[r * kC + i] = i < r ? bt * __uint_as_float(raw32[j]) : 0.f;
+                        const float a = __uint_as_float(rh[j]) + __uint_as_float(rl[j]) + Am[r * kC + i];
+                        Am[r * kC + i] = i < r ? bt * a : 0.f;
                     }
                 } else {
                     const int r = 16 * R + lane - kBlk;
@@ -615,7 +656,9 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int i = 32 * cb + 16 * hb + j;
-                            pv[j] = i <= r ? __uint_as_float(raw32[16 * hb + j]) : 0.f;
+                            const float pvv = __uint_as_float(rh[16 * hb + j]) + __uint_as_float(rl[16 * hb + j]) +
+                                              Pp[r * kC + i];
+                            pv[j] = i <= r ? pvv : 0.f;
                         }
                         store_row_bf16(tP, r, 32 * cb + 16 * hb, pv, kC);
                     }
@@ -704,7 +747,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         *reinterpret_cast<uint4 *>(blk + kOffKDT + o) = *reinterpret_cast<const uint4 *>(Y + kPtOffKDT + o);
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tb, 256);
+    if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
 // ---------------------------------------------------------------- state pass
