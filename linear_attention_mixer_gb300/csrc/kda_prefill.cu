@@ -495,6 +495,14 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     }
     unsigned short braw = 0;
     if (tid < kC && tid < n) braw = ld_nc_u16(bl + (size_t)(e.t0 + tid) * H + h);
+    // this thread's per-channel parameters, loaded while the staging copies are in flight
+    const int pc = tid & (kD - 1);
+    float4 wts[3];
+#pragma unroll
+    for (int x = 0; x < 3; ++x)
+        wts[x] = __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)x * D + (size_t)h * kD + pc) * kK));
+    const float p_dt = __ldg(dt_bias + (size_t)h * kD + pc);
+    const float p_eA = expf(__ldg(A_log + h));
     cp_async_wait_all();
     tc::fence_before_sync();
     __syncthreads();
@@ -509,7 +517,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         float *dst[3] = {Yq, Yk, Yv};
 #pragma unroll
         for (int x = 0; x < 3; ++x) {
-            const float4 wt = __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)x * D + c) * kK));
+            const float4 wt = wts[x];
             const T *col = raw + (size_t)x * kRows * kD + i;
             float h0 = IO<T>::ld(col + (r0 + 0) * kD), h1 = IO<T>::ld(col + (r0 + 1) * kD),
                   h2 = IO<T>::ld(col + (r0 + 2) * kD);
@@ -522,8 +530,8 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 h0 = h1; h1 = h2; h2 = xin;
             }
         }
-        const float eA = expf(__ldg(A_log + h));
-        const float dt = __ldg(dt_bias + c);
+        const float eA = p_eA, dt = p_dt;
+        (void)c;
 #pragma unroll 8
         for (int rr = 0; rr < 32; ++rr) {
             const int r = r0 + rr;
@@ -1059,10 +1067,23 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(raw[j]);
         }
+        // sums of squares over this warp's 32 v for its 32 tokens: a reduce-scatter butterfly
+        // (31 shuffles) that leaves the sum of token r0 + lane in lane `lane`
+        {
+            float sq[32];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const float s2 = warp_sum(o[r] * o[r]);
-            if (lane == 0) red[qtr * kC + r0 + r] = s2;
+            for (int j = 0; j < 32; ++j) sq[j] = o[j] * o[j];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                const bool upper = (lane & off) != 0;
+#pragma unroll
+                for (int j = 0; j < off; ++j) {
+                    const float keep = upper ? sq[j + off] : sq[j];
+                    const float send = upper ? sq[j] : sq[j + off];
+                    sq[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            red[qtr * kC + r0 + lane] = sq[0];
         }
         // refresh the S^T operand from the updated FP32 state
         {
@@ -1096,7 +1117,9 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 const int rr = r0 + r;
                 const float ms = (red[rr] + red[kC + rr] + red[2 * kC + rr] + red[3 * kC + rr]) * (1.0f / kD);
                 const float gv = __bfloat162float(__ushort_as_bfloat16(graw[r]));
-                const float sg = __fdividef(1.0f, 1.0f + __expf(-gv));
+                // sigmoid(g) = (1 + tanh(g/2)) / 2; the hardware tanh's error is below the BF16
+                // rounding of the output it multiplies
+                const float sg = fmaf(0.5f, tanh_approx(0.5f * gv), 0.5f);
                 IO<T>::st(out + (size_t)(e.t0 + rr) * D + (size_t)h * kD + vi, sg * nw * (o[r] * rsqrtf(ms + rms_eps)));
             }
         }

@@ -97,4 +97,12 @@ __device__ __forceinline__ unsigned short ld_nc_u16(const void *p)
     return v;
 }
 
+// Hardware tanh approximation (max relative error about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x)
+{
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 }  // namespace kda
