@@ -440,7 +440,7 @@ constexpr int kPtOffPp = 0;                         // FP32 partial of P during 
 constexpr int kPrepTcSmem = 4 * kC * kYS * 4 + kPtY + kC * 4 + 64;
 
 template <typename T>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(512, 1)
 prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
                const float *__restrict__ A_log, const T *__restrict__ tail_all,
                const int32_t *__restrict__ slots, int H, int max_slots,
@@ -480,7 +480,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     {
         const T *srcs[4] = {q, k, v, z};
         const T *tl0 = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD;
-        for (int e2 = tid; e2 < 4 * kRows * 16; e2 += 256) {
+        for (int e2 = tid; e2 < 4 * kRows * 16; e2 += 512) {
             const int x = e2 / (kRows * 16), rem = e2 - x * (kRows * 16);
             const int j = rem >> 4, vec = rem & 15;
             const int p = j - 3;
@@ -496,11 +496,9 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     unsigned short braw = 0;
     if (tid < kC && tid < n) braw = ld_nc_u16(bl + (size_t)(e.t0 + tid) * H + h);
     // this thread's per-channel parameters, loaded while the staging copies are in flight
-    const int pc = tid & (kD - 1);
-    float4 wts[3];
-#pragma unroll
-    for (int x = 0; x < 3; ++x)
-        wts[x] = __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)x * D + (size_t)h * kD + pc) * kK));
+    const int pc = tid & (kD - 1), px = tid >> 7;  // channel, stream (q, k, v, or the gate)
+    const float4 p_w = px < 3 ? __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)px * D + (size_t)h * kD + pc) * kK))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
     const float p_dt = __ldg(dt_bias + (size_t)h * kD + pc);
     const float p_eA = expf(__ldg(A_log + h));
     cp_async_wait_all();
@@ -510,40 +508,32 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     const uint32_t tb = *tslot;
     if (tid < kC) sbeta[tid] = tid < n ? sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
 
-    // 1. conv + SiLU (sliding window in registers) and 2. the gates, thread (i, half)
-    {
-        const int i = tid & (kD - 1), half = tid >> 7, r0 = 32 * half;
-        const size_t c = (size_t)h * kD + i;
-        float *dst[3] = {Yq, Yk, Yv};
-#pragma unroll
-        for (int x = 0; x < 3; ++x) {
-            const float4 wt = wts[x];
-            const T *col = raw + (size_t)x * kRows * kD + i;
-            float h0 = IO<T>::ld(col + (r0 + 0) * kD), h1 = IO<T>::ld(col + (r0 + 1) * kD),
-                  h2 = IO<T>::ld(col + (r0 + 2) * kD);
+    // 1. conv + SiLU (sliding window in registers) for stream px < 3, 2. the gates for px == 3;
+    //    thread (channel pc, stream px) walks all 64 rows
+    if (px < 3) {
+        float *dst = px == 0 ? Yq : (px == 1 ? Yk : Yv);
+        const T *col = raw + (size_t)px * kRows * kD + pc;
+        float h0 = IO<T>::ld(col), h1 = IO<T>::ld(col + kD), h2 = IO<T>::ld(col + 2 * kD);
 #pragma unroll 8
-            for (int rr = 0; rr < 32; ++rr) {
-                const int r = r0 + rr;
-                const float xin = IO<T>::ld(col + (r + 3) * kD);
-                const float cv = fmaf(wt.x, h0, fmaf(wt.y, h1, fmaf(wt.z, h2, wt.w * xin)));
-                dst[x][r * kYS + i] = r < n ? __fdividef(cv, 1.0f + __expf(-cv)) : 0.f;
-                h0 = h1; h1 = h2; h2 = xin;
-            }
+        for (int r = 0; r < kC; ++r) {
+            const float xin = IO<T>::ld(col + (r + 3) * kD);
+            const float cv = fmaf(p_w.x, h0, fmaf(p_w.y, h1, fmaf(p_w.z, h2, p_w.w * xin)));
+            dst[r * kYS + pc] = r < n ? __fdividef(cv, 1.0f + __expf(-cv)) : 0.f;
+            h0 = h1; h1 = h2; h2 = xin;
         }
-        const float eA = p_eA, dt = p_dt;
-        (void)c;
+    } else {
+        const T *col = raw + ((size_t)3 * kRows + 3) * kD + pc;
 #pragma unroll 8
-        for (int rr = 0; rr < 32; ++rr) {
-            const int r = r0 + rr;
-            const float zz = IO<T>::ld(raw + ((size_t)3 * kRows + r + 3) * kD + i);
-            const float sg = __fdividef(1.0f, 1.0f + __expf(-eA * (zz + dt)));
-            AL[r * kYS + i] = r < n ? __expf(gmin * sg) : 1.f;
+        for (int r = 0; r < kC; ++r) {
+            const float zz = IO<T>::ld(col + r * kD);
+            const float sg = __fdividef(1.0f, 1.0f + __expf(-p_eA * (zz + p_dt)));
+            AL[r * kYS + pc] = r < n ? __expf(gmin * sg) : 1.f;
         }
     }
     __syncthreads();
     // 3. L2 norms and beta (warp w: rows w + 8m); zero the MMA tiles (raw is no longer needed)
-    for (int m = 0; m < kC / 8; ++m) {
-        const int r = warp + 8 * m;
+    for (int m = 0; m < kC / 16; ++m) {
+        const int r = warp + 16 * m;
         float4 a = reinterpret_cast<float4 *>(Yq + r * kYS)[lane];
         float4 b = reinterpret_cast<float4 *>(Yk + r * kYS)[lane];
         const float sq = warp_sum(a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w);
@@ -554,14 +544,15 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         reinterpret_cast<float4 *>(Yq + r * kYS)[lane] = a;
         reinterpret_cast<float4 *>(Yk + r * kYS)[lane] = b;
     }
-    for (int o = tid * 16; o < 65536; o += 256 * 16)
+    for (int o = tid * 16; o < 65536; o += 512 * 16)
         *reinterpret_cast<uint4 *>(Y + o) = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 
     // 4. A and P on the tensor core, one 16-row block at a time (reference row nR = 16 R).
     //    TMEM columns 128 R .. +63: tile x hi right factors; 128 R + 64 .. +63: tile x lo.
     unsigned char *tA = Y + kPtOffTA, *tBh = Y + kPtOffTBh, *tBl = Y + kPtOffTBl;
-    constexpr uint32_t id64 = tc::idesc_bf16(128, 64);
+    static_assert(kPtOffTBl - kPtOffTBh == 64 * kD * 2, "lo rows follow the hi rows of one N = 128 tile");
+    constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
     auto split = [](unsigned char *hi_tile, unsigned char *lo_tile, uint32_t off_hi, uint32_t off_lo, float x) {
         const __nv_bfloat16 hb = __float2bfloat16_rn(x);
         *reinterpret_cast<__nv_bfloat16 *>(hi_tile + off_hi) = hb;
@@ -584,7 +575,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                       Yq[r * kYS + c] * prod);
                 split(tBh, tBl, tc::kmajor_off(r, c, kD), tc::kmajor_off(r, c, kD), Yk[r * kYS + c] * __frcp_rn(prod));
             }
-        } else {
+        } else if (tid < 2 * kD) {
             // rows i < nR: right factors exp(G_nR - G_i) = prod_{t=i+1..nR} alpha_t
             const int c = tid - kD;
             float prod = 1.f;
@@ -598,13 +589,11 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         __syncthreads();
         tc::fence_after_sync();
         if (tid == 0) {
+            // tBh (rows 0..63) and tBl (rows 64..127) form one N = 128 operand: one MMA group
+            // writes the hi products to columns 128 R .. +63 and the lo products to +64 .. +127
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tb + 128 * R, tc::kmajor_desc(tA, kk, kD), tc::kmajor_desc(tBh, kk, kD), id64, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tb + 128 * R + 64, tc::kmajor_desc(tA, kk, kD), tc::kmajor_desc(tBl, kk, kD), id64,
-                             kk > 0);
+                tc::mma_bf16(tb + 128 * R, tc::kmajor_desc(tA, kk, kD), tc::kmajor_desc(tBh, kk, kD), id128, kk > 0);
             tc::mma_commit(bar);
         }
         good &= mbar_wait_bounded(bar, (uint32_t)(R & 1), kTcWaitLimit);  // the tiles are reused
@@ -617,68 +606,62 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     float *Am = reinterpret_cast<float *>(Y + kPtOffA);
     float *Pp = reinterpret_cast<float *>(Y + kPtOffPp);
     unsigned char *tP = Y + kPtOffP;
-    if ((warp & 3) == 1) {
+    if ((warp & 3) == 1) {  // warps 1, 5, 9, 13: block R = warp / 4
         const int lanes1 = 32 << 16;
+        const int R = warp >> 2;
         uint32_t raw32[32];
 #pragma unroll 1
-        for (int Rb = 0; Rb < 2; ++Rb) {
-            const int R = 2 * (warp >> 2) + Rb;
-#pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-                tc::tmem_ld32_nowait(tb + lanes1 + 128 * R + 32 * cb, raw32);
-                tc::tmem_wait_ld();
-                const int r = 16 * R + (lane & 15);
-                float *dstp = lane < kBlk ? Am : Pp;
+        for (int cb = 0; cb < 2; ++cb) {
+            tc::tmem_ld32_nowait(tb + lanes1 + 128 * R + 32 * cb, raw32);
+            tc::tmem_wait_ld();
+            const int r = 16 * R + (lane & 15);
+            float *dstp = lane < kBlk ? Am : Pp;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) dstp[r * kC + 32 * cb + j] = __uint_as_float(raw32[j]);
-            }
+            for (int j = 0; j < 32; ++j) dstp[r * kC + 32 * cb + j] = __uint_as_float(raw32[j]);
         }
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if ((warp & 3) == 0) {
+    if ((warp & 3) == 0) {  // warps 0, 4, 8, 12: block R = warp / 4
+        const int R = warp >> 2;
         uint32_t rh[32], rl[32];
 #pragma unroll 1
-        for (int Rb = 0; Rb < 2; ++Rb) {
-            const int R = 2 * (warp >> 2) + Rb;
-#pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-                tc::tmem_ld32_nowait(tb + 128 * R + 32 * cb, rh);
-                tc::tmem_ld32_nowait(tb + 128 * R + 64 + 32 * cb, rl);
-                tc::tmem_wait_ld();
-                if (lane < kBlk) {
-                    const int r = 16 * R + lane;
-                    const float bt = sbeta[r];
+        for (int cb = 0; cb < 2; ++cb) {
+            tc::tmem_ld32_nowait(tb + 128 * R + 32 * cb, rh);
+            tc::tmem_ld32_nowait(tb + 128 * R + 64 + 32 * cb, rl);
+            tc::tmem_wait_ld();
+            if (lane < kBlk) {
+                const int r = 16 * R + lane;
+                const float bt = sbeta[r];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int i = 32 * cb + j;
-                        const float a = __uint_as_float(rh[j]) + __uint_as_float(rl[j]) + Am[r * kC + i];
-                        Am[r * kC + i] = i < r ? bt * a : 0.f;
+                for (int j = 0; j < 32; ++j) {
+                    const int i = 32 * cb + j;
+                    const float a = __uint_as_float(rh[j]) + __uint_as_float(rl[j]) + Am[r * kC + i];
+                    Am[r * kC + i] = i < r ? bt * a : 0.f;
+                }
+            } else {
+                const int r = 16 * R + lane - kBlk;
+                float pv[16];
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int i = 32 * cb + 16 * hb + j;
+                        const float pvv = __uint_as_float(rh[16 * hb + j]) + __uint_as_float(rl[16 * hb + j]) +
+                                          Pp[r * kC + i];
+                        pv[j] = i <= r ? pvv : 0.f;
                     }
-                } else {
-                    const int r = 16 * R + lane - kBlk;
-                    float pv[16];
-#pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int i = 32 * cb + 16 * hb + j;
-                            const float pvv = __uint_as_float(rh[16 * hb + j]) + __uint_as_float(rl[16 * hb + j]) +
-                                              Pp[r * kC + i];
-                            pv[j] = i <= r ? pvv : 0.f;
-                        }
-                        store_row_bf16(tP, r, 32 * cb + 16 * hb, pv, kC);
-                    }
+                    store_row_bf16(tP, r, 32 * cb + 16 * hb, pv, kC);
                 }
             }
         }
     }
     if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
     unsigned char *blk = chunks + (size_t)blockIdx.x * kTcChunkBytes;
-    // 6. Forward substitution (I + A) X = Diag(beta) B, one column per thread:
+    // 6. Forward substitution (I + A) X = Diag(beta) B, one column per thread (threads 0..255):
     //    columns 0..127 of B are k o exp(G) (-> W), 128..255 are v (-> U').
-    {
+    if (tid < 2 * kD) {
         const int j = tid;
         const bool isk = j < kD;
         const int cj = isk ? j : j - kD;
@@ -724,7 +707,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             st_bf16(tQG, tc::kmajor_off(r, c, kD), Yq[r * kYS + c] * gp);
         }
         reinterpret_cast<float *>(blk + kOffG)[c] = gp;  // exp(G_last): alpha = 1 past the chunk
-    } else {
+    } else if (tid < 2 * kD) {
         const int c = tid - kD;
         unsigned char *tKDT = Y + kPtOffKDT;
         float gp = 1.f, kd[8];
@@ -747,11 +730,11 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     }
     __syncthreads();
     // 8. the operand tiles to the chunk block with 16-byte stores
-    for (int o = tid * 16; o < 32768; o += 256 * 16)  // W and QG
+    for (int o = tid * 16; o < 32768; o += 512 * 16)  // W and QG
         *reinterpret_cast<uint4 *>(blk + kOffW + o) = *reinterpret_cast<const uint4 *>(Y + kPtOffW + o);
-    for (int o = tid * 16; o < 8192; o += 256 * 16)
+    for (int o = tid * 16; o < 8192; o += 512 * 16)
         *reinterpret_cast<uint4 *>(blk + kOffP + o) = *reinterpret_cast<const uint4 *>(Y + kPtOffP + o);
-    for (int o = tid * 16; o < 16384; o += 256 * 16)
+    for (int o = tid * 16; o < 16384; o += 512 * 16)
         *reinterpret_cast<uint4 *>(blk + kOffKDT + o) = *reinterpret_cast<const uint4 *>(Y + kPtOffKDT + o);
     tc::fence_before_sync();
     __syncthreads();
@@ -961,14 +944,15 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         bulk_g2s(sm + stage * kTcStageBytes, src, kTcStageBytes, &bar[stage]);
         bulk_g2s(sgam + stage * kD, src + kOffG, kD * 4, &bar[stage]);
     };
-    constexpr uint32_t id64 = tc::idesc_bf16(128, 64), id128 = tc::idesc_bf16(128, 128);
-    auto mma1 = [&](const unsigned char *stage) {  // thread 0 only: D1 = S^T W^T, D2 = S^T QG^T
+    constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
+    // W (rows 0..63) and QG (rows 64..127) form one N = 128 B operand, P (rows 0..63) and KDT
+    // (rows 64..191) one N = 192 operand, so each MMA group is a single run of K steps.
+    static_assert(kOffQG - kOffW == 64 * kD * 2 && kOffKDT - kOffP == 64 * kC * 2, "adjacent operand tiles");
+    constexpr uint32_t id192 = tc::idesc_bf16(128, 192);
+    auto mma1 = [&](const unsigned char *stage) {  // thread 0 only: [D1 | D2] = S^T [W | QG]^T
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            tc::mma_bf16(tb, tc::kmajor_desc(sST, kk, kD), tc::kmajor_desc(stage + kOffW, kk, kD), id64, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            tc::mma_bf16(tb + 64, tc::kmajor_desc(sST, kk, kD), tc::kmajor_desc(stage + kOffQG, kk, kD), id64, kk > 0);
+            tc::mma_bf16(tb, tc::kmajor_desc(sST, kk, kD), tc::kmajor_desc(stage + kOffW, kk, kD), id128, kk > 0);
         tc::mma_commit(&bar[2]);
     };
 
@@ -1045,14 +1029,10 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         tc::fence_before_sync();
         if (__syncthreads_or(!good)) { aborted = true; break; }
         tc::fence_after_sync();
-        if (tid == 0) {
+        if (tid == 0) {  // [D2 | D3] += U^T [P | KDT]^T
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                tc::mma_bf16(tb + 64, tc::kmajor_desc(sUT, kk, kC), tc::kmajor_desc(stage + kOffP, kk, kC), id64, 1);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc::mma_bf16(tb + 128, tc::kmajor_desc(sUT, kk, kC), tc::kmajor_desc(stage + kOffKDT, kk, kC), id128,
-                             1);
+                tc::mma_bf16(tb + 64, tc::kmajor_desc(sUT, kk, kC), tc::kmajor_desc(stage + kOffP, kk, kC), id192, 1);
             tc::mma_commit(&bar[3]);
         }
         good &= mbar_wait_bounded(&bar[3], ph2, kTcWaitLimit);
@@ -1214,7 +1194,7 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
         if constexpr (kTC) {
             e = cudaFuncSetAttribute(prep_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepTcSmem);
             if (e != cudaSuccess) return e;
-            prep_tc_kernel<T><<<(unsigned)(total_chunks * H), 256, kPrepTcSmem, stream>>>(
+            prep_tc_kernel<T><<<(unsigned)(total_chunks * H), 512, kPrepTcSmem, stream>>>(
                 p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
                 (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, chunks, st.err,
                 c.gate_lower_bound, c.l2_eps, c.q_scale);
