@@ -418,12 +418,10 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 
 // ---------------------------------------------------------------- prep on tensor cores
 // BF16 path, one CTA (256 threads) per (chunk, head). Differences from prep_kernel:
-//  * every decay factor is a running product of the per-token gates alpha_t = exp(gk_t) along
-//    the chunk (one thread per channel), not an exp of a difference of cumulative sums:
-//      exp(G_r - G_n) = prod_{t=n+1..r} alpha_t,  exp(G_r) = prod_{t<=r} alpha_t,
-//      exp(G_last - G_r) = prod_{t=r+1..last} alpha_t
-//    (all <= 1; on a block diagonal the right factor is the reciprocal of a product of at most
-//    15 gates, <= e^75, finite in FP32);
+//  * every decay factor is the exp of a difference of the cumulative log decay G (one scan per
+//    channel), so all 512 threads write factor elements independently:
+//      exp(G_r - G_n) <= 1 (left), exp(G_n - G_i) <= 1 for i <= n (right), <= e^75 on a block
+//      diagonal; exp(G_r), exp(G_last - G_r) <= 1; all finite in FP32;
 //  * A and P come from tcgen05: for each 16-row block R an M = 128 tile whose rows 0..15 are
 //    k_r o exp(G_r - G_n) and rows 16..31 are q_r o exp(G_r - G_n) times the block's
 //    right-factor tile k_i o exp(G_n - G_i) (N = 64 rows i, K = 128 channels). Every factor is
@@ -434,9 +432,13 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 // alpha, then one reused region: raw inputs -> MMA tiles -> output tiles + A.
 constexpr int kYS = kD + 4;                         // padded FP32 row
 constexpr int kPtY = 73728;                         // reused region
-constexpr int kPtOffW = 0, kPtOffQG = 16384, kPtOffKDT = 32768, kPtOffP = 49152, kPtOffA = 57344;
-constexpr int kPtOffTA = 0, kPtOffTBh = 32768, kPtOffTBl = 49152;  // MMA tiles (before the output tiles)
-constexpr int kPtOffPp = 0;                         // FP32 partial of P during the read-back
+// MMA tiles (padded layout, written element by element without bank conflicts)
+constexpr int kPadTile128 = tc::kmajor_pad_bytes(128, kD);  // 36,864
+constexpr int kPtOffTA = 0, kPtOffTBh = kPadTile128, kPtOffTBl = kPadTile128 + kPadTile128 / 2;
+// read-back and output stage: P partial, P tile, W (padded), A
+constexpr int kPtOffPp = 0, kPtOffP = 16384, kPtOffW = 24576, kPtOffA = 57344;
+static_assert(kPtOffTBh + kPadTile128 <= kPtY && kPtOffA + kC * kC * 4 <= kPtY, "prep staging region");
+static_assert(kPtOffW + tc::kmajor_pad_bytes(64, kD) <= kPtOffA, "W must not overlap A (read by the solve)");
 constexpr int kPrepTcSmem = 4 * kC * kYS * 4 + kPtY + kC * 4 + 64;
 
 template <typename T>
@@ -454,8 +456,8 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     float *Yq = smf;                                  // [64][132] q^
     float *Yk = Yq + kC * kYS;                        // [64][132] k^
     float *Yv = Yk + kC * kYS;                        // [64][132] v
-    float *AL = Yv + kC * kYS;                        // [64][132] alpha (1 beyond the chunk)
-    unsigned char *Y = reinterpret_cast<unsigned char *>(AL + kC * kYS);
+    float *GL = Yv + kC * kYS;                        // [64][132] gk, then G = cumulative log decay
+    unsigned char *Y = reinterpret_cast<unsigned char *>(GL + kC * kYS);
     float *sbeta = reinterpret_cast<float *>(Y + kPtY);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sbeta + kC);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 1);
@@ -527,10 +529,20 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         for (int r = 0; r < kC; ++r) {
             const float zz = IO<T>::ld(col + r * kD);
             const float sg = __fdividef(1.0f, 1.0f + __expf(-p_eA * (zz + p_dt)));
-            AL[r * kYS + pc] = r < n ? __expf(gmin * sg) : 1.f;
+            GL[r * kYS + pc] = r < n ? gmin * sg : 0.f;  // gk; 0 (no decay) past the chunk
         }
     }
     __syncthreads();
+    // 2b. G_r = sum_{t<=r} gk_t per channel (threads 0..127); every decay factor below is an
+    //     exp of a difference of G, computed independently per element
+    if (tid < kD) {
+        float acc = 0.f;
+#pragma unroll 16
+        for (int r = 0; r < kC; ++r) {
+            acc += GL[r * kYS + tid];
+            GL[r * kYS + tid] = acc;
+        }
+    }
     // 3. L2 norms and beta (warp w: rows w + 8m); zero the MMA tiles (raw is no longer needed)
     for (int m = 0; m < kC / 16; ++m) {
         const int r = warp + 16 * m;
@@ -544,14 +556,14 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         reinterpret_cast<float4 *>(Yq + r * kYS)[lane] = a;
         reinterpret_cast<float4 *>(Yk + r * kYS)[lane] = b;
     }
-    for (int o = tid * 16; o < 65536; o += 512 * 16)
+    for (int o = tid * 16; o < kPtY; o += 512 * 16)
         *reinterpret_cast<uint4 *>(Y + o) = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 
     // 4. A and P on the tensor core, one 16-row block at a time (reference row nR = 16 R).
     //    TMEM columns 128 R .. +63: tile x hi right factors; 128 R + 64 .. +63: tile x lo.
     unsigned char *tA = Y + kPtOffTA, *tBh = Y + kPtOffTBh, *tBl = Y + kPtOffTBl;
-    static_assert(kPtOffTBl - kPtOffTBh == 64 * kD * 2, "lo rows follow the hi rows of one N = 128 tile");
+    static_assert(kPtOffTBl - kPtOffTBh == tc::kmajor_pad_bytes(64, kD), "lo rows follow the hi rows of one tile");
     constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
     auto split = [](unsigned char *hi_tile, unsigned char *lo_tile, uint32_t off_hi, uint32_t off_lo, float x) {
         const __nv_bfloat16 hb = __float2bfloat16_rn(x);
@@ -561,28 +573,22 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     bool good = true;
     for (int R = 0; R < kC / kBlk; ++R) {
         const int nR = R * kBlk;
-        if (tid < kD) {
-            // rows nR..nR+15: left factors (tile rows 0..31 hi, 32..63 lo) and the
-            // diagonal-block right factors
-            const int c = tid;
-            float prod = 1.f;
-#pragma unroll 4
-            for (int rr = 0; rr < kBlk; ++rr) {
-                const int r = nR + rr;
-                if (rr > 0) prod *= AL[r * kYS + c];
-                split(tA, tA, tc::kmajor_off(rr, c, kD), tc::kmajor_off(2 * kBlk + rr, c, kD), Yk[r * kYS + c] * prod);
-                split(tA, tA, tc::kmajor_off(kBlk + rr, c, kD), tc::kmajor_off(3 * kBlk + rr, c, kD),
-                      Yq[r * kYS + c] * prod);
-                split(tBh, tBl, tc::kmajor_off(r, c, kD), tc::kmajor_off(r, c, kD), Yk[r * kYS + c] * __frcp_rn(prod));
-            }
-        } else if (tid < 2 * kD) {
-            // rows i < nR: right factors exp(G_nR - G_i) = prod_{t=i+1..nR} alpha_t
-            const int c = tid - kD;
-            float prod = 1.f;
-            for (int i = nR - 1; i >= 0; --i) {
-                prod *= AL[(i + 1) * kYS + c];
-                split(tBh, tBl, tc::kmajor_off(i, c, kD), tc::kmajor_off(i, c, kD), Yk[i * kYS + c] * prod);
-            }
+        // rows nR..nR+15: left factors k_r, q_r o exp(G_r - G_nR) (tile rows 0..31 hi, 32..63 lo)
+        // and the diagonal-block right factors k_r o exp(G_nR - G_r) (<= e^75)
+        for (int e2 = tid; e2 < kBlk * kD; e2 += 512) {
+            const int rr = e2 >> 7, c = e2 & (kD - 1), r = nR + rr;
+            const float gd = GL[r * kYS + c] - GL[nR * kYS + c];
+            const float f = __expf(gd);
+            split(tA, tA, tc::kmajor_off_pad(rr, c, kD), tc::kmajor_off_pad(2 * kBlk + rr, c, kD), Yk[r * kYS + c] * f);
+            split(tA, tA, tc::kmajor_off_pad(kBlk + rr, c, kD), tc::kmajor_off_pad(3 * kBlk + rr, c, kD),
+                  Yq[r * kYS + c] * f);
+            split(tBh, tBl, tc::kmajor_off_pad(r, c, kD), tc::kmajor_off_pad(r, c, kD), Yk[r * kYS + c] * __expf(-gd));
+        }
+        // rows i < nR: right factors k_i o exp(G_nR - G_i) (<= 1)
+        for (int e2 = tid; e2 < nR * kD; e2 += 512) {
+            const int i = e2 >> 7, c = e2 & (kD - 1);
+            split(tBh, tBl, tc::kmajor_off_pad(i, c, kD), tc::kmajor_off_pad(i, c, kD),
+                  Yk[i * kYS + c] * __expf(GL[nR * kYS + c] - GL[i * kYS + c]));
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
@@ -593,7 +599,8 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             // writes the hi products to columns 128 R .. +63 and the lo products to +64 .. +127
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tb + 128 * R, tc::kmajor_desc(tA, kk, kD), tc::kmajor_desc(tBh, kk, kD), id128, kk > 0);
+                tc::mma_bf16(tb + 128 * R, tc::kmajor_desc_pad(tA, kk, kD), tc::kmajor_desc_pad(tBh, kk, kD), id128,
+                             kk > 0);
             tc::mma_commit(bar);
         }
         good &= mbar_wait_bounded(bar, (uint32_t)(R & 1), kTcWaitLimit);  // the tiles are reused
@@ -659,20 +666,47 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     }
     if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
     unsigned char *blk = chunks + (size_t)blockIdx.x * kTcChunkBytes;
-    // 6. Forward substitution (I + A) X = Diag(beta) B, one column per thread (threads 0..255):
+    // 6. Q o exp(G) and (K o exp(G_last - G))^T straight to the chunk block, the chunk decay
+    //    exp(G_last) (G is constant past the chunk, so row 63 holds G_last); then q^ is no
+    //    longer needed and its array takes K o exp(G), the solve's right-hand side.
+    for (int e2 = tid; e2 < kC * kD; e2 += 512) {
+        const int r = e2 >> 7, c = e2 & (kD - 1);
+        st_bf16(blk + kOffQG, tc::kmajor_off(r, c, kD), Yq[r * kYS + c] * __expf(GL[r * kYS + c]));
+    }
+    for (int ch = tid; ch < kD * (kC / 8); ch += 512) {  // one 16-byte chunk: channel c, rows 8 rb .. +7
+        const int c = ch & (kD - 1), rb = ch >> 7;
+        const float gl = GL[(kC - 1) * kYS + c];
+        uint32_t wv[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int r = 8 * rb + 2 * t;
+            const __nv_bfloat162 p2 =
+                __floats2bfloat162_rn(Yk[r * kYS + c] * __expf(gl - GL[r * kYS + c]),
+                                      Yk[(r + 1) * kYS + c] * __expf(gl - GL[(r + 1) * kYS + c]));
+            wv[t] = *reinterpret_cast<const uint32_t *>(&p2);
+        }
+        *reinterpret_cast<uint4 *>(blk + kOffKDT + tc::kmajor_off(c, 8 * rb, kC)) =
+            make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+    if (tid < kD) reinterpret_cast<float *>(blk + kOffG)[tid] = __expf(GL[(kC - 1) * kYS + tid]);
+    __syncthreads();  // q^ has been read
+    float *Kg = Yq;
+    for (int e2 = tid; e2 < kC * kD; e2 += 512) {
+        const int r = e2 >> 7, c = e2 & (kD - 1);
+        Kg[r * kYS + c] = Yk[r * kYS + c] * __expf(GL[r * kYS + c]);
+    }
+    __syncthreads();
+    // 7. Forward substitution (I + A) X = Diag(beta) B, one column per thread (threads 0..255):
     //    columns 0..127 of B are k o exp(G) (-> W), 128..255 are v (-> U').
     if (tid < 2 * kD) {
         const int j = tid;
         const bool isk = j < kD;
         const int cj = isk ? j : j - kD;
+        const float *Bsrc = isk ? Kg : Yv;
         float X[kC];
-        float gp = 1.f;  // exp(G_r) of channel cj, a running product
 #pragma unroll
         for (int r = 0; r < kC; ++r) {
-            float bb;
-            if (isk) { gp *= AL[r * kYS + cj]; bb = Yk[r * kYS + cj] * gp; }
-            else bb = Yv[r * kYS + cj];
-            float x0 = sbeta[r] * bb, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+            float x0 = sbeta[r] * Bsrc[r * kYS + cj], x1 = 0.f, x2 = 0.f, x3 = 0.f;
 #pragma unroll
             for (int i = 0; i + 4 <= r; i += 4) {
                 const float4 a4 = *reinterpret_cast<const float4 *>(Am + r * kC + i);
@@ -686,56 +720,24 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             X[r] = (x0 + x1) + (x2 + x3);
         }
         if (isk) {
-            unsigned char *tW = Y + kPtOffW;  // the MMA tiles are free now
+            unsigned char *tW = Y + kPtOffW;  // the MMA tiles are free now (padded layout)
 #pragma unroll
-            for (int r = 0; r < kC; ++r) st_bf16(tW, tc::kmajor_off(r, cj, kD), X[r]);
+            for (int r = 0; r < kC; ++r) st_bf16(tW, tc::kmajor_off_pad(r, cj, kD), X[r]);
         } else {
             float *Up = reinterpret_cast<float *>(blk + kOffUp);
 #pragma unroll
             for (int r = 0; r < kC; ++r) Up[r * kD + cj] = X[r];
         }
     }
-    // 7. Q o exp(G) (threads 0..127, forward products) and (K o exp(G_last - G))^T
-    //    (threads 128..255, backward products; alpha is 1 beyond the chunk), the chunk decay
-    if (tid < kD) {
-        const int c = tid;
-        unsigned char *tQG = Y + kPtOffQG;
-        float gp = 1.f;
-#pragma unroll 4
-        for (int r = 0; r < kC; ++r) {
-            gp *= AL[r * kYS + c];
-            st_bf16(tQG, tc::kmajor_off(r, c, kD), Yq[r * kYS + c] * gp);
-        }
-        reinterpret_cast<float *>(blk + kOffG)[c] = gp;  // exp(G_last): alpha = 1 past the chunk
-    } else if (tid < 2 * kD) {
-        const int c = tid - kD;
-        unsigned char *tKDT = Y + kPtOffKDT;
-        float gp = 1.f, kd[8];
-#pragma unroll 1
-        for (int rb = kC / 8 - 1; rb >= 0; --rb) {
-#pragma unroll
-            for (int t = 7; t >= 0; --t) {
-                const int r = 8 * rb + t;
-                kd[t] = Yk[r * kYS + c] * gp;
-                gp *= AL[r * kYS + c];
-            }
-            uint32_t wv[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const __nv_bfloat162 p2 = __floats2bfloat162_rn(kd[2 * t], kd[2 * t + 1]);
-                wv[t] = *reinterpret_cast<const uint32_t *>(&p2);
-            }
-            *reinterpret_cast<uint4 *>(tKDT + tc::kmajor_off(c, 8 * rb, kC)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        }
-    }
     __syncthreads();
-    // 8. the operand tiles to the chunk block with 16-byte stores
-    for (int o = tid * 16; o < 32768; o += 512 * 16)  // W and QG
-        *reinterpret_cast<uint4 *>(blk + kOffW + o) = *reinterpret_cast<const uint4 *>(Y + kPtOffW + o);
+    // 8. the W tile (padded -> dense) and the P tile to the chunk block with 16-byte stores
+    for (int c2 = tid; c2 < 1024; c2 += 512) {
+        const int g8 = c2 >> 7, j = (c2 >> 3) & 15, r8 = c2 & 7;
+        const unsigned char *src = Y + kPtOffW + g8 * (kD / 8) * tc::kPadLBO + j * tc::kPadLBO + r8 * 16;
+        *reinterpret_cast<uint4 *>(blk + kOffW + c2 * 16) = *reinterpret_cast<const uint4 *>(src);
+    }
     for (int o = tid * 16; o < 8192; o += 512 * 16)
         *reinterpret_cast<uint4 *>(blk + kOffP + o) = *reinterpret_cast<const uint4 *>(Y + kPtOffP + o);
-    for (int o = tid * 16; o < 16384; o += 512 * 16)
-        *reinterpret_cast<uint4 *>(blk + kOffKDT + o) = *reinterpret_cast<const uint4 *>(Y + kPtOffKDT + o);
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tb, 512);

@@ -46,6 +46,20 @@ __device__ __forceinline__ uint64_t kmajor_desc(const void *tile, int kk, int Kd
     return smem_desc(smem_u32(tile) + (uint32_t)kk * 256u, 128u, (uint32_t)Kd * 16u);
 }
 
+// Padded variant for tiles written element by element: K-adjacent core matrices 144 bytes
+// apart (LBO = 144) so that the 16-byte chunks one warp writes for 32 consecutive k fall in
+// different banks; 8-row groups are Kd * 18 bytes apart.
+constexpr int kPadLBO = 144;
+__host__ __device__ __forceinline__ uint32_t kmajor_off_pad(int r, int k, int Kd)
+{
+    return (uint32_t)((r >> 3) * (Kd / 8) * kPadLBO + (k >> 3) * kPadLBO + (r & 7) * 16 + (k & 7) * 2);
+}
+__host__ __device__ constexpr int kmajor_pad_bytes(int rows, int Kd) { return (rows / 8) * (Kd / 8) * kPadLBO; }
+__device__ __forceinline__ uint64_t kmajor_desc_pad(const void *tile, int kk, int Kd)
+{
+    return smem_desc(smem_u32(tile) + (uint32_t)kk * 2u * kPadLBO, (uint32_t)kPadLBO, (uint32_t)(Kd / 8) * kPadLBO);
+}
+
 // Instruction descriptor: kind::f16, BF16 x BF16 -> FP32, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
 {

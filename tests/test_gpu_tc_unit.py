@@ -20,22 +20,24 @@ def lib(tmp_path_factory):
                    check=True)
     L = ctypes.CDLL(str(out))
     L.tc_gemm_test.restype = ctypes.c_int
-    L.tc_gemm_test.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    L.tc_gemm_test.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                                        ctypes.c_void_p]
     return L
 
 
-@pytest.mark.parametrize("N,K", [(64, 128), (128, 64), (64, 64), (128, 128)])
-def test_tc_gemm_matches_torch(lib, N, K):
+@pytest.mark.parametrize("N,K,pad", [(64, 128, 0), (128, 64, 0), (64, 64, 0), (128, 128, 0), (192, 64, 0),
+                                     (128, 128, 1), (64, 128, 1)])
+def test_tc_gemm_matches_torch(lib, N, K, pad):
     torch.manual_seed(N + K)
     A = torch.randn(128, K, device="cuda").to(torch.bfloat16)
     B = torch.randn(N, K, device="cuda").to(torch.bfloat16)
     D = torch.full((128, N), float("nan"), device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = lib.tc_gemm_test(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, K, status.data_ptr(),
+    rc = lib.tc_gemm_test(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, K, pad, status.data_ptr(),
                           torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert rc == 0 and int(status.item()) == 0
     ref = 3.0 * (A.double() @ B.double().T)
     err = (D.double() - ref).abs().max().item() / ref.abs().max().item()
-    print(f"tcgen05 GEMM 128x{N}x{K}: rel err {err:.2e}")
+    print(f"tcgen05 GEMM 128x{N}x{K} ({'padded' if pad else 'dense'} layout): rel err {err:.2e}")
     assert err < 1e-5
