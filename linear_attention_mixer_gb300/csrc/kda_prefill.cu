@@ -909,8 +909,8 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     unsigned char *sST = sm + 2 * kTcStageBytes;           // S^T [v][k] BF16, K-major, 32 KB
     unsigned char *sUT = sST + 32768;                      // U^T [v][r] BF16, K-major, 16 KB
     float *sgam = reinterpret_cast<float *>(sUT + 16384);  // [2 stages][128] chunk decay
-    float *red = sgam + 2 * kD;                            // [4 lane quarters][64 tokens]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(red + 4 * kC);  // full[0..1], mma1, mma2
+    float *red = sgam + 2 * kD;                            // [2 chunk parities][64 tokens] sums of squares
+    uint64_t *bar = reinterpret_cast<uint64_t *>(red + 4 * kC);  // full[0..1], mma1, mma2 (red uses 2 x 64)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
 
     const int h = blockIdx.x, seq = blockIdx.y;
@@ -931,6 +931,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
     }
+    if (tid < 2 * kC) red[tid] = 0.f;
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -986,10 +987,13 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     const float nw = __ldg(norm_w + vi);
     uint32_t ph1 = 0, ph2 = 0;
     int it = 0;
+    ChunkEntry e_next = c_first < c_last ? table[c_first] : ChunkEntry{0, 0, 0, 0};
     for (int ci = c_first; ci < c_last; ++ci, ++it) {
         const int st = it & 1;
         const unsigned char *stage = sm + st * kTcStageBytes;
-        const ChunkEntry e = table[ci];
+        const ChunkEntry e = e_next;  // read one chunk ahead
+        if (ci + 1 < c_last) e_next = table[ci + 1];
+        float *redc = red + st * kC;
         // output-gate logits of this thread's tokens, kept as raw bits until the epilogue so the
         // loads do not block the warp; their latency hides behind the MMAs
         static_assert(sizeof(T) == 2, "the tensor-core path reads BF16 gate logits");
@@ -1065,7 +1069,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                     sq[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
                 }
             }
-            red[qtr * kC + r0 + lane] = sq[0];
+            atomicAdd(&redc[r0 + lane], sq[0]);  // the four lane quarters add up over v
         }
         // refresh the S^T operand from the updated FP32 state
         {
@@ -1093,17 +1097,25 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 if (good) mma1(sm + (st ^ 1) * kTcStageBytes);
             }
         }
+        // the other parity's sums were last read in the previous chunk's epilogue: clear them
+        if (tid < kC) red[(st ^ 1) * kC + tid] = 0.f;
+        // gated RMSNorm of this thread's 32 tokens: all arithmetic first, then the stores
+        {
+            __nv_bfloat16 y[32];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            if (r0 + r < e.n) {
-                const int rr = r0 + r;
-                const float ms = (red[rr] + red[kC + rr] + red[2 * kC + rr] + red[3 * kC + rr]) * (1.0f / kD);
+            for (int r = 0; r < 32; ++r) {
+                const float rinv = rsqrtf(redc[r0 + r] * (1.0f / kD) + rms_eps);
                 const float gv = __bfloat162float(__ushort_as_bfloat16(graw[r]));
                 // sigmoid(g) = (1 + tanh(g/2)) / 2; the hardware tanh's error is below the BF16
                 // rounding of the output it multiplies
                 const float sg = fmaf(0.5f, tanh_approx(0.5f * gv), 0.5f);
-                IO<T>::st(out + (size_t)(e.t0 + rr) * D + (size_t)h * kD + vi, sg * nw * (o[r] * rsqrtf(ms + rms_eps)));
+                y[r] = __float2bfloat16_rn(sg * nw * (o[r] * rinv));
             }
+            T *obase = out + (size_t)(e.t0 + r0) * D + (size_t)h * kD + vi;
+            const int nv = e.n - r0;  // rows of this thread's half that exist
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+                if (r < nv) obase[(size_t)r * D] = y[r];
         }
     }
 
