@@ -41,6 +41,9 @@ DEC_BYTES_PER_UNIT = 2 * DH * DH * 4 + 5 * DH * 2 + 2 + DH * 2 + 2 * 3 * (KCONV 
 PRE_FLOP_PER_TOKEN_HEAD = 2 * (3 * DH * DH + 5 * CHUNK * DH)
 # algorithmic bytes per token of prefill with BF16 I/O: q,k,v,z,g,b in, out
 PRE_BYTES_PER_TOKEN = (5 * D + H + D) * 2
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch at B=256,
+# from one ncu capture of the decode kernel as it stands; None once that kernel changes.
+DEC_TRAFFIC_B256 = 1_699_759_616 + 1_611_778_048
 
 
 def _peaks():
@@ -483,7 +486,8 @@ def run_kda(args):
             "value": Bd * args.steps * ws / (total_ms_max / 1e3),
             "ms_per_step": total_ms_max / args.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": DEC_TRAFFIC_B256 if Bd == B_DEC else None,
                          "kernel": "decode_persistent_kernel<bf16,3>", "bytes_per_launch": dec_bytes,
                          "launch_ms": r["launch_ms"], "peak_note": src},
             "e2e": {"value": Bd * r["e2e_steps"] * ws / (e2e_ms_max / 1e3), "unit": "tokens/s",

@@ -218,9 +218,11 @@ kda_status kda_prefill(const kda_config_t *cfg, const kda_layer_params *params, 
  *   slots .. out, stream: as for kda_prefill.
  * Its scratch is a file-scope __device__ array of KDA_NOALLOC_WORKSPACE_BYTES
  * (128 MiB; every GPU that loads the library holds it until the process exits).
- * A call whose workspace need exceeds it (about 148 KB per (chunk of 64 tokens,
- * head) plus 512 B per (token, head)) returns KDA_ERR_INVALID before enqueuing
- * anything; split such a call. The first call on a device looks up the array's
+ * A call whose workspace need exceeds it returns KDA_ERR_INVALID before
+ * enqueuing anything; split such a call. The need is about 90.6 KB per (chunk
+ * of 64 tokens, head) with BF16 I/O (about 15 chunks, 980 tokens, of one
+ * sequence at 96 heads), and 148 KB per (chunk, head) plus 512 B per (token,
+ * head) with FP32 I/O. The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current; make that
  * first call before any stream capture. All calls on a device share the array
  * and it keeps the previous call's contents: calls whose work overlaps on the

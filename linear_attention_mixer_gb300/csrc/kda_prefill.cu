@@ -22,6 +22,9 @@
 //                       pass over the chunks carrying S; writes o and the final
 //                       state, and the new conv history
 //   epilogue_kernel     gated per-head RMSNorm of o
+// With BF16 I/O, prep_tc_kernel (A and P on tensor cores) and state_tc_kernel (one CTA
+// per (sequence, head), the chunk products on tensor cores, the RMSNorm fused) replace
+// prep_kernel, state_kernel and epilogue_kernel.
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
@@ -417,7 +420,7 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 }
 
 // ---------------------------------------------------------------- prep on tensor cores
-// BF16 path, one CTA (256 threads) per (chunk, head). Differences from prep_kernel:
+// BF16 path, one CTA (512 threads) per (chunk, head). Differences from prep_kernel:
 //  * every decay factor is the exp of a difference of the cumulative log decay G (one scan per
 //    channel), so all 512 threads write factor elements independently:
 //      exp(G_r - G_n) <= 1 (left), exp(G_n - G_i) <= 1 for i <= n (right), <= e^75 on a block
