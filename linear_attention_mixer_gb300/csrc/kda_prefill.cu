@@ -422,27 +422,73 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 // ---------------------------------------------------------------- prep on tensor cores
 // BF16 path, one CTA (512 threads) per (chunk, head). Differences from prep_kernel:
 //  * every decay factor is the exp of a difference of the cumulative log decay G (one scan per
-//    channel), so all 512 threads write factor elements independently:
+//    channel), so threads form factor elements independently, 8 channels at a time:
 //      exp(G_r - G_n) <= 1 (left), exp(G_n - G_i) <= 1 for i <= n (right), <= e^75 on a block
 //      diagonal; exp(G_r), exp(G_last - G_r) <= 1; all finite in FP32;
-//  * A and P come from tcgen05: for each 16-row block R an M = 128 tile whose rows 0..15 are
-//    k_r o exp(G_r - G_n) and rows 16..31 are q_r o exp(G_r - G_n) times the block's
-//    right-factor tile k_i o exp(G_n - G_i) (N = 64 rows i, K = 128 channels). Every factor is
-//    split into BF16 hi + lo parts (lo = x - hi): rows 32..63 of the tile hold the lo parts and
-//    a second right-factor tile holds lo, so hi*hi + lo*hi + hi*lo is accumulated (the products
-//    then carry about FP32-level error instead of BF16's 2^-9).
+//  * A and P come from tcgen05: for each 16-row block R (reference row n = 16 R) the left tile
+//    holds k_r o exp(G_r - G_n) (rows 0..15) and q_r o exp(G_r - G_n) (rows 16..31) as BF16 hi
+//    parts, and their lo parts (x - hi) in rows 32..63; the right tile holds k_i o exp(G_n - G_i)
+//    for i < n + 16, hi and lo. Three MMA chains accumulate hi*hi + lo*hi + hi*lo into one TMEM
+//    accumulator (the lo-left operand is the left tile seen from row 32), so A and P carry about
+//    FP32-level error instead of BF16's 2^-9;
+//  * the solve is explicit: T = (I + A)^-1 by forward substitution on identity columns, then
+//    [W | U'] = T [Diag(beta) K o exp(G) | Diag(beta) V] as one M = 128, N = 256, K = 64
+//    MMA group, again split hi/lo;
+//  * warps 8..15 write Q o exp(G), (K o exp(G_last - G))^T and exp(G_last) while warps 0..7
+//    build the A/P tiles, so both run at once;
+//  * the CTA that will most likely run next on this SM has its q, k, v, z rows prefetched to L2.
 // Shared memory: FP32 [64][132] arrays (rows padded against bank conflicts) for q^, k^, v and
-// alpha, then one reused region: raw inputs -> MMA tiles -> output tiles + A.
-constexpr int kYS = kD + 4;                         // padded FP32 row
-constexpr int kPtY = 73728;                         // reused region
-// MMA tiles (padded layout, written element by element without bank conflicts)
-constexpr int kPadTile128 = tc::kmajor_pad_bytes(128, kD);  // 36,864
-constexpr int kPtOffTA = 0, kPtOffTBh = kPadTile128, kPtOffTBl = kPadTile128 + kPadTile128 / 2;
-// read-back and output stage: P partial, P tile, W (padded), A
-constexpr int kPtOffPp = 0, kPtOffP = 16384, kPtOffW = 24576, kPtOffA = 57344;
-static_assert(kPtOffTBh + kPadTile128 <= kPtY && kPtOffA + kC * kC * 4 <= kPtY, "prep staging region");
-static_assert(kPtOffW + tc::kmajor_pad_bytes(64, kD) <= kPtOffA, "W must not overlap A (read by the solve)");
+// G, then one reused region (raw inputs -> A/P tiles -> B_lo, T tile, A matrix), and after the
+// A/P phase the q^ array holds B_hi.
+constexpr int kYS = kD + 4;   // padded FP32 row
+constexpr int kMS = kC + 4;   // row pitch of the FP32 A / T matrix (16-byte aligned rows)
+constexpr int kPtY = 73728;   // reused region
+// A/P phase: left tile [64][128], right tiles hi and lo [<= 64][128]. The lo-left descriptor
+// starts 8 KB into the left tile and covers 128 rows (32 KB): it ends inside the region.
+constexpr int kPtL = 0, kPtRh = 16384, kPtRl = 32768;
+// solve phase: B_lo [256][64], T tile [hi rows 0..63, lo rows 64..127][64] (the lo descriptor
+// covers rows 64..191, ending 24 KB into the tile) and the FP32 matrix M [64][68].
+constexpr int kPtBl = 0, kPtT = 32768, kPtM = 49152;
+static_assert(kPtL + 8192 + 32768 <= kPtY && kPtRl + 16384 <= kPtY, "A/P tiles");
+static_assert(kPtT + 24576 <= kPtY && kPtM + kC * kMS * 4 <= kPtY, "solve tiles");
+static_assert(256 * kC * 2 <= kC * kYS * 4, "B_hi must fit in the q^ array");
 constexpr int kPrepTcSmem = 4 * kC * kYS * 4 + kPtY + kC * 4 + 64;
+
+// 8 FP32 values -> BF16 hi parts (nearest) and lo parts (x - hi, nearest), 16 bytes each
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo)
+{
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(&p);
+        h[i] = u;
+        const __nv_bfloat162 q = __floats2bfloat162_rn(x[2 * i] - __uint_as_float(u << 16),
+                                                       x[2 * i + 1] - __uint_as_float(u & 0xFFFF0000u));
+        l[i] = *reinterpret_cast<const uint32_t *>(&q);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float *x)
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t *>(&p);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ void ld8f(const float *p, float *x)
+{
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void st16(unsigned char *p, uint4 v) { *reinterpret_cast<uint4 *>(p) = v; }
 
 template <typename T>
 __global__ void __launch_bounds__(512, 1)
@@ -453,7 +499,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                const T *__restrict__ z, const T *__restrict__ bl,
                unsigned char *__restrict__ chunks, int32_t *__restrict__ err,
-               float gmin, float l2_eps, float q_scale)
+               float gmin, float l2_eps, float q_scale, int pf_stride)
 {
     extern __shared__ __align__(1024) float smf[];
     float *Yq = smf;                                  // [64][132] q^
@@ -483,7 +529,6 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     T *raw = reinterpret_cast<T *>(Y);
     static_assert(4 * kRows * kD * sizeof(T) <= kPtY, "raw staging must fit in the reused region");
     {
-        const T *srcs[4] = {q, k, v, z};
         const T *tl0 = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD;
         for (int e2 = tid; e2 < 4 * kRows * 16; e2 += 512) {
             const int x = e2 / (kRows * 16), rem = e2 - x * (kRows * 16);
@@ -491,11 +536,23 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             const int p = j - 3;
             const bool live = p < n && !(x == 3 && p < 0);
             const int pos = e.pos0 + p;
-            const T *srcp = !live ? srcs[0] + (size_t)e.t0 * D + (size_t)h * kD  // any valid address
-                          : pos >= 0 ? srcs[x] + (size_t)(e.t0 + p) * D + (size_t)h * kD
+            const T *src = x == 0 ? q : x == 1 ? k : x == 2 ? v : z;
+            const T *srcp = !live ? q + (size_t)e.t0 * D + (size_t)h * kD  // any valid address
+                          : pos >= 0 ? src + (size_t)(e.t0 + p) * D + (size_t)h * kD
                                      : tl0 + (size_t)(x * 3 + (pos + 3)) * D;
             cp_async16(raw + ((size_t)x * kRows + j) * kD + 8 * vec, reinterpret_cast<const uint4 *>(srcp) + vec,
                        live ? 16u : 0u);
+        }
+    }
+    // the next CTA on this SM is most likely blockIdx.x + pf_stride: its rows go to L2 now
+    if (tid < 4 * kC && blockIdx.x + (unsigned)pf_stride < gridDim.x) {
+        const unsigned nb = blockIdx.x + (unsigned)pf_stride;
+        const int c2 = (int)(nb / (unsigned)H), h2 = (int)(nb - (unsigned)c2 * (unsigned)H);
+        const ChunkEntry e2 = table[c2];
+        const int x = tid >> 6, r = tid & (kC - 1);
+        if (r < e2.n) {
+            const T *src = (x == 0 ? q : x == 1 ? k : x == 2 ? v : z) + (size_t)(e2.t0 + r) * D + (size_t)h2 * kD;
+            prefetch_l2_bulk(src, kD * sizeof(T));
         }
     }
     unsigned short braw = 0;
@@ -536,8 +593,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
     }
     __syncthreads();
-    // 2b. G_r = sum_{t<=r} gk_t per channel (threads 0..127); every decay factor below is an
-    //     exp of a difference of G, computed independently per element
+    // 2b. G_r = sum_{t<=r} gk_t per channel (warps 0..3), while warps 4..15 take the L2 norms
     if (tid < kD) {
         float acc = 0.f;
 #pragma unroll 16
@@ -545,204 +601,271 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             acc += GL[r * kYS + tid];
             GL[r * kYS + tid] = acc;
         }
+    } else {
+        for (int r = warp - 4; r < kC; r += 12) {
+            float4 a = reinterpret_cast<float4 *>(Yq + r * kYS)[lane];
+            float4 b = reinterpret_cast<float4 *>(Yk + r * kYS)[lane];
+            const float sq = warp_sum(a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w);
+            const float sk = warp_sum(b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w);
+            const float rq = q_scale / sqrtf(sq + l2_eps), rk = 1.0f / sqrtf(sk + l2_eps);
+            a.x *= rq; a.y *= rq; a.z *= rq; a.w *= rq;
+            b.x *= rk; b.y *= rk; b.z *= rk; b.w *= rk;
+            reinterpret_cast<float4 *>(Yq + r * kYS)[lane] = a;
+            reinterpret_cast<float4 *>(Yk + r * kYS)[lane] = b;
+        }
     }
-    // 3. L2 norms and beta (warp w: rows w + 8m); zero the MMA tiles (raw is no longer needed)
-    for (int m = 0; m < kC / 16; ++m) {
-        const int r = warp + 16 * m;
-        float4 a = reinterpret_cast<float4 *>(Yq + r * kYS)[lane];
-        float4 b = reinterpret_cast<float4 *>(Yk + r * kYS)[lane];
-        const float sq = warp_sum(a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w);
-        const float sk = warp_sum(b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w);
-        const float rq = q_scale / sqrtf(sq + l2_eps), rk = 1.0f / sqrtf(sk + l2_eps);
-        a.x *= rq; a.y *= rq; a.z *= rq; a.w *= rq;
-        b.x *= rk; b.y *= rk; b.z *= rk; b.w *= rk;
-        reinterpret_cast<float4 *>(Yq + r * kYS)[lane] = a;
-        reinterpret_cast<float4 *>(Yk + r * kYS)[lane] = b;
-    }
-    for (int o = tid * 16; o < kPtY; o += 512 * 16)
-        *reinterpret_cast<uint4 *>(Y + o) = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 
-    // 4. A and P on the tensor core, one 16-row block at a time (reference row nR = 16 R).
-    //    TMEM columns 128 R .. +63: tile x hi right factors; 128 R + 64 .. +63: tile x lo.
-    unsigned char *tA = Y + kPtOffTA, *tBh = Y + kPtOffTBh, *tBl = Y + kPtOffTBl;
-    static_assert(kPtOffTBl - kPtOffTBh == tc::kmajor_pad_bytes(64, kD), "lo rows follow the hi rows of one tile");
-    constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
-    auto split = [](unsigned char *hi_tile, unsigned char *lo_tile, uint32_t off_hi, uint32_t off_lo, float x) {
-        const __nv_bfloat16 hb = __float2bfloat16_rn(x);
-        *reinterpret_cast<__nv_bfloat16 *>(hi_tile + off_hi) = hb;
-        *reinterpret_cast<__nv_bfloat16 *>(lo_tile + off_lo) = __float2bfloat16_rn(x - __bfloat162float(hb));
-    };
+    unsigned char *blk = chunks + (size_t)blockIdx.x * kTcChunkBytes;
     bool good = true;
-    for (int R = 0; R < kC / kBlk; ++R) {
-        const int nR = R * kBlk;
-        // rows nR..nR+15: left factors k_r, q_r o exp(G_r - G_nR) (tile rows 0..31 hi, 32..63 lo)
-        // and the diagonal-block right factors k_r o exp(G_nR - G_r) (<= e^75)
-        for (int e2 = tid; e2 < kBlk * kD; e2 += 512) {
-            const int rr = e2 >> 7, c = e2 & (kD - 1), r = nR + rr;
-            const float gd = GL[r * kYS + c] - GL[nR * kYS + c];
-            const float f = __expf(gd);
-            split(tA, tA, tc::kmajor_off_pad(rr, c, kD), tc::kmajor_off_pad(2 * kBlk + rr, c, kD), Yk[r * kYS + c] * f);
-            split(tA, tA, tc::kmajor_off_pad(kBlk + rr, c, kD), tc::kmajor_off_pad(3 * kBlk + rr, c, kD),
-                  Yq[r * kYS + c] * f);
-            split(tBh, tBl, tc::kmajor_off_pad(r, c, kD), tc::kmajor_off_pad(r, c, kD), Yk[r * kYS + c] * __expf(-gd));
-        }
-        // rows i < nR: right factors k_i o exp(G_nR - G_i) (<= 1)
-        for (int e2 = tid; e2 < nR * kD; e2 += 512) {
-            const int i = e2 >> 7, c = e2 & (kD - 1);
-            split(tBh, tBl, tc::kmajor_off_pad(i, c, kD), tc::kmajor_off_pad(i, c, kD),
-                  Yk[i * kYS + c] * __expf(GL[nR * kYS + c] - GL[i * kYS + c]));
-        }
-        tc::fence_smem_to_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-        if (tid == 0) {
-            // tBh (rows 0..63) and tBl (rows 64..127) form one N = 128 operand: one MMA group
-            // writes the hi products to columns 128 R .. +63 and the lo products to +64 .. +127
+    if (warp < 8) {
+        // 3. A and P on the tensor core, one 16-row block R at a time; block R accumulates in
+        //    TMEM columns 64 R .. 64 R + 16 (R + 1) - 1, rows 0..15 A, rows 16..31 P.
+        unsigned char *tL = Y + kPtL, *tRh = Y + kPtRh, *tRl = Y + kPtRl;
+        for (int R = 0; R < kC / kBlk; ++R) {
+            const int nR = R * kBlk;
+            {   // left factors of rows nR..nR+15 and the diagonal-block right factors (<= e^75)
+                const int rr = (tid & 7) | ((tid >> 7) << 3), c0 = 8 * ((tid >> 3) & 15), r = nR + rr;
+                float kv[8], qv[8], gr[8], gn[8], kl[8], ql[8], kd[8];
+                ld8f(Yk + r * kYS + c0, kv);
+                ld8f(Yq + r * kYS + c0, qv);
+                ld8f(GL + r * kYS + c0, gr);
+                ld8f(GL + nR * kYS + c0, gn);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tb + 128 * R, tc::kmajor_desc_pad(tA, kk, kD), tc::kmajor_desc_pad(tBh, kk, kD), id128,
-                             kk > 0);
-            tc::mma_commit(bar);
-        }
-        good &= mbar_wait_bounded(bar, (uint32_t)(R & 1), kTcWaitLimit);  // the tiles are reused
-        tc::fence_after_sync();
-    }
-    // 5. read back. Rows 32..63 of the hi accumulator (lo-left x hi-right) live in TMEM lane
-    //    quarter 1 (warps 1, 5): they land first as FP32 partials; then quarter 0 (warps 0, 4)
-    //    adds rows 0..31 of both accumulators (hi x hi, hi x lo) and writes A (FP32, beta and
-    //    mask applied) and the P tile (BF16, inclusive mask).
-    float *Am = reinterpret_cast<float *>(Y + kPtOffA);
-    float *Pp = reinterpret_cast<float *>(Y + kPtOffPp);
-    unsigned char *tP = Y + kPtOffP;
-    if ((warp & 3) == 1) {  // warps 1, 5, 9, 13: block R = warp / 4
-        const int lanes1 = 32 << 16;
-        const int R = warp >> 2;
-        uint32_t raw32[32];
-#pragma unroll 1
-        for (int cb = 0; cb < 2; ++cb) {
-            tc::tmem_ld32_nowait(tb + lanes1 + 128 * R + 32 * cb, raw32);
-            tc::tmem_wait_ld();
-            const int r = 16 * R + (lane & 15);
-            float *dstp = lane < kBlk ? Am : Pp;
+                for (int j = 0; j < 8; ++j) {
+                    const float gd = gr[j] - gn[j];
+                    const float f = __expf(gd);
+                    kl[j] = kv[j] * f;
+                    ql[j] = qv[j] * f;
+                    kd[j] = kv[j] * __expf(-gd);
+                }
+                uint4 hi, lo;
+                split8(kl, hi, lo);
+                st16(tL + tc::kmajor_off(rr, c0, kD), hi);
+                st16(tL + tc::kmajor_off(2 * kBlk + rr, c0, kD), lo);
+                split8(ql, hi, lo);
+                st16(tL + tc::kmajor_off(kBlk + rr, c0, kD), hi);
+                st16(tL + tc::kmajor_off(3 * kBlk + rr, c0, kD), lo);
+                split8(kd, hi, lo);
+                st16(tRh + tc::kmajor_off(r, c0, kD), hi);
+                st16(tRl + tc::kmajor_off(r, c0, kD), lo);
+            }
+            // right factors of rows i < nR: k_i o exp(G_nR - G_i) (<= 1)
+            for (int u = tid; u < kBlk * nR; u += 256) {
+                const int i = (u & 7) | ((u >> 7) << 3), c0 = 8 * ((u >> 3) & 15);
+                float kv[8], gi[8], gn[8], kx[8];
+                ld8f(Yk + i * kYS + c0, kv);
+                ld8f(GL + i * kYS + c0, gi);
+                ld8f(GL + nR * kYS + c0, gn);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) dstp[r * kC + 32 * cb + j] = __uint_as_float(raw32[j]);
+                for (int j = 0; j < 8; ++j) kx[j] = kv[j] * __expf(gn[j] - gi[j]);
+                uint4 hi, lo;
+                split8(kx, hi, lo);
+                st16(tRh + tc::kmajor_off(i, c0, kD), hi);
+                st16(tRl + tc::kmajor_off(i, c0, kD), lo);
+            }
+            tc::fence_smem_to_async();
+            tc::fence_before_sync();
+            named_bar_sync(1, 256);
+            tc::fence_after_sync();
+            if (tid == 0) {
+                const uint32_t id = tc::idesc_bf16(128, kBlk * (R + 1));
+                const uint32_t d = tb + 64 * R;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    tc::mma_bf16(d, tc::kmajor_desc(tL, kk, kD), tc::kmajor_desc(tRh, kk, kD), id, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)  // lo-left rows (tile rows 32..63) x hi-right
+                    tc::mma_bf16(d, tc::kmajor_desc(tL + 2 * kBlk * 16 * kD / 8, kk, kD),
+                                 tc::kmajor_desc(tRh, kk, kD), id, 1);
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    tc::mma_bf16(d, tc::kmajor_desc(tL, kk, kD), tc::kmajor_desc(tRl, kk, kD), id, 1);
+                tc::mma_commit(bar);
+            }
+            good &= mbar_wait_bounded(bar, (uint32_t)(R & 1), kTcWaitLimit);  // the tiles are reused
+            tc::fence_after_sync();
         }
+    } else {
+        // 4. (warps 8..15) Q o exp(G), (K o exp(G_last - G))^T and exp(G_last) to the chunk block
+        //    (G is constant past the chunk, so row 63 holds G_last)
+        const int t2 = tid - 256;
+        for (int u = t2; u < kC * (kD / 8); u += 256) {
+            const int r = (u & 7) | ((u >> 7) << 3), c0 = 8 * ((u >> 3) & 15);
+            float qv[8], gr[8], o[8];
+            ld8f(Yq + r * kYS + c0, qv);
+            ld8f(GL + r * kYS + c0, gr);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] = qv[j] * __expf(gr[j]);
+            st16(blk + kOffQG + tc::kmajor_off(r, c0, kD), pack8_bf16(o));
+        }
+        for (int u = t2; u < kD * (kC / 8); u += 256) {  // channel c, rows 8 rb .. +7
+            const int c = u & (kD - 1), rb = u >> 7;
+            const float gl = GL[(kC - 1) * kYS + c];
+            float o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int r = 8 * rb + j;
+                o[j] = Yk[r * kYS + c] * __expf(gl - GL[r * kYS + c]);
+            }
+            st16(blk + kOffKDT + tc::kmajor_off(c, 8 * rb, kC), pack8_bf16(o));
+        }
+        if (t2 < kD) reinterpret_cast<float *>(blk + kOffG)[t2] = __expf(GL[(kC - 1) * kYS + t2]);
     }
     tc::fence_before_sync();
-    __syncthreads();
+    if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
     tc::fence_after_sync();
-    if ((warp & 3) == 0) {  // warps 0, 4, 8, 12: block R = warp / 4
+
+    // 5. warps 0, 4, 8, 12 read block R = warp / 4 back: A (beta and the strict mask applied) to
+    //    the FP32 matrix M, P (inclusive mask) straight to the chunk block. The other warps build
+    //    the solve's B operand: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the
+    //    64 chunk rows, hi parts in the q^ array (free now), lo parts in the region.
+    float *Mm = reinterpret_cast<float *>(Y + kPtM);
+    unsigned char *tBh = reinterpret_cast<unsigned char *>(Yq), *tBl = Y + kPtBl, *tT = Y + kPtT;
+    if ((warp & 3) == 0) {
         const int R = warp >> 2;
-        uint32_t rh[32], rl[32];
-#pragma unroll 1
-        for (int cb = 0; cb < 2; ++cb) {
-            tc::tmem_ld32_nowait(tb + 128 * R + 32 * cb, rh);
-            tc::tmem_ld32_nowait(tb + 128 * R + 64 + 32 * cb, rl);
-            tc::tmem_wait_ld();
-            if (lane < kBlk) {
-                const int r = 16 * R + lane;
-                const float bt = sbeta[r];
+        uint32_t a0[32], a1[32];
+        tc::tmem_ld32_nowait(tb + 64 * R, a0);
+        tc::tmem_ld32_nowait(tb + 64 * R + 32, a1);
+        tc::tmem_wait_ld();
+        // columns >= 16 (R + 1) were not written by block R's MMA; the masks drop them
+        if (lane < kBlk) {
+            const int r = kBlk * R + lane;
+            const float bt = sbeta[r];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int i = 32 * cb + j;
-                    const float a = __uint_as_float(rh[j]) + __uint_as_float(rl[j]) + Am[r * kC + i];
-                    Am[r * kC + i] = i < r ? bt * a : 0.f;
+            for (int i4 = 0; i4 < kC / 4; ++i4) {
+                float o[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int i = 4 * i4 + t;
+                    const float a = __uint_as_float(i < 32 ? a0[i] : a1[i - 32]);
+                    o[t] = i < r ? bt * a : 0.f;
                 }
-            } else {
-                const int r = 16 * R + lane - kBlk;
-                float pv[16];
+                reinterpret_cast<float4 *>(Mm + r * kMS)[i4] = make_float4(o[0], o[1], o[2], o[3]);
+            }
+        } else {
+            const int r = kBlk * R + lane - kBlk;
 #pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
+            for (int g8 = 0; g8 < kC / 8; ++g8) {
+                float o[8];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int i = 32 * cb + 16 * hb + j;
-                        const float pvv = __uint_as_float(rh[16 * hb + j]) + __uint_as_float(rl[16 * hb + j]) +
-                                          Pp[r * kC + i];
-                        pv[j] = i <= r ? pvv : 0.f;
-                    }
-                    store_row_bf16(tP, r, 32 * cb + 16 * hb, pv, kC);
+                for (int t = 0; t < 8; ++t) {
+                    const int i = 8 * g8 + t;
+                    const float pv = __uint_as_float(i < 32 ? a0[i] : a1[i - 32]);
+                    o[t] = i <= r ? pv : 0.f;
                 }
+                st16(blk + kOffP + tc::kmajor_off(r, 8 * g8, kC), pack8_bf16(o));
             }
         }
-    }
-    if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
-    unsigned char *blk = chunks + (size_t)blockIdx.x * kTcChunkBytes;
-    // 6. Q o exp(G) and (K o exp(G_last - G))^T straight to the chunk block, the chunk decay
-    //    exp(G_last) (G is constant past the chunk, so row 63 holds G_last); then q^ is no
-    //    longer needed and its array takes K o exp(G), the solve's right-hand side.
-    for (int e2 = tid; e2 < kC * kD; e2 += 512) {
-        const int r = e2 >> 7, c = e2 & (kD - 1);
-        st_bf16(blk + kOffQG, tc::kmajor_off(r, c, kD), Yq[r * kYS + c] * __expf(GL[r * kYS + c]));
-    }
-    for (int ch = tid; ch < kD * (kC / 8); ch += 512) {  // one 16-byte chunk: channel c, rows 8 rb .. +7
-        const int c = ch & (kD - 1), rb = ch >> 7;
-        const float gl = GL[(kC - 1) * kYS + c];
-        uint32_t wv[4];
+    } else {
+        const int bt = (warp - 1 - (warp >> 2)) * 32 + lane;  // 0..383 over the 12 other warps
+        for (int u = bt; u < 256 * (kC / 8); u += 384) {
+            const int nn = u & 255, i0 = 8 * (u >> 8);
+            float o[8];
+            if (nn < kD) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int r = 8 * rb + 2 * t;
-            const __nv_bfloat162 p2 =
-                __floats2bfloat162_rn(Yk[r * kYS + c] * __expf(gl - GL[r * kYS + c]),
-                                      Yk[(r + 1) * kYS + c] * __expf(gl - GL[(r + 1) * kYS + c]));
-            wv[t] = *reinterpret_cast<const uint32_t *>(&p2);
+                for (int j = 0; j < 8; ++j)
+                    o[j] = sbeta[i0 + j] * (Yk[(i0 + j) * kYS + nn] * __expf(GL[(i0 + j) * kYS + nn]));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = sbeta[i0 + j] * Yv[(i0 + j) * kYS + nn - kD];
+            }
+            uint4 hi, lo;
+            split8(o, hi, lo);
+            st16(tBh + tc::kmajor_off(nn, i0, kC), hi);
+            st16(tBl + tc::kmajor_off(nn, i0, kC), lo);
         }
-        *reinterpret_cast<uint4 *>(blk + kOffKDT + tc::kmajor_off(c, 8 * rb, kC)) =
-            make_uint4(wv[0], wv[1], wv[2], wv[3]);
-    }
-    if (tid < kD) reinterpret_cast<float *>(blk + kOffG)[tid] = __expf(GL[(kC - 1) * kYS + tid]);
-    __syncthreads();  // q^ has been read
-    float *Kg = Yq;
-    for (int e2 = tid; e2 < kC * kD; e2 += 512) {
-        const int r = e2 >> 7, c = e2 & (kD - 1);
-        Kg[r * kYS + c] = Yk[r * kYS + c] * __expf(GL[r * kYS + c]);
     }
     __syncthreads();
-    // 7. Forward substitution (I + A) X = Diag(beta) B, one column per thread (threads 0..255):
-    //    columns 0..127 of B are k o exp(G) (-> W), 128..255 are v (-> U').
-    if (tid < 2 * kD) {
+    // 6. T = (I + A)^-1, column j by thread j (warps 0, 1): forward substitution on e_j. Once
+    //    both warps have read A, column j overwrites M as T's column (M[r][j] = T[r][j]).
+    if (tid < kC) {
         const int j = tid;
-        const bool isk = j < kD;
-        const int cj = isk ? j : j - kD;
-        const float *Bsrc = isk ? Kg : Yv;
         float X[kC];
 #pragma unroll
         for (int r = 0; r < kC; ++r) {
-            float x0 = sbeta[r] * Bsrc[r * kYS + cj], x1 = 0.f, x2 = 0.f, x3 = 0.f;
+            float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
 #pragma unroll
             for (int i = 0; i + 4 <= r; i += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(Am + r * kC + i);
+                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + r * kMS + i);
                 x0 = fmaf(-a4.x, X[i], x0);
                 x1 = fmaf(-a4.y, X[i + 1], x1);
                 x2 = fmaf(-a4.z, X[i + 2], x2);
                 x3 = fmaf(-a4.w, X[i + 3], x3);
             }
 #pragma unroll
-            for (int i = r & ~3; i < r; ++i) x0 = fmaf(-Am[r * kC + i], X[i], x0);
-            X[r] = (x0 + x1) + (x2 + x3);
+            for (int i = r & ~3; i < r; ++i) x0 = fmaf(-Mm[r * kMS + i], X[i], x0);
+            X[r] = r == j ? 1.f : (r < j ? 0.f : (x0 + x1) + (x2 + x3));
         }
-        if (isk) {
-            unsigned char *tW = Y + kPtOffW;  // the MMA tiles are free now (padded layout)
+        named_bar_sync(2, kC);
 #pragma unroll
-            for (int r = 0; r < kC; ++r) st_bf16(tW, tc::kmajor_off_pad(r, cj, kD), X[r]);
-        } else {
-            float *Up = reinterpret_cast<float *>(blk + kOffUp);
-#pragma unroll
-            for (int r = 0; r < kC; ++r) Up[r * kD + cj] = X[r];
-        }
+        for (int r = 0; r < kC; ++r) Mm[r * kMS + j] = X[r];
     }
     __syncthreads();
-    // 8. the W tile (padded -> dense) and the P tile to the chunk block with 16-byte stores
-    for (int c2 = tid; c2 < 1024; c2 += 512) {
-        const int g8 = c2 >> 7, j = (c2 >> 3) & 15, r8 = c2 & 7;
-        const unsigned char *src = Y + kPtOffW + g8 * (kD / 8) * tc::kPadLBO + j * tc::kPadLBO + r8 * 16;
-        *reinterpret_cast<uint4 *>(blk + kOffW + c2 * 16) = *reinterpret_cast<const uint4 *>(src);
+    {   // T -> BF16 hi (tile rows 0..63) and lo (rows 64..127), one 8-column group per thread
+        const int r = (tid & 7) | ((tid >> 6) << 3), c0 = 8 * ((tid >> 3) & 7);
+        float tv[8];
+        ld8f(Mm + r * kMS + c0, tv);
+        uint4 hi, lo;
+        split8(tv, hi, lo);
+        st16(tT + tc::kmajor_off(r, c0, kC), hi);
+        st16(tT + tc::kmajor_off(kC + r, c0, kC), lo);
     }
-    for (int o = tid * 16; o < 8192; o += 512 * 16)
-        *reinterpret_cast<uint4 *>(blk + kOffP + o) = *reinterpret_cast<const uint4 *>(Y + kPtOffP + o);
+    tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
+    tc::fence_after_sync();
+    // 7. [W | U'] (rows r, columns: 128 channels of W, then 128 of U') in TMEM columns 256..511
+    if (tid == 0) {
+        constexpr uint32_t id = tc::idesc_bf16(128, 256);
+        const uint32_t d = tb + 256;
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+            tc::mma_bf16(d, tc::kmajor_desc(tT, kk, kC), tc::kmajor_desc(tBh, kk, kC), id, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)  // lo T rows (tile rows 64..127) x hi B
+            tc::mma_bf16(d, tc::kmajor_desc(tT + kC * 16 * kC / 8, kk, kC), tc::kmajor_desc(tBh, kk, kC), id, 1);
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+            tc::mma_bf16(d, tc::kmajor_desc(tT, kk, kC), tc::kmajor_desc(tBl, kk, kC), id, 1);
+        tc::mma_commit(bar);
+    }
+    good = mbar_wait_bounded(bar, 0u, kTcWaitLimit);  // fifth completion of the barrier
+    tc::fence_after_sync();
+    // 8. warps on lane quarters 0 and 1 (rows 0..63) write W (BF16 tile) and U' (FP32 rows)
+    if ((warp & 3) < 2 && good) {
+        const int qd = warp & 3, part = warp >> 2;  // part 0, 1: W columns; 2, 3: U' columns
+        const int r = 32 * qd + lane;
+        uint32_t c0v[32], c1v[32];
+        const uint32_t ta = tb + ((uint32_t)(32 * qd) << 16) + 256 + 64 * part;
+        tc::tmem_ld32_nowait(ta, c0v);
+        tc::tmem_ld32_nowait(ta + 32, c1v);
+        tc::tmem_wait_ld();
+        if (part < 2) {
+#pragma unroll
+            for (int g8 = 0; g8 < 8; ++g8) {
+                float o[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int cc = 8 * g8 + t;
+                    o[t] = __uint_as_float(cc < 32 ? c0v[cc] : c1v[cc - 32]);
+                }
+                st16(blk + kOffW + tc::kmajor_off(r, 64 * part + 8 * g8, kD), pack8_bf16(o));
+            }
+        } else {
+            float4 *dst = reinterpret_cast<float4 *>(blk + kOffUp) + (r * kD + 64 * (part - 2)) / 4;
+#pragma unroll
+            for (int i4 = 0; i4 < 16; ++i4) {
+                const int cc = 4 * i4;
+                dst[i4] = make_float4(__uint_as_float(cc < 32 ? c0v[cc] : c1v[cc - 32]),
+                                      __uint_as_float(cc + 1 < 32 ? c0v[cc + 1] : c1v[cc + 1 - 32]),
+                                      __uint_as_float(cc + 2 < 32 ? c0v[cc + 2] : c1v[cc + 2 - 32]),
+                                      __uint_as_float(cc + 3 < 32 ? c0v[cc + 3] : c1v[cc + 3 - 32]));
+            }
+        }
+    }
+    tc::fence_before_sync();
+    if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
@@ -1209,12 +1332,15 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
     if (e != cudaSuccess) return e;
     if (total_chunks > 0) {
         if constexpr (kTC) {
+            int sms = 0;
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, st.device);
+            if (e != cudaSuccess) return e;
             e = cudaFuncSetAttribute(prep_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepTcSmem);
             if (e != cudaSuccess) return e;
             prep_tc_kernel<T><<<(unsigned)(total_chunks * H), 512, kPrepTcSmem, stream>>>(
                 p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
                 (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, chunks, st.err,
-                c.gate_lower_bound, c.l2_eps, c.q_scale);
+                c.gate_lower_bound, c.l2_eps, c.q_scale, sms);
         } else {
             const int prep_smem = kPrepSmemFloats * (int)sizeof(float);
             e = cudaFuncSetAttribute(prep_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);

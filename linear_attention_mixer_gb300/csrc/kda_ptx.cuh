@@ -89,6 +89,18 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes % 16 == 0); no completion.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32) of the CTA; id 1..15 (0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // 16-bit read-only global load whose result is not needed until later (no conversion here).
 __device__ __forceinline__ unsigned short ld_nc_u16(const void *p)
 {
