@@ -29,7 +29,9 @@
  *    allocated on.
  *  - All tensors are dense, row-major, with the layouts given below. The caller
  *    owns every input, output and parameter buffer; the library owns the state.
- *  - Device pointers must be 16-byte aligned.
+ *  - The row tensors q, k, v, z, g and out must be 16-byte aligned (calls that
+ *    get one that is not return KDA_ERR_INVALID); b needs only its element
+ *    alignment. Other device pointers must be 16-byte aligned.
  *  - Calls that use the same kda_state must be ordered (same stream, or
  *    synchronised by the caller); the library keeps per-state workspace.
  */

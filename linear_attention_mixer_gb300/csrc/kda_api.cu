@@ -295,6 +295,7 @@ kda_status kda_decode_token(const kda_config_t *cfg, const kda_layer_params *par
     if (B < 0) return fail(KDA_ERR_INVALID, "B must be >= 0 (got %d)", B);
     if (B == 0) return KDA_OK;
     if (!slots || !q || !k || !v || !z || !b || !g || !out) return fail(KDA_ERR_INVALID, "a tensor pointer is NULL");
+    if (!kda::io_aligned(q, k, v, z, g, out)) return fail(KDA_ERR_INVALID, "q, k, v, z, g or out is not 16-byte aligned");
     if ((int64_t)B * cfg->num_heads > INT_MAX) return fail(KDA_ERR_INVALID, "B * num_heads exceeds the grid limit");
     if (!device_matches(st)) return KDA_ERR_INVALID;
     cudaError_t e = kda::launch_decode(*st, *params, slots, B, q, k, v, z, b, g, out,
@@ -327,6 +328,8 @@ kda_status kda_prefill(const kda_config_t *cfg, const kda_layer_params *params, 
     const int64_t total_T = cu_seqlens_host[N];
     if (total_T > 0 && (!q || !k || !v || !z || !b || !g || !out))
         return fail(KDA_ERR_INVALID, "a tensor pointer is NULL");
+    if (total_T > 0 && !kda::io_aligned(q, k, v, z, g, out))
+        return fail(KDA_ERR_INVALID, "q, k, v, z, g or out is not 16-byte aligned");
     if (total_chunks * cfg->num_heads > INT_MAX || (total_T * cfg->num_heads + 7) / 8 > INT_MAX)
         return fail(KDA_ERR_INVALID, "too many tokens for one call");
     if (!device_matches(st)) return KDA_ERR_INVALID;

@@ -66,6 +66,16 @@ cudaError_t launch_prefill(const State &st, const kda_layer_params &p, const int
 
 // Error text and config checks shared by every entry point (kda_api.cu).
 kda_status record_error(kda_status s, const char *msg);
+// true when the per-token row tensors are 16-byte aligned (their rows move as bulk and
+// tensor copies of whole 16-byte units; b is read element by element and needs no more
+// than its own alignment)
+inline bool io_aligned(const void *q, const void *k, const void *v, const void *z, const void *g, const void *out)
+{
+    const uintptr_t u = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(z) |
+                        reinterpret_cast<uintptr_t>(g) | reinterpret_cast<uintptr_t>(out);
+    return (u & 15u) == 0;
+}
 bool config_ok(const kda_config_t *c);
 
 }  // namespace kda

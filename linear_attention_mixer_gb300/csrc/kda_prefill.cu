@@ -25,6 +25,9 @@
 // With BF16 I/O, prep_tc_kernel (A and P on tensor cores) and state_tc_kernel (one CTA
 // per (sequence, head), the chunk products on tensor cores, the RMSNorm fused) replace
 // prep_kernel, state_kernel and epilogue_kernel.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
@@ -421,35 +424,40 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 
 // ---------------------------------------------------------------- prep on tensor cores
 // BF16 path, one CTA (512 threads) per (chunk, head). Differences from prep_kernel:
+//  * the chunk's raw rows arrive by bulk copies on one mbarrier, and the CTA that will most
+//    likely run next on this SM has its q, k, v, z rows prefetched to L2;
 //  * every decay factor is the exp of a difference of the cumulative log decay G (one scan per
 //    channel), so threads form factor elements independently, 8 channels at a time:
 //      exp(G_r - G_n) <= 1 (left), exp(G_n - G_i) <= 1 for i <= n (right), <= e^75 on a block
 //      diagonal; exp(G_r), exp(G_last - G_r) <= 1; all finite in FP32;
-//  * A and P come from tcgen05: for each 16-row block R (reference row n = 16 R) the left tile
-//    holds k_r o exp(G_r - G_n) (rows 0..15) and q_r o exp(G_r - G_n) (rows 16..31) as BF16 hi
-//    parts, and their lo parts (x - hi) in rows 32..63; the right tile holds k_i o exp(G_n - G_i)
-//    for i < n + 16, hi and lo. Three MMA chains accumulate hi*hi + lo*hi + hi*lo into one TMEM
-//    accumulator (the lo-left operand is the left tile seen from row 32), so A and P carry about
-//    FP32-level error instead of BF16's 2^-9;
-//  * the solve is explicit: T = (I + A)^-1 by forward substitution on identity columns, then
-//    [W | U'] = T [Diag(beta) K o exp(G) | Diag(beta) V] as one M = 128, N = 256, K = 64
-//    MMA group, again split hi/lo;
+//  * A and P come from tcgen05 in one accumulator: left rows are k_r o exp(G_r - G_n) (rows
+//    0..63) and q_r o exp(G_r - G_n) (rows 64..127), n = 16 (r / 16) the first row of r's
+//    16-row block; right rows are, for each block R, k_i o exp(G_n - G_i) for i < n + 16
+//    (160 rows in all). Row r of block R reads the columns of R's own right rows. Every factor
+//    is split into a BF16 hi part and a lo part (x - hi) and three MMA chains accumulate
+//    hi*hi + lo*hi + hi*lo, so A and P carry about FP32-level error instead of BF16's 2^-9.
+//    The tiles are built one half of the channels at a time (24 MMAs in all: an MMA has a
+//    fixed issue cost, so few wide ones beat many narrow ones);
+//  * the solve is explicit: T = (I + A)^-1 by blocked inversion (16 x 16 diagonal blocks by
+//    forward substitution, then one block row at a time), then W = T Diag(beta) (K o exp(G))
+//    and U'^T = (Diag(beta) V)^T T^T on the tensor core, again split hi/lo;
 //  * warps 8..15 write Q o exp(G), (K o exp(G_last - G))^T and exp(G_last) while warps 0..7
-//    build the A/P tiles, so both run at once;
-//  * the CTA that will most likely run next on this SM has its q, k, v, z rows prefetched to L2.
+//    build the A/P tiles, so both run at once.
 // Shared memory: FP32 [64][132] arrays (rows padded against bank conflicts) for q^, k^, v and
-// G, then one reused region (raw inputs -> A/P tiles -> B_lo, T tile, A matrix), and after the
-// A/P phase the q^ array holds B_hi.
+// G, then one reused region (raw inputs -> A/P tiles -> B_lo, T tile, A matrix); after the A/P
+// phase the q^ array holds B_hi, and after the B build the v and G arrays hold T and scratch.
 constexpr int kYS = kD + 4;   // padded FP32 row
-constexpr int kMS = kC + 4;   // row pitch of the FP32 A / T matrix (16-byte aligned rows)
+constexpr int kMS = kC + 4;   // row pitch of the FP32 A / T matrices (16-byte aligned rows)
 constexpr int kPtY = 73728;   // reused region
-// A/P phase: left tile [64][128], right tiles hi and lo [<= 64][128]. The lo-left descriptor
-// starts 8 KB into the left tile and covers 128 rows (32 KB): it ends inside the region.
-constexpr int kPtL = 0, kPtRh = 16384, kPtRl = 32768;
-// solve phase: B_lo [256][64], T tile [hi rows 0..63, lo rows 64..127][64] (the lo descriptor
-// covers rows 64..191, ending 24 KB into the tile) and the FP32 matrix M [64][68].
+// A/P phase, one half of the channels at a time: left tiles hi and lo [128 rows: k rows 0..63,
+// q rows 64..127][64 channels], right tiles hi and lo [160 rows][64], block R's segment of
+// right rows (i < 16 (R + 1), reference row 16 R) starting at row 8 R (R + 1).
+constexpr int kApN = 160;
+constexpr int kApLh = 0, kApLl = 16384, kApRh = 32768, kApRl = 32768 + kApN * 128;
+// solve phase: B_lo [256][64], T tile [hi rows 0..63, lo rows 64..127][64] (a descriptor
+// starting at row 64 covers rows 64..191, ending 24 KB into the tile) and the FP32 A matrix.
 constexpr int kPtBl = 0, kPtT = 32768, kPtM = 49152;
-static_assert(kPtL + 8192 + 32768 <= kPtY && kPtRl + 16384 <= kPtY, "A/P tiles");
+static_assert(kApRl + kApN * 128 <= kPtY, "A/P tiles");
 static_assert(kPtT + 24576 <= kPtY && kPtM + kC * kMS * 4 <= kPtY, "solve tiles");
 static_assert(256 * kC * 2 <= kC * kYS * 4, "B_hi must fit in the q^ array");
 constexpr int kPrepTcSmem = 4 * kC * kYS * 4 + kPtY + kC * 4 + 64;
@@ -490,6 +498,17 @@ __device__ __forceinline__ void ld8f(const float *p, float *x)
 
 __device__ __forceinline__ void st16(unsigned char *p, uint4 v) { *reinterpret_cast<uint4 *>(p) = v; }
 
+// Three MMA chains hi*hi + lo*hi + hi*lo into one accumulator. The descriptors are those of
+// K-step 0; step kk starts 256 bytes (16 descriptor units) later.
+__device__ __forceinline__ void mma_split3(uint32_t d, uint64_t a_hi, uint64_t a_lo, uint64_t b_hi, uint64_t b_lo,
+                                           uint32_t idesc, int ksteps, bool acc0)
+{
+    for (int kk = 0; kk < ksteps; ++kk)
+        tc::mma_bf16(d, a_hi + 16u * kk, b_hi + 16u * kk, idesc, (acc0 || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < ksteps; ++kk) tc::mma_bf16(d, a_lo + 16u * kk, b_hi + 16u * kk, idesc, 1u);
+    for (int kk = 0; kk < ksteps; ++kk) tc::mma_bf16(d, a_hi + 16u * kk, b_lo + 16u * kk, idesc, 1u);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(512, 1)
 prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
@@ -499,7 +518,9 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                const T *__restrict__ z, const T *__restrict__ bl,
                unsigned char *__restrict__ chunks, int32_t *__restrict__ err,
-               float gmin, float l2_eps, float q_scale, int pf_stride)
+               float gmin, float l2_eps, float q_scale, int pf_stride, int box_rows,
+               const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z)
 {
     extern __shared__ __align__(1024) float smf[];
     float *Yq = smf;                                  // [64][132] q^
@@ -508,8 +529,8 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     float *GL = Yv + kC * kYS;                        // [64][132] gk, then G = cumulative log decay
     unsigned char *Y = reinterpret_cast<unsigned char *>(GL + kC * kYS);
     float *sbeta = reinterpret_cast<float *>(Y + kPtY);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sbeta + kC);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 1);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbeta + kC);  // [0] inputs, [1..2] A/P buffers, [3] solve
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 4);
 
     const int chunk = blockIdx.x / H, h = blockIdx.x - (blockIdx.x / H) * H;
     const ChunkEntry e = table[chunk];
@@ -521,38 +542,46 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     const size_t D = (size_t)H * kD;
 
     if (warp == 0) tc::tmem_alloc(tslot, 512);
-    if (tid == 0) { mbar_init(bar, 1); fence_mbar_init(); }
-
-    // 0. raw q, k, v rows with 3 rows of history, and z, staged with asynchronous 16-byte
-    //    copies (zero-filled past the chunk); the beta logits are loaded meanwhile
-    constexpr int kRows = kC + 3;  // staged row j holds position j - 3 of the chunk
+    // staged row j of stream x holds position j - 3 of the chunk; 3 spare rows at the end take
+    // the overhang of a box that starts at the chunk's first row
+    constexpr int kRows = kC + 6;
     T *raw = reinterpret_cast<T *>(Y);
     static_assert(4 * kRows * kD * sizeof(T) <= kPtY, "raw staging must fit in the reused region");
-    {
-        const T *tl0 = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD;
-        for (int e2 = tid; e2 < 4 * kRows * 16; e2 += 512) {
-            const int x = e2 / (kRows * 16), rem = e2 - x * (kRows * 16);
-            const int j = rem >> 4, vec = rem & 15;
-            const int p = j - 3;
-            const bool live = p < n && !(x == 3 && p < 0);
-            const int pos = e.pos0 + p;
-            const T *src = x == 0 ? q : x == 1 ? k : x == 2 ? v : z;
-            const T *srcp = !live ? q + (size_t)e.t0 * D + (size_t)h * kD  // any valid address
-                          : pos >= 0 ? src + (size_t)(e.t0 + p) * D + (size_t)h * kD
-                                     : tl0 + (size_t)(x * 3 + (pos + 3)) * D;
-            cp_async16(raw + ((size_t)x * kRows + j) * kD + 8 * vec, reinterpret_cast<const uint4 *>(srcp) + vec,
-                       live ? 16u : 0u);
+    static_assert((kRows * kD * sizeof(T)) % 128 == 0, "TMA destinations must be 128-byte aligned");
+    if (tid == 32) {
+        // 0. one 2-D box of box_rows rows (x = the head's 128 channels) per stream: from 3 rows
+        //    before the chunk, or, for a sequence's first chunk (and for z), from its first row,
+        //    with the 3 history rows then taken from the conv tail. Rows past the chunk are
+        //    whatever follows in the tensor (or zero past its end): every value computed from
+        //    them is masked.
+        for (int i = 0; i < 4; ++i) mbar_init(bars + i, 1);
+        fence_mbar_init();
+        const bool first = e.pos0 == 0;
+        mbar_arrive_expect_tx(bars, (uint32_t)((4 * box_rows + (first ? 9 : 0)) * kD * sizeof(T)));
+        const int hx = h * kD;
+        const int ylo = first ? e.t0 : e.t0 - 3, jlo = first ? 3 : 0;
+        tma_load_2d(raw + (size_t)(0 * kRows + jlo) * kD, &tm_q, hx, ylo, bars);
+        tma_load_2d(raw + (size_t)(1 * kRows + jlo) * kD, &tm_k, hx, ylo, bars);
+        tma_load_2d(raw + (size_t)(2 * kRows + jlo) * kD, &tm_v, hx, ylo, bars);
+        tma_load_2d(raw + (size_t)(3 * kRows + 3) * kD, &tm_z, hx, e.t0, bars);
+        if (first) {
+            const T *tl0 = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD;
+            for (int x = 0; x < 3; ++x)
+                for (int j = 0; j < 3; ++j)
+                    bulk_g2s(raw + (size_t)(x * kRows + j) * kD, tl0 + (size_t)(x * 3 + j) * D, kD * sizeof(T), bars);
         }
     }
-    // the next CTA on this SM is most likely blockIdx.x + pf_stride: its rows go to L2 now
-    if (tid < 4 * kC && blockIdx.x + (unsigned)pf_stride < gridDim.x) {
+    // the next CTA on this SM is most likely blockIdx.x + pf_stride: its boxes go to L2 now
+    if (tid == 256 && blockIdx.x + (unsigned)pf_stride < gridDim.x) {
         const unsigned nb = blockIdx.x + (unsigned)pf_stride;
         const int c2 = (int)(nb / (unsigned)H), h2 = (int)(nb - (unsigned)c2 * (unsigned)H);
         const ChunkEntry e2 = table[c2];
-        const int x = tid >> 6, r = tid & (kC - 1);
-        if (r < e2.n) {
-            const T *src = (x == 0 ? q : x == 1 ? k : x == 2 ? v : z) + (size_t)(e2.t0 + r) * D + (size_t)h2 * kD;
-            prefetch_l2_bulk(src, kD * sizeof(T));
+        if (e2.n > 0) {
+            const int y2 = e2.pos0 == 0 ? e2.t0 : e2.t0 - 3;
+            tma_prefetch_2d(&tm_q, h2 * kD, y2);
+            tma_prefetch_2d(&tm_k, h2 * kD, y2);
+            tma_prefetch_2d(&tm_v, h2 * kD, y2);
+            tma_prefetch_2d(&tm_z, h2 * kD, e2.t0);
         }
     }
     unsigned short braw = 0;
@@ -563,33 +592,48 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                               : make_float4(0.f, 0.f, 0.f, 0.f);
     const float p_dt = __ldg(dt_bias + (size_t)h * kD + pc);
     const float p_eA = expf(__ldg(A_log + h));
-    cp_async_wait_all();
     tc::fence_before_sync();
-    __syncthreads();
+    __syncthreads();  // barrier init and TMEM base visible
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
+    bool good = mbar_wait_bounded(bars, 0u, kTcWaitLimit);
     if (tid < kC) sbeta[tid] = tid < n ? sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
 
     // 1. conv + SiLU (sliding window in registers) for stream px < 3, 2. the gates for px == 3;
-    //    thread (channel pc, stream px) walks all 64 rows
+    //    thread (channel pc, stream px) walks all 64 rows, 32 at a time so that 32 independent
+    //    exponentials are in flight; the sigmoids' reciprocals run on the FMA pipe. Exponents
+    //    are capped at 80 (the sigmoid is then below 2e-35 and the SiLU output tiny either way).
     if (px < 3) {
         float *dst = px == 0 ? Yq : (px == 1 ? Yk : Yv);
         const T *col = raw + (size_t)px * kRows * kD + pc;
         float h0 = IO<T>::ld(col), h1 = IO<T>::ld(col + kD), h2 = IO<T>::ld(col + 2 * kD);
-#pragma unroll 8
-        for (int r = 0; r < kC; ++r) {
-            const float xin = IO<T>::ld(col + (r + 3) * kD);
-            const float cv = fmaf(p_w.x, h0, fmaf(p_w.y, h1, fmaf(p_w.z, h2, p_w.w * xin)));
-            dst[r * kYS + pc] = r < n ? __fdividef(cv, 1.0f + __expf(-cv)) : 0.f;
-            h0 = h1; h1 = h2; h2 = xin;
+#pragma unroll 1
+        for (int r0 = 0; r0 < kC; r0 += 32) {
+            float cv[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const float xin = IO<T>::ld(col + (r0 + u + 3) * kD);
+                cv[u] = fmaf(p_w.x, h0, fmaf(p_w.y, h1, fmaf(p_w.z, h2, p_w.w * xin)));
+                h0 = h1; h1 = h2; h2 = xin;
+            }
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const float sg = rcp_newton(1.0f + __expf(fminf(-cv[u], 80.f)));
+                dst[(r0 + u) * kYS + pc] = r0 + u < n ? cv[u] * sg : 0.f;
+            }
         }
     } else {
         const T *col = raw + ((size_t)3 * kRows + 3) * kD + pc;
-#pragma unroll 8
-        for (int r = 0; r < kC; ++r) {
-            const float zz = IO<T>::ld(col + r * kD);
-            const float sg = __fdividef(1.0f, 1.0f + __expf(-p_eA * (zz + p_dt)));
-            GL[r * kYS + pc] = r < n ? gmin * sg : 0.f;  // gk; 0 (no decay) past the chunk
+#pragma unroll 1
+        for (int r0 = 0; r0 < kC; r0 += 32) {
+            float zz[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) zz[u] = IO<T>::ld(col + (r0 + u) * kD);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const float sg = rcp_newton(1.0f + __expf(fminf(-p_eA * (zz[u] + p_dt), 80.f)));
+                GL[(r0 + u) * kYS + pc] = r0 + u < n ? gmin * sg : 0.f;  // gk; 0 (no decay) past the chunk
+            }
         }
     }
     __syncthreads();
@@ -617,42 +661,46 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     __syncthreads();
 
     unsigned char *blk = chunks + (size_t)blockIdx.x * kTcChunkBytes;
-    bool good = true;
     if (warp < 8) {
-        // 3. A and P on the tensor core, one 16-row block R at a time; block R accumulates in
-        //    TMEM columns 64 R .. 64 R + 16 (R + 1) - 1, rows 0..15 A, rows 16..31 P.
-        unsigned char *tL = Y + kPtL, *tRh = Y + kPtRh, *tRl = Y + kPtRl;
-        for (int R = 0; R < kC / kBlk; ++R) {
-            const int nR = R * kBlk;
-            {   // left factors of rows nR..nR+15 and the diagonal-block right factors (<= e^75)
-                const int rr = (tid & 7) | ((tid >> 7) << 3), c0 = 8 * ((tid >> 3) & 15), r = nR + rr;
-                float kv[8], qv[8], gr[8], gn[8], kl[8], ql[8], kd[8];
+        // 3. A and P on the tensor core: the four 16-row blocks share one accumulator of 160
+        //    TMEM columns (lane = left row, column = right row; only each block's own segment
+        //    is used), built and multiplied one half of the channels at a time.
+        unsigned char *tLh = Y + kApLh, *tLl = Y + kApLl, *tRh = Y + kApRh, *tRl = Y + kApRl;
+        for (int half = 0; half < 2; ++half) {
+            const int c_h = half * (kD / 2);
+            if (half) {
+                good &= mbar_wait_bounded(bars + 1, 0u, kTcWaitLimit);  // half 0 has read the tiles
+                tc::fence_after_sync();
+            }
+            // left rows r (k) and 64 + r (q): factor exp(G_r - G_n), n = 16 (r / 16)
+            for (int u = tid; u < kC * 8; u += 256) {
+                const int r = (u & 7) | ((u >> 6) << 3), cl = 8 * ((u >> 3) & 7), c0 = c_h + cl;
+                const int nR = r & ~(kBlk - 1);
+                float kv[8], qv[8], gr[8], gn[8], kl[8], ql[8];
                 ld8f(Yk + r * kYS + c0, kv);
                 ld8f(Yq + r * kYS + c0, qv);
                 ld8f(GL + r * kYS + c0, gr);
                 ld8f(GL + nR * kYS + c0, gn);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float gd = gr[j] - gn[j];
-                    const float f = __expf(gd);
+                    const float f = __expf(gr[j] - gn[j]);
                     kl[j] = kv[j] * f;
                     ql[j] = qv[j] * f;
-                    kd[j] = kv[j] * __expf(-gd);
                 }
                 uint4 hi, lo;
                 split8(kl, hi, lo);
-                st16(tL + tc::kmajor_off(rr, c0, kD), hi);
-                st16(tL + tc::kmajor_off(2 * kBlk + rr, c0, kD), lo);
+                st16(tLh + tc::kmajor_off(r, cl, kD / 2), hi);
+                st16(tLl + tc::kmajor_off(r, cl, kD / 2), lo);
                 split8(ql, hi, lo);
-                st16(tL + tc::kmajor_off(kBlk + rr, c0, kD), hi);
-                st16(tL + tc::kmajor_off(3 * kBlk + rr, c0, kD), lo);
-                split8(kd, hi, lo);
-                st16(tRh + tc::kmajor_off(r, c0, kD), hi);
-                st16(tRl + tc::kmajor_off(r, c0, kD), lo);
+                st16(tLh + tc::kmajor_off(kC + r, cl, kD / 2), hi);
+                st16(tLl + tc::kmajor_off(kC + r, cl, kD / 2), lo);
             }
-            // right factors of rows i < nR: k_i o exp(G_nR - G_i) (<= 1)
-            for (int u = tid; u < kBlk * nR; u += 256) {
-                const int i = (u & 7) | ((u >> 7) << 3), c0 = 8 * ((u >> 3) & 15);
+            // right rows: segment R, row i < 16 (R + 1): k_i o exp(G_nR - G_i) (<= 1 for i <= nR,
+            // <= e^75 on the diagonal block)
+            for (int u = tid; u < kApN * 8; u += 256) {
+                const int row = (u & 7) | ((u >> 6) << 3), cl = 8 * ((u >> 3) & 7), c0 = c_h + cl;
+                const int R = row < 16 ? 0 : (row < 48 ? 1 : (row < 96 ? 2 : 3));
+                const int i = row - 8 * R * (R + 1), nR = kBlk * R;
                 float kv[8], gi[8], gn[8], kx[8];
                 ld8f(Yk + i * kYS + c0, kv);
                 ld8f(GL + i * kYS + c0, gi);
@@ -661,31 +709,21 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 for (int j = 0; j < 8; ++j) kx[j] = kv[j] * __expf(gn[j] - gi[j]);
                 uint4 hi, lo;
                 split8(kx, hi, lo);
-                st16(tRh + tc::kmajor_off(i, c0, kD), hi);
-                st16(tRl + tc::kmajor_off(i, c0, kD), lo);
+                st16(tRh + tc::kmajor_off(row, cl, kD / 2), hi);
+                st16(tRl + tc::kmajor_off(row, cl, kD / 2), lo);
             }
             tc::fence_smem_to_async();
             tc::fence_before_sync();
             named_bar_sync(1, 256);
             tc::fence_after_sync();
             if (tid == 0) {
-                const uint32_t id = tc::idesc_bf16(128, kBlk * (R + 1));
-                const uint32_t d = tb + 64 * R;
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)
-                    tc::mma_bf16(d, tc::kmajor_desc(tL, kk, kD), tc::kmajor_desc(tRh, kk, kD), id, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)  // lo-left rows (tile rows 32..63) x hi-right
-                    tc::mma_bf16(d, tc::kmajor_desc(tL + 2 * kBlk * 16 * kD / 8, kk, kD),
-                                 tc::kmajor_desc(tRh, kk, kD), id, 1);
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)
-                    tc::mma_bf16(d, tc::kmajor_desc(tL, kk, kD), tc::kmajor_desc(tRl, kk, kD), id, 1);
-                tc::mma_commit(bar);
+                mma_split3(tb, tc::kmajor_desc(tLh, 0, kD / 2), tc::kmajor_desc(tLl, 0, kD / 2),
+                           tc::kmajor_desc(tRh, 0, kD / 2), tc::kmajor_desc(tRl, 0, kD / 2),
+                           tc::idesc_bf16(128, kApN), kD / 2 / 16, half != 0);
+                tc::mma_commit(bars + 1);
             }
-            good &= mbar_wait_bounded(bar, (uint32_t)(R & 1), kTcWaitLimit);  // the tiles are reused
-            tc::fence_after_sync();
         }
+        good &= mbar_wait_bounded(bars + 1, 1u, kTcWaitLimit);  // second completion: half 1
     } else {
         // 4. (warps 8..15) Q o exp(G), (K o exp(G_last - G))^T and exp(G_last) to the chunk block
         //    (G is constant past the chunk, so row 63 holds G_last)
@@ -716,21 +754,23 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
     tc::fence_after_sync();
 
-    // 5. warps 0, 4, 8, 12 read block R = warp / 4 back: A (beta and the strict mask applied) to
-    //    the FP32 matrix M, P (inclusive mask) straight to the chunk block. The other warps build
-    //    the solve's B operand: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the
+    // 5. warps 0..7 read A and P back: A (beta and the strict mask applied) to the FP32 matrix
+    //    M, P (inclusive mask) straight to the chunk block. Warps 8..15 build the solve operands: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the
     //    64 chunk rows, hi parts in the q^ array (free now), lo parts in the region.
     float *Mm = reinterpret_cast<float *>(Y + kPtM);
     unsigned char *tBh = reinterpret_cast<unsigned char *>(Yq), *tBl = Y + kPtBl, *tT = Y + kPtT;
-    if ((warp & 3) == 0) {
-        const int R = warp >> 2;
+    if (warp < 8) {
+        // lane quarter qd holds left rows 32 qd .. +31 (k rows for qd < 2, q rows after);
+        // this warp reads block R's segment, used by lanes 16 half .. +15
+        const int qd = warp & 3, half = warp >> 2, R = 2 * (qd & 1) + half, oR = 8 * R * (R + 1);
         uint32_t a0[32], a1[32];
-        tc::tmem_ld32_nowait(tb + 64 * R, a0);
-        tc::tmem_ld32_nowait(tb + 64 * R + 32, a1);
+        const uint32_t ta = tb + ((uint32_t)(32 * qd) << 16) + oR;
+        tc::tmem_ld32_nowait(ta, a0);
+        tc::tmem_ld32_nowait(ta + 32, a1);
         tc::tmem_wait_ld();
-        // columns >= 16 (R + 1) were not written by block R's MMA; the masks drop them
-        if (lane < kBlk) {
-            const int r = kBlk * R + lane;
+        // columns past the segment belong to other blocks; the masks (i < r, i <= r) drop them
+        if ((lane >> 4) == half && qd < 2) {
+            const int r = 32 * qd + lane;
             const float bt = sbeta[r];
 #pragma unroll
             for (int i4 = 0; i4 < kC / 4; ++i4) {
@@ -743,8 +783,8 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 }
                 reinterpret_cast<float4 *>(Mm + r * kMS)[i4] = make_float4(o[0], o[1], o[2], o[3]);
             }
-        } else {
-            const int r = kBlk * R + lane - kBlk;
+        } else if ((lane >> 4) == half) {
+            const int r = 32 * (qd - 2) + lane;
 #pragma unroll
             for (int g8 = 0; g8 < kC / 8; ++g8) {
                 float o[8];
@@ -758,8 +798,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             }
         }
     } else {
-        const int bt = (warp - 1 - (warp >> 2)) * 32 + lane;  // 0..383 over the 12 other warps
-        for (int u = bt; u < 256 * (kC / 8); u += 384) {
+        for (int u = tid - 256; u < 256 * (kC / 8); u += 256) {
             const int nn = u & 255, i0 = 8 * (u >> 8);
             float o[8];
             if (nn < kD) {
@@ -777,35 +816,79 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
     }
     __syncthreads();
-    // 6. T = (I + A)^-1, column j by thread j (warps 0, 1): forward substitution on e_j. Once
-    //    both warps have read A, column j overwrites M as T's column (M[r][j] = T[r][j]).
+    // 6. T = (I + A)^-1 into Tf (the v array; rows of pitch kMS), blocked by 16:
+    //    diagonal blocks T_RR = (I + A_RR)^-1 by forward substitution (threads 0..63, one column
+    //    each) while the other threads clear the blocks above the diagonal; then for block rows
+    //    R = 1..3, Y_S = sum_{K=S}^{R-1} A_RK T_KS and T_RS = -T_RR Y_S for S < R.
+    float *Tf = Yv, *Ys = GL;  // Ys: [3][16][16] scratch
     if (tid < kC) {
-        const int j = tid;
-        float X[kC];
+        const int R = tid >> 4, j = tid & (kBlk - 1), nR = kBlk * R;
+        float x[kBlk];
 #pragma unroll
-        for (int r = 0; r < kC; ++r) {
-            float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+        for (int r = 0; r < kBlk; ++r) {
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int i = 0; i + 4 <= r; i += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + r * kMS + i);
-                x0 = fmaf(-a4.x, X[i], x0);
-                x1 = fmaf(-a4.y, X[i + 1], x1);
-                x2 = fmaf(-a4.z, X[i + 2], x2);
-                x3 = fmaf(-a4.w, X[i + 3], x3);
+            for (int i = 0; i < r; ++i) {
+                if (i & 1) s1 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s1);
+                else s0 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s0);
             }
-#pragma unroll
-            for (int i = r & ~3; i < r; ++i) x0 = fmaf(-Mm[r * kMS + i], X[i], x0);
-            X[r] = r == j ? 1.f : (r < j ? 0.f : (x0 + x1) + (x2 + x3));
+            x[r] = r == j ? 1.f : (r < j ? 0.f : s0 + s1);
+            Tf[(nR + r) * kMS + nR + j] = x[r];
         }
-        named_bar_sync(2, kC);
-#pragma unroll
-        for (int r = 0; r < kC; ++r) Mm[r * kMS + j] = X[r];
+    } else {
+        for (int u = tid - kC; u < kC * kC; u += 512 - kC) {
+            const int r = u >> 6, c = u & (kC - 1);
+            if (c >= kBlk * (r / kBlk + 1)) Tf[r * kMS + c] = 0.f;
+        }
     }
     __syncthreads();
+    for (int R = 1; R < kC / kBlk; ++R) {
+        const int nR = kBlk * R;
+        // one 1 x 4 strip (S, a, b0..b0+3) per thread (at most 192 strips)
+        const int S = tid >> 6, a = (tid >> 2) & (kBlk - 1), b0 = 4 * (tid & 3);
+        if (tid < R * 64) {
+            float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+            for (int K = S; K < R; ++K) {
+                const float *Ar = Mm + (nR + a) * kMS + kBlk * K;
+                const float *Tc = Tf + (kBlk * K) * kMS + kBlk * S + b0;
+#pragma unroll
+                for (int kk = 0; kk < kBlk; kk += 2) {
+                    const float a0 = Ar[kk], a1 = Ar[kk + 1];
+                    const float4 t0 = *reinterpret_cast<const float4 *>(Tc + kk * kMS);
+                    const float4 t1 = *reinterpret_cast<const float4 *>(Tc + (kk + 1) * kMS);
+                    s0.x = fmaf(a0, t0.x, s0.x); s0.y = fmaf(a0, t0.y, s0.y);
+                    s0.z = fmaf(a0, t0.z, s0.z); s0.w = fmaf(a0, t0.w, s0.w);
+                    s1.x = fmaf(a1, t1.x, s1.x); s1.y = fmaf(a1, t1.y, s1.y);
+                    s1.z = fmaf(a1, t1.z, s1.z); s1.w = fmaf(a1, t1.w, s1.w);
+                }
+            }
+            *reinterpret_cast<float4 *>(Ys + S * kBlk * kBlk + a * kBlk + b0) =
+                make_float4(s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w);
+        }
+        __syncthreads();
+        if (tid < R * 64) {
+            const float *Tr = Tf + (nR + a) * kMS + nR;
+            const float *Yc = Ys + S * kBlk * kBlk + b0;
+            float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+#pragma unroll
+            for (int kk = 0; kk < kBlk; kk += 2) {
+                const float a0 = Tr[kk], a1 = Tr[kk + 1];
+                const float4 y0 = *reinterpret_cast<const float4 *>(Yc + kk * kBlk);
+                const float4 y1 = *reinterpret_cast<const float4 *>(Yc + (kk + 1) * kBlk);
+                s0.x = fmaf(a0, y0.x, s0.x); s0.y = fmaf(a0, y0.y, s0.y);
+                s0.z = fmaf(a0, y0.z, s0.z); s0.w = fmaf(a0, y0.w, s0.w);
+                s1.x = fmaf(a1, y1.x, s1.x); s1.y = fmaf(a1, y1.y, s1.y);
+                s1.z = fmaf(a1, y1.z, s1.z); s1.w = fmaf(a1, y1.w, s1.w);
+            }
+            *reinterpret_cast<float4 *>(Tf + (nR + a) * kMS + kBlk * S + b0) =
+                make_float4(-(s0.x + s1.x), -(s0.y + s1.y), -(s0.z + s1.z), -(s0.w + s1.w));
+        }
+        __syncthreads();
+    }
     {   // T -> BF16 hi (tile rows 0..63) and lo (rows 64..127), one 8-column group per thread
         const int r = (tid & 7) | ((tid >> 6) << 3), c0 = 8 * ((tid >> 3) & 7);
         float tv[8];
-        ld8f(Mm + r * kMS + c0, tv);
+        ld8f(Tf + r * kMS + c0, tv);
         uint4 hi, lo;
         split8(tv, hi, lo);
         st16(tT + tc::kmajor_off(r, c0, kC), hi);
@@ -815,54 +898,40 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    // 7. [W | U'] (rows r, columns: 128 channels of W, then 128 of U') in TMEM columns 256..511
+    // 7. W (rows r = lanes 0..63, 128 channel columns at TMEM 256..383) = T B_K^T, and
+    //    U'^T (rows v = lanes 0..127, 64 row columns at TMEM 384..447) = B_V T^T
     if (tid == 0) {
-        constexpr uint32_t id = tc::idesc_bf16(128, 256);
-        const uint32_t d = tb + 256;
-#pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk)
-            tc::mma_bf16(d, tc::kmajor_desc(tT, kk, kC), tc::kmajor_desc(tBh, kk, kC), id, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk)  // lo T rows (tile rows 64..127) x hi B
-            tc::mma_bf16(d, tc::kmajor_desc(tT + kC * 16 * kC / 8, kk, kC), tc::kmajor_desc(tBh, kk, kC), id, 1);
-#pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk)
-            tc::mma_bf16(d, tc::kmajor_desc(tT, kk, kC), tc::kmajor_desc(tBl, kk, kC), id, 1);
-        tc::mma_commit(bar);
+        const uint64_t dT = tc::kmajor_desc(tT, 0, kC), dTlo = dT + ((kC / 8) * kC * 16 >> 4);
+        const uint64_t dBh = tc::kmajor_desc(tBh, 0, kC), dBl = tc::kmajor_desc(tBl, 0, kC);
+        const uint64_t vOff = (uint64_t)((kD / 8) * kC * 16 >> 4);  // B rows 128.. = (beta V)^T
+        mma_split3(tb + 256, dT, dTlo, dBh, dBl, tc::idesc_bf16(128, kD), kC / 16, false);
+        mma_split3(tb + 384, dBh + vOff, dBl + vOff, dT, dTlo, tc::idesc_bf16(128, kC), kC / 16, false);
+        tc::mma_commit(bars + 3);
     }
-    good = mbar_wait_bounded(bar, 0u, kTcWaitLimit);  // fifth completion of the barrier
+    good = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bars + 3, 0u, kTcWaitLimit));  // warp-uniform
     tc::fence_after_sync();
-    // 8. warps on lane quarters 0 and 1 (rows 0..63) write W (BF16 tile) and U' (FP32 rows)
-    if ((warp & 3) < 2 && good) {
-        const int qd = warp & 3, part = warp >> 2;  // part 0, 1: W columns; 2, 3: U' columns
-        const int r = 32 * qd + lane;
-        uint32_t c0v[32], c1v[32];
-        const uint32_t ta = tb + ((uint32_t)(32 * qd) << 16) + 256 + 64 * part;
-        tc::tmem_ld32_nowait(ta, c0v);
-        tc::tmem_ld32_nowait(ta + 32, c1v);
-        tc::tmem_wait_ld();
-        if (part < 2) {
+    // 8. W: warps on lane quarters 0 and 1 (rows 0..63), 32 channels each, as BF16 16-byte
+    //    chunks; U': every warp, 16 rows r of its 32 lanes v, coalesced FP32 stores
+    if (good) {
+        const int qd = warp & 3, part = warp >> 2;
+        if (qd < 2) {
+            const int r = 32 * qd + lane;
+            uint32_t wv[32];
+            tc::tmem_ld32_nowait(tb + ((uint32_t)(32 * qd) << 16) + 256 + 32 * part, wv);
+            tc::tmem_wait_ld();
 #pragma unroll
-            for (int g8 = 0; g8 < 8; ++g8) {
+            for (int g8 = 0; g8 < 4; ++g8) {
                 float o[8];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const int cc = 8 * g8 + t;
-                    o[t] = __uint_as_float(cc < 32 ? c0v[cc] : c1v[cc - 32]);
-                }
-                st16(blk + kOffW + tc::kmajor_off(r, 64 * part + 8 * g8, kD), pack8_bf16(o));
-            }
-        } else {
-            float4 *dst = reinterpret_cast<float4 *>(blk + kOffUp) + (r * kD + 64 * (part - 2)) / 4;
-#pragma unroll
-            for (int i4 = 0; i4 < 16; ++i4) {
-                const int cc = 4 * i4;
-                dst[i4] = make_float4(__uint_as_float(cc < 32 ? c0v[cc] : c1v[cc - 32]),
-                                      __uint_as_float(cc + 1 < 32 ? c0v[cc + 1] : c1v[cc + 1 - 32]),
-                                      __uint_as_float(cc + 2 < 32 ? c0v[cc + 2] : c1v[cc + 2 - 32]),
-                                      __uint_as_float(cc + 3 < 32 ? c0v[cc + 3] : c1v[cc + 3 - 32]));
+                for (int t = 0; t < 8; ++t) o[t] = __uint_as_float(wv[8 * g8 + t]);
+                st16(blk + kOffW + tc::kmajor_off(r, 32 * part + 8 * g8, kD), pack8_bf16(o));
             }
         }
+        float uv[16];
+        tc::tmem_ld16(tb + ((uint32_t)(32 * qd) << 16) + 384 + 16 * part, uv);
+        float *Up = reinterpret_cast<float *>(blk + kOffUp) + 32 * qd + lane;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) Up[(16 * part + t) * kD] = uv[t];
     }
     tc::fence_before_sync();
     if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
@@ -1310,6 +1379,31 @@ epilogue_kernel(const float *__restrict__ obuf, const float *__restrict__ norm_w
     IO<T>::st(op + 3, sigmoidf_(IO<T>::ld(gp + 3)) * w.w * (o.w * rinv));
 }
 
+// Tensor map of a packed [rows][D] BF16 input for 2-D box copies of box_rows rows x 128
+// channels (one head). The encoder comes from the driver through the runtime, so the
+// library does not link the driver library itself.
+cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t D, int box_rows)
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            fn = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <typename T>
 cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32_t *slots,
                          const int32_t *cu, int N, int64_t total_T, int64_t total_chunks,
@@ -1335,12 +1429,21 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
             int sms = 0;
             e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, st.device);
             if (e != cudaSuccess) return e;
+            // boxes of 67 rows (3 history rows + a chunk); never taller than the tensor
+            const int box_rows = (int)(total_T < kC + 3 ? total_T : kC + 3);
+            const int64_t Dm = (int64_t)H * kD;
+            CUtensorMap tmq, tmk, tmv, tmz;
+            if ((e = encode_rows_map(&tmq, q, total_T, Dm, box_rows)) != cudaSuccess ||
+                (e = encode_rows_map(&tmk, k, total_T, Dm, box_rows)) != cudaSuccess ||
+                (e = encode_rows_map(&tmv, v, total_T, Dm, box_rows)) != cudaSuccess ||
+                (e = encode_rows_map(&tmz, z, total_T, Dm, box_rows)) != cudaSuccess)
+                return e;
             e = cudaFuncSetAttribute(prep_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepTcSmem);
             if (e != cudaSuccess) return e;
             prep_tc_kernel<T><<<(unsigned)(total_chunks * H), 512, kPrepTcSmem, stream>>>(
                 p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
                 (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, chunks, st.err,
-                c.gate_lower_bound, c.l2_eps, c.q_scale, sms);
+                c.gate_lower_bound, c.l2_eps, c.q_scale, sms, box_rows, tmq, tmk, tmv, tmz);
         } else {
             const int prep_smem = kPrepSmemFloats * (int)sizeof(float);
             e = cudaFuncSetAttribute(prep_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);

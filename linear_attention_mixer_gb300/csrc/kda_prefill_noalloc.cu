@@ -75,6 +75,8 @@ extern "C" kda_status kda_prefill_noalloc(const kda_config_t *cfg, const kda_lay
     const int64_t total_T = cu_seqlens_host[N];
     if (total_T > 0 && (!q || !k || !v || !z || !b || !g || !out))
         return kda::record_error(KDA_ERR_INVALID, "a tensor pointer is NULL");
+    if (total_T > 0 && !kda::io_aligned(q, k, v, z, g, out))
+        return kda::record_error(KDA_ERR_INVALID, "q, k, v, z, g or out is not 16-byte aligned");
     const size_t need = kda::prefill_workspace_bytes(*cfg, total_chunks, total_T, N);
     if (need > KDA_NOALLOC_WORKSPACE_BYTES - kErrRegion) {
         snprintf(msg, sizeof(msg),

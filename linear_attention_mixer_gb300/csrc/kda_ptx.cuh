@@ -89,6 +89,26 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// 2-D tiled tensor copy global -> shared (box of the tensor map at element coordinates
+// (x inner, y outer)) completing on an mbarrier. x * element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// L2 prefetch of one box of a tensor map.
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes % 16 == 0); no completion.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
 {
@@ -107,6 +127,18 @@ __device__ __forceinline__ unsigned short ld_nc_u16(const void *p)
     unsigned short v;
     asm volatile("ld.global.nc.b16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
+}
+
+// 1/x for x in [1, 2^126] without the special-function unit: Newton-Raphson iteration
+// y <- y + y (1 - x y), whose relative error squares each step, from the seed obtained by
+// negating the exponent in the IEEE-754 bit pattern (2^-e (2 - m) / 2 for x = 2^e (1 + m),
+// at most 12.5% high). Three steps reach FP32 rounding (0.125^8 < 2^-24).
+__device__ __forceinline__ float rcp_newton(float x)
+{
+    float y = __uint_as_float(0x7F000000u - __float_as_uint(x));
+#pragma unroll
+    for (int i = 0; i < 3; ++i) y = fmaf(y, fmaf(-x, y, 1.0f), y);
+    return y;
 }
 
 // Hardware tanh approximation (max relative error about 2^-11).

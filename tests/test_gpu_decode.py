@@ -171,6 +171,12 @@ def test_decode_argument_errors():
         rc = K.lib().kda_decode_token(ctypes.byref(other), ctypes.byref(p), st, ctypes.c_void_p(slots.data_ptr()), 1,
                                       *ptrs, None)
         assert rc == K.KDA_ERR_INVALID and "config" in K.kda_last_error()
+        # a tensor pointer that is not 16-byte aligned is rejected before anything is enqueued
+        qbad = torch.empty(H * d + 4, device="cuda")[1:H * d + 1].view(1, H * d)
+        bad = [ctypes.c_void_p(x.data_ptr()) for x in (qbad, t["k"], t["v"], t["z"], t["b"], t["g"], out)]
+        rc = K.lib().kda_decode_token(ctypes.byref(cfg), ctypes.byref(p), st, ctypes.c_void_p(slots.data_ptr()), 1,
+                                      *bad, None)
+        assert rc == K.KDA_ERR_INVALID and "aligned" in K.kda_last_error()
         # the binding refuses tensors of the wrong dtype before calling in
         with pytest.raises(TypeError):
             K.kda_decode_token(other, p, st, slots, t["q"], t["k"], t["v"], t["z"], t["b"], t["g"], out)
