@@ -441,8 +441,7 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 //  * the solve is explicit: T = (I + A)^-1 by blocked inversion (16 x 16 diagonal blocks by
 //    forward substitution, then one block row at a time), then W = T Diag(beta) (K o exp(G))
 //    and U'^T = (Diag(beta) V)^T T^T on the tensor core, again split hi/lo;
-//  * warps 8..15 write Q o exp(G), (K o exp(G_last - G))^T and exp(G_last) while warps 0..7
-//    build the A/P tiles, so both run at once.
+//  * Q o exp(G), (K o exp(G_last - G))^T and exp(G_last) are written while the A/P MMAs run.
 // Shared memory: FP32 [64][132] arrays (rows padded against bank conflicts) for q^, k^, v and
 // G, then one reused region (raw inputs -> A/P tiles -> B_lo, T tile, A matrix); after the A/P
 // phase the q^ array holds B_hi, and after the B build the v and G arrays hold T and scratch.
@@ -601,10 +600,10 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
 
     // 1. conv + SiLU (sliding window in registers) for stream px < 3, 2. the gates for px == 3;
     //    thread (channel pc, stream px) walks all 64 rows, 32 at a time so that 32 independent
-    //    exponentials are in flight; the sigmoids' reciprocals run on the FMA pipe. Exponents
-    //    are capped at 80 (the sigmoid is then below 2e-35 and the SiLU output tiny either way).
+    //    exponentials are in flight. Exponents are capped at 80 (the sigmoid is then below 2e-35
+    //    and the SiLU output tiny either way).
     if (px < 3) {
-        float *dst = px == 0 ? Yq : (px == 1 ? Yk : Yv);
+        float *dst = Yq + px * (kC * kYS);  // Yq, Yk, Yv are consecutive: the stores stay shared
         const T *col = raw + (size_t)px * kRows * kD + pc;
         float h0 = IO<T>::ld(col), h1 = IO<T>::ld(col + kD), h2 = IO<T>::ld(col + 2 * kD);
 #pragma unroll 1
@@ -618,7 +617,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             }
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
-                const float sg = rcp_newton(1.0f + __expf(fminf(-cv[u], 80.f)));
+                const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-cv[u], 80.f)));
                 dst[(r0 + u) * kYS + pc] = r0 + u < n ? cv[u] * sg : 0.f;
             }
         }
@@ -631,7 +630,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             for (int u = 0; u < 32; ++u) zz[u] = IO<T>::ld(col + (r0 + u) * kD);
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
-                const float sg = rcp_newton(1.0f + __expf(fminf(-p_eA * (zz[u] + p_dt), 80.f)));
+                const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[u] + p_dt), 80.f)));
                 GL[(r0 + u) * kYS + pc] = r0 + u < n ? gmin * sg : 0.f;  // gk; 0 (no decay) past the chunk
             }
         }
@@ -661,19 +660,24 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     __syncthreads();
 
     unsigned char *blk = chunks + (size_t)blockIdx.x * kTcChunkBytes;
-    if (warp < 8) {
-        // 3. A and P on the tensor core: the four 16-row blocks share one accumulator of 160
-        //    TMEM columns (lane = left row, column = right row; only each block's own segment
-        //    is used), built and multiplied one half of the channels at a time.
-        unsigned char *tLh = Y + kApLh, *tLl = Y + kApLl, *tRh = Y + kApRh, *tRl = Y + kApRl;
-        for (int half = 0; half < 2; ++half) {
-            const int c_h = half * (kD / 2);
-            if (half) {
-                good &= mbar_wait_bounded(bars + 1, 0u, kTcWaitLimit);  // half 0 has read the tiles
-                tc::fence_after_sync();
-            }
-            // left rows r (k) and 64 + r (q): factor exp(G_r - G_n), n = 16 (r / 16)
-            for (int u = tid; u < kC * 8; u += 256) {
+    // 3. A and P on the tensor core: the four 16-row blocks share one accumulator of 160 TMEM
+    //    columns (lane = left row, column = right row; only each block's own segment is used),
+    //    built and multiplied one half of the channels at a time by all 16 warps. While the
+    //    MMAs of half 0 run, the CTA writes Q o exp(G) to the chunk block; while those of half 1
+    //    run, (K o exp(G_last - G))^T and exp(G_last) (G is constant past the chunk, so row 63
+    //    holds G_last).
+    unsigned char *tLh = Y + kApLh, *tLl = Y + kApLl, *tRh = Y + kApRh, *tRl = Y + kApRl;
+    for (int half = 0; half < 2; ++half) {
+        const int c_h = half * (kD / 2);
+        if (half) {
+            good &= mbar_wait_bounded(bars + 1, 0u, kTcWaitLimit);  // half 0 has read the tiles
+            tc::fence_after_sync();
+        }
+        // items 0..511: left rows r (k) and 64 + r (q), factor exp(G_r - G_n), n = 16 (r / 16);
+        // items 512..1791: right rows, segment R, row i < 16 (R + 1): k_i o exp(G_nR - G_i)
+        // (<= 1 for i <= nR, <= e^75 on the diagonal block)
+        for (int u = tid; u < kC * 8 + kApN * 8; u += 512) {
+            if (u < kC * 8) {
                 const int r = (u & 7) | ((u >> 6) << 3), cl = 8 * ((u >> 3) & 7), c0 = c_h + cl;
                 const int nR = r & ~(kBlk - 1);
                 float kv[8], qv[8], gr[8], gn[8], kl[8], ql[8];
@@ -683,7 +687,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 ld8f(GL + nR * kYS + c0, gn);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float f = __expf(gr[j] - gn[j]);
+                    const float f = exp_ftz(gr[j] - gn[j]);
                     kl[j] = kv[j] * f;
                     ql[j] = qv[j] * f;
                 }
@@ -694,11 +698,9 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 split8(ql, hi, lo);
                 st16(tLh + tc::kmajor_off(kC + r, cl, kD / 2), hi);
                 st16(tLl + tc::kmajor_off(kC + r, cl, kD / 2), lo);
-            }
-            // right rows: segment R, row i < 16 (R + 1): k_i o exp(G_nR - G_i) (<= 1 for i <= nR,
-            // <= e^75 on the diagonal block)
-            for (int u = tid; u < kApN * 8; u += 256) {
-                const int row = (u & 7) | ((u >> 6) << 3), cl = 8 * ((u >> 3) & 7), c0 = c_h + cl;
+            } else {
+                const int w2 = u - kC * 8;
+                const int row = (w2 & 7) | ((w2 >> 6) << 3), cl = 8 * ((w2 >> 3) & 7), c0 = c_h + cl;
                 const int R = row < 16 ? 0 : (row < 48 ? 1 : (row < 96 ? 2 : 3));
                 const int i = row - 8 * R * (R + 1), nR = kBlk * R;
                 float kv[8], gi[8], gn[8], kx[8];
@@ -706,50 +708,49 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 ld8f(GL + i * kYS + c0, gi);
                 ld8f(GL + nR * kYS + c0, gn);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) kx[j] = kv[j] * __expf(gn[j] - gi[j]);
+                for (int j = 0; j < 8; ++j) kx[j] = kv[j] * exp_ftz(gn[j] - gi[j]);
                 uint4 hi, lo;
                 split8(kx, hi, lo);
                 st16(tRh + tc::kmajor_off(row, cl, kD / 2), hi);
                 st16(tRl + tc::kmajor_off(row, cl, kD / 2), lo);
             }
-            tc::fence_smem_to_async();
-            tc::fence_before_sync();
-            named_bar_sync(1, 256);
-            tc::fence_after_sync();
-            if (tid == 0) {
-                mma_split3(tb, tc::kmajor_desc(tLh, 0, kD / 2), tc::kmajor_desc(tLl, 0, kD / 2),
-                           tc::kmajor_desc(tRh, 0, kD / 2), tc::kmajor_desc(tRl, 0, kD / 2),
-                           tc::idesc_bf16(128, kApN), kD / 2 / 16, half != 0);
-                tc::mma_commit(bars + 1);
-            }
         }
-        good &= mbar_wait_bounded(bars + 1, 1u, kTcWaitLimit);  // second completion: half 1
-    } else {
-        // 4. (warps 8..15) Q o exp(G), (K o exp(G_last - G))^T and exp(G_last) to the chunk block
-        //    (G is constant past the chunk, so row 63 holds G_last)
-        const int t2 = tid - 256;
-        for (int u = t2; u < kC * (kD / 8); u += 256) {
-            const int r = (u & 7) | ((u >> 7) << 3), c0 = 8 * ((u >> 3) & 15);
-            float qv[8], gr[8], o[8];
-            ld8f(Yq + r * kYS + c0, qv);
-            ld8f(GL + r * kYS + c0, gr);
+        tc::fence_smem_to_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (tid == 0) {
+            mma_split3(tb, tc::kmajor_desc(tLh, 0, kD / 2), tc::kmajor_desc(tLl, 0, kD / 2),
+                       tc::kmajor_desc(tRh, 0, kD / 2), tc::kmajor_desc(tRl, 0, kD / 2), tc::idesc_bf16(128, kApN),
+                       kD / 2 / 16, half != 0);
+            tc::mma_commit(bars + 1);
+        }
+        if (half == 0) {
+            for (int u = tid; u < kC * (kD / 8); u += 512) {
+                const int r = (u & 7) | ((u >> 7) << 3), c0 = 8 * ((u >> 3) & 15);
+                float qv[8], gr[8], o[8];
+                ld8f(Yq + r * kYS + c0, qv);
+                ld8f(GL + r * kYS + c0, gr);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = qv[j] * __expf(gr[j]);
-            st16(blk + kOffQG + tc::kmajor_off(r, c0, kD), pack8_bf16(o));
-        }
-        for (int u = t2; u < kD * (kC / 8); u += 256) {  // channel c, rows 8 rb .. +7
-            const int c = u & (kD - 1), rb = u >> 7;
-            const float gl = GL[(kC - 1) * kYS + c];
-            float o[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int r = 8 * rb + j;
-                o[j] = Yk[r * kYS + c] * __expf(gl - GL[r * kYS + c]);
+                for (int j = 0; j < 8; ++j) o[j] = qv[j] * exp_ftz(gr[j]);
+                st16(blk + kOffQG + tc::kmajor_off(r, c0, kD), pack8_bf16(o));
             }
-            st16(blk + kOffKDT + tc::kmajor_off(c, 8 * rb, kC), pack8_bf16(o));
+        } else {
+            for (int u = tid; u < kD * (kC / 8); u += 512) {  // channel c, rows 8 rb .. +7
+                const int c = u & (kD - 1), rb = u >> 7;
+                const float gl = GL[(kC - 1) * kYS + c];
+                float o[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int r = 8 * rb + j;
+                    o[j] = Yk[r * kYS + c] * exp_ftz(gl - GL[r * kYS + c]);
+                }
+                st16(blk + kOffKDT + tc::kmajor_off(c, 8 * rb, kC), pack8_bf16(o));
+            }
+            if (tid < kD) reinterpret_cast<float *>(blk + kOffG)[tid] = exp_ftz(GL[(kC - 1) * kYS + tid]);
         }
-        if (t2 < kD) reinterpret_cast<float *>(blk + kOffG)[t2] = __expf(GL[(kC - 1) * kYS + t2]);
     }
+    good &= mbar_wait_bounded(bars + 1, 1u, kTcWaitLimit);  // second completion: half 1
     tc::fence_before_sync();
     if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
     tc::fence_after_sync();
@@ -804,7 +805,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             if (nn < kD) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    o[j] = sbeta[i0 + j] * (Yk[(i0 + j) * kYS + nn] * __expf(GL[(i0 + j) * kYS + nn]));
+                    o[j] = sbeta[i0 + j] * (Yk[(i0 + j) * kYS + nn] * exp_ftz(GL[(i0 + j) * kYS + nn]));
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) o[j] = sbeta[i0 + j] * Yv[(i0 + j) * kYS + nn - kD];

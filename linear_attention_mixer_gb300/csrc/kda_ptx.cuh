@@ -129,15 +129,20 @@ __device__ __forceinline__ unsigned short ld_nc_u16(const void *p)
     return v;
 }
 
-// 1/x for x in [1, 2^126] without the special-function unit: Newton-Raphson iteration
-// y <- y + y (1 - x y), whose relative error squares each step, from the seed obtained by
-// negating the exponent in the IEEE-754 bit pattern (2^-e (2 - m) / 2 for x = 2^e (1 + m),
-// at most 12.5% high). Three steps reach FP32 rounding (0.125^8 < 2^-24).
-__device__ __forceinline__ float rcp_newton(float x)
+// exp(x) by the special-function unit's base-2 exponential (about 2 ulp); results below the
+// smallest normal number (x < -87.3) flush to zero.
+__device__ __forceinline__ float exp_ftz(float x)
 {
-    float y = __uint_as_float(0x7F000000u - __float_as_uint(x));
-#pragma unroll
-    for (int i = 0; i < 3; ++i) y = fmaf(y, fmaf(-x, y, 1.0f), y);
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+    return y;
+}
+
+// 1/x by the special-function unit (about 1 ulp); denormal inputs and results flush to zero.
+__device__ __forceinline__ float rcp_ftz(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
