@@ -659,7 +659,9 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     }
     __syncthreads();
 
-    unsigned char *blk = chunks + (size_t)blockIdx.x * kTcChunkBytes;
+    // blocks are head-major (block of chunk c, head h at h * total_chunks + c), so one head's
+    // consecutive chunks are adjacent for the state pass
+    unsigned char *blk = chunks + ((size_t)h * (gridDim.x / (unsigned)H) + chunk) * kTcChunkBytes;
     // 3. A and P on the tensor core: the four 16-row blocks share one accumulator of 160 TMEM
     //    columns (lane = left row, column = right row; only each block's own segment is used),
     //    built and multiplied one half of the channels at a time by all 16 warps. While the
@@ -756,7 +758,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     tc::fence_after_sync();
 
     // 5. warps 0..7 read A and P back: A (beta and the strict mask applied) to the FP32 matrix
-    //    M, P (inclusive mask) straight to the chunk block. Warps 8..15 build the solve operands: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the
+    //    M, P (inclusive mask) straight to the chunk block. Then all warps build the solve operands: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the
     //    64 chunk rows, hi parts in the q^ array (free now), lo parts in the region.
     float *Mm = reinterpret_cast<float *>(Y + kPtM);
     unsigned char *tBh = reinterpret_cast<unsigned char *>(Yq), *tBl = Y + kPtBl, *tT = Y + kPtT;
@@ -798,8 +800,9 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 st16(blk + kOffP + tc::kmajor_off(r, 8 * g8, kC), pack8_bf16(o));
             }
         }
-    } else {
-        for (int u = tid - 256; u < 256 * (kC / 8); u += 256) {
+    }
+    {   // every warp (warps 0..7 after their read-back) builds a share of the B operand
+        for (int u = tid; u < 256 * (kC / 8); u += 512) {
             const int nn = u & 255, i0 = 8 * (u >> 8);
             float o[8];
             if (nn < kD) {
@@ -1095,7 +1098,7 @@ __global__ void __launch_bounds__(256, 1)
 state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__restrict__ err,
                 const int32_t *__restrict__ slots, int H, int max_slots,
                 const ChunkEntry *__restrict__ table, const int32_t *__restrict__ seq_first,
-                const unsigned char *__restrict__ chunks,
+                const unsigned char *__restrict__ chunks, int total_chunks,
                 const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                 const T *__restrict__ g, const float *__restrict__ norm_w, T *__restrict__ out, float rms_eps)
 {
@@ -1137,11 +1140,15 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     const int k0 = 64 * grp;   // this thread's state columns k0 .. k0+63
     const int r0 = 32 * grp;   // this thread's tokens r0 .. r0+31
 
-    auto issue = [&](int stage, int ci) {  // thread 0 only
-        const unsigned char *src = chunks + ((size_t)ci * H + h) * kTcChunkBytes;
+    // thread 0 only: chunk ci's block into a stage, and the two blocks after it into L2 (one
+    // block in flight per SM arrives too slowly from HBM to hide behind a chunk's work)
+    auto issue = [&](int stage, int ci) {
+        const unsigned char *src = chunks + ((size_t)h * total_chunks + ci) * kTcChunkBytes;
         mbar_arrive_expect_tx(&bar[stage], kTcChunkBytes);
         bulk_g2s(sm + stage * kTcStageBytes, src, kTcStageBytes, &bar[stage]);
         bulk_g2s(sgam + stage * kD, src + kOffG, kD * 4, &bar[stage]);
+        for (int a = 1; a <= 2; ++a)
+            if (ci + a < c_last) prefetch_l2_bulk(src + (size_t)a * kTcChunkBytes, kTcChunkBytes);
     };
     constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
     // W (rows 0..63) and QG (rows 64..127) form one N = 128 B operand, P (rows 0..63) and KDT
@@ -1175,6 +1182,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     __syncthreads();
     tc::fence_after_sync();
     bool good = true, aborted = false;
+    bool stage_ok = true, issued2 = false;  // this chunk's copy landed; chunk ci + 2 requested
     if (tid == 0 && c_first < c_last) {
         good &= mbar_wait_bounded(&bar[0], 0, kTcWaitLimit);
         if (good) mma1(sm);
@@ -1198,7 +1206,9 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         for (int r = 0; r < 32; ++r)
             graw[r] = ld_nc_u16(g + (size_t)(e.t0 + min(r0 + r, e.n - 1)) * D + (size_t)h * kD + vi);
 
-        good &= mbar_wait_bounded(&bar[st], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
+        stage_ok = mbar_wait_bounded(&bar[st], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
+        good &= stage_ok;
+        issued2 = false;
         // D3 = Diag(gC) on its columns, while MMA1 runs on D1 / D2
         {
             const float *gam = sgam + st * kD + k0;
@@ -1240,6 +1250,12 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         good &= mbar_wait_bounded(&bar[3], ph2, kTcWaitLimit);
         ph2 ^= 1u;
         tc::fence_after_sync();
+        // the stage is consumed (U' and gC were read before MMA2, which read P and KDT): request
+        // chunk ci + 2 into it now
+        if (tid == 0 && good && ci + 2 < c_last) {
+            issue(st, ci + 2);
+            issued2 = true;
+        }
         // O^T on this thread's tokens, their partial sums of squares over this warp's 32 v
         float o[32];
         {
@@ -1285,9 +1301,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         if (__syncthreads_or(!good)) { aborted = true; break; }
         tc::fence_after_sync();
         if (tid == 0) {
-            // the stage is consumed (both MMA groups done, U' and gC read): request chunk ci + 2,
-            // then start the next chunk's first MMAs before this chunk's epilogue
-            if (ci + 2 < c_last) issue(st, ci + 2);
+            // start the next chunk's first MMAs before this chunk's epilogue
             if (ci + 1 < c_last) {
                 good &= mbar_wait_bounded(&bar[st ^ 1], (uint32_t)(((it + 1) >> 1) & 1), kTcWaitLimit);
                 if (good) mma1(sm + (st ^ 1) * kTcStageBytes);
@@ -1300,7 +1314,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             __nv_bfloat16 y[32];
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
-                const float rinv = rsqrtf(redc[r0 + r] * (1.0f / kD) + rms_eps);
+                const float rinv = rsqrt_ftz(redc[r0 + r] * (1.0f / kD) + rms_eps);
                 const float gv = __bfloat162float(__ushort_as_bfloat16(graw[r]));
                 // sigmoid(g) = (1 + tanh(g/2)) / 2; the hardware tanh's error is below the BF16
                 // rounding of the output it multiplies
@@ -1318,11 +1332,12 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     if (aborted) {
         if (tid == 0) {
             atomicExch(err, KDA_ERR_TIMEOUT);
-            // let this CTA's outstanding copies and MMAs land before its memory goes away
-            for (int j = 0; j < 2; ++j) {
-                const int it2 = it + j;
-                if (c_first + it2 < c_last) mbar_wait_bounded(&bar[it2 & 1], (uint32_t)((it2 >> 1) & 1), kTcWaitLimit);
-            }
+            // let this CTA's outstanding copies and MMAs land before its memory goes away: this
+            // chunk's copy if its wait gave up, the next chunk's, and chunk it + 2's if requested
+            if (!stage_ok) mbar_wait_bounded(&bar[it & 1], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
+            if (c_first + it + 1 < c_last)
+                mbar_wait_bounded(&bar[(it + 1) & 1], (uint32_t)(((it + 1) >> 1) & 1), kTcWaitLimit);
+            if (issued2) mbar_wait_bounded(&bar[it & 1], (uint32_t)(((it + 2) >> 1) & 1), kTcWaitLimit);
             mbar_wait_bounded(&bar[2], ph1, kTcWaitLimit);
             mbar_wait_bounded(&bar[3], ph2, kTcWaitLimit);
         }
@@ -1461,7 +1476,7 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
         e = cudaFuncSetAttribute(state_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateTcSmem);
         if (e != cudaSuccess) return e;
         state_tc_kernel<T><<<dim3(H, N), 256, kStateTcSmem, stream>>>(
-            st.S, (T *)st.tail, st.err, slots, H, st.max_slots, table, seq_first, chunks,
+            st.S, (T *)st.tail, st.err, slots, H, st.max_slots, table, seq_first, chunks, (int)total_chunks,
             (const T *)q, (const T *)k, (const T *)v, (const T *)g, p.norm_w, (T *)out, c.rms_eps);
         return cudaGetLastError();
     } else {

@@ -146,6 +146,14 @@ __device__ __forceinline__ float rcp_ftz(float x)
     return y;
 }
 
+// 1/sqrt(x) by the special-function unit (about 1 ulp); denormals flush to zero.
+__device__ __forceinline__ float rsqrt_ftz(float x)
+{
+    float y;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Hardware tanh approximation (max relative error about 2^-11).
 __device__ __forceinline__ float tanh_approx(float x)
 {
