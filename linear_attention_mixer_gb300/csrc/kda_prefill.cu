@@ -27,6 +27,7 @@
 // prep_kernel, state_kernel and epilogue_kernel.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <string.h>
 
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
@@ -1100,7 +1101,8 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 const ChunkEntry *__restrict__ table, const int32_t *__restrict__ seq_first,
                 const unsigned char *__restrict__ chunks, int total_chunks,
                 const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-                const T *__restrict__ g, const float *__restrict__ norm_w, T *__restrict__ out, float rms_eps)
+                const float *__restrict__ norm_w, T *__restrict__ out, float rms_eps, int box_rows,
+                const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_out)
 {
     extern __shared__ __align__(1024) float smf[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(smf);
@@ -1109,8 +1111,12 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     unsigned char *sUT = sST + 32768;                      // U^T [v][r] BF16, K-major, 16 KB
     float *sgam = reinterpret_cast<float *>(sUT + 16384);  // [2 stages][128] chunk decay
     float *red = sgam + 2 * kD;                            // [2 chunk parities][64 tokens] sums of squares
-    uint64_t *bar = reinterpret_cast<uint64_t *>(red + 4 * kC);  // full[0..1], mma1, mma2 (red uses 2 x 64)
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
+    // barriers: [0..1] W|QG of stage 0/1, [2] mma1, [3] mma2, [4] g rows, [5..6] the rest of stage 0/1
+    uint64_t *bar = reinterpret_cast<uint64_t *>(red + 4 * kC);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 7);
+    // after MMA2 the U^T buffer holds this chunk's gate logits [64 r][128 v] (one TMA box), and
+    // the epilogue overwrites them in place with the output rows
+    __nv_bfloat16 *sGY = reinterpret_cast<__nv_bfloat16 *>(sUT);
 
     const int h = blockIdx.x, seq = blockIdx.y;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
@@ -1127,7 +1133,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
 
     if (w == 0) tc::tmem_alloc(tslot, 256);
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < 7; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
     }
     if (tid < 2 * kC) red[tid] = 0.f;
@@ -1140,15 +1146,17 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     const int k0 = 64 * grp;   // this thread's state columns k0 .. k0+63
     const int r0 = 32 * grp;   // this thread's tokens r0 .. r0+31
 
-    // thread 0 only: chunk ci's block into a stage, and the two blocks after it into L2 (one
-    // block in flight per SM arrives too slowly from HBM to hide behind a chunk's work)
+    // thread 0 only: chunk ci's block into a stage as two copies, W|QG (all that MMA1 reads)
+    // first on bar[stage], then P|KDT|U'|gC on bar[5 + stage]
+    static_assert(kOffW == 0 && kOffQG + kD * kC * 2 == kOffP, "W|QG lead the block");
     auto issue = [&](int stage, int ci) {
         const unsigned char *src = chunks + ((size_t)h * total_chunks + ci) * kTcChunkBytes;
-        mbar_arrive_expect_tx(&bar[stage], kTcChunkBytes);
-        bulk_g2s(sm + stage * kTcStageBytes, src, kTcStageBytes, &bar[stage]);
-        bulk_g2s(sgam + stage * kD, src + kOffG, kD * 4, &bar[stage]);
-        for (int a = 1; a <= 2; ++a)
-            if (ci + a < c_last) prefetch_l2_bulk(src + (size_t)a * kTcChunkBytes, kTcChunkBytes);
+        unsigned char *dst = sm + stage * kTcStageBytes;
+        mbar_arrive_expect_tx(&bar[stage], kOffP);
+        bulk_g2s(dst, src, kOffP, &bar[stage]);
+        mbar_arrive_expect_tx(&bar[5 + stage], kTcChunkBytes - kOffP);
+        bulk_g2s(dst + kOffP, src + kOffP, kTcStageBytes - kOffP, &bar[5 + stage]);
+        bulk_g2s(sgam + stage * kD, src + kOffG, kD * 4, &bar[5 + stage]);
     };
     constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
     // W (rows 0..63) and QG (rows 64..127) form one N = 128 B operand, P (rows 0..63) and KDT
@@ -1175,14 +1183,17 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     }
     tc::tmem_wait_st();
     tc::fence_smem_to_async();
-    if (tid == 0)
+    if (tid == 0) {
         for (int i = 0; i < 2; ++i)
             if (c_first + i < c_last) issue(i, c_first + i);
+        if (c_first < c_last) tma_prefetch_2d(&tm_g, h * kD, table[c_first].t0);
+    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     bool good = true, aborted = false;
     bool stage_ok = true, issued2 = false;  // this chunk's copy landed; chunk ci + 2 requested
+    int gpar = -1;                          // parity of a gate-logit box still in flight, or -1
     if (tid == 0 && c_first < c_last) {
         good &= mbar_wait_bounded(&bar[0], 0, kTcWaitLimit);
         if (good) mma1(sm);
@@ -1196,17 +1207,16 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         const int st = it & 1;
         const unsigned char *stage = sm + st * kTcStageBytes;
         const ChunkEntry e = e_next;  // read one chunk ahead
-        if (ci + 1 < c_last) e_next = table[ci + 1];
+        if (ci + 1 < c_last) {
+            e_next = table[ci + 1];
+            // the next chunk's gate logits into L2 now: its box is fetched a chunk from now and
+            // an HBM round trip would stall the epilogue
+            if (tid == 0) tma_prefetch_2d(&tm_g, h * kD, e_next.t0);
+        }
         float *redc = red + st * kC;
-        // output-gate logits of this thread's tokens, kept as raw bits until the epilogue so the
-        // loads do not block the warp; their latency hides behind the MMAs
         static_assert(sizeof(T) == 2, "the tensor-core path reads BF16 gate logits");
-        unsigned short graw[32];
-#pragma unroll
-        for (int r = 0; r < 32; ++r)
-            graw[r] = ld_nc_u16(g + (size_t)(e.t0 + min(r0 + r, e.n - 1)) * D + (size_t)h * kD + vi);
 
-        stage_ok = mbar_wait_bounded(&bar[st], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
+        stage_ok = mbar_wait_bounded(&bar[5 + st], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
         good &= stage_ok;
         issued2 = false;
         // D3 = Diag(gC) on its columns, while MMA1 runs on D1 / D2
@@ -1225,6 +1235,10 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         }
         good &= mbar_wait_bounded(&bar[2], ph1, kTcWaitLimit);
         ph1 ^= 1u;
+        // the previous chunk's epilogue is done with the U^T buffer (its output box has been
+        // read out by the TMA store)
+        if (tid == 0) bulk_wait_read_all();
+        __syncthreads();
         tc::fence_after_sync();
         // U^T = U'^T - (W S)^T on this thread's tokens, as the BF16 A operand
         {
@@ -1252,6 +1266,13 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         tc::fence_after_sync();
         // the stage is consumed (U' and gC were read before MMA2, which read P and KDT): request
         // chunk ci + 2 into it now
+        // MMA2 has read U^T: the buffer takes this chunk's gate logits (requested first: copies
+        // are served in order and the epilogue needs these sooner than the next block)
+        if (tid == 0 && good) {
+            mbar_arrive_expect_tx(&bar[4], (uint32_t)(box_rows * kD * sizeof(T)));
+            tma_load_2d(sUT, &tm_g, h * kD, e.t0, &bar[4]);
+        }
+        if (good) gpar = it & 1;
         if (tid == 0 && good && ci + 2 < c_last) {
             issue(st, ci + 2);
             issued2 = true;
@@ -1309,23 +1330,37 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         }
         // the other parity's sums were last read in the previous chunk's epilogue: clear them
         if (tid < kC) red[(st ^ 1) * kC + tid] = 0.f;
-        // gated RMSNorm of this thread's 32 tokens: all arithmetic first, then the stores
+        // gated RMSNorm of this thread's 32 tokens: the gate logits from the U^T buffer, the
+        // BF16 results written back over them; a full chunk leaves as one TMA box
+        if (mbar_wait_bounded(&bar[4], (uint32_t)(it & 1), kTcWaitLimit)) gpar = -1;
+        else good = false;
         {
             __nv_bfloat16 y[32];
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
                 const float rinv = rsqrt_ftz(redc[r0 + r] * (1.0f / kD) + rms_eps);
-                const float gv = __bfloat162float(__ushort_as_bfloat16(graw[r]));
+                const float gv = __bfloat162float(sGY[(r0 + r) * kD + vi]);
                 // sigmoid(g) = (1 + tanh(g/2)) / 2; the hardware tanh's error is below the BF16
                 // rounding of the output it multiplies
                 const float sg = fmaf(0.5f, tanh_approx(0.5f * gv), 0.5f);
                 y[r] = __float2bfloat16_rn(sg * nw * (o[r] * rinv));
             }
-            T *obase = out + (size_t)(e.t0 + r0) * D + (size_t)h * kD + vi;
-            const int nv = e.n - r0;  // rows of this thread's half that exist
+            if (e.n == kC) {
 #pragma unroll
-            for (int r = 0; r < 32; ++r)
-                if (r < nv) obase[(size_t)r * D] = y[r];
+                for (int r = 0; r < 32; ++r) sGY[(r0 + r) * kD + vi] = y[r];
+                tc::fence_smem_to_async();
+                __syncthreads();
+                if (tid == 0) {
+                    tma_store_2d(&tm_out, h * kD, e.t0, sGY);
+                    bulk_commit_group();
+                }
+            } else {
+                T *obase = out + (size_t)(e.t0 + r0) * D + (size_t)h * kD + vi;
+                const int nv = e.n - r0;  // rows of this thread's half that exist
+#pragma unroll
+                for (int r = 0; r < 32; ++r)
+                    if (r < nv) obase[(size_t)r * D] = y[r];
+            }
         }
     }
 
@@ -1334,10 +1369,19 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             atomicExch(err, KDA_ERR_TIMEOUT);
             // let this CTA's outstanding copies and MMAs land before its memory goes away: this
             // chunk's copy if its wait gave up, the next chunk's, and chunk it + 2's if requested
-            if (!stage_ok) mbar_wait_bounded(&bar[it & 1], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
-            if (c_first + it + 1 < c_last)
-                mbar_wait_bounded(&bar[(it + 1) & 1], (uint32_t)(((it + 1) >> 1) & 1), kTcWaitLimit);
-            if (issued2) mbar_wait_bounded(&bar[it & 1], (uint32_t)(((it + 2) >> 1) & 1), kTcWaitLimit);
+            // (each chunk's copy completes on two barriers: W|QG and the rest)
+            if (!stage_ok) mbar_wait_bounded(&bar[5 + (it & 1)], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
+            if (c_first + it + 1 < c_last) {
+                const uint32_t p1 = (uint32_t)(((it + 1) >> 1) & 1);
+                mbar_wait_bounded(&bar[(it + 1) & 1], p1, kTcWaitLimit);
+                mbar_wait_bounded(&bar[5 + ((it + 1) & 1)], p1, kTcWaitLimit);
+            }
+            if (issued2) {
+                const uint32_t p2 = (uint32_t)(((it + 2) >> 1) & 1);
+                mbar_wait_bounded(&bar[it & 1], p2, kTcWaitLimit);
+                mbar_wait_bounded(&bar[5 + (it & 1)], p2, kTcWaitLimit);
+            }
+            if (gpar >= 0) mbar_wait_bounded(&bar[4], (uint32_t)gpar, kTcWaitLimit);
             mbar_wait_bounded(&bar[2], ph1, kTcWaitLimit);
             mbar_wait_bounded(&bar[3], ph2, kTcWaitLimit);
         }
@@ -1369,6 +1413,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             }
         }
     }
+    if (tid == 0) bulk_wait_all();  // committed output boxes are written before the CTA exits
     tc::fence_before_sync();
     __syncthreads();
     if (w == 0) tc::tmem_dealloc(tb, 256);
@@ -1475,9 +1520,20 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
     if constexpr (kTC) {
         e = cudaFuncSetAttribute(state_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateTcSmem);
         if (e != cudaSuccess) return e;
+        // gate logits in and output rows out as 64-row boxes (never taller than the tensor)
+        const int box_g = (int)(total_T < kC ? total_T : kC);
+        CUtensorMap tmg, tmo;
+        if (total_T > 0) {
+            if ((e = encode_rows_map(&tmg, g, total_T, (int64_t)H * kD, box_g)) != cudaSuccess ||
+                (e = encode_rows_map(&tmo, out, total_T, (int64_t)H * kD, box_g)) != cudaSuccess)
+                return e;
+        } else {
+            memset(&tmg, 0, sizeof(tmg));
+            memset(&tmo, 0, sizeof(tmo));
+        }
         state_tc_kernel<T><<<dim3(H, N), 256, kStateTcSmem, stream>>>(
             st.S, (T *)st.tail, st.err, slots, H, st.max_slots, table, seq_first, chunks, (int)total_chunks,
-            (const T *)q, (const T *)k, (const T *)v, (const T *)g, p.norm_w, (T *)out, c.rms_eps);
+            (const T *)q, (const T *)k, (const T *)v, p.norm_w, (T *)out, c.rms_eps, box_g, tmg, tmo);
         return cudaGetLastError();
     } else {
         const int state_smem = kStateSmemFloats * (int)sizeof(float);

@@ -100,6 +100,22 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, 
         : "memory");
 }
 
+// 2-D tiled tensor copy shared -> global of one box at element coordinates (x, y), tracked
+// by the issuing thread's bulk group (commit with bulk_commit_group). x * element size must be
+// a multiple of 16 and (x, y) must not be negative.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, int x, int y, const void *src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the thread's committed bulk stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// the thread's committed bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // L2 prefetch of one box of a tensor map.
 __device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int x, int y)
 {
