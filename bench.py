@@ -140,8 +140,9 @@ def _barrier(ws):
 
 # ------------------------------------------------------------------ reference arm
 
-def _oracle_decode_sample(n_seq: int, steps: int, seed: int = 2):
-    """Time the FP64 oracle on n_seq sequences x 96 heads for `steps` decode tokens."""
+def _oracle_decode_sample(n_seq: int, steps: int, seed: int = 2, nthreads: int = 0):
+    """Time the FP64 oracle on n_seq sequences x 96 heads for `steps` decode tokens
+    (nthreads 0: every host core)."""
     import numpy as np
 
     import kda_inputs as KI
@@ -153,7 +154,7 @@ def _oracle_decode_sample(n_seq: int, steps: int, seed: int = 2):
     tok = KI.make_tokens(n_seq * steps, H, DH, seed, bf16=True)
     oc = O.OracleCfg(H=H, d=DH)
     slots = np.arange(n_seq, dtype=np.int32)
-    nt = O.max_threads()
+    nt = nthreads or O.max_threads()
     times = []
     for s in range(steps):
         rows = slice(s * n_seq, (s + 1) * n_seq)
@@ -163,7 +164,7 @@ def _oracle_decode_sample(n_seq: int, steps: int, seed: int = 2):
     return times, nt
 
 
-def _oracle_prefill_sample(T: int, n_heads: int, seed: int = 3):
+def _oracle_prefill_sample(T: int, n_heads: int, seed: int = 3, nthreads: int = 0):
     import numpy as np
 
     import kda_inputs as KI
@@ -173,7 +174,7 @@ def _oracle_prefill_sample(T: int, n_heads: int, seed: int = 3):
     tok = KI.make_tokens(T, n_heads, DH, seed, bf16=True)
     oc = O.OracleCfg(H=n_heads, d=DH)
     S, tail = O.new_state(oc)
-    nt = O.max_threads()
+    nt = nthreads or O.max_threads()
     t0 = time.perf_counter()
     O.sequence(oc, p, S, tail, tok, nthreads=nt)
     return time.perf_counter() - t0, nt
@@ -186,18 +187,26 @@ def cpu_baseline_decode(target_s: float = 12.0):
     steps = max(1, min(20, int(target_s / max(t1[0], 1e-3))))
     times, nt = _oracle_decode_sample(n_seq, steps)
     tot = sum(times)
+    n1, s1 = 4, 2  # single thread: a smaller sample of the same shape
+    t_one, _ = _oracle_decode_sample(n1, s1, nthreads=1)
     return {"value": n_seq * steps / tot, "unit": "tokens/s", "cores": nt, "kind": "oracle",
             "sample": f"FP64 oracle, {steps} decode steps x {n_seq} sequences x {H} heads x {DH} "
-                      f"(B=256 workload shape), OpenMP over (sequence, head) units"}
+                      f"(B=256 workload shape), OpenMP over (sequence, head) units",
+            "value_1thread": n1 * s1 / sum(t_one),
+            "sample_1thread": f"FP64 oracle on one core, {s1} decode steps x {n1} sequences x {H} heads"}
 
 
 def cpu_baseline_prefill():
-    """Bounded sample: 1024 tokens x 8 heads of the T=8192 prefill, scaled to 96 heads."""
-    T, nh = 1024, 8
+    """Bounded sample: 2048 tokens x 32 heads of the T=8192 prefill, scaled to 96 heads."""
+    T, nh = 2048, 32
     t, nt = _oracle_prefill_sample(T, nh)
+    T1 = 256
+    t1, _ = _oracle_prefill_sample(T1, 1, nthreads=1)
     return {"value": T / (t * H / nh), "unit": "tokens/s", "cores": nt, "kind": "oracle",
             "sample": f"FP64 oracle, sequential per token, {T} tokens x {nh} heads (scaled to {H} heads), "
-                      f"OpenMP over heads"}
+                      f"OpenMP over heads",
+            "value_1thread": T1 / (t1 * H),
+            "sample_1thread": f"FP64 oracle on one core, {T1} tokens x 1 head (scaled to {H} heads)"}
 
 
 def run_reference(args):

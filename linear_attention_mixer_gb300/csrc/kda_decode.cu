@@ -1,11 +1,10 @@
 // kda_decode.cu - fused one-token KDA decode for a batch of sequences.
 //
-// One CTA per (sequence, head). The 64 KB FP32 state of the unit is read once
-// and written once; every other step of the per-head recurrence (kimi_k3.c
-// header comment, "KDA per-head recurrence") is fused around that single pass:
-//   ShortConv4 + SiLU on q,k,v (history shifted in place), L2 norms with the
-//   q scale, the decay gate alpha and beta, the delta-rule update with its
-//   readout, and the gated per-head RMSNorm.
+// Every step of the per-head recurrence (kimi_k3.c header comment, "KDA per-head
+// recurrence") is fused around one read and one write of the unit's 64 KB FP32
+// state: ShortConv4 + SiLU on q,k,v (history shifted in place), L2 norms with the
+// q scale, the decay gate alpha and beta, the delta-rule update with its readout,
+// and the gated per-head RMSNorm.
 //
 // The update is evaluated in the form
 //   S^ = Diag(alpha) S,  p = S^T k,  r = S^T q   (column reductions of S^)
@@ -30,127 +29,8 @@ __device__ __forceinline__ float4 add4(float4 x, float4 y) {
     return make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(256, 2)
-decode_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
-              const float *__restrict__ A_log, const float *__restrict__ norm_w,
-              float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__restrict__ err,
-              const int32_t *__restrict__ slots, int H, int max_slots,
-              const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-              const T *__restrict__ z, const T *__restrict__ bl, const T *__restrict__ g,
-              T *__restrict__ out, float gmin, float l2_eps, float rms_eps, float q_scale)
-{
-    const int unit = blockIdx.x;
-    const int r = unit / H, h = unit - r * H;
-    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
-    const int slot = slots[r];
-    if (slot < 0 || slot >= max_slots) {
-        if (tid == 0) atomicExch(err, kErrBadSlot);
-        return;
-    }
-    const size_t D = (size_t)H * kD;
-    float4 *S4 = reinterpret_cast<float4 *>(S_all + ((size_t)slot * H + h) * kD * kD);
-
-    // 1. Put the whole 64 KB state in flight before the prologue arithmetic.
-    float4 s[16];
-#pragma unroll
-    for (int m = 0; m < 16; ++m) s[m] = ld_stream(S4 + (w + 8 * m) * 32 + l);
-
-    __shared__ float sh_k[kD], sh_q[kD], sh_a[kD], sh_v[kD], sh_gw[kD];
-    __shared__ float4 red[2][8][32];
-    __shared__ float part[3][4];
-
-    // 2. Prologue: thread i < 128 owns channel i of this head.
-    float yq = 0.f, yk = 0.f, yv = 0.f, alpha = 0.f, gw = 0.f;
-    if (tid < kD) {
-        const int i = tid;
-        const size_t c = (size_t)h * kD + i;
-        const size_t row = (size_t)r * D + c;
-        T *tl = tail_all + (size_t)slot * 3 * (kK - 1) * D + c;
-        const T *src[3] = {q, k, v};
-        float y[3];
-#pragma unroll
-        for (int x = 0; x < 3; ++x) {
-            const float4 wt = __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)x * D + c) * kK));
-            const T raw = src[x][row];
-            const T h0 = tl[(x * 3 + 0) * D], h1 = tl[(x * 3 + 1) * D], h2 = tl[(x * 3 + 2) * D];
-            const float cv = fmaf(wt.x, IO<T>::ld(&h0), fmaf(wt.y, IO<T>::ld(&h1),
-                             fmaf(wt.z, IO<T>::ld(&h2), wt.w * IO<T>::ld(&raw))));
-            y[x] = siluf_(cv);
-            // history holds raw inputs, oldest first
-            tl[(x * 3 + 0) * D] = h1;
-            tl[(x * 3 + 1) * D] = h2;
-            tl[(x * 3 + 2) * D] = raw;
-        }
-        yq = y[0]; yk = y[1]; yv = y[2];
-        const float zz = IO<T>::ld(z + row) + __ldg(dt_bias + c);
-        alpha = expf(gmin * sigmoidf_(expf(__ldg(A_log + h)) * zz));
-        gw = sigmoidf_(IO<T>::ld(g + row)) * __ldg(norm_w + i);
-        const float a0 = warp_sum(yq * yq), a1 = warp_sum(yk * yk), a2 = warp_sum(yq * yk);
-        if (l == 0) { part[0][w] = a0; part[1][w] = a1; part[2][w] = a2; }
-    }
-    const float beta = sigmoidf_(IO<T>::ld(bl + (size_t)r * H + h));
-    __syncthreads();
-    const float sqq = part[0][0] + part[0][1] + part[0][2] + part[0][3];
-    const float skk = part[1][0] + part[1][1] + part[1][2] + part[1][3];
-    const float sqk = part[2][0] + part[2][1] + part[2][2] + part[2][3];
-    const float rq = q_scale / sqrtf(sqq + l2_eps);
-    const float rk = 1.0f / sqrtf(skk + l2_eps);
-    const float kq = sqk * rq * rk;  // k^ . q^
-    if (tid < kD) {
-        sh_k[tid] = yk * rk;
-        sh_q[tid] = yq * rq;
-        sh_a[tid] = alpha;
-        sh_v[tid] = yv;
-        sh_gw[tid] = gw;
-    }
-    __syncthreads();
-
-    // 3. Column reductions of Diag(alpha) S against k^ and q^ over this thread's rows.
-    float4 p = f4(0.f), rr = f4(0.f);
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        const int i = w + 8 * m;
-        const float a = sh_a[i];
-        p = fma4(a * sh_k[i], s[m], p);
-        rr = fma4(a * sh_q[i], s[m], rr);
-    }
-    red[0][w][l] = p;
-    red[1][w][l] = rr;
-    __syncthreads();
-    float4 P = red[0][0][l], R = red[1][0][l];
-#pragma unroll
-    for (int ww = 1; ww < 8; ++ww) { P = add4(P, red[0][ww][l]); R = add4(R, red[1][ww][l]); }
-    const float4 vv = reinterpret_cast<const float4 *>(sh_v)[l];
-    const float4 u = make_float4(beta * (vv.x - P.x), beta * (vv.y - P.y), beta * (vv.z - P.z), beta * (vv.w - P.w));
-    const float4 o = fma4(kq, u, R);
-
-    // 4. Write S' = Diag(alpha) S + k^ u^T.
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        const int i = w + 8 * m;
-        const float a = sh_a[i], kk = sh_k[i];
-        const float4 sv = s[m];
-        st_stream(S4 + i * 32 + l, make_float4(fmaf(a, sv.x, kk * u.x), fmaf(a, sv.y, kk * u.y),
-                                               fmaf(a, sv.z, kk * u.z), fmaf(a, sv.w, kk * u.w)));
-    }
-
-    // 5. Gated RMSNorm of o (warp 0 holds all 128 columns).
-    if (w == 0) {
-        const float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
-        const float rinv = 1.0f / sqrtf(ss * (1.0f / kD) + rms_eps);
-        const float4 gw4 = reinterpret_cast<const float4 *>(sh_gw)[l];
-        T *dst = out + (size_t)r * D + (size_t)h * kD + 4 * l;
-        IO<T>::st(dst + 0, gw4.x * (o.x * rinv));
-        IO<T>::st(dst + 1, gw4.y * (o.y * rinv));
-        IO<T>::st(dst + 2, gw4.z * (o.z * rinv));
-        IO<T>::st(dst + 3, gw4.w * (o.w * rinv));
-    }
-}
-
-
 // ---------------------------------------------------------------------------
-// Persistent variant: one CTA per SM walks a contiguous range of units in
+// One CTA per SM walks a contiguous range of units in
 // head-major order (unit = h * B + r, so the per-head conv taps and dt_bias
 // change rarely and stay in shared memory). Each unit's 64 KB state, its
 // q,k,v,z,g rows and its conv history arrive by bulk async copies into a ring

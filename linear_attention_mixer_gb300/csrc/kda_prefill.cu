@@ -93,11 +93,6 @@ __device__ __forceinline__ void store_row_bf16(unsigned char *tile, int row, int
     *reinterpret_cast<uint4 *>(tile + tc::kmajor_off(row, k0 + 8, Kd)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-__device__ __forceinline__ void st_bf16(unsigned char *tile, uint32_t off, float x)
-{
-    *reinterpret_cast<__nv_bfloat16 *>(tile + off) = __float2bfloat16_rn(x);
-}
-
 // ---------------------------------------------------------------- chunk table
 // One thread builds the chunk list. The device copy of cu_seqlens is checked
 // against what the host sized the launch for (N + 1 entries, starting at 0,
@@ -137,8 +132,8 @@ __global__ void chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_
 }
 
 // ---------------------------------------------------------------- prep
-// TC = true writes the BF16 tensor-core block (kTcChunkBytes); false the FP32 block.
-template <typename T, bool TC>
+// FP32 I/O: writes the FP32 chunk block (kChunkFloats per (chunk, head)).
+template <typename T>
 __global__ void __launch_bounds__(256, 1)
 prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
             const float *__restrict__ A_log, const T *__restrict__ tail_all,
@@ -319,108 +314,46 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
         __syncthreads();
     }
 
-    if constexpr (TC) {
-        unsigned char *blk = chunks + (size_t)blockIdx.x * kTcChunkBytes;
-        // operand tiles are built in the (now free) KRT / KL / QL region, P in the A region
-        unsigned char *tW = reinterpret_cast<unsigned char *>(KRT);   // 16 KB
-        unsigned char *tQG = tW + 16384;                              // 16 KB
-        unsigned char *tKDT = reinterpret_cast<unsigned char *>(KL);  // 16 KB (KL + QL)
-        unsigned char *tP = reinterpret_cast<unsigned char *>(Am);    // 8 KB, after the solve
-        float *Up = reinterpret_cast<float *>(blk + kOffUp);
-        // 5. Forward substitution (I + A) X = Diag(beta) B, one column per thread:
-        //    columns 0..127 of B are k o exp(G) (-> W), 128..255 are v (-> U').
-        {
-            const int j = tid;
-            const bool isk = j < kD;
-            const int cj = isk ? j : j - kD;
-            float X[kC];
+    float *out = reinterpret_cast<float *>(chunks) + (size_t)blockIdx.x * kChunkFloats;
+    float *W = out, *Up = W + kC * kD, *QG = Up + kC * kD, *KD = QG + kC * kD, *P = KD + kC * kD,
+          *GC = P + kC * kC;
+    // 5. Forward substitution (I + A) X = Diag(beta) B, one column per thread:
+    //    columns 0..127 of B are k o exp(G), 128..255 are v.
+    {
+        const int j = tid;
+        const bool isk = j < kD;
+        const int cj = isk ? j : j - kD;
+        float X[kC];
 #pragma unroll
-            for (int r = 0; r < kC; ++r) {
-                const float bb = isk ? Yk[r * kD + cj] * expf(G[r * kD + cj]) : Yv[r * kD + cj];
-                // four independent partial sums over i, A read 4 at a time
-                float x0 = sbeta[r] * bb, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+        for (int r = 0; r < kC; ++r) {
+            const float bb = isk ? Yk[r * kD + cj] * expf(G[r * kD + cj]) : Yv[r * kD + cj];
+            // four independent partial sums over i, A read 4 at a time
+            float x0 = sbeta[r] * bb, x1 = 0.f, x2 = 0.f, x3 = 0.f;
 #pragma unroll
-                for (int i = 0; i + 4 <= r; i += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(Am + r * kC + i);
-                    x0 = fmaf(-a4.x, X[i], x0);
-                    x1 = fmaf(-a4.y, X[i + 1], x1);
-                    x2 = fmaf(-a4.z, X[i + 2], x2);
-                    x3 = fmaf(-a4.w, X[i + 3], x3);
-                }
-#pragma unroll
-                for (int i = r & ~3; i < r; ++i) x0 = fmaf(-Am[r * kC + i], X[i], x0);
-                X[r] = (x0 + x1) + (x2 + x3);
+            for (int i = 0; i + 4 <= r; i += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Am + r * kC + i);
+                x0 = fmaf(-a4.x, X[i], x0);
+                x1 = fmaf(-a4.y, X[i + 1], x1);
+                x2 = fmaf(-a4.z, X[i + 2], x2);
+                x3 = fmaf(-a4.w, X[i + 3], x3);
             }
-            if (isk) {
 #pragma unroll
-                for (int r = 0; r < kC; ++r) st_bf16(tW, tc::kmajor_off(r, cj, kD), X[r]);
-            } else {
-#pragma unroll
-                for (int r = 0; r < kC; ++r) Up[r * kD + cj] = X[r];
-            }
+            for (int i = r & ~3; i < r; ++i) x0 = fmaf(-Am[r * kC + i], X[i], x0);
+            X[r] = (x0 + x1) + (x2 + x3);
         }
-        // 6. Q o exp(G) and (K o exp(G_last - G))^T tiles, the chunk decay
-        for (int e2 = tid; e2 < kC * kD; e2 += 256) {
-            const int r = e2 / kD, c = e2 - r * kD;
-            const float g = G[r * kD + c];
-            st_bf16(tQG, tc::kmajor_off(r, c, kD), Yq[e2] * expf(g));
-            st_bf16(tKDT, tc::kmajor_off(c, r, kC), Yk[e2] * expf(G[(n - 1) * kD + c] - g));
-        }
-        if (tid < kD) reinterpret_cast<float *>(blk + kOffG)[tid] = expf(G[(n - 1) * kD + tid]);
-        __syncthreads();  // the solve no longer reads A
-        for (int e2 = tid; e2 < kC * kC; e2 += 256) {
-            const int r = e2 / kC, i = e2 - r * kC;
-            st_bf16(tP, tc::kmajor_off(r, i, kC), Pm[e2]);
-        }
-        __syncthreads();
-        for (int o = tid * 16; o < 32768; o += 256 * 16)  // W and QG
-            *reinterpret_cast<uint4 *>(blk + kOffW + o) = *reinterpret_cast<const uint4 *>(tW + o);
-        for (int o = tid * 16; o < 8192; o += 256 * 16)
-            *reinterpret_cast<uint4 *>(blk + kOffP + o) = *reinterpret_cast<const uint4 *>(tP + o);
-        for (int o = tid * 16; o < 16384; o += 256 * 16)
-            *reinterpret_cast<uint4 *>(blk + kOffKDT + o) = *reinterpret_cast<const uint4 *>(tKDT + o);
-    } else {
-        float *out = reinterpret_cast<float *>(chunks) + (size_t)blockIdx.x * kChunkFloats;
-        float *W = out, *Up = W + kC * kD, *QG = Up + kC * kD, *KD = QG + kC * kD, *P = KD + kC * kD,
-              *GC = P + kC * kC;
-        // 5. Forward substitution (I + A) X = Diag(beta) B, one column per thread:
-        //    columns 0..127 of B are k o exp(G), 128..255 are v.
-        {
-            const int j = tid;
-            const bool isk = j < kD;
-            const int cj = isk ? j : j - kD;
-            float X[kC];
+        float *dstc = isk ? W : Up;
 #pragma unroll
-            for (int r = 0; r < kC; ++r) {
-                const float bb = isk ? Yk[r * kD + cj] * expf(G[r * kD + cj]) : Yv[r * kD + cj];
-                // four independent partial sums over i, A read 4 at a time
-                float x0 = sbeta[r] * bb, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-#pragma unroll
-                for (int i = 0; i + 4 <= r; i += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(Am + r * kC + i);
-                    x0 = fmaf(-a4.x, X[i], x0);
-                    x1 = fmaf(-a4.y, X[i + 1], x1);
-                    x2 = fmaf(-a4.z, X[i + 2], x2);
-                    x3 = fmaf(-a4.w, X[i + 3], x3);
-                }
-#pragma unroll
-                for (int i = r & ~3; i < r; ++i) x0 = fmaf(-Am[r * kC + i], X[i], x0);
-                X[r] = (x0 + x1) + (x2 + x3);
-            }
-            float *dstc = isk ? W : Up;
-#pragma unroll
-            for (int r = 0; r < kC; ++r) dstc[r * kD + cj] = X[r];
-        }
-        // 6. The remaining chunk factors.
-        for (int e2 = tid; e2 < kC * kD; e2 += 256) {
-            const int r = e2 / kD, c = e2 - r * kD;
-            const float g = G[r * kD + c];
-            QG[e2] = Yq[e2] * expf(g);
-            KD[e2] = Yk[e2] * expf(G[(n - 1) * kD + c] - g);
-        }
-        for (int e2 = tid; e2 < kC * kC; e2 += 256) P[e2] = Pm[e2];
-        if (tid < kD) GC[tid] = expf(G[(n - 1) * kD + tid]);
+        for (int r = 0; r < kC; ++r) dstc[r * kD + cj] = X[r];
     }
+    // 6. The remaining chunk factors.
+    for (int e2 = tid; e2 < kC * kD; e2 += 256) {
+        const int r = e2 / kD, c = e2 - r * kD;
+        const float g = G[r * kD + c];
+        QG[e2] = Yq[e2] * expf(g);
+        KD[e2] = Yk[e2] * expf(G[(n - 1) * kD + c] - g);
+    }
+    for (int e2 = tid; e2 < kC * kC; e2 += 256) P[e2] = Pm[e2];
+    if (tid < kD) GC[tid] = expf(G[(n - 1) * kD + tid]);
 }
 
 // ---------------------------------------------------------------- prep on tensor cores
@@ -1507,9 +1440,9 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
                 c.gate_lower_bound, c.l2_eps, c.q_scale, sms, box_rows, tmq, tmk, tmv, tmz);
         } else {
             const int prep_smem = kPrepSmemFloats * (int)sizeof(float);
-            e = cudaFuncSetAttribute(prep_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
+            e = cudaFuncSetAttribute(prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
             if (e != cudaSuccess) return e;
-            prep_kernel<T, false><<<(unsigned)(total_chunks * H), 256, prep_smem, stream>>>(
+            prep_kernel<T><<<(unsigned)(total_chunks * H), 256, prep_smem, stream>>>(
                 p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
                 (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, chunks,
                 c.gate_lower_bound, c.l2_eps, c.q_scale);
