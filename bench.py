@@ -355,8 +355,8 @@ def _time_decode_b1(K, cfg, params, gen, dev, stream):
 
     for i in range(10):
         b1_step(i)
-    b1_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
-    for i in range(50):
+    b1_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(200)]
+    for i in range(200):
         flush.fill_(i & 0xFF)  # evict the 6.3 MB state from L2 between steps
         b1_ev[i][0].record(stream)
         b1_step(i)
