@@ -43,7 +43,7 @@ PRE_FLOP_PER_TOKEN_HEAD = 2 * (3 * DH * DH + 5 * CHUNK * DH)
 PRE_BYTES_PER_TOKEN = (5 * D + H + D) * 2
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch at B=256,
 # from one ncu capture of the decode kernel as it stands; None once that kernel changes.
-DEC_TRAFFIC_B256 = 1_699_761_408 + 1_611_806_976
+DEC_TRAFFIC_B256 = None  # re-measure after a decode kernel change
 
 
 def _peaks():
@@ -368,6 +368,38 @@ def _time_decode_b1(K, cfg, params, gen, dev, stream):
     return b1_us
 
 
+def _time_decode_multi(K, cfg, params, gen, dev, stream, Bd, n, reps=50):
+    """kda_decode_tokens: n tokens for each of Bd sequences per call (one pass over the
+    states). Returns ms per call (median of per-call events; inputs cycle over a ring and
+    the 1.6 GB of state is larger than L2)."""
+    import torch
+    st = K.kda_state_alloc(cfg, Bd)
+    _fill_state_random(K, cfg, st, Bd, gen, dev)
+    ring = [_inputs(Bd * n, gen, dev, torch.bfloat16) for _ in range(4)]
+    slots = torch.arange(Bd, dtype=torch.int32, device=dev)
+    out = torch.empty(Bd * n, D, dtype=torch.bfloat16, device=dev)
+
+    def call(i):
+        x = ring[i % 4]
+        K.kda_decode_tokens(cfg, params, st, slots, n, x["q"], x["k"], x["v"], x["z"], x["b"], x["g"], out, stream)
+
+    for i in range(5):
+        call(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        ev[i][0].record(stream)
+        call(i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    assert K.kda_state_poll_error(st) == 0
+    K.kda_state_free(st)
+    del ring, out
+    torch.cuda.empty_cache()
+    return ms
+
+
 def _time_prefill(K, args, cfg, params, gen, dev, stream):
     import torch
     Tp = args.prefill_tokens
@@ -510,6 +542,17 @@ def run_kda(args):
                                              "(L2 flushed between steps)",
                                  "latency_us": b1_us, "bytes_per_step": DEC_BYTES_PER_UNIT * H,
                                  "achieved_gbs": DEC_BYTES_PER_UNIT * H / (b1_us / 1e6) / 1e9}
+            # speculative-verify style decode: n tokens per sequence per call, one state pass
+            line["decode_multi"] = []
+            for n in (4, 8):
+                mms = _time_decode_multi(K, cfg, params, gen, dev, stream, Bd, n)
+                mbytes = Bd * H * (2 * DH * DH * 4 + n * (5 * DH * 2 + 2 + DH * 2) + 2 * 3 * (KCONV - 1) * DH * 2)
+                line["decode_multi"].append({
+                    "workload": f"kda_decode_tokens, B={Bd} sequences x n={n} tokens per call, 96 heads x 128, "
+                                f"BF16 I/O, FP32 state",
+                    "n": n, "ms_per_call": mms, "tokens_per_s": Bd * n / (mms / 1e3),
+                    "vs_n_single_token_calls": n * line["ms_per_step"] / mms,
+                    "achieved_gbs": mbytes / (mms / 1e3) / 1e9, "bytes_per_call": mbytes})
     if args.only in ("all", "prefill"):
         pre_ms = _time_prefill(K, args, cfg, params, gen, dev, stream)
         pre_flop = PRE_FLOP_PER_TOKEN_HEAD * Tp * H

@@ -180,8 +180,31 @@ kda_status kda_decode_token(const kda_config_t *cfg, const kda_layer_params *par
                             const void *b, const void *g, void *out, void *stream);
 
 /*
+ * n consecutive decode tokens for each of B independent sequences in one call:
+ * the per-head recurrence above applied n times in token order (kimi_k3.c
+ * header, "KDA per-head recurrence"), identical in result to n calls of
+ * kda_decode_token, but each sequence's state is read and written once. For
+ * verifying n speculative draft tokens (kimi_k3.c K3Seq/K3Row multiplexed decode;
+ * the state can only be taken back by restore, so take a kda_state_snapshot of
+ * the rows first and, on a rejected draft, restore it and call again with the
+ * accepted prefix).
+ *   n        1 .. KDA_DECODE_MAX_TOKENS
+ *   slots    device int32 [B], distinct; bad ids as in kda_decode_token
+ *   q,k,v,z,g  device [B][n][H*d] io_dtype (token t of row r at r*n + t)
+ *   b        device [B][n][H] io_dtype
+ *   out      device [B][n][H*d] io_dtype (must not alias an input)
+ * B == 0 is a no-op. Errors: KDA_ERR_INVALID (NULL pointer, B < 0, n out of
+ * range, a row tensor not 16-byte aligned, config mismatch), KDA_ERR_CUDA.
+ */
+#define KDA_DECODE_MAX_TOKENS 8
+kda_status kda_decode_tokens(const kda_config_t *cfg, const kda_layer_params *params, kda_state *st,
+                             const int32_t *slots, int32_t B, int32_t n,
+                             const void *q, const void *k, const void *v, const void *z,
+                             const void *b, const void *g, void *out, void *stream);
+
+/*
  * Prefill N variable-length sequences packed along the token axis
- * (kimi_k3.c: K3_CHUNK "prefill chunk size"; the per-token recurrence above
+ * (kimi_k3.c ENV list, the K3_CHUNK entry; the per-token recurrence above
  * evaluated in chunks of C tokens with the WY/UT rewrite, which is exact in
  * real arithmetic). Each sequence continues from its slot's current state and
  * conv history and leaves its final state and history in the slot; nothing

@@ -304,6 +304,29 @@ kda_status kda_decode_token(const kda_config_t *cfg, const kda_layer_params *par
     return KDA_OK;
 }
 
+kda_status kda_decode_tokens(const kda_config_t *cfg, const kda_layer_params *params, kda_state *h,
+                             const int32_t *slots, int32_t B, int32_t n, const void *q, const void *k,
+                             const void *v, const void *z, const void *b, const void *g, void *out, void *stream)
+{
+    if (!h) return fail(KDA_ERR_INVALID, "state is NULL");
+    State *st = reinterpret_cast<State *>(h);
+    if (!cfg_check(cfg)) return KDA_ERR_INVALID;
+    if (!cfg_same(*cfg, st->cfg)) return fail(KDA_ERR_INVALID, "config differs from the state's config");
+    if (!params_check(params)) return KDA_ERR_INVALID;
+    if (B < 0) return fail(KDA_ERR_INVALID, "B must be >= 0 (got %d)", B);
+    if (n < 1 || n > KDA_DECODE_MAX_TOKENS)
+        return fail(KDA_ERR_INVALID, "n must be in [1, %d] (got %d)", KDA_DECODE_MAX_TOKENS, n);
+    if (B == 0) return KDA_OK;
+    if (!slots || !q || !k || !v || !z || !b || !g || !out) return fail(KDA_ERR_INVALID, "a tensor pointer is NULL");
+    if (!kda::io_aligned(q, k, v, z, g, out)) return fail(KDA_ERR_INVALID, "q, k, v, z, g or out is not 16-byte aligned");
+    if ((int64_t)B * n * cfg->num_heads > INT_MAX) return fail(KDA_ERR_INVALID, "B * n * num_heads is too large");
+    if (!device_matches(st)) return KDA_ERR_INVALID;
+    cudaError_t e = kda::launch_decode_multi(*st, *params, slots, B, n, q, k, v, z, b, g, out,
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kda_decode_tokens launch");
+    return KDA_OK;
+}
+
 kda_status kda_prefill(const kda_config_t *cfg, const kda_layer_params *params, kda_state *h,
                        const int32_t *slots, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int32_t N,
                        const void *q, const void *k, const void *v, const void *z, const void *b, const void *g,

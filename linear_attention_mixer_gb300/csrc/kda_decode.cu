@@ -119,7 +119,7 @@ decode_persistent_kernel(const float *__restrict__ conv_w, const float *__restri
         const int h = u / B, r = u - (u / B) * B;
         const int slot = slots[r];
         const bool bad = slot < 0 || slot >= max_slots;
-        const float beta = sigmoidf_(IO<T>::ld(bl + (size_t)r * H + h));
+        const float beta = sigmoid_ftz(IO<T>::ld(bl + (size_t)r * H + h));
         if (h != cur_h) {  // new head: its conv taps and dt_bias into shared memory
             if (tid < kD) {
                 const size_t c = (size_t)h * kD + tid;
@@ -151,7 +151,7 @@ decode_persistent_kernel(const float *__restrict__ conv_w, const float *__restri
                 const float4 wt = cw[x * kD + i];
                 const T h0 = tl[(x * 3 + 0) * kD + i], h1 = tl[(x * 3 + 1) * kD + i], h2 = tl[(x * 3 + 2) * kD + i];
                 const T raw = in[x * kD + i];
-                y[x] = siluf_(fmaf(wt.x, IO<T>::ld(&h0), fmaf(wt.y, IO<T>::ld(&h1),
+                y[x] = silu_ftz(fmaf(wt.x, IO<T>::ld(&h0), fmaf(wt.y, IO<T>::ld(&h1),
                               fmaf(wt.z, IO<T>::ld(&h2), wt.w * IO<T>::ld(&raw)))));
                 tl_g[(size_t)(x * 3 + 0) * D + i] = h1;
                 tl_g[(size_t)(x * 3 + 1) * D + i] = h2;
@@ -159,8 +159,8 @@ decode_persistent_kernel(const float *__restrict__ conv_w, const float *__restri
             }
             yq = y[0]; yk = y[1];
             sh_v[i] = y[2];
-            sh_a[i] = expf(gmin * sigmoidf_(eA * (IO<T>::ld(in + 3 * kD + i) + sdt[i])));
-            sh_gw[i] = sigmoidf_(IO<T>::ld(in + 4 * kD + i)) * snw[i];
+            sh_a[i] = exp_ftz(gmin * sigmoid_ftz(eA * (IO<T>::ld(in + 3 * kD + i) + sdt[i])));
+            sh_gw[i] = sigmoid_ftz(IO<T>::ld(in + 4 * kD + i)) * snw[i];
             const float a0 = warp_sum(yq * yq), a1 = warp_sum(yk * yk), a2 = warp_sum(yq * yk);
             if (l == 0) { part[w] = a0; part[4 + w] = a1; part[8 + w] = a2; }
         }
@@ -173,8 +173,8 @@ decode_persistent_kernel(const float *__restrict__ conv_w, const float *__restri
         const float sqq = part[0] + part[1] + part[2] + part[3];
         const float skk = part[4] + part[5] + part[6] + part[7];
         const float sqk = part[8] + part[9] + part[10] + part[11];
-        const float rq = q_scale / sqrtf(sqq + l2_eps);
-        const float rk = 1.0f / sqrtf(skk + l2_eps);
+        const float rq = q_scale * rsqrt_ftz(sqq + l2_eps);
+        const float rk = rsqrt_ftz(skk + l2_eps);
         const float kq = sqk * rq * rk;
         if (tid < kD) { sh_k[tid] = yk * rk; sh_q[tid] = yq * rq; }
         __syncthreads();
@@ -207,7 +207,7 @@ decode_persistent_kernel(const float *__restrict__ conv_w, const float *__restri
         }
         if (w == 0) {
             const float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
-            const float rinv = 1.0f / sqrtf(ss * (1.0f / kD) + rms_eps);
+            const float rinv = rsqrt_ftz(ss * (1.0f / kD) + rms_eps);
             const float4 gw4 = reinterpret_cast<const float4 *>(sh_gw)[l];
             T *dst = out + (size_t)r * D + (size_t)h * kD + 4 * l;
             IO<T>::st(dst + 0, gw4.x * (o.x * rinv));

@@ -1,0 +1,282 @@
+// kda_decode_multi.cu - n consecutive decode tokens per sequence in one pass over
+// the state (verification of speculative drafts, or any short run of known tokens).
+//
+// Each (sequence, head) unit is the per-head recurrence of the kimi_k3.c header
+// comment ("KDA per-head recurrence") applied n times in order. The unit's 64 KB
+// FP32 state is read once, stays in registers across the n tokens and is written
+// once, so n tokens cost one state round trip instead of n. Per token the
+// arithmetic is the single-token decode's (conv + SiLU, L2 norms, gates, the
+// delta-rule update in the expanded form S' = Diag(a) S + k u^T with
+// u = beta (v - (Diag(a) S)^T k), the readout o = S'^T q and the gated RMSNorm);
+// the conv history slides through the run in registers.
+//
+// One CTA per SM walks a contiguous range of units (head-major); the state, the
+// n input rows of each of q,k,v,z,g and the history of the next unit arrive by
+// bulk copies into the other of two shared-memory stages while the current unit
+// is computed. Thread layout as in the single-token decode: warp w owns state
+// rows w + 8m, lane l columns 4l..4l+3.
+#include "kda_internal.cuh"
+#include "kda_ptx.cuh"
+
+namespace kda {
+namespace {
+
+template <typename T>
+struct MultiStage {
+    static constexpr int kS = kD * kD * 4;                             // state
+    static constexpr int kRow = kD * (int)sizeof(T);                   // one row of one head
+    static constexpr int kIn = 5 * KDA_DECODE_MAX_TOKENS * kRow;       // [5][n][d] q,k,v,z,g
+    static constexpr int kTail = 9 * kRow;                             // [3][3][d] history
+    static constexpr int kBytes = kS + kIn + kTail;
+};
+
+constexpr uint32_t kMultiWaitLimit = 1u << 26;
+
+__device__ __forceinline__ float4 m_fma4(float a, float4 x, float4 y)
+{
+    return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256, 1)
+decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
+                    const float *__restrict__ A_log, const float *__restrict__ norm_w,
+                    float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__restrict__ err,
+                    const int32_t *__restrict__ slots, int B, int n, int H, int max_slots,
+                    const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                    const T *__restrict__ z, const T *__restrict__ bl, const T *__restrict__ g,
+                    T *__restrict__ out, float gmin, float l2_eps, float rms_eps, float q_scale)
+{
+    using L = MultiStage<T>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int kNT = KDA_DECODE_MAX_TOKENS;
+    float *sh_k = reinterpret_cast<float *>(smem + 2 * L::kBytes);  // [token][d] k^ of every token
+    float *sh_q = sh_k + kNT * kD, *sh_a = sh_q + kNT * kD, *sh_v = sh_a + kNT * kD, *sh_gw = sh_v + kNT * kD;
+    float4 *red = reinterpret_cast<float4 *>(sh_gw + kNT * kD);  // [2 token parities][2][8][32]
+    float *part = reinterpret_cast<float *>(red + 2 * 2 * 8 * 32);  // [token][3][4] quarter sums of squares
+    float *sbeta = part + kNT * 12;                                  // [token] beta
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sbeta + kNT);       // [2]
+
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    const int n_units = B * H;
+    const int per = (n_units + gridDim.x - 1) / gridDim.x;
+    const int u_begin = blockIdx.x * per;
+    const int u_end = min(n_units, u_begin + per);
+    if (u_begin >= u_end) return;
+    const size_t D = (size_t)H * kD;
+    const T *src5[5] = {q, k, v, z, g};
+
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](int stage, int u) {  // thread 0 only
+        const int h = u / B, r = u - (u / B) * B;
+        const int slot = slots[r];
+        unsigned char *st = smem + stage * L::kBytes;
+        if (slot < 0 || slot >= max_slots) {
+            mbar_arrive(&bar[stage]);  // completes the phase with no data
+            return;
+        }
+        mbar_arrive_expect_tx(&bar[stage], (uint32_t)(L::kS + (5 * n + 9) * L::kRow));
+        bulk_g2s_hint(st, S_all + ((size_t)slot * H + h) * kD * kD, L::kS, &bar[stage], pol);
+        for (int x = 0; x < 5; ++x)
+            for (int t = 0; t < n; ++t)
+                bulk_g2s(st + L::kS + (x * KDA_DECODE_MAX_TOKENS + t) * L::kRow,
+                         src5[x] + ((size_t)r * n + t) * D + (size_t)h * kD, L::kRow, &bar[stage]);
+        for (int e = 0; e < 9; ++e)
+            bulk_g2s(st + L::kS + L::kIn + e * L::kRow, tail_all + ((size_t)slot * 9 + e) * D + (size_t)h * kD,
+                     L::kRow, &bar[stage]);
+    };
+
+    if (tid == 0) issue(0, u_begin);
+    bool timed_out = false;
+    int it = 0;
+    for (int u = u_begin; u < u_end; ++u, ++it) {
+        const int stage = it & 1;
+        if (tid == 0 && u + 1 < u_end) issue(stage ^ 1, u + 1);  // the other stage is free
+        const int h = u / B, r = u - (u / B) * B;
+        const int slot = slots[r];
+        const bool bad = slot < 0 || slot >= max_slots;
+        // per-unit scalars and parameters are loaded before the wait, so their latency hides
+        // behind the copies (the beta logit of each token, and channel tid & 127's taps)
+        T braw = T(0.f);
+        if (tid < n) braw = bl[((size_t)r * n + tid) * H + h];
+        const int pi = tid & (kD - 1);
+        const size_t pc = (size_t)h * kD + pi;
+        float4 wt[3];
+#pragma unroll
+        for (int x = 0; x < 3; ++x) wt[x] = __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)x * D + pc) * kK));
+        const float dti = __ldg(dt_bias + pc), nwi = __ldg(norm_w + pi);
+        const float eA = expf(__ldg(A_log + h));
+        const bool ok = mbar_wait_bounded(&bar[stage], (uint32_t)((it >> 1) & 1), kMultiWaitLimit);
+        if (__syncthreads_or(!ok)) { timed_out = true; break; }
+        if (bad) {
+            if (tid == 0) atomicExch(err, kErrBadSlot);
+            __syncthreads();
+            continue;
+        }
+        const unsigned char *st = smem + stage * L::kBytes;
+        const T *in = reinterpret_cast<const T *>(st + L::kS);          // [5][8][d]
+        const T *tl = reinterpret_cast<const T *>(st + L::kS + L::kIn);  // [3][3][d]
+
+        // the unit's state tile in registers for the whole run
+        float4 s[16];
+        const float4 *S4s = reinterpret_cast<const float4 *>(st);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) s[m] = S4s[(w + 8 * m) * 32 + l];
+
+        // prologue of every token at once (it does not depend on the state): thread (channel
+        // i, token parity tg) takes tokens tg, tg + 2, ...; the conv window of token t is raw
+        // rows t-3 .. t, the first ones from the history
+        {
+            const int i = pi, tg = tid >> 7;
+            if (tid < n) sbeta[tid] = sigmoid_ftz(IO<T>::ld(&braw));
+            auto raw = [&](int x, int j) -> float {  // raw input of stream x at token j (j >= -3)
+                return j >= 0 ? IO<T>::ld(in + (x * KDA_DECODE_MAX_TOKENS + j) * kD + i)
+                              : IO<T>::ld(tl + (x * 3 + (j + 3)) * kD + i);
+            };
+            for (int t = tg; t < n; t += 2) {
+                float y[3];
+#pragma unroll
+                for (int x = 0; x < 3; ++x)
+                    y[x] = silu_ftz(fmaf(wt[x].x, raw(x, t - 3), fmaf(wt[x].y, raw(x, t - 2),
+                                  fmaf(wt[x].z, raw(x, t - 1), wt[x].w * raw(x, t)))));
+                sh_q[t * kD + i] = y[0];
+                sh_k[t * kD + i] = y[1];
+                sh_v[t * kD + i] = y[2];
+                sh_a[t * kD + i] = exp_ftz(gmin * sigmoid_ftz(eA * (IO<T>::ld(in + (3 * KDA_DECODE_MAX_TOKENS + t) * kD + i) + dti)));
+                sh_gw[t * kD + i] = sigmoid_ftz(IO<T>::ld(in + (4 * KDA_DECODE_MAX_TOKENS + t) * kD + i)) * nwi;
+                const float a0 = warp_sum(y[0] * y[0]), a1 = warp_sum(y[1] * y[1]), a2 = warp_sum(y[0] * y[1]);
+                if (l == 0) { part[t * 12 + (w & 3)] = a0; part[t * 12 + 4 + (w & 3)] = a1; part[t * 12 + 8 + (w & 3)] = a2; }
+            }
+            __syncthreads();
+            for (int t = tg; t < n; t += 2) {
+                const float *pt = part + t * 12;
+                const float rq = q_scale * rsqrt_ftz((pt[0] + pt[1] + pt[2] + pt[3]) + l2_eps);
+                const float rk = rsqrt_ftz((pt[4] + pt[5] + pt[6] + pt[7]) + l2_eps);
+                sh_k[t * kD + i] *= rk;
+                sh_q[t * kD + i] *= rq;
+            }
+            __syncthreads();
+        }
+
+        // the tokens in order: one barrier each (the warp partials alternate between two buffers)
+        for (int t = 0; t < n; ++t) {
+            const size_t row = (size_t)r * n + t;
+            const float *pt = part + t * 12;
+            const float sqq = pt[0] + pt[1] + pt[2] + pt[3];
+            const float skk = pt[4] + pt[5] + pt[6] + pt[7];
+            const float sqk = pt[8] + pt[9] + pt[10] + pt[11];
+            const float kq = sqk * (q_scale * rsqrt_ftz(sqq + l2_eps)) * (rsqrt_ftz(skk + l2_eps));
+            const float beta = sbeta[t];
+            const float *ka = sh_k + t * kD, *qa = sh_q + t * kD, *aa = sh_a + t * kD;
+            float4 p = make_float4(0.f, 0.f, 0.f, 0.f), rr = p;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int i = w + 8 * m;
+                const float a = aa[i];
+                p = m_fma4(a * ka[i], s[m], p);
+                rr = m_fma4(a * qa[i], s[m], rr);
+            }
+            float4 *rb = red + (t & 1) * (2 * 8 * 32);
+            rb[(0 * 8 + w) * 32 + l] = p;
+            rb[(1 * 8 + w) * 32 + l] = rr;
+            __syncthreads();
+            float4 P = rb[l], R = rb[8 * 32 + l];
+#pragma unroll
+            for (int ww = 1; ww < 8; ++ww) {
+                const float4 a = rb[ww * 32 + l], b2 = rb[(8 + ww) * 32 + l];
+                P = make_float4(P.x + a.x, P.y + a.y, P.z + a.z, P.w + a.w);
+                R = make_float4(R.x + b2.x, R.y + b2.y, R.z + b2.z, R.w + b2.w);
+            }
+            const float4 vv = reinterpret_cast<const float4 *>(sh_v + t * kD)[l];
+            const float4 uu = make_float4(beta * (vv.x - P.x), beta * (vv.y - P.y), beta * (vv.z - P.z),
+                                          beta * (vv.w - P.w));
+            const float4 o = m_fma4(kq, uu, R);
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int i = w + 8 * m;
+                const float a = aa[i], kk = ka[i];
+                s[m] = make_float4(fmaf(a, s[m].x, kk * uu.x), fmaf(a, s[m].y, kk * uu.y),
+                                   fmaf(a, s[m].z, kk * uu.z), fmaf(a, s[m].w, kk * uu.w));
+            }
+            if (w == 0) {
+                const float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
+                const float rinv = rsqrt_ftz(ss * (1.0f / kD) + rms_eps);
+                const float4 gw4 = reinterpret_cast<const float4 *>(sh_gw + t * kD)[l];
+                T *dst = out + row * D + (size_t)h * kD + 4 * l;
+                IO<T>::st(dst + 0, gw4.x * (o.x * rinv));
+                IO<T>::st(dst + 1, gw4.y * (o.y * rinv));
+                IO<T>::st(dst + 2, gw4.z * (o.z * rinv));
+                IO<T>::st(dst + 3, gw4.w * (o.w * rinv));
+            }
+        }
+        // the state after the run, and the new history (the last three raw inputs)
+        float4 *S4 = reinterpret_cast<float4 *>(S_all + ((size_t)slot * H + h) * kD * kD);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) st_stream(S4 + (w + 8 * m) * 32 + l, s[m]);
+        if (tid < kD) {
+            T *tg_out = tail_all + (size_t)slot * 9 * D + (size_t)h * kD + tid;
+#pragma unroll
+            for (int x = 0; x < 3; ++x)
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int tok = n - 3 + j;
+                    tg_out[(size_t)(x * 3 + j) * D] = tok >= 0 ? in[(x * KDA_DECODE_MAX_TOKENS + tok) * kD + tid]
+                                                               : tl[(x * 3 + (tok + 3)) * kD + tid];
+                }
+        }
+        __syncthreads();  // the stage, the prologue arrays and the partials are free
+    }
+    if (timed_out) {
+        if (tid == 0) {
+            atomicExch(err, KDA_ERR_TIMEOUT);
+            // the copy for the next unit may still be in flight
+            if (u_begin + it + 1 < u_end) mbar_wait_bounded(&bar[(it + 1) & 1], (uint32_t)(((it + 1) >> 1) & 1), kMultiWaitLimit);
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T>
+cudaError_t launch_multi_typed(const State &st, const kda_layer_params &p, const int32_t *slots, int B, int n,
+                               const void *q, const void *k, const void *v, const void *z, const void *b,
+                               const void *g, void *out, cudaStream_t stream)
+{
+    using L = MultiStage<T>;
+    const kda_config_t &c = st.cfg;
+    const int H = c.num_heads;
+    const size_t smem = 2 * (size_t)L::kBytes + 5 * KDA_DECODE_MAX_TOKENS * kD * 4 + 2 * 2 * 8 * 32 * 16 +
+                        KDA_DECODE_MAX_TOKENS * 13 * 4 + 2 * 8;
+    cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, st.device);
+    if (e != cudaSuccess) return e;
+    const int n_units = B * H;
+    const int grid = n_units < sms ? n_units : sms;
+    decode_multi_kernel<T><<<grid, 256, smem, stream>>>(
+        p.conv_w, p.dt_bias, p.A_log, p.norm_w, st.S, (T *)st.tail, st.err, slots, B, n, H, st.max_slots,
+        (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, (const T *)g, (T *)out,
+        c.gate_lower_bound, c.l2_eps, c.rms_eps, c.q_scale);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_multi(const State &st, const kda_layer_params &p, const int32_t *slots, int B, int n,
+                                const void *q, const void *k, const void *v, const void *z, const void *b,
+                                const void *g, void *out, cudaStream_t stream)
+{
+    if (st.cfg.io_dtype == KDA_BF16)
+        return launch_multi_typed<__nv_bfloat16>(st, p, slots, B, n, q, k, v, z, b, g, out, stream);
+    return launch_multi_typed<float>(st, p, slots, B, n, q, k, v, z, b, g, out, stream);
+}
+
+}  // namespace kda

@@ -57,6 +57,9 @@ constexpr int32_t kErrBadSlot = KDA_ERR_DEVICE;
 cudaError_t launch_decode(const State &st, const kda_layer_params &p, const int32_t *slots, int B,
                           const void *q, const void *k, const void *v, const void *z, const void *b,
                           const void *g, void *out, cudaStream_t stream);
+cudaError_t launch_decode_multi(const State &st, const kda_layer_params &p, const int32_t *slots, int B, int n,
+                                const void *q, const void *k, const void *v, const void *z, const void *b,
+                                const void *g, void *out, cudaStream_t stream);
 
 size_t prefill_workspace_bytes(const kda_config_t &cfg, int64_t total_chunks, int64_t total_T, int N);
 cudaError_t launch_prefill(const State &st, const kda_layer_params &p, const int32_t *slots,

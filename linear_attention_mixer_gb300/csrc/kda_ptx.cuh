@@ -170,6 +170,11 @@ __device__ __forceinline__ float rsqrt_ftz(float x)
     return y;
 }
 
+// sigmoid(x) = 1 / (1 + e^-x) and SiLU(x) = x sigmoid(x) from the two SFU functions above;
+// for very negative x, e^-x overflows to +inf and the reciprocal gives exactly 0.
+__device__ __forceinline__ float sigmoid_ftz(float x) { return rcp_ftz(1.0f + exp_ftz(-x)); }
+__device__ __forceinline__ float silu_ftz(float x) { return x * rcp_ftz(1.0f + exp_ftz(-x)); }
+
 // Hardware tanh approximation (max relative error about 2^-11).
 __device__ __forceinline__ float tanh_approx(float x)
 {

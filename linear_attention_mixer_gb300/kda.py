@@ -17,6 +17,7 @@ KDA_OK, KDA_ERR_INVALID, KDA_ERR_OOM, KDA_ERR_CUDA, KDA_ERR_BLOB, KDA_ERR_TIMEOU
 KDA_F32, KDA_BF16 = 0, 1
 KDA_BLOB_MAGIC = 0x3141444B
 KDA_BLOB_VERSION = 1
+KDA_DECODE_MAX_TOKENS = 8  # most tokens per row in one kda_decode_tokens call
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID", 2: "KDA_ERR_OOM", 3: "KDA_ERR_CUDA",
                 4: "KDA_ERR_BLOB", 5: "KDA_ERR_TIMEOUT", 6: "KDA_ERR_DEVICE"}
 
@@ -69,6 +70,8 @@ SIGNATURES = [
     ("kda_state_restore", _I32, [_VP, _PI32, _I32, _VP, _I32, _VP]),
     ("kda_decode_token", _I32, [ctypes.POINTER(kda_config_t), ctypes.POINTER(kda_layer_params), _VP, _VP, _I32,
                                 _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    ("kda_decode_tokens", _I32, [ctypes.POINTER(kda_config_t), ctypes.POINTER(kda_layer_params), _VP, _VP, _I32,
+                                 _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("kda_prefill", _I32, [ctypes.POINTER(kda_config_t), ctypes.POINTER(kda_layer_params), _VP, _VP, _VP, _PI32,
                            _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("kda_prefill_noalloc", _I32, [ctypes.POINTER(kda_config_t), ctypes.POINTER(kda_layer_params), _VP, _VP, _I32,
@@ -202,6 +205,22 @@ def kda_decode_token(cfg: kda_config_t, params: kda_layer_params, st, slots: tor
     _check(lib().kda_decode_token(ctypes.byref(cfg), ctypes.byref(params), st, _dev(slots, torch.int32, "slots"), B,
                                   _dev(q, dt, "q"), _dev(k, dt, "k"), _dev(v, dt, "v"), _dev(z, dt, "z"),
                                   _dev(b, dt, "b"), _dev(g, dt, "g"), _dev(out, dt, "out"), _stream(stream)))
+
+
+def kda_decode_tokens(cfg: kda_config_t, params: kda_layer_params, st, slots: torch.Tensor, n: int,
+                      q, k, v, z, b, g, out, stream=None) -> None:
+    """n consecutive decode tokens per row: q,k,v,z,g,out [B][n][H*d], b [B][n][H]."""
+    dt = _torch_io_dtype(cfg)
+    B = int(slots.numel())
+    D = cfg.num_heads * cfg.head_dim
+    for name, t, width in (("q", q, D), ("k", k, D), ("v", v, D), ("z", z, D), ("g", g, D),
+                           ("b", b, cfg.num_heads), ("out", out, D)):
+        if t.numel() != B * n * width:
+            raise ValueError(f"{name} must hold {B} x {n} x {width} elements, got {tuple(t.shape)}")
+    _check(lib().kda_decode_tokens(ctypes.byref(cfg), ctypes.byref(params), st, _dev(slots, torch.int32, "slots"),
+                                   B, int(n), _dev(q, dt, "q"), _dev(k, dt, "k"), _dev(v, dt, "v"),
+                                   _dev(z, dt, "z"), _dev(b, dt, "b"), _dev(g, dt, "g"), _dev(out, dt, "out"),
+                                   _stream(stream)))
 
 
 def kda_prefill(cfg: kda_config_t, params: kda_layer_params, st, slots: torch.Tensor, cu_seqlens: torch.Tensor,

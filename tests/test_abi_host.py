@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("kda_config", "kda_state_alloc", "kda_state_free", "kda_state_reset", "kda_state_snapshot",
-                 "kda_state_restore", "kda_decode_token", "kda_prefill", "kda_last_error"):
+                 "kda_state_restore", "kda_decode_token", "kda_decode_tokens", "kda_prefill", "kda_last_error"):
         assert want in names
 
 
@@ -75,6 +75,8 @@ def test_null_and_bad_arguments_rejected_before_the_device(K):
                               *([None] * 7), None) == K.KDA_ERR_INVALID
     assert L.kda_prefill(ctypes.byref(cfg), ctypes.byref(params), None, None, None, None, 1,
                          *([None] * 7), None) == K.KDA_ERR_INVALID
+    assert L.kda_decode_tokens(ctypes.byref(cfg), ctypes.byref(params), None, None, 1, 2,
+                               *([None] * 7), None) == K.KDA_ERR_INVALID
     out = ctypes.c_void_p()
     assert L.kda_state_alloc(ctypes.byref(cfg), 0, ctypes.byref(out)) == K.KDA_ERR_INVALID
     assert out.value is None

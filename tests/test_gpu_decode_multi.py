@@ -1,0 +1,131 @@
+"""kda_decode_tokens (n decode tokens per row in one pass over the state) through the C ABI:
+against the FP64 oracle run token by token, against n calls of kda_decode_token, and the
+snapshot/restore rollback a speculative verifier uses."""
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs as KI
+import linear_attention_mixer_gb300 as K
+from tests.kda_testutil import (TOL_BF16, TOL_F32, dev_params, dev_tokens, download_state, rel_err, to_np,
+                                upload_state)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from linear_attention_mixer_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+def _run_multi(cfg, params, st, slots_np, tok, bf16, n):
+    B = len(slots_np)
+    D = cfg.num_heads * cfg.head_dim
+    t = dev_tokens(tok, bf16)
+    out = torch.empty(B * n, D, device="cuda", dtype=t["q"].dtype)
+    K.kda_decode_tokens(cfg, params, st, torch.tensor(slots_np, dtype=torch.int32, device="cuda"), n,
+                        t["q"], t["k"], t["v"], t["z"], t["b"], t["g"], out)
+    return to_np(out).reshape(B, n, D)
+
+
+def _run_single(cfg, params, st, slots_np, tok, bf16, n):
+    B = len(slots_np)
+    D = cfg.num_heads * cfg.head_dim
+    slots = torch.tensor(slots_np, dtype=torch.int32, device="cuda")
+    outs = []
+    for s in range(n):
+        t = dev_tokens(tok, bf16, rows=np.arange(B) * n + s)
+        out = torch.empty(B, D, device="cuda", dtype=t["q"].dtype)
+        K.kda_decode_token(cfg, params, st, slots, t["q"], t["k"], t["v"], t["z"], t["b"], t["g"], out)
+        outs.append(to_np(out))
+    return np.stack(outs, axis=1)  # [B][n][D]
+
+
+@pytest.mark.parametrize("bf16,H,B,n", [(False, 2, 3, 1), (False, 2, 3, 8), (False, 2, 2, 5),
+                                        (True, 96, 3, 4), (True, 96, 2, 8)])
+def test_decode_tokens_matches_oracle_and_single_calls(oracle_mod, bf16, H, B, n):
+    d, seed = 128, 70 + n + H
+    p = KI.make_params(H, d, 4, seed)
+    tok = KI.make_tokens(B * n, H, d, seed, bf16=bf16)  # row r, token t at r * n + t
+    S0 = KI.make_state(B, H, d, seed)
+    T0 = KI.make_tail(B, H, d, 4, seed, bf16=bf16)
+    cfg = K.kda_config(H, d, K.KDA_BF16 if bf16 else K.KDA_F32)
+    params = dev_params(p)
+    st = K.kda_state_alloc(cfg, 2 * B)
+    try:
+        multi_slots, single_slots = list(range(B)), list(range(B, 2 * B))
+        upload_state(cfg, st, multi_slots, S0, T0)
+        upload_state(cfg, st, single_slots, S0, T0)
+        got = _run_multi(cfg, params, st, multi_slots, tok, bf16, n)
+        one = _run_single(cfg, params, st, single_slots, tok, bf16, n)
+        Sm, tm = download_state(cfg, st, multi_slots)
+        Ss, ts = download_state(cfg, st, single_slots)
+        assert K.kda_state_poll_error(st) == 0
+    finally:
+        K.kda_state_free(st)
+    # one pass over n tokens is n single-token steps: the same arithmetic per token, bit for bit
+    d_out, d_s = rel_err(got, one), rel_err(Sm, Ss)
+    assert np.array_equal(got, one) and np.array_equal(Sm, Ss)
+    assert np.array_equal(tm, ts)
+    oc = oracle_mod.OracleCfg(H=H, d=d)
+    worst_o = worst_s = 0.0
+    for r in range(B):
+        S = S0[r].astype(np.float64)
+        tail = T0[r].astype(np.float64)
+        ref = oracle_mod.sequence(oc, p, S, tail, {m: a[r * n:(r + 1) * n] for m, a in tok.items()})
+        worst_o = max(worst_o, rel_err(got[r], ref))
+        worst_s = max(worst_s, rel_err(Sm[r], S))
+        assert np.array_equal(tm[r], tail.astype(np.float32))
+    tol = TOL_BF16 if bf16 else TOL_F32
+    print(f"decode_tokens {'bf16' if bf16 else 'fp32'} H={H} B={B} n={n}: out {worst_o:.2e} state {worst_s:.2e}; "
+          f"vs single-token calls out {d_out:.1e} state {d_s:.1e} ({'bit-exact' if d_out == 0 and d_s == 0 else 'close'})")
+    assert worst_o <= tol and worst_s <= tol
+
+
+def test_speculative_rollback_and_argument_errors():
+    """Verify a draft of 6 tokens from a snapshot, reject after 3: restore the snapshot and
+    run the accepted 3 again. The slot then equals one that only ever saw those 3 tokens
+    (bit for bit). Bad slot ids are skipped and recorded; n outside [1, 8] is refused."""
+    H, d, B, n, j = 4, 128, 2, 6, 3
+    p = KI.make_params(H, d, 4, 91)
+    tok = KI.make_tokens(B * n, H, d, 91, bf16=True)
+    acc = {m: a.reshape(B, n, -1)[:, :j].reshape(B * j, -1) for m, a in tok.items()}  # accepted prefix
+    S0 = KI.make_state(B, H, d, 91)
+    T0 = KI.make_tail(B, H, d, 4, 91, bf16=True)
+    cfg = K.kda_config(H, d, K.KDA_BF16)
+    params = dev_params(p)
+    st = K.kda_state_alloc(cfg, 2 * B)
+    try:
+        spec, ref = list(range(B)), list(range(B, 2 * B))
+        upload_state(cfg, st, spec, S0, T0)
+        upload_state(cfg, st, ref, S0, T0)
+        snap = torch.empty(K.kda_state_blob_bytes(st, B), dtype=torch.uint8, device="cuda")
+        K.kda_state_snapshot(st, spec, snap)
+        _run_multi(cfg, params, st, spec, tok, True, n)  # the draft
+        K.kda_state_restore(st, spec, snap)              # rejected after j tokens
+        out_spec = _run_multi(cfg, params, st, spec, acc, True, j)
+        out_ref = _run_multi(cfg, params, st, ref, acc, True, j)
+        Sa, ta = download_state(cfg, st, spec)
+        Sb, tb = download_state(cfg, st, ref)
+        assert K.kda_state_poll_error(st) == 0
+        assert np.array_equal(out_spec, out_ref)
+        assert np.array_equal(Sa, Sb) and np.array_equal(ta, tb)
+
+        # a bad slot id: the row is skipped, the others run, the error word records it
+        t = dev_tokens(acc, True)
+        out = torch.empty(B * j, H * d, device="cuda", dtype=torch.bfloat16)
+        bad = torch.tensor([0, 7 * B], dtype=torch.int32, device="cuda")
+        K.kda_decode_tokens(cfg, params, st, bad, j, t["q"], t["k"], t["v"], t["z"], t["b"], t["g"], out)
+        assert K.kda_state_poll_error(st) == K.KDA_ERR_DEVICE
+        import ctypes
+        sl = torch.tensor(spec, dtype=torch.int32, device="cuda")
+        ptrs = [ctypes.c_void_p(x.data_ptr()) for x in (t["q"], t["k"], t["v"], t["z"], t["b"], t["g"], out)]
+        for bad_n in (0, K.KDA_DECODE_MAX_TOKENS + 1):
+            rc = K.lib().kda_decode_tokens(ctypes.byref(cfg), ctypes.byref(params), st, ctypes.c_void_p(sl.data_ptr()),
+                                           B, bad_n, *ptrs, None)
+            assert rc == K.KDA_ERR_INVALID and "n must be" in K.kda_last_error()
+        assert K.kda_state_poll_error(st) == 0  # nothing was enqueued
+    finally:
+        K.kda_state_free(st)
