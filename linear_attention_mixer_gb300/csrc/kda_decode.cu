@@ -12,22 +12,17 @@
 // which is (I - beta k k^T) Diag(alpha) S + beta k v^T expanded, so the state
 // stays in registers between the reductions and the write-back.
 //
-// Thread layout (256 threads, 8 warps): warp w owns state rows i = w + 8m
-// (m = 0..15) and lane l owns columns 4l..4l+3 of each of them, so every warp
-// load/store instruction moves one full 512-byte row.
+// Thread layout (256 threads, 8 warps): warp w owns state rows 16w .. 16w+15
+// and lane l owns columns 4l..4l+3 of each of them, so every warp load/store
+// instruction moves one full 512-byte row. The per-token step (column
+// reductions, update, RMSNorm) is shared with the multi-token decode
+// (kda_decode_common.cuh).
+#include "kda_decode_common.cuh"
 #include "kda_internal.cuh"
 #include "kda_ptx.cuh"
 
 namespace kda {
 namespace {
-
-__device__ __forceinline__ float4 f4(float a) { return make_float4(a, a, a, a); }
-__device__ __forceinline__ float4 fma4(float a, float4 x, float4 y) {
-    return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
-}
-__device__ __forceinline__ float4 add4(float4 x, float4 y) {
-    return make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
-}
 
 // ---------------------------------------------------------------------------
 // One CTA per SM walks a contiguous range of units in
@@ -62,9 +57,10 @@ decode_persistent_kernel(const float *__restrict__ conv_w, const float *__restri
     float4 *cw = reinterpret_cast<float4 *>(smem + NS * L::kBytes);   // [3][d] conv taps of the current head
     float *sdt = reinterpret_cast<float *>(cw + 3 * kD);               // [d]
     float *snw = sdt + kD;                                             // [d]
-    float *sh_k = snw + kD, *sh_q = sh_k + kD, *sh_a = sh_q + kD, *sh_v = sh_a + kD, *sh_gw = sh_v + kD;
-    float4 *red = reinterpret_cast<float4 *>(sh_gw + kD);               // [2][8][32]
-    float *part = reinterpret_cast<float *>(red + 2 * 8 * 32);         // [3][4]
+    float *sh_k = snw + kD, *sh_a = sh_k + kD, *sh_v = sh_a + kD, *sh_gw = sh_v + kD;
+    float *sh_ak = sh_gw + kD, *sh_aq = sh_ak + kD, *su = sh_aq + kD, *so = su + kD;  // [d] each
+    float *red = so + kD;                                              // [2][8][d] warp partials
+    float *part = red + 2 * 8 * kD;                                    // [3][4]
     uint64_t *bar = reinterpret_cast<uint64_t *>(part + 16);           // [NS]
 
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
@@ -168,7 +164,7 @@ decode_persistent_kernel(const float *__restrict__ conv_w, const float *__restri
         float4 s[16];
         const float4 *S4s = reinterpret_cast<const float4 *>(st);
 #pragma unroll
-        for (int m = 0; m < 16; ++m) s[m] = S4s[(w + 8 * m) * 32 + l];
+        for (int m = 0; m < 16; ++m) s[m] = S4s[(16 * w + m) * 32 + l];
         __syncthreads();
         const float sqq = part[0] + part[1] + part[2] + part[3];
         const float skk = part[4] + part[5] + part[6] + part[7];
@@ -176,45 +172,18 @@ decode_persistent_kernel(const float *__restrict__ conv_w, const float *__restri
         const float rq = q_scale * rsqrt_ftz(sqq + l2_eps);
         const float rk = rsqrt_ftz(skk + l2_eps);
         const float kq = sqk * rq * rk;
-        if (tid < kD) { sh_k[tid] = yk * rk; sh_q[tid] = yq * rq; }
-        __syncthreads();
-
-        float4 p = f4(0.f), rr = f4(0.f);
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const int i = w + 8 * m;
-            const float a = sh_a[i];
-            p = fma4(a * sh_k[i], s[m], p);
-            rr = fma4(a * sh_q[i], s[m], rr);
+        if (tid < kD) {
+            const float kn = yk * rk, a = sh_a[tid];
+            sh_k[tid] = kn;
+            sh_ak[tid] = a * kn;
+            sh_aq[tid] = a * (yq * rq);
         }
-        red[(0 * 8 + w) * 32 + l] = p;
-        red[(1 * 8 + w) * 32 + l] = rr;
         __syncthreads();
-        float4 P = red[l], R = red[8 * 32 + l];
-#pragma unroll
-        for (int ww = 1; ww < 8; ++ww) { P = add4(P, red[ww * 32 + l]); R = add4(R, red[(8 + ww) * 32 + l]); }
-        const float4 vv = reinterpret_cast<const float4 *>(sh_v)[l];
-        const float4 uu = make_float4(beta * (vv.x - P.x), beta * (vv.y - P.y), beta * (vv.z - P.z), beta * (vv.w - P.w));
-        const float4 o = fma4(kq, uu, R);
+        decode_token_step<T>(s, sh_ak, sh_aq, sh_a, sh_k, sh_v, sh_gw, beta, kq, red, su, so,
+                             out + (size_t)r * D + (size_t)h * kD, rms_eps, w, l);
         float4 *S4 = reinterpret_cast<float4 *>(S_all + ((size_t)slot * H + h) * kD * kD);
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const int i = w + 8 * m;
-            const float a = sh_a[i], kk = sh_k[i];
-            const float4 sv = s[m];
-            st_stream(S4 + i * 32 + l, make_float4(fmaf(a, sv.x, kk * uu.x), fmaf(a, sv.y, kk * uu.y),
-                                                   fmaf(a, sv.z, kk * uu.z), fmaf(a, sv.w, kk * uu.w)));
-        }
-        if (w == 0) {
-            const float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
-            const float rinv = rsqrt_ftz(ss * (1.0f / kD) + rms_eps);
-            const float4 gw4 = reinterpret_cast<const float4 *>(sh_gw)[l];
-            T *dst = out + (size_t)r * D + (size_t)h * kD + 4 * l;
-            IO<T>::st(dst + 0, gw4.x * (o.x * rinv));
-            IO<T>::st(dst + 1, gw4.y * (o.y * rinv));
-            IO<T>::st(dst + 2, gw4.z * (o.z * rinv));
-            IO<T>::st(dst + 3, gw4.w * (o.w * rinv));
-        }
+        for (int m = 0; m < 16; ++m) st_stream(S4 + (16 * w + m) * 32 + l, s[m]);
         __syncthreads();  // the stage, sh_* and red are free for the next unit
     }
     if (timed_out) {
@@ -237,8 +206,8 @@ cudaError_t launch_persistent(const State &st, const kda_layer_params &p, const 
 {
     const kda_config_t &c = st.cfg;
     const int H = c.num_heads;
-    const size_t smem = (size_t)NS * StageLayout<T>::kBytes + 3 * kD * 16 + 2 * kD * 4 + 5 * kD * 4 +
-                        2 * 8 * 32 * 16 + 16 * 4 + NS * 8;
+    const size_t smem = (size_t)NS * StageLayout<T>::kBytes + 3 * kD * 16 + 2 * kD * 4 + 8 * kD * 4 +
+                        2 * 8 * kD * 4 + 16 * 4 + NS * 8;
     cudaError_t e = cudaFuncSetAttribute(decode_persistent_kernel<T, NS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

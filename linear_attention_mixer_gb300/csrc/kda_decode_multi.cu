@@ -13,8 +13,9 @@
 // One CTA per SM walks a contiguous range of units (head-major); the state, the
 // n input rows of each of q,k,v,z,g and the history of the next unit arrive by
 // bulk copies into the other of two shared-memory stages while the current unit
-// is computed. Thread layout as in the single-token decode: warp w owns state
-// rows w + 8m, lane l columns 4l..4l+3.
+// is computed. The per-token state step is the single-token decode's
+// (kda_decode_common.cuh): warp w owns state rows 16w .. 16w+15, lane l columns 4l..4l+3.
+#include "kda_decode_common.cuh"
 #include "kda_internal.cuh"
 #include "kda_ptx.cuh"
 
@@ -32,11 +33,6 @@ struct MultiStage {
 
 constexpr uint32_t kMultiWaitLimit = 1u << 26;
 
-__device__ __forceinline__ float4 m_fma4(float a, float4 x, float4 y)
-{
-    return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
-}
-
 template <typename T>
 __global__ void __launch_bounds__(256, 1)
 decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
@@ -52,8 +48,10 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
     constexpr int kNT = KDA_DECODE_MAX_TOKENS;
     float *sh_k = reinterpret_cast<float *>(smem + 2 * L::kBytes);  // [token][d] k^ of every token
     float *sh_q = sh_k + kNT * kD, *sh_a = sh_q + kNT * kD, *sh_v = sh_a + kNT * kD, *sh_gw = sh_v + kNT * kD;
-    float4 *red = reinterpret_cast<float4 *>(sh_gw + kNT * kD);  // [2 token parities][2][8][32]
-    float *part = reinterpret_cast<float *>(red + 2 * 2 * 8 * 32);  // [token][3][4] quarter sums of squares
+    float *sh_ak = sh_gw + kNT * kD, *sh_aq = sh_ak + kNT * kD;  // alpha k^ and alpha q^ per row
+    float *su = sh_aq + kNT * kD, *so = su + kD;  // [d] u and o of the current token
+    float *red = so + kD;                          // [2][8][d] warp partials
+    float *part = red + 2 * 8 * kD;                // [token][3][4] quarter sums of squares
     float *sbeta = part + kNT * 12;                                  // [token] beta
     uint64_t *bar = reinterpret_cast<uint64_t *>(sbeta + kNT);       // [2]
 
@@ -128,7 +126,7 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
         float4 s[16];
         const float4 *S4s = reinterpret_cast<const float4 *>(st);
 #pragma unroll
-        for (int m = 0; m < 16; ++m) s[m] = S4s[(w + 8 * m) * 32 + l];
+        for (int m = 0; m < 16; ++m) s[m] = S4s[(16 * w + m) * 32 + l];
 
         // prologue of every token at once (it does not depend on the state): thread (channel
         // i, token parity tg) takes tokens tg, tg + 2, ...; the conv window of token t is raw
@@ -159,13 +157,15 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
                 const float *pt = part + t * 12;
                 const float rq = q_scale * rsqrt_ftz((pt[0] + pt[1] + pt[2] + pt[3]) + l2_eps);
                 const float rk = rsqrt_ftz((pt[4] + pt[5] + pt[6] + pt[7]) + l2_eps);
-                sh_k[t * kD + i] *= rk;
-                sh_q[t * kD + i] *= rq;
+                const float kn = sh_k[t * kD + i] * rk, qn = sh_q[t * kD + i] * rq, a = sh_a[t * kD + i];
+                sh_k[t * kD + i] = kn;
+                sh_ak[t * kD + i] = a * kn;
+                sh_aq[t * kD + i] = a * qn;
             }
             __syncthreads();
         }
 
-        // the tokens in order: one barrier each (the warp partials alternate between two buffers)
+        // the tokens in order
         for (int t = 0; t < n; ++t) {
             const size_t row = (size_t)r * n + t;
             const float *pt = part + t * 12;
@@ -173,53 +173,14 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
             const float skk = pt[4] + pt[5] + pt[6] + pt[7];
             const float sqk = pt[8] + pt[9] + pt[10] + pt[11];
             const float kq = sqk * (q_scale * rsqrt_ftz(sqq + l2_eps)) * (rsqrt_ftz(skk + l2_eps));
-            const float beta = sbeta[t];
-            const float *ka = sh_k + t * kD, *qa = sh_q + t * kD, *aa = sh_a + t * kD;
-            float4 p = make_float4(0.f, 0.f, 0.f, 0.f), rr = p;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int i = w + 8 * m;
-                const float a = aa[i];
-                p = m_fma4(a * ka[i], s[m], p);
-                rr = m_fma4(a * qa[i], s[m], rr);
-            }
-            float4 *rb = red + (t & 1) * (2 * 8 * 32);
-            rb[(0 * 8 + w) * 32 + l] = p;
-            rb[(1 * 8 + w) * 32 + l] = rr;
-            __syncthreads();
-            float4 P = rb[l], R = rb[8 * 32 + l];
-#pragma unroll
-            for (int ww = 1; ww < 8; ++ww) {
-                const float4 a = rb[ww * 32 + l], b2 = rb[(8 + ww) * 32 + l];
-                P = make_float4(P.x + a.x, P.y + a.y, P.z + a.z, P.w + a.w);
-                R = make_float4(R.x + b2.x, R.y + b2.y, R.z + b2.z, R.w + b2.w);
-            }
-            const float4 vv = reinterpret_cast<const float4 *>(sh_v + t * kD)[l];
-            const float4 uu = make_float4(beta * (vv.x - P.x), beta * (vv.y - P.y), beta * (vv.z - P.z),
-                                          beta * (vv.w - P.w));
-            const float4 o = m_fma4(kq, uu, R);
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int i = w + 8 * m;
-                const float a = aa[i], kk = ka[i];
-                s[m] = make_float4(fmaf(a, s[m].x, kk * uu.x), fmaf(a, s[m].y, kk * uu.y),
-                                   fmaf(a, s[m].z, kk * uu.z), fmaf(a, s[m].w, kk * uu.w));
-            }
-            if (w == 0) {
-                const float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
-                const float rinv = rsqrt_ftz(ss * (1.0f / kD) + rms_eps);
-                const float4 gw4 = reinterpret_cast<const float4 *>(sh_gw + t * kD)[l];
-                T *dst = out + row * D + (size_t)h * kD + 4 * l;
-                IO<T>::st(dst + 0, gw4.x * (o.x * rinv));
-                IO<T>::st(dst + 1, gw4.y * (o.y * rinv));
-                IO<T>::st(dst + 2, gw4.z * (o.z * rinv));
-                IO<T>::st(dst + 3, gw4.w * (o.w * rinv));
-            }
+            decode_token_step<T>(s, sh_ak + t * kD, sh_aq + t * kD, sh_a + t * kD, sh_k + t * kD, sh_v + t * kD,
+                                 sh_gw + t * kD, sbeta[t], kq, red, su, so, out + row * D + (size_t)h * kD, rms_eps,
+                                 w, l);
         }
         // the state after the run, and the new history (the last three raw inputs)
         float4 *S4 = reinterpret_cast<float4 *>(S_all + ((size_t)slot * H + h) * kD * kD);
 #pragma unroll
-        for (int m = 0; m < 16; ++m) st_stream(S4 + (w + 8 * m) * 32 + l, s[m]);
+        for (int m = 0; m < 16; ++m) st_stream(S4 + (16 * w + m) * 32 + l, s[m]);
         if (tid < kD) {
             T *tg_out = tail_all + (size_t)slot * 9 * D + (size_t)h * kD + tid;
 #pragma unroll
@@ -251,7 +212,7 @@ cudaError_t launch_multi_typed(const State &st, const kda_layer_params &p, const
     using L = MultiStage<T>;
     const kda_config_t &c = st.cfg;
     const int H = c.num_heads;
-    const size_t smem = 2 * (size_t)L::kBytes + 5 * KDA_DECODE_MAX_TOKENS * kD * 4 + 2 * 2 * 8 * 32 * 16 +
+    const size_t smem = 2 * (size_t)L::kBytes + 7 * KDA_DECODE_MAX_TOKENS * kD * 4 + 2 * kD * 4 + 2 * 8 * kD * 4 +
                         KDA_DECODE_MAX_TOKENS * 13 * 4 + 2 * 8;
     cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
