@@ -562,7 +562,7 @@ def run_kda(args):
         line["prefill"] = {
             "workload": f"prefill 1 sequence T={Tp}, 96 heads x 128, chunk 64, BF16 I/O",
             "value": Tp / (pre_ms / 1e3), "unit": "tokens/s", "ms": pre_ms, "reps": args.prefill_reps,
-            "gpu_launches_per_call": 4,
+            "gpu_launches_per_call": 3,  # chunk table, prep_tc, state_tc
             "roofline_tensor": {"bound": "tensor", "achieved": pre_tflops, "peak": peaks["bf16_tflops"],
                                 "unit": "TFLOP/s", "frac": pre_tflops / peaks["bf16_tflops"],
                                 "flop_per_call": pre_flop, "peak_note": src},
@@ -571,7 +571,7 @@ def run_kda(args):
         if args.only == "prefill":
             line["value"] = Tp / (pre_ms / 1e3)
             line["ms_per_step"] = pre_ms
-            line["gpu_launches"] = 4 * args.prefill_reps
+            line["gpu_launches"] = 3 * args.prefill_reps
     if args.only == "all":
         line["varlen"] = _time_varlen(K, args, cfg, params, gen, dev, stream)
     if rank == 0 and not args.no_cpu_baseline:
