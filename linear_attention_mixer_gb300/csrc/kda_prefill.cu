@@ -533,24 +533,23 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     if (tid < kC) sbeta[tid] = tid < n ? sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
 
     // 1. conv + SiLU (sliding window in registers) for stream px < 3, 2. the gates for px == 3;
-    //    thread (channel pc, stream px) walks all 64 rows, 32 at a time so that 32 independent
-    //    exponentials are in flight. Exponents are capped at 80 (the sigmoid is then below 2e-35
-    //    and the SiLU output tiny either way).
+    //    thread (channel pc, stream px) walks all 64 rows, 8 at a time. Exponents are capped at 80
+    //    (the sigmoid is then below 2e-35 and the SiLU output tiny either way).
     if (px < 3) {
         float *dst = Yq + px * (kC * kYS);  // Yq, Yk, Yv are consecutive: the stores stay shared
         const T *col = raw + (size_t)px * kRows * kD + pc;
         float h0 = IO<T>::ld(col), h1 = IO<T>::ld(col + kD), h2 = IO<T>::ld(col + 2 * kD);
 #pragma unroll 1
-        for (int r0 = 0; r0 < kC; r0 += 32) {
-            float cv[32];
+        for (int r0 = 0; r0 < kC; r0 += 8) {
+            float cv[8];
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const float xin = IO<T>::ld(col + (r0 + u + 3) * kD);
                 cv[u] = fmaf(p_w.x, h0, fmaf(p_w.y, h1, fmaf(p_w.z, h2, p_w.w * xin)));
                 h0 = h1; h1 = h2; h2 = xin;
             }
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-cv[u], 80.f)));
                 dst[(r0 + u) * kYS + pc] = r0 + u < n ? cv[u] * sg : 0.f;
             }
@@ -558,12 +557,12 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     } else {
         const T *col = raw + ((size_t)3 * kRows + 3) * kD + pc;
 #pragma unroll 1
-        for (int r0 = 0; r0 < kC; r0 += 32) {
-            float zz[32];
+        for (int r0 = 0; r0 < kC; r0 += 8) {
+            float zz[8];
 #pragma unroll
-            for (int u = 0; u < 32; ++u) zz[u] = IO<T>::ld(col + (r0 + u) * kD);
+            for (int u = 0; u < 8; ++u) zz[u] = IO<T>::ld(col + (r0 + u) * kD);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[u] + p_dt), 80.f)));
                 GL[(r0 + u) * kYS + pc] = r0 + u < n ? gmin * sg : 0.f;  // gk; 0 (no decay) past the chunk
             }
@@ -609,44 +608,39 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             good &= mbar_wait_bounded(bars + 1, 0u, kTcWaitLimit);  // half 0 has read the tiles
             tc::fence_after_sync();
         }
-        // items 0..511: left rows r (k) and 64 + r (q), factor exp(G_r - G_n), n = 16 (r / 16);
-        // items 512..1791: right rows, segment R, row i < 16 (R + 1): k_i o exp(G_nR - G_i)
-        // (<= 1 for i <= nR, <= e^75 on the diagonal block)
-        for (int u = tid; u < kC * 8 + kApN * 8; u += 512) {
-            if (u < kC * 8) {
-                const int r = (u & 7) | ((u >> 6) << 3), cl = 8 * ((u >> 3) & 7), c0 = c_h + cl;
-                const int nR = r & ~(kBlk - 1);
-                float kv[8], qv[8], gr[8], gn[8], kl[8], ql[8];
-                ld8f(Yk + r * kYS + c0, kv);
-                ld8f(Yq + r * kYS + c0, qv);
-                ld8f(GL + r * kYS + c0, gr);
-                ld8f(GL + nR * kYS + c0, gn);
+        // item (row r, 8-channel group): k_r, q_r and G_r are read once; the item writes the left
+        // rows r (k) and 64 + r (q) with factor exp(G_r - G_n), n = 16 (r / 16), and row r of every
+        // right segment R >= r / 16: k_r o exp(G_16R - G_r) (<= 1 for R > r / 16, <= e^75 on the
+        // diagonal block)
+        {
+            const int u = tid;  // 512 items, one per thread
+            const int r = (u & 7) | ((u >> 6) << 3), cl = 8 * ((u >> 3) & 7), c0 = c_h + cl;
+            const int b = r >> 4;
+            float kv[8], qv[8], gr[8], gn[8], kl[8], ql[8];
+            ld8f(Yk + r * kYS + c0, kv);
+            ld8f(Yq + r * kYS + c0, qv);
+            ld8f(GL + r * kYS + c0, gr);
+            ld8f(GL + kBlk * b * kYS + c0, gn);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float f = exp_ftz(gr[j] - gn[j]);
-                    kl[j] = kv[j] * f;
-                    ql[j] = qv[j] * f;
-                }
-                uint4 hi, lo;
-                split8(kl, hi, lo);
-                st16(tLh + tc::kmajor_off(r, cl, kD / 2), hi);
-                st16(tLl + tc::kmajor_off(r, cl, kD / 2), lo);
-                split8(ql, hi, lo);
-                st16(tLh + tc::kmajor_off(kC + r, cl, kD / 2), hi);
-                st16(tLl + tc::kmajor_off(kC + r, cl, kD / 2), lo);
-            } else {
-                const int w2 = u - kC * 8;
-                const int row = (w2 & 7) | ((w2 >> 6) << 3), cl = 8 * ((w2 >> 3) & 7), c0 = c_h + cl;
-                const int R = row < 16 ? 0 : (row < 48 ? 1 : (row < 96 ? 2 : 3));
-                const int i = row - 8 * R * (R + 1), nR = kBlk * R;
-                float kv[8], gi[8], gn[8], kx[8];
-                ld8f(Yk + i * kYS + c0, kv);
-                ld8f(GL + i * kYS + c0, gi);
-                ld8f(GL + nR * kYS + c0, gn);
+            for (int j = 0; j < 8; ++j) {
+                const float f = exp_ftz(gr[j] - gn[j]);
+                kl[j] = kv[j] * f;
+                ql[j] = qv[j] * f;
+            }
+            uint4 hi, lo;
+            split8(kl, hi, lo);
+            st16(tLh + tc::kmajor_off(r, cl, kD / 2), hi);
+            st16(tLl + tc::kmajor_off(r, cl, kD / 2), lo);
+            split8(ql, hi, lo);
+            st16(tLh + tc::kmajor_off(kC + r, cl, kD / 2), hi);
+            st16(tLl + tc::kmajor_off(kC + r, cl, kD / 2), lo);
+            for (int R = b; R < kC / kBlk; ++R) {  // warp-uniform: a warp's 8 rows share a block
+                if (R != b) ld8f(GL + kBlk * R * kYS + c0, gn);
+                float kx[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) kx[j] = kv[j] * exp_ftz(gn[j] - gi[j]);
-                uint4 hi, lo;
+                for (int j = 0; j < 8; ++j) kx[j] = kv[j] * exp_ftz(gn[j] - gr[j]);
                 split8(kx, hi, lo);
+                const int row = 8 * R * (R + 1) + r;
                 st16(tRh + tc::kmajor_off(row, cl, kD / 2), hi);
                 st16(tRl + tc::kmajor_off(row, cl, kD / 2), lo);
             }
