@@ -555,7 +555,10 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             }
         }
     } else {
+        // the gate thread of channel pc also carries G_r = sum_{t<=r} gk_t down the rows (gk = 0,
+        // no decay, past the chunk, so G stays at G_last there)
         const T *col = raw + ((size_t)3 * kRows + 3) * kD + pc;
+        float acc = 0.f;
 #pragma unroll 1
         for (int r0 = 0; r0 < kC; r0 += 8) {
             float zz[8];
@@ -564,31 +567,23 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[u] + p_dt), 80.f)));
-                GL[(r0 + u) * kYS + pc] = r0 + u < n ? gmin * sg : 0.f;  // gk; 0 (no decay) past the chunk
+                acc += r0 + u < n ? gmin * sg : 0.f;
+                GL[(r0 + u) * kYS + pc] = acc;
             }
         }
     }
     __syncthreads();
-    // 2b. G_r = sum_{t<=r} gk_t per channel (warps 0..3), while warps 4..15 take the L2 norms
-    if (tid < kD) {
-        float acc = 0.f;
-#pragma unroll 16
-        for (int r = 0; r < kC; ++r) {
-            acc += GL[r * kYS + tid];
-            GL[r * kYS + tid] = acc;
-        }
-    } else {
-        for (int r = warp - 4; r < kC; r += 12) {
-            float4 a = reinterpret_cast<float4 *>(Yq + r * kYS)[lane];
-            float4 b = reinterpret_cast<float4 *>(Yk + r * kYS)[lane];
-            const float sq = warp_sum(a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w);
-            const float sk = warp_sum(b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w);
-            const float rq = q_scale / sqrtf(sq + l2_eps), rk = 1.0f / sqrtf(sk + l2_eps);
-            a.x *= rq; a.y *= rq; a.z *= rq; a.w *= rq;
-            b.x *= rk; b.y *= rk; b.z *= rk; b.w *= rk;
-            reinterpret_cast<float4 *>(Yq + r * kYS)[lane] = a;
-            reinterpret_cast<float4 *>(Yk + r * kYS)[lane] = b;
-        }
+    // 2b. the L2 norms of q and k, rows r = warp + 16 m
+    for (int r = warp; r < kC; r += 16) {
+        float4 a = reinterpret_cast<float4 *>(Yq + r * kYS)[lane];
+        float4 b = reinterpret_cast<float4 *>(Yk + r * kYS)[lane];
+        const float sq = warp_sum(a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w);
+        const float sk = warp_sum(b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w);
+        const float rq = q_scale * rsqrt_ftz(sq + l2_eps), rk = rsqrt_ftz(sk + l2_eps);
+        a.x *= rq; a.y *= rq; a.z *= rq; a.w *= rq;
+        b.x *= rk; b.y *= rk; b.z *= rk; b.w *= rk;
+        reinterpret_cast<float4 *>(Yq + r * kYS)[lane] = a;
+        reinterpret_cast<float4 *>(Yk + r * kYS)[lane] = b;
     }
     __syncthreads();
 
