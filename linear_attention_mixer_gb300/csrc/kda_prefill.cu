@@ -379,6 +379,25 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 // Shared memory: FP32 [64][132] arrays (rows padded against bank conflicts) for q^, k^, v and
 // G, then one reused region (raw inputs -> A/P tiles -> B_lo, T tile, A matrix); after the A/P
 // phase the q^ array holds B_hi, and after the B build the v and G arrays hold T and scratch.
+// sum_{k < N} a[k] (b[k pb], ..., b[k pb + 3]): a row of one matrix times a 4-column strip of
+// another, both in shared memory, with two interleaved accumulators
+template <int N>
+__device__ __forceinline__ float4 strip4(const float *a, const float *b, int pb)
+{
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+#pragma unroll
+    for (int k = 0; k < N; k += 2) {
+        const float a0 = a[k], a1 = a[k + 1];
+        const float4 t0 = *reinterpret_cast<const float4 *>(b + k * pb);
+        const float4 t1 = *reinterpret_cast<const float4 *>(b + (k + 1) * pb);
+        s0.x = fmaf(a0, t0.x, s0.x); s0.y = fmaf(a0, t0.y, s0.y);
+        s0.z = fmaf(a0, t0.z, s0.z); s0.w = fmaf(a0, t0.w, s0.w);
+        s1.x = fmaf(a1, t1.x, s1.x); s1.y = fmaf(a1, t1.y, s1.y);
+        s1.z = fmaf(a1, t1.z, s1.z); s1.w = fmaf(a1, t1.w, s1.w);
+    }
+    return make_float4(s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w);
+}
+
 constexpr int kYS = kD + 4;   // padded FP32 row
 constexpr int kMS = kC + 4;   // row pitch of the FP32 A / T matrices (16-byte aligned rows)
 constexpr int kPtY = 73728;   // reused region
@@ -573,17 +592,31 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
     }
     __syncthreads();
-    // 2b. the L2 norms of q and k, rows r = warp + 16 m
-    for (int r = warp; r < kC; r += 16) {
-        float4 a = reinterpret_cast<float4 *>(Yq + r * kYS)[lane];
-        float4 b = reinterpret_cast<float4 *>(Yk + r * kYS)[lane];
-        const float sq = warp_sum(a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w);
-        const float sk = warp_sum(b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w);
+    // 2b. the L2 norms of q and k: warp w takes rows 4 w .. 4 w + 3, 8 lanes a row, lane j of a
+    //     row the channels 4 j + 32 i (i < 4), so each quarter warp reads 128 contiguous bytes
+    {
+        const int r = 4 * warp + (lane >> 3), j = lane & 7;
+        float4 *qr = reinterpret_cast<float4 *>(Yq + r * kYS) + j, *kr = reinterpret_cast<float4 *>(Yk + r * kYS) + j;
+        float4 a[4], b[4];
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            a[i] = qr[8 * i];
+            b[i] = kr[8 * i];
+            sq += a[i].x * a[i].x + a[i].y * a[i].y + a[i].z * a[i].z + a[i].w * a[i].w;
+            sk += b[i].x * b[i].x + b[i].y * b[i].y + b[i].z * b[i].z + b[i].w * b[i].w;
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+            sk += __shfl_xor_sync(0xFFFFFFFFu, sk, o);
+        }
         const float rq = q_scale * rsqrt_ftz(sq + l2_eps), rk = rsqrt_ftz(sk + l2_eps);
-        a.x *= rq; a.y *= rq; a.z *= rq; a.w *= rq;
-        b.x *= rk; b.y *= rk; b.z *= rk; b.w *= rk;
-        reinterpret_cast<float4 *>(Yq + r * kYS)[lane] = a;
-        reinterpret_cast<float4 *>(Yk + r * kYS)[lane] = b;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            qr[8 * i] = make_float4(a[i].x * rq, a[i].y * rq, a[i].z * rq, a[i].w * rq);
+            kr[8 * i] = make_float4(b[i].x * rk, b[i].y * rk, b[i].z * rk, b[i].w * rk);
+        }
     }
     __syncthreads();
 
@@ -743,11 +776,17 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
     }
     __syncthreads();
-    // 6. T = (I + A)^-1 into Tf (the v array; rows of pitch kMS), blocked by 16:
-    //    diagonal blocks T_RR = (I + A_RR)^-1 by forward substitution (threads 0..63, one column
-    //    each) while the other threads clear the blocks above the diagonal; then for block rows
-    //    R = 1..3, Y_S = sum_{K=S}^{R-1} A_RK T_KS and T_RS = -T_RR Y_S for S < R.
-    float *Tf = Yv, *Ys = GL;  // Ys: [3][16][16] scratch
+    // 6. T = (I + A)^-1 into Tf (the v array; rows of pitch kMS), by blocks of 16 and a
+    //    two-level merge. Diagonal blocks T_RR = (I + A_RR)^-1 by forward substitution (threads
+    //    0..63, one column each) while the other threads clear the blocks above the diagonal.
+    //    With X = rows/columns 0..31 and Y = 32..63, T_YX = -T_YY A_YX T_XX, and inside each
+    //    half T_10 = -T_11 A_10 T_00, T_32 = -T_33 A_32 T_22. Three phases:
+    //      1. Y1_p = A_(2p+1)(2p) T_(2p)(2p) (p = 0, 1), Z0 = A_Y0 T_00, Z1 = A_Y1 T_11;
+    //      2. T_10 = -T_11 Y1_0, T_32 = -T_33 Y1_1, and Y2 = A_YX T_XX, whose left half is
+    //         Z0 + A_Y1 T_10 = Z0 - Z1 Y1_0 and whose right half is Z1;
+    //      3. T_YX = -T_YY Y2.
+    float *Tf = Yv, *Y1 = GL, *Y2 = GL + 2 * kBlk * kBlk;  // Y1: [2][16][16], Y2: [32][kY2]
+    constexpr int kY2 = 36;
     if (tid < kC) {
         const int R = tid >> 4, j = tid & (kBlk - 1), nR = kBlk * R;
         float x[kBlk];
@@ -760,8 +799,10 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 else s0 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s0);
             }
             x[r] = r == j ? 1.f : (r < j ? 0.f : s0 + s1);
-            Tf[(nR + r) * kMS + nR + j] = x[r];
         }
+        // stored after the loop, so that no shared store sits between the loads of the rows
+#pragma unroll
+        for (int r = 0; r < kBlk; ++r) Tf[(nR + r) * kMS + nR + j] = x[r];
     } else {
         for (int u = tid - kC; u < kC * kC; u += 512 - kC) {
             const int r = u >> 6, c = u & (kC - 1);
@@ -769,49 +810,42 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
     }
     __syncthreads();
-    for (int R = 1; R < kC / kBlk; ++R) {
-        const int nR = kBlk * R;
-        // one 1 x 4 strip (S, a, b0..b0+3) per thread (at most 192 strips)
-        const int S = tid >> 6, a = (tid >> 2) & (kBlk - 1), b0 = 4 * (tid & 3);
-        if (tid < R * 64) {
-            float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-            for (int K = S; K < R; ++K) {
-                const float *Ar = Mm + (nR + a) * kMS + kBlk * K;
-                const float *Tc = Tf + (kBlk * K) * kMS + kBlk * S + b0;
-#pragma unroll
-                for (int kk = 0; kk < kBlk; kk += 2) {
-                    const float a0 = Ar[kk], a1 = Ar[kk + 1];
-                    const float4 t0 = *reinterpret_cast<const float4 *>(Tc + kk * kMS);
-                    const float4 t1 = *reinterpret_cast<const float4 *>(Tc + (kk + 1) * kMS);
-                    s0.x = fmaf(a0, t0.x, s0.x); s0.y = fmaf(a0, t0.y, s0.y);
-                    s0.z = fmaf(a0, t0.z, s0.z); s0.w = fmaf(a0, t0.w, s0.w);
-                    s1.x = fmaf(a1, t1.x, s1.x); s1.y = fmaf(a1, t1.y, s1.y);
-                    s1.z = fmaf(a1, t1.z, s1.z); s1.w = fmaf(a1, t1.w, s1.w);
-                }
-            }
-            *reinterpret_cast<float4 *>(Ys + S * kBlk * kBlk + a * kBlk + b0) =
-                make_float4(s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w);
-        }
-        __syncthreads();
-        if (tid < R * 64) {
-            const float *Tr = Tf + (nR + a) * kMS + nR;
-            const float *Yc = Ys + S * kBlk * kBlk + b0;
-            float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-#pragma unroll
-            for (int kk = 0; kk < kBlk; kk += 2) {
-                const float a0 = Tr[kk], a1 = Tr[kk + 1];
-                const float4 y0 = *reinterpret_cast<const float4 *>(Yc + kk * kBlk);
-                const float4 y1 = *reinterpret_cast<const float4 *>(Yc + (kk + 1) * kBlk);
-                s0.x = fmaf(a0, y0.x, s0.x); s0.y = fmaf(a0, y0.y, s0.y);
-                s0.z = fmaf(a0, y0.z, s0.z); s0.w = fmaf(a0, y0.w, s0.w);
-                s1.x = fmaf(a1, y1.x, s1.x); s1.y = fmaf(a1, y1.y, s1.y);
-                s1.z = fmaf(a1, y1.z, s1.z); s1.w = fmaf(a1, y1.w, s1.w);
-            }
-            *reinterpret_cast<float4 *>(Tf + (nR + a) * kMS + kBlk * S + b0) =
-                make_float4(-(s0.x + s1.x), -(s0.y + s1.y), -(s0.z + s1.z), -(s0.w + s1.w));
-        }
-        __syncthreads();
+    // phase 1: one 1 x 4 strip per thread (threads 0..383)
+    if (tid < 128) {
+        const int p = tid >> 6, a = (tid >> 2) & (kBlk - 1), b0 = 4 * (tid & 3), o = 2 * kBlk * p;
+        const float4 y = strip4<kBlk>(Mm + (o + kBlk + a) * kMS + o, Tf + o * kMS + o + b0, kMS);
+        *reinterpret_cast<float4 *>(Y1 + p * kBlk * kBlk + a * kBlk + b0) = y;
+    } else if (tid < 384) {
+        const int t = tid - 128, hz = t >> 7, a = (t >> 2) & 31, b0 = 4 * (t & 3), o = kBlk * hz;
+        const float4 z = strip4<kBlk>(Mm + (2 * kBlk + a) * kMS + o, Tf + o * kMS + o + b0, kMS);
+        *reinterpret_cast<float4 *>(Y2 + a * kY2 + o + b0) = z;
     }
+    __syncthreads();
+    // phase 2 (threads 0..255); each thread overwrites only its own strip of Z0
+    if (tid < 128) {
+        const int p = tid >> 6, a = (tid >> 2) & (kBlk - 1), b0 = 4 * (tid & 3), o = 2 * kBlk * p;
+        const float4 y = strip4<kBlk>(Tf + (o + kBlk + a) * kMS + o + kBlk, Y1 + p * kBlk * kBlk + b0, kBlk);
+        *reinterpret_cast<float4 *>(Tf + (o + kBlk + a) * kMS + o + b0) = make_float4(-y.x, -y.y, -y.z, -y.w);
+    } else if (tid < 256) {
+        const int t = tid - 128, a = t >> 2, b0 = 4 * (t & 3);
+        const float4 y = strip4<kBlk>(Y2 + a * kY2 + kBlk, Y1 + b0, kBlk);
+        float4 *z = reinterpret_cast<float4 *>(Y2 + a * kY2 + b0);
+        const float4 z0 = *z;
+        *z = make_float4(z0.x - y.x, z0.y - y.y, z0.z - y.z, z0.w - y.w);
+    }
+    __syncthreads();
+    // phase 3 (threads 0..255): rows 32 + a; the rows of block 3 also take T_32
+    if (tid < 256) {
+        const int a = 8 * (warp & 3) + (lane >> 2), c0 = 4 * (4 * (warp >> 2) + (lane & 3));
+        const float *Tr = Tf + (2 * kBlk + a) * kMS + 2 * kBlk;
+        float4 y = strip4<kBlk>(Tr, Y2 + c0, kY2);
+        if ((warp & 3) >= 2) {  // warp-uniform
+            const float4 y2 = strip4<kBlk>(Tr + kBlk, Y2 + kBlk * kY2 + c0, kY2);
+            y = make_float4(y.x + y2.x, y.y + y2.y, y.z + y2.z, y.w + y2.w);
+        }
+        *reinterpret_cast<float4 *>(Tf + (2 * kBlk + a) * kMS + c0) = make_float4(-y.x, -y.y, -y.z, -y.w);
+    }
+    __syncthreads();
     {   // T -> BF16 hi (tile rows 0..63) and lo (rows 64..127), one 8-column group per thread
         const int r = (tid & 7) | ((tid >> 6) << 3), c0 = 8 * ((tid >> 3) & 7);
         float tv[8];
