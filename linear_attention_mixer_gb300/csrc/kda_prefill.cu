@@ -379,23 +379,56 @@ prep_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
 // Shared memory: FP32 [64][132] arrays (rows padded against bank conflicts) for q^, k^, v and
 // G, then one reused region (raw inputs -> A/P tiles -> B_lo, T tile, A matrix); after the A/P
 // phase the q^ array holds B_hi, and after the B build the v and G arrays hold T and scratch.
-// sum_{k < N} a[k] (b[k pb], ..., b[k pb + 3]): a row of one matrix times a 4-column strip of
-// another, both in shared memory, with two interleaved accumulators
-template <int N>
-__device__ __forceinline__ float4 strip4(const float *a, const float *b, int pb)
+// c[i][j] += sum_{k < 4 G} a[i pa + k] b[k pb + j] (i < 2, j < 4): a 2 x 4 register tile of a
+// product of two FP32 matrices in shared memory, a read 4 k at a time as float4 along its rows
+template <int G>
+__device__ __forceinline__ void tile24(float (&c)[2][4], const float *a, int pa, const float *b, int pb)
 {
-    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
 #pragma unroll
-    for (int k = 0; k < N; k += 2) {
-        const float a0 = a[k], a1 = a[k + 1];
-        const float4 t0 = *reinterpret_cast<const float4 *>(b + k * pb);
-        const float4 t1 = *reinterpret_cast<const float4 *>(b + (k + 1) * pb);
-        s0.x = fmaf(a0, t0.x, s0.x); s0.y = fmaf(a0, t0.y, s0.y);
-        s0.z = fmaf(a0, t0.z, s0.z); s0.w = fmaf(a0, t0.w, s0.w);
-        s1.x = fmaf(a1, t1.x, s1.x); s1.y = fmaf(a1, t1.y, s1.y);
-        s1.z = fmaf(a1, t1.z, s1.z); s1.w = fmaf(a1, t1.w, s1.w);
+    for (int g = 0; g < G; ++g) {
+        const float4 a0 = *reinterpret_cast<const float4 *>(a + 4 * g);
+        const float4 a1 = *reinterpret_cast<const float4 *>(a + pa + 4 * g);
+        float4 bv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bv[j] = *reinterpret_cast<const float4 *>(b + (4 * g + j) * pb);
+        const float x0[4] = {a0.x, a0.y, a0.z, a0.w}, x1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            c[0][0] = fmaf(x0[j], bv[j].x, c[0][0]); c[0][1] = fmaf(x0[j], bv[j].y, c[0][1]);
+            c[0][2] = fmaf(x0[j], bv[j].z, c[0][2]); c[0][3] = fmaf(x0[j], bv[j].w, c[0][3]);
+            c[1][0] = fmaf(x1[j], bv[j].x, c[1][0]); c[1][1] = fmaf(x1[j], bv[j].y, c[1][1]);
+            c[1][2] = fmaf(x1[j], bv[j].z, c[1][2]); c[1][3] = fmaf(x1[j], bv[j].w, c[1][3]);
+        }
     }
-    return make_float4(s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w);
+}
+
+// 2 x 4 tile rows r, r + 1, columns c .. c + 3, times sg, to the BF16 T tile: hi parts in rows
+// r, r + 1 and lo parts in rows 64 + r, 64 + r + 1 (8 bytes per row)
+__device__ __forceinline__ void put24_split(unsigned char *tile, int r, int c, const float (&v)[2][4], float sg)
+{
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        uint32_t h[2], l[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float x0 = sg * v[i][2 * e], x1 = sg * v[i][2 * e + 1];
+            const __nv_bfloat162 p = __floats2bfloat162_rn(x0, x1);
+            const uint32_t u = *reinterpret_cast<const uint32_t *>(&p);
+            h[e] = u;
+            const __nv_bfloat162 q = __floats2bfloat162_rn(x0 - __uint_as_float(u << 16), x1 - __uint_as_float(u & 0xFFFF0000u));
+            l[e] = *reinterpret_cast<const uint32_t *>(&q);
+        }
+        *reinterpret_cast<uint2 *>(tile + tc::kmajor_off(r + i, c, kC)) = make_uint2(h[0], h[1]);
+        *reinterpret_cast<uint2 *>(tile + tc::kmajor_off(kC + r + i, c, kC)) = make_uint2(l[0], l[1]);
+    }
+}
+
+// a 2 x 4 tile times sg to dst (row pitch pd), one float4 per row
+__device__ __forceinline__ void put24(float *dst, int pd, const float (&c)[2][4], float sg)
+{
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        *reinterpret_cast<float4 *>(dst + i * pd) = make_float4(sg * c[i][0], sg * c[i][1], sg * c[i][2], sg * c[i][3]);
 }
 
 constexpr int kYS = kD + 4;   // padded FP32 row
@@ -408,9 +441,10 @@ constexpr int kApN = 160;
 constexpr int kApLh = 0, kApLl = 16384, kApRh = 32768, kApRl = 32768 + kApN * 128;
 // solve phase: B_lo [256][64], T tile [hi rows 0..63, lo rows 64..127][64] (a descriptor
 // starting at row 64 covers rows 64..191, ending 24 KB into the tile) and the FP32 A matrix.
-constexpr int kPtBl = 0, kPtT = 32768, kPtM = 49152;
+// The diagonal blocks T_RR of the inverse follow M, as [4][16][kTD] FP32.
+constexpr int kPtBl = 0, kPtT = 32768, kPtM = 49152, kTD = 20, kPtD = kPtM + kC * kMS * 4;
 static_assert(kApRl + kApN * 128 <= kPtY, "A/P tiles");
-static_assert(kPtT + 24576 <= kPtY && kPtM + kC * kMS * 4 <= kPtY, "solve tiles");
+static_assert(kPtT + 24576 <= kPtY && kPtD + 4 * 16 * kTD * 4 <= kPtY, "solve tiles");
 static_assert(256 * kC * 2 <= kC * kYS * 4, "B_hi must fit in the q^ array");
 constexpr int kPrepTcSmem = 4 * kC * kYS * 4 + kPtY + kC * 4 + 64;
 
@@ -714,9 +748,10 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     tc::fence_after_sync();
 
     // 5. warps 0..7 read A and P back: A (beta and the strict mask applied) to the FP32 matrix
-    //    M, P (inclusive mask) straight to the chunk block. Then all warps build the solve operands: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the
-    //    64 chunk rows, hi parts in the q^ array (free now), lo parts in the region.
-    float *Mm = reinterpret_cast<float *>(Y + kPtM);
+    //    M, P (inclusive mask) straight to the chunk block. Then all warps build the solve
+    //    operands: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the 64 chunk
+    //    rows, hi parts in the q^ array (free now), lo parts in the region.
+    float *Mm = reinterpret_cast<float *>(Y + kPtM), *TD = reinterpret_cast<float *>(Y + kPtD);
     unsigned char *tBh = reinterpret_cast<unsigned char *>(Yq), *tBl = Y + kPtBl, *tT = Y + kPtT;
     if (warp < 8) {
         // lane quarter qd holds left rows 32 qd .. +31 (k rows for qd < 2, q rows after);
@@ -776,17 +811,22 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
     }
     __syncthreads();
-    // 6. T = (I + A)^-1 into Tf (the v array; rows of pitch kMS), by blocks of 16 and a
-    //    two-level merge. Diagonal blocks T_RR = (I + A_RR)^-1 by forward substitution (threads
-    //    0..63, one column each) while the other threads clear the blocks above the diagonal.
-    //    With X = rows/columns 0..31 and Y = 32..63, T_YX = -T_YY A_YX T_XX, and inside each
-    //    half T_10 = -T_11 A_10 T_00, T_32 = -T_33 A_32 T_22. Three phases:
-    //      1. Y1_p = A_(2p+1)(2p) T_(2p)(2p) (p = 0, 1), Z0 = A_Y0 T_00, Z1 = A_Y1 T_11;
-    //      2. T_10 = -T_11 Y1_0, T_32 = -T_33 Y1_1, and Y2 = A_YX T_XX, whose left half is
-    //         Z0 + A_Y1 T_10 = Z0 - Z1 Y1_0 and whose right half is Z1;
+    // 6. T = (I + A)^-1 as BF16 hi and lo parts in the T tile, by blocks of 16 and a two-level
+    //    merge. Phase 0: the diagonal blocks TD, T_RR = (I + A_RR)^-1, by forward substitution
+    //    (threads 0..63, one column each) while threads 64..447 write the zero blocks above the
+    //    diagonal (columns c >= 16 (r / 16 + 1)) to the tile. With X = rows/columns 0..31 and Y = 32..63,
+    //    T_YX = -T_YY A_YX T_XX, and inside each half T_10 = -T_11 A_10 T_00,
+    //    T_32 = -T_33 A_32 T_22. Three phases:
+    //      1. Y1_p = A_(2p+1)(2p) T_(2p)(2p) (p = 0, 1), Z0 = A_Y0 T_00, Z1 = A_Y1 T_11, and
+    //         the diagonal blocks to the tile;
+    //      2. T_10 = -T_11 Y1_0, T_32 = -T_33 Y1_1 (also kept in FP32), and Y2 = A_YX T_XX,
+    //         whose left half is Z0 + A_Y1 T_10 = Z0 - Z1 Y1_0 and whose right half is Z1;
     //      3. T_YX = -T_YY Y2.
-    float *Tf = Yv, *Y1 = GL, *Y2 = GL + 2 * kBlk * kBlk;  // Y1: [2][16][16], Y2: [32][kY2]
+    //    Each product is tiled 2 x 4 per thread (rows 2 rp, 2 rp + 1; columns 4 ct .. 4 ct + 3);
+    //    the 8 lanes of a quarter warp share their rows and take consecutive column tiles.
+    float *T32 = Yv, *Y1 = GL, *Y2 = GL + 2 * kBlk * kBlk;  // T32: [16][kMS], Y1: [2][16][16], Y2: [32][kY2]
     constexpr int kY2 = 36;
+    // phase 0
     if (tid < kC) {
         const int R = tid >> 4, j = tid & (kBlk - 1), nR = kBlk * R;
         float x[kBlk];
@@ -802,58 +842,66 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
         // stored after the loop, so that no shared store sits between the loads of the rows
 #pragma unroll
-        for (int r = 0; r < kBlk; ++r) Tf[(nR + r) * kMS + nR + j] = x[r];
-    } else {
-        for (int u = tid - kC; u < kC * kC; u += 512 - kC) {
-            const int r = u >> 6, c = u & (kC - 1);
-            if (c >= kBlk * (r / kBlk + 1)) Tf[r * kMS + c] = 0.f;
-        }
+        for (int r = 0; r < kBlk; ++r) TD[(nR + r) * kTD + j] = x[r];
+    } else if (tid < kC + 384) {
+        const int u = (tid - kC) % 192, lo = (tid - kC) / 192;  // 192 groups of 8 columns per part
+        const int r = u < 96 ? u / 6 : (u < 160 ? kBlk + (u - 96) / 4 : 2 * kBlk + (u - 160) / 2);
+        const int g = u < 96 ? 2 + u % 6 : (u < 160 ? 4 + (u - 96) % 4 : 6 + (u - 160) % 2);
+        st16(tT + tc::kmajor_off(lo * kC + r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
     }
     __syncthreads();
-    // phase 1: one 1 x 4 strip per thread (threads 0..383)
-    if (tid < 128) {
-        const int p = tid >> 6, a = (tid >> 2) & (kBlk - 1), b0 = 4 * (tid & 3), o = 2 * kBlk * p;
-        const float4 y = strip4<kBlk>(Mm + (o + kBlk + a) * kMS + o, Tf + o * kMS + o + b0, kMS);
-        *reinterpret_cast<float4 *>(Y1 + p * kBlk * kBlk + a * kBlk + b0) = y;
-    } else if (tid < 384) {
-        const int t = tid - 128, hz = t >> 7, a = (t >> 2) & 31, b0 = 4 * (t & 3), o = kBlk * hz;
-        const float4 z = strip4<kBlk>(Mm + (2 * kBlk + a) * kMS + o, Tf + o * kMS + o + b0, kMS);
-        *reinterpret_cast<float4 *>(Y2 + a * kY2 + o + b0) = z;
-    }
-    __syncthreads();
-    // phase 2 (threads 0..255); each thread overwrites only its own strip of Z0
-    if (tid < 128) {
-        const int p = tid >> 6, a = (tid >> 2) & (kBlk - 1), b0 = 4 * (tid & 3), o = 2 * kBlk * p;
-        const float4 y = strip4<kBlk>(Tf + (o + kBlk + a) * kMS + o + kBlk, Y1 + p * kBlk * kBlk + b0, kBlk);
-        *reinterpret_cast<float4 *>(Tf + (o + kBlk + a) * kMS + o + b0) = make_float4(-y.x, -y.y, -y.z, -y.w);
-    } else if (tid < 256) {
-        const int t = tid - 128, a = t >> 2, b0 = 4 * (t & 3);
-        const float4 y = strip4<kBlk>(Y2 + a * kY2 + kBlk, Y1 + b0, kBlk);
-        float4 *z = reinterpret_cast<float4 *>(Y2 + a * kY2 + b0);
-        const float4 z0 = *z;
-        *z = make_float4(z0.x - y.x, z0.y - y.y, z0.z - y.z, z0.w - y.w);
-    }
-    __syncthreads();
-    // phase 3 (threads 0..255): rows 32 + a; the rows of block 3 also take T_32
-    if (tid < 256) {
-        const int a = 8 * (warp & 3) + (lane >> 2), c0 = 4 * (4 * (warp >> 2) + (lane & 3));
-        const float *Tr = Tf + (2 * kBlk + a) * kMS + 2 * kBlk;
-        float4 y = strip4<kBlk>(Tr, Y2 + c0, kY2);
-        if ((warp & 3) >= 2) {  // warp-uniform
-            const float4 y2 = strip4<kBlk>(Tr + kBlk, Y2 + kBlk * kY2 + c0, kY2);
-            y = make_float4(y.x + y2.x, y.y + y2.y, y.z + y2.z, y.w + y2.w);
-        }
-        *reinterpret_cast<float4 *>(Tf + (2 * kBlk + a) * kMS + c0) = make_float4(-y.x, -y.y, -y.z, -y.w);
-    }
-    __syncthreads();
-    {   // T -> BF16 hi (tile rows 0..63) and lo (rows 64..127), one 8-column group per thread
-        const int r = (tid & 7) | ((tid >> 6) << 3), c0 = 8 * ((tid >> 3) & 7);
+    // phase 1 (threads 0..319)
+    if (tid < 64) {
+        const int p = tid >> 5, rp = (tid >> 2) & 7, ct = tid & 3, o = 2 * kBlk * p;
+        float c[2][4] = {};
+        tile24<kBlk / 4>(c, Mm + (o + kBlk + 2 * rp) * kMS + o, kMS, TD + o * kTD + 4 * ct, kTD);
+        put24(Y1 + p * kBlk * kBlk + 2 * rp * kBlk + 4 * ct, kBlk, c, 1.f);
+    } else if (tid < 192) {
+        const int t = tid - 64, rp = t >> 3, ct = t & 7, o = kBlk * (ct >> 2);
+        float c[2][4] = {};
+        tile24<kBlk / 4>(c, Mm + (2 * kBlk + 2 * rp) * kMS + o, kMS, TD + o * kTD + 4 * (ct & 3), kTD);
+        put24(Y2 + 2 * rp * kY2 + 4 * ct, kY2, c, 1.f);
+    } else if (tid < 320) {
+        const int t = tid - 192, R = t >> 5, r = kBlk * R + ((t >> 1) & (kBlk - 1)), g = t & 1;
         float tv[8];
-        ld8f(Tf + r * kMS + c0, tv);
+        ld8f(TD + r * kTD + 8 * g, tv);
         uint4 hi, lo;
         split8(tv, hi, lo);
-        st16(tT + tc::kmajor_off(r, c0, kC), hi);
-        st16(tT + tc::kmajor_off(kC + r, c0, kC), lo);
+        st16(tT + tc::kmajor_off(r, kBlk * R + 8 * g, kC), hi);
+        st16(tT + tc::kmajor_off(kC + r, kBlk * R + 8 * g, kC), lo);
+    }
+    __syncthreads();
+    // phase 2 (threads 0..127); each thread overwrites only its own tile of Z0
+    if (tid < 64) {
+        const int p = tid >> 5, rp = (tid >> 2) & 7, ct = tid & 3, o = 2 * kBlk * p;
+        float c[2][4] = {};
+        tile24<kBlk / 4>(c, TD + (o + kBlk + 2 * rp) * kTD, kTD, Y1 + p * kBlk * kBlk + 4 * ct, kBlk);
+        put24_split(tT, o + kBlk + 2 * rp, o + 4 * ct, c, -1.f);
+        if (p) put24(T32 + 2 * rp * kMS + 4 * ct, kMS, c, -1.f);
+    } else if (tid < 128) {
+        const int t = tid - 64, rp = t >> 2, ct = t & 3;
+        float c[2][4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float4 z = *reinterpret_cast<const float4 *>(Y2 + (2 * rp + i) * kY2 + 4 * ct);
+            c[i][0] = -z.x; c[i][1] = -z.y; c[i][2] = -z.z; c[i][3] = -z.w;
+        }
+        tile24<kBlk / 4>(c, Y2 + 2 * rp * kY2 + kBlk, kY2, Y1 + 4 * ct, kBlk);
+        put24(Y2 + 2 * rp * kY2 + 4 * ct, kY2, c, -1.f);
+    }
+    __syncthreads();
+    // phase 3 (threads 0..127): rows 32 + 2 rp (+1); T_YY's rows are [T_22 0] for warps 0, 1
+    // and [T_32 T_33] for warps 2, 3
+    if (tid < 128) {
+        const int rp = tid >> 3, ct = tid & 7;
+        float c[2][4] = {};
+        if (warp < 2) {
+            tile24<kBlk / 4>(c, TD + (2 * kBlk + 2 * rp) * kTD, kTD, Y2 + 4 * ct, kY2);
+        } else {
+            tile24<kBlk / 4>(c, T32 + (2 * rp - kBlk) * kMS, kMS, Y2 + 4 * ct, kY2);
+            tile24<kBlk / 4>(c, TD + (2 * kBlk + 2 * rp) * kTD, kTD, Y2 + kBlk * kY2 + 4 * ct, kY2);
+        }
+        put24_split(tT, 2 * kBlk + 2 * rp, 4 * ct, c, -1.f);
     }
     tc::fence_smem_to_async();
     tc::fence_before_sync();
