@@ -586,8 +586,8 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     if (tid < kC) sbeta[tid] = tid < n ? sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
 
     // 1. conv + SiLU (sliding window in registers) for stream px < 3, 2. the gates for px == 3;
-    //    thread (channel pc, stream px) walks all 64 rows, 8 at a time. Exponents are capped at 80
-    //    (the sigmoid is then below 2e-35 and the SiLU output tiny either way).
+    //    thread (channel pc, stream px) walks all 64 rows, 8 at a time. The gate's exponent is
+    //    capped at 80 (the sigmoid is then below 2e-35).
     if (px < 3) {
         float *dst = Yq + px * (kC * kYS);  // Yq, Yk, Yv are consecutive: the stores stay shared
         const T *col = raw + (size_t)px * kRows * kD + pc;
@@ -603,7 +603,9 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-cv[u], 80.f)));
+                // sigmoid(x) = (1 + tanh(x/2)) / 2: one SFU operation instead of two; the
+                // hardware tanh's error (about 2^-11 relative) is far below BF16's rounding
+                const float sg = fmaf(0.5f, tanh_approx(0.5f * cv[u]), 0.5f);
                 dst[(r0 + u) * kYS + pc] = r0 + u < n ? cv[u] * sg : 0.f;
             }
         }
