@@ -504,7 +504,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                const T *__restrict__ z, const T *__restrict__ bl,
                unsigned char *__restrict__ chunks, int32_t *__restrict__ err,
-               float gmin, float l2_eps, float q_scale, int pf_stride, int box_rows,
+               float gmin, float l2_eps, float q_scale, int n_items, int box_rows,
                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z)
 {
@@ -518,434 +518,470 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbeta + kC);  // [0] inputs, [1..2] A/P buffers, [3] solve
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 4);
 
-    const int chunk = blockIdx.x / H, h = blockIdx.x - (blockIdx.x / H) * H;
-    const ChunkEntry e = table[chunk];
-    if (e.n <= 0) return;  // empty entry: the chunk list was rejected
-    const int slot = slots[e.seq];
-    if (slot < 0 || slot >= max_slots) return;  // recorded by the state pass
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = e.n;
     const size_t D = (size_t)H * kD;
-
-    if (warp == 0) tc::tmem_alloc(tslot, 512);
     // staged row j of stream x holds position j - 3 of the chunk; 3 spare rows at the end take
     // the overhang of a box that starts at the chunk's first row
     constexpr int kRows = kC + 6;
     T *raw = reinterpret_cast<T *>(Y);
     static_assert(4 * kRows * kD * sizeof(T) <= kPtY, "raw staging must fit in the reused region");
     static_assert((kRows * kD * sizeof(T)) % 128 == 0, "TMA destinations must be 128-byte aligned");
-    if (tid == 32) {
-        // 0. one 2-D box of box_rows rows (x = the head's 128 channels) per stream: from 3 rows
-        //    before the chunk, or, for a sequence's first chunk (and for z), from its first row,
-        //    with the 3 history rows then taken from the conv tail. Rows past the chunk are
-        //    whatever follows in the tensor (or zero past its end): every value computed from
-        //    them is masked.
-        for (int i = 0; i < 4; ++i) mbar_init(bars + i, 1);
-        fence_mbar_init();
-        const bool first = e.pos0 == 0;
+
+    // One CTA per SM takes the items (chunk, head) = blockIdx.x + i gridDim.x, chunk-major. An
+    // item is skipped when its chunk entry is empty (the chunk list was rejected) or its slot is
+    // out of range (recorded by the state pass); every thread decides alike.
+    auto item_ok = [&](int it) {
+        const ChunkEntry ei = table[it / H];
+        if (ei.n <= 0) return false;
+        const int si = slots[ei.seq];
+        return si >= 0 && si < max_slots;
+    };
+    auto next_item = [&](int it) {
+        while (it < n_items && !item_ok(it)) it += (int)gridDim.x;
+        return it;
+    };
+    // 0. (one thread) an item's inputs, counted on bars[0]: one 2-D box of box_rows rows (x = the
+    //    head's 128 channels) per stream, from 3 rows before the chunk, or, for a sequence's
+    //    first chunk (and for z), from its first row, with the 3 history rows then taken from
+    //    the conv tail. Rows past the chunk are whatever follows in the tensor (or zero past its
+    //    end): every value computed from them is masked.
+    auto stage = [&](int it) {
+        const int ci = it / H, hi = it - ci * H;
+        const ChunkEntry ei = table[ci];
+        const bool first = ei.pos0 == 0;
         mbar_arrive_expect_tx(bars, (uint32_t)((4 * box_rows + (first ? 9 : 0)) * kD * sizeof(T)));
-        const int hx = h * kD;
-        const int ylo = first ? e.t0 : e.t0 - 3, jlo = first ? 3 : 0;
+        const int hx = hi * kD;
+        const int ylo = first ? ei.t0 : ei.t0 - 3, jlo = first ? 3 : 0;
         tma_load_2d(raw + (size_t)(0 * kRows + jlo) * kD, &tm_q, hx, ylo, bars);
         tma_load_2d(raw + (size_t)(1 * kRows + jlo) * kD, &tm_k, hx, ylo, bars);
         tma_load_2d(raw + (size_t)(2 * kRows + jlo) * kD, &tm_v, hx, ylo, bars);
-        tma_load_2d(raw + (size_t)(3 * kRows + 3) * kD, &tm_z, hx, e.t0, bars);
+        tma_load_2d(raw + (size_t)(3 * kRows + 3) * kD, &tm_z, hx, ei.t0, bars);
         if (first) {
-            const T *tl0 = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD;
+            const T *tl0 = tail_all + (size_t)slots[ei.seq] * 3 * (kK - 1) * D + (size_t)hi * kD;
             for (int x = 0; x < 3; ++x)
                 for (int j = 0; j < 3; ++j)
                     bulk_g2s(raw + (size_t)(x * kRows + j) * kD, tl0 + (size_t)(x * 3 + j) * D, kD * sizeof(T), bars);
         }
+    };
+
+    if (warp == 0) tc::tmem_alloc(tslot, 512);
+    int it = next_item((int)blockIdx.x);
+    if (tid == 32) {
+        for (int i = 0; i < 4; ++i) mbar_init(bars + i, 1);
+        fence_mbar_init();
+        if (it < n_items) stage(it);
     }
-    // the next CTA on this SM is most likely blockIdx.x + pf_stride: its boxes go to L2 now
-    if (tid == 256 && blockIdx.x + (unsigned)pf_stride < gridDim.x) {
-        const unsigned nb = blockIdx.x + (unsigned)pf_stride;
-        const int c2 = (int)(nb / (unsigned)H), h2 = (int)(nb - (unsigned)c2 * (unsigned)H);
-        const ChunkEntry e2 = table[c2];
-        if (e2.n > 0) {
+    tc::fence_before_sync();
+    __syncthreads();  // barrier init and TMEM base visible
+    tc::fence_after_sync();
+    const uint32_t tb = *tslot;
+    bool good = true;
+    bool staged = false;  // (thread 32) the next item's copies are in flight
+    uint32_t done = 0;    // items processed: the phase parity of bars[0] and bars[3]
+    for (; it < n_items; ++done) {
+        const int chunk = it / H, h = it - chunk * H;
+        const int n = table[chunk].n;
+        const int nxt = next_item(it + (int)gridDim.x);
+        // the next item's boxes go to L2 now; its copies start once this item's operand tiles
+        // have been consumed
+        if (tid == 256 && nxt < n_items) {
+            const int c2 = nxt / H, h2 = nxt - c2 * H;
+            const ChunkEntry e2 = table[c2];
             const int y2 = e2.pos0 == 0 ? e2.t0 : e2.t0 - 3;
             tma_prefetch_2d(&tm_q, h2 * kD, y2);
             tma_prefetch_2d(&tm_k, h2 * kD, y2);
             tma_prefetch_2d(&tm_v, h2 * kD, y2);
             tma_prefetch_2d(&tm_z, h2 * kD, e2.t0);
         }
-    }
-    unsigned short braw = 0;
-    if (tid < kC && tid < n) braw = ld_nc_u16(bl + (size_t)(e.t0 + tid) * H + h);
-    // this thread's per-channel parameters, loaded while the staging copies are in flight
-    const int pc = tid & (kD - 1), px = tid >> 7;  // channel, stream (q, k, v, or the gate)
-    const float4 p_w = px < 3 ? __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)px * D + (size_t)h * kD + pc) * kK))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float p_dt = __ldg(dt_bias + (size_t)h * kD + pc);
-    const float p_eA = expf(__ldg(A_log + h));
-    tc::fence_before_sync();
-    __syncthreads();  // barrier init and TMEM base visible
-    tc::fence_after_sync();
-    const uint32_t tb = *tslot;
-    bool good = mbar_wait_bounded(bars, 0u, kTcWaitLimit);
-    if (tid < kC) sbeta[tid] = tid < n ? sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
+        const int t0 = table[chunk].t0;
+        unsigned short braw = 0;
+        if (tid < kC && tid < n) braw = ld_nc_u16(bl + (size_t)(t0 + tid) * H + h);
+        // this thread's per-channel parameters, loaded while the staging copies are in flight
+        const int pc = tid & (kD - 1), px = tid >> 7;  // channel, stream (q, k, v, or the gate)
+        const float4 p_w = px < 3 ? __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)px * D + (size_t)h * kD + pc) * kK))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float p_dt = __ldg(dt_bias + (size_t)h * kD + pc);
+        const float p_eA = expf(__ldg(A_log + h));
+        good &= mbar_wait_bounded(bars, done & 1u, kTcWaitLimit);
+        staged = false;
+        if (tid < kC) sbeta[tid] = tid < n ? sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
 
-    // 1. conv + SiLU (sliding window in registers) for stream px < 3, 2. the gates for px == 3;
-    //    thread (channel pc, stream px) walks all 64 rows, 8 at a time. The gate's exponent is
-    //    capped at 80 (the sigmoid is then below 2e-35).
-    if (px < 3) {
-        float *dst = Yq + px * (kC * kYS);  // Yq, Yk, Yv are consecutive: the stores stay shared
-        const T *col = raw + (size_t)px * kRows * kD + pc;
-        float h0 = IO<T>::ld(col), h1 = IO<T>::ld(col + kD), h2 = IO<T>::ld(col + 2 * kD);
+        // 1. conv + SiLU (sliding window in registers) for stream px < 3, 2. the gates for px == 3;
+        //    thread (channel pc, stream px) walks all 64 rows, 8 at a time. The gate's exponent is
+        //    capped at 80 (the sigmoid is then below 2e-35).
+        if (px < 3) {
+            float *dst = Yq + px * (kC * kYS);  // Yq, Yk, Yv are consecutive: the stores stay shared
+            const T *col = raw + (size_t)px * kRows * kD + pc;
+            float h0 = IO<T>::ld(col), h1 = IO<T>::ld(col + kD), h2 = IO<T>::ld(col + 2 * kD);
 #pragma unroll 1
-        for (int r0 = 0; r0 < kC; r0 += 8) {
-            float cv[8];
+            for (int r0 = 0; r0 < kC; r0 += 8) {
+                float cv[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float xin = IO<T>::ld(col + (r0 + u + 3) * kD);
-                cv[u] = fmaf(p_w.x, h0, fmaf(p_w.y, h1, fmaf(p_w.z, h2, p_w.w * xin)));
-                h0 = h1; h1 = h2; h2 = xin;
-            }
+                for (int u = 0; u < 8; ++u) {
+                    const float xin = IO<T>::ld(col + (r0 + u + 3) * kD);
+                    cv[u] = fmaf(p_w.x, h0, fmaf(p_w.y, h1, fmaf(p_w.z, h2, p_w.w * xin)));
+                    h0 = h1; h1 = h2; h2 = xin;
+                }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                // sigmoid(x) = (1 + tanh(x/2)) / 2: one SFU operation instead of two; the
-                // hardware tanh's error (about 2^-11 relative) is far below BF16's rounding
-                const float sg = fmaf(0.5f, tanh_approx(0.5f * cv[u]), 0.5f);
-                dst[(r0 + u) * kYS + pc] = r0 + u < n ? cv[u] * sg : 0.f;
+                for (int u = 0; u < 8; ++u) {
+                    // sigmoid(x) = (1 + tanh(x/2)) / 2: one SFU operation instead of two; the
+                    // hardware tanh's error (about 2^-11 relative) is far below BF16's rounding
+                    const float sg = fmaf(0.5f, tanh_approx(0.5f * cv[u]), 0.5f);
+                    dst[(r0 + u) * kYS + pc] = r0 + u < n ? cv[u] * sg : 0.f;
+                }
             }
-        }
-    } else {
-        // the gate thread of channel pc also carries G_r = sum_{t<=r} gk_t down the rows (gk = 0,
-        // no decay, past the chunk, so G stays at G_last there)
-        const T *col = raw + ((size_t)3 * kRows + 3) * kD + pc;
-        float acc = 0.f;
+        } else {
+            // the gate thread of channel pc also carries G_r = sum_{t<=r} gk_t down the rows (gk = 0,
+            // no decay, past the chunk, so G stays at G_last there)
+            const T *col = raw + ((size_t)3 * kRows + 3) * kD + pc;
+            float acc = 0.f;
 #pragma unroll 1
-        for (int r0 = 0; r0 < kC; r0 += 8) {
-            float zz[8];
+            for (int r0 = 0; r0 < kC; r0 += 8) {
+                float zz[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) zz[u] = IO<T>::ld(col + (r0 + u) * kD);
+                for (int u = 0; u < 8; ++u) zz[u] = IO<T>::ld(col + (r0 + u) * kD);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[u] + p_dt), 80.f)));
-                acc += r0 + u < n ? gmin * sg : 0.f;
-                GL[(r0 + u) * kYS + pc] = acc;
+                for (int u = 0; u < 8; ++u) {
+                    const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[u] + p_dt), 80.f)));
+                    acc += r0 + u < n ? gmin * sg : 0.f;
+                    GL[(r0 + u) * kYS + pc] = acc;
+                }
             }
         }
-    }
-    __syncthreads();
-    // 2b. the L2 norms of q and k: warp w takes rows 4 w .. 4 w + 3, 8 lanes a row, lane j of a
-    //     row the channels 4 j + 32 i (i < 4), so each quarter warp reads 128 contiguous bytes
-    {
-        const int r = 4 * warp + (lane >> 3), j = lane & 7;
-        float4 *qr = reinterpret_cast<float4 *>(Yq + r * kYS) + j, *kr = reinterpret_cast<float4 *>(Yk + r * kYS) + j;
-        float4 a[4], b[4];
-        float sq = 0.f, sk = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            a[i] = qr[8 * i];
-            b[i] = kr[8 * i];
-            sq += a[i].x * a[i].x + a[i].y * a[i].y + a[i].z * a[i].z + a[i].w * a[i].w;
-            sk += b[i].x * b[i].x + b[i].y * b[i].y + b[i].z * b[i].z + b[i].w * b[i].w;
-        }
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-            sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-            sk += __shfl_xor_sync(0xFFFFFFFFu, sk, o);
-        }
-        const float rq = q_scale * rsqrt_ftz(sq + l2_eps), rk = rsqrt_ftz(sk + l2_eps);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            qr[8 * i] = make_float4(a[i].x * rq, a[i].y * rq, a[i].z * rq, a[i].w * rq);
-            kr[8 * i] = make_float4(b[i].x * rk, b[i].y * rk, b[i].z * rk, b[i].w * rk);
-        }
-    }
-    __syncthreads();
-
-    // blocks are head-major (block of chunk c, head h at h * total_chunks + c), so one head's
-    // consecutive chunks are adjacent for the state pass
-    unsigned char *blk = chunks + ((size_t)h * (gridDim.x / (unsigned)H) + chunk) * kTcChunkBytes;
-    // 3. A and P on the tensor core: the four 16-row blocks share one accumulator of 160 TMEM
-    //    columns (lane = left row, column = right row; only each block's own segment is used),
-    //    built and multiplied one half of the channels at a time by all 16 warps. While the
-    //    MMAs of half 0 run, the CTA writes Q o exp(G) to the chunk block; while those of half 1
-    //    run, (K o exp(G_last - G))^T and exp(G_last) (G is constant past the chunk, so row 63
-    //    holds G_last).
-    unsigned char *tLh = Y + kApLh, *tLl = Y + kApLl, *tRh = Y + kApRh, *tRl = Y + kApRl;
-    for (int half = 0; half < 2; ++half) {
-        const int c_h = half * (kD / 2);
-        if (half) {
-            good &= mbar_wait_bounded(bars + 1, 0u, kTcWaitLimit);  // half 0 has read the tiles
-            tc::fence_after_sync();
-        }
-        // item (row r, 8-channel group): k_r, q_r and G_r are read once; the item writes the left
-        // rows r (k) and 64 + r (q) with factor exp(G_r - G_n), n = 16 (r / 16), and row r of every
-        // right segment R >= r / 16: k_r o exp(G_16R - G_r) (<= 1 for R > r / 16, <= e^75 on the
-        // diagonal block)
+        __syncthreads();
+        // 2b. the L2 norms of q and k: warp w takes rows 4 w .. 4 w + 3, 8 lanes a row, lane j of a
+        //     row the channels 4 j + 32 i (i < 4), so each quarter warp reads 128 contiguous bytes
         {
-            const int u = tid;  // 512 items, one per thread
-            const int r = (u & 7) | ((u >> 6) << 3), cl = 8 * ((u >> 3) & 7), c0 = c_h + cl;
-            const int b = r >> 4;
-            float kv[8], qv[8], gr[8], gn[8], kl[8], ql[8];
-            ld8f(Yk + r * kYS + c0, kv);
-            ld8f(Yq + r * kYS + c0, qv);
-            ld8f(GL + r * kYS + c0, gr);
-            ld8f(GL + kBlk * b * kYS + c0, gn);
+            const int r = 4 * warp + (lane >> 3), j = lane & 7;
+            float4 *qr = reinterpret_cast<float4 *>(Yq + r * kYS) + j, *kr = reinterpret_cast<float4 *>(Yk + r * kYS) + j;
+            float4 a[4], b[4];
+            float sq = 0.f, sk = 0.f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float f = exp_ftz(gr[j] - gn[j]);
-                kl[j] = kv[j] * f;
-                ql[j] = qv[j] * f;
+            for (int i = 0; i < 4; ++i) {
+                a[i] = qr[8 * i];
+                b[i] = kr[8 * i];
+                sq += a[i].x * a[i].x + a[i].y * a[i].y + a[i].z * a[i].z + a[i].w * a[i].w;
+                sk += b[i].x * b[i].x + b[i].y * b[i].y + b[i].z * b[i].z + b[i].w * b[i].w;
             }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+                sk += __shfl_xor_sync(0xFFFFFFFFu, sk, o);
+            }
+            const float rq = q_scale * rsqrt_ftz(sq + l2_eps), rk = rsqrt_ftz(sk + l2_eps);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                qr[8 * i] = make_float4(a[i].x * rq, a[i].y * rq, a[i].z * rq, a[i].w * rq);
+                kr[8 * i] = make_float4(b[i].x * rk, b[i].y * rk, b[i].z * rk, b[i].w * rk);
+            }
+        }
+        __syncthreads();
+
+        // blocks are head-major (block of chunk c, head h at h * total_chunks + c), so one head's
+        // consecutive chunks are adjacent for the state pass
+        unsigned char *blk = chunks + ((size_t)h * (unsigned)(n_items / H) + chunk) * kTcChunkBytes;
+        // 3. A and P on the tensor core: the four 16-row blocks share one accumulator of 160 TMEM
+        //    columns (lane = left row, column = right row; only each block's own segment is used),
+        //    built and multiplied one half of the channels at a time by all 16 warps. While the
+        //    MMAs of half 0 run, the CTA writes Q o exp(G) to the chunk block; while those of half 1
+        //    run, (K o exp(G_last - G))^T and exp(G_last) (G is constant past the chunk, so row 63
+        //    holds G_last).
+        unsigned char *tLh = Y + kApLh, *tLl = Y + kApLl, *tRh = Y + kApRh, *tRl = Y + kApRl;
+        for (int half = 0; half < 2; ++half) {
+            const int c_h = half * (kD / 2);
+            if (half) {
+                good &= mbar_wait_bounded(bars + 1, 0u, kTcWaitLimit);  // half 0 has read the tiles
+                tc::fence_after_sync();
+            }
+            // item (row r, 8-channel group): k_r, q_r and G_r are read once; the item writes the left
+            // rows r (k) and 64 + r (q) with factor exp(G_r - G_n), n = 16 (r / 16), and row r of every
+            // right segment R >= r / 16: k_r o exp(G_16R - G_r) (<= 1 for R > r / 16, <= e^75 on the
+            // diagonal block)
+            {
+                const int u = tid;  // 512 items, one per thread
+                const int r = (u & 7) | ((u >> 6) << 3), cl = 8 * ((u >> 3) & 7), c0 = c_h + cl;
+                const int b = r >> 4;
+                float kv[8], qv[8], gr[8], gn[8], kl[8], ql[8];
+                ld8f(Yk + r * kYS + c0, kv);
+                ld8f(Yq + r * kYS + c0, qv);
+                ld8f(GL + r * kYS + c0, gr);
+                ld8f(GL + kBlk * b * kYS + c0, gn);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float f = exp_ftz(gr[j] - gn[j]);
+                    kl[j] = kv[j] * f;
+                    ql[j] = qv[j] * f;
+                }
+                uint4 hi, lo;
+                split8(kl, hi, lo);
+                st16(tLh + tc::kmajor_off(r, cl, kD / 2), hi);
+                st16(tLl + tc::kmajor_off(r, cl, kD / 2), lo);
+                split8(ql, hi, lo);
+                st16(tLh + tc::kmajor_off(kC + r, cl, kD / 2), hi);
+                st16(tLl + tc::kmajor_off(kC + r, cl, kD / 2), lo);
+                for (int R = b; R < kC / kBlk; ++R) {  // warp-uniform: a warp's 8 rows share a block
+                    if (R != b) ld8f(GL + kBlk * R * kYS + c0, gn);
+                    float kx[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) kx[j] = kv[j] * exp_ftz(gn[j] - gr[j]);
+                    split8(kx, hi, lo);
+                    const int row = 8 * R * (R + 1) + r;
+                    st16(tRh + tc::kmajor_off(row, cl, kD / 2), hi);
+                    st16(tRl + tc::kmajor_off(row, cl, kD / 2), lo);
+                }
+            }
+            tc::fence_smem_to_async();
+            tc::fence_before_sync();
+            __syncthreads();
+            tc::fence_after_sync();
+            if (tid == 0) {
+                mma_split3(tb, tc::kmajor_desc(tLh, 0, kD / 2), tc::kmajor_desc(tLl, 0, kD / 2),
+                           tc::kmajor_desc(tRh, 0, kD / 2), tc::kmajor_desc(tRl, 0, kD / 2), tc::idesc_bf16(128, kApN),
+                           kD / 2 / 16, half != 0);
+                tc::mma_commit(bars + 1);
+            }
+            if (half == 0) {
+                for (int u = tid; u < kC * (kD / 8); u += 512) {
+                    const int r = (u & 7) | ((u >> 7) << 3), c0 = 8 * ((u >> 3) & 15);
+                    float qv[8], gr[8], o[8];
+                    ld8f(Yq + r * kYS + c0, qv);
+                    ld8f(GL + r * kYS + c0, gr);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) o[j] = qv[j] * exp_ftz(gr[j]);
+                    st16(blk + kOffQG + tc::kmajor_off(r, c0, kD), pack8_bf16(o));
+                }
+            } else {
+                for (int u = tid; u < kD * (kC / 8); u += 512) {  // channel c, rows 8 rb .. +7
+                    const int c = u & (kD - 1), rb = u >> 7;
+                    const float gl = GL[(kC - 1) * kYS + c];
+                    float o[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int r = 8 * rb + j;
+                        o[j] = Yk[r * kYS + c] * exp_ftz(gl - GL[r * kYS + c]);
+                    }
+                    st16(blk + kOffKDT + tc::kmajor_off(c, 8 * rb, kC), pack8_bf16(o));
+                }
+                if (tid < kD) reinterpret_cast<float *>(blk + kOffG)[tid] = exp_ftz(GL[(kC - 1) * kYS + tid]);
+            }
+        }
+        good &= mbar_wait_bounded(bars + 1, 1u, kTcWaitLimit);  // second completion: half 1
+        tc::fence_before_sync();
+        if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
+        tc::fence_after_sync();
+
+        // 5. warps 0..7 read A and P back: A (beta and the strict mask applied) to the FP32 matrix
+        //    M, P (inclusive mask) straight to the chunk block. Then all warps build the solve
+        //    operands: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the 64 chunk
+        //    rows, hi parts in the q^ array (free now), lo parts in the region.
+        float *Mm = reinterpret_cast<float *>(Y + kPtM), *TD = reinterpret_cast<float *>(Y + kPtD);
+        unsigned char *tBh = reinterpret_cast<unsigned char *>(Yq), *tBl = Y + kPtBl, *tT = Y + kPtT;
+        if (warp < 8) {
+            // lane quarter qd holds left rows 32 qd .. +31 (k rows for qd < 2, q rows after);
+            // this warp reads block R's segment, used by lanes 16 half .. +15
+            const int qd = warp & 3, half = warp >> 2, R = 2 * (qd & 1) + half, oR = 8 * R * (R + 1);
+            uint32_t a0[32], a1[32];
+            const uint32_t ta = tb + ((uint32_t)(32 * qd) << 16) + oR;
+            tc::tmem_ld32_nowait(ta, a0);
+            tc::tmem_ld32_nowait(ta + 32, a1);
+            tc::tmem_wait_ld();
+            // columns past the segment belong to other blocks; the masks (i < r, i <= r) drop them
+            if ((lane >> 4) == half && qd < 2) {
+                const int r = 32 * qd + lane;
+                const float bt = sbeta[r];
+#pragma unroll
+                for (int i4 = 0; i4 < kC / 4; ++i4) {
+                    float o[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int i = 4 * i4 + t;
+                        const float a = __uint_as_float(i < 32 ? a0[i] : a1[i - 32]);
+                        o[t] = i < r ? bt * a : 0.f;
+                    }
+                    reinterpret_cast<float4 *>(Mm + r * kMS)[i4] = make_float4(o[0], o[1], o[2], o[3]);
+                }
+            } else if ((lane >> 4) == half) {
+                const int r = 32 * (qd - 2) + lane;
+#pragma unroll
+                for (int g8 = 0; g8 < kC / 8; ++g8) {
+                    float o[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const int i = 8 * g8 + t;
+                        const float pv = __uint_as_float(i < 32 ? a0[i] : a1[i - 32]);
+                        o[t] = i <= r ? pv : 0.f;
+                    }
+                    st16(blk + kOffP + tc::kmajor_off(r, 8 * g8, kC), pack8_bf16(o));
+                }
+            }
+        }
+        {   // every warp (warps 0..7 after their read-back) builds a share of the B operand
+            for (int u = tid; u < 256 * (kC / 8); u += 512) {
+                const int nn = u & 255, i0 = 8 * (u >> 8);
+                float o[8];
+                if (nn < kD) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        o[j] = sbeta[i0 + j] * (Yk[(i0 + j) * kYS + nn] * exp_ftz(GL[(i0 + j) * kYS + nn]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) o[j] = sbeta[i0 + j] * Yv[(i0 + j) * kYS + nn - kD];
+                }
+                uint4 hi, lo;
+                split8(o, hi, lo);
+                st16(tBh + tc::kmajor_off(nn, i0, kC), hi);
+                st16(tBl + tc::kmajor_off(nn, i0, kC), lo);
+            }
+        }
+        __syncthreads();
+        // 6. T = (I + A)^-1 as BF16 hi and lo parts in the T tile, by blocks of 16 and a two-level
+        //    merge. Phase 0: the diagonal blocks TD, T_RR = (I + A_RR)^-1, by forward substitution
+        //    (threads 0..63, one column each) while threads 64..447 write the zero blocks above the
+        //    diagonal (columns c >= 16 (r / 16 + 1)) to the tile. With X = rows/columns 0..31 and Y = 32..63,
+        //    T_YX = -T_YY A_YX T_XX, and inside each half T_10 = -T_11 A_10 T_00,
+        //    T_32 = -T_33 A_32 T_22. Three phases:
+        //      1. Y1_p = A_(2p+1)(2p) T_(2p)(2p) (p = 0, 1), Z0 = A_Y0 T_00, Z1 = A_Y1 T_11, and
+        //         the diagonal blocks to the tile;
+        //      2. T_10 = -T_11 Y1_0, T_32 = -T_33 Y1_1 (also kept in FP32), and Y2 = A_YX T_XX,
+        //         whose left half is Z0 + A_Y1 T_10 = Z0 - Z1 Y1_0 and whose right half is Z1;
+        //      3. T_YX = -T_YY Y2.
+        //    Each product is tiled 2 x 4 per thread (rows 2 rp, 2 rp + 1; columns 4 ct .. 4 ct + 3);
+        //    the 8 lanes of a quarter warp share their rows and take consecutive column tiles.
+        float *T32 = Yv, *Y1 = GL, *Y2 = GL + 2 * kBlk * kBlk;  // T32: [16][kMS], Y1: [2][16][16], Y2: [32][kY2]
+        constexpr int kY2 = 36;
+        // phase 0
+        if (tid < kC) {
+            const int R = tid >> 4, j = tid & (kBlk - 1), nR = kBlk * R;
+            float x[kBlk];
+#pragma unroll
+            for (int r = 0; r < kBlk; ++r) {
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < r; ++i) {
+                    if (i & 1) s1 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s1);
+                    else s0 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s0);
+                }
+                x[r] = r == j ? 1.f : (r < j ? 0.f : s0 + s1);
+            }
+            // stored after the loop, so that no shared store sits between the loads of the rows
+#pragma unroll
+            for (int r = 0; r < kBlk; ++r) TD[(nR + r) * kTD + j] = x[r];
+        } else if (tid < kC + 384) {
+            const int u = (tid - kC) % 192, lo = (tid - kC) / 192;  // 192 groups of 8 columns per part
+            const int r = u < 96 ? u / 6 : (u < 160 ? kBlk + (u - 96) / 4 : 2 * kBlk + (u - 160) / 2);
+            const int g = u < 96 ? 2 + u % 6 : (u < 160 ? 4 + (u - 96) % 4 : 6 + (u - 160) % 2);
+            st16(tT + tc::kmajor_off(lo * kC + r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
+        }
+        __syncthreads();
+        // phase 1 (threads 0..319)
+        if (tid < 64) {
+            const int p = tid >> 5, rp = (tid >> 2) & 7, ct = tid & 3, o = 2 * kBlk * p;
+            float c[2][4] = {};
+            tile24<kBlk / 4>(c, Mm + (o + kBlk + 2 * rp) * kMS + o, kMS, TD + o * kTD + 4 * ct, kTD);
+            put24(Y1 + p * kBlk * kBlk + 2 * rp * kBlk + 4 * ct, kBlk, c, 1.f);
+        } else if (tid < 192) {
+            const int t = tid - 64, rp = t >> 3, ct = t & 7, o = kBlk * (ct >> 2);
+            float c[2][4] = {};
+            tile24<kBlk / 4>(c, Mm + (2 * kBlk + 2 * rp) * kMS + o, kMS, TD + o * kTD + 4 * (ct & 3), kTD);
+            put24(Y2 + 2 * rp * kY2 + 4 * ct, kY2, c, 1.f);
+        } else if (tid < 320) {
+            const int t = tid - 192, R = t >> 5, r = kBlk * R + ((t >> 1) & (kBlk - 1)), g = t & 1;
+            float tv[8];
+            ld8f(TD + r * kTD + 8 * g, tv);
             uint4 hi, lo;
-            split8(kl, hi, lo);
-            st16(tLh + tc::kmajor_off(r, cl, kD / 2), hi);
-            st16(tLl + tc::kmajor_off(r, cl, kD / 2), lo);
-            split8(ql, hi, lo);
-            st16(tLh + tc::kmajor_off(kC + r, cl, kD / 2), hi);
-            st16(tLl + tc::kmajor_off(kC + r, cl, kD / 2), lo);
-            for (int R = b; R < kC / kBlk; ++R) {  // warp-uniform: a warp's 8 rows share a block
-                if (R != b) ld8f(GL + kBlk * R * kYS + c0, gn);
-                float kx[8];
+            split8(tv, hi, lo);
+            st16(tT + tc::kmajor_off(r, kBlk * R + 8 * g, kC), hi);
+            st16(tT + tc::kmajor_off(kC + r, kBlk * R + 8 * g, kC), lo);
+        }
+        __syncthreads();
+        // phase 2 (threads 0..127); each thread overwrites only its own tile of Z0
+        if (tid < 64) {
+            const int p = tid >> 5, rp = (tid >> 2) & 7, ct = tid & 3, o = 2 * kBlk * p;
+            float c[2][4] = {};
+            tile24<kBlk / 4>(c, TD + (o + kBlk + 2 * rp) * kTD, kTD, Y1 + p * kBlk * kBlk + 4 * ct, kBlk);
+            put24_split(tT, o + kBlk + 2 * rp, o + 4 * ct, c, -1.f);
+            if (p) put24(T32 + 2 * rp * kMS + 4 * ct, kMS, c, -1.f);
+        } else if (tid < 128) {
+            const int t = tid - 64, rp = t >> 2, ct = t & 3;
+            float c[2][4];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) kx[j] = kv[j] * exp_ftz(gn[j] - gr[j]);
-                split8(kx, hi, lo);
-                const int row = 8 * R * (R + 1) + r;
-                st16(tRh + tc::kmajor_off(row, cl, kD / 2), hi);
-                st16(tRl + tc::kmajor_off(row, cl, kD / 2), lo);
+            for (int i = 0; i < 2; ++i) {
+                const float4 z = *reinterpret_cast<const float4 *>(Y2 + (2 * rp + i) * kY2 + 4 * ct);
+                c[i][0] = -z.x; c[i][1] = -z.y; c[i][2] = -z.z; c[i][3] = -z.w;
             }
+            tile24<kBlk / 4>(c, Y2 + 2 * rp * kY2 + kBlk, kY2, Y1 + 4 * ct, kBlk);
+            put24(Y2 + 2 * rp * kY2 + 4 * ct, kY2, c, -1.f);
+        }
+        __syncthreads();
+        // phase 3 (threads 0..127): rows 32 + 2 rp (+1); T_YY's rows are [T_22 0] for warps 0, 1
+        // and [T_32 T_33] for warps 2, 3
+        if (tid < 128) {
+            const int rp = tid >> 3, ct = tid & 7;
+            float c[2][4] = {};
+            if (warp < 2) {
+                tile24<kBlk / 4>(c, TD + (2 * kBlk + 2 * rp) * kTD, kTD, Y2 + 4 * ct, kY2);
+            } else {
+                tile24<kBlk / 4>(c, T32 + (2 * rp - kBlk) * kMS, kMS, Y2 + 4 * ct, kY2);
+                tile24<kBlk / 4>(c, TD + (2 * kBlk + 2 * rp) * kTD, kTD, Y2 + kBlk * kY2 + 4 * ct, kY2);
+            }
+            put24_split(tT, 2 * kBlk + 2 * rp, 4 * ct, c, -1.f);
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
+        // 7. W (rows r = lanes 0..63, 128 channel columns at TMEM 256..383) = T B_K^T, and
+        //    U'^T (rows v = lanes 0..127, 64 row columns at TMEM 384..447) = B_V T^T
         if (tid == 0) {
-            mma_split3(tb, tc::kmajor_desc(tLh, 0, kD / 2), tc::kmajor_desc(tLl, 0, kD / 2),
-                       tc::kmajor_desc(tRh, 0, kD / 2), tc::kmajor_desc(tRl, 0, kD / 2), tc::idesc_bf16(128, kApN),
-                       kD / 2 / 16, half != 0);
-            tc::mma_commit(bars + 1);
+            const uint64_t dT = tc::kmajor_desc(tT, 0, kC), dTlo = dT + ((kC / 8) * kC * 16 >> 4);
+            const uint64_t dBh = tc::kmajor_desc(tBh, 0, kC), dBl = tc::kmajor_desc(tBl, 0, kC);
+            const uint64_t vOff = (uint64_t)((kD / 8) * kC * 16 >> 4);  // B rows 128.. = (beta V)^T
+            mma_split3(tb + 256, dT, dTlo, dBh, dBl, tc::idesc_bf16(128, kD), kC / 16, false);
+            mma_split3(tb + 384, dBh + vOff, dBl + vOff, dT, dTlo, tc::idesc_bf16(128, kC), kC / 16, false);
+            tc::mma_commit(bars + 3);
         }
-        if (half == 0) {
-            for (int u = tid; u < kC * (kD / 8); u += 512) {
-                const int r = (u & 7) | ((u >> 7) << 3), c0 = 8 * ((u >> 3) & 15);
-                float qv[8], gr[8], o[8];
-                ld8f(Yq + r * kYS + c0, qv);
-                ld8f(GL + r * kYS + c0, gr);
+        good = __all_sync(0xFFFFFFFFu, good && mbar_wait_bounded(bars + 3, done & 1u, kTcWaitLimit));  // warp-uniform
+        tc::fence_after_sync();
+        // the operand tiles are consumed: the next item's inputs may land in the reused region
+        if (tid == 32 && good && nxt < n_items) {
+            tc::fence_smem_to_async();
+            stage(nxt);
+            staged = true;
+        }
+        // 8. W: warps on lane quarters 0 and 1 (rows 0..63), 32 channels each, as BF16 16-byte
+        //    chunks; U': every warp, 16 rows r of its 32 lanes v, coalesced FP32 stores
+        if (good) {
+            const int qd = warp & 3, part = warp >> 2;
+            if (qd < 2) {
+                const int r = 32 * qd + lane;
+                uint32_t wv[32];
+                tc::tmem_ld32_nowait(tb + ((uint32_t)(32 * qd) << 16) + 256 + 32 * part, wv);
+                tc::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = qv[j] * exp_ftz(gr[j]);
-                st16(blk + kOffQG + tc::kmajor_off(r, c0, kD), pack8_bf16(o));
-            }
-        } else {
-            for (int u = tid; u < kD * (kC / 8); u += 512) {  // channel c, rows 8 rb .. +7
-                const int c = u & (kD - 1), rb = u >> 7;
-                const float gl = GL[(kC - 1) * kYS + c];
-                float o[8];
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    float o[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int r = 8 * rb + j;
-                    o[j] = Yk[r * kYS + c] * exp_ftz(gl - GL[r * kYS + c]);
+                    for (int t = 0; t < 8; ++t) o[t] = __uint_as_float(wv[8 * g8 + t]);
+                    st16(blk + kOffW + tc::kmajor_off(r, 32 * part + 8 * g8, kD), pack8_bf16(o));
                 }
-                st16(blk + kOffKDT + tc::kmajor_off(c, 8 * rb, kC), pack8_bf16(o));
             }
-            if (tid < kD) reinterpret_cast<float *>(blk + kOffG)[tid] = exp_ftz(GL[(kC - 1) * kYS + tid]);
+            float uv[16];
+            tc::tmem_ld16(tb + ((uint32_t)(32 * qd) << 16) + 384 + 16 * part, uv);
+            float *Up = reinterpret_cast<float *>(blk + kOffUp) + 32 * qd + lane;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) Up[(16 * part + t) * kD] = uv[t];
         }
-    }
-    good &= mbar_wait_bounded(bars + 1, 1u, kTcWaitLimit);  // second completion: half 1
-    tc::fence_before_sync();
-    if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
-    tc::fence_after_sync();
-
-    // 5. warps 0..7 read A and P back: A (beta and the strict mask applied) to the FP32 matrix
-    //    M, P (inclusive mask) straight to the chunk block. Then all warps build the solve
-    //    operands: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the 64 chunk
-    //    rows, hi parts in the q^ array (free now), lo parts in the region.
-    float *Mm = reinterpret_cast<float *>(Y + kPtM), *TD = reinterpret_cast<float *>(Y + kPtD);
-    unsigned char *tBh = reinterpret_cast<unsigned char *>(Yq), *tBl = Y + kPtBl, *tT = Y + kPtT;
-    if (warp < 8) {
-        // lane quarter qd holds left rows 32 qd .. +31 (k rows for qd < 2, q rows after);
-        // this warp reads block R's segment, used by lanes 16 half .. +15
-        const int qd = warp & 3, half = warp >> 2, R = 2 * (qd & 1) + half, oR = 8 * R * (R + 1);
-        uint32_t a0[32], a1[32];
-        const uint32_t ta = tb + ((uint32_t)(32 * qd) << 16) + oR;
-        tc::tmem_ld32_nowait(ta, a0);
-        tc::tmem_ld32_nowait(ta + 32, a1);
-        tc::tmem_wait_ld();
-        // columns past the segment belong to other blocks; the masks (i < r, i <= r) drop them
-        if ((lane >> 4) == half && qd < 2) {
-            const int r = 32 * qd + lane;
-            const float bt = sbeta[r];
-#pragma unroll
-            for (int i4 = 0; i4 < kC / 4; ++i4) {
-                float o[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int i = 4 * i4 + t;
-                    const float a = __uint_as_float(i < 32 ? a0[i] : a1[i - 32]);
-                    o[t] = i < r ? bt * a : 0.f;
-                }
-                reinterpret_cast<float4 *>(Mm + r * kMS)[i4] = make_float4(o[0], o[1], o[2], o[3]);
-            }
-        } else if ((lane >> 4) == half) {
-            const int r = 32 * (qd - 2) + lane;
-#pragma unroll
-            for (int g8 = 0; g8 < kC / 8; ++g8) {
-                float o[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const int i = 8 * g8 + t;
-                    const float pv = __uint_as_float(i < 32 ? a0[i] : a1[i - 32]);
-                    o[t] = i <= r ? pv : 0.f;
-                }
-                st16(blk + kOffP + tc::kmajor_off(r, 8 * g8, kC), pack8_bf16(o));
-            }
+        tc::fence_before_sync();
+        const bool bad = __syncthreads_or(!good);
+        tc::fence_after_sync();
+        if (bad) {
+            if (tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
+            break;
         }
+        it = nxt;
     }
-    {   // every warp (warps 0..7 after their read-back) builds a share of the B operand
-        for (int u = tid; u < 256 * (kC / 8); u += 512) {
-            const int nn = u & 255, i0 = 8 * (u >> 8);
-            float o[8];
-            if (nn < kD) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    o[j] = sbeta[i0 + j] * (Yk[(i0 + j) * kYS + nn] * exp_ftz(GL[(i0 + j) * kYS + nn]));
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = sbeta[i0 + j] * Yv[(i0 + j) * kYS + nn - kD];
-            }
-            uint4 hi, lo;
-            split8(o, hi, lo);
-            st16(tBh + tc::kmajor_off(nn, i0, kC), hi);
-            st16(tBl + tc::kmajor_off(nn, i0, kC), lo);
-        }
-    }
-    __syncthreads();
-    // 6. T = (I + A)^-1 as BF16 hi and lo parts in the T tile, by blocks of 16 and a two-level
-    //    merge. Phase 0: the diagonal blocks TD, T_RR = (I + A_RR)^-1, by forward substitution
-    //    (threads 0..63, one column each) while threads 64..447 write the zero blocks above the
-    //    diagonal (columns c >= 16 (r / 16 + 1)) to the tile. With X = rows/columns 0..31 and Y = 32..63,
-    //    T_YX = -T_YY A_YX T_XX, and inside each half T_10 = -T_11 A_10 T_00,
-    //    T_32 = -T_33 A_32 T_22. Three phases:
-    //      1. Y1_p = A_(2p+1)(2p) T_(2p)(2p) (p = 0, 1), Z0 = A_Y0 T_00, Z1 = A_Y1 T_11, and
-    //         the diagonal blocks to the tile;
-    //      2. T_10 = -T_11 Y1_0, T_32 = -T_33 Y1_1 (also kept in FP32), and Y2 = A_YX T_XX,
-    //         whose left half is Z0 + A_Y1 T_10 = Z0 - Z1 Y1_0 and whose right half is Z1;
-    //      3. T_YX = -T_YY Y2.
-    //    Each product is tiled 2 x 4 per thread (rows 2 rp, 2 rp + 1; columns 4 ct .. 4 ct + 3);
-    //    the 8 lanes of a quarter warp share their rows and take consecutive column tiles.
-    float *T32 = Yv, *Y1 = GL, *Y2 = GL + 2 * kBlk * kBlk;  // T32: [16][kMS], Y1: [2][16][16], Y2: [32][kY2]
-    constexpr int kY2 = 36;
-    // phase 0
-    if (tid < kC) {
-        const int R = tid >> 4, j = tid & (kBlk - 1), nR = kBlk * R;
-        float x[kBlk];
-#pragma unroll
-        for (int r = 0; r < kBlk; ++r) {
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < r; ++i) {
-                if (i & 1) s1 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s1);
-                else s0 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s0);
-            }
-            x[r] = r == j ? 1.f : (r < j ? 0.f : s0 + s1);
-        }
-        // stored after the loop, so that no shared store sits between the loads of the rows
-#pragma unroll
-        for (int r = 0; r < kBlk; ++r) TD[(nR + r) * kTD + j] = x[r];
-    } else if (tid < kC + 384) {
-        const int u = (tid - kC) % 192, lo = (tid - kC) / 192;  // 192 groups of 8 columns per part
-        const int r = u < 96 ? u / 6 : (u < 160 ? kBlk + (u - 96) / 4 : 2 * kBlk + (u - 160) / 2);
-        const int g = u < 96 ? 2 + u % 6 : (u < 160 ? 4 + (u - 96) % 4 : 6 + (u - 160) % 2);
-        st16(tT + tc::kmajor_off(lo * kC + r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
-    }
-    __syncthreads();
-    // phase 1 (threads 0..319)
-    if (tid < 64) {
-        const int p = tid >> 5, rp = (tid >> 2) & 7, ct = tid & 3, o = 2 * kBlk * p;
-        float c[2][4] = {};
-        tile24<kBlk / 4>(c, Mm + (o + kBlk + 2 * rp) * kMS + o, kMS, TD + o * kTD + 4 * ct, kTD);
-        put24(Y1 + p * kBlk * kBlk + 2 * rp * kBlk + 4 * ct, kBlk, c, 1.f);
-    } else if (tid < 192) {
-        const int t = tid - 64, rp = t >> 3, ct = t & 7, o = kBlk * (ct >> 2);
-        float c[2][4] = {};
-        tile24<kBlk / 4>(c, Mm + (2 * kBlk + 2 * rp) * kMS + o, kMS, TD + o * kTD + 4 * (ct & 3), kTD);
-        put24(Y2 + 2 * rp * kY2 + 4 * ct, kY2, c, 1.f);
-    } else if (tid < 320) {
-        const int t = tid - 192, R = t >> 5, r = kBlk * R + ((t >> 1) & (kBlk - 1)), g = t & 1;
-        float tv[8];
-        ld8f(TD + r * kTD + 8 * g, tv);
-        uint4 hi, lo;
-        split8(tv, hi, lo);
-        st16(tT + tc::kmajor_off(r, kBlk * R + 8 * g, kC), hi);
-        st16(tT + tc::kmajor_off(kC + r, kBlk * R + 8 * g, kC), lo);
-    }
-    __syncthreads();
-    // phase 2 (threads 0..127); each thread overwrites only its own tile of Z0
-    if (tid < 64) {
-        const int p = tid >> 5, rp = (tid >> 2) & 7, ct = tid & 3, o = 2 * kBlk * p;
-        float c[2][4] = {};
-        tile24<kBlk / 4>(c, TD + (o + kBlk + 2 * rp) * kTD, kTD, Y1 + p * kBlk * kBlk + 4 * ct, kBlk);
-        put24_split(tT, o + kBlk + 2 * rp, o + 4 * ct, c, -1.f);
-        if (p) put24(T32 + 2 * rp * kMS + 4 * ct, kMS, c, -1.f);
-    } else if (tid < 128) {
-        const int t = tid - 64, rp = t >> 2, ct = t & 3;
-        float c[2][4];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float4 z = *reinterpret_cast<const float4 *>(Y2 + (2 * rp + i) * kY2 + 4 * ct);
-            c[i][0] = -z.x; c[i][1] = -z.y; c[i][2] = -z.z; c[i][3] = -z.w;
-        }
-        tile24<kBlk / 4>(c, Y2 + 2 * rp * kY2 + kBlk, kY2, Y1 + 4 * ct, kBlk);
-        put24(Y2 + 2 * rp * kY2 + 4 * ct, kY2, c, -1.f);
-    }
-    __syncthreads();
-    // phase 3 (threads 0..127): rows 32 + 2 rp (+1); T_YY's rows are [T_22 0] for warps 0, 1
-    // and [T_32 T_33] for warps 2, 3
-    if (tid < 128) {
-        const int rp = tid >> 3, ct = tid & 7;
-        float c[2][4] = {};
-        if (warp < 2) {
-            tile24<kBlk / 4>(c, TD + (2 * kBlk + 2 * rp) * kTD, kTD, Y2 + 4 * ct, kY2);
-        } else {
-            tile24<kBlk / 4>(c, T32 + (2 * rp - kBlk) * kMS, kMS, Y2 + 4 * ct, kY2);
-            tile24<kBlk / 4>(c, TD + (2 * kBlk + 2 * rp) * kTD, kTD, Y2 + kBlk * kY2 + 4 * ct, kY2);
-        }
-        put24_split(tT, 2 * kBlk + 2 * rp, 4 * ct, c, -1.f);
-    }
-    tc::fence_smem_to_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    // 7. W (rows r = lanes 0..63, 128 channel columns at TMEM 256..383) = T B_K^T, and
-    //    U'^T (rows v = lanes 0..127, 64 row columns at TMEM 384..447) = B_V T^T
-    if (tid == 0) {
-        const uint64_t dT = tc::kmajor_desc(tT, 0, kC), dTlo = dT + ((kC / 8) * kC * 16 >> 4);
-        const uint64_t dBh = tc::kmajor_desc(tBh, 0, kC), dBl = tc::kmajor_desc(tBl, 0, kC);
-        const uint64_t vOff = (uint64_t)((kD / 8) * kC * 16 >> 4);  // B rows 128.. = (beta V)^T
-        mma_split3(tb + 256, dT, dTlo, dBh, dBl, tc::idesc_bf16(128, kD), kC / 16, false);
-        mma_split3(tb + 384, dBh + vOff, dBl + vOff, dT, dTlo, tc::idesc_bf16(128, kC), kC / 16, false);
-        tc::mma_commit(bars + 3);
-    }
-    good = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bars + 3, 0u, kTcWaitLimit));  // warp-uniform
-    tc::fence_after_sync();
-    // 8. W: warps on lane quarters 0 and 1 (rows 0..63), 32 channels each, as BF16 16-byte
-    //    chunks; U': every warp, 16 rows r of its 32 lanes v, coalesced FP32 stores
-    if (good) {
-        const int qd = warp & 3, part = warp >> 2;
-        if (qd < 2) {
-            const int r = 32 * qd + lane;
-            uint32_t wv[32];
-            tc::tmem_ld32_nowait(tb + ((uint32_t)(32 * qd) << 16) + 256 + 32 * part, wv);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8) {
-                float o[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) o[t] = __uint_as_float(wv[8 * g8 + t]);
-                st16(blk + kOffW + tc::kmajor_off(r, 32 * part + 8 * g8, kD), pack8_bf16(o));
-            }
-        }
-        float uv[16];
-        tc::tmem_ld16(tb + ((uint32_t)(32 * qd) << 16) + 384 + 16 * part, uv);
-        float *Up = reinterpret_cast<float *>(blk + kOffUp) + 32 * qd + lane;
-#pragma unroll
-        for (int t = 0; t < 16; ++t) Up[(16 * part + t) * kD] = uv[t];
-    }
-    tc::fence_before_sync();
-    if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
+    // after an abort the next item's copies may still be in flight: wait for them (bounded)
+    if (staged) mbar_wait_bounded(bars, (done + 1) & 1u, kTcWaitLimit);
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
@@ -1507,10 +1543,12 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
                 return e;
             e = cudaFuncSetAttribute(prep_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepTcSmem);
             if (e != cudaSuccess) return e;
-            prep_tc_kernel<T><<<(unsigned)(total_chunks * H), 512, kPrepTcSmem, stream>>>(
+            // persistent: one CTA per SM strides over the (chunk, head) items
+            const int n_items = total_chunks * H;
+            prep_tc_kernel<T><<<(unsigned)(n_items < sms ? n_items : sms), 512, kPrepTcSmem, stream>>>(
                 p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
                 (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, chunks, st.err,
-                c.gate_lower_bound, c.l2_eps, c.q_scale, sms, box_rows, tmq, tmk, tmv, tmz);
+                c.gate_lower_bound, c.l2_eps, c.q_scale, n_items, box_rows, tmq, tmk, tmv, tmz);
         } else {
             const int prep_smem = kPrepSmemFloats * (int)sizeof(float);
             e = cudaFuncSetAttribute(prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
