@@ -490,6 +490,51 @@ def _time_varlen(K, args, cfg, params, gen, dev, stream):
             "decode_ms_per_step": dec_ms / steps, "decode_tokens_per_s": N * steps / (dec_ms / 1e3)}
 
 
+def _time_photo(K, cfg, params, gen, dev, stream, prefill_ms):
+    """Photo take and restore of one sequence slot (96 heads x 128, one layer), in pinned host
+    memory and parked in a file, against re-prefilling the T-token prompt it stands for. The
+    calls synchronise their stream, so they are timed on the host clock (median)."""
+    import shutil
+
+    import torch
+    st = K.kda_state_alloc(cfg, 2)
+    _fill_state_random(K, cfg, st, 2, gen, dev)
+    torch.cuda.synchronize()
+    tokens = list(range(4096))
+    res = {"photo_bytes": K.kda_state_blob_bytes(st, 1)}
+    tmp = tempfile.mkdtemp(prefix="kda_photo_bench_")
+    try:
+        for mode, d, reps in (("ram", None, 20), ("file", tmp, 5)):
+            ps = K.kda_photo_store_create(2, d)
+            try:
+                pid = K.kda_photo_take(ps, [st], 0, tokens, stream)  # first take allocates
+                K.kda_photo_restore(ps, pid, [st], 1, stream)
+                tt, tr = [], []
+                for _ in range(reps):
+                    t0 = time.perf_counter()
+                    pid = K.kda_photo_take(ps, [st], 0, tokens, stream)
+                    t1 = time.perf_counter()
+                    K.kda_photo_restore(ps, pid, [st], 1, stream)
+                    t2 = time.perf_counter()
+                    tt.append((t1 - t0) * 1e3)
+                    tr.append((t2 - t1) * 1e3)
+            finally:
+                K.kda_photo_store_free(ps)
+            res[f"{mode}_take_ms"] = statistics.median(tt)
+            res[f"{mode}_restore_ms"] = statistics.median(tr)
+            res[f"{mode}_restore_gbs"] = res["photo_bytes"] / (res[f"{mode}_restore_ms"] / 1e3) / 1e9
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+        K.kda_state_free(st)
+    res["workload"] = ("kda_photo take/restore of one sequence slot (96 heads x 128, 1 KDA layer, FP32 state + "
+                       "BF16 conv history), pinned host memory and a parked file; host clock, median")
+    if prefill_ms is not None:
+        res["reprefill_ms"] = prefill_ms
+        res["reprefill_tokens"] = T_PRE
+        res["ram_restore_vs_reprefill"] = prefill_ms / res["ram_restore_ms"]
+    return res
+
+
 def run_kda(args):
     import torch
     ws, rank, local = _dist()
@@ -574,6 +619,8 @@ def run_kda(args):
             line["gpu_launches"] = 3 * args.prefill_reps
     if args.only == "all":
         line["varlen"] = _time_varlen(K, args, cfg, params, gen, dev, stream)
+        line["photo"] = _time_photo(K, cfg, params, gen, dev, stream,
+                                    line["prefill"]["ms"] if Tp == T_PRE else None)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode()
         if "prefill" in line:

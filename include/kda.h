@@ -52,7 +52,8 @@ typedef enum {
     KDA_ERR_CUDA = 3,     /* a CUDA runtime call failed (message holds cudaGetErrorString) */
     KDA_ERR_BLOB = 4,     /* a snapshot blob has the wrong magic, version, geometry or size */
     KDA_ERR_TIMEOUT = 5,  /* a bounded device-side wait gave up */
-    KDA_ERR_DEVICE = 6    /* a kernel recorded a bad index (see kda_state_poll_error) */
+    KDA_ERR_DEVICE = 6,   /* a kernel recorded a bad index (see kda_state_poll_error) */
+    KDA_ERR_IO = 7        /* a photo file could not be written or read back */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -259,6 +260,75 @@ kda_status kda_prefill_noalloc(const kda_config_t *cfg, const kda_layer_params *
                                const int32_t *cu_seqlens_host, int32_t N,
                                const void *q, const void *k, const void *v, const void *z,
                                const void *b, const void *g, void *out, void *stream);
+
+/*
+ * Recurrent-state photos (kimi_k3.c header, the COLI_K3_CKPT and
+ * COLI_K3_CKPT_DIR serve options). A store keeps up to `capacity` photos of
+ * one sequence slot across a stack of KDA layers (one kda_state per layer),
+ * each taken after a token prefix, normally at a turn boundary. When a later
+ * prompt diverges from an earlier one (an edit), kda_photo_find names the
+ * deepest photo whose prefix is still a prefix of the new prompt: restoring it
+ * and prefilling only the tokens after it replaces a prefill from token 0.
+ *   capacity  photos kept. 0 turns the store off (kda_photo_take stores
+ *             nothing). A negative value means "not given": 2 when dir is
+ *             set, else 0. A given value always wins.
+ *   dir       NULL keeps photos in pinned host memory. Otherwise each photo is
+ *             parked in a file under dir (an existing directory). Files are
+ *             removed when their photo is evicted and when the store is freed,
+ *             so no photo outlives its store.
+ * A photo holds, per layer, the kda_state_snapshot blob of the slot, and a
+ * copy of the prefix's token ids, which kda_photo_find compares exactly.
+ * All calls on one store are serialised by a lock inside it.
+ */
+typedef struct kda_photo_store kda_photo_store;
+
+/* Errors: KDA_ERR_INVALID (out == NULL, dir not a directory), KDA_ERR_OOM. */
+kda_status kda_photo_store_create(int32_t capacity, const char *dir, kda_photo_store **out);
+
+/* Free the store, its host memory and its files. NULL is a no-op. */
+kda_status kda_photo_store_free(kda_photo_store *ps);
+
+/* Photos held now, and the capacity the store resolved (0 for NULL). */
+int32_t kda_photo_count(const kda_photo_store *ps);
+int32_t kda_photo_capacity(const kda_photo_store *ps);
+
+/*
+ * Photo of slot `slot` of each of the n_layers states layers[0..n_layers) (all
+ * of one geometry) after the prefix tokens[0..n_tokens) (host int32 ids). The
+ * states must hold that prefix's result. The copies are enqueued on `stream`
+ * and the call synchronises it before returning, so the photo is complete and
+ * the states may move on. A photo of the same prefix is replaced. When the
+ * store is full, the least recently used photo (by take or restore) is
+ * evicted. A store of capacity 0 returns KDA_OK and *photo_id = -1.
+ *   photo_id  optional out: the new photo's id (ids are never reused).
+ * Errors: KDA_ERR_INVALID (NULL store or layers, tokens == NULL with
+ * n_tokens > 0, n_layers < 1, n_tokens < 0, slot out of range for a layer,
+ * layers of different geometry), KDA_ERR_OOM, KDA_ERR_CUDA, KDA_ERR_IO. On an
+ * error the store keeps the photos it had.
+ */
+kda_status kda_photo_take(kda_photo_store *ps, kda_state *const *layers, int32_t n_layers, int32_t slot,
+                          const int32_t *tokens, int64_t n_tokens, int32_t *photo_id, void *stream);
+
+/*
+ * The deepest photo whose prefix equals tokens[0..len) for some len <=
+ * n_tokens (the most recently taken one on a tie): *photo_id and *prefix_len,
+ * or -1 and 0 when there is none. Host only; nothing is copied.
+ * Errors: KDA_ERR_INVALID (NULL store or outputs, tokens == NULL with
+ * n_tokens > 0, n_tokens < 0).
+ */
+kda_status kda_photo_find(const kda_photo_store *ps, const int32_t *tokens, int64_t n_tokens,
+                          int32_t *photo_id, int64_t *prefix_len);
+
+/*
+ * Put photo photo_id back into slot `slot` of the n_layers states, which must
+ * match the photo's layer count and each layer's geometry. The copies are
+ * enqueued on `stream` and the call synchronises it before returning.
+ * Errors: KDA_ERR_INVALID (unknown or evicted id, NULL arguments, a layer
+ * count other than the photo's, slot out of range), KDA_ERR_BLOB (a layer of
+ * another geometry), KDA_ERR_IO, KDA_ERR_CUDA.
+ */
+kda_status kda_photo_restore(kda_photo_store *ps, int32_t photo_id, kda_state *const *layers, int32_t n_layers,
+                             int32_t slot, void *stream);
 
 /*
  * Synchronise the device, read and clear the state's device error word.

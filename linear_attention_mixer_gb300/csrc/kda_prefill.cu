@@ -1152,7 +1152,11 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     unsigned char *sST = sm + 2 * kTcStageBytes;           // S^T [v][k] BF16, K-major, 32 KB
     unsigned char *sUT = sST + 32768;                      // U^T [v][r] BF16, K-major, 16 KB
     float *sgam = reinterpret_cast<float *>(sUT + 16384);  // [2 stages][128] chunk decay
-    float *red = sgam + 2 * kD;                            // [2 chunk parities][64 tokens] sums of squares
+    // [64 tokens][4 value quarters] partial sums of squares, added in a fixed order (so that the
+    // outputs do not depend on the order the warps finish in). One buffer is enough: a chunk's
+    // RMSNorm reads them before the barrier that ends every full chunk, and only a sequence's
+    // last chunk can be ragged.
+    float *red = sgam + 2 * kD;
     // barriers: [0..1] W|QG of stage 0/1, [2] mma1, [3] mma2, [4] g rows, [5..6] the rest of stage 0/1
     uint64_t *bar = reinterpret_cast<uint64_t *>(red + 4 * kC);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 7);
@@ -1178,7 +1182,6 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         for (int i = 0; i < 7; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
     }
-    if (tid < 2 * kC) red[tid] = 0.f;
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -1255,7 +1258,6 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             // an HBM round trip would stall the epilogue
             if (tid == 0) tma_prefetch_2d(&tm_g, h * kD, e_next.t0);
         }
-        float *redc = red + st * kC;
         static_assert(sizeof(T) == 2, "the tensor-core path reads BF16 gate logits");
 
         stage_ok = mbar_wait_bounded(&bar[5 + st], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
@@ -1344,7 +1346,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                     sq[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
                 }
             }
-            atomicAdd(&redc[r0 + lane], sq[0]);  // the four lane quarters add up over v
+            red[(r0 + lane) * 4 + qtr] = sq[0];  // the four lane quarters are added in the epilogue
         }
         // refresh the S^T operand from the updated FP32 state
         {
@@ -1370,8 +1372,6 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 if (good) mma1(sm + (st ^ 1) * kTcStageBytes);
             }
         }
-        // the other parity's sums were last read in the previous chunk's epilogue: clear them
-        if (tid < kC) red[(st ^ 1) * kC + tid] = 0.f;
         // gated RMSNorm of this thread's 32 tokens: the gate logits from the U^T buffer, the
         // BF16 results written back over them; a full chunk leaves as one TMA box
         if (mbar_wait_bounded(&bar[4], (uint32_t)(it & 1), kTcWaitLimit)) gpar = -1;
@@ -1380,7 +1380,8 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             __nv_bfloat16 y[32];
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
-                const float rinv = rsqrt_ftz(redc[r0 + r] * (1.0f / kD) + rms_eps);
+                const float4 pq = reinterpret_cast<const float4 *>(red)[r0 + r];
+                const float rinv = rsqrt_ftz(((pq.x + pq.y) + (pq.z + pq.w)) * (1.0f / kD) + rms_eps);
                 const float gv = __bfloat162float(sGY[(r0 + r) * kD + vi]);
                 // sigmoid(g) = (1 + tanh(g/2)) / 2; the hardware tanh's error is below the BF16
                 // rounding of the output it multiplies

@@ -13,13 +13,14 @@ import os
 
 import torch
 
-KDA_OK, KDA_ERR_INVALID, KDA_ERR_OOM, KDA_ERR_CUDA, KDA_ERR_BLOB, KDA_ERR_TIMEOUT, KDA_ERR_DEVICE = range(7)
+KDA_OK, KDA_ERR_INVALID, KDA_ERR_OOM, KDA_ERR_CUDA, KDA_ERR_BLOB, KDA_ERR_TIMEOUT, KDA_ERR_DEVICE, KDA_ERR_IO = range(8)
 KDA_F32, KDA_BF16 = 0, 1
 KDA_BLOB_MAGIC = 0x3141444B
 KDA_BLOB_VERSION = 1
 KDA_DECODE_MAX_TOKENS = 8  # most tokens per row in one kda_decode_tokens call
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID", 2: "KDA_ERR_OOM", 3: "KDA_ERR_CUDA",
-                4: "KDA_ERR_BLOB", 5: "KDA_ERR_TIMEOUT", 6: "KDA_ERR_DEVICE"}
+                4: "KDA_ERR_BLOB", 5: "KDA_ERR_TIMEOUT", 6: "KDA_ERR_DEVICE",
+                7: "KDA_ERR_IO"}
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkda.so")
@@ -77,6 +78,13 @@ SIGNATURES = [
     ("kda_prefill_noalloc", _I32, [ctypes.POINTER(kda_config_t), ctypes.POINTER(kda_layer_params), _VP, _VP, _I32,
                                    _VP, _VP, _VP, _PI32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("kda_state_poll_error", _I32, [_VP, _PI32]),
+    ("kda_photo_store_create", _I32, [_I32, ctypes.c_char_p, ctypes.POINTER(_VP)]),
+    ("kda_photo_store_free", _I32, [_VP]),
+    ("kda_photo_count", _I32, [_VP]),
+    ("kda_photo_capacity", _I32, [_VP]),
+    ("kda_photo_take", _I32, [_VP, ctypes.POINTER(_VP), _I32, _I32, _PI32, ctypes.c_int64, _PI32, _VP]),
+    ("kda_photo_find", _I32, [_VP, _PI32, ctypes.c_int64, _PI32, ctypes.POINTER(ctypes.c_int64)]),
+    ("kda_photo_restore", _I32, [_VP, _I32, ctypes.POINTER(_VP), _I32, _I32, _VP]),
     ("kda_last_error", ctypes.c_char_p, []),
 ]
 
@@ -273,6 +281,53 @@ def kda_prefill_noalloc(cfg: kda_config_t, params: kda_layer_params, S: torch.Te
                                      _dev(cu_seqlens, torch.int32, "cu_seqlens"), cu_p, N,
                                      _dev(q, dt, "q"), _dev(k, dt, "k"), _dev(v, dt, "v"), _dev(z, dt, "z"),
                                      _dev(b, dt, "b"), _dev(g, dt, "g"), _dev(out, dt, "out"), _stream(stream)))
+
+
+def _layers(layers):
+    hs = [layers] if isinstance(layers, _VP) else list(layers)
+    arr = (_VP * len(hs))(*[h.value if isinstance(h, _VP) else h for h in hs])
+    return arr, len(hs)
+
+
+def kda_photo_store_create(capacity: int = -1, dir: str | None = None) -> ctypes.c_void_p:
+    """A photo store: capacity < 0 means "not given" (2 with a directory, else 0 = off)."""
+    h = _VP()
+    _check(lib().kda_photo_store_create(capacity, None if dir is None else dir.encode(), ctypes.byref(h)))
+    return h
+
+
+def kda_photo_store_free(ps) -> None:
+    _check(lib().kda_photo_store_free(ps))
+
+
+def kda_photo_count(ps) -> int:
+    return int(lib().kda_photo_count(ps))
+
+
+def kda_photo_capacity(ps) -> int:
+    return int(lib().kda_photo_capacity(ps))
+
+
+def kda_photo_take(ps, layers, slot: int, tokens, stream=None) -> int:
+    """Photo of `slot` of each state in `layers` after the host token prefix; returns its id (-1: store off)."""
+    arr, n = _layers(layers)
+    tok, tp = _host_i32(tokens)
+    pid = ctypes.c_int32()
+    _check(lib().kda_photo_take(ps, arr, n, slot, tp, len(tok), ctypes.byref(pid), _stream(stream)))
+    return int(pid.value)
+
+
+def kda_photo_find(ps, tokens) -> tuple[int, int]:
+    """(photo id, prefix length) of the deepest photo whose prefix starts `tokens`, or (-1, 0)."""
+    tok, tp = _host_i32(tokens)
+    pid, plen = ctypes.c_int32(), ctypes.c_int64()
+    _check(lib().kda_photo_find(ps, tp, len(tok), ctypes.byref(pid), ctypes.byref(plen)))
+    return int(pid.value), int(plen.value)
+
+
+def kda_photo_restore(ps, photo_id: int, layers, slot: int, stream=None) -> None:
+    arr, n = _layers(layers)
+    _check(lib().kda_photo_restore(ps, photo_id, arr, n, slot, _stream(stream)))
 
 
 def kda_state_poll_error(st) -> int:

@@ -201,3 +201,25 @@ def test_prefill_8192_bf16_full_size(oracle_mod):
     assert rel_err(Sg[0], S) <= TOL_BF16
     assert np.array_equal(tg[0], tail.astype(np.float32))
     assert np.isfinite(got).all()
+
+
+def test_prefill_is_bit_reproducible():
+    """The same prefill, repeated into fresh slots, gives bit-identical outputs, states and
+    conv histories (every reduction on the path runs in a fixed order)."""
+    H, d = 8, 128
+    p = KI.make_params(H, d, 4, 29)
+    tok = KI.make_tokens(700, H, d, 29, bf16=True)
+    cfg = K.kda_config(H, d, K.KDA_BF16)
+    params = dev_params(p)
+    st = K.kda_state_alloc(cfg, 4)
+    try:
+        runs = []
+        for s in range(4):
+            out, _ = _prefill(cfg, params, st, [s], [700], tok, True)
+            S, t = download_state(cfg, st, [s])
+            runs.append((out, S, t))
+        assert K.kda_state_poll_error(st) == 0
+    finally:
+        K.kda_state_free(st)
+    for out, S, t in runs[1:]:
+        assert np.array_equal(out, runs[0][0]) and np.array_equal(S, runs[0][1]) and np.array_equal(t, runs[0][2])
