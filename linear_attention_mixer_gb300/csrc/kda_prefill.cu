@@ -575,8 +575,42 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     __syncthreads();  // barrier init and TMEM base visible
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
+    // 8. an item's W and U' from TMEM to its chunk block, by ng groups of four warps (gi = this
+    //    warp's group): W (lanes 0..63, columns 256..383) as BF16 16-byte chunks by the warps on
+    //    lane quarters 0 and 1, U' (lanes 0..127, columns 384..447) as coalesced FP32 stores.
+    //    They stay in TMEM until the next item's W/U' MMAs, so each item's are written while the
+    //    next item solves for T, by warps that the solve leaves idle.
+    auto write_wu = [&](unsigned char *b, int gi, int ng) {
+        const int qd = warp & 3;
+        if (qd < 2) {
+            const int r = 32 * qd + lane;
+            for (int c32 = 0; c32 < 4 / ng; ++c32) {
+                const int col = (kD / ng) * gi + 32 * c32;
+                uint32_t wv[32];
+                tc::tmem_ld32_nowait(tb + ((uint32_t)(32 * qd) << 16) + 256 + col, wv);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    float o[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) o[t] = __uint_as_float(wv[8 * g8 + t]);
+                    st16(b + kOffW + tc::kmajor_off(r, col + 8 * g8, kD), pack8_bf16(o));
+                }
+            }
+        }
+        for (int c16 = 0; c16 < 4 / ng; ++c16) {
+            const int col = (kC / ng) * gi + 16 * c16;
+            float uv[16];
+            tc::tmem_ld16(tb + ((uint32_t)(32 * qd) << 16) + 384 + col, uv);
+            float *Up = reinterpret_cast<float *>(b + kOffUp) + 32 * qd + lane;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) Up[(col + t) * kD] = uv[t];
+        }
+    };
     bool good = true;
     bool staged = false;  // (thread 32) the next item's copies are in flight
+    bool aborted = false;
+    unsigned char *blk_prev = nullptr;  // the previous item's block: its W and U' are still in TMEM
     uint32_t done = 0;    // items processed: the phase parity of bars[0] and bars[3]
     for (; it < n_items; ++done) {
         const int chunk = it / H, h = it - chunk * H;
@@ -834,97 +868,104 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             }
         }
         __syncthreads();
-        // 6. T = (I + A)^-1 as BF16 hi and lo parts in the T tile, by blocks of 16 and a two-level
-        //    merge. Phase 0: the diagonal blocks TD, T_RR = (I + A_RR)^-1, by forward substitution
-        //    (threads 0..63, one column each) while threads 64..447 write the zero blocks above the
-        //    diagonal (columns c >= 16 (r / 16 + 1)) to the tile. With X = rows/columns 0..31 and Y = 32..63,
-        //    T_YX = -T_YY A_YX T_XX, and inside each half T_10 = -T_11 A_10 T_00,
-        //    T_32 = -T_33 A_32 T_22. Three phases:
-        //      1. Y1_p = A_(2p+1)(2p) T_(2p)(2p) (p = 0, 1), Z0 = A_Y0 T_00, Z1 = A_Y1 T_11, and
-        //         the diagonal blocks to the tile;
-        //      2. T_10 = -T_11 Y1_0, T_32 = -T_33 Y1_1 (also kept in FP32), and Y2 = A_YX T_XX,
-        //         whose left half is Z0 + A_Y1 T_10 = Z0 - Z1 Y1_0 and whose right half is Z1;
-        //      3. T_YX = -T_YY Y2.
-        //    Each product is tiled 2 x 4 per thread (rows 2 rp, 2 rp + 1; columns 4 ct .. 4 ct + 3);
-        //    the 8 lanes of a quarter warp share their rows and take consecutive column tiles.
-        float *T32 = Yv, *Y1 = GL, *Y2 = GL + 2 * kBlk * kBlk;  // T32: [16][kMS], Y1: [2][16][16], Y2: [32][kY2]
-        constexpr int kY2 = 36;
-        // phase 0
-        if (tid < kC) {
-            const int R = tid >> 4, j = tid & (kBlk - 1), nR = kBlk * R;
-            float x[kBlk];
+        if (warp >= 8) {
+            tc::fence_after_sync();
+            if (blk_prev) write_wu(blk_prev, (warp >> 2) - 2, 2);
+        } else {
+            // 6. T = (I + A)^-1 as BF16 hi and lo parts in the T tile, by blocks of 16 and a two-level
+            //    merge, by warps 0..7 (a 256-thread named barrier between phases). Phase 0: the diagonal
+            //    blocks TD, T_RR = (I + A_RR)^-1, by forward substitution (threads 0..63, one column
+            //    each) while threads 64..255 write the zero blocks above the diagonal (columns
+            //    c >= 16 (r / 16 + 1)) to the tile. With X = rows/columns 0..31 and Y = 32..63,
+            //    T_YX = -T_YY A_YX T_XX, and inside each half T_10 = -T_11 A_10 T_00,
+            //    T_32 = -T_33 A_32 T_22. Three phases:
+            //      1. Y1_p = A_(2p+1)(2p) T_(2p)(2p) (p = 0, 1), Z0 = A_Y0 T_00, Z1 = A_Y1 T_11;
+            //      2. T_10 = -T_11 Y1_0, T_32 = -T_33 Y1_1 (also kept in FP32), and Y2 = A_YX T_XX,
+            //         whose left half is Z0 + A_Y1 T_10 = Z0 - Z1 Y1_0 and whose right half is Z1;
+            //         and the diagonal blocks to the tile;
+            //      3. T_YX = -T_YY Y2.
+            //    Each product is tiled 2 x 4 per thread (rows 2 rp, 2 rp + 1; columns 4 ct .. 4 ct + 3);
+            //    the 8 lanes of a quarter warp share their rows and take consecutive column tiles.
+            float *T32 = Yv, *Y1 = GL, *Y2 = GL + 2 * kBlk * kBlk;  // T32: [16][kMS], Y1: [2][16][16], Y2: [32][kY2]
+            constexpr int kY2 = 36;
+            // phase 0
+            if (tid < kC) {
+                const int R = tid >> 4, j = tid & (kBlk - 1), nR = kBlk * R;
+                float x[kBlk];
 #pragma unroll
-            for (int r = 0; r < kBlk; ++r) {
-                float s0 = 0.f, s1 = 0.f;
+                for (int r = 0; r < kBlk; ++r) {
+                    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int i = 0; i < r; ++i) {
-                    if (i & 1) s1 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s1);
-                    else s0 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s0);
+                    for (int i = 0; i < r; ++i) {
+                        if (i & 1) s1 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s1);
+                        else s0 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s0);
+                    }
+                    x[r] = r == j ? 1.f : (r < j ? 0.f : s0 + s1);
                 }
-                x[r] = r == j ? 1.f : (r < j ? 0.f : s0 + s1);
-            }
-            // stored after the loop, so that no shared store sits between the loads of the rows
+                // stored after the loop, so that no shared store sits between the loads of the rows
 #pragma unroll
-            for (int r = 0; r < kBlk; ++r) TD[(nR + r) * kTD + j] = x[r];
-        } else if (tid < kC + 384) {
-            const int u = (tid - kC) % 192, lo = (tid - kC) / 192;  // 192 groups of 8 columns per part
-            const int r = u < 96 ? u / 6 : (u < 160 ? kBlk + (u - 96) / 4 : 2 * kBlk + (u - 160) / 2);
-            const int g = u < 96 ? 2 + u % 6 : (u < 160 ? 4 + (u - 96) % 4 : 6 + (u - 160) % 2);
-            st16(tT + tc::kmajor_off(lo * kC + r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
-        }
-        __syncthreads();
-        // phase 1 (threads 0..319)
-        if (tid < 64) {
-            const int p = tid >> 5, rp = (tid >> 2) & 7, ct = tid & 3, o = 2 * kBlk * p;
-            float c[2][4] = {};
-            tile24<kBlk / 4>(c, Mm + (o + kBlk + 2 * rp) * kMS + o, kMS, TD + o * kTD + 4 * ct, kTD);
-            put24(Y1 + p * kBlk * kBlk + 2 * rp * kBlk + 4 * ct, kBlk, c, 1.f);
-        } else if (tid < 192) {
-            const int t = tid - 64, rp = t >> 3, ct = t & 7, o = kBlk * (ct >> 2);
-            float c[2][4] = {};
-            tile24<kBlk / 4>(c, Mm + (2 * kBlk + 2 * rp) * kMS + o, kMS, TD + o * kTD + 4 * (ct & 3), kTD);
-            put24(Y2 + 2 * rp * kY2 + 4 * ct, kY2, c, 1.f);
-        } else if (tid < 320) {
-            const int t = tid - 192, R = t >> 5, r = kBlk * R + ((t >> 1) & (kBlk - 1)), g = t & 1;
-            float tv[8];
-            ld8f(TD + r * kTD + 8 * g, tv);
-            uint4 hi, lo;
-            split8(tv, hi, lo);
-            st16(tT + tc::kmajor_off(r, kBlk * R + 8 * g, kC), hi);
-            st16(tT + tc::kmajor_off(kC + r, kBlk * R + 8 * g, kC), lo);
-        }
-        __syncthreads();
-        // phase 2 (threads 0..127); each thread overwrites only its own tile of Z0
-        if (tid < 64) {
-            const int p = tid >> 5, rp = (tid >> 2) & 7, ct = tid & 3, o = 2 * kBlk * p;
-            float c[2][4] = {};
-            tile24<kBlk / 4>(c, TD + (o + kBlk + 2 * rp) * kTD, kTD, Y1 + p * kBlk * kBlk + 4 * ct, kBlk);
-            put24_split(tT, o + kBlk + 2 * rp, o + 4 * ct, c, -1.f);
-            if (p) put24(T32 + 2 * rp * kMS + 4 * ct, kMS, c, -1.f);
-        } else if (tid < 128) {
-            const int t = tid - 64, rp = t >> 2, ct = t & 3;
-            float c[2][4];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float4 z = *reinterpret_cast<const float4 *>(Y2 + (2 * rp + i) * kY2 + 4 * ct);
-                c[i][0] = -z.x; c[i][1] = -z.y; c[i][2] = -z.z; c[i][3] = -z.w;
-            }
-            tile24<kBlk / 4>(c, Y2 + 2 * rp * kY2 + kBlk, kY2, Y1 + 4 * ct, kBlk);
-            put24(Y2 + 2 * rp * kY2 + 4 * ct, kY2, c, -1.f);
-        }
-        __syncthreads();
-        // phase 3 (threads 0..127): rows 32 + 2 rp (+1); T_YY's rows are [T_22 0] for warps 0, 1
-        // and [T_32 T_33] for warps 2, 3
-        if (tid < 128) {
-            const int rp = tid >> 3, ct = tid & 7;
-            float c[2][4] = {};
-            if (warp < 2) {
-                tile24<kBlk / 4>(c, TD + (2 * kBlk + 2 * rp) * kTD, kTD, Y2 + 4 * ct, kY2);
+                for (int r = 0; r < kBlk; ++r) TD[(nR + r) * kTD + j] = x[r];
             } else {
-                tile24<kBlk / 4>(c, T32 + (2 * rp - kBlk) * kMS, kMS, Y2 + 4 * ct, kY2);
-                tile24<kBlk / 4>(c, TD + (2 * kBlk + 2 * rp) * kTD, kTD, Y2 + kBlk * kY2 + 4 * ct, kY2);
+                const int u = tid - kC;  // 192 groups of 8 columns, hi and lo parts
+                const int r = u < 96 ? u / 6 : (u < 160 ? kBlk + (u - 96) / 4 : 2 * kBlk + (u - 160) / 2);
+                const int g = u < 96 ? 2 + u % 6 : (u < 160 ? 4 + (u - 96) % 4 : 6 + (u - 160) % 2);
+                st16(tT + tc::kmajor_off(r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
+                st16(tT + tc::kmajor_off(kC + r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
             }
-            put24_split(tT, 2 * kBlk + 2 * rp, 4 * ct, c, -1.f);
+            named_bar_sync(1, 256);
+            // phase 1 (threads 0..191)
+            if (tid < 64) {
+                const int p = tid >> 5, rp = (tid >> 2) & 7, ct = tid & 3, o = 2 * kBlk * p;
+                float c[2][4] = {};
+                tile24<kBlk / 4>(c, Mm + (o + kBlk + 2 * rp) * kMS + o, kMS, TD + o * kTD + 4 * ct, kTD);
+                put24(Y1 + p * kBlk * kBlk + 2 * rp * kBlk + 4 * ct, kBlk, c, 1.f);
+            } else if (tid < 192) {
+                const int t = tid - 64, rp = t >> 3, ct = t & 7, o = kBlk * (ct >> 2);
+                float c[2][4] = {};
+                tile24<kBlk / 4>(c, Mm + (2 * kBlk + 2 * rp) * kMS + o, kMS, TD + o * kTD + 4 * (ct & 3), kTD);
+                put24(Y2 + 2 * rp * kY2 + 4 * ct, kY2, c, 1.f);
+            }
+            named_bar_sync(1, 256);
+            // phase 2; each thread overwrites only its own tile of Z0
+            if (tid < 64) {
+                const int p = tid >> 5, rp = (tid >> 2) & 7, ct = tid & 3, o = 2 * kBlk * p;
+                float c[2][4] = {};
+                tile24<kBlk / 4>(c, TD + (o + kBlk + 2 * rp) * kTD, kTD, Y1 + p * kBlk * kBlk + 4 * ct, kBlk);
+                put24_split(tT, o + kBlk + 2 * rp, o + 4 * ct, c, -1.f);
+                if (p) put24(T32 + 2 * rp * kMS + 4 * ct, kMS, c, -1.f);
+            } else if (tid < 128) {
+                const int t = tid - 64, rp = t >> 2, ct = t & 3;
+                float c[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const float4 z = *reinterpret_cast<const float4 *>(Y2 + (2 * rp + i) * kY2 + 4 * ct);
+                    c[i][0] = -z.x; c[i][1] = -z.y; c[i][2] = -z.z; c[i][3] = -z.w;
+                }
+                tile24<kBlk / 4>(c, Y2 + 2 * rp * kY2 + kBlk, kY2, Y1 + 4 * ct, kBlk);
+                put24(Y2 + 2 * rp * kY2 + 4 * ct, kY2, c, -1.f);
+            } else {
+                const int t = tid - 128, R = t >> 5, r = kBlk * R + ((t >> 1) & (kBlk - 1)), g = t & 1;
+                float tv[8];
+                ld8f(TD + r * kTD + 8 * g, tv);
+                uint4 hi, lo;
+                split8(tv, hi, lo);
+                st16(tT + tc::kmajor_off(r, kBlk * R + 8 * g, kC), hi);
+                st16(tT + tc::kmajor_off(kC + r, kBlk * R + 8 * g, kC), lo);
+            }
+            named_bar_sync(1, 256);
+            // phase 3 (threads 0..127): rows 32 + 2 rp (+1); T_YY's rows are [T_22 0] for warps 0, 1
+            // and [T_32 T_33] for warps 2, 3
+            if (tid < 128) {
+                const int rp = tid >> 3, ct = tid & 7;
+                float c[2][4] = {};
+                if (warp < 2) {
+                    tile24<kBlk / 4>(c, TD + (2 * kBlk + 2 * rp) * kTD, kTD, Y2 + 4 * ct, kY2);
+                } else {
+                    tile24<kBlk / 4>(c, T32 + (2 * rp - kBlk) * kMS, kMS, Y2 + 4 * ct, kY2);
+                    tile24<kBlk / 4>(c, TD + (2 * kBlk + 2 * rp) * kTD, kTD, Y2 + kBlk * kY2 + 4 * ct, kY2);
+                }
+                put24_split(tT, 2 * kBlk + 2 * rp, 4 * ct, c, -1.f);
+            }
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
@@ -948,40 +989,20 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             stage(nxt);
             staged = true;
         }
-        // 8. W: warps on lane quarters 0 and 1 (rows 0..63), 32 channels each, as BF16 16-byte
-        //    chunks; U': every warp, 16 rows r of its 32 lanes v, coalesced FP32 stores
-        if (good) {
-            const int qd = warp & 3, part = warp >> 2;
-            if (qd < 2) {
-                const int r = 32 * qd + lane;
-                uint32_t wv[32];
-                tc::tmem_ld32_nowait(tb + ((uint32_t)(32 * qd) << 16) + 256 + 32 * part, wv);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
-                    float o[8];
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) o[t] = __uint_as_float(wv[8 * g8 + t]);
-                    st16(blk + kOffW + tc::kmajor_off(r, 32 * part + 8 * g8, kD), pack8_bf16(o));
-                }
-            }
-            float uv[16];
-            tc::tmem_ld16(tb + ((uint32_t)(32 * qd) << 16) + 384 + 16 * part, uv);
-            float *Up = reinterpret_cast<float *>(blk + kOffUp) + 32 * qd + lane;
-#pragma unroll
-            for (int t = 0; t < 16; ++t) Up[(16 * part + t) * kD] = uv[t];
-        }
+        blk_prev = blk;
         tc::fence_before_sync();
         const bool bad = __syncthreads_or(!good);
         tc::fence_after_sync();
         if (bad) {
             if (tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
+            aborted = true;
             break;
         }
         it = nxt;
     }
     // after an abort the next item's copies may still be in flight: wait for them (bounded)
     if (staged) mbar_wait_bounded(bars, (done + 1) & 1u, kTcWaitLimit);
+    if (!aborted && blk_prev) write_wu(blk_prev, warp >> 2, 4);  // the last item's W and U'
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
