@@ -1398,11 +1398,13 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         if (mbar_wait_bounded(&bar[4], (uint32_t)(it & 1), kTcWaitLimit)) gpar = -1;
         else good = false;
         {
+            // lane t forms the RMS factor of token r0 + t once; the loop takes it by shuffle
+            const float4 pl = reinterpret_cast<const float4 *>(red)[r0 + lane];
+            const float rinv_l = rsqrt_ftz(((pl.x + pl.y) + (pl.z + pl.w)) * (1.0f / kD) + rms_eps);
             __nv_bfloat16 y[32];
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
-                const float4 pq = reinterpret_cast<const float4 *>(red)[r0 + r];
-                const float rinv = rsqrt_ftz(((pq.x + pq.y) + (pq.z + pq.w)) * (1.0f / kD) + rms_eps);
+                const float rinv = __shfl_sync(0xFFFFFFFFu, rinv_l, r);
                 const float gv = __bfloat162float(sGY[(r0 + r) * kD + vi]);
                 // sigmoid(g) = (1 + tanh(g/2)) / 2; the hardware tanh's error is below the BF16
                 // rounding of the output it multiplies
