@@ -33,8 +33,11 @@ struct MultiStage {
 
 constexpr uint32_t kMultiWaitLimit = 1u << 26;
 
-template <typename T>
-__global__ void __launch_bounds__(256, 1)
+// NST stage buffers per CTA. NST = 1 fits two CTAs (two units) on an SM, so that one unit's
+// serial token chain overlaps the other's; NST = 2 keeps one CTA per SM and prefetches its
+// next unit instead.
+template <typename T, int NST>
+__global__ void __launch_bounds__(256, 3 - NST)
 decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
                     const float *__restrict__ A_log, const float *__restrict__ norm_w,
                     float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__restrict__ err,
@@ -46,10 +49,11 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
     using L = MultiStage<T>;
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int kNT = KDA_DECODE_MAX_TOKENS;
-    float *sh_k = reinterpret_cast<float *>(smem + 2 * L::kBytes);  // [token][d] k^ of every token
+    float *sh_k = reinterpret_cast<float *>(smem + NST * L::kBytes);  // [token][d] k^ of every token
     float *sh_q = sh_k + kNT * kD, *sh_a = sh_q + kNT * kD, *sh_v = sh_a + kNT * kD, *sh_gw = sh_v + kNT * kD;
-    float *sh_ak = sh_gw + kNT * kD, *sh_aq = sh_ak + kNT * kD;  // alpha k^ and alpha q^ per row
-    float *su = sh_aq + kNT * kD, *so = su + kD;  // [d] u and o of the current token
+    // NST = 2: alpha k^ and alpha q^ per row; NST = 1 forms them on the fly and sh_q holds q^
+    float *sh_ak = sh_gw + kNT * kD, *sh_aq = sh_ak + kNT * kD;
+    float *su = (NST == 2 ? sh_aq + kNT * kD : sh_gw + kNT * kD), *so = su + kD;  // [d] u, o of the current token
     float *red = so + kD;                          // [2][8][d] warp partials
     float *part = red + 2 * 8 * kD;                // [token][3][4] quarter sums of squares
     float *sbeta = part + kNT * 12;                                  // [token] beta
@@ -65,8 +69,7 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
     const T *src5[5] = {q, k, v, z, g};
 
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int i = 0; i < NST; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -95,8 +98,9 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
     bool timed_out = false;
     int it = 0;
     for (int u = u_begin; u < u_end; ++u, ++it) {
-        const int stage = it & 1;
-        if (tid == 0 && u + 1 < u_end) issue(stage ^ 1, u + 1);  // the other stage is free
+        const int stage = NST == 2 ? (it & 1) : 0;
+        if (NST == 2 && tid == 0 && u + 1 < u_end) issue(stage ^ 1, u + 1);  // the other stage is free
+        if (NST == 1 && tid == 0 && it > 0) issue(0, u);  // the previous unit ended with a barrier
         const int h = u / B, r = u - (u / B) * B;
         const int slot = slots[r];
         const bool bad = slot < 0 || slot >= max_slots;
@@ -111,7 +115,7 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
         for (int x = 0; x < 3; ++x) wt[x] = __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)x * D + pc) * kK));
         const float dti = __ldg(dt_bias + pc), nwi = __ldg(norm_w + pi);
         const float eA = expf(__ldg(A_log + h));
-        const bool ok = mbar_wait_bounded(&bar[stage], (uint32_t)((it >> 1) & 1), kMultiWaitLimit);
+        const bool ok = mbar_wait_bounded(&bar[stage], (uint32_t)((NST == 2 ? it >> 1 : it) & 1), kMultiWaitLimit);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         if (bad) {
             if (tid == 0) atomicExch(err, kErrBadSlot);
@@ -159,8 +163,12 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
                 const float rk = rsqrt_ftz((pt[4] + pt[5] + pt[6] + pt[7]) + l2_eps);
                 const float kn = sh_k[t * kD + i] * rk, qn = sh_q[t * kD + i] * rq, a = sh_a[t * kD + i];
                 sh_k[t * kD + i] = kn;
-                sh_ak[t * kD + i] = a * kn;
-                sh_aq[t * kD + i] = a * qn;
+                if constexpr (NST == 2) {
+                    sh_ak[t * kD + i] = a * kn;
+                    sh_aq[t * kD + i] = a * qn;
+                } else {
+                    sh_q[t * kD + i] = qn;
+                }
             }
             __syncthreads();
         }
@@ -173,9 +181,9 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
             const float skk = pt[4] + pt[5] + pt[6] + pt[7];
             const float sqk = pt[8] + pt[9] + pt[10] + pt[11];
             const float kq = sqk * (q_scale * rsqrt_ftz(sqq + l2_eps)) * (rsqrt_ftz(skk + l2_eps));
-            decode_token_step<T>(s, sh_ak + t * kD, sh_aq + t * kD, sh_a + t * kD, sh_k + t * kD, sh_v + t * kD,
-                                 sh_gw + t * kD, sbeta[t], kq, red, su, so, out + row * D + (size_t)h * kD, rms_eps,
-                                 w, l);
+            decode_token_step<T, NST == 1>(s, sh_ak + t * kD, (NST == 2 ? sh_aq : sh_q) + t * kD, sh_a + t * kD,
+                                           sh_k + t * kD, sh_v + t * kD, sh_gw + t * kD, sbeta[t], kq, red, su, so,
+                                           out + row * D + (size_t)h * kD, rms_eps, w, l);
         }
         // the state after the run, and the new history (the last three raw inputs)
         float4 *S4 = reinterpret_cast<float4 *>(S_all + ((size_t)slot * H + h) * kD * kD);
@@ -197,14 +205,16 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
     if (timed_out) {
         if (tid == 0) {
             atomicExch(err, KDA_ERR_TIMEOUT);
-            // the copy for the next unit may still be in flight
-            if (u_begin + it + 1 < u_end) mbar_wait_bounded(&bar[(it + 1) & 1], (uint32_t)(((it + 1) >> 1) & 1), kMultiWaitLimit);
+            // copies that may still be in flight: the next unit's (NST = 2) or the one waited on
+            if (NST == 2 && u_begin + it + 1 < u_end)
+                mbar_wait_bounded(&bar[(it + 1) & 1], (uint32_t)(((it + 1) >> 1) & 1), kMultiWaitLimit);
+            if (NST == 1) mbar_wait_bounded(&bar[0], (uint32_t)(it & 1), kMultiWaitLimit);  // the copy that timed out
         }
         __syncthreads();
     }
 }
 
-template <typename T>
+template <typename T, int NST>
 cudaError_t launch_multi_typed(const State &st, const kda_layer_params &p, const int32_t *slots, int B, int n,
                                const void *q, const void *k, const void *v, const void *z, const void *b,
                                const void *g, void *out, cudaStream_t stream)
@@ -212,17 +222,18 @@ cudaError_t launch_multi_typed(const State &st, const kda_layer_params &p, const
     using L = MultiStage<T>;
     const kda_config_t &c = st.cfg;
     const int H = c.num_heads;
-    const size_t smem = 2 * (size_t)L::kBytes + 7 * KDA_DECODE_MAX_TOKENS * kD * 4 + 2 * kD * 4 + 2 * 8 * kD * 4 +
-                        KDA_DECODE_MAX_TOKENS * 13 * 4 + 2 * 8;
-    cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = NST * (size_t)L::kBytes + (NST == 2 ? 7 : 5) * KDA_DECODE_MAX_TOKENS * kD * 4 + 2 * kD * 4 +
+                        2 * 8 * kD * 4 + KDA_DECODE_MAX_TOKENS * 13 * 4 + 2 * 8;
+    cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<T, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, st.device);
     if (e != cudaSuccess) return e;
     const int n_units = B * H;
-    const int grid = n_units < sms ? n_units : sms;
-    decode_multi_kernel<T><<<grid, 256, smem, stream>>>(
+    const int ctas = (3 - NST) * sms;  // CTAs resident at once
+    const int grid = n_units < ctas ? n_units : ctas;
+    decode_multi_kernel<T, NST><<<grid, 256, smem, stream>>>(
         p.conv_w, p.dt_bias, p.A_log, p.norm_w, st.S, (T *)st.tail, st.err, slots, B, n, H, st.max_slots,
         (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, (const T *)g, (T *)out,
         c.gate_lower_bound, c.l2_eps, c.rms_eps, c.q_scale);
@@ -236,8 +247,8 @@ cudaError_t launch_decode_multi(const State &st, const kda_layer_params &p, cons
                                 const void *g, void *out, cudaStream_t stream)
 {
     if (st.cfg.io_dtype == KDA_BF16)
-        return launch_multi_typed<__nv_bfloat16>(st, p, slots, B, n, q, k, v, z, b, g, out, stream);
-    return launch_multi_typed<float>(st, p, slots, B, n, q, k, v, z, b, g, out, stream);
+        return launch_multi_typed<__nv_bfloat16, 1>(st, p, slots, B, n, q, k, v, z, b, g, out, stream);
+    return launch_multi_typed<float, 2>(st, p, slots, B, n, q, k, v, z, b, g, out, stream);
 }
 
 }  // namespace kda

@@ -129,3 +129,35 @@ def test_speculative_rollback_and_argument_errors():
         assert K.kda_state_poll_error(st) == 0  # nothing was enqueued
     finally:
         K.kda_state_free(st)
+
+
+def test_bad_slot_then_good_units_in_one_cta():
+    """384 units (B = 4 at H = 96) give some CTAs two units, so a skipped unit (row 0, bad
+    slot) is followed by a good one in the same CTA: rows 1..3 must equal a run without
+    the bad row, bit for bit, and the error word records the bad id."""
+    H, d, B, n = 96, 128, 4, 2
+    p = KI.make_params(H, d, 4, 17)
+    tok = KI.make_tokens(B * n, H, d, 17, bf16=True)
+    S0 = KI.make_state(B, H, d, 17)
+    T0 = KI.make_tail(B, H, d, 4, 17, bf16=True)
+    cfg = K.kda_config(H, d, K.KDA_BF16)
+    params = dev_params(p)
+    st = K.kda_state_alloc(cfg, 2 * B)
+    try:
+        upload_state(cfg, st, list(range(B)), S0, T0)
+        upload_state(cfg, st, list(range(B, 2 * B)), S0, T0)
+        t = dev_tokens(tok, True)
+        out_bad = torch.zeros(B * n, H * d, device="cuda", dtype=torch.bfloat16)
+        slots_bad = torch.tensor([9 * B, 1, 2, 3], dtype=torch.int32, device="cuda")
+        K.kda_decode_tokens(cfg, params, st, slots_bad, n, t["q"], t["k"], t["v"], t["z"], t["b"], t["g"], out_bad)
+        assert K.kda_state_poll_error(st) == K.KDA_ERR_DEVICE
+        out_ok = torch.zeros(B * n, H * d, device="cuda", dtype=torch.bfloat16)
+        slots_ok = torch.tensor([B, B + 1, B + 2, B + 3], dtype=torch.int32, device="cuda")
+        K.kda_decode_tokens(cfg, params, st, slots_ok, n, t["q"], t["k"], t["v"], t["z"], t["b"], t["g"], out_ok)
+        assert K.kda_state_poll_error(st) == 0
+        assert torch.equal(out_bad[n:], out_ok[n:])
+        Sa, ta = download_state(cfg, st, [1, 2, 3])
+        Sb, tb = download_state(cfg, st, [B + 1, B + 2, B + 3])
+        assert np.array_equal(Sa, Sb) and np.array_equal(ta, tb)
+    finally:
+        K.kda_state_free(st)
