@@ -43,7 +43,7 @@ PRE_FLOP_PER_TOKEN_HEAD = 2 * (3 * DH * DH + 5 * CHUNK * DH)
 PRE_BYTES_PER_TOKEN = (5 * D + H + D) * 2
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch at B=256,
 # from one ncu capture of the decode kernel as it stands; None once that kernel changes.
-DEC_TRAFFIC_B256 = 1_699_831_040 + 1_611_405_056
+DEC_TRAFFIC_B256 = 1_699_824_128 + 1_611_796_992
 
 
 def _peaks():
