@@ -434,6 +434,54 @@ def _time_prefill(K, args, cfg, params, gen, dev, stream):
     return pre_ms
 
 
+HIDDEN = 7168  # Kimi K3 hidden width (the input side of the gate/beta projections)
+
+
+def _time_gate_proj(K, args, gen, dev, stream, reps=20):
+    """kda_gate_proj on T = prefill-length tokens at hidden 7168, 96 heads; L2 flushed
+    (256 MB written) before every timed call, so each call reads x and the weights from HBM."""
+    import torch
+    T = args.prefill_tokens
+    bf = torch.bfloat16
+    gcfg = K.kda_config(H, DH, K.KDA_BF16)
+    x = torch.randn(T, HIDDEN, generator=gen, device=dev).to(bf)
+    fa = (torch.randn(DH, HIDDEN, generator=gen, device=dev) * HIDDEN ** -0.5).to(bf)
+    fb = (torch.randn(D, DH, generator=gen, device=dev) * DH ** -0.5).to(bf)
+    bp = (torch.randn(H, HIDDEN, generator=gen, device=dev) * HIDDEN ** -0.5).to(bf)
+    z = torch.empty(T, D, dtype=bf, device=dev)
+    b = torch.empty(T, H, dtype=bf, device=dev)
+    ws = torch.empty(K.kda_gate_proj_workspace_bytes(gcfg, HIDDEN, T), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        K.kda_gate_proj(gcfg, x, fa, fb, bp, z, b, ws, stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        K.kda_gate_proj(gcfg, x, fa, fb, bp, z, b, ws, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(c) for a, c in ev)
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    flop = 2 * T * (HIDDEN * (DH + H) + DH * D)
+    nbytes = 2 * (T * HIDDEN + T * D + T * H + (DH + H) * HIDDEN + D * DH)
+    peaks = _peaks()
+    src = "of measured" if peaks["source"] == "measured" else "of fallback"
+    tf, gbs = flop / (ms / 1e3) / 1e12, nbytes / (ms / 1e3) / 1e9
+    del x, z, ws, flush
+    torch.cuda.empty_cache()
+    return {"workload": f"kda_gate_proj: z = W_fb(W_fa x), b = W_b x for T={T} tokens, hidden {HIDDEN}, "
+                        f"96 heads x 128, BF16 in/out, FP32 accumulation (L2 flushed before each call)",
+            "ms": ms, "value": T / (ms / 1e3), "unit": "tokens/s", "reps": reps,
+            "gpu_launches_per_call": 2,  # gp_in_kernel, gp_out_kernel (+ a 4-byte memset)
+            "roofline_hbm": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": gbs / peaks["hbm_gbs"], "bytes_per_call": nbytes, "peak_note": src},
+            "roofline_tensor": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                                "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "flop_per_call": flop,
+                                "peak_note": src}}
+
+
 def _time_varlen(K, args, cfg, params, gen, dev, stream):
     """Varlen workload: 16 sequences ~U[512, 16384] (seeded lengths), prefill all, snapshot /
     reset / restore sequences 0-7, then 128 batched decode steps; tokens/s of both phases."""
@@ -617,6 +665,12 @@ def run_kda(args):
             line["value"] = Tp / (pre_ms / 1e3)
             line["ms_per_step"] = pre_ms
             line["gpu_launches"] = 3 * args.prefill_reps
+    if args.only in ("all", "gate_proj"):
+        line["gate_proj"] = _time_gate_proj(K, args, gen, dev, stream)
+        if args.only == "gate_proj":
+            line["value"] = line["gate_proj"]["value"]
+            line["ms_per_step"] = line["gate_proj"]["ms"]
+            line["gpu_launches"] = 2 * line["gate_proj"]["reps"]
     if args.only == "all":
         line["varlen"] = _time_varlen(K, args, cfg, params, gen, dev, stream)
         line["photo"] = _time_photo(K, cfg, params, gen, dev, stream,
@@ -641,7 +695,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
     ap.add_argument("--prefill-reps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "gate_proj"], default="all",
                     help="time one part only (small profiling runs); the JSON line keeps its keys")
     ap.add_argument("--batch", type=int, default=B_DEC, help="decode batch (profiling runs)")
     ap.add_argument("--prefill-tokens", type=int, default=T_PRE, help="prefill length (profiling runs)")

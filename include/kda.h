@@ -262,6 +262,42 @@ kda_status kda_prefill_noalloc(const kda_config_t *cfg, const kda_layer_params *
                                const void *b, const void *g, void *out, void *stream);
 
 /*
+ * The decay-gate and beta input projections of a KDA layer (kimi_k3.c header
+ * comment, block "KDA per-head recurrence": the gate pre-activation is the
+ * low-rank product W_fb (W_fa x) and the beta logit is W_b x; struct Kda:
+ * fa [hd][hidden], fb [proj][hd], bp [heads][hidden]). Per token:
+ *   f = W_fa x  (d values),  z = W_fb f  (H*d values),  b = W_b x  (H values)
+ * z and b are what kda_prefill / kda_decode_token take (dt_bias and the
+ * sigmoids are applied there).
+ *   hidden     width of x; a positive multiple of 64 (7168 for Kimi K3)
+ *   T          tokens (rows of x); 0 is a no-op
+ *   x          device BF16 [T][hidden]
+ *   w_fa       device BF16 [d][hidden]
+ *   w_fb       device BF16 [H*d][d]
+ *   w_b        device BF16 [H][hidden]
+ *   z          device BF16 [T][H*d]     out
+ *   b          device BF16 [T][H]       out (2-byte aligned)
+ *   workspace  device scratch of at least kda_gate_proj_workspace_bytes(cfg,
+ *              hidden, T) bytes, 16-byte aligned, owned by the caller. Its
+ *              first int32 is an error word: the call clears it and a kernel
+ *              writes KDA_ERR_TIMEOUT there if a bounded wait gave up (read it
+ *              after synchronising if needed). Calls that share a workspace
+ *              must be ordered.
+ * Products accumulate in FP32 on the tensor cores; f is rounded to BF16 once
+ * before the second product, and z, b are rounded to BF16 (nearest even).
+ * Needs cfg->io_dtype == KDA_BF16 and num_heads <= 128. Errors:
+ * KDA_ERR_INVALID (bad shape, dtype, alignment, NULL pointer, workspace too
+ * small), KDA_ERR_CUDA. The hidden dimension is split over several CTAs when
+ * T is small, so the workspace need depends on the current device's SM count:
+ * query it on the device that runs the call. The query returns 0 for invalid
+ * arguments.
+ */
+size_t kda_gate_proj_workspace_bytes(const kda_config_t *cfg, int32_t hidden, int64_t T);
+kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int64_t T, const void *x, const void *w_fa,
+                         const void *w_fb, const void *w_b, void *z, void *b, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/*
  * Recurrent-state photos (kimi_k3.c header, the COLI_K3_CKPT and
  * COLI_K3_CKPT_DIR serve options). A store keeps up to `capacity` photos of
  * one sequence slot across a stack of KDA layers (one kda_state per layer),

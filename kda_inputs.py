@@ -25,7 +25,8 @@ import numpy as np
 
 _STREAMS = {"conv_w": 1, "dt_bias": 2, "A_log": 3, "norm_w": 4,
             "q": 11, "k": 12, "v": 13, "z": 14, "b": 15, "g": 16,
-            "state": 21, "tail": 22, "lengths": 31, "slots": 32}
+            "state": 21, "tail": 22, "lengths": 31, "slots": 32,
+            "x": 41, "w_fa": 42, "w_fb": 43, "w_b": 44}
 
 
 def _rng(seed: int, stream: str, sub: int = 0) -> np.random.Generator:
@@ -104,6 +105,18 @@ def make_tail(n: int, H: int, d: int, K: int, seed: int, bf16: bool) -> np.ndarr
     """A filled conv history [n, 3, K-1, H*d] float32 (raw inputs, ~ N(0, 1))."""
     x = _rng(seed, "tail").standard_normal((n, 3, K - 1, H * d), dtype=np.float32)
     return bf16_round(x) if bf16 else x
+
+
+def make_gate_proj(T: int, hidden: int, H: int, d: int, seed: int, sub: int = 0) -> dict:
+    """Inputs of the gate/beta input projections, rounded to BF16 (float32 arrays):
+    hidden states x [T, hidden] ~ N(0, 1) and random-init weights scaled by their fan-in,
+    W_fa [d, hidden] ~ N(0, 1/hidden), W_fb [H*d, d] ~ N(0, 1/d), W_b [H, hidden] ~
+    N(0, 1/hidden), so that f, z and b come out ~ N(0, 1) like the mixer's inputs."""
+    x = _rng(seed, "x", sub).standard_normal((T, hidden), dtype=np.float32)
+    fa = _rng(seed, "w_fa").standard_normal((d, hidden), dtype=np.float32) * np.float32(hidden ** -0.5)
+    fb = _rng(seed, "w_fb").standard_normal((H * d, d), dtype=np.float32) * np.float32(d ** -0.5)
+    bp = _rng(seed, "w_b").standard_normal((H, hidden), dtype=np.float32) * np.float32(hidden ** -0.5)
+    return {"x": bf16_round(x), "w_fa": bf16_round(fa), "w_fb": bf16_round(fb), "w_b": bf16_round(bp)}
 
 
 def varlen_lengths(n: int, lo: int, hi: int, seed: int) -> np.ndarray:

@@ -1,0 +1,534 @@
+// kda_gate_proj.cu - the decay-gate and beta input projections of a KDA layer on
+// tcgen05 tensor cores (kimi_k3.c header comment, block "KDA per-head recurrence":
+// the decay gate's pre-activation is the low-rank product W_fb (W_fa x) and the
+// beta logit is W_b x; struct Kda stores fa as [hd][hidden], fb as [proj][hd] and
+// bp as [heads][hidden]):
+//
+//   f = W_fa x    d = 128 values per token
+//   b = W_b x     H values per token
+//   z = W_fb f    H*d values per token
+//
+// dt_bias and the sigmoids stay in the mixer kernels, which take z and b as inputs.
+//
+// Two launches on the caller's stream:
+//  1. gp_in_kernel: [f | b] = x [W_fa; W_b]^T for a tile of 128 tokens over one
+//     slice of the hidden dimension. When there are too few token tiles to fill
+//     the GPU the hidden dimension is split over several CTAs (split-K); each
+//     writes its FP32 partial sums to the caller's workspace.
+//  2. gp_out_kernel: persistent, one CTA per SM. Each CTA walks a contiguous range
+//     of (token tile, 256-column tile of z) items. On entering a token tile it adds
+//     that tile's partial sums in a fixed order (so results do not depend on
+//     timing), writes b, and rounds f to BF16 as the A operand. W_fb tiles stream
+//     through a two-stage TMA ring into two TMEM accumulators, so one item's
+//     epilogue (TMEM -> BF16 -> TMA store) runs under the next item's MMAs.
+//
+// Operand tiles are K-major without swizzle, exactly as TMA lands them: a box of
+// 8 columns (16 bytes) by R rows arrives as R consecutive 16-byte rows, so core
+// matrices adjacent along K sit R*16 bytes apart (LBO) and 8-row groups 128 bytes
+// apart (SBO). The z output is staged in the 128-byte swizzled layout (16-byte
+// chunk c of row r at chunk c ^ (r % 8)), which keeps the epilogue's shared-memory
+// writes free of bank conflicts, and leaves by TMA box stores.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "kda_internal.cuh"
+#include "kda_ptx.cuh"
+#include "kda_tc.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kGpTile = 128;      // tokens per tile (MMA M)
+constexpr int kGpKs = 64;         // hidden columns per pipeline stage
+constexpr int kGpStages = 4;      // stages of the first product's ring
+constexpr int kGpN2 = 256;        // z columns per item (MMA N of the second product)
+constexpr int kGpMaxSplit = 16;   // most hidden-dimension slices per token tile
+constexpr int kGpZBox = 64;       // z columns per TMA store box (128 bytes, the swizzle span)
+constexpr uint32_t kGpSpin = 1u << 26;
+constexpr int kGpOutThreads = 192;  // warps 0-3 epilogue, warp 4 producer, warp 5 MMA issuer
+constexpr int kGpAlign = 1024;      // slack to align the dynamic shared memory base
+
+__host__ __device__ constexpr int gp_n1(int H) { return kD + ((H + 15) / 16) * 16; }
+__host__ __device__ constexpr int gp_in_stage_bytes(int n1) { return (kGpTile + n1) * kGpKs * 2; }
+constexpr int kGpFBytes = kGpTile * kD * 2;         // f tile, BF16
+constexpr int kGpWBytes = kGpN2 * kD * 2;           // one W_fb tile, BF16
+constexpr int kGpStgWarp = 32 * kGpN2 * 2;          // one warp's z staging (32 rows x 256 columns)
+constexpr int kGpOutSmem = kGpFBytes + 2 * kGpWBytes + 4 * kGpStgWarp + 128 + kGpAlign;
+
+__device__ __forceinline__ unsigned char *align_smem(unsigned char *p)
+{
+    const uint32_t a = smem_u32(p);
+    return p + (((a + kGpAlign - 1) & ~(uint32_t)(kGpAlign - 1)) - a);
+}
+
+// AND of pred over `count` threads at named barrier `id` (also a barrier).
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// ---------------------------------------------------------------- first product
+// CTA (tile, split): [f | b] partial sums of tokens tile*128 .. +127 over hidden
+// columns [k0*64, k1*64). Thread 0 issues the TMA copies, thread 32 the MMAs; all
+// four warps then move the accumulator (TMEM lane = token) to the workspace.
+__global__ void __launch_bounds__(128, 1)
+gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_fa,
+             const __grid_constant__ CUtensorMap tm_bp, float *__restrict__ part, int T, int ksteps, int splits,
+             int n1, int x_rows, int bp_rows, int32_t *err)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = align_smem(smem_raw);
+    const int sb = gp_in_stage_bytes(n1);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kGpStages * sb);
+    uint64_t *empty = full + kGpStages;
+    uint64_t *done = empty + kGpStages;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x, split = blockIdx.y;
+    const int k0 = (int)((int64_t)split * ksteps / splits), k1 = (int)((int64_t)(split + 1) * ksteps / splits);
+    const int nk = k1 - k0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGpStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tc::tmem_alloc(tslot, 256);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    bool ok = true;
+
+    if (threadIdx.x == 0) {
+        const uint32_t bytes = (uint32_t)(x_rows + kD + bp_rows) * 16u * (kGpKs / 8);
+        int issued = 0;
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % kGpStages;
+            if (i >= kGpStages && !mbar_wait_bounded(&empty[s], ((i / kGpStages) - 1) & 1, kGpSpin)) {
+                ok = false;
+                break;
+            }
+            unsigned char *xs = smem + s * sb;
+            unsigned char *ws = xs + kGpTile * kGpKs * 2;
+            mbar_arrive_expect_tx(&full[s], bytes);
+            const int kx = (k0 + i) * kGpKs;
+#pragma unroll
+            for (int g = 0; g < kGpKs / 8; ++g) {
+                tma_load_2d(xs + g * kGpTile * 16, &tm_x, kx + 8 * g, tile * kGpTile, &full[s]);
+                tma_load_2d(ws + g * n1 * 16, &tm_fa, kx + 8 * g, 0, &full[s]);
+                tma_load_2d(ws + g * n1 * 16 + kD * 16, &tm_bp, kx + 8 * g, 0, &full[s]);
+            }
+            issued = i + 1;
+        }
+        // the last copy into each stage has landed before the CTA can exit
+        for (int i = issued > kGpStages ? issued - kGpStages : 0; i < issued; ++i)
+            if (!mbar_wait_bounded(&full[i % kGpStages], (i / kGpStages) & 1, kGpSpin)) ok = false;
+    } else if (threadIdx.x == 32) {
+        const uint32_t idesc = tc::idesc_bf16(kGpTile, n1);
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % kGpStages;
+            if (!mbar_wait_bounded(&full[s], (i / kGpStages) & 1, kGpSpin)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            const uint32_t xs = smem_u32(smem + s * sb), ws = xs + kGpTile * kGpKs * 2;
+#pragma unroll
+            for (int kk = 0; kk < kGpKs / 16; ++kk) {
+                const uint64_t a = tc::smem_desc(xs + kk * 2 * kGpTile * 16, kGpTile * 16, 128);
+                const uint64_t b = tc::smem_desc(ws + kk * 2 * n1 * 16, n1 * 16, 128);
+                tc::mma_bf16(tmem, a, b, idesc, (uint32_t)(i | kk));
+            }
+            tc::mma_commit(&empty[s]);
+        }
+        tc::mma_commit(done);
+    }
+    __syncwarp();
+
+    if (!mbar_wait_bounded(done, 0, kGpSpin)) ok = false;
+    tc::fence_after_sync();
+    const int t = tile * kGpTile + warp * 32 + lane;
+    float *dst = part + ((size_t)split * T + (size_t)t) * n1;
+    for (int c = 0; c < n1; c += 16) {
+        float v[16];
+        tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+        if (t < T) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                reinterpret_cast<float4 *>(dst + c)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+    }
+    if (!ok) atomicExch(err, KDA_ERR_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 256);
+    }
+}
+
+// ---------------------------------------------------------------- second product
+__global__ void __launch_bounds__(kGpOutThreads, 1)
+gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__ CUtensorMap tm_z,
+              const float *__restrict__ part, __nv_bfloat16 *__restrict__ bout, int T, int H, int HD, int n1,
+              int splits, int ntiles, int items, int fb_rows, int32_t *err)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = align_smem(smem_raw);
+    unsigned char *f_t = smem;                       // [16 k groups][128 rows][8 BF16]
+    unsigned char *wbuf = f_t + kGpFBytes;           // 2 x [16 k groups][256 rows][8 BF16]
+    unsigned char *stg = wbuf + 2 * kGpWBytes;       // 4 warps x 4 boxes x [32 rows][64 BF16], swizzled
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stg + 4 * kGpStgWarp);
+    uint64_t *wfull = bars, *wempty = bars + 2, *accfull = bars + 4, *ready = bars + 6, *fin = bars + 8;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 9);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i0 = (int)((int64_t)blockIdx.x * items / gridDim.x);
+    const int i1 = (int)((int64_t)(blockIdx.x + 1) * items / gridDim.x);
+    const int n = i1 - i0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 9; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    if (warp == 4) tc::tmem_alloc(tslot, 2 * kGpN2);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            bool ok = true;
+            int issued = 0;
+            const uint32_t bytes = (uint32_t)fb_rows * 16u * (kD / 8);
+            for (int j = 0; j < n; ++j) {
+                const int s = j & 1;
+                if (j >= 2 && !mbar_wait_bounded(&wempty[s], ((j >> 1) - 1) & 1, kGpSpin)) {
+                    ok = false;
+                    break;
+                }
+                const int nt = (i0 + j) % ntiles;
+                unsigned char *w = wbuf + s * kGpWBytes;
+                mbar_arrive_expect_tx(&wfull[s], bytes);
+#pragma unroll
+                for (int g = 0; g < kD / 8; ++g) tma_load_2d(w + g * kGpN2 * 16, &tm_fb, 8 * g, nt * kGpN2, &wfull[s]);
+                issued = j + 1;
+            }
+            for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+                if (!mbar_wait_bounded(&wfull[j & 1], (j >> 1) & 1, kGpSpin)) ok = false;
+            if (!ok) atomicExch(err, KDA_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        if (lane == 0) {
+            bool ok = true;
+            const uint32_t idesc = tc::idesc_bf16(kGpTile, kGpN2);
+            const uint32_t a0 = smem_u32(f_t);
+            for (int j = 0; j < n; ++j) {
+                const int s = j & 1;
+                const uint32_t par = (j >> 1) & 1;
+                if (!mbar_wait_bounded(&ready[s], par, kGpSpin) || !mbar_wait_bounded(&wfull[s], par, kGpSpin)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t b0 = smem_u32(wbuf + s * kGpWBytes);
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint64_t a = tc::smem_desc(a0 + kk * 2 * kGpTile * 16, kGpTile * 16, 128);
+                    const uint64_t b = tc::smem_desc(b0 + kk * 2 * kGpN2 * 16, kGpN2 * 16, 128);
+                    tc::mma_bf16(tmem + (uint32_t)(s * kGpN2), a, b, idesc, (uint32_t)kk);
+                }
+                tc::mma_commit(&wempty[s]);
+                tc::mma_commit(&accfull[s]);
+            }
+            // every MMA has finished with TMEM and shared memory before the CTA exits
+            tc::mma_commit(fin);
+            if (!mbar_wait_bounded(fin, 0, kGpSpin)) ok = false;
+            if (!ok) atomicExch(err, KDA_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        const int r = threadIdx.x;  // token row within the tile
+        // Sum the partials of token tile m (fixed order), round f to the BF16 A operand and,
+        // for the CTA that owns the tile's first z columns, write b.
+        auto form = [&](int m, bool with_b) {
+            const int t = m * kGpTile + r;
+            const float *row = part + (size_t)t * n1;
+            const size_t sstride = (size_t)T * n1;
+#pragma unroll 4
+            for (int g = 0; g < kD / 8; ++g) {
+                float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (t < T) {
+                    for (int s = 0; s < splits; ++s) {
+                        const float4 *p = reinterpret_cast<const float4 *>(row + s * sstride + g * 8);
+                        const float4 u = p[0], w = p[1];
+                        a[0] += u.x; a[1] += u.y; a[2] += u.z; a[3] += u.w;
+                        a[4] += w.x; a[5] += w.y; a[6] += w.z; a[7] += w.w;
+                    }
+                }
+                *reinterpret_cast<uint4 *>(f_t + g * kGpTile * 16 + r * 16) =
+                    make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]),
+                               pack_bf16(a[6], a[7]));
+            }
+            if (with_b && t < T) {
+                for (int h = 0; h < H; ++h) {
+                    float acc = 0.f;
+                    for (int s = 0; s < splits; ++s) acc += row[s * sstride + kD + h];
+                    bout[(size_t)t * H + h] = __float2bfloat16_rn(acc);
+                }
+            }
+            tc::fence_smem_to_async();
+            named_bar_sync(1, 128);
+        };
+
+        bool ok = true;
+        if (n > 0) {
+            form(i0 / ntiles, i0 % ntiles == 0);
+            if (r == 0) mbar_arrive(&ready[0]);
+        }
+        unsigned char *my = stg + warp * kGpStgWarp;
+        for (int j = 0; j < n; ++j) {
+            const int gi = i0 + j, m = gi / ntiles, nt = gi % ntiles, s = j & 1;
+            const bool next_same = j + 1 < n && (gi + 1) / ntiles == m;
+            // the next item reuses this f tile: let its MMAs start now (its accumulator was
+            // released by the barrier at the end of the previous item)
+            if (next_same && r == 0) mbar_arrive(&ready[(j + 1) & 1]);
+            ok = named_bar_and(2, 128, mbar_wait_bounded(&accfull[s], (j >> 1) & 1, kGpSpin));
+            if (!ok) break;
+            tc::fence_after_sync();
+            // this warp's previous stores have finished reading its staging buffer
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            const uint32_t tbase = tmem + (uint32_t)(s * kGpN2) + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < kGpN2 / 32; ++c) {
+                uint32_t v[32];
+                tc::tmem_ld32_nowait(tbase + (uint32_t)(c * 32), v);
+                tc::tmem_wait_ld();
+                // columns c*32 .. +31 = 16-byte chunks (c&1)*4 .. +3 of box c/2
+                unsigned char *box = my + (c >> 1) * (32 * kGpZBox * 2) + lane * (kGpZBox * 2);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = ((c & 1) * 4 + q) ^ (lane & 7);
+                    *reinterpret_cast<uint4 *>(box + chunk * 16) = make_uint4(
+                        pack_bf16(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                        pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                        pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                        pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                }
+            }
+            tc::fence_smem_to_async();
+            __syncwarp();
+            if (lane == 0) {
+                const int y = m * kGpTile + warp * 32;
+                if (y < T) {
+#pragma unroll
+                    for (int bx = 0; bx < kGpN2 / kGpZBox; ++bx) {
+                        const int x = nt * kGpN2 + bx * kGpZBox;
+                        if (x < HD) tma_store_2d(&tm_z, x, y, my + bx * (32 * kGpZBox * 2));
+                    }
+                }
+                bulk_commit_group();
+            }
+            // every warp has read its lanes of accumulator s
+            tc::fence_before_sync();
+            named_bar_sync(1, 128);
+            if (j + 1 < n && !next_same) {
+                // MMAs of item j are complete (accfull waited), so the f tile is free
+                form((gi + 1) / ntiles, (gi + 1) % ntiles == 0);
+                if (r == 0) mbar_arrive(&ready[(j + 1) & 1]);
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        if (!ok && r == 0) atomicExch(err, KDA_ERR_TIMEOUT);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 4) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 2 * kGpN2);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+thread_local char g_msg[256];
+
+kda_status gp_fail(kda_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return record_error(s, g_msg);
+}
+
+cudaError_t encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                      uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz)
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            fn = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// hidden-dimension slices per token tile: enough CTAs to cover the SMs, at most
+// kGpMaxSplit and never more than the 64-column steps there are
+int gp_splits(int64_t mtiles, int ksteps, int sms)
+{
+    int64_t s = mtiles >= sms ? 1 : sms / mtiles;
+    if (s > kGpMaxSplit) s = kGpMaxSplit;
+    if (s > ksteps) s = ksteps;
+    return s < 1 ? 1 : (int)s;
+}
+
+// Host-side argument checks that need no device; returns KDA_OK or the status.
+kda_status gp_check(const kda_config_t *cfg, int32_t hidden, int64_t T)
+{
+    if (!config_ok(cfg)) return KDA_ERR_INVALID;
+    if (cfg->io_dtype != KDA_BF16)
+        return gp_fail(KDA_ERR_INVALID, "kda_gate_proj supports BF16 I/O only (io_dtype must be KDA_BF16)");
+    if (cfg->num_heads > 128) return gp_fail(KDA_ERR_INVALID, "kda_gate_proj needs num_heads <= 128 (got %d)", cfg->num_heads);
+    if (hidden < kGpKs || hidden % kGpKs != 0)
+        return gp_fail(KDA_ERR_INVALID, "hidden must be a positive multiple of %d (got %d)", kGpKs, hidden);
+    if (T < 0) return gp_fail(KDA_ERR_INVALID, "T must be >= 0 (got %lld)", (long long)T);
+    const int64_t ntiles = ((int64_t)cfg->num_heads * kD + kGpN2 - 1) / kGpN2;
+    if (T > INT_MAX || ((T + kGpTile - 1) / kGpTile) * ntiles > INT_MAX)
+        return gp_fail(KDA_ERR_INVALID, "T = %lld is too large for one call", (long long)T);
+    return KDA_OK;
+}
+
+kda_status gp_sms(int *sms)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return gp_fail(KDA_ERR_CUDA, "kda_gate_proj: device query failed: %s", cudaGetErrorString(e));
+    }
+    return KDA_OK;
+}
+
+constexpr size_t kGpErrBytes = 256;  // the error word, padded so the partial sums stay aligned
+
+size_t gp_workspace(const kda_config_t &cfg, int32_t hidden, int64_t T, int sms, int *splits_out)
+{
+    const int64_t mtiles = (T + kGpTile - 1) / kGpTile;
+    const int splits = gp_splits(mtiles, hidden / kGpKs, sms);
+    if (splits_out) *splits_out = splits;
+    return kGpErrBytes + (size_t)splits * (size_t)T * (size_t)gp_n1(cfg.num_heads) * sizeof(float);
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" size_t kda_gate_proj_workspace_bytes(const kda_config_t *cfg, int32_t hidden, int64_t T)
+{
+    if (kda::gp_check(cfg, hidden, T) != KDA_OK) return 0;
+    int sms = 0;
+    if (kda::gp_sms(&sms) != KDA_OK) return 0;
+    return kda::gp_workspace(*cfg, hidden, T, sms, nullptr);
+}
+
+extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int64_t T, const void *x,
+                                    const void *w_fa, const void *w_fb, const void *w_b, void *z, void *b,
+                                    void *workspace, size_t workspace_bytes, void *stream)
+{
+    using namespace kda;
+    kda_status st = gp_check(cfg, hidden, T);
+    if (st != KDA_OK) return st;
+    if (!workspace) return gp_fail(KDA_ERR_INVALID, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return gp_fail(KDA_ERR_INVALID, "workspace is not 16-byte aligned");
+    if (T == 0) return KDA_OK;
+    if (!x || !w_fa || !w_fb || !w_b || !z || !b) return gp_fail(KDA_ERR_INVALID, "a tensor pointer is NULL");
+    const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_fa) |
+                         reinterpret_cast<uintptr_t>(w_fb) | reinterpret_cast<uintptr_t>(w_b) |
+                         reinterpret_cast<uintptr_t>(z);
+    if (al & 15u) return gp_fail(KDA_ERR_INVALID, "x, w_fa, w_fb, w_b or z is not 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(b) & 1u) return gp_fail(KDA_ERR_INVALID, "b is not 2-byte aligned");
+    int sms = 0;
+    if ((st = gp_sms(&sms)) != KDA_OK) return st;
+    int splits = 1;
+    const size_t need = gp_workspace(*cfg, hidden, T, sms, &splits);
+    if (workspace_bytes < need)
+        return gp_fail(KDA_ERR_INVALID, "workspace holds %zu bytes; this call needs %zu", workspace_bytes, need);
+
+    const int H = cfg->num_heads, HD = H * kD, n1 = gp_n1(H);
+    const int mtiles = (int)((T + kGpTile - 1) / kGpTile);
+    const int ntiles = (HD + kGpN2 - 1) / kGpN2;
+    const int items = mtiles * ntiles;
+    // boxes never taller than their tensor
+    const int x_rows = (int)(T < kGpTile ? T : kGpTile);
+    const int fb_rows = HD < kGpN2 ? HD : kGpN2;
+    const int z_rows = (int)(T < 32 ? T : 32);
+    CUtensorMap tm_x, tm_fa, tm_bp, tm_fb, tm_z;
+    cudaError_t e;
+    if ((e = encode_2d(&tm_x, x, hidden, T, (uint64_t)hidden * 2, 8, x_rows, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+            cudaSuccess ||
+        (e = encode_2d(&tm_fa, w_fa, hidden, kD, (uint64_t)hidden * 2, 8, kD, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+            cudaSuccess ||
+        (e = encode_2d(&tm_bp, w_b, hidden, H, (uint64_t)hidden * 2, 8, H, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+            cudaSuccess ||
+        (e = encode_2d(&tm_fb, w_fb, kD, HD, kD * 2, 8, fb_rows, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess ||
+        (e = encode_2d(&tm_z, z, HD, T, (uint64_t)HD * 2, kGpZBox, z_rows, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            cudaSuccess)
+        return gp_fail(KDA_ERR_CUDA, "kda_gate_proj: tensor map encoding failed: %s", cudaGetErrorString(e));
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t *err = static_cast<int32_t *>(workspace);
+    float *part = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + kGpErrBytes);
+    const int in_smem = kGpStages * gp_in_stage_bytes(n1) + 128 + kGpAlign;
+    if ((e = cudaMemsetAsync(err, 0, sizeof(int32_t), s)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(gp_in_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, in_smem)) !=
+            cudaSuccess ||
+        (e = cudaFuncSetAttribute(gp_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGpOutSmem)) !=
+            cudaSuccess)
+        return gp_fail(KDA_ERR_CUDA, "kda_gate_proj: %s", cudaGetErrorString(e));
+    gp_in_kernel<<<dim3(mtiles, splits), 128, in_smem, s>>>(tm_x, tm_fa, tm_bp, part, (int)T, hidden / kGpKs,
+                                                            splits, n1, x_rows, H, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return gp_fail(KDA_ERR_CUDA, "gp_in_kernel launch: %s", cudaGetErrorString(e));
+    const int grid = items < sms ? items : sms;
+    gp_out_kernel<<<grid, kGpOutThreads, kGpOutSmem, s>>>(tm_fb, tm_z, part, static_cast<__nv_bfloat16 *>(b),
+                                                          (int)T, H, HD, n1, splits, ntiles, items, fb_rows, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return gp_fail(KDA_ERR_CUDA, "gp_out_kernel launch: %s", cudaGetErrorString(e));
+    return KDA_OK;
+}

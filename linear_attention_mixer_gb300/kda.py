@@ -78,6 +78,9 @@ SIGNATURES = [
     ("kda_prefill_noalloc", _I32, [ctypes.POINTER(kda_config_t), ctypes.POINTER(kda_layer_params), _VP, _VP, _I32,
                                    _VP, _VP, _VP, _PI32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("kda_state_poll_error", _I32, [_VP, _PI32]),
+    ("kda_gate_proj_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(kda_config_t), _I32, ctypes.c_int64]),
+    ("kda_gate_proj", _I32, [ctypes.POINTER(kda_config_t), _I32, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP,
+                             _VP, ctypes.c_size_t, _VP]),
     ("kda_photo_store_create", _I32, [_I32, ctypes.c_char_p, ctypes.POINTER(_VP)]),
     ("kda_photo_store_free", _I32, [_VP]),
     ("kda_photo_count", _I32, [_VP]),
@@ -281,6 +284,28 @@ def kda_prefill_noalloc(cfg: kda_config_t, params: kda_layer_params, S: torch.Te
                                      _dev(cu_seqlens, torch.int32, "cu_seqlens"), cu_p, N,
                                      _dev(q, dt, "q"), _dev(k, dt, "k"), _dev(v, dt, "v"), _dev(z, dt, "z"),
                                      _dev(b, dt, "b"), _dev(g, dt, "g"), _dev(out, dt, "out"), _stream(stream)))
+
+
+def kda_gate_proj_workspace_bytes(cfg: kda_config_t, hidden: int, T: int) -> int:
+    return int(lib().kda_gate_proj_workspace_bytes(ctypes.byref(cfg), int(hidden), int(T)))
+
+
+def kda_gate_proj(cfg: kda_config_t, x, w_fa, w_fb, w_b, z, b, workspace: torch.Tensor, stream=None) -> None:
+    """z = W_fb (W_fa x), b = W_b x for x [T, hidden]; every tensor BF16 except the
+    workspace (any dtype, at least kda_gate_proj_workspace_bytes bytes)."""
+    H, d = cfg.num_heads, cfg.head_dim
+    if x.dim() != 2:
+        raise ValueError("x must be [T, hidden]")
+    T, hidden = int(x.shape[0]), int(x.shape[1])
+    for name, t, shape in (("w_fa", w_fa, (d, hidden)), ("w_fb", w_fb, (H * d, d)), ("w_b", w_b, (H, hidden)),
+                           ("z", z, (T, H * d)), ("b", b, (T, H))):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {list(shape)}, got {list(t.shape)}")
+    bf = torch.bfloat16
+    ws = _dev(workspace, None, "workspace")
+    _check(lib().kda_gate_proj(ctypes.byref(cfg), hidden, T, _dev(x, bf, "x"), _dev(w_fa, bf, "w_fa"),
+                               _dev(w_fb, bf, "w_fb"), _dev(w_b, bf, "w_b"), _dev(z, bf, "z"), _dev(b, bf, "b"),
+                               ws, workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def _layers(layers):

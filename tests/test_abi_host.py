@@ -96,3 +96,27 @@ def test_binding_marshalling_checks(K):
     cfg = K.kda_config(2, 128, K.KDA_F32)
     with pytest.raises(TypeError):
         K.kda_layer_params_from(torch.zeros(3, 256, 4), torch.zeros(256), torch.zeros(2), torch.zeros(128))
+
+
+def test_gate_proj_arguments_rejected_before_the_device(K):
+    """kda_gate_proj checks dtype, geometry, workspace and alignment on the host; the
+    workspace query returns 0 for the same invalid arguments. T = 0 is a no-op."""
+    L = K.lib()
+    bf = K.kda_config(96, 128, K.KDA_BF16)
+    f32 = K.kda_config(96, 128, K.KDA_F32)
+    wide = K.kda_config(200, 128, K.KDA_BF16)
+    fake = ctypes.c_void_p(1 << 20)  # an aligned address that is never dereferenced
+    args = [fake] * 6
+    for cfg, hidden, T, why in ((f32, 7168, 16, "BF16"), (bf, 100, 16, "multiple of 64"), (bf, 0, 16, "multiple"),
+                                (wide, 7168, 16, "num_heads"), (bf, 7168, -1, "T must be")):
+        assert L.kda_gate_proj_workspace_bytes(ctypes.byref(cfg), hidden, T) == 0
+        assert L.kda_gate_proj(ctypes.byref(cfg), hidden, T, *args, fake, 1 << 30, None) == K.KDA_ERR_INVALID
+        assert why in K.kda_last_error()
+    assert L.kda_gate_proj(ctypes.byref(bf), 7168, 16, *args, None, 1 << 30, None) == K.KDA_ERR_INVALID
+    assert L.kda_gate_proj(ctypes.byref(bf), 7168, 16, *args, ctypes.c_void_p((1 << 20) + 8), 1 << 30,
+                           None) == K.KDA_ERR_INVALID
+    assert L.kda_gate_proj(ctypes.byref(bf), 7168, 16, None, *args[1:], fake, 1 << 30, None) == K.KDA_ERR_INVALID
+    assert L.kda_gate_proj(ctypes.byref(bf), 7168, 16, ctypes.c_void_p((1 << 20) + 2), *args[1:], fake, 1 << 30,
+                           None) == K.KDA_ERR_INVALID
+    assert "16-byte aligned" in K.kda_last_error()
+    assert L.kda_gate_proj(ctypes.byref(bf), 7168, 0, *args, fake, 0, None) == K.KDA_OK

@@ -1,0 +1,85 @@
+"""GPU parity of kda_gate_proj (the decay-gate and beta input projections,
+z = W_fb (W_fa x) and b = W_b x) against the FP64 oracle in oracle/gate_proj.py, on
+the same seeded BF16 inputs. The bound is the BF16-I/O one, max|diff| / max|ref| <=
+2e-2 per output tensor; the kernel rounds f to BF16 once and z, b on output, which
+puts the error near 2^-9."""
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs as KI
+import linear_attention_mixer_gb300 as K
+from kda_testutil import TOL_BF16, rel_err
+from oracle.gate_proj import gate_proj
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(cfg, inp, dev="cuda", workspace=None, repeat=1):
+    T, hidden = inp["x"].shape
+    H, d = cfg.num_heads, cfg.head_dim
+    t = {n: torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(torch.bfloat16) for n, a in inp.items()}
+    z = torch.full((T, H * d), float("nan"), device=dev, dtype=torch.bfloat16)
+    b = torch.full((T, H), float("nan"), device=dev, dtype=torch.bfloat16)
+    if workspace is None:
+        workspace = torch.empty(K.kda_gate_proj_workspace_bytes(cfg, hidden, T), dtype=torch.uint8, device=dev)
+    outs = []
+    for _ in range(repeat):
+        K.kda_gate_proj(cfg, t["x"], t["w_fa"], t["w_fb"], t["w_b"], z, b, workspace)
+        torch.cuda.synchronize()
+        outs.append((z.float().cpu().numpy(), b.float().cpu().numpy()))
+    err_word = int(workspace[:4].view(torch.int32).item())
+    assert err_word == 0
+    return outs
+
+
+# (H, hidden, T): ragged token tiles, head counts that are not multiples of 16 (padded
+# beta rows) or of 2 (a half-width last z tile), single-step and long hidden dimensions,
+# split-K on and off, and the Kimi K3 geometry (96 heads, hidden 7168)
+CASES = [(4, 192, 300), (1, 64, 5), (3, 128, 129), (2, 256, 1), (96, 512, 4096), (96, 7168, 1000),
+         (17, 320, 777), (128, 1024, 2000)]
+
+
+@pytest.mark.parametrize("H,hidden,T", CASES)
+def test_gate_proj_matches_oracle(H, hidden, T):
+    cfg = K.kda_config(H, 128, K.KDA_BF16)
+    inp = KI.make_gate_proj(T, hidden, H, 128, seed=hidden + T + H)
+    (z, b), = _run(cfg, inp)
+    z_ref, b_ref = gate_proj(inp["x"], inp["w_fa"], inp["w_fb"], inp["w_b"])
+    ez, eb = rel_err(z, z_ref), rel_err(b, b_ref)
+    print(f"gate_proj H={H} hidden={hidden} T={T}: z {ez:.2e}, b {eb:.2e}")
+    assert np.isfinite(z).all() and np.isfinite(b).all()
+    assert ez <= TOL_BF16 and eb <= TOL_BF16
+
+
+def test_gate_proj_full_size_sampled_rows():
+    """T = 8192 tokens at hidden 7168 and 96 heads (the prefill workload's token count),
+    in the launch configuration the benchmark times; 384 sampled rows against the oracle,
+    including the first and last token tiles."""
+    H, hidden, T = 96, 7168, 8192
+    cfg = K.kda_config(H, 128, K.KDA_BF16)
+    inp = KI.make_gate_proj(T, hidden, H, 128, seed=5)
+    (z, b), = _run(cfg, inp)
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([np.arange(0, 64), np.arange(T - 64, T), rng.integers(0, T, 256)]))
+    z_ref, b_ref = gate_proj(inp["x"][rows], inp["w_fa"], inp["w_fb"], inp["w_b"])
+    ez, eb = rel_err(z[rows], z_ref), rel_err(b[rows], b_ref)
+    print(f"gate_proj full size, {len(rows)} rows: z {ez:.2e}, b {eb:.2e}")
+    assert np.isfinite(z).all() and np.isfinite(b).all()
+    assert ez <= TOL_BF16 and eb <= TOL_BF16
+
+
+def test_gate_proj_repeatable_and_workspace_checked():
+    """Two calls on the same inputs give identical bits (the split-K partials are added in
+    a fixed order); a workspace one byte short is refused before anything runs."""
+    H, hidden, T = 96, 1024, 300
+    cfg = K.kda_config(H, 128, K.KDA_BF16)
+    inp = KI.make_gate_proj(T, hidden, H, 128, seed=9)
+    (z1, b1), (z2, b2) = _run(cfg, inp, repeat=2)
+    assert np.array_equal(z1, z2) and np.array_equal(b1, b2)
+    need = K.kda_gate_proj_workspace_bytes(cfg, hidden, T)
+    assert need > 0
+    with pytest.raises(K.KdaError) as ei:
+        _run(cfg, inp, workspace=torch.empty(need - 1, dtype=torch.uint8, device="cuda"))
+    assert ei.value.status == K.KDA_ERR_INVALID
+
