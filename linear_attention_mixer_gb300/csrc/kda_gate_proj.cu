@@ -17,17 +17,20 @@
 //     writes its FP32 partial sums to the caller's workspace.
 //  2. gp_out_kernel: persistent, one CTA per SM. Each CTA walks a contiguous range
 //     of (token tile, 256-column tile of z) items. On entering a token tile it adds
-//     that tile's partial sums in a fixed order (so results do not depend on
-//     timing), writes b, and rounds f to BF16 as the A operand. W_fb tiles stream
+//     that tile's f partial sums in a fixed order (so results do not depend on
+//     timing) and rounds f to BF16 as the A operand. Each item also adds up and
+//     writes ceil(H / z tiles) heads of b for its token tile, under its MMAs, so
+//     b costs every item the same small amount. W_fb tiles stream
 //     through a two-stage TMA ring into two TMEM accumulators, so one item's
 //     epilogue (TMEM -> BF16 -> TMA store) runs under the next item's MMAs.
 //
-// Operand tiles are K-major without swizzle, exactly as TMA lands them: a box of
-// 8 columns (16 bytes) by R rows arrives as R consecutive 16-byte rows, so core
-// matrices adjacent along K sit R*16 bytes apart (LBO) and 8-row groups 128 bytes
-// apart (SBO). The z output is staged in the 128-byte swizzled layout (16-byte
-// chunk c of row r at chunk c ^ (r % 8)), which keeps the epilogue's shared-memory
-// writes free of bank conflicts, and leaves by TMA box stores.
+// Every tile in shared memory uses the 128-byte swizzled layout: a row holds 64
+// BF16 (128 bytes) and its 16-byte chunk c sits at chunk c ^ (row % 8), in blocks of
+// 8 rows (1024 bytes) on 1024-byte boundaries. TMA lands operand boxes of 64
+// columns in that layout (few, wide requests), the MMA descriptors read it as
+// K-major with 8-row groups 1024 bytes apart (a K step of 16 advances the start
+// by 32 bytes), and the f tile and the z staging written by threads use it too,
+// which keeps their shared-memory stores free of bank conflicts.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -50,15 +53,18 @@ constexpr int kGpN2 = 256;        // z columns per item (MMA N of the second pro
 constexpr int kGpMaxSplit = 16;   // most hidden-dimension slices per token tile
 constexpr int kGpZBox = 64;       // z columns per TMA store box (128 bytes, the swizzle span)
 constexpr uint32_t kGpSpin = 1u << 26;
-constexpr int kGpOutThreads = 192;  // warps 0-3 epilogue, warp 4 producer, warp 5 MMA issuer
+constexpr int kGpEpiWarps = 8;      // second product: epilogue warps (two per TMEM lane quadrant)
+constexpr int kGpEpiThreads = 32 * kGpEpiWarps;
+constexpr int kGpOutThreads = kGpEpiThreads + 96;  // + producer, MMA issuer and b warps
 constexpr int kGpAlign = 1024;      // slack to align the dynamic shared memory base
 
 __host__ __device__ constexpr int gp_n1(int H) { return kD + ((H + 15) / 16) * 16; }
 __host__ __device__ constexpr int gp_in_stage_bytes(int n1) { return (kGpTile + n1) * kGpKs * 2; }
+constexpr int kGpAtom = 128;                        // bytes per swizzled row (64 BF16)
 constexpr int kGpFBytes = kGpTile * kD * 2;         // f tile, BF16
 constexpr int kGpWBytes = kGpN2 * kD * 2;           // one W_fb tile, BF16
-constexpr int kGpStgWarp = 32 * kGpN2 * 2;          // one warp's z staging (32 rows x 256 columns)
-constexpr int kGpOutSmem = kGpFBytes + 2 * kGpWBytes + 4 * kGpStgWarp + 128 + kGpAlign;
+constexpr int kGpStgWarp = 32 * 128 * 2;            // one epilogue warp's z staging (32 rows x 128 columns)
+constexpr int kGpOutSmem = kGpFBytes + 2 * kGpWBytes + kGpEpiWarps * kGpStgWarp + 128 + kGpAlign;
 
 __device__ __forceinline__ unsigned char *align_smem(unsigned char *p)
 {
@@ -79,6 +85,20 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool 
         : "r"((uint32_t)pred), "r"(id), "r"(count)
         : "memory");
     return r != 0;
+}
+
+// K-major, 128-byte-swizzle shared-memory descriptor for a tile whose rows are 128
+// bytes and whose 8-row groups are 1024 bytes apart (start must lie in a 1024-byte
+// aligned tile; a K step moves it by 32 bytes).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;             // leading byte offset (unused by swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset: 8-row groups
+    d |= (uint64_t)1 << 46;             // descriptor version for this architecture
+    d |= (uint64_t)2 << 61;             // layout: 128-byte swizzle
+    return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
@@ -124,7 +144,7 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
     bool ok = true;
 
     if (threadIdx.x == 0) {
-        const uint32_t bytes = (uint32_t)(x_rows + kD + bp_rows) * 16u * (kGpKs / 8);
+        const uint32_t bytes = (uint32_t)(x_rows + kD + bp_rows) * kGpAtom;
         int issued = 0;
         for (int i = 0; i < nk; ++i) {
             const int s = i % kGpStages;
@@ -133,15 +153,12 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
                 break;
             }
             unsigned char *xs = smem + s * sb;
-            unsigned char *ws = xs + kGpTile * kGpKs * 2;
+            unsigned char *ws = xs + kGpTile * kGpAtom;  // W_fa rows, then W_b rows at row 128
             mbar_arrive_expect_tx(&full[s], bytes);
             const int kx = (k0 + i) * kGpKs;
-#pragma unroll
-            for (int g = 0; g < kGpKs / 8; ++g) {
-                tma_load_2d(xs + g * kGpTile * 16, &tm_x, kx + 8 * g, tile * kGpTile, &full[s]);
-                tma_load_2d(ws + g * n1 * 16, &tm_fa, kx + 8 * g, 0, &full[s]);
-                tma_load_2d(ws + g * n1 * 16 + kD * 16, &tm_bp, kx + 8 * g, 0, &full[s]);
-            }
+            tma_load_2d(xs, &tm_x, kx, tile * kGpTile, &full[s]);
+            tma_load_2d(ws, &tm_fa, kx, 0, &full[s]);
+            tma_load_2d(ws + kD * kGpAtom, &tm_bp, kx, 0, &full[s]);
             issued = i + 1;
         }
         // the last copy into each stage has landed before the CTA can exit
@@ -156,13 +173,10 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
                 break;
             }
             tc::fence_after_sync();
-            const uint32_t xs = smem_u32(smem + s * sb), ws = xs + kGpTile * kGpKs * 2;
+            const uint32_t xs = smem_u32(smem + s * sb), ws = xs + kGpTile * kGpAtom;
 #pragma unroll
-            for (int kk = 0; kk < kGpKs / 16; ++kk) {
-                const uint64_t a = tc::smem_desc(xs + kk * 2 * kGpTile * 16, kGpTile * 16, 128);
-                const uint64_t b = tc::smem_desc(ws + kk * 2 * n1 * 16, n1 * 16, 128);
-                tc::mma_bf16(tmem, a, b, idesc, (uint32_t)(i | kk));
-            }
+            for (int kk = 0; kk < kGpKs / 16; ++kk)
+                tc::mma_bf16(tmem, sw128_desc(xs + kk * 32), sw128_desc(ws + kk * 32), idesc, (uint32_t)(i | kk));
             tc::mma_commit(&empty[s]);
         }
         tc::mma_commit(done);
@@ -192,17 +206,20 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
 }
 
 // ---------------------------------------------------------------- second product
+// Warps 0-7 form the f tile and run the epilogue: warp w reads TMEM lanes
+// 32*(w%4) .. +31 (tokens) and z columns 128*(w/4) .. +127 of each item. Warp 8
+// lane 0 streams W_fb tiles, warp 9 lane 0 issues the MMAs, warp 10 writes b.
 __global__ void __launch_bounds__(kGpOutThreads, 1)
 gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__ CUtensorMap tm_z,
               const float *__restrict__ part, __nv_bfloat16 *__restrict__ bout, int T, int H, int HD, int n1,
-              int splits, int ntiles, int items, int fb_rows, int32_t *err)
+              int splits, int ntiles, int items, int fb_rows, int hb, int32_t *err)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = align_smem(smem_raw);
-    unsigned char *f_t = smem;                       // [16 k groups][128 rows][8 BF16]
-    unsigned char *wbuf = f_t + kGpFBytes;           // 2 x [16 k groups][256 rows][8 BF16]
-    unsigned char *stg = wbuf + 2 * kGpWBytes;       // 4 warps x 4 boxes x [32 rows][64 BF16], swizzled
-    uint64_t *bars = reinterpret_cast<uint64_t *>(stg + 4 * kGpStgWarp);
+    unsigned char *f_t = smem;                       // [2 k halves][128 rows][64 BF16]
+    unsigned char *wbuf = f_t + kGpFBytes;           // 2 x [2 k halves][256 rows][64 BF16]
+    unsigned char *stg = wbuf + 2 * kGpWBytes;       // 8 warps x 2 boxes x [32 rows][64 BF16]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stg + kGpEpiWarps * kGpStgWarp);
     uint64_t *wfull = bars, *wempty = bars + 2, *accfull = bars + 4, *ready = bars + 6, *fin = bars + 8;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 9);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -214,17 +231,17 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
         for (int s = 0; s < 9; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
-    if (warp == 4) tc::tmem_alloc(tslot, 2 * kGpN2);
+    if (warp == kGpEpiWarps) tc::tmem_alloc(tslot, 2 * kGpN2);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
 
-    if (warp == 4) {
+    if (warp == kGpEpiWarps) {
         if (lane == 0) {
             bool ok = true;
             int issued = 0;
-            const uint32_t bytes = (uint32_t)fb_rows * 16u * (kD / 8);
+            const uint32_t bytes = (uint32_t)fb_rows * kGpAtom * 2;
             for (int j = 0; j < n; ++j) {
                 const int s = j & 1;
                 if (j >= 2 && !mbar_wait_bounded(&wempty[s], ((j >> 1) - 1) & 1, kGpSpin)) {
@@ -234,8 +251,8 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
                 const int nt = (i0 + j) % ntiles;
                 unsigned char *w = wbuf + s * kGpWBytes;
                 mbar_arrive_expect_tx(&wfull[s], bytes);
-#pragma unroll
-                for (int g = 0; g < kD / 8; ++g) tma_load_2d(w + g * kGpN2 * 16, &tm_fb, 8 * g, nt * kGpN2, &wfull[s]);
+                tma_load_2d(w, &tm_fb, 0, nt * kGpN2, &wfull[s]);
+                tma_load_2d(w + kGpN2 * kGpAtom, &tm_fb, kGpKs, nt * kGpN2, &wfull[s]);
                 issued = j + 1;
             }
             for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
@@ -243,7 +260,7 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
             if (!ok) atomicExch(err, KDA_ERR_TIMEOUT);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == kGpEpiWarps + 1) {
         if (lane == 0) {
             bool ok = true;
             const uint32_t idesc = tc::idesc_bf16(kGpTile, kGpN2);
@@ -259,9 +276,10 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
                 const uint32_t b0 = smem_u32(wbuf + s * kGpWBytes);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint64_t a = tc::smem_desc(a0 + kk * 2 * kGpTile * 16, kGpTile * 16, 128);
-                    const uint64_t b = tc::smem_desc(b0 + kk * 2 * kGpN2 * 16, kGpN2 * 16, 128);
-                    tc::mma_bf16(tmem + (uint32_t)(s * kGpN2), a, b, idesc, (uint32_t)kk);
+                    const uint32_t koff = (uint32_t)(kk & 3) * 32;
+                    tc::mma_bf16(tmem + (uint32_t)(s * kGpN2),
+                                 sw128_desc(a0 + (uint32_t)(kk >> 2) * (kGpTile * kGpAtom) + koff),
+                                 sw128_desc(b0 + (uint32_t)(kk >> 2) * (kGpN2 * kGpAtom) + koff), idesc, (uint32_t)kk);
                 }
                 tc::mma_commit(&wempty[s]);
                 tc::mma_commit(&accfull[s]);
@@ -272,44 +290,73 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
             if (!ok) atomicExch(err, KDA_ERR_TIMEOUT);
         }
         __syncwarp();
+    } else if (warp == kGpEpiWarps + 2) {
+        // b for each item: heads nt*hb .. +hb-1 (hb <= 2) of its 128 tokens, partials added in a
+        // fixed order; element e = lane + 32 i is token e / nh, head h0 + e % nh
+        for (int j = 0; j < n; ++j) {
+            const int gi = i0 + j, m = gi / ntiles, nt = gi % ntiles;
+            const int h0 = nt * hb, nh = H - h0 < hb ? H - h0 : hb;
+            if (nh <= 0) continue;
+            const int cnt = kGpTile * nh;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int sp = 0; sp < splits; ++sp) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = lane + 32 * i, t = m * kGpTile + e / nh;
+                    v[i] = (e < cnt && t < T) ? part[((size_t)sp * T + t) * n1 + kD + h0 + e % nh] : 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] += v[i];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i, t = m * kGpTile + e / nh;
+                if (e < cnt && t < T) bout[(size_t)t * H + h0 + e % nh] = __float2bfloat16_rn(acc[i]);
+            }
+        }
     } else {
-        const int r = threadIdx.x;  // token row within the tile
-        // Sum the partials of token tile m (fixed order), round f to the BF16 A operand and,
-        // for the CTA that owns the tile's first z columns, write b.
-        auto form = [&](int m, bool with_b) {
-            const int t = m * kGpTile + r;
-            const float *row = part + (size_t)t * n1;
-            const size_t sstride = (size_t)T * n1;
-#pragma unroll 4
-            for (int g = 0; g < kD / 8; ++g) {
-                float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                if (t < T) {
-                    for (int s = 0; s < splits; ++s) {
-                        const float4 *p = reinterpret_cast<const float4 *>(row + s * sstride + g * 8);
-                        const float4 u = p[0], w = p[1];
-                        a[0] += u.x; a[1] += u.y; a[2] += u.z; a[3] += u.w;
-                        a[4] += w.x; a[5] += w.y; a[6] += w.z; a[7] += w.w;
+        const int hh = warp >> 2;              // which 128 of the item's 256 z columns
+        // Sum the f partials of token tile m (fixed order) and round them to the BF16 A
+        // operand. Warp w takes rows w, w+8, ..., and lane l columns 4l .. 4l+3 of each, so
+        // every load instruction reads whole rows (coalesced).
+        auto form = [&](int m) {
+            const float4 *base = reinterpret_cast<const float4 *>(part) + lane;
+            const size_t sstride = (size_t)T * n1 / 4, rstride = (size_t)n1 / 4;
+#pragma unroll 2
+            for (int half = 0; half < 2; ++half) {
+                float4 acc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int sp = 0; sp < splits; ++sp) {
+                    float4 u[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int t = m * kGpTile + (half * 8 + i) * 8 + warp;
+                        u[i] = t < T ? base[sp * sstride + (size_t)t * rstride] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        acc[i].x += u[i].x; acc[i].y += u[i].y; acc[i].z += u[i].z; acc[i].w += u[i].w;
                     }
                 }
-                *reinterpret_cast<uint4 *>(f_t + g * kGpTile * 16 + r * 16) =
-                    make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]),
-                               pack_bf16(a[6], a[7]));
-            }
-            if (with_b && t < T) {
-                for (int h = 0; h < H; ++h) {
-                    float acc = 0.f;
-                    for (int s = 0; s < splits; ++s) acc += row[s * sstride + kD + h];
-                    bout[(size_t)t * H + h] = __float2bfloat16_rn(acc);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rw = (half * 8 + i) * 8 + warp;
+                    // columns 4l .. 4l+3: k half l/16, 16-byte chunk (l%16)/2, 8-byte half l%2
+                    *reinterpret_cast<uint2 *>(f_t + (lane >> 4) * (kGpTile * kGpAtom) + rw * kGpAtom +
+                                               ((((lane & 15) >> 1) ^ (rw & 7)) * 16) + (lane & 1) * 8) =
+                        make_uint2(pack_bf16(acc[i].x, acc[i].y), pack_bf16(acc[i].z, acc[i].w));
                 }
             }
             tc::fence_smem_to_async();
-            named_bar_sync(1, 128);
+            named_bar_sync(1, kGpEpiThreads);
         };
 
         bool ok = true;
         if (n > 0) {
-            form(i0 / ntiles, i0 % ntiles == 0);
-            if (r == 0) mbar_arrive(&ready[0]);
+            form(i0 / ntiles);
+            if (threadIdx.x == 0) mbar_arrive(&ready[0]);
         }
         unsigned char *my = stg + warp * kGpStgWarp;
         for (int j = 0; j < n; ++j) {
@@ -317,24 +364,25 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
             const bool next_same = j + 1 < n && (gi + 1) / ntiles == m;
             // the next item reuses this f tile: let its MMAs start now (its accumulator was
             // released by the barrier at the end of the previous item)
-            if (next_same && r == 0) mbar_arrive(&ready[(j + 1) & 1]);
-            ok = named_bar_and(2, 128, mbar_wait_bounded(&accfull[s], (j >> 1) & 1, kGpSpin));
+            if (next_same && threadIdx.x == 0) mbar_arrive(&ready[(j + 1) & 1]);
+            ok = named_bar_and(2, kGpEpiThreads, mbar_wait_bounded(&accfull[s], (j >> 1) & 1, kGpSpin));
             if (!ok) break;
             tc::fence_after_sync();
             // this warp's previous stores have finished reading its staging buffer
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
-            const uint32_t tbase = tmem + (uint32_t)(s * kGpN2) + ((uint32_t)(warp * 32) << 16);
+            const uint32_t tbase = tmem + (uint32_t)(s * kGpN2 + hh * 128) + ((uint32_t)((warp & 3) * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < kGpN2 / 32; ++c) {
-                uint32_t v[32];
-                tc::tmem_ld32_nowait(tbase + (uint32_t)(c * 32), v);
+            for (int c = 0; c < 128 / kGpZBox; ++c) {
+                // columns hh*128 + c*64 .. +63 = the 8 16-byte chunks of box c (two TMEM loads, one wait)
+                uint32_t v[64];
+                tc::tmem_ld32_nowait(tbase + (uint32_t)(c * 64), v);
+                tc::tmem_ld32_nowait(tbase + (uint32_t)(c * 64 + 32), v + 32);
                 tc::tmem_wait_ld();
-                // columns c*32 .. +31 = 16-byte chunks (c&1)*4 .. +3 of box c/2
-                unsigned char *box = my + (c >> 1) * (32 * kGpZBox * 2) + lane * (kGpZBox * 2);
+                unsigned char *box = my + c * (32 * kGpZBox * 2) + lane * (kGpZBox * 2);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = ((c & 1) * 4 + q) ^ (lane & 7);
+                for (int q = 0; q < 8; ++q) {
+                    const int chunk = q ^ (lane & 7);
                     *reinterpret_cast<uint4 *>(box + chunk * 16) = make_uint4(
                         pack_bf16(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
                         pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
@@ -345,11 +393,11 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
             tc::fence_smem_to_async();
             __syncwarp();
             if (lane == 0) {
-                const int y = m * kGpTile + warp * 32;
+                const int y = m * kGpTile + (warp & 3) * 32;
                 if (y < T) {
 #pragma unroll
-                    for (int bx = 0; bx < kGpN2 / kGpZBox; ++bx) {
-                        const int x = nt * kGpN2 + bx * kGpZBox;
+                    for (int bx = 0; bx < 128 / kGpZBox; ++bx) {
+                        const int x = nt * kGpN2 + hh * 128 + bx * kGpZBox;
                         if (x < HD) tma_store_2d(&tm_z, x, y, my + bx * (32 * kGpZBox * 2));
                     }
                 }
@@ -357,19 +405,19 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
             }
             // every warp has read its lanes of accumulator s
             tc::fence_before_sync();
-            named_bar_sync(1, 128);
+            named_bar_sync(1, kGpEpiThreads);
             if (j + 1 < n && !next_same) {
                 // MMAs of item j are complete (accfull waited), so the f tile is free
-                form((gi + 1) / ntiles, (gi + 1) % ntiles == 0);
-                if (r == 0) mbar_arrive(&ready[(j + 1) & 1]);
+                form((gi + 1) / ntiles);
+                if (threadIdx.x == 0) mbar_arrive(&ready[(j + 1) & 1]);
             }
         }
         if (lane == 0) bulk_wait_all();
-        if (!ok && r == 0) atomicExch(err, KDA_ERR_TIMEOUT);
+        if (!ok && threadIdx.x == 0) atomicExch(err, KDA_ERR_TIMEOUT);
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == kGpEpiWarps) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, 2 * kGpN2);
     }
@@ -502,13 +550,11 @@ extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int
     const int z_rows = (int)(T < 32 ? T : 32);
     CUtensorMap tm_x, tm_fa, tm_bp, tm_fb, tm_z;
     cudaError_t e;
-    if ((e = encode_2d(&tm_x, x, hidden, T, (uint64_t)hidden * 2, 8, x_rows, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
-            cudaSuccess ||
-        (e = encode_2d(&tm_fa, w_fa, hidden, kD, (uint64_t)hidden * 2, 8, kD, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
-            cudaSuccess ||
-        (e = encode_2d(&tm_bp, w_b, hidden, H, (uint64_t)hidden * 2, 8, H, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
-            cudaSuccess ||
-        (e = encode_2d(&tm_fb, w_fb, kD, HD, kD * 2, 8, fb_rows, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess ||
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if ((e = encode_2d(&tm_x, x, hidden, T, (uint64_t)hidden * 2, kGpKs, x_rows, sw)) != cudaSuccess ||
+        (e = encode_2d(&tm_fa, w_fa, hidden, kD, (uint64_t)hidden * 2, kGpKs, kD, sw)) != cudaSuccess ||
+        (e = encode_2d(&tm_bp, w_b, hidden, H, (uint64_t)hidden * 2, kGpKs, H, sw)) != cudaSuccess ||
+        (e = encode_2d(&tm_fb, w_fb, kD, HD, kD * 2, kGpKs, fb_rows, sw)) != cudaSuccess ||
         (e = encode_2d(&tm_z, z, HD, T, (uint64_t)HD * 2, kGpZBox, z_rows, CU_TENSOR_MAP_SWIZZLE_128B)) !=
             cudaSuccess)
         return gp_fail(KDA_ERR_CUDA, "kda_gate_proj: tensor map encoding failed: %s", cudaGetErrorString(e));
@@ -527,8 +573,11 @@ extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int
                                                             splits, n1, x_rows, H, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return gp_fail(KDA_ERR_CUDA, "gp_in_kernel launch: %s", cudaGetErrorString(e));
     const int grid = items < sms ? items : sms;
+    const int hb = (H + ntiles - 1) / ntiles;  // <= 2: ntiles = ceil(H / 2)
+    if (hb > 2) return gp_fail(KDA_ERR_INVALID, "kda_gate_proj: internal tiling error (hb = %d)", hb);
     gp_out_kernel<<<grid, kGpOutThreads, kGpOutSmem, s>>>(tm_fb, tm_z, part, static_cast<__nv_bfloat16 *>(b),
-                                                          (int)T, H, HD, n1, splits, ntiles, items, fb_rows, err);
+                                                          (int)T, H, HD, n1, splits, ntiles, items, fb_rows,
+                                                          hb, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return gp_fail(KDA_ERR_CUDA, "gp_out_kernel launch: %s", cudaGetErrorString(e));
     return KDA_OK;
 }
