@@ -209,6 +209,25 @@ def cpu_baseline_prefill():
             "sample_1thread": f"FP64 oracle on one core, {T1} tokens x 1 head (scaled to {H} heads)"}
 
 
+def cpu_baseline_gate_proj(T: int = 2048):
+    """Bounded sample: the FP64 projection oracle (numpy matmuls) on T tokens at hidden 7168, 96 heads."""
+    import os
+    import kda_inputs as KI
+    from oracle.gate_proj import gate_proj
+    inp = KI.make_gate_proj(T, HIDDEN, H, DH, seed=6)
+    gate_proj(inp["x"][:64], inp["w_fa"], inp["w_fb"], inp["w_b"])  # warm-up
+    t0 = time.perf_counter()
+    gate_proj(inp["x"], inp["w_fa"], inp["w_fb"], inp["w_b"])
+    t = time.perf_counter() - t0
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max(i.get("num_threads", 1) for i in threadpool_info()) or os.cpu_count()
+    except Exception:  # threadpoolctl absent: numpy's BLAS uses every core by default
+        cores = os.cpu_count()
+    return {"value": T / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"FP64 projection oracle (numpy BLAS matmuls), {T} tokens x hidden {HIDDEN}, {H} heads"}
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -679,6 +698,8 @@ def run_kda(args):
         line["cpu_baseline"] = cpu_baseline_decode()
         if "prefill" in line:
             line["prefill"]["cpu_baseline"] = cpu_baseline_prefill()
+        if "gate_proj" in line:
+            line["gate_proj"]["cpu_baseline"] = cpu_baseline_gate_proj()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -11,16 +11,16 @@
 // dt_bias and the sigmoids stay in the mixer kernels, which take z and b as inputs.
 //
 // Two launches on the caller's stream:
-//  1. gp_in_kernel: [f | b] = x [W_fa; W_b]^T for a tile of 128 tokens over one
-//     slice of the hidden dimension. When there are too few token tiles to fill
-//     the GPU the hidden dimension is split over several CTAs (split-K); each
-//     writes its FP32 partial sums to the caller's workspace.
+//  1. gp_in_kernel: [f | b] = x [W_fa; W_b]^T for two tiles of 128 tokens over one
+//     slice of the hidden dimension (the weight boxes serve both tiles). When there
+//     are too few tile pairs to fill the GPU the hidden dimension is split over
+//     several CTAs (split-K); each writes its FP32 partial sums to the caller's
+//     workspace.
 //  2. gp_out_kernel: persistent, one CTA per SM. Each CTA walks a contiguous range
 //     of (token tile, 256-column tile of z) items. On entering a token tile it adds
-//     that tile's f partial sums in a fixed order (so results do not depend on
-//     timing) and rounds f to BF16 as the A operand. Each item also adds up and
-//     writes ceil(H / z tiles) heads of b for its token tile, under its MMAs, so
-//     b costs every item the same small amount. W_fb tiles stream
+//     that tile's partial sums in a fixed order (so results do not depend on
+//     timing), rounds f to BF16 as the A operand, and, if it owns the tile's first
+//     z columns, writes the tile's b. W_fb tiles stream
 //     through a two-stage TMA ring into two TMEM accumulators, so one item's
 //     epilogue (TMEM -> BF16 -> TMA store) runs under the next item's MMAs.
 //
@@ -48,18 +48,18 @@ namespace {
 
 constexpr int kGpTile = 128;      // tokens per tile (MMA M)
 constexpr int kGpKs = 64;         // hidden columns per pipeline stage
-constexpr int kGpStages = 4;      // stages of the first product's ring
+constexpr int kGpStages = 3;      // stages of the first product's ring
 constexpr int kGpN2 = 256;        // z columns per item (MMA N of the second product)
 constexpr int kGpMaxSplit = 16;   // most hidden-dimension slices per token tile
 constexpr int kGpZBox = 64;       // z columns per TMA store box (128 bytes, the swizzle span)
 constexpr uint32_t kGpSpin = 1u << 26;
 constexpr int kGpEpiWarps = 8;      // second product: epilogue warps (two per TMEM lane quadrant)
 constexpr int kGpEpiThreads = 32 * kGpEpiWarps;
-constexpr int kGpOutThreads = kGpEpiThreads + 96;  // + producer, MMA issuer and b warps
+constexpr int kGpOutThreads = kGpEpiThreads + 64;  // + producer and MMA issuer warps
 constexpr int kGpAlign = 1024;      // slack to align the dynamic shared memory base
 
 __host__ __device__ constexpr int gp_n1(int H) { return kD + ((H + 15) / 16) * 16; }
-__host__ __device__ constexpr int gp_in_stage_bytes(int n1) { return (kGpTile + n1) * kGpKs * 2; }
+__host__ __device__ constexpr int gp_in_stage_bytes(int n1) { return (2 * kGpTile + n1) * kGpKs * 2; }
 constexpr int kGpAtom = 128;                        // bytes per swizzled row (64 BF16)
 constexpr int kGpFBytes = kGpTile * kD * 2;         // f tile, BF16
 constexpr int kGpWBytes = kGpN2 * kD * 2;           // one W_fb tile, BF16
@@ -108,9 +108,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 }
 
 // ---------------------------------------------------------------- first product
-// CTA (tile, split): [f | b] partial sums of tokens tile*128 .. +127 over hidden
-// columns [k0*64, k1*64). Thread 0 issues the TMA copies, thread 32 the MMAs; all
-// four warps then move the accumulator (TMEM lane = token) to the workspace.
+// CTA (pair, split): [f | b] partial sums of the two token tiles pair*256 .. +127 and
+// pair*256+128 .. +255 over the 64-column steps split, split + splits, ... of the hidden
+// dimension. Each stage brings both tiles'
+// x boxes and one (W_fa | W_b) box, which the MMAs of both accumulators share. Thread 0
+// issues the TMA copies, thread 32 the MMAs. At the end all four warps move each
+// accumulator (TMEM lane = token) through a padded shared-memory tile to coalesced stores.
 __global__ void __launch_bounds__(128, 1)
 gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_fa,
              const __grid_constant__ CUtensorMap tm_bp, float *__restrict__ part, int T, int ksteps, int splits,
@@ -124,9 +127,11 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
     uint64_t *done = empty + kGpStages;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x, split = blockIdx.y;
-    const int k0 = (int)((int64_t)split * ksteps / splits), k1 = (int)((int64_t)(split + 1) * ksteps / splits);
-    const int nk = k1 - k0;
+    const int tok0 = blockIdx.x * 2 * kGpTile, split = blockIdx.y;
+    const int ntile = tok0 + kGpTile < T ? 2 : 1;  // token tiles this CTA holds
+    // slice `split` takes the 64-column steps split, split + splits, ...: the CTAs of one
+    // token-tile pair read neighbouring 128-byte pieces of the same rows at about the same time
+    const int nk = (ksteps - split + splits - 1) / splits;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGpStages; ++s) {
@@ -136,7 +141,7 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
         mbar_init(done, 1);
         fence_mbar_init();
     }
-    if (warp == 0) tc::tmem_alloc(tslot, 256);
+    if (warp == 0) tc::tmem_alloc(tslot, 512);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -144,7 +149,7 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
     bool ok = true;
 
     if (threadIdx.x == 0) {
-        const uint32_t bytes = (uint32_t)(x_rows + kD + bp_rows) * kGpAtom;
+        const uint32_t bytes = (uint32_t)(ntile * x_rows + kD + bp_rows) * kGpAtom;
         int issued = 0;
         for (int i = 0; i < nk; ++i) {
             const int s = i % kGpStages;
@@ -152,11 +157,12 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
                 ok = false;
                 break;
             }
-            unsigned char *xs = smem + s * sb;
-            unsigned char *ws = xs + kGpTile * kGpAtom;  // W_fa rows, then W_b rows at row 128
+            unsigned char *xs = smem + s * sb;                  // x of tile 0, then of tile 1
+            unsigned char *ws = xs + 2 * kGpTile * kGpAtom;     // W_fa rows, then W_b rows at row 128
             mbar_arrive_expect_tx(&full[s], bytes);
-            const int kx = (k0 + i) * kGpKs;
-            tma_load_2d(xs, &tm_x, kx, tile * kGpTile, &full[s]);
+            const int kx = (split + i * splits) * kGpKs;
+            tma_load_2d(xs, &tm_x, kx, tok0, &full[s]);
+            if (ntile == 2) tma_load_2d(xs + kGpTile * kGpAtom, &tm_x, kx, tok0 + kGpTile, &full[s]);
             tma_load_2d(ws, &tm_fa, kx, 0, &full[s]);
             tma_load_2d(ws + kD * kGpAtom, &tm_bp, kx, 0, &full[s]);
             issued = i + 1;
@@ -173,10 +179,15 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
                 break;
             }
             tc::fence_after_sync();
-            const uint32_t xs = smem_u32(smem + s * sb), ws = xs + kGpTile * kGpAtom;
+            const uint32_t xs = smem_u32(smem + s * sb), ws = xs + 2 * kGpTile * kGpAtom;
 #pragma unroll
-            for (int kk = 0; kk < kGpKs / 16; ++kk)
-                tc::mma_bf16(tmem, sw128_desc(xs + kk * 32), sw128_desc(ws + kk * 32), idesc, (uint32_t)(i | kk));
+            for (int kk = 0; kk < kGpKs / 16; ++kk) {
+                const uint64_t bd = sw128_desc(ws + kk * 32);
+                tc::mma_bf16(tmem, sw128_desc(xs + kk * 32), bd, idesc, (uint32_t)(i | kk));
+                if (ntile == 2)
+                    tc::mma_bf16(tmem + 256, sw128_desc(xs + kGpTile * kGpAtom + kk * 32), bd, idesc,
+                                 (uint32_t)(i | kk));
+            }
             tc::mma_commit(&empty[s]);
         }
         tc::mma_commit(done);
@@ -185,34 +196,60 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
 
     if (!mbar_wait_bounded(done, 0, kGpSpin)) ok = false;
     tc::fence_after_sync();
-    const int t = tile * kGpTile + warp * 32 + lane;
-    float *dst = part + ((size_t)split * T + (size_t)t) * n1;
-    for (int c = 0; c < n1; c += 16) {
-        float v[16];
-        tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
-        if (t < T) {
+    // the stages are free now: each accumulator goes to a [128][n1 + 4] FP32 tile (the pad
+    // keeps the row-per-thread writes free of bank conflicts), then leaves as whole rows
+    float *tile = reinterpret_cast<float *>(smem);
+    const int pitch = n1 + 4, row = warp * 32 + lane;
+    for (int a = 0; a < ntile; ++a) {
+        const uint32_t ta = tmem + (uint32_t)(a * 256) + ((uint32_t)(warp * 32) << 16);
+        float *dst = tile + row * pitch;
+        int c = 0;
+        // 64 columns per TMEM wait (its latency, not the load, is what costs)
+        for (; c + 64 <= n1; c += 64) {
+            uint32_t v[64];
+            tc::tmem_ld32_nowait(ta + (uint32_t)c, v);
+            tc::tmem_ld32_nowait(ta + (uint32_t)c + 32, v + 32);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                *reinterpret_cast<float4 *>(dst + c + 4 * q) =
+                    make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+        for (; c < n1; c += 16) {
+            float v[16];
+            tc::tmem_ld16(ta + (uint32_t)c, v);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                reinterpret_cast<float4 *>(dst + c)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                *reinterpret_cast<float4 *>(dst + c + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
+        __syncthreads();
+        for (int r = warp; r < kGpTile; r += 4) {
+            const int t = tok0 + a * kGpTile + r;
+            if (t >= T) break;
+            float4 *dst = reinterpret_cast<float4 *>(part + ((size_t)split * T + (size_t)t) * n1);
+            const float4 *src = reinterpret_cast<const float4 *>(tile + r * pitch);
+            for (int c4 = lane; c4 < n1 / 4; c4 += 32) dst[c4] = src[c4];
+        }
+        __syncthreads();
     }
     if (!ok) atomicExch(err, KDA_ERR_TIMEOUT);
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, 256);
+        tc::tmem_dealloc(tmem, 512);
     }
 }
 
 // ---------------------------------------------------------------- second product
-// Warps 0-7 form the f tile and run the epilogue: warp w reads TMEM lanes
-// 32*(w%4) .. +31 (tokens) and z columns 128*(w/4) .. +127 of each item. Warp 8
-// lane 0 streams W_fb tiles, warp 9 lane 0 issues the MMAs, warp 10 writes b.
+// Warps 0-7 form the f tile (and write b) and run the epilogue: warp w reads TMEM
+// lanes 32*(w%4) .. +31 (tokens) and z columns 128*(w/4) .. +127 of each item.
+// Warp 8 lane 0 streams W_fb tiles, warp 9 lane 0 issues the MMAs.
 __global__ void __launch_bounds__(kGpOutThreads, 1)
 gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__ CUtensorMap tm_z,
               const float *__restrict__ part, __nv_bfloat16 *__restrict__ bout, int T, int H, int HD, int n1,
-              int splits, int ntiles, int items, int fb_rows, int hb, int32_t *err)
+              int splits, int ntiles, int items, int fb_rows, int32_t *err)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = align_smem(smem_raw);
@@ -290,63 +327,48 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
             if (!ok) atomicExch(err, KDA_ERR_TIMEOUT);
         }
         __syncwarp();
-    } else if (warp == kGpEpiWarps + 2) {
-        // b for each item: heads nt*hb .. +hb-1 (hb <= 2) of its 128 tokens, partials added in a
-        // fixed order; element e = lane + 32 i is token e / nh, head h0 + e % nh
-        for (int j = 0; j < n; ++j) {
-            const int gi = i0 + j, m = gi / ntiles, nt = gi % ntiles;
-            const int h0 = nt * hb, nh = H - h0 < hb ? H - h0 : hb;
-            if (nh <= 0) continue;
-            const int cnt = kGpTile * nh;
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int sp = 0; sp < splits; ++sp) {
-                float v[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int e = lane + 32 * i, t = m * kGpTile + e / nh;
-                    v[i] = (e < cnt && t < T) ? part[((size_t)sp * T + t) * n1 + kD + h0 + e % nh] : 0.f;
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] += v[i];
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = lane + 32 * i, t = m * kGpTile + e / nh;
-                if (e < cnt && t < T) bout[(size_t)t * H + h0 + e % nh] = __float2bfloat16_rn(acc[i]);
-            }
-        }
     } else {
         const int hh = warp >> 2;              // which 128 of the item's 256 z columns
-        // Sum the f partials of token tile m (fixed order) and round them to the BF16 A
-        // operand. Warp w takes rows w, w+8, ..., and lane l columns 4l .. 4l+3 of each, so
-        // every load instruction reads whole rows (coalesced).
-        auto form = [&](int m) {
+        // Sum the partials of token tile m (fixed order), round f to the BF16 A operand and, when
+        // with_b, write the tile's b. Warp w takes rows w, w+8, ..., and lane l f columns
+        // 4l .. 4l+3 and b heads 4l .. 4l+3 of each, so every load instruction reads whole rows.
+        auto form = [&](int m, bool with_b) {
             const float4 *base = reinterpret_cast<const float4 *>(part) + lane;
             const size_t sstride = (size_t)T * n1 / 4, rstride = (size_t)n1 / 4;
-#pragma unroll 2
+            const bool bl = with_b && 4 * lane < H;  // this lane's b heads exist
+#pragma unroll 1
             for (int half = 0; half < 2; ++half) {
-                float4 acc[8];
+                float4 acc[8], bacc[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int i = 0; i < 8; ++i) acc[i] = bacc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int sp = 0; sp < splits; ++sp) {
-                    float4 u[8];
+                    float4 u[8], w[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int t = m * kGpTile + (half * 8 + i) * 8 + warp;
-                        u[i] = t < T ? base[sp * sstride + (size_t)t * rstride] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float4 *src = base + sp * sstride + (size_t)t * rstride;
+                        u[i] = t < T ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        w[i] = (bl && t < T) ? src[kD / 4] : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         acc[i].x += u[i].x; acc[i].y += u[i].y; acc[i].z += u[i].z; acc[i].w += u[i].w;
+                        bacc[i].x += w[i].x; bacc[i].y += w[i].y; bacc[i].z += w[i].z; bacc[i].w += w[i].w;
                     }
                 }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int rw = (half * 8 + i) * 8 + warp;
+                    const int rw = (half * 8 + i) * 8 + warp, t = m * kGpTile + rw;
                     // columns 4l .. 4l+3: k half l/16, 16-byte chunk (l%16)/2, 8-byte half l%2
                     *reinterpret_cast<uint2 *>(f_t + (lane >> 4) * (kGpTile * kGpAtom) + rw * kGpAtom +
                                                ((((lane & 15) >> 1) ^ (rw & 7)) * 16) + (lane & 1) * 8) =
                         make_uint2(pack_bf16(acc[i].x, acc[i].y), pack_bf16(acc[i].z, acc[i].w));
+                    if (bl && t < T) {
+                        const float bv[4] = {bacc[i].x, bacc[i].y, bacc[i].z, bacc[i].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (4 * lane + j < H) bout[(size_t)t * H + 4 * lane + j] = __float2bfloat16_rn(bv[j]);
+                    }
                 }
             }
             tc::fence_smem_to_async();
@@ -355,7 +377,7 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
 
         bool ok = true;
         if (n > 0) {
-            form(i0 / ntiles);
+            form(i0 / ntiles, i0 % ntiles == 0);
             if (threadIdx.x == 0) mbar_arrive(&ready[0]);
         }
         unsigned char *my = stg + warp * kGpStgWarp;
@@ -408,7 +430,7 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
             named_bar_sync(1, kGpEpiThreads);
             if (j + 1 < n && !next_same) {
                 // MMAs of item j are complete (accfull waited), so the f tile is free
-                form((gi + 1) / ntiles);
+                form((gi + 1) / ntiles, (gi + 1) % ntiles == 0);
                 if (threadIdx.x == 0) mbar_arrive(&ready[(j + 1) & 1]);
             }
         }
@@ -458,11 +480,11 @@ cudaError_t encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// hidden-dimension slices per token tile: enough CTAs to cover the SMs, at most
+// hidden-dimension slices per pair of token tiles: enough CTAs to cover the SMs, at most
 // kGpMaxSplit and never more than the 64-column steps there are
-int gp_splits(int64_t mtiles, int ksteps, int sms)
+int gp_splits(int64_t pairs, int ksteps, int sms)
 {
-    int64_t s = mtiles >= sms ? 1 : sms / mtiles;
+    int64_t s = pairs >= sms ? 1 : sms / pairs;
     if (s > kGpMaxSplit) s = kGpMaxSplit;
     if (s > ksteps) s = ksteps;
     return s < 1 ? 1 : (int)s;
@@ -500,8 +522,8 @@ constexpr size_t kGpErrBytes = 256;  // the error word, padded so the partial su
 
 size_t gp_workspace(const kda_config_t &cfg, int32_t hidden, int64_t T, int sms, int *splits_out)
 {
-    const int64_t mtiles = (T + kGpTile - 1) / kGpTile;
-    const int splits = gp_splits(mtiles, hidden / kGpKs, sms);
+    const int64_t pairs = (T + 2 * kGpTile - 1) / (2 * kGpTile);
+    const int splits = gp_splits(pairs, hidden / kGpKs, sms);
     if (splits_out) *splits_out = splits;
     return kGpErrBytes + (size_t)splits * (size_t)T * (size_t)gp_n1(cfg.num_heads) * sizeof(float);
 }
@@ -569,15 +591,13 @@ extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int
         (e = cudaFuncSetAttribute(gp_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGpOutSmem)) !=
             cudaSuccess)
         return gp_fail(KDA_ERR_CUDA, "kda_gate_proj: %s", cudaGetErrorString(e));
-    gp_in_kernel<<<dim3(mtiles, splits), 128, in_smem, s>>>(tm_x, tm_fa, tm_bp, part, (int)T, hidden / kGpKs,
+    gp_in_kernel<<<dim3((mtiles + 1) / 2, splits), 128, in_smem, s>>>(tm_x, tm_fa, tm_bp, part, (int)T, hidden / kGpKs,
                                                             splits, n1, x_rows, H, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return gp_fail(KDA_ERR_CUDA, "gp_in_kernel launch: %s", cudaGetErrorString(e));
     const int grid = items < sms ? items : sms;
-    const int hb = (H + ntiles - 1) / ntiles;  // <= 2: ntiles = ceil(H / 2)
-    if (hb > 2) return gp_fail(KDA_ERR_INVALID, "kda_gate_proj: internal tiling error (hb = %d)", hb);
     gp_out_kernel<<<grid, kGpOutThreads, kGpOutSmem, s>>>(tm_fb, tm_z, part, static_cast<__nv_bfloat16 *>(b),
                                                           (int)T, H, HD, n1, splits, ntiles, items, fb_rows,
-                                                          hb, err);
+                                                          err);
     if ((e = cudaGetLastError()) != cudaSuccess) return gp_fail(KDA_ERR_CUDA, "gp_out_kernel launch: %s", cudaGetErrorString(e));
     return KDA_OK;
 }
