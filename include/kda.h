@@ -287,10 +287,9 @@ kda_status kda_prefill_noalloc(const kda_config_t *cfg, const kda_layer_params *
  * before the second product, and z, b are rounded to BF16 (nearest even).
  * Needs cfg->io_dtype == KDA_BF16 and num_heads <= 128. Errors:
  * KDA_ERR_INVALID (bad shape, dtype, alignment, NULL pointer, workspace too
- * small), KDA_ERR_CUDA. The hidden dimension is split over several CTAs when
- * T is small, so the workspace need depends on the current device's SM count:
- * query it on the device that runs the call. The query returns 0 for invalid
- * arguments.
+ * small), KDA_ERR_CUDA. The workspace need is 256 bytes plus T * (d + 16
+ * ceil(H / 16)) FP32 values (the sums W_fa x and W_b x); the query returns 0
+ * for invalid arguments and does not touch the device.
  */
 size_t kda_gate_proj_workspace_bytes(const kda_config_t *cfg, int32_t hidden, int64_t T);
 kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int64_t T, const void *x, const void *w_fa,

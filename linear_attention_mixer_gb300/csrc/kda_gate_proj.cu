@@ -50,7 +50,7 @@ constexpr int kGpTile = 128;      // tokens per tile (MMA M)
 constexpr int kGpKs = 64;         // hidden columns per pipeline stage
 constexpr int kGpStages = 3;      // stages of the first product's ring
 constexpr int kGpN2 = 256;        // z columns per item (MMA N of the second product)
-constexpr int kGpMaxSplit = 16;   // most hidden-dimension slices per token tile
+constexpr int kGpMaxSplit = 8;    // most hidden-dimension slices per token-tile pair (one cluster)
 constexpr int kGpZBox = 64;       // z columns per TMA store box (128 bytes, the swizzle span)
 constexpr uint32_t kGpSpin = 1u << 26;
 constexpr int kGpEpiWarps = 8;      // second product: epilogue warps (two per TMEM lane quadrant)
@@ -101,6 +101,35 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     return d;
 }
 
+// Thread-block cluster helpers: this CTA's rank, the cluster-window address of a shared
+// variable in CTA `rank`, a 16-byte load through that window, and a full cluster barrier
+// (release / acquire: shared-memory writes before it are visible to every CTA after it).
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -112,8 +141,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 // pair*256+128 .. +255 over the 64-column steps split, split + splits, ... of the hidden
 // dimension. Each stage brings both tiles'
 // x boxes and one (W_fa | W_b) box, which the MMAs of both accumulators share. Thread 0
-// issues the TMA copies, thread 32 the MMAs. At the end all four warps move each
-// accumulator (TMEM lane = token) through a padded shared-memory tile to coalesced stores.
+// issues the TMA copies, thread 32 the MMAs. The S slices of one pair form a thread-block
+// cluster: at the end each CTA puts an accumulator (TMEM lane = token) into a padded
+// shared-memory tile, and after a cluster barrier CTA q adds rows q*128/S .. (q+1)*128/S - 1
+// of all S slices' tiles, in slice order, through distributed shared memory, and stores the
+// sums as whole rows. Only the sums leave the chip.
 __global__ void __launch_bounds__(128, 1)
 gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_fa,
              const __grid_constant__ CUtensorMap tm_bp, float *__restrict__ part, int T, int ksteps, int splits,
@@ -132,6 +164,9 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
     // slice `split` takes the 64-column steps split, split + splits, ...: the CTAs of one
     // token-tile pair read neighbouring 128-byte pieces of the same rows at about the same time
     const int nk = (ksteps - split + splits - 1) / splits;
+    // the second product may be scheduled now (it waits for this grid to finish before it
+    // reads the sums)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGpStages; ++s) {
@@ -223,15 +258,23 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
             for (int q = 0; q < 4; ++q)
                 *reinterpret_cast<float4 *>(dst + c + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
-        __syncthreads();
-        for (int r = warp; r < kGpTile; r += 4) {
+        cluster_sync_all();  // every slice's tile is in place
+        const int q = (int)cluster_rank(), r0 = q * kGpTile / splits, r1 = (q + 1) * kGpTile / splits;
+        for (int r = r0 + warp; r < r1; r += 4) {
             const int t = tok0 + a * kGpTile + r;
             if (t >= T) break;
-            float4 *dst = reinterpret_cast<float4 *>(part + ((size_t)split * T + (size_t)t) * n1);
-            const float4 *src = reinterpret_cast<const float4 *>(tile + r * pitch);
-            for (int c4 = lane; c4 < n1 / 4; c4 += 32) dst[c4] = src[c4];
+            float4 *dst = reinterpret_cast<float4 *>(part + (size_t)t * n1);
+            const uint32_t src = smem_u32(tile + r * pitch);
+            for (int c4 = lane; c4 < n1 / 4; c4 += 32) {
+                float4 acc = ld_cluster_f4(cluster_map(src + 16u * c4, 0));
+                for (int sp = 1; sp < splits; ++sp) {
+                    const float4 u = ld_cluster_f4(cluster_map(src + 16u * c4, (uint32_t)sp));
+                    acc.x += u.x; acc.y += u.y; acc.z += u.z; acc.w += u.w;
+                }
+                dst[c4] = acc;
+            }
         }
-        __syncthreads();
+        cluster_sync_all();  // every CTA is done reading the tiles
     }
     if (!ok) atomicExch(err, KDA_ERR_TIMEOUT);
     tc::fence_before_sync();
@@ -376,6 +419,8 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
         };
 
         bool ok = true;
+        // the first product (the previous grid in the stream) has finished and its sums are visible
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         if (n > 0) {
             form(i0 / ntiles, i0 % ntiles == 0);
             if (threadIdx.x == 0) mbar_arrive(&ready[0]);
@@ -520,12 +565,10 @@ kda_status gp_sms(int *sms)
 
 constexpr size_t kGpErrBytes = 256;  // the error word, padded so the partial sums stay aligned
 
-size_t gp_workspace(const kda_config_t &cfg, int32_t hidden, int64_t T, int sms, int *splits_out)
+// the error word, then the sums [T][n1] FP32 of [f | b]
+size_t gp_workspace(const kda_config_t &cfg, int64_t T)
 {
-    const int64_t pairs = (T + 2 * kGpTile - 1) / (2 * kGpTile);
-    const int splits = gp_splits(pairs, hidden / kGpKs, sms);
-    if (splits_out) *splits_out = splits;
-    return kGpErrBytes + (size_t)splits * (size_t)T * (size_t)gp_n1(cfg.num_heads) * sizeof(float);
+    return kGpErrBytes + (size_t)T * (size_t)gp_n1(cfg.num_heads) * sizeof(float);
 }
 
 }  // namespace
@@ -534,9 +577,7 @@ size_t gp_workspace(const kda_config_t &cfg, int32_t hidden, int64_t T, int sms,
 extern "C" size_t kda_gate_proj_workspace_bytes(const kda_config_t *cfg, int32_t hidden, int64_t T)
 {
     if (kda::gp_check(cfg, hidden, T) != KDA_OK) return 0;
-    int sms = 0;
-    if (kda::gp_sms(&sms) != KDA_OK) return 0;
-    return kda::gp_workspace(*cfg, hidden, T, sms, nullptr);
+    return kda::gp_workspace(*cfg, T);
 }
 
 extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int64_t T, const void *x,
@@ -557,8 +598,8 @@ extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int
     if (reinterpret_cast<uintptr_t>(b) & 1u) return gp_fail(KDA_ERR_INVALID, "b is not 2-byte aligned");
     int sms = 0;
     if ((st = gp_sms(&sms)) != KDA_OK) return st;
-    int splits = 1;
-    const size_t need = gp_workspace(*cfg, hidden, T, sms, &splits);
+    const size_t need = gp_workspace(*cfg, T);
+    const int splits = gp_splits((T + 2 * kGpTile - 1) / (2 * kGpTile), hidden / kGpKs, sms);
     if (workspace_bytes < need)
         return gp_fail(KDA_ERR_INVALID, "workspace holds %zu bytes; this call needs %zu", workspace_bytes, need);
 
@@ -591,13 +632,32 @@ extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int
         (e = cudaFuncSetAttribute(gp_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGpOutSmem)) !=
             cudaSuccess)
         return gp_fail(KDA_ERR_CUDA, "kda_gate_proj: %s", cudaGetErrorString(e));
-    gp_in_kernel<<<dim3((mtiles + 1) / 2, splits), 128, in_smem, s>>>(tm_x, tm_fa, tm_bp, part, (int)T, hidden / kGpKs,
-                                                            splits, n1, x_rows, H, err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return gp_fail(KDA_ERR_CUDA, "gp_in_kernel launch: %s", cudaGetErrorString(e));
+    // the slices of a token-tile pair form one cluster (they reduce their sums on chip)
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute at[1];
+    lc.gridDim = dim3((unsigned)((mtiles + 1) / 2), (unsigned)splits, 1);
+    lc.blockDim = dim3(128, 1, 1);
+    lc.dynamicSmemBytes = (size_t)in_smem;
+    lc.stream = s;
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = (unsigned)splits;
+    at[0].val.clusterDim.z = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&lc, gp_in_kernel, tm_x, tm_fa, tm_bp, part, (int)T, hidden / kGpKs, splits, n1,
+                                x_rows, H, err)) != cudaSuccess)
+        return gp_fail(KDA_ERR_CUDA, "gp_in_kernel launch: %s", cudaGetErrorString(e));
+    // programmatic dependent launch: gp_out's prologue and first W_fb copies overlap the end of
+    // gp_in; its epilogue warps wait for gp_in before reading the sums
     const int grid = items < sms ? items : sms;
-    gp_out_kernel<<<grid, kGpOutThreads, kGpOutSmem, s>>>(tm_fb, tm_z, part, static_cast<__nv_bfloat16 *>(b),
-                                                          (int)T, H, HD, n1, splits, ntiles, items, fb_rows,
-                                                          err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return gp_fail(KDA_ERR_CUDA, "gp_out_kernel launch: %s", cudaGetErrorString(e));
+    lc.gridDim = dim3((unsigned)grid, 1, 1);
+    lc.blockDim = dim3(kGpOutThreads, 1, 1);
+    lc.dynamicSmemBytes = (size_t)kGpOutSmem;
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    if ((e = cudaLaunchKernelEx(&lc, gp_out_kernel, tm_fb, tm_z, (const float *)part, static_cast<__nv_bfloat16 *>(b),
+                                (int)T, H, HD, n1, 1, ntiles, items, fb_rows, err)) != cudaSuccess)
+        return gp_fail(KDA_ERR_CUDA, "gp_out_kernel launch: %s", cudaGetErrorString(e));
     return KDA_OK;
 }
