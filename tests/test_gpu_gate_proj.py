@@ -83,3 +83,33 @@ def test_gate_proj_repeatable_and_workspace_checked():
         _run(cfg, inp, workspace=torch.empty(need - 1, dtype=torch.uint8, device="cuda"))
     assert ei.value.status == K.KDA_ERR_INVALID
 
+
+
+# T chosen so that the hidden dimension is split 3, 2 and 1 times on a 152-SM GB300 (tile pairs
+# of 256 tokens: 50, 64 and 256 pairs); 1 means no cluster reduction at all. Rows are sampled,
+# including the first and last token tiles.
+@pytest.mark.parametrize("H,hidden,T", [(96, 1024, 12800), (96, 512, 16384), (8, 512, 65536)])
+def test_gate_proj_large_T_sampled_rows(H, hidden, T):
+    cfg = K.kda_config(H, 128, K.KDA_BF16)
+    inp = KI.make_gate_proj(T, hidden, H, 128, seed=T + H)
+    (z, b), = _run(cfg, inp)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([np.arange(0, 130), np.arange(T - 130, T), rng.integers(0, T, 256)]))
+    z_ref, b_ref = gate_proj(inp["x"][rows], inp["w_fa"], inp["w_fb"], inp["w_b"])
+    ez, eb = rel_err(z[rows], z_ref), rel_err(b[rows], b_ref)
+    print(f"gate_proj H={H} hidden={hidden} T={T}, {len(rows)} rows: z {ez:.2e}, b {eb:.2e}")
+    assert np.isfinite(z).all() and np.isfinite(b).all()
+    assert ez <= TOL_BF16 and eb <= TOL_BF16
+
+
+def test_gate_proj_zero_input_gives_exact_zeros():
+    """x = 0 makes every product 0: z and b must be exactly zero (no stale workspace or
+    staging data leaks into the outputs), also right after a call on nonzero inputs."""
+    H, hidden, T = 96, 512, 700
+    cfg = K.kda_config(H, 128, K.KDA_BF16)
+    inp = KI.make_gate_proj(T, hidden, H, 128, seed=13)
+    ws = torch.empty(K.kda_gate_proj_workspace_bytes(cfg, hidden, T), dtype=torch.uint8, device="cuda")
+    _run(cfg, inp, workspace=ws)
+    inp["x"] = np.zeros_like(inp["x"])
+    (z, b), = _run(cfg, inp, workspace=ws)
+    assert not z.any() and not b.any()
