@@ -13,14 +13,15 @@
 // Two launches on the caller's stream:
 //  1. gp_in_kernel: [f | b] = x [W_fa; W_b]^T for two tiles of 128 tokens over one
 //     slice of the hidden dimension (the weight boxes serve both tiles). When there
-//     are too few tile pairs to fill the GPU the hidden dimension is split over
-//     several CTAs (split-K); each writes its FP32 partial sums to the caller's
-//     workspace.
-//  2. gp_out_kernel: persistent, one CTA per SM. Each CTA walks a contiguous range
-//     of (token tile, 256-column tile of z) items. On entering a token tile it adds
-//     that tile's partial sums in a fixed order (so results do not depend on
-//     timing), rounds f to BF16 as the A operand, and, if it owns the tile's first
-//     z columns, writes the tile's b. W_fb tiles stream
+//     are too few tile pairs to fill the GPU the hidden dimension is split over up
+//     to 8 CTAs (split-K), which form a thread-block cluster and add their partial
+//     sums on chip, in slice order (so results do not depend on timing). The FP32
+//     sums go to the caller's workspace.
+//  2. gp_out_kernel: persistent, one CTA per SM, launched as a programmatic
+//     dependent grid so that its prologue overlaps gp_in. Each CTA walks a
+//     contiguous range of (token tile, 256-column tile of z) items. On entering a
+//     token tile it reads the tile's sums, rounds f to BF16 as the A operand and,
+//     if it owns the tile's first z columns, writes the tile's b. W_fb tiles stream
 //     through a two-stage TMA ring into two TMEM accumulators, so one item's
 //     epilogue (TMEM -> BF16 -> TMA store) runs under the next item's MMAs.
 //
@@ -139,16 +140,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 // ---------------------------------------------------------------- first product
 // CTA (pair, split): [f | b] partial sums of the two token tiles pair*256 .. +127 and
 // pair*256+128 .. +255 over the 64-column steps split, split + splits, ... of the hidden
-// dimension. Each stage brings both tiles'
-// x boxes and one (W_fa | W_b) box, which the MMAs of both accumulators share. Thread 0
-// issues the TMA copies, thread 32 the MMAs. The S slices of one pair form a thread-block
+// dimension. Each stage brings both tiles' x boxes and one (W_fa | W_b) box, which the
+// MMAs of both accumulators share. Thread 0 issues the TMA copies, thread 32 the MMAs.
+// The S slices of one pair form a thread-block
 // cluster: at the end each CTA puts an accumulator (TMEM lane = token) into a padded
 // shared-memory tile, and after a cluster barrier CTA q adds rows q*128/S .. (q+1)*128/S - 1
 // of all S slices' tiles, in slice order, through distributed shared memory, and stores the
 // sums as whole rows. Only the sums leave the chip.
 __global__ void __launch_bounds__(128, 1)
 gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_fa,
-             const __grid_constant__ CUtensorMap tm_bp, float *__restrict__ part, int T, int ksteps, int splits,
+             const __grid_constant__ CUtensorMap tm_bp, float *__restrict__ sums, int T, int ksteps, int splits,
              int n1, int x_rows, int bp_rows, int32_t *err)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -263,7 +264,7 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
         for (int r = r0 + warp; r < r1; r += 4) {
             const int t = tok0 + a * kGpTile + r;
             if (t >= T) break;
-            float4 *dst = reinterpret_cast<float4 *>(part + (size_t)t * n1);
+            float4 *dst = reinterpret_cast<float4 *>(sums + (size_t)t * n1);
             const uint32_t src = smem_u32(tile + r * pitch);
             for (int c4 = lane; c4 < n1 / 4; c4 += 32) {
                 float4 acc = ld_cluster_f4(cluster_map(src + 16u * c4, 0));
@@ -291,8 +292,8 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
 // Warp 8 lane 0 streams W_fb tiles, warp 9 lane 0 issues the MMAs.
 __global__ void __launch_bounds__(kGpOutThreads, 1)
 gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__ CUtensorMap tm_z,
-              const float *__restrict__ part, __nv_bfloat16 *__restrict__ bout, int T, int H, int HD, int n1,
-              int splits, int ntiles, int items, int fb_rows, int32_t *err)
+              const float *__restrict__ sums, __nv_bfloat16 *__restrict__ bout, int T, int H, int HD, int n1,
+              int ntiles, int items, int fb_rows, int32_t *err)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = align_smem(smem_raw);
@@ -372,32 +373,22 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
         __syncwarp();
     } else {
         const int hh = warp >> 2;              // which 128 of the item's 256 z columns
-        // Sum the partials of token tile m (fixed order), round f to the BF16 A operand and, when
-        // with_b, write the tile's b. Warp w takes rows w, w+8, ..., and lane l f columns
-        // 4l .. 4l+3 and b heads 4l .. 4l+3 of each, so every load instruction reads whole rows.
+        // Round token tile m's f sums to the BF16 A operand and, when with_b, write the tile's b.
+        // Warp w takes rows w, w+8, ..., and lane l f columns 4l .. 4l+3 and b heads 4l .. 4l+3
+        // of each, so every load instruction reads whole rows.
         auto form = [&](int m, bool with_b) {
-            const float4 *base = reinterpret_cast<const float4 *>(part) + lane;
-            const size_t sstride = (size_t)T * n1 / 4, rstride = (size_t)n1 / 4;
+            const float4 *base = reinterpret_cast<const float4 *>(sums) + lane;
+            const size_t rstride = (size_t)n1 / 4;
             const bool bl = with_b && 4 * lane < H;  // this lane's b heads exist
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 float4 acc[8], bacc[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = bacc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int sp = 0; sp < splits; ++sp) {
-                    float4 u[8], w[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int t = m * kGpTile + (half * 8 + i) * 8 + warp;
-                        const float4 *src = base + sp * sstride + (size_t)t * rstride;
-                        u[i] = t < T ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-                        w[i] = (bl && t < T) ? src[kD / 4] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        acc[i].x += u[i].x; acc[i].y += u[i].y; acc[i].z += u[i].z; acc[i].w += u[i].w;
-                        bacc[i].x += w[i].x; bacc[i].y += w[i].y; bacc[i].z += w[i].z; bacc[i].w += w[i].w;
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    const int t = m * kGpTile + (half * 8 + i) * 8 + warp;
+                    const float4 *src = base + (size_t)t * rstride;
+                    acc[i] = t < T ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    bacc[i] = (bl && t < T) ? src[kD / 4] : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -624,7 +615,7 @@ extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int32_t *err = static_cast<int32_t *>(workspace);
-    float *part = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + kGpErrBytes);
+    float *sums = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + kGpErrBytes);
     const int in_smem = kGpStages * gp_in_stage_bytes(n1) + 128 + kGpAlign;
     if ((e = cudaMemsetAsync(err, 0, sizeof(int32_t), s)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(gp_in_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, in_smem)) !=
@@ -645,7 +636,7 @@ extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int
     at[0].val.clusterDim.z = 1;
     lc.attrs = at;
     lc.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&lc, gp_in_kernel, tm_x, tm_fa, tm_bp, part, (int)T, hidden / kGpKs, splits, n1,
+    if ((e = cudaLaunchKernelEx(&lc, gp_in_kernel, tm_x, tm_fa, tm_bp, sums, (int)T, hidden / kGpKs, splits, n1,
                                 x_rows, H, err)) != cudaSuccess)
         return gp_fail(KDA_ERR_CUDA, "gp_in_kernel launch: %s", cudaGetErrorString(e));
     // programmatic dependent launch: gp_out's prologue and first W_fb copies overlap the end of
@@ -656,8 +647,8 @@ extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int
     lc.dynamicSmemBytes = (size_t)kGpOutSmem;
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
-    if ((e = cudaLaunchKernelEx(&lc, gp_out_kernel, tm_fb, tm_z, (const float *)part, static_cast<__nv_bfloat16 *>(b),
-                                (int)T, H, HD, n1, 1, ntiles, items, fb_rows, err)) != cudaSuccess)
+    if ((e = cudaLaunchKernelEx(&lc, gp_out_kernel, tm_fb, tm_z, (const float *)sums, static_cast<__nv_bfloat16 *>(b),
+                                (int)T, H, HD, n1, ntiles, items, fb_rows, err)) != cudaSuccess)
         return gp_fail(KDA_ERR_CUDA, "gp_out_kernel launch: %s", cudaGetErrorString(e));
     return KDA_OK;
 }
