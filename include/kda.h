@@ -271,21 +271,22 @@ kda_status kda_prefill_noalloc(const kda_config_t *cfg, const kda_layer_params *
  * sigmoids are applied there).
  *   hidden     width of x; a positive multiple of 64 (7168 for Kimi K3)
  *   T          tokens (rows of x); 0 is a no-op
- *   x          device BF16 [T][hidden]
- *   w_fa       device BF16 [d][hidden]
- *   w_fb       device BF16 [H*d][d]
- *   w_b        device BF16 [H][hidden]
- *   z          device BF16 [T][H*d]     out
- *   b          device BF16 [T][H]       out (2-byte aligned)
+ *   x          device io_dtype [T][hidden]
+ *   w_fa       device io_dtype [d][hidden]
+ *   w_fb       device io_dtype [H*d][d]
+ *   w_b        device io_dtype [H][hidden]
+ *   z          device io_dtype [T][H*d]     out
+ *   b          device io_dtype [T][H]       out (aligned to its element size)
  *   workspace  device scratch of at least kda_gate_proj_workspace_bytes(cfg,
  *              hidden, T) bytes, 16-byte aligned, owned by the caller. Its
  *              first int32 is an error word: the call clears it and a kernel
  *              writes KDA_ERR_TIMEOUT there if a bounded wait gave up (read it
  *              after synchronising if needed). Calls that share a workspace
  *              must be ordered.
- * Products accumulate in FP32 on the tensor cores; f is rounded to BF16 once
- * before the second product, and z, b are rounded to BF16 (nearest even).
- * Needs cfg->io_dtype == KDA_BF16 and num_heads <= 128. Errors:
+ * With BF16 I/O the products run on the tensor cores and accumulate in FP32; f
+ * is rounded to BF16 once before the second product, and z, b are rounded to
+ * BF16 (nearest even). With FP32 I/O they run on CUDA cores in FP32 throughout
+ * (the correctness path). Needs num_heads <= 128. Errors:
  * KDA_ERR_INVALID (bad shape, dtype, alignment, NULL pointer, workspace too
  * small), KDA_ERR_CUDA. The workspace need is 256 bytes plus T * (d + 16
  * ceil(H / 16)) FP32 values (the sums W_fa x and W_b x); the query returns 0

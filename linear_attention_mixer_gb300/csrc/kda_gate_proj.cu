@@ -481,6 +481,59 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
     }
 }
 
+// ---------------------------------------------------------------- FP32 I/O path
+// With FP32 I/O the same products run on CUDA cores in FP32, the correctness path for FP32
+// configurations (as the FP32 prefill kernels are): C[M][N] = A[M][K] B[N][K]^T in 64 x 64
+// output tiles, 256 threads with 4 x 4 outputs each, K staged through shared memory 16 at a
+// time. Each output is one FP32 dot product in k order, so results do not depend on timing.
+__global__ void __launch_bounds__(256)
+gp_f32_gemm_kernel(const float *__restrict__ A, int lda, const float *__restrict__ B, int ldb, float *__restrict__ C,
+                   int ldc, int M, int N, int K)
+{
+    __shared__ float As[16][68], Bs[16][68];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        for (int e = threadIdx.x; e < 64 * 16; e += 256) {
+            const int r = e >> 4, c = e & 15;  // 16 consecutive k of one row per 16 threads
+            As[c][r] = (m0 + r < M && k0 + c < K) ? A[(size_t)(m0 + r) * lda + k0 + c] : 0.f;
+            Bs[c][r] = (n0 + r < N && k0 + c < K) ? B[(size_t)(n0 + r) * ldb + k0 + c] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            const float4 a = *reinterpret_cast<const float4 *>(&As[kk][4 * ty]);
+            const float4 bb = *reinterpret_cast<const float4 *>(&Bs[kk][4 * tx]);
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int m = m0 + 4 * ty + i, n = n0 + 4 * tx + j;
+            if (m < M && n < N) C[(size_t)m * ldc + n] = acc[i][j];
+        }
+}
+
+cudaError_t gp_f32_gemm(const float *A, int lda, const float *B, int ldb, float *C, int ldc, int M, int N, int K,
+                        cudaStream_t s)
+{
+    const dim3 grid((unsigned)((N + 63) / 64), (unsigned)((M + 63) / 64));
+    gp_f32_gemm_kernel<<<grid, 256, 0, s>>>(A, lda, B, ldb, C, ldc, M, N, K);
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- host side
 thread_local char g_msg[256];
 
@@ -530,8 +583,6 @@ int gp_splits(int64_t pairs, int ksteps, int sms)
 kda_status gp_check(const kda_config_t *cfg, int32_t hidden, int64_t T)
 {
     if (!config_ok(cfg)) return KDA_ERR_INVALID;
-    if (cfg->io_dtype != KDA_BF16)
-        return gp_fail(KDA_ERR_INVALID, "kda_gate_proj supports BF16 I/O only (io_dtype must be KDA_BF16)");
     if (cfg->num_heads > 128) return gp_fail(KDA_ERR_INVALID, "kda_gate_proj needs num_heads <= 128 (got %d)", cfg->num_heads);
     if (hidden < kGpKs || hidden % kGpKs != 0)
         return gp_fail(KDA_ERR_INVALID, "hidden must be a positive multiple of %d (got %d)", kGpKs, hidden);
@@ -586,9 +637,26 @@ extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int
                          reinterpret_cast<uintptr_t>(w_fb) | reinterpret_cast<uintptr_t>(w_b) |
                          reinterpret_cast<uintptr_t>(z);
     if (al & 15u) return gp_fail(KDA_ERR_INVALID, "x, w_fa, w_fb, w_b or z is not 16-byte aligned");
-    if (reinterpret_cast<uintptr_t>(b) & 1u) return gp_fail(KDA_ERR_INVALID, "b is not 2-byte aligned");
+    if (reinterpret_cast<uintptr_t>(b) & (cfg->io_dtype == KDA_F32 ? 3u : 1u))
+        return gp_fail(KDA_ERR_INVALID, "b is not aligned to its element size");
     int sms = 0;
     if ((st = gp_sms(&sms)) != KDA_OK) return st;
+    if (cfg->io_dtype == KDA_F32) {
+        // f into the workspace, b and z straight to the outputs
+        cudaStream_t s32 = static_cast<cudaStream_t>(stream);
+        float *f = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + kGpErrBytes);
+        const int H = cfg->num_heads, HD = H * kD;
+        cudaError_t e;
+        if ((e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s32)) != cudaSuccess ||
+            (e = gp_f32_gemm(static_cast<const float *>(x), hidden, static_cast<const float *>(w_fa), hidden, f, kD,
+                             (int)T, kD, hidden, s32)) != cudaSuccess ||
+            (e = gp_f32_gemm(static_cast<const float *>(x), hidden, static_cast<const float *>(w_b), hidden,
+                             static_cast<float *>(b), H, (int)T, H, hidden, s32)) != cudaSuccess ||
+            (e = gp_f32_gemm(f, kD, static_cast<const float *>(w_fb), kD, static_cast<float *>(z), HD, (int)T, HD, kD,
+                             s32)) != cudaSuccess)
+            return gp_fail(KDA_ERR_CUDA, "kda_gate_proj (FP32): %s", cudaGetErrorString(e));
+        return KDA_OK;
+    }
     const size_t need = gp_workspace(*cfg, T);
     const int splits = gp_splits((T + 2 * kGpTile - 1) / (2 * kGpTile), hidden / kGpKs, sms);
     if (workspace_bytes < need)

@@ -291,8 +291,8 @@ def kda_gate_proj_workspace_bytes(cfg: kda_config_t, hidden: int, T: int) -> int
 
 
 def kda_gate_proj(cfg: kda_config_t, x, w_fa, w_fb, w_b, z, b, workspace: torch.Tensor, stream=None) -> None:
-    """z = W_fb (W_fa x), b = W_b x for x [T, hidden]; every tensor BF16 except the
-    workspace (any dtype, at least kda_gate_proj_workspace_bytes bytes)."""
+    """z = W_fb (W_fa x), b = W_b x for x [T, hidden]; every tensor in the config's I/O dtype
+    except the workspace (any dtype, at least kda_gate_proj_workspace_bytes bytes)."""
     H, d = cfg.num_heads, cfg.head_dim
     if x.dim() != 2:
         raise ValueError("x must be [T, hidden]")
@@ -301,7 +301,7 @@ def kda_gate_proj(cfg: kda_config_t, x, w_fa, w_fb, w_b, z, b, workspace: torch.
                            ("z", z, (T, H * d)), ("b", b, (T, H))):
         if tuple(t.shape) != shape:
             raise ValueError(f"{name} must be {list(shape)}, got {list(t.shape)}")
-    bf = torch.bfloat16
+    bf = _torch_io_dtype(cfg)
     ws = _dev(workspace, None, "workspace")
     _check(lib().kda_gate_proj(ctypes.byref(cfg), hidden, T, _dev(x, bf, "x"), _dev(w_fa, bf, "w_fa"),
                                _dev(w_fb, bf, "w_fb"), _dev(w_b, bf, "w_b"), _dev(z, bf, "z"), _dev(b, bf, "b"),

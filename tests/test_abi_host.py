@@ -99,7 +99,7 @@ def test_binding_marshalling_checks(K):
 
 
 def test_gate_proj_arguments_rejected_before_the_device(K):
-    """kda_gate_proj checks dtype, geometry, workspace and alignment on the host; the
+    """kda_gate_proj checks geometry, workspace and alignment on the host; the
     workspace query returns 0 for the same invalid arguments. T = 0 is a no-op."""
     L = K.lib()
     bf = K.kda_config(96, 128, K.KDA_BF16)
@@ -107,7 +107,7 @@ def test_gate_proj_arguments_rejected_before_the_device(K):
     wide = K.kda_config(200, 128, K.KDA_BF16)
     fake = ctypes.c_void_p(1 << 20)  # an aligned address that is never dereferenced
     args = [fake] * 6
-    for cfg, hidden, T, why in ((f32, 7168, 16, "BF16"), (bf, 100, 16, "multiple of 64"), (bf, 0, 16, "multiple"),
+    for cfg, hidden, T, why in ((bf, 100, 16, "multiple of 64"), (f32, 100, 16, "multiple of 64"), (bf, 0, 16, "multiple"),
                                 (wide, 7168, 16, "num_heads"), (bf, 7168, -1, "T must be")):
         assert L.kda_gate_proj_workspace_bytes(ctypes.byref(cfg), hidden, T) == 0
         assert L.kda_gate_proj(ctypes.byref(cfg), hidden, T, *args, fake, 1 << 30, None) == K.KDA_ERR_INVALID
@@ -120,3 +120,6 @@ def test_gate_proj_arguments_rejected_before_the_device(K):
                            None) == K.KDA_ERR_INVALID
     assert "16-byte aligned" in K.kda_last_error()
     assert L.kda_gate_proj(ctypes.byref(bf), 7168, 0, *args, fake, 0, None) == K.KDA_OK
+    # the workspace holds the error word and T x (d + 16 ceil(H / 16)) FP32 sums, for either dtype
+    for cfg in (bf, f32):
+        assert L.kda_gate_proj_workspace_bytes(ctypes.byref(cfg), 7168, 1000) == 256 + 1000 * (128 + 96) * 4
