@@ -13,9 +13,10 @@
  *   o     = S^T q                             read after the update
  *   out   = sigmoid(g) * RMSNorm_head(o)      RMSNorm weight [d], shared by all heads
  *
- * The W_q/W_k/W_v/W_o/W_g/W_b and decay projections stay outside: callers pass
- * the post-projection q, k, v, the gate pre-activation z (without dt_bias), the
- * beta logits b and the output-gate logits g.
+ * The W_q/W_k/W_v/W_o/W_g projections stay outside: callers pass the
+ * post-projection q, k, v, the gate pre-activation z (without dt_bias), the
+ * beta logits b and the output-gate logits g. z and b can come from
+ * kda_gate_proj below (the decay-gate and beta projections of the hidden state).
  *
  * Conventions for every entry point:
  *  - Status codes are returned; no call exits the process or traps on the GPU.
