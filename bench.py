@@ -717,6 +717,13 @@ def run_kda(args):
                     "n": n, "ms_per_call": mms, "tokens_per_s": Bd * n / (mms / 1e3),
                     "vs_n_single_token_calls": n * line["ms_per_step"] / mms,
                     "achieved_gbs": mbytes / (mms / 1e3) / 1e9, "bytes_per_call": mbytes})
+    if args.only == "decode_multi":
+        line["decode_multi"] = []
+        for n in (4, 8):
+            mms = _time_decode_multi(K, cfg, params, gen, dev, stream, Bd, n)
+            line["decode_multi"].append({"n": n, "ms_per_call": mms, "tokens_per_s": Bd * n / (mms / 1e3)})
+        line["value"] = line["decode_multi"][-1]["tokens_per_s"]
+        line["ms_per_step"] = line["decode_multi"][-1]["ms_per_call"]
     if args.only in ("all", "prefill"):
         pre_ms = _time_prefill(K, args, cfg, params, gen, dev, stream)
         pre_flop = PRE_FLOP_PER_TOKEN_HEAD * Tp * H
@@ -768,7 +775,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
     ap.add_argument("--prefill-reps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "gate_proj"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "decode_multi", "prefill", "gate_proj"], default="all",
                     help="time one part only (small profiling runs); the JSON line keeps its keys")
     ap.add_argument("--batch", type=int, default=B_DEC, help="decode batch (profiling runs)")
     ap.add_argument("--prefill-tokens", type=int, default=T_PRE, help="prefill length (profiling runs)")

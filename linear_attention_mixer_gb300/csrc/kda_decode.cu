@@ -59,8 +59,8 @@ decode_persistent_kernel(const float *__restrict__ conv_w, const float *__restri
     float *snw = sdt + kD;                                             // [d]
     float *sh_k = snw + kD, *sh_a = sh_k + kD, *sh_v = sh_a + kD, *sh_gw = sh_v + kD;
     float *sh_ak = sh_gw + kD, *sh_aq = sh_ak + kD, *su = sh_aq + kD, *so = su + kD;  // [d] each
-    float *red = so + kD;                                              // [2][8][d] warp partials
-    float *part = red + 2 * 8 * kD;                                    // [3][4]
+    float *red = so + kD;                                              // warp partials of p and r (kRedFloats)
+    float *part = red + kRedFloats;                                    // [3][4]
     uint64_t *bar = reinterpret_cast<uint64_t *>(part + 16);           // [NS]
 
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
@@ -207,7 +207,7 @@ cudaError_t launch_persistent(const State &st, const kda_layer_params &p, const 
     const kda_config_t &c = st.cfg;
     const int H = c.num_heads;
     const size_t smem = (size_t)NS * StageLayout<T>::kBytes + 3 * kD * 16 + 2 * kD * 4 + 8 * kD * 4 +
-                        2 * 8 * kD * 4 + 16 * 4 + NS * 8;
+                        kRedFloats * 4 + 16 * 4 + NS * 8;
     cudaError_t e = cudaFuncSetAttribute(decode_persistent_kernel<T, NS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

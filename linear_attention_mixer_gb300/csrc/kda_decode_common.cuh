@@ -15,6 +15,13 @@
 
 namespace kda {
 
+// The warp partials of p sit at red[0 .. 8 kD) and those of r at red[kRedR .. kRedR + 8 kD).
+// The 16-float gap keeps the two apart by a bank offset: in the column finish, lanes 0..15 read
+// p and lanes 16..31 read r of the same columns, and without it every such load would be a
+// two-way bank conflict.
+constexpr int kRedR = 8 * kD + 16;
+constexpr int kRedFloats = kRedR + 8 * kD;
+
 __device__ __forceinline__ float4 dc_fma4(float a, float4 x, float4 y)
 {
     return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
@@ -104,7 +111,7 @@ __device__ __forceinline__ void dc_norm_store(float4 oo, const float *gw, T *out
 }
 
 // ak[i] = a_i k^_i, aq[i] = a_i q^_i, a[i], k[i] (k^), v[c], gw[c]: shared-memory vectors of 128
-// red: [2][8][128] floats (warp partials of p and r), su, so: [128] floats (u and o).
+// red: kRedFloats floats (warp partials of p and of r, see kRedR), su, so: [128] floats (u and o).
 // kq = k^ . q^. out_row: this unit's 128 output values. Contains two __syncthreads.
 // With kFly, ak and aq are not read: the coefficients come from a, k and aq, which then holds q^.
 template <typename T, bool kFly = false>
@@ -117,13 +124,13 @@ __device__ __forceinline__ void decode_token_step(float4 (&s)[16], const float *
     float4 p, rr;
     if constexpr (kFly) dc_partials_akq(s, a, k, aq, w, p, rr);
     else dc_partials(s, ak, aq, w, p, rr);
-    reinterpret_cast<float4 *>(red)[(0 * 8 + w) * 32 + l] = p;
-    reinterpret_cast<float4 *>(red)[(1 * 8 + w) * 32 + l] = rr;
+    reinterpret_cast<float4 *>(red)[w * 32 + l] = p;
+    reinterpret_cast<float4 *>(red + kRedR)[w * 32 + l] = rr;
     __syncthreads();
     // 2. warp w finishes columns 16w .. 16w+15: lanes 0..15 sum p, lanes 16..31 sum r
     {
         const int c = 16 * w + (l & 15), which = l >> 4;
-        const float *col = red + which * 8 * kD + c;
+        const float *col = red + which * kRedR + c;
         float acc = col[0];
 #pragma unroll
         for (int ww = 1; ww < 8; ++ww) acc += col[ww * kD];

@@ -54,8 +54,8 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
     // NST = 2: alpha k^ and alpha q^ per row; NST = 1 forms them on the fly and sh_q holds q^
     float *sh_ak = sh_gw + kNT * kD, *sh_aq = sh_ak + kNT * kD;
     float *su = (NST == 2 ? sh_aq + kNT * kD : sh_gw + kNT * kD), *so = su + kD;  // [d] u, o of the current token
-    float *red = so + kD;                          // [2][8][d] warp partials
-    float *part = red + 2 * 8 * kD;                // [token][3][4] quarter sums of squares
+    float *red = so + kD;                          // warp partials of p and r (kRedFloats)
+    float *part = red + kRedFloats;                // [token][3][4] quarter sums of squares
     float *sbeta = part + kNT * 12;                                  // [token] beta
     uint64_t *bar = reinterpret_cast<uint64_t *>(sbeta + kNT);       // [2]
 
@@ -223,7 +223,7 @@ cudaError_t launch_multi_typed(const State &st, const kda_layer_params &p, const
     const kda_config_t &c = st.cfg;
     const int H = c.num_heads;
     const size_t smem = NST * (size_t)L::kBytes + (NST == 2 ? 7 : 5) * KDA_DECODE_MAX_TOKENS * kD * 4 + 2 * kD * 4 +
-                        2 * 8 * kD * 4 + KDA_DECODE_MAX_TOKENS * 13 * 4 + 2 * 8;
+                        kRedFloats * 4 + KDA_DECODE_MAX_TOKENS * 13 * 4 + 2 * 8;
     cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<T, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
