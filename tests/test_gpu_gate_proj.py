@@ -127,3 +127,41 @@ def test_gate_proj_fp32_matches_oracle(H, hidden, T):
     ez, eb = rel_err(z, z_ref), rel_err(b, b_ref)
     print(f"gate_proj FP32 H={H} hidden={hidden} T={T}: z {ez:.2e}, b {eb:.2e}")
     assert ez <= TOL_F32 and eb <= TOL_F32
+
+
+def test_gate_proj_feeds_the_mixer_fp32(oracle_mod):
+    """The projection composed with the mixer, in FP32 (hidden state x -> kda_gate_proj -> z, b ->
+    kda_prefill over two ragged sequences), against the oracle doing the same from x (its own
+    projection, then its sequential recurrence): the mixer's FP32 bound of 1e-3."""
+    from tests.kda_testutil import dev_params, to_np
+    H, d, hidden, lens = 4, 128, 256, [70, 33]
+    T = sum(lens)
+    cfg = K.kda_config(H, d, K.KDA_F32)
+    gp = KI.make_gate_proj(T, hidden, H, d, seed=21)
+    p = KI.make_params(H, d, 4, seed=21)
+    tok = KI.make_tokens(T, H, d, seed=21, bf16=False)
+    (z, b), = _run(cfg, gp)
+    dev = {n: torch.from_numpy(np.ascontiguousarray(tok[n])).cuda() for n in ("q", "k", "v", "g")}
+    dev["z"], dev["b"] = torch.from_numpy(z).cuda(), torch.from_numpy(b).cuda()
+    cu_h = np.array([0, lens[0], T], dtype=np.int32)
+    st = K.kda_state_alloc(cfg, 2)
+    try:
+        out = torch.empty(T, H * d, device="cuda")
+        K.kda_prefill(cfg, dev_params(p), st, torch.tensor([0, 1], dtype=torch.int32, device="cuda"),
+                      torch.tensor(cu_h, device="cuda"), cu_h, dev["q"], dev["k"], dev["v"], dev["z"], dev["b"],
+                      dev["g"], out)
+        got = to_np(out)
+        assert K.kda_state_poll_error(st) == 0
+    finally:
+        K.kda_state_free(st)
+    z_o, b_o = gate_proj(gp["x"], gp["w_fa"], gp["w_fb"], gp["w_b"])
+    oc = oracle_mod.OracleCfg(H=H, d=d)
+    refs = []
+    for s0, s1 in ((0, lens[0]), (lens[0], T)):
+        seq = {n: tok[n][s0:s1] for n in ("q", "k", "v", "g")}
+        seq["z"], seq["b"] = z_o[s0:s1], b_o[s0:s1]
+        S, tail = oracle_mod.new_state(oc)
+        refs.append(oracle_mod.sequence(oc, p, S, tail, seq))
+    err = rel_err(got, np.concatenate(refs))
+    print(f"gate_proj -> prefill, FP32, {T} tokens: rel err {err:.2e}")
+    assert err <= TOL_F32
