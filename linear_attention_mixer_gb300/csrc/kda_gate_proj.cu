@@ -117,13 +117,14 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
+// (no memory clobber: several of these may be in flight at once; the cluster barrier before
+// them orders them after the peers' writes)
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr)
 {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
+                 : "r"(addr));
     return v;
 }
 __device__ __forceinline__ void cluster_sync_all()
@@ -266,14 +267,29 @@ gp_in_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ C
             if (t >= T) break;
             float4 *dst = reinterpret_cast<float4 *>(sums + (size_t)t * n1);
             const uint32_t src = smem_u32(tile + r * pitch);
-            for (int c4 = lane; c4 < n1 / 4; c4 += 32) {
-                float4 acc = ld_cluster_f4(cluster_map(src + 16u * c4, 0));
-                for (int sp = 1; sp < splits; ++sp) {
-                    const float4 u = ld_cluster_f4(cluster_map(src + 16u * c4, (uint32_t)sp));
-                    acc.x += u.x; acc.y += u.y; acc.z += u.z; acc.w += u.w;
+            // this lane's chunks lane and lane + 32 of the row (n1 / 4 <= 64): all slices' values
+            // are requested before any is added (remote loads are slow; issued one after another
+            // each would wait for the previous one), then added in slice order
+            const int c4a = lane, c4b = lane + 32;
+            const bool hb = c4b < n1 / 4;
+            float4 ua[kGpMaxSplit], ub[kGpMaxSplit];
+#pragma unroll
+            for (int sp = 0; sp < kGpMaxSplit; ++sp) {
+                if (sp < splits) {
+                    ua[sp] = ld_cluster_f4(cluster_map(src + 16u * c4a, (uint32_t)sp));
+                    if (hb) ub[sp] = ld_cluster_f4(cluster_map(src + 16u * c4b, (uint32_t)sp));
                 }
-                dst[c4] = acc;
             }
+            float4 acc = ua[0], accb = hb ? ub[0] : acc;
+#pragma unroll
+            for (int sp = 1; sp < kGpMaxSplit; ++sp) {
+                if (sp < splits) {
+                    acc.x += ua[sp].x; acc.y += ua[sp].y; acc.z += ua[sp].z; acc.w += ua[sp].w;
+                    if (hb) { accb.x += ub[sp].x; accb.y += ub[sp].y; accb.z += ub[sp].z; accb.w += ub[sp].w; }
+                }
+            }
+            dst[c4a] = acc;
+            if (hb) dst[c4b] = accb;
         }
         cluster_sync_all();  // every CTA is done reading the tiles
     }
