@@ -508,7 +508,7 @@ gp_f32_gemm_kernel(const float *__restrict__ A, int lda, const float *__restrict
 {
     __shared__ float As[16][68], Bs[16][68];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    const int m0 = blockIdx.x * 64, n0 = blockIdx.y * 64;  // rows on x: T may exceed 65535 tiles
     float acc[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -545,7 +545,7 @@ gp_f32_gemm_kernel(const float *__restrict__ A, int lda, const float *__restrict
 cudaError_t gp_f32_gemm(const float *A, int lda, const float *B, int ldb, float *C, int ldc, int M, int N, int K,
                         cudaStream_t s)
 {
-    const dim3 grid((unsigned)((N + 63) / 64), (unsigned)((M + 63) / 64));
+    const dim3 grid((unsigned)((M + 63) / 64), (unsigned)((N + 63) / 64));
     gp_f32_gemm_kernel<<<grid, 256, 0, s>>>(A, lda, B, ldb, C, ldc, M, N, K);
     return cudaGetLastError();
 }
