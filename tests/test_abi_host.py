@@ -123,3 +123,27 @@ def test_gate_proj_arguments_rejected_before_the_device(K):
     # the workspace holds the error word and T x (d + 16 ceil(H / 16)) FP32 sums, for either dtype
     for cfg in (bf, f32):
         assert L.kda_gate_proj_workspace_bytes(ctypes.byref(cfg), 7168, 1000) == 256 + 1000 * (128 + 96) * 4
+
+
+def test_header_is_plain_c_and_a_c_program_links(K, tmp_path):
+    """include/kda.h compiles as C99 with warnings as errors, and a C program links against
+    libkda.so and calls it (kda_config and an argument check need no GPU)."""
+    src = tmp_path / "use_kda.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "kda.h"\n'
+        "int main(void) {\n"
+        "    kda_config_t c;\n"
+        "    if (kda_config(&c, 96, 128, KDA_BF16) != KDA_OK) return 1;\n"
+        "    if (c.num_heads != 96 || c.head_dim != 128 || c.conv_kernel != 4) return 2;\n"
+        "    if (kda_config(&c, 96, 64, KDA_BF16) != KDA_ERR_INVALID) return 3;\n"
+        "    if (kda_last_error()[0] == 0) return 4;\n"
+        "    if (kda_gate_proj_workspace_bytes(&c, 7168, 10) != 256 + 10 * (128 + 96) * 4) return 5;\n"
+        "    printf(\"ok\\n\");\n"
+        "    return 0;\n"
+        "}\n")
+    exe = tmp_path / "use_kda"
+    libdir = os.path.dirname(K.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-L", libdir, "-lkda", "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
