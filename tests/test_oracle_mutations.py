@@ -30,6 +30,9 @@ MUTATIONS = [
     ("RMS over the sum, not the mean", "double r = 1.0 / sqrt(ms / d + eps);", "double r = 1.0 / sqrt(ms + eps);"),
     ("output gate without sigmoid", "out[i] = kdao_sigmoid(g[i]) * (o[i] * r * w[i]);", "out[i] = g[i] * (o[i] * r * w[i]);"),
     ("beta without sigmoid", "const double beta = kdao_sigmoid((double)b[(long)t * ldb]);", "const double beta = (double)b[(long)t * ldb];"),
+    ("dt_bias of head 0 for every head", "(double)dt_bias[h * d + i]", "(double)dt_bias[i]"),
+    ("A_log of head 0 for every head", "kdao_gate_alpha((double)A_log[h],", "kdao_gate_alpha((double)A_log[0],"),
+    ("z of the first token for every token", "(double)z[(long)t * ld + i]", "(double)z[i]"),
     ("k normalised with the q scale", "kdao_l2norm(d, xk, cfg->l2_eps, 1.0, kh);", "kdao_l2norm(d, xk, cfg->l2_eps, cfg->q_scale, kh);"),
 ]
 

@@ -393,3 +393,53 @@ def test_bf16_round_is_nearest_even():
     assert y[3] == -2.5
     assert np.all(np.abs(y - x) <= np.abs(x) * 2.0 ** -8)
     assert np.array_equal(KI.from_bf16_bits(KI.to_bf16_bits(y)), y)
+
+
+# ---------------- per-head gate wiring through the whole pipeline ----------------
+
+def test_gate_wiring_per_head_and_channel(oracle_mod):
+    """Three tokens from a zero state and history, H = 3 heads whose A_log differ and whose
+    dt_bias differ per channel. The expected values are the page's formula written with numpy
+    matrix products: x_t = SiLU(sum of taps over the raw inputs seen so far), the gate
+    alpha_t[c] = exp(-5 sigmoid(exp(A_log[h]) (z_t[c] + dt_bias[h d + c]))), and
+    S_t = (I - b_t k_t k_t^T) Diag(alpha_t) S_{t-1} + b_t k_t v_t^T, o_t = S_t^T q_t.
+    From the second token on the decay of S_1 enters o and S, so using another head's
+    A_log, another head's dt_bias or another token's z changes the result
+    (kimi_k3.c header comment, block "KDA per-head recurrence")."""
+    H, d, T = 3, 16, 3
+    cfg = oracle_mod.OracleCfg(H=H, d=d)
+    p = KI.make_params(H, d, 4, seed=14)
+    p.A_log[:] = np.array([0.05, 1.3, 2.6], dtype=np.float32)   # distinct per head
+    tok = KI.make_tokens(T, H, d, 14, False)
+    S, tail = oracle_mod.new_state(cfg)
+    out = oracle_mod.sequence(cfg, p, S, tail, tok)
+
+    sig = lambda x: 1.0 / (1.0 + np.exp(-x))
+    for h in range(H):
+        sl = slice(h * d, (h + 1) * d)
+        W = p.conv_w[:, sl, :].astype(np.float64)            # [3, d, 4], oldest tap first
+        raw = {n: tok[n][:, sl].astype(np.float64) for n in "qkv"}
+        St = np.zeros((d, d))
+        for t in range(T):
+            feat = {}
+            for i, n in enumerate("qkv"):
+                window = np.zeros((4, d))                       # rows: x_{t-3} .. x_t
+                for j in range(4):
+                    s = t - 3 + j
+                    if s >= 0:
+                        window[j] = raw[n][s]
+                pre = np.einsum("cj,jc->c", W[i], window)
+                feat[n] = pre * sig(pre)
+            qh = feat["q"] / np.sqrt(feat["q"] @ feat["q"] + 1e-6) * d ** -0.5
+            kh = feat["k"] / np.sqrt(feat["k"] @ feat["k"] + 1e-6)
+            arg = np.exp(float(p.A_log[h])) * (tok["z"][t, sl].astype(np.float64)
+                                               + p.dt_bias[sl].astype(np.float64))
+            alpha = np.exp(-5.0 * sig(arg))
+            beta = sig(float(tok["b"][t, h]))
+            St = (np.eye(d) - beta * np.outer(kh, kh)) @ np.diag(alpha) @ St + beta * np.outer(kh, feat["v"])
+            o = St.T @ qh
+            ref = sig(tok["g"][t, sl].astype(np.float64)) * p.norm_w * o / np.sqrt(np.mean(o * o) + 1e-6)
+            np.testing.assert_allclose(out[t, sl], ref, rtol=1e-11, atol=1e-13, err_msg=f"h={h} t={t}")
+        np.testing.assert_allclose(S[h], St, rtol=1e-11, atol=1e-14, err_msg=f"state h={h}")
+    # the decay really acts here: with alpha = 1 forced the last state would differ
+    assert np.abs(S[1]).max() > 0
