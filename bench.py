@@ -429,9 +429,27 @@ def _time_decode_b1(K, cfg, params, gen, dev, stream):
         b1_ev[i][1].record(stream)
     torch.cuda.synchronize()
     b1_us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in b1_ev)
+    # host time of one kda_decode_token call (CPU clock, no synchronisation): the C entry point
+    # called through ctypes with its arguments built once, so the figure is the library's own
+    # host path (checks, launch) plus one ctypes call
+    import ctypes
+    x = x1[0]
+    args_c = (ctypes.byref(cfg), ctypes.byref(params), st1, ctypes.c_void_p(s1.data_ptr()), 1,
+              *(ctypes.c_void_p(x[n].data_ptr()) for n in ("q", "k", "v", "z", "b", "g")),
+              ctypes.c_void_p(o1.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+    fn = K.lib().kda_decode_token
+    host_us = []
+    for rep in range(5):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(100):
+            rc = fn(*args_c)
+        host_us.append((time.perf_counter() - t0) / 100 * 1e6)
+        assert rc == 0
+    torch.cuda.synchronize()
     K.kda_state_free(st1)
     del flush
-    return b1_us
+    return b1_us, statistics.median(host_us)
 
 
 def _time_decode_multi(K, cfg, params, gen, dev, stream, Bd, n, reps=50):
@@ -701,10 +719,13 @@ def run_kda(args):
             "clocks": r["clocks"],
         })
         if args.only == "all":
-            b1_us = _time_decode_b1(K, cfg, params, gen, dev, stream)
+            b1_us, host_us = _time_decode_b1(K, cfg, params, gen, dev, stream)
             line["decode_b1"] = {"workload": "decode B=1, 96 heads x 128, BF16 I/O, FP32 state "
                                              "(L2 flushed between steps)",
-                                 "latency_us": b1_us, "bytes_per_step": DEC_BYTES_PER_UNIT * H,
+                                 "latency_us": b1_us, "host_us_per_call": host_us,
+                                 "host_note": "CPU clock per kda_decode_token call, no synchronisation, "
+                                              "100 calls back to back through ctypes, median of 5",
+                                 "bytes_per_step": DEC_BYTES_PER_UNIT * H,
                                  "achieved_gbs": DEC_BYTES_PER_UNIT * H / (b1_us / 1e6) / 1e9}
             # speculative-verify style decode: n tokens per sequence per call, one state pass
             line["decode_multi"] = []
@@ -767,7 +788,24 @@ def run_kda(args):
     return 0
 
 
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _self_launch(n: int, argv) -> int:
+    """--gpus N > 1 without a launcher: re-run this script under torch.distributed.run,
+    one process per GPU on this node (independent replicas), rendezvous on 127.0.0.1.
+    Rank 0 prints the JSON line; the return code is the launcher's."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.abspath(__file__)] + list(argv)
+    return subprocess.run(cmd, cwd=ROOT).returncode
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
@@ -780,6 +818,8 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=B_DEC, help="decode batch (profiling runs)")
     ap.add_argument("--prefill-tokens", type=int, default=T_PRE, help="prefill length (profiling runs)")
     args = ap.parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return _self_launch(args.gpus, argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -239,21 +239,24 @@ kda_status kda_prefill(const kda_config_t *cfg, const kda_layer_params *params, 
  *   S      device FP32 [max_slots][H][d][d], caller-owned (layout of a kda_state's S)
  *   tail   device io_dtype [max_slots][3][K-1][H*d], caller-owned conv history
  *   err    device int32 word that receives KDA_ERR_DEVICE for a bad slot id or a
- *          cu_seqlens that disagrees with cu_seqlens_host; never cleared by the
- *          library. NULL: a word inside the static workspace is used (and cleared
- *          at the start of each call), and such errors are not reported.
+ *          cu_seqlens that disagrees with cu_seqlens_host, or KDA_ERR_TIMEOUT if
+ *          a bounded device-side wait gave up; never cleared by the library.
+ *          NULL: a word inside the static workspace is used (and cleared at the
+ *          start of each call), and such errors are not reported.
  *   slots .. out, stream: as for kda_prefill.
  * Its scratch is a file-scope __device__ array of KDA_NOALLOC_WORKSPACE_BYTES
  * (128 MiB; every GPU that loads the library holds it until the process exits).
  * A call whose workspace need exceeds it returns KDA_ERR_INVALID before
  * enqueuing anything; split such a call. The need is about 90.6 KB per (chunk
- * of 64 tokens, head) with BF16 I/O (about 15 chunks, 980 tokens, of one
+ * of 64 tokens, head) with BF16 I/O (at most 960 tokens, 15 chunks, of one
  * sequence at 96 heads), and 148 KB per (chunk, head) plus 512 B per (token,
- * head) with FP32 I/O. The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture. All calls on a device share the array
- * and it keeps the previous call's contents: calls whose work overlaps on the
- * GPU race, so order them (one stream, or events).
+ * head) with FP32 I/O. Every call looks up the array's device address in the
+ * current context (cudaGetSymbolAddress, which allocates nothing), so the
+ * address stays valid after cudaDeviceReset and in any context; the first
+ * call in a context may load the library's module there, so make it before
+ * any stream capture. All calls on a device share the array and it keeps the
+ * previous call's contents: calls whose work overlaps on the GPU race, so
+ * order them (one stream, or events).
  */
 #define KDA_NOALLOC_WORKSPACE_BYTES ((size_t)128 << 20)
 kda_status kda_prefill_noalloc(const kda_config_t *cfg, const kda_layer_params *params, float *S, void *tail,

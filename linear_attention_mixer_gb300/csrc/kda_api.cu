@@ -150,6 +150,7 @@ kda_status kda_state_alloc(const kda_config_t *cfg, int32_t max_slots, kda_state
     st->cfg = *cfg;
     st->max_slots = max_slots;
     cudaError_t e = cudaGetDevice(&st->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&st->sms, cudaDevAttrMultiProcessorCount, st->device);
     const size_t sb = state_bytes(*cfg) * (size_t)max_slots, tb = tail_bytes(*cfg) * (size_t)max_slots;
     if (e == cudaSuccess) e = cudaMalloc(&st->S, sb);
     if (e == cudaSuccess) e = cudaMalloc(&st->tail, tb);

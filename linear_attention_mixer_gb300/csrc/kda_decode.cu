@@ -208,13 +208,11 @@ cudaError_t launch_persistent(const State &st, const kda_layer_params &p, const 
     const int H = c.num_heads;
     const size_t smem = (size_t)NS * StageLayout<T>::kBytes + 3 * kD * 16 + 2 * kD * 4 + 8 * kD * 4 +
                         kRedFloats * 4 + 16 * 4 + NS * 8;
-    cudaError_t e = cudaFuncSetAttribute(decode_persistent_kernel<T, NS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = raise_smem_once(st, sizeof(T) == 2 ? kSmemDecodeBf16 : kSmemDecodeF32,
+                                    decode_persistent_kernel<T, NS>, smem);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
+    int sms = 0;
+    if ((e = state_sms(st, &sms)) != cudaSuccess) return e;
     const int n_units = B * H;
     const int grid = n_units < sms ? n_units : sms;
     decode_persistent_kernel<T, NS><<<grid, 256, smem, stream>>>(

@@ -224,12 +224,11 @@ cudaError_t launch_multi_typed(const State &st, const kda_layer_params &p, const
     const int H = c.num_heads;
     const size_t smem = NST * (size_t)L::kBytes + (NST == 2 ? 7 : 5) * KDA_DECODE_MAX_TOKENS * kD * 4 + 2 * kD * 4 +
                         kRedFloats * 4 + KDA_DECODE_MAX_TOKENS * 13 * 4 + 2 * 8;
-    cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<T, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = raise_smem_once(st, sizeof(T) == 2 ? kSmemMultiBf16 : kSmemMultiF32,
+                                    decode_multi_kernel<T, NST>, smem);
     if (e != cudaSuccess) return e;
     int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, st.device);
-    if (e != cudaSuccess) return e;
+    if ((e = state_sms(st, &sms)) != cudaSuccess) return e;
     const int n_units = B * H;
     const int ctas = (3 - NST) * sms;  // CTAs resident at once
     const int grid = n_units < ctas ? n_units : ctas;

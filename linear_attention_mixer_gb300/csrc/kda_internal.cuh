@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/kda.h"
 
 namespace kda {
@@ -24,7 +26,38 @@ struct State {
     int32_t *err;     // device error word (0 = none)
     void *ws;         // prefill workspace
     size_t ws_bytes;
+    int sms;          // SM count of the device, read once when the state is made (0: not read)
+    // Kernels whose dynamic shared-memory limit has been raised on this state's device, one
+    // bit each (kSmem* below). Raising it is a host driver call; doing it once per state keeps
+    // it off the per-call path of the decode entry points. A state does not outlive its
+    // device context, so the bits cannot go stale.
+    mutable std::atomic<uint32_t> smem_raised;
 };
+
+enum : uint32_t {
+    kSmemDecodeBf16 = 1u << 0, kSmemDecodeF32 = 1u << 1, kSmemMultiBf16 = 1u << 2, kSmemMultiF32 = 1u << 3,
+    kSmemPrepTc = 1u << 4, kSmemPrepF32 = 1u << 5, kSmemStateTc = 1u << 6, kSmemStateF32 = 1u << 7,
+};
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` once per state.
+template <typename Fn>
+inline cudaError_t raise_smem_once(const State &st, uint32_t bit, Fn *kernel, size_t bytes)
+{
+    if (st.smem_raised.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) st.smem_raised.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+// The SM count of the state's device (read at allocation; looked up if the state has none).
+inline cudaError_t state_sms(const State &st, int *sms)
+{
+    if (st.sms > 0) {
+        *sms = st.sms;
+        return cudaSuccess;
+    }
+    return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, st.device);
+}
 
 // ---------------------------------------------------------------- IO types
 template <typename T> struct IO;

@@ -1554,8 +1554,7 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
     if (total_chunks > 0) {
         if constexpr (kTC) {
             int sms = 0;
-            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, st.device);
-            if (e != cudaSuccess) return e;
+            if ((e = state_sms(st, &sms)) != cudaSuccess) return e;
             // boxes of 67 rows (3 history rows + a chunk); never taller than the tensor
             const int box_rows = (int)(total_T < kC + 3 ? total_T : kC + 3);
             const int64_t Dm = (int64_t)H * kD;
@@ -1565,7 +1564,7 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
                 (e = encode_rows_map(&tmv, v, total_T, Dm, box_rows)) != cudaSuccess ||
                 (e = encode_rows_map(&tmz, z, total_T, Dm, box_rows)) != cudaSuccess)
                 return e;
-            e = cudaFuncSetAttribute(prep_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepTcSmem);
+            e = raise_smem_once(st, kSmemPrepTc, prep_tc_kernel<T>, kPrepTcSmem);
             if (e != cudaSuccess) return e;
             // persistent: one CTA per SM strides over the (chunk, head) items
             const int n_items = total_chunks * H;
@@ -1575,7 +1574,7 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
                 c.gate_lower_bound, c.l2_eps, c.q_scale, n_items, box_rows, tmq, tmk, tmv, tmz);
         } else {
             const int prep_smem = kPrepSmemFloats * (int)sizeof(float);
-            e = cudaFuncSetAttribute(prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
+            e = raise_smem_once(st, kSmemPrepF32, prep_kernel<T>, prep_smem);
             if (e != cudaSuccess) return e;
             prep_kernel<T><<<(unsigned)(total_chunks * H), 256, prep_smem, stream>>>(
                 p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
@@ -1586,7 +1585,7 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
         if (e != cudaSuccess) return e;
     }
     if constexpr (kTC) {
-        e = cudaFuncSetAttribute(state_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateTcSmem);
+        e = raise_smem_once(st, kSmemStateTc, state_tc_kernel<T>, kStateTcSmem);
         if (e != cudaSuccess) return e;
         // gate logits in and output rows out as 64-row boxes (never taller than the tensor)
         const int box_g = (int)(total_T < kC ? total_T : kC);
@@ -1605,7 +1604,7 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
         return cudaGetLastError();
     } else {
         const int state_smem = kStateSmemFloats * (int)sizeof(float);
-        e = cudaFuncSetAttribute(state_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem);
+        e = raise_smem_once(st, kSmemStateF32, state_kernel<T>, state_smem);
         if (e != cudaSuccess) return e;
         state_kernel<T><<<dim3(kD / kVB, H, N), 256, state_smem, stream>>>(
             st.S, (T *)st.tail, st.err, slots, H, st.max_slots, table, seq_first,

@@ -16,7 +16,6 @@
 // and the o buffer are fully rewritten by each call; only the error word must
 // start at zero, and it is cleared at the start of every call.
 #include <cstdio>
-#include <mutex>
 
 #include "kda_internal.cuh"
 
@@ -26,25 +25,22 @@ constexpr size_t kErrRegion = 256;  // first 256 bytes: the error word used when
 
 __device__ __align__(256) unsigned char g_noalloc_ws[KDA_NOALLOC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 256;
-std::mutex g_mu;
-void *g_ws_addr[kMaxDevices];  // device address of g_noalloc_ws, per device
-
-// Once per device, with that device current: the device address of the array.
-// The array's host-side name is only a stand-in; kernels must get this address.
-kda_status workspace_address(int dev, unsigned char **out)
+// The device address of the array in the current context. The array's host-side
+// name is only a stand-in; kernels must get this address. It is looked up on
+// every call (cudaGetSymbolAddress allocates nothing), so it stays right after a
+// cudaDeviceReset and in whichever context is current; a cached address could
+// point into a context that no longer exists. The first lookup in a context may
+// load the library's module there.
+kda_status workspace_address(unsigned char **out)
 {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_ws_addr[dev]) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_ws);
-        if (e != cudaSuccess || !p) {
-            cudaGetLastError();
-            return kda::record_error(KDA_ERR_CUDA, cudaGetErrorString(e));
-        }
-        g_ws_addr[dev] = p;
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_ws);
+    if (e != cudaSuccess || !p) {
+        cudaGetLastError();
+        return kda::record_error(KDA_ERR_CUDA, e != cudaSuccess ? cudaGetErrorString(e)
+                                                                : "cudaGetSymbolAddress gave a null address");
     }
-    *out = static_cast<unsigned char *>(g_ws_addr[dev]);
+    *out = static_cast<unsigned char *>(p);
     return KDA_OK;
 }
 
@@ -87,9 +83,8 @@ extern "C" kda_status kda_prefill_noalloc(const kda_config_t *cfg, const kda_lay
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return kda::record_error(KDA_ERR_CUDA, cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices) return kda::record_error(KDA_ERR_INVALID, "device ordinal out of range");
     unsigned char *base = nullptr;
-    const kda_status s = workspace_address(dev, &base);
+    const kda_status s = workspace_address(&base);
     if (s != KDA_OK) return s;
 
     cudaStream_t strm = static_cast<cudaStream_t>(stream);

@@ -51,3 +51,21 @@ def test_two_rank_timing_reduction():
         assert mx == 15.0
         assert value == pytest.approx(256 * 7 * 2 / 0.015)
         assert rc == 0
+
+
+def test_bench_gpus_2_launches_two_ranks():
+    """bench.py --gpus 2 run without a launcher starts two ranks itself (torch.distributed.run
+    on 127.0.0.1); with the reference arm rank 0 prints one line carrying n_gpus 2 and the
+    other rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, "bench.py", "--gpus", "2", "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["impl"] == "reference" and line["value"] > 0
