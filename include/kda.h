@@ -247,8 +247,8 @@ kda_status kda_prefill(const kda_config_t *cfg, const kda_layer_params *params, 
  * Its scratch is a file-scope __device__ array of KDA_NOALLOC_WORKSPACE_BYTES
  * (128 MiB; every GPU that loads the library holds it until the process exits).
  * A call whose workspace need exceeds it returns KDA_ERR_INVALID before
- * enqueuing anything; split such a call. The need is about 90.6 KB per (chunk
- * of 64 tokens, head) with BF16 I/O (at most 960 tokens, 15 chunks, of one
+ * enqueuing anything; split such a call. The need is about 131.6 KB per (chunk
+ * of 64 tokens, head) with BF16 I/O (at most 640 tokens, 10 chunks, of one
  * sequence at 96 heads), and 148 KB per (chunk, head) plus 512 B per (token,
  * head) with FP32 I/O. Every call looks up the array's device address in the
  * current context (cudaGetSymbolAddress, which allocates nothing), so the

@@ -42,19 +42,30 @@ constexpr int kKRS = kC + 1;  // padded row of the transposed right factor (no b
 constexpr int kPrepSmemFloats = 4 * kC * kD + 2 * kC * kC + kD * kKRS + 2 * kBlk * kD + kC;
 constexpr int kStateSmemFloats = kD * kVB + 3 * kC * kD + 2 * kC * kVB + kC * kC + kD;
 
-// Tensor-core path (BF16 I/O): per (chunk, head) the prep kernel writes one block that
-// the state kernel brings into shared memory with a single bulk copy. Operand tiles are
-// BF16 in the K-major interleaved layout of kda_tc.cuh:
-//   W   [64 r][128 k]  B operand of  S^T W^T          (N = 64,  K = 128)
-//   QG  [64 r][128 k]  B operand of  S^T QG^T         (N = 64,  K = 128)
-//   P   [64 r][64 i]   B operand of  U^T P^T          (N = 64,  K = 64)
-//   KDT [128 k][64 r]  B operand of  U^T KD           (N = 128, K = 64)
-//   U'  [64 r][128 v]  FP32, subtracted in registers
-//   gC  [128]          FP32 chunk decay exp(G_last)
-constexpr int kOffW = 0, kOffQG = 16384, kOffP = 32768, kOffKDT = 40960, kOffUp = 57344, kOffG = 90112;
-constexpr int kTcChunkBytes = 90624;
-constexpr int kTcStageBytes = kOffG;  // W..U' go to a 1024-aligned stage, gC to its own buffer
-constexpr int kStateTcSmem = 2 * kTcStageBytes + 32768 + 16384 + 2 * kD * 4 + 4 * kC * 4 + 64;
+// Tensor-core path (BF16 I/O): per (chunk, head) the prep kernel writes one block that the
+// state kernel reads as two bulk copies (tile A with exp(G_last), then tile B) plus U' read
+// by its threads. Operand tiles are BF16 in the K-major interleaved layout of kda_tc.cuh.
+// The factors that carry the state (W, K o exp(G_last - G), and P for the output's U term)
+// are stored as a BF16 high part and a low part (x - high): with single BF16 operands the
+// state drifts by up to a few percent when the decay is near 1, beta near 1 and the keys
+// strongly correlated (the products then cancel), so each product is formed as
+// hi*hi + lo*hi + hi*lo, about 16 bits of mantissa.
+//   tile A [192 rows][128 k]: rows 0..63 W_hi [r][k], 64..127 QG [r][k], 128..191 W_lo
+//          B operands of S^T [W_hi | QG]^T (N = 128), S^T W_hi^T and S^T W_lo^T (N = 64)
+//   gamma  [128] FP32 exp(G_last), right after tile A (it travels with tile A's copy)
+//   tile B [384 rows][64 r]: rows 0..63 P_hi [r][i], 64..191 KDT_hi [k][r], 192..255 P_lo,
+//          256..383 KDT_lo; B operands of U^T [P | KDT] (N = 192, hi rows or lo rows)
+//   U'     [64 r][128 v] FP32, read by the state pass's threads
+constexpr int kOffTA = 0, kOffGam = 49152, kOffTB = 49664, kOffUp = 98816;
+constexpr int kTcChunkBytes = 131584;
+constexpr int kStageABytes = kOffTB;   // tile A + gamma
+constexpr int kStageBBytes = kOffUp - kOffTB;
+static_assert(kStageBBytes == 49152 && kOffUp + kC * kD * 4 == kTcChunkBytes, "chunk block layout");
+// state_tc_kernel shared memory: S^T hi | S^T lo | U^T hi | U^T lo | stage A | stage B | g/out rows | sums | barriers
+constexpr int kSmST = 0, kSmUT = 65536, kSmA = 98304, kSmB = kSmA + kStageABytes, kSmGY = kSmB + kStageBBytes;
+constexpr int kSmRed = kSmGY + kC * kD * 2, kSmBar = kSmRed + 4 * kC * 4;
+constexpr int kStateTcSmem = kSmBar + 8 * 8 + 16;
+static_assert(kSmB % 128 == 0 && kSmGY % 128 == 0, "TMA and bulk destinations");
 static_assert(kStateTcSmem <= 232448, "state_tc_kernel shared memory");
 constexpr uint32_t kTcWaitLimit = 1u << 26;
 
@@ -594,7 +605,10 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                     float o[8];
 #pragma unroll
                     for (int t = 0; t < 8; ++t) o[t] = __uint_as_float(wv[8 * g8 + t]);
-                    st16(b + kOffW + tc::kmajor_off(r, col + 8 * g8, kD), pack8_bf16(o));
+                    uint4 hi, lo;
+                    split8(o, hi, lo);
+                    st16(b + kOffTA + tc::kmajor_off(r, col + 8 * g8, kD), hi);
+                    st16(b + kOffTA + tc::kmajor_off(2 * kC + r, col + 8 * g8, kD), lo);
                 }
             }
         }
@@ -782,7 +796,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                     ld8f(GL + r * kYS + c0, gr);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) o[j] = qv[j] * exp_ftz(gr[j]);
-                    st16(blk + kOffQG + tc::kmajor_off(r, c0, kD), pack8_bf16(o));
+                    st16(blk + kOffTA + tc::kmajor_off(kC + r, c0, kD), pack8_bf16(o));
                 }
             } else {
                 for (int u = tid; u < kD * (kC / 8); u += 512) {  // channel c, rows 8 rb .. +7
@@ -794,9 +808,12 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                         const int r = 8 * rb + j;
                         o[j] = Yk[r * kYS + c] * exp_ftz(gl - GL[r * kYS + c]);
                     }
-                    st16(blk + kOffKDT + tc::kmajor_off(c, 8 * rb, kC), pack8_bf16(o));
+                    uint4 hi, lo;
+                    split8(o, hi, lo);
+                    st16(blk + kOffTB + tc::kmajor_off(kC + c, 8 * rb, kC), hi);
+                    st16(blk + kOffTB + tc::kmajor_off(4 * kC + c, 8 * rb, kC), lo);
                 }
-                if (tid < kD) reinterpret_cast<float *>(blk + kOffG)[tid] = exp_ftz(GL[(kC - 1) * kYS + tid]);
+                if (tid < kD) reinterpret_cast<float *>(blk + kOffGam)[tid] = exp_ftz(GL[(kC - 1) * kYS + tid]);
             }
         }
         good &= mbar_wait_bounded(bars + 1, 1u, kTcWaitLimit);  // second completion: half 1
@@ -845,7 +862,10 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                         const float pv = __uint_as_float(i < 32 ? a0[i] : a1[i - 32]);
                         o[t] = i <= r ? pv : 0.f;
                     }
-                    st16(blk + kOffP + tc::kmajor_off(r, 8 * g8, kC), pack8_bf16(o));
+                    uint4 hi, lo;
+                    split8(o, hi, lo);
+                    st16(blk + kOffTB + tc::kmajor_off(r, 8 * g8, kC), hi);
+                    st16(blk + kOffTB + tc::kmajor_off(3 * kC + r, 8 * g8, kC), lo);
                 }
             }
         }
@@ -1148,15 +1168,20 @@ state_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__res
 // One CTA (256 threads) per (sequence, head). TMEM lane v holds value index v:
 //   D1 = S^T W^T     [v][r]  TMEM columns   0.. 63
 //   D2 = S^T QG^T    [v][r]  TMEM columns  64..127, then += U^T P^T  -> O^T
-//   D3 = S^T         [v][k]  TMEM columns 128..255, FP32 state, scaled by gC and += U^T KD
-// Warps w and w+4 share lane quarter w%4 and split the columns in halves (grp = w/4).
-// S^T is also kept in shared memory as a BF16 A operand. Per chunk c:
-//   [MMA1(c): D1, D2 issued at the end of c-1] | scale D3 by gC | U^T = U'^T - D1 -> BF16 |
-//   MMA2(c): D2 += U^T P^T, D3 += U^T KD | O^T -> registers, sums of squares | S^T operand
-//   refreshed from D3 | chunk c+2 requested, MMA1(c+1) issued | gated RMSNorm of c written out
-// so the output epilogue of c overlaps MMA1(c+1). Chunk blocks arrive by bulk copy into two
-// shared-memory stages. Every wait is bounded; on expiry the error word gets KDA_ERR_TIMEOUT
-// and the CTA drains what it issued and returns.
+//   D3 = S^T         [v][k]  TMEM columns 128..255, the FP32 state, scaled by gamma and += U^T KD
+// Warps w and w + 4 share lane quarter w % 4 and split the columns in halves (grp = w / 4).
+// S^T and U^T are kept in shared memory as BF16 high and low parts (A operands), and each
+// product that carries the state is formed as hi*hi + lo*hi + hi*lo:
+//   MMA1: [D1 | D2] = S_hi^T [W_hi | QG]^T, D1 += S_lo^T W_hi^T + S_hi^T W_lo^T
+//   MMA2: [D2 | D3] += U_hi^T [P_hi | KDT_hi] + U_lo^T [P_hi | KDT_hi] + U_hi^T [P_lo | KDT_lo]
+// Per chunk c:
+//   [MMA1(c) in flight] scale D3 by gamma; U'(c) loaded to registers | U^T = U' - D1 -> hi/lo |
+//   MMA2(c); stage A of c + 1 requested | S^T hi/lo refreshed from D3, O^T read, sums of
+//   squares; stage B of c + 1 and the gate rows of c requested | MMA1(c + 1) issued |
+//   gated RMSNorm of c written out (over MMA1(c + 1)).
+// Chunk blocks arrive by bulk copy into one stage A and one stage B buffer; each is refilled as
+// soon as the MMA that reads it has completed, and block c + 2 is prefetched into L2. Every wait
+// is bounded; on expiry the error word gets KDA_ERR_TIMEOUT and the CTA drains what it issued.
 template <typename T>
 __global__ void __launch_bounds__(256, 1)
 state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__restrict__ err,
@@ -1167,23 +1192,20 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 const float *__restrict__ norm_w, T *__restrict__ out, float rms_eps, int box_rows,
                 const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_out)
 {
+    static_assert(sizeof(T) == 2, "the tensor-core path reads BF16 gate logits");
     extern __shared__ __align__(1024) float smf[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(smf);
-    // [stage 0 | stage 1 | S^T | U^T | gC x2 | red | barriers]; operand tiles 1024-aligned
-    unsigned char *sST = sm + 2 * kTcStageBytes;           // S^T [v][k] BF16, K-major, 32 KB
-    unsigned char *sUT = sST + 32768;                      // U^T [v][r] BF16, K-major, 16 KB
-    float *sgam = reinterpret_cast<float *>(sUT + 16384);  // [2 stages][128] chunk decay
+    unsigned char *sSTh = sm + kSmST, *sSTl = sSTh + 32768;   // S^T [v][k] BF16, K = 128
+    unsigned char *sUTh = sm + kSmUT, *sUTl = sUTh + 16384;   // U^T [v][r] BF16, K = 64
+    unsigned char *sA = sm + kSmA, *sB = sm + kSmB;
+    const float *sgam = reinterpret_cast<const float *>(sA + kOffGam);
+    __nv_bfloat16 *sGY = reinterpret_cast<__nv_bfloat16 *>(sm + kSmGY);  // gate rows, then output rows
     // [64 tokens][4 value quarters] partial sums of squares, added in a fixed order (so that the
-    // outputs do not depend on the order the warps finish in). One buffer is enough: a chunk's
-    // RMSNorm reads them before the barrier that ends every full chunk, and only a sequence's
-    // last chunk can be ragged.
-    float *red = sgam + 2 * kD;
-    // barriers: [0..1] W|QG of stage 0/1, [2] mma1, [3] mma2, [4] g rows, [5..6] the rest of stage 0/1
-    uint64_t *bar = reinterpret_cast<uint64_t *>(red + 4 * kC);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 7);
-    // after MMA2 the U^T buffer holds this chunk's gate logits [64 r][128 v] (one TMA box), and
-    // the epilogue overwrites them in place with the output rows
-    __nv_bfloat16 *sGY = reinterpret_cast<__nv_bfloat16 *>(sUT);
+    // outputs do not depend on the order the warps finish in)
+    float *red = reinterpret_cast<float *>(sm + kSmRed);
+    // barriers: [0] stage A, [1] stage B, [2] MMA1, [3] MMA2, [4] gate rows
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kSmBar);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 8);
 
     const int h = blockIdx.x, seq = blockIdx.y;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
@@ -1197,10 +1219,11 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     const size_t D = (size_t)H * kD;
     const int c_first = seq_first[seq], c_last = seq_first[seq + 1];
     float *Sg = S_all + ((size_t)slot * H + h) * kD * kD;
+    auto block_of = [&](int ci) { return chunks + ((size_t)h * total_chunks + ci) * kTcChunkBytes; };
 
     if (w == 0) tc::tmem_alloc(tslot, 256);
     if (tid == 0) {
-        for (int i = 0; i < 7; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
     }
     tc::fence_before_sync();
@@ -1212,31 +1235,54 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     const int k0 = 64 * grp;   // this thread's state columns k0 .. k0+63
     const int r0 = 32 * grp;   // this thread's tokens r0 .. r0+31
 
-    // thread 0 only: chunk ci's block into a stage as two copies, W|QG (all that MMA1 reads)
-    // first on bar[stage], then P|KDT|U'|gC on bar[5 + stage]
-    static_assert(kOffW == 0 && kOffQG + kD * kC * 2 == kOffP, "W|QG lead the block");
-    auto issue = [&](int stage, int ci) {
-        const unsigned char *src = chunks + ((size_t)h * total_chunks + ci) * kTcChunkBytes;
-        unsigned char *dst = sm + stage * kTcStageBytes;
-        mbar_arrive_expect_tx(&bar[stage], kOffP);
-        bulk_g2s(dst, src, kOffP, &bar[stage]);
-        mbar_arrive_expect_tx(&bar[5 + stage], kTcChunkBytes - kOffP);
-        bulk_g2s(dst + kOffP, src + kOffP, kTcStageBytes - kOffP, &bar[5 + stage]);
-        bulk_g2s(sgam + stage * kD, src + kOffG, kD * 4, &bar[5 + stage]);
+    // thread 0 only: the two copies of a chunk block
+    auto issue_a = [&](int ci) {
+        mbar_arrive_expect_tx(&bar[0], kStageABytes);
+        bulk_g2s(sA, block_of(ci) + kOffTA, kStageABytes, &bar[0]);
     };
-    constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
-    // W (rows 0..63) and QG (rows 64..127) form one N = 128 B operand, P (rows 0..63) and KDT
-    // (rows 64..191) one N = 192 operand, so each MMA group is a single run of K steps.
-    static_assert(kOffQG - kOffW == 64 * kD * 2 && kOffKDT - kOffP == 64 * kC * 2, "adjacent operand tiles");
+    auto issue_b = [&](int ci) {
+        mbar_arrive_expect_tx(&bar[1], kStageBBytes);
+        bulk_g2s(sB, block_of(ci) + kOffTB, kStageBBytes, &bar[1]);
+    };
+    constexpr uint32_t id64 = tc::idesc_bf16(128, 64), id128 = tc::idesc_bf16(128, 128);
     constexpr uint32_t id192 = tc::idesc_bf16(128, 192);
-    auto mma1 = [&](const unsigned char *stage) {  // thread 0 only: [D1 | D2] = S^T [W | QG]^T
+    auto mma1 = [&]() {  // thread 0 only
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            tc::mma_bf16(tb, tc::kmajor_desc(sST, kk, kD), tc::kmajor_desc(stage + kOffW, kk, kD), id128, kk > 0);
+            tc::mma_bf16(tb, tc::kmajor_desc(sSTh, kk, kD), tc::kmajor_desc(sA, kk, kD), id128, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            tc::mma_bf16(tb, tc::kmajor_desc(sSTl, kk, kD), tc::kmajor_desc(sA, kk, kD), id64, 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            tc::mma_bf16(tb, tc::kmajor_desc(sSTh, kk, kD), tc::kmajor_desc(sA + 2 * kC * kD * 2, kk, kD), id64, 1);
         tc::mma_commit(&bar[2]);
     };
+    auto mma2 = [&]() {  // thread 0 only
+        unsigned char *sBlo = sB + 3 * kC * kC * 2;  // rows 192.. of tile B
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16(tb + 64, tc::kmajor_desc(sUTh, kk, kC), tc::kmajor_desc(sB, kk, kC), id192, 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16(tb + 64, tc::kmajor_desc(sUTl, kk, kC), tc::kmajor_desc(sB, kk, kC), id192, 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16(tb + 64, tc::kmajor_desc(sUTh, kk, kC), tc::kmajor_desc(sBlo, kk, kC), id192, 1);
+        tc::mma_commit(&bar[3]);
+    };
+    // 16 values -> BF16 high and low parts at (row, k .. k + 15) of two K-major tiles
+    auto put16_split = [](unsigned char *th, unsigned char *tl, int row, int kc, const float *x, int Kd) {
+        uint4 hi, lo;
+        split8(x, hi, lo);
+        st16(th + tc::kmajor_off(row, kc, Kd), hi);
+        st16(tl + tc::kmajor_off(row, kc, Kd), lo);
+        split8(x + 8, hi, lo);
+        st16(th + tc::kmajor_off(row, kc + 8, Kd), hi);
+        st16(tl + tc::kmajor_off(row, kc + 8, Kd), lo);
+    };
 
-    // initial state: S[k][v] -> D3 row v (FP32) and the BF16 operand row v
+    // initial state: S[k][v] -> D3 row v (FP32) and the BF16 operand parts of row v
     float vals[32];
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
@@ -1244,105 +1290,135 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
 #pragma unroll
         for (int j = 0; j < 32; ++j) vals[j] = Sg[(size_t)(kb + j) * kD + vi];
         tc::tmem_st32(tD3 + kb, vals);
-        store_row_bf16(sST, vi, kb, vals, kD);
-        store_row_bf16(sST, vi, kb + 16, vals + 16, kD);
+        put16_split(sSTh, sSTl, vi, kb, vals, kD);
+        put16_split(sSTh, sSTl, vi, kb + 16, vals + 16, kD);
     }
     tc::tmem_wait_st();
     tc::fence_smem_to_async();
-    if (tid == 0) {
-        for (int i = 0; i < 2; ++i)
-            if (c_first + i < c_last) issue(i, c_first + i);
-        if (c_first < c_last) tma_prefetch_2d(&tm_g, h * kD, table[c_first].t0);
+    if (tid == 0 && c_first < c_last) {
+        issue_a(c_first);
+        issue_b(c_first);
+        if (c_first + 1 < c_last) prefetch_l2_bulk(block_of(c_first + 1), kTcChunkBytes);
+        tma_prefetch_2d(&tm_g, h * kD, table[c_first].t0);
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     bool good = true, aborted = false;
-    bool stage_ok = true, issued2 = false;  // this chunk's copy landed; chunk ci + 2 requested
-    int gpar = -1;                          // parity of a gate-logit box still in flight, or -1
+    // copies in flight when a wait gives up: stage A / B of the next chunk, gate rows
+    bool a_pending = false, b_pending = false, g_pending = false, mma1_pending = false, mma2_pending = false;
+    uint32_t pa = 0, pb = 0, p1 = 0, p2 = 0, pg = 0;  // phases of bars 0..4
     if (tid == 0 && c_first < c_last) {
-        good &= mbar_wait_bounded(&bar[0], 0, kTcWaitLimit);
-        if (good) mma1(sm);
+        good &= mbar_wait_bounded(&bar[0], pa, kTcWaitLimit);
+        if (good) {
+            mma1();
+            mma1_pending = true;
+        }
     }
+    pa ^= 1u;
 
     const float nw = __ldg(norm_w + vi);
-    uint32_t ph1 = 0, ph2 = 0;
-    int it = 0;
     ChunkEntry e_next = c_first < c_last ? table[c_first] : ChunkEntry{0, 0, 0, 0};
-    for (int ci = c_first; ci < c_last; ++ci, ++it) {
-        const int st = it & 1;
-        const unsigned char *stage = sm + st * kTcStageBytes;
+    for (int ci = c_first; ci < c_last; ++ci) {
         const ChunkEntry e = e_next;  // read one chunk ahead
         if (ci + 1 < c_last) {
             e_next = table[ci + 1];
-            // the next chunk's gate logits into L2 now: its box is fetched a chunk from now and
-            // an HBM round trip would stall the epilogue
-            if (tid == 0) tma_prefetch_2d(&tm_g, h * kD, e_next.t0);
+            if (tid == 0) {
+                // the next chunk's gate rows and the block after next into L2: their copies are
+                // requested within this chunk and an HBM round trip would stall them
+                tma_prefetch_2d(&tm_g, h * kD, e_next.t0);
+                if (ci + 2 < c_last) prefetch_l2_bulk(block_of(ci + 2), kTcChunkBytes);
+            }
         }
-        static_assert(sizeof(T) == 2, "the tensor-core path reads BF16 gate logits");
-
-        stage_ok = mbar_wait_bounded(&bar[5 + st], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
-        good &= stage_ok;
-        issued2 = false;
-        // D3 = Diag(gC) on its columns, while MMA1 runs on D1 / D2
+        // U' of this thread's tokens, loaded while MMA1 runs (a warp reads 128 contiguous bytes
+        // per token)
+        float up[32];
         {
-            const float *gam = sgam + st * kD + k0;
+            const float *Up = reinterpret_cast<const float *>(block_of(ci) + kOffUp) + vi;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) up[j] = __ldcs(Up + (size_t)(r0 + j) * kD);
+        }
+        // D3 = Diag(gamma) on this thread's columns (stage A has landed: MMA1 reads it)
+        {
+            const bool landed = mbar_wait_bounded(&bar[0], pa ^ 1u, kTcWaitLimit);
+            good &= landed;
+            uint32_t raw[32];
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                tc::tmem_ld32_nowait(tD3 + k0 + 32 * half, raw);
+                tc::tmem_wait_ld();
+                const float *gam = sgam + k0 + 32 * half;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]) * gam[j];
+                tc::tmem_st32(tD3 + k0 + 32 * half, vals);
+            }
+            tc::tmem_wait_st();
+        }
+        {
+            const bool ok = mbar_wait_bounded(&bar[2], p1, kTcWaitLimit);
+            good &= ok;
+            if (tid == 0 && ok) mma1_pending = false;
+        }
+        p1 ^= 1u;
+        tc::fence_after_sync();
+        // U^T = U'^T - (W S)^T on this thread's tokens, as BF16 high and low parts
+        {
+            uint32_t raw[32];
+            tc::tmem_ld32_nowait(tD1 + r0, raw);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) vals[j] = up[j] - __uint_as_float(raw[j]);
+            put16_split(sUTh, sUTl, vi, r0, vals, kC);
+            put16_split(sUTh, sUTl, vi, r0 + 16, vals + 16, kC);
+        }
+        tc::fence_smem_to_async();
+        tc::fence_before_sync();
+        if (__syncthreads_or(!good)) { aborted = true; break; }
+        tc::fence_after_sync();
+        if (tid == 0) {
+            // MMA1 has read stage A and every thread has read gamma: refill it with the next chunk
+            if (ci + 1 < c_last) {
+                issue_a(ci + 1);
+                a_pending = true;
+            }
+            good &= mbar_wait_bounded(&bar[1], pb, kTcWaitLimit);
+            if (good) {
+                mma2();
+                mma2_pending = true;
+            }
+        }
+        pb ^= 1u;
+        good &= mbar_wait_bounded(&bar[3], p2, kTcWaitLimit);
+        p2 ^= 1u;
+        tc::fence_after_sync();
+        if (tid == 0 && good) {
+            mma2_pending = false;
+            if (ci + 1 < c_last) {
+                issue_b(ci + 1);
+                b_pending = true;
+            }
+            // this chunk's gate rows into the gate/output buffer once the previous output box
+            // has been read out of it
+            bulk_wait_read_all();
+            mbar_arrive_expect_tx(&bar[4], (uint32_t)(box_rows * kD * sizeof(T)));
+            tma_load_2d(sGY, &tm_g, h * kD, e.t0, &bar[4]);
+            g_pending = true;
+        }
+        // refresh the S^T operand parts from the updated FP32 state
+        {
             uint32_t raw[32];
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 tc::tmem_ld32_nowait(tD3 + k0 + 32 * half, raw);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]) * gam[32 * half + j];
-                tc::tmem_st32(tD3 + k0 + 32 * half, vals);
+                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
+                put16_split(sSTh, sSTl, vi, k0 + 32 * half, vals, kD);
+                put16_split(sSTh, sSTl, vi, k0 + 32 * half + 16, vals + 16, kD);
             }
-            tc::tmem_wait_st();
         }
-        good &= mbar_wait_bounded(&bar[2], ph1, kTcWaitLimit);
-        ph1 ^= 1u;
-        // the previous chunk's epilogue is done with the U^T buffer (its output box has been
-        // read out by the TMA store)
-        if (tid == 0) bulk_wait_read_all();
-        __syncthreads();
-        tc::fence_after_sync();
-        // U^T = U'^T - (W S)^T on this thread's tokens, as the BF16 A operand
-        {
-            const float *Up = reinterpret_cast<const float *>(stage + kOffUp);
-            uint32_t raw[32];
-            tc::tmem_ld32_nowait(tD1 + r0, raw);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) vals[j] = Up[(r0 + j) * kD + vi] - __uint_as_float(raw[j]);
-            store_row_bf16(sUT, vi, r0, vals, kC);
-            store_row_bf16(sUT, vi, r0 + 16, vals + 16, kC);
-        }
-        tc::fence_smem_to_async();
-        tc::fence_before_sync();
-        if (__syncthreads_or(!good)) { aborted = true; break; }
-        tc::fence_after_sync();
-        if (tid == 0) {  // [D2 | D3] += U^T [P | KDT]^T
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc::mma_bf16(tb + 64, tc::kmajor_desc(sUT, kk, kC), tc::kmajor_desc(stage + kOffP, kk, kC), id192, 1);
-            tc::mma_commit(&bar[3]);
-        }
-        good &= mbar_wait_bounded(&bar[3], ph2, kTcWaitLimit);
-        ph2 ^= 1u;
-        tc::fence_after_sync();
-        // the stage is consumed (U' and gC were read before MMA2, which read P and KDT): request
-        // chunk ci + 2 into it now
-        // MMA2 has read U^T: the buffer takes this chunk's gate logits (requested first: copies
-        // are served in order and the epilogue needs these sooner than the next block)
-        if (tid == 0 && good) {
-            mbar_arrive_expect_tx(&bar[4], (uint32_t)(box_rows * kD * sizeof(T)));
-            tma_load_2d(sUT, &tm_g, h * kD, e.t0, &bar[4]);
-        }
-        if (good) gpar = it & 1;
-        if (tid == 0 && good && ci + 2 < c_last) {
-            issue(st, ci + 2);
-            issued2 = true;
-        }
-        // O^T on this thread's tokens, their partial sums of squares over this warp's 32 v
+        // O^T on this thread's tokens and their sums of squares over this warp's 32 v: a
+        // reduce-scatter butterfly (31 shuffles) leaves the sum of token r0 + lane in lane `lane`
         float o[32];
         {
             uint32_t raw[32];
@@ -1350,10 +1426,6 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             tc::tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(raw[j]);
-        }
-        // sums of squares over this warp's 32 v for its 32 tokens: a reduce-scatter butterfly
-        // (31 shuffles) that leaves the sum of token r0 + lane in lane `lane`
-        {
             float sq[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) sq[j] = o[j] * o[j];
@@ -1367,38 +1439,29 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                     sq[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
                 }
             }
-            red[(r0 + lane) * 4 + qtr] = sq[0];  // the four lane quarters are added in the epilogue
-        }
-        // refresh the S^T operand from the updated FP32 state
-        {
-            uint32_t raw[32];
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                tc::tmem_ld32_nowait(tD3 + k0 + 32 * half, raw);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
-                store_row_bf16(sST, vi, k0 + 32 * half, vals, kD);
-                store_row_bf16(sST, vi, k0 + 32 * half + 16, vals + 16, kD);
-            }
+            red[(r0 + lane) * 4 + qtr] = sq[0];
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
         if (__syncthreads_or(!good)) { aborted = true; break; }
         tc::fence_after_sync();
-        if (tid == 0) {
-            // start the next chunk's first MMAs before this chunk's epilogue
-            if (ci + 1 < c_last) {
-                good &= mbar_wait_bounded(&bar[st ^ 1], (uint32_t)(((it + 1) >> 1) & 1), kTcWaitLimit);
-                if (good) mma1(sm + (st ^ 1) * kTcStageBytes);
+        if (tid == 0 && ci + 1 < c_last) {
+            // the next chunk's first MMAs run under this chunk's epilogue
+            good &= mbar_wait_bounded(&bar[0], pa, kTcWaitLimit);
+            if (good) {
+                a_pending = false;
+                mma1();
+                mma1_pending = true;
             }
         }
-        // gated RMSNorm of this thread's 32 tokens: the gate logits from the U^T buffer, the
-        // BF16 results written back over them; a full chunk leaves as one TMA box
-        if (mbar_wait_bounded(&bar[4], (uint32_t)(it & 1), kTcWaitLimit)) gpar = -1;
-        else good = false;
+        if (ci + 1 < c_last) pa ^= 1u;
+        // gated RMSNorm of this thread's 32 tokens: the gate logits from the buffer, the BF16
+        // results written back over them; a full chunk leaves as one TMA box
+        const bool g_ok = mbar_wait_bounded(&bar[4], pg, kTcWaitLimit);
+        pg ^= 1u;
+        good &= g_ok;
+        if (tid == 0 && g_ok) g_pending = false;
         {
-            // lane t forms the RMS factor of token r0 + t once; the loop takes it by shuffle
             const float4 pl = reinterpret_cast<const float4 *>(red)[r0 + lane];
             const float rinv_l = rsqrt_ftz(((pl.x + pl.y) + (pl.z + pl.w)) * (1.0f / kD) + rms_eps);
             __nv_bfloat16 y[32];
@@ -1411,7 +1474,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 const float sg = fmaf(0.5f, tanh_approx(0.5f * gv), 0.5f);
                 y[r] = __float2bfloat16_rn(sg * nw * (o[r] * rinv));
             }
-            if (e.n == kC) {
+            if (e.n == kC) {  // each thread overwrites only the gate values it has read
 #pragma unroll
                 for (int r = 0; r < 32; ++r) sGY[(r0 + r) * kD + vi] = y[r];
                 tc::fence_smem_to_async();
@@ -1430,26 +1493,15 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         }
     }
 
-    if (aborted) {
+    if (__syncthreads_or(aborted || !good)) {
         if (tid == 0) {
             atomicExch(err, KDA_ERR_TIMEOUT);
-            // let this CTA's outstanding copies and MMAs land before its memory goes away: this
-            // chunk's copy if its wait gave up, the next chunk's, and chunk it + 2's if requested
-            // (each chunk's copy completes on two barriers: W|QG and the rest)
-            if (!stage_ok) mbar_wait_bounded(&bar[5 + (it & 1)], (uint32_t)((it >> 1) & 1), kTcWaitLimit);
-            if (c_first + it + 1 < c_last) {
-                const uint32_t p1 = (uint32_t)(((it + 1) >> 1) & 1);
-                mbar_wait_bounded(&bar[(it + 1) & 1], p1, kTcWaitLimit);
-                mbar_wait_bounded(&bar[5 + ((it + 1) & 1)], p1, kTcWaitLimit);
-            }
-            if (issued2) {
-                const uint32_t p2 = (uint32_t)(((it + 2) >> 1) & 1);
-                mbar_wait_bounded(&bar[it & 1], p2, kTcWaitLimit);
-                mbar_wait_bounded(&bar[5 + (it & 1)], p2, kTcWaitLimit);
-            }
-            if (gpar >= 0) mbar_wait_bounded(&bar[4], (uint32_t)gpar, kTcWaitLimit);
-            mbar_wait_bounded(&bar[2], ph1, kTcWaitLimit);
-            mbar_wait_bounded(&bar[3], ph2, kTcWaitLimit);
+            // let this CTA's outstanding copies and MMAs land before its memory goes away
+            if (a_pending) mbar_wait_bounded(&bar[0], pa, kTcWaitLimit);
+            if (b_pending) mbar_wait_bounded(&bar[1], pb, kTcWaitLimit);
+            if (g_pending) mbar_wait_bounded(&bar[4], pg, kTcWaitLimit);
+            if (mma1_pending) mbar_wait_bounded(&bar[2], p1, kTcWaitLimit);
+            if (mma2_pending) mbar_wait_bounded(&bar[3], p2, kTcWaitLimit);
         }
     } else {
         // final state back to HBM: S[k][v] from D3 row v, columns of this thread's half
