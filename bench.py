@@ -566,6 +566,98 @@ def _time_gate_proj(K, args, gen, dev, stream, reps=20):
                                 "peak_note": src}}
 
 
+KDA_LAYERS = 69  # KDA layers of the Kimi K3 stack (the header comment's architecture block)
+
+
+def _time_layer_stack(K, args, cfg, gen, dev, stream, reps=5):
+    """Whole KDA layers at decode B=256 (hidden 7168, 96 heads x 128): per layer one product
+    with the stacked W_q/W_k/W_v/W_g, the gate/beta projections, the mixer and W_o with the
+    residual, all on the library's kernels with synthetic random-init weights. Times one layer
+    (per-stage CUDA events, so the mixer's share is known) and the 69-layer stack (as many
+    layers as device memory holds, stated). Weights and states (0.9 GB + 1.7 GB per layer) are
+    far larger than L2."""
+    import torch
+
+    from linear_attention_mixer_gb300.layer import KdaLayerRunner, random_layer_weights
+    Bd = args.batch
+    runner = KdaLayerRunner(cfg, HIDDEN, Bd, dev)
+    slots = torch.arange(Bd, dtype=torch.int32, device=dev)
+    per_layer = (4 * D * HIDDEN + DH * HIDDEN + D * DH + H * HIDDEN + HIDDEN * D) * 2 + \
+        Bd * (H * DH * DH * 4 + 3 * (KCONV - 1) * D * 2)
+    free, _ = torch.cuda.mem_get_info(dev)
+    n_layers = int(max(1, min(KDA_LAYERS, (free - (8 << 30)) // per_layer)))
+    layers, states = [], []
+    try:
+        for _ in range(n_layers):
+            layers.append(random_layer_weights(H, DH, HIDDEN, gen, dev))
+            states.append(K.kda_state_alloc(cfg, Bd))
+        x0 = torch.randn(Bd, HIDDEN, generator=gen, device=dev).to(torch.bfloat16)
+        bufs = [torch.empty_like(x0), torch.empty_like(x0)]
+
+        def stack_step():
+            x = x0
+            for li in range(n_layers):
+                y = bufs[li & 1]
+                runner.decode(layers[li], states[li], slots, x, y, stream)
+                x = y
+
+        # one layer, stage by stage
+        lw, st = layers[0], states[0]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        stage = {"qkvg_proj": [], "gate_proj": [], "mixer": [], "out_proj": [], "layer": []}
+        D4 = runner.qkvg.view(4, Bd, D)
+        for rep in range(reps + 2):
+            ev[0].record(stream)
+            K.kda_linear(x0, lw.w_qkvg, D4, runner.ws_lin, ysplit=D, stream=stream)
+            ev[1].record(stream)
+            K.kda_gate_proj(cfg, x0, lw.w_fa, lw.w_fb, lw.w_b, runner.z, runner.b, runner.ws_gp, stream)
+            ev[2].record(stream)
+            K.kda_decode_token(cfg, lw.params, st, slots, D4[0], D4[1], D4[2], runner.z, runner.b, D4[3],
+                               runner.o, stream)
+            ev[3].record(stream)
+            K.kda_linear(runner.o, lw.w_o, bufs[0], runner.ws_lin, r=x0, stream=stream)
+            ev[4].record(stream)
+            torch.cuda.synchronize()
+            if rep >= 2:
+                for key, a, b in (("qkvg_proj", 0, 1), ("gate_proj", 1, 2), ("mixer", 2, 3), ("out_proj", 3, 4),
+                                  ("layer", 0, 4)):
+                    stage[key].append(ev[a].elapsed_time(ev[b]))
+        med = {k: statistics.median(v) for k, v in stage.items()}
+        # the stack
+        stack_step()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(reps):
+            stack_step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        stack_ms = t0.elapsed_time(t1) / reps
+        for st_ in states:
+            assert K.kda_state_poll_error(st_) == 0
+    finally:
+        for st_ in states:
+            K.kda_state_free(st_)
+        del layers
+        torch.cuda.empty_cache()
+    peaks = _peaks()
+    w_qkvg, w_o = 4 * D * HIDDEN * 2, HIDDEN * D * 2
+    gbs = lambda nbytes, ms: nbytes / (ms / 1e3) / 1e9
+    return {"workload": f"KDA layer decode, B={Bd} sequences, hidden {HIDDEN}, 96 heads x 128, BF16 I/O, FP32 state: "
+                        "stacked W_q/W_k/W_v/W_g product, gate/beta projections, mixer, W_o with the residual "
+                        "(synthetic random-init weights)",
+            "layer_ms": med["layer"], "layer_tokens_per_s": Bd / (med["layer"] / 1e3),
+            "stage_ms": {k: med[k] for k in ("qkvg_proj", "gate_proj", "mixer", "out_proj")},
+            "mixer_share": med["mixer"] / med["layer"],
+            "qkvg_proj_gbs": gbs(w_qkvg + Bd * HIDDEN * 2 + 4 * Bd * D * 2, med["qkvg_proj"]),
+            "out_proj_gbs": gbs(w_o + Bd * D * 2 + 2 * Bd * HIDDEN * 2, med["out_proj"]),
+            "hbm_peak_gbs": peaks["hbm_gbs"],
+            "stack_layers": n_layers, "stack_ms": stack_ms, "stack_tokens_per_s": Bd / (stack_ms / 1e3),
+            "stack_note": f"{n_layers} of the model's {KDA_LAYERS} KDA layers chained (each layer's output is the "
+                          "next one's input), one decode token for all sequences per step, mean of "
+                          f"{reps} steps"}
+
+
 def _time_varlen(K, args, cfg, params, gen, dev, stream):
     """Varlen workload: 16 sequences ~U[512, 16384] (seeded lengths), prefill all, snapshot /
     reset / restore sequences 0-7, then 128 batched decode steps; tokens/s of both phases."""
@@ -770,6 +862,11 @@ def run_kda(args):
             line["value"] = line["gate_proj"]["value"]
             line["ms_per_step"] = line["gate_proj"]["ms"]
             line["gpu_launches"] = 2 * line["gate_proj"]["reps"]
+    if args.only in ("all", "layer"):
+        line["layer"] = _time_layer_stack(K, args, cfg, gen, dev, stream)
+        if args.only == "layer":
+            line["value"] = line["layer"]["stack_tokens_per_s"]
+            line["ms_per_step"] = line["layer"]["stack_ms"]
     if args.only == "all":
         line["varlen"] = _time_varlen(K, args, cfg, params, gen, dev, stream)
         line["photo"] = _time_photo(K, cfg, params, gen, dev, stream,
@@ -813,7 +910,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
     ap.add_argument("--prefill-reps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "decode_multi", "prefill", "gate_proj"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "decode_multi", "prefill", "gate_proj", "layer"], default="all",
                     help="time one part only (small profiling runs); the JSON line keeps its keys")
     ap.add_argument("--batch", type=int, default=B_DEC, help="decode batch (profiling runs)")
     ap.add_argument("--prefill-tokens", type=int, default=T_PRE, help="prefill length (profiling runs)")

@@ -302,6 +302,39 @@ kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int64_t T, con
                          size_t workspace_bytes, void *stream);
 
 /*
+ * The dense projections around the mixer: y = x W^T (+ r) in BF16 with FP32
+ * accumulation on the tensor cores. A KDA layer takes q, k, v and the output-gate
+ * logits g from W_q, W_k, W_v, W_g applied to the hidden state x, and applies W_o to
+ * the mixer's gated output (kimi_k3.c header comment, block "KDA per-head
+ * recurrence": q,k,v = SiLU(ShortConv4(W{q,k,v} x)), out = W_o [sigmoid(W_g x) *
+ * RMSNorm_head(o)]; struct Kda: W q, k, v, o, g). They carry no KDA arithmetic; the
+ * library provides them so that a whole layer runs on its own kernels.
+ *   M, N, K    rows of x and y, rows of W (output columns), columns of x and W;
+ *              N a multiple of 128, K a multiple of 64, M >= 0 (0 is a no-op)
+ *   x          device BF16 [M][K]
+ *   w          device BF16 [N][K]
+ *   r          device BF16 [M][N] added to the product before rounding, or NULL;
+ *              only with ysplit == 0 or ysplit == N
+ *   y          device BF16, out. ysplit == 0 (or N): [M][N]. Otherwise the columns
+ *              are split into N / ysplit consecutive matrices [M][ysplit] (column
+ *              n goes to matrix n / ysplit), e.g. q, k, v and g from one product
+ *              with the four weight matrices stacked; ysplit a multiple of 128
+ *              that divides N
+ *   workspace  device scratch of at least kda_linear_workspace_bytes(M, N, K)
+ *              bytes (query with the call's device current), 16-byte aligned; its
+ *              first int32 is an error word the call clears and a kernel sets to
+ *              KDA_ERR_TIMEOUT if a bounded wait gave up. Calls sharing a
+ *              workspace must be ordered.
+ * All pointers 16-byte aligned. When the tile grid is too small to fill the GPU the
+ * K dimension is split; the partial sums are added in split order, so results do
+ * not depend on timing. Errors: KDA_ERR_INVALID (shape, alignment, NULL pointer,
+ * workspace too small), KDA_ERR_CUDA.
+ */
+size_t kda_linear_workspace_bytes(int32_t M, int32_t N, int32_t K);
+kda_status kda_linear(int32_t M, int32_t N, int32_t K, const void *x, const void *w, const void *r, void *y,
+                      int32_t ysplit, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Recurrent-state photos (kimi_k3.c header, the COLI_K3_CKPT and
  * COLI_K3_CKPT_DIR serve options). A store keeps up to `capacity` photos of
  * one sequence slot across a stack of KDA layers (one kda_state per layer),

@@ -81,6 +81,8 @@ SIGNATURES = [
     ("kda_gate_proj_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(kda_config_t), _I32, ctypes.c_int64]),
     ("kda_gate_proj", _I32, [ctypes.POINTER(kda_config_t), _I32, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP,
                              _VP, ctypes.c_size_t, _VP]),
+    ("kda_linear_workspace_bytes", ctypes.c_size_t, [_I32, _I32, _I32]),
+    ("kda_linear", _I32, [_I32, _I32, _I32, _VP, _VP, _VP, _VP, _I32, _VP, ctypes.c_size_t, _VP]),
     ("kda_photo_store_create", _I32, [_I32, ctypes.c_char_p, ctypes.POINTER(_VP)]),
     ("kda_photo_store_free", _I32, [_VP]),
     ("kda_photo_count", _I32, [_VP]),
@@ -306,6 +308,27 @@ def kda_gate_proj(cfg: kda_config_t, x, w_fa, w_fb, w_b, z, b, workspace: torch.
     _check(lib().kda_gate_proj(ctypes.byref(cfg), hidden, T, _dev(x, bf, "x"), _dev(w_fa, bf, "w_fa"),
                                _dev(w_fb, bf, "w_fb"), _dev(w_b, bf, "w_b"), _dev(z, bf, "z"), _dev(b, bf, "b"),
                                ws, workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kda_linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().kda_linear_workspace_bytes(int(M), int(N), int(K)))
+
+
+def kda_linear(x, w, y, workspace: torch.Tensor, r=None, ysplit: int = 0, stream=None) -> None:
+    """y = x w^T (+ r), BF16: x [M, K], w [N, K], y [M, N] (or [N / ysplit, M, ysplit] with ysplit)."""
+    bf = torch.bfloat16
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError("x must be [M, K] and w [N, K]")
+    M, K = int(x.shape[0]), int(x.shape[1])
+    N = int(w.shape[0])
+    if y.numel() != M * N:
+        raise ValueError(f"y must hold {M} x {N} elements, got {tuple(y.shape)}")
+    if r is not None and r.numel() != M * N:
+        raise ValueError(f"r must hold {M} x {N} elements, got {tuple(r.shape)}")
+    _check(lib().kda_linear(M, N, K, _dev(x, bf, "x"), _dev(w, bf, "w"),
+                            _VP(None) if r is None else _dev(r, bf, "r"), _dev(y, bf, "y"), int(ysplit),
+                            _dev(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+                            _stream(stream)))
 
 
 def _layers(layers):
