@@ -64,7 +64,7 @@ static_assert(kStageBBytes == 49152 && kOffUp + kC * kD * 4 == kTcChunkBytes, "c
 // state_tc_kernel shared memory: S^T hi | S^T lo | U^T hi | U^T lo | stage A | stage B | g/out rows | sums | barriers
 constexpr int kSmST = 0, kSmUT = 65536, kSmA = 98304, kSmB = kSmA + kStageABytes, kSmGY = kSmB + kStageBBytes;
 constexpr int kSmRed = kSmGY + kC * kD * 2, kSmBar = kSmRed + 4 * kC * 4;
-constexpr int kStateTcSmem = kSmBar + 8 * 8 + 16;
+constexpr int kStateTcSmem = kSmBar + 12 * 8 + 16;
 static_assert(kSmB % 128 == 0 && kSmGY % 128 == 0, "TMA and bulk destinations");
 static_assert(kStateTcSmem <= 232448, "state_tc_kernel shared memory");
 constexpr uint32_t kTcWaitLimit = 1u << 26;
@@ -1165,25 +1165,45 @@ state_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__res
 }
 
 // ---------------------------------------------------------------- state pass on tensor cores
-// One CTA (256 threads) per (sequence, head). TMEM lane v holds value index v:
+// One CTA per (sequence, head), warp-specialised, 416 threads. TMEM lane v holds value index v:
 //   D1 = S^T W^T     [v][r]  TMEM columns   0.. 63
 //   D2 = S^T QG^T    [v][r]  TMEM columns  64..127, then += U^T P^T  -> O^T
-//   D3 = S^T         [v][k]  TMEM columns 128..255, the FP32 state, scaled by gamma and += U^T KD
-// Warps w and w + 4 share lane quarter w % 4 and split the columns in halves (grp = w / 4).
+//   D3 = S^T         [v][k]  TMEM columns 128..255, the FP32 state (scaled by the chunk's decay
+//                            before MMA2, += U^T KD)
 // S^T and U^T are kept in shared memory as BF16 high and low parts (A operands), and each
 // product that carries the state is formed as hi*hi + lo*hi + hi*lo:
 //   MMA1: [D1 | D2] = S_hi^T [W_hi | QG]^T, D1 += S_lo^T W_hi^T + S_hi^T W_lo^T
 //   MMA2: [D2 | D3] += U_hi^T [P_hi | KDT_hi] + U_lo^T [P_hi | KDT_hi] + U_hi^T [P_lo | KDT_lo]
-// Per chunk c:
-//   [MMA1(c) in flight] scale D3 by gamma; U'(c) loaded to registers | U^T = U' - D1 -> hi/lo |
-//   MMA2(c); stage A of c + 1 requested | S^T hi/lo refreshed from D3, O^T read, sums of
-//   squares; stage B of c + 1 and the gate rows of c requested | MMA1(c + 1) issued |
-//   gated RMSNorm of c written out (over MMA1(c + 1)).
-// Chunk blocks arrive by bulk copy into one stage A and one stage B buffer; each is refilled as
-// soon as the MMA that reads it has completed, and block c + 2 is prefetched into L2. Every wait
-// is bounded; on expiry the error word gets KDA_ERR_TIMEOUT and the CTA drains what it issued.
+// Roles (each hand-off is an mbarrier; every wait is bounded):
+//   warps 0-7  (state): per chunk, U^T = U' - D1 -> hi/lo (after MMA1), then after MMA2 the
+//              S^T operand refresh from D3 and the next chunk's decay put on D3. Warps w and
+//              w + 4 share lane quarter w % 4 and split the columns in halves.
+//   warp 8     (issuer, one lane): MMA1 once S^T is ready and D2 has been read out, MMA2 once
+//              U^T is ready; the chunk-block copies (stage A after MMA1, stage B after MMA2),
+//              the gate-row boxes and the L2 prefetches.
+//   warps 9-12 (epilogue): O^T from D2 right after MMA2 (so MMA1 of the next chunk may start),
+//              then the gated RMSNorm and the output box, under the next chunk's products.
+// The serial chain per chunk is MMA1 -> U -> MMA2 -> refresh; the epilogue and the copies
+// run beside it.
+constexpr int kStThreads = 416;
+
+// AND of pred over the `count` threads of named barrier `id` (also a barrier), so that every
+// thread of a group takes the same branch after a bounded wait.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
 template <typename T>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kStThreads, 1)
 state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__restrict__ err,
                 const int32_t *__restrict__ slots, int H, int max_slots,
                 const ChunkEntry *__restrict__ table, const int32_t *__restrict__ seq_first,
@@ -1203,14 +1223,14 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     // [64 tokens][4 value quarters] partial sums of squares, added in a fixed order (so that the
     // outputs do not depend on the order the warps finish in)
     float *red = reinterpret_cast<float *>(sm + kSmRed);
-    // barriers: [0] stage A, [1] stage B, [2] MMA1, [3] MMA2, [4] gate rows
+    // [0] stage A landed, [1] stage B landed, [2] MMA1 done, [3] MMA2 done, [4] gate rows landed,
+    // [5] U^T ready (8 warps), [6] S^T ready (8 warps), [7] D2 read out (4 warps), [8] output box
+    // read out of the gate/output buffer (1 thread)
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kSmBar);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 8);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 12);
 
     const int h = blockIdx.x, seq = blockIdx.y;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const int qtr = w & 3, grp = w >> 2;
-    const int vi = 32 * qtr + lane;  // value index = TMEM lane of this thread
     const int slot = slots[seq];
     if (slot < 0 || slot >= max_slots) {
         if (tid == 0) atomicExch(err, kErrBadSlot);
@@ -1218,303 +1238,126 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     }
     const size_t D = (size_t)H * kD;
     const int c_first = seq_first[seq], c_last = seq_first[seq + 1];
+    const int n_chunks = c_last - c_first;
     float *Sg = S_all + ((size_t)slot * H + h) * kD * kD;
     auto block_of = [&](int ci) { return chunks + ((size_t)h * total_chunks + ci) * kTcChunkBytes; };
 
     if (w == 0) tc::tmem_alloc(tslot, 256);
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
+        mbar_init(&bar[5], 8);
+        mbar_init(&bar[6], 8);
+        mbar_init(&bar[7], 4);
+        mbar_init(&bar[8], 1);
         fence_mbar_init();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    const uint32_t lanes = (uint32_t)(32 * qtr) << 16;  // this warp's TMEM lane quarter
-    const uint32_t tD1 = tb + lanes, tD2 = tb + lanes + 64, tD3 = tb + lanes + 128;
-    const int k0 = 64 * grp;   // this thread's state columns k0 .. k0+63
-    const int r0 = 32 * grp;   // this thread's tokens r0 .. r0+31
+    bool good = true;
 
-    // thread 0 only: the two copies of a chunk block
-    auto issue_a = [&](int ci) {
-        mbar_arrive_expect_tx(&bar[0], kStageABytes);
-        bulk_g2s(sA, block_of(ci) + kOffTA, kStageABytes, &bar[0]);
-    };
-    auto issue_b = [&](int ci) {
-        mbar_arrive_expect_tx(&bar[1], kStageBBytes);
-        bulk_g2s(sB, block_of(ci) + kOffTB, kStageBBytes, &bar[1]);
-    };
-    constexpr uint32_t id64 = tc::idesc_bf16(128, 64), id128 = tc::idesc_bf16(128, 128);
-    constexpr uint32_t id192 = tc::idesc_bf16(128, 192);
-    auto mma1 = [&]() {  // thread 0 only
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            tc::mma_bf16(tb, tc::kmajor_desc(sSTh, kk, kD), tc::kmajor_desc(sA, kk, kD), id128, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            tc::mma_bf16(tb, tc::kmajor_desc(sSTl, kk, kD), tc::kmajor_desc(sA, kk, kD), id64, 1);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            tc::mma_bf16(tb, tc::kmajor_desc(sSTh, kk, kD), tc::kmajor_desc(sA + 2 * kC * kD * 2, kk, kD), id64, 1);
-        tc::mma_commit(&bar[2]);
-    };
-    auto mma2 = [&]() {  // thread 0 only
-        unsigned char *sBlo = sB + 3 * kC * kC * 2;  // rows 192.. of tile B
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16(tb + 64, tc::kmajor_desc(sUTh, kk, kC), tc::kmajor_desc(sB, kk, kC), id192, 1);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16(tb + 64, tc::kmajor_desc(sUTl, kk, kC), tc::kmajor_desc(sB, kk, kC), id192, 1);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16(tb + 64, tc::kmajor_desc(sUTh, kk, kC), tc::kmajor_desc(sBlo, kk, kC), id192, 1);
-        tc::mma_commit(&bar[3]);
-    };
-    // 16 values -> BF16 high and low parts at (row, k .. k + 15) of two K-major tiles
-    auto put16_split = [](unsigned char *th, unsigned char *tl, int row, int kc, const float *x, int Kd) {
-        uint4 hi, lo;
-        split8(x, hi, lo);
-        st16(th + tc::kmajor_off(row, kc, Kd), hi);
-        st16(tl + tc::kmajor_off(row, kc, Kd), lo);
-        split8(x + 8, hi, lo);
-        st16(th + tc::kmajor_off(row, kc + 8, Kd), hi);
-        st16(tl + tc::kmajor_off(row, kc + 8, Kd), lo);
-    };
-
-    // initial state: S[k][v] -> D3 row v (FP32) and the BF16 operand parts of row v
-    float vals[32];
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-        const int kb = k0 + 32 * half;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) vals[j] = Sg[(size_t)(kb + j) * kD + vi];
-        tc::tmem_st32(tD3 + kb, vals);
-        put16_split(sSTh, sSTl, vi, kb, vals, kD);
-        put16_split(sSTh, sSTl, vi, kb + 16, vals + 16, kD);
-    }
-    tc::tmem_wait_st();
-    tc::fence_smem_to_async();
-    if (tid == 0 && c_first < c_last) {
-        issue_a(c_first);
-        issue_b(c_first);
-        if (c_first + 1 < c_last) prefetch_l2_bulk(block_of(c_first + 1), kTcChunkBytes);
-        tma_prefetch_2d(&tm_g, h * kD, table[c_first].t0);
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    bool good = true, aborted = false;
-    // copies in flight when a wait gives up: stage A / B of the next chunk, gate rows
-    bool a_pending = false, b_pending = false, g_pending = false, mma1_pending = false, mma2_pending = false;
-    uint32_t pa = 0, pb = 0, p1 = 0, p2 = 0, pg = 0;  // phases of bars 0..4
-    if (tid == 0 && c_first < c_last) {
-        good &= mbar_wait_bounded(&bar[0], pa, kTcWaitLimit);
-        if (good) {
-            mma1();
-            mma1_pending = true;
-        }
-    }
-    pa ^= 1u;
-
-    const float nw = __ldg(norm_w + vi);
-    ChunkEntry e_next = c_first < c_last ? table[c_first] : ChunkEntry{0, 0, 0, 0};
-    for (int ci = c_first; ci < c_last; ++ci) {
-        const ChunkEntry e = e_next;  // read one chunk ahead
-        if (ci + 1 < c_last) {
-            e_next = table[ci + 1];
-            if (tid == 0) {
-                // the next chunk's gate rows and the block after next into L2: their copies are
-                // requested within this chunk and an HBM round trip would stall them
-                tma_prefetch_2d(&tm_g, h * kD, e_next.t0);
-                if (ci + 2 < c_last) prefetch_l2_bulk(block_of(ci + 2), kTcChunkBytes);
-            }
-        }
-        // U' of this thread's tokens, loaded while MMA1 runs (a warp reads 128 contiguous bytes
-        // per token)
-        float up[32];
-        {
-            const float *Up = reinterpret_cast<const float *>(block_of(ci) + kOffUp) + vi;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) up[j] = __ldcs(Up + (size_t)(r0 + j) * kD);
-        }
-        // D3 = Diag(gamma) on this thread's columns (stage A has landed: MMA1 reads it)
-        {
-            const bool landed = mbar_wait_bounded(&bar[0], pa ^ 1u, kTcWaitLimit);
-            good &= landed;
-            uint32_t raw[32];
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                tc::tmem_ld32_nowait(tD3 + k0 + 32 * half, raw);
-                tc::tmem_wait_ld();
-                const float *gam = sgam + k0 + 32 * half;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]) * gam[j];
-                tc::tmem_st32(tD3 + k0 + 32 * half, vals);
-            }
-            tc::tmem_wait_st();
-        }
-        {
-            const bool ok = mbar_wait_bounded(&bar[2], p1, kTcWaitLimit);
-            good &= ok;
-            if (tid == 0 && ok) mma1_pending = false;
-        }
-        p1 ^= 1u;
-        tc::fence_after_sync();
-        // U^T = U'^T - (W S)^T on this thread's tokens, as BF16 high and low parts
-        {
-            uint32_t raw[32];
-            tc::tmem_ld32_nowait(tD1 + r0, raw);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) vals[j] = up[j] - __uint_as_float(raw[j]);
-            put16_split(sUTh, sUTl, vi, r0, vals, kC);
-            put16_split(sUTh, sUTl, vi, r0 + 16, vals + 16, kC);
-        }
-        tc::fence_smem_to_async();
-        tc::fence_before_sync();
-        if (__syncthreads_or(!good)) { aborted = true; break; }
-        tc::fence_after_sync();
-        if (tid == 0) {
-            // MMA1 has read stage A and every thread has read gamma: refill it with the next chunk
-            if (ci + 1 < c_last) {
-                issue_a(ci + 1);
-                a_pending = true;
-            }
-            good &= mbar_wait_bounded(&bar[1], pb, kTcWaitLimit);
-            if (good) {
-                mma2();
-                mma2_pending = true;
-            }
-        }
-        pb ^= 1u;
-        good &= mbar_wait_bounded(&bar[3], p2, kTcWaitLimit);
-        p2 ^= 1u;
-        tc::fence_after_sync();
-        if (tid == 0 && good) {
-            mma2_pending = false;
-            if (ci + 1 < c_last) {
-                issue_b(ci + 1);
-                b_pending = true;
-            }
-            // this chunk's gate rows into the gate/output buffer once the previous output box
-            // has been read out of it
-            bulk_wait_read_all();
-            mbar_arrive_expect_tx(&bar[4], (uint32_t)(box_rows * kD * sizeof(T)));
-            tma_load_2d(sGY, &tm_g, h * kD, e.t0, &bar[4]);
-            g_pending = true;
-        }
-        // refresh the S^T operand parts from the updated FP32 state
-        {
-            uint32_t raw[32];
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                tc::tmem_ld32_nowait(tD3 + k0 + 32 * half, raw);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
-                put16_split(sSTh, sSTl, vi, k0 + 32 * half, vals, kD);
-                put16_split(sSTh, sSTl, vi, k0 + 32 * half + 16, vals + 16, kD);
-            }
-        }
-        // O^T on this thread's tokens and their sums of squares over this warp's 32 v: a
-        // reduce-scatter butterfly (31 shuffles) leaves the sum of token r0 + lane in lane `lane`
-        float o[32];
-        {
-            uint32_t raw[32];
-            tc::tmem_ld32_nowait(tD2 + r0, raw);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(raw[j]);
-            float sq[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sq[j] = o[j] * o[j];
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                const bool upper = (lane & off) != 0;
-#pragma unroll
-                for (int j = 0; j < off; ++j) {
-                    const float keep = upper ? sq[j + off] : sq[j];
-                    const float send = upper ? sq[j] : sq[j + off];
-                    sq[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                }
-            }
-            red[(r0 + lane) * 4 + qtr] = sq[0];
-        }
-        tc::fence_smem_to_async();
-        tc::fence_before_sync();
-        if (__syncthreads_or(!good)) { aborted = true; break; }
-        tc::fence_after_sync();
-        if (tid == 0 && ci + 1 < c_last) {
-            // the next chunk's first MMAs run under this chunk's epilogue
-            good &= mbar_wait_bounded(&bar[0], pa, kTcWaitLimit);
-            if (good) {
-                a_pending = false;
-                mma1();
-                mma1_pending = true;
-            }
-        }
-        if (ci + 1 < c_last) pa ^= 1u;
-        // gated RMSNorm of this thread's 32 tokens: the gate logits from the buffer, the BF16
-        // results written back over them; a full chunk leaves as one TMA box
-        const bool g_ok = mbar_wait_bounded(&bar[4], pg, kTcWaitLimit);
-        pg ^= 1u;
-        good &= g_ok;
-        if (tid == 0 && g_ok) g_pending = false;
-        {
-            const float4 pl = reinterpret_cast<const float4 *>(red)[r0 + lane];
-            const float rinv_l = rsqrt_ftz(((pl.x + pl.y) + (pl.z + pl.w)) * (1.0f / kD) + rms_eps);
-            __nv_bfloat16 y[32];
-#pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                const float rinv = __shfl_sync(0xFFFFFFFFu, rinv_l, r);
-                const float gv = __bfloat162float(sGY[(r0 + r) * kD + vi]);
-                // sigmoid(g) = (1 + tanh(g/2)) / 2; the hardware tanh's error is below the BF16
-                // rounding of the output it multiplies
-                const float sg = fmaf(0.5f, tanh_approx(0.5f * gv), 0.5f);
-                y[r] = __float2bfloat16_rn(sg * nw * (o[r] * rinv));
-            }
-            if (e.n == kC) {  // each thread overwrites only the gate values it has read
-#pragma unroll
-                for (int r = 0; r < 32; ++r) sGY[(r0 + r) * kD + vi] = y[r];
-                tc::fence_smem_to_async();
-                __syncthreads();
-                if (tid == 0) {
-                    tma_store_2d(&tm_out, h * kD, e.t0, sGY);
-                    bulk_commit_group();
-                }
-            } else {
-                T *obase = out + (size_t)(e.t0 + r0) * D + (size_t)h * kD + vi;
-                const int nv = e.n - r0;  // rows of this thread's half that exist
-#pragma unroll
-                for (int r = 0; r < 32; ++r)
-                    if (r < nv) obase[(size_t)r * D] = y[r];
-            }
-        }
-    }
-
-    if (__syncthreads_or(aborted || !good)) {
-        if (tid == 0) {
-            atomicExch(err, KDA_ERR_TIMEOUT);
-            // let this CTA's outstanding copies and MMAs land before its memory goes away
-            if (a_pending) mbar_wait_bounded(&bar[0], pa, kTcWaitLimit);
-            if (b_pending) mbar_wait_bounded(&bar[1], pb, kTcWaitLimit);
-            if (g_pending) mbar_wait_bounded(&bar[4], pg, kTcWaitLimit);
-            if (mma1_pending) mbar_wait_bounded(&bar[2], p1, kTcWaitLimit);
-            if (mma2_pending) mbar_wait_bounded(&bar[3], p2, kTcWaitLimit);
-        }
-    } else {
-        // final state back to HBM: S[k][v] from D3 row v, columns of this thread's half
-        uint32_t raw[32];
+    if (w < 8) {
+        // ------------------------------------------------------------ state warps
+        const int qtr = w & 3, grp = w >> 2;
+        const int vi = 32 * qtr + lane;
+        const uint32_t lanes = (uint32_t)(32 * qtr) << 16;
+        const uint32_t tD1 = tb + lanes, tD3 = tb + lanes + 128;
+        const int k0 = 64 * grp, r0 = 32 * grp;
+        auto put16_split = [](unsigned char *th, unsigned char *tl, int row, int kc, const float *x, int Kd) {
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            st16(th + tc::kmajor_off(row, kc, Kd), hi);
+            st16(tl + tc::kmajor_off(row, kc, Kd), lo);
+            split8(x + 8, hi, lo);
+            st16(th + tc::kmajor_off(row, kc + 8, Kd), hi);
+            st16(tl + tc::kmajor_off(row, kc + 8, Kd), lo);
+        };
+        float vals[32];
+        // initial state: S[k][v] -> D3 row v (FP32) and the BF16 operand parts of row v
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
-            tc::tmem_ld32_nowait(tD3 + k0 + 32 * half, raw);
-            tc::tmem_wait_ld();
+            const int kb = k0 + 32 * half;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) Sg[(size_t)(k0 + 32 * half + j) * kD + vi] = __uint_as_float(raw[j]);
+            for (int j = 0; j < 32; ++j) vals[j] = Sg[(size_t)(kb + j) * kD + vi];
+            put16_split(sSTh, sSTl, vi, kb, vals, kD);
+            put16_split(sSTh, sSTl, vi, kb + 16, vals + 16, kD);
+            if (n_chunks > 0) {  // the first chunk's decay (stage A brings its gamma)
+                if (half == 0) good &= mbar_wait_bounded(&bar[0], 0, kTcWaitLimit);
+                const float *gam = sgam + kb;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) vals[j] *= gam[j];
+            }
+            tc::tmem_st32(tD3 + kb, vals);
         }
+        tc::tmem_wait_st();
+        tc::fence_smem_to_async();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[6]);  // S^T of the first chunk is ready
+        for (int it = 0; it < n_chunks && good; ++it) {
+            const int ci = c_first + it;
+            const uint32_t par = (uint32_t)(it & 1);
+            // U' of this thread's tokens (a warp reads 128 contiguous bytes per token)
+            float up[32];
+            {
+                const float *Up = reinterpret_cast<const float *>(block_of(ci) + kOffUp) + vi;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) up[j] = __ldcs(Up + (size_t)(r0 + j) * kD);
+            }
+            if (!(good = mbar_wait_bounded(&bar[2], par, kTcWaitLimit))) break;
+            tc::fence_after_sync();
+            {   // U^T = U'^T - (W S)^T on this thread's tokens, as BF16 high and low parts
+                uint32_t raw[32];
+                tc::tmem_ld32_nowait(tD1 + r0, raw);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) vals[j] = up[j] - __uint_as_float(raw[j]);
+                put16_split(sUTh, sUTl, vi, r0, vals, kC);
+                put16_split(sUTh, sUTl, vi, r0 + 16, vals + 16, kC);
+            }
+            tc::fence_smem_to_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[5]);
+            if (!(good = mbar_wait_bounded(&bar[3], par, kTcWaitLimit))) break;
+            tc::fence_after_sync();
+            // refresh the S^T operand parts from the updated FP32 state and put the next chunk's
+            // decay on D3 (its gamma arrives with stage A of the next chunk)
+            const bool has_next = it + 1 < n_chunks;
+            if (has_next && !(good = mbar_wait_bounded(&bar[0], (uint32_t)((it + 1) & 1), kTcWaitLimit))) break;
+            {
+                uint32_t raw[32];
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    tc::tmem_ld32_nowait(tD3 + k0 + 32 * half, raw);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
+                    if (has_next) {
+                        put16_split(sSTh, sSTl, vi, k0 + 32 * half, vals, kD);
+                        put16_split(sSTh, sSTl, vi, k0 + 32 * half + 16, vals + 16, kD);
+                        const float *gam = sgam + k0 + 32 * half;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) vals[j] *= gam[j];
+                        tc::tmem_st32(tD3 + k0 + 32 * half, vals);
+                    } else {  // the final state back to HBM: S[k][v] from D3 row v
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) Sg[(size_t)(k0 + 32 * half + j) * kD + vi] = vals[j];
+                    }
+                }
+                tc::tmem_wait_st();
+            }
+            if (has_next) {
+                tc::fence_smem_to_async();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[6]);
+            }
+        }
+        if (!good) atomicExch(err, KDA_ERR_TIMEOUT);
         // new conv history (the last K-1 raw inputs of the sequence)
-        if (c_last > c_first && tid < kD) {
+        if (good && n_chunks > 0 && tid < kD) {
             const int start = table[c_first].t0;
             const int len = table[c_last - 1].t0 + table[c_last - 1].n - start;
             T *tl = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD + tid;
@@ -1530,8 +1373,187 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 }
             }
         }
+    } else if (w == 8) {
+        // ------------------------------------------------------------ issuer
+        if (lane == 0 && n_chunks > 0) {
+            auto issue_a = [&](int ci) {
+                mbar_arrive_expect_tx(&bar[0], kStageABytes);
+                bulk_g2s(sA, block_of(ci) + kOffTA, kStageABytes, &bar[0]);
+            };
+            auto issue_b = [&](int ci) {
+                mbar_arrive_expect_tx(&bar[1], kStageBBytes);
+                bulk_g2s(sB, block_of(ci) + kOffTB, kStageBBytes, &bar[1]);
+            };
+            auto prefetch_block = [&](int ci) {  // into L2 ahead of its copies, 16 KB per request
+                const unsigned char *src = block_of(ci);
+                for (int off = 0; off < kTcChunkBytes; off += 16384)
+                    prefetch_l2_bulk(src + off, (uint32_t)min(16384, kTcChunkBytes - off));
+            };
+            constexpr uint32_t id64 = tc::idesc_bf16(128, 64), id128 = tc::idesc_bf16(128, 128);
+            constexpr uint32_t id192 = tc::idesc_bf16(128, 192);
+            const uint64_t dSh = tc::kmajor_desc(sSTh, 0, kD), dSl = tc::kmajor_desc(sSTl, 0, kD);
+            const uint64_t dA = tc::kmajor_desc(sA, 0, kD), dAlo = tc::kmajor_desc(sA + 2 * kC * kD * 2, 0, kD);
+            const uint64_t dUh = tc::kmajor_desc(sUTh, 0, kC), dUl = tc::kmajor_desc(sUTl, 0, kC);
+            const uint64_t dB = tc::kmajor_desc(sB, 0, kC), dBlo = tc::kmajor_desc(sB + 3 * kC * kC * 2, 0, kC);
+            issue_a(c_first);
+            issue_b(c_first);
+            if (n_chunks > 1) prefetch_block(c_first + 1);
+            if (n_chunks > 2) prefetch_block(c_first + 2);
+            tma_prefetch_2d(&tm_g, h * kD, table[c_first].t0);
+            // copies and products in flight when a wait gives up
+            int a_out = 1, b_out = 1, g_out = 0, m1_out = 0, m2_out = 0;
+            for (int it = 0; it < n_chunks && good; ++it) {
+                const int ci = c_first + it;
+                const uint32_t par = (uint32_t)(it & 1);
+                if (it + 1 < n_chunks) tma_prefetch_2d(&tm_g, h * kD, table[ci + 1].t0);
+                if (it + 2 < n_chunks) prefetch_block(ci + 2);
+                // MMA1: S^T ready, D2 read out by the epilogue of the previous chunk, stage A landed
+                good = mbar_wait_bounded(&bar[6], par, kTcWaitLimit) && mbar_wait_bounded(&bar[7], par, kTcWaitLimit) &&
+                       mbar_wait_bounded(&bar[0], par, kTcWaitLimit);
+                if (!good) break;
+                a_out = 0;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tb, dSh + 16u * kk, dA + 16u * kk, id128, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tb, dSl + 16u * kk, dA + 16u * kk, id64, 1);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tb, dSh + 16u * kk, dAlo + 16u * kk, id64, 1);
+                tc::mma_commit(&bar[2]);
+                m1_out = 1;
+                if (!(good = mbar_wait_bounded(&bar[2], par, kTcWaitLimit))) break;
+                m1_out = 0;
+                // stage A is free (MMA1 read its tiles; its gamma was used by the previous refresh)
+                if (it + 1 < n_chunks) {
+                    issue_a(ci + 1);
+                    a_out = 1;
+                }
+                // MMA2: U^T ready, stage B landed
+                good = mbar_wait_bounded(&bar[5], par, kTcWaitLimit) && mbar_wait_bounded(&bar[1], par, kTcWaitLimit);
+                if (!good) break;
+                b_out = 0;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tb + 64, dUh + 16u * kk, dB + 16u * kk, id192, 1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tb + 64, dUl + 16u * kk, dB + 16u * kk, id192, 1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tb + 64, dUh + 16u * kk, dBlo + 16u * kk, id192, 1);
+                tc::mma_commit(&bar[3]);
+                m2_out = 1;
+                if (!(good = mbar_wait_bounded(&bar[3], par, kTcWaitLimit))) break;
+                m2_out = 0;
+                if (it + 1 < n_chunks) {
+                    issue_b(ci + 1);
+                    b_out = 1;
+                }
+                // this chunk's gate rows, once the previous output box has left the buffer
+                if (!(good = mbar_wait_bounded(&bar[8], par, kTcWaitLimit))) break;
+                mbar_arrive_expect_tx(&bar[4], (uint32_t)(box_rows * kD * sizeof(T)));
+                tma_load_2d(sGY, &tm_g, h * kD, table[ci].t0, &bar[4]);
+                g_out = 1;
+            }
+            if (!good) {
+                atomicExch(err, KDA_ERR_TIMEOUT);
+                // let what this CTA issued land before its memory goes away (bounded; the phases
+                // of a copy that never completed are not waited on twice)
+                if (a_out) mbar_wait_bounded(&bar[0], 0, kTcWaitLimit);
+                if (b_out) mbar_wait_bounded(&bar[1], 0, kTcWaitLimit);
+                if (m1_out) mbar_wait_bounded(&bar[2], 0, kTcWaitLimit);
+                if (m2_out) mbar_wait_bounded(&bar[3], 0, kTcWaitLimit);
+                (void)g_out;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue warps
+        const int qe = w & 3;                     // TMEM lane quarter of this warp
+        const int vi = 32 * qe + lane;            // value index
+        const int et = tid - 9 * 32;              // 0 .. 127 within the epilogue group
+        const uint32_t tD2 = tb + ((uint32_t)(32 * qe) << 16) + 64;
+        const float nw = __ldg(norm_w + vi);
+        if (et == 0) mbar_arrive(&bar[8]);        // the gate/output buffer starts free
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[7]);      // D2 may be written by the first MMA1
+        for (int it = 0; it < n_chunks; ++it) {
+            const int ci = c_first + it;
+            const uint32_t par = (uint32_t)(it & 1);
+            const ChunkEntry e = table[ci];
+            if (!bar_and(2, 128, mbar_wait_bounded(&bar[3], par, kTcWaitLimit))) { good = false; break; }
+            tc::fence_after_sync();
+            float o[64];
+            {
+                uint32_t raw[64];
+                tc::tmem_ld32_nowait(tD2, raw);
+                tc::tmem_ld32_nowait(tD2 + 32, raw + 32);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 64; ++j) o[j] = __uint_as_float(raw[j]);
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[7]);  // D2 is free for the next chunk's MMA1
+            // sums of squares over this warp's 32 v for each token: a reduce-scatter butterfly per
+            // 32 tokens (31 shuffles) leaves the sum of token 32 hf + lane in lane `lane`
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float sq[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sq[j] = o[32 * hf + j] * o[32 * hf + j];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) {
+                    const bool upper = (lane & off) != 0;
+#pragma unroll
+                    for (int j = 0; j < off; ++j) {
+                        const float keep = upper ? sq[j + off] : sq[j];
+                        const float send = upper ? sq[j] : sq[j + off];
+                        sq[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                }
+                red[(32 * hf + lane) * 4 + qe] = sq[0];
+            }
+            // (the AND is also the barrier after every warp's sums are in red)
+            if (!bar_and(2, 128, mbar_wait_bounded(&bar[4], par, kTcWaitLimit))) { good = false; break; }
+            // gated RMSNorm; the BF16 results overwrite the gate logits in place
+            float rinv_l[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const float4 pl = reinterpret_cast<const float4 *>(red)[32 * hf + lane];
+                rinv_l[hf] = rsqrt_ftz(((pl.x + pl.y) + (pl.z + pl.w)) * (1.0f / kD) + rms_eps);
+            }
+            __nv_bfloat16 y[64];
+#pragma unroll
+            for (int r = 0; r < 64; ++r) {
+                const float rinv = __shfl_sync(0xFFFFFFFFu, rinv_l[r >> 5], r & 31);
+                const float gv = __bfloat162float(sGY[r * kD + vi]);
+                // sigmoid(g) = (1 + tanh(g/2)) / 2; the hardware tanh's error is below the BF16
+                // rounding of the output it multiplies
+                const float sg = fmaf(0.5f, tanh_approx(0.5f * gv), 0.5f);
+                y[r] = __float2bfloat16_rn(sg * nw * (o[r] * rinv));
+            }
+            if (e.n == kC) {  // each thread overwrites only the gate values it has read
+#pragma unroll
+                for (int r = 0; r < 64; ++r) sGY[r * kD + vi] = y[r];
+                tc::fence_smem_to_async();
+                named_bar_sync(2, 128);
+                if (et == 0) {
+                    tma_store_2d(&tm_out, h * kD, e.t0, sGY);
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                    mbar_arrive(&bar[8]);
+                }
+            } else {
+                T *obase = out + (size_t)e.t0 * D + (size_t)h * kD + vi;
+#pragma unroll
+                for (int r = 0; r < 64; ++r)
+                    if (r < e.n) obase[(size_t)r * D] = y[r];
+                named_bar_sync(2, 128);
+                if (et == 0) mbar_arrive(&bar[8]);
+            }
+        }
+        if (!good) atomicExch(err, KDA_ERR_TIMEOUT);
+        if (et == 0) bulk_wait_all();  // committed output boxes are written before the CTA exits
     }
-    if (tid == 0) bulk_wait_all();  // committed output boxes are written before the CTA exits
     tc::fence_before_sync();
     __syncthreads();
     if (w == 0) tc::tmem_dealloc(tb, 256);
@@ -1650,7 +1672,7 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
             memset(&tmg, 0, sizeof(tmg));
             memset(&tmo, 0, sizeof(tmo));
         }
-        state_tc_kernel<T><<<dim3(H, N), 256, kStateTcSmem, stream>>>(
+        state_tc_kernel<T><<<dim3(H, N), kStThreads, kStateTcSmem, stream>>>(
             st.S, (T *)st.tail, st.err, slots, H, st.max_slots, table, seq_first, chunks, (int)total_chunks,
             (const T *)q, (const T *)k, (const T *)v, p.norm_w, (T *)out, c.rms_eps, box_g, tmg, tmo);
         return cudaGetLastError();
