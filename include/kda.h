@@ -302,6 +302,29 @@ kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int64_t T, con
                          size_t workspace_bytes, void *stream);
 
 /*
+ * The gate/beta input projections folded into the prefill (kimi_k3.c header comment, block
+ * "KDA per-head recurrence": z = W_fb (W_fa x), beta = sigmoid(W_b x); struct Kda: fa
+ * [hd][hidden], fb [proj][hd], bp [heads][hidden]). z, H*d values per token, is never
+ * written to memory: kda_gate_proj_in produces the first product f = W_fa x (d values per
+ * token) and b = W_b x, and kda_prefill_gate_fused forms z = W_fb f inside the prefill, on
+ * the tensor cores, in FP32 (f is rounded to BF16 once, as in kda_gate_proj).
+ * kda_gate_proj_in:
+ *   hidden, T, x, w_fa, w_b, workspace: as for kda_gate_proj (the same workspace size)
+ *   f     device BF16 [T][d]    out
+ *   b     device BF16 [T][H]    out (aligned to its element size)
+ * kda_prefill_gate_fused: kda_prefill with z replaced by
+ *   f     device BF16 [total_T][d], 16-byte aligned: f = W_fa x of every token
+ *   w_fb  device BF16 [H*d][d], 16-byte aligned
+ * Both need BF16 I/O (KDA_ERR_INVALID otherwise). Errors as for kda_gate_proj / kda_prefill.
+ */
+kda_status kda_gate_proj_in(const kda_config_t *cfg, int32_t hidden, int64_t T, const void *x, const void *w_fa,
+                            const void *w_b, void *f, void *b, void *workspace, size_t workspace_bytes, void *stream);
+kda_status kda_prefill_gate_fused(const kda_config_t *cfg, const kda_layer_params *params, kda_state *state,
+                                  const int32_t *slots, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                                  int32_t N, const void *q, const void *k, const void *v, const void *f,
+                                  const void *w_fb, const void *b, const void *g, void *out, void *stream);
+
+/*
  * The dense projections around the mixer: y = x W^T (+ r) in BF16 with FP32
  * accumulation on the tensor cores. A KDA layer takes q, k, v and the output-gate
  * logits g from W_q, W_k, W_v, W_g applied to the hidden state x, and applies W_o to

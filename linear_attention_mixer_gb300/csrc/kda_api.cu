@@ -328,10 +328,12 @@ kda_status kda_decode_tokens(const kda_config_t *cfg, const kda_layer_params *pa
     return KDA_OK;
 }
 
-kda_status kda_prefill(const kda_config_t *cfg, const kda_layer_params *params, kda_state *h,
-                       const int32_t *slots, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int32_t N,
-                       const void *q, const void *k, const void *v, const void *z, const void *b, const void *g,
-                       void *out, void *stream)
+namespace {
+// kda_prefill, or with f and w_fb (z NULL) the prefill that forms z = W_fb f itself
+kda_status prefill_entry(const kda_config_t *cfg, const kda_layer_params *params, kda_state *h,
+                         const int32_t *slots, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int32_t N,
+                         const void *q, const void *k, const void *v, const void *z, const void *b, const void *g,
+                         void *out, void *stream, bool fused, const void *f, const void *w_fb)
 {
     if (!h) return fail(KDA_ERR_INVALID, "state is NULL");
     State *st = reinterpret_cast<State *>(h);
@@ -350,10 +352,13 @@ kda_status kda_prefill(const kda_config_t *cfg, const kda_layer_params *params, 
         total_chunks += (len + kda::kC - 1) / kda::kC;
     }
     const int64_t total_T = cu_seqlens_host[N];
-    if (total_T > 0 && (!q || !k || !v || !z || !b || !g || !out))
+    if (fused && cfg->io_dtype != KDA_BF16)
+        return fail(KDA_ERR_INVALID, "the fused gate projection needs BF16 I/O");
+    if (total_T > 0 && (!q || !k || !v || (fused ? (!f || !w_fb) : !z) || !b || !g || !out))
         return fail(KDA_ERR_INVALID, "a tensor pointer is NULL");
-    if (total_T > 0 && !kda::io_aligned(q, k, v, z, g, out))
-        return fail(KDA_ERR_INVALID, "q, k, v, z, g or out is not 16-byte aligned");
+    if (total_T > 0 && !kda::io_aligned(q, k, v, fused ? f : z, g, out))
+        return fail(KDA_ERR_INVALID, "q, k, v, %s, g or out is not 16-byte aligned", fused ? "f" : "z");
+    if (fused && (reinterpret_cast<uintptr_t>(w_fb) & 15u)) return fail(KDA_ERR_INVALID, "w_fb is not 16-byte aligned");
     if (total_chunks * cfg->num_heads > INT_MAX || (total_T * cfg->num_heads + 7) / 8 > INT_MAX)
         return fail(KDA_ERR_INVALID, "too many tokens for one call");
     if (!device_matches(st)) return KDA_ERR_INVALID;
@@ -371,9 +376,29 @@ kda_status kda_prefill(const kda_config_t *cfg, const kda_layer_params *params, 
         st->ws_bytes = need;
     }
     cudaError_t e = kda::launch_prefill(*st, *params, slots, cu_seqlens, N, total_T, total_chunks, q, k, v, z, b,
-                                        g, out, st->ws, static_cast<cudaStream_t>(stream));
+                                        g, out, st->ws, static_cast<cudaStream_t>(stream), fused ? f : nullptr,
+                                        fused ? w_fb : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "kda_prefill launch");
     return KDA_OK;
+}
+}  // namespace
+
+kda_status kda_prefill(const kda_config_t *cfg, const kda_layer_params *params, kda_state *h,
+                       const int32_t *slots, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int32_t N,
+                       const void *q, const void *k, const void *v, const void *z, const void *b, const void *g,
+                       void *out, void *stream)
+{
+    return prefill_entry(cfg, params, h, slots, cu_seqlens, cu_seqlens_host, N, q, k, v, z, b, g, out, stream,
+                         false, nullptr, nullptr);
+}
+
+kda_status kda_prefill_gate_fused(const kda_config_t *cfg, const kda_layer_params *params, kda_state *h,
+                                  const int32_t *slots, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                                  int32_t N, const void *q, const void *k, const void *v, const void *f,
+                                  const void *w_fb, const void *b, const void *g, void *out, void *stream)
+{
+    return prefill_entry(cfg, params, h, slots, cu_seqlens, cu_seqlens_host, N, q, k, v, nullptr, b, g, out, stream,
+                         true, f, w_fb);
 }
 
 kda_status kda_state_poll_error(kda_state *h, int32_t *code)

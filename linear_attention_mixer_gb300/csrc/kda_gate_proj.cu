@@ -497,6 +497,28 @@ gp_out_kernel(const __grid_constant__ CUtensorMap tm_fb, const __grid_constant__
     }
 }
 
+// ---------------------------------------------------------------- first product only
+// f (BF16 [T][d]) and b (BF16 [T][H]) from the FP32 sums of gp_in ([T][n1]: f then b): for a
+// prefill that forms z = W_fb f itself. Thread t4 of a row rounds 4 consecutive values.
+__global__ void __launch_bounds__(256)
+gp_f_kernel(const float *__restrict__ sums, __nv_bfloat16 *__restrict__ f, __nv_bfloat16 *__restrict__ bout,
+            int64_t T, int H, int n1)
+{
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;  // (row, 4 columns of f | b)
+    const int per = kD / 4 + (H + 3) / 4;
+    const int64_t t = i / per;
+    if (t >= T) return;
+    const int c4 = (int)(i - t * per);
+    const float *src = sums + (size_t)t * n1;
+    if (c4 < kD / 4) {
+        const float4 v = reinterpret_cast<const float4 *>(src)[c4];
+        *reinterpret_cast<uint2 *>(f + (size_t)t * kD + 4 * c4) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+    } else {
+        const int h0 = 4 * (c4 - kD / 4);
+        for (int j = 0; j < 4 && h0 + j < H; ++j) bout[(size_t)t * H + h0 + j] = __float2bfloat16_rn(src[kD + h0 + j]);
+    }
+}
+
 // ---------------------------------------------------------------- FP32 I/O path
 // With FP32 I/O the same products run on CUDA cores in FP32, the correctness path for FP32
 // configurations (as the FP32 prefill kernels are): C[M][N] = A[M][K] B[N][K]^T in 64 x 64
@@ -734,5 +756,66 @@ extern "C" kda_status kda_gate_proj(const kda_config_t *cfg, int32_t hidden, int
     if ((e = cudaLaunchKernelEx(&lc, gp_out_kernel, tm_fb, tm_z, (const float *)sums, static_cast<__nv_bfloat16 *>(b),
                                 (int)T, H, HD, n1, ntiles, items, fb_rows, err)) != cudaSuccess)
         return gp_fail(KDA_ERR_CUDA, "gp_out_kernel launch: %s", cudaGetErrorString(e));
+    return KDA_OK;
+}
+
+extern "C" kda_status kda_gate_proj_in(const kda_config_t *cfg, int32_t hidden, int64_t T, const void *x,
+                                       const void *w_fa, const void *w_b, void *f, void *b, void *workspace,
+                                       size_t workspace_bytes, void *stream)
+{
+    using namespace kda;
+    kda_status st = gp_check(cfg, hidden, T);
+    if (st != KDA_OK) return st;
+    if (cfg->io_dtype != KDA_BF16) return gp_fail(KDA_ERR_INVALID, "kda_gate_proj_in needs BF16 I/O");
+    if (!workspace) return gp_fail(KDA_ERR_INVALID, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return gp_fail(KDA_ERR_INVALID, "workspace is not 16-byte aligned");
+    if (T == 0) return KDA_OK;
+    if (!x || !w_fa || !w_b || !f || !b) return gp_fail(KDA_ERR_INVALID, "a tensor pointer is NULL");
+    const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_fa) |
+                         reinterpret_cast<uintptr_t>(w_b) | reinterpret_cast<uintptr_t>(f);
+    if (al & 15u) return gp_fail(KDA_ERR_INVALID, "x, w_fa, w_b or f is not 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(b) & 1u) return gp_fail(KDA_ERR_INVALID, "b is not aligned to its element size");
+    int sms = 0;
+    if ((st = gp_sms(&sms)) != KDA_OK) return st;
+    const size_t need = gp_workspace(*cfg, T);
+    if (workspace_bytes < need)
+        return gp_fail(KDA_ERR_INVALID, "workspace holds %zu bytes; this call needs %zu", workspace_bytes, need);
+    const int splits = gp_splits((T + 2 * kGpTile - 1) / (2 * kGpTile), hidden / kGpKs, sms);
+    const int H = cfg->num_heads, n1 = gp_n1(H);
+    const int mtiles = (int)((T + kGpTile - 1) / kGpTile);
+    const int x_rows = (int)(T < kGpTile ? T : kGpTile);
+    CUtensorMap tm_x, tm_fa, tm_bp;
+    cudaError_t e;
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if ((e = encode_2d(&tm_x, x, hidden, T, (uint64_t)hidden * 2, kGpKs, x_rows, sw)) != cudaSuccess ||
+        (e = encode_2d(&tm_fa, w_fa, hidden, kD, (uint64_t)hidden * 2, kGpKs, kD, sw)) != cudaSuccess ||
+        (e = encode_2d(&tm_bp, w_b, hidden, H, (uint64_t)hidden * 2, kGpKs, H, sw)) != cudaSuccess)
+        return gp_fail(KDA_ERR_CUDA, "kda_gate_proj_in: tensor map encoding failed: %s", cudaGetErrorString(e));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t *err = static_cast<int32_t *>(workspace);
+    float *sums = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + kGpErrBytes);
+    const int in_smem = kGpStages * gp_in_stage_bytes(n1) + 128 + kGpAlign;
+    if ((e = cudaMemsetAsync(err, 0, sizeof(int32_t), s)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(gp_in_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, in_smem)) != cudaSuccess)
+        return gp_fail(KDA_ERR_CUDA, "kda_gate_proj_in: %s", cudaGetErrorString(e));
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute at[1];
+    lc.gridDim = dim3((unsigned)((mtiles + 1) / 2), (unsigned)splits, 1);
+    lc.blockDim = dim3(128, 1, 1);
+    lc.dynamicSmemBytes = (size_t)in_smem;
+    lc.stream = s;
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = (unsigned)splits;
+    at[0].val.clusterDim.z = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&lc, gp_in_kernel, tm_x, tm_fa, tm_bp, sums, (int)T, hidden / kGpKs, splits, n1,
+                                x_rows, H, err)) != cudaSuccess)
+        return gp_fail(KDA_ERR_CUDA, "gp_in_kernel launch: %s", cudaGetErrorString(e));
+    const int64_t threads = T * (kD / 4 + (H + 3) / 4);
+    gp_f_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(sums, static_cast<__nv_bfloat16 *>(f),
+                                                                 static_cast<__nv_bfloat16 *>(b), T, H, n1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return gp_fail(KDA_ERR_CUDA, "gp_f_kernel launch: %s", cudaGetErrorString(e));
     return KDA_OK;
 }

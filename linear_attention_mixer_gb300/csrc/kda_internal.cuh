@@ -95,10 +95,12 @@ cudaError_t launch_decode_multi(const State &st, const kda_layer_params &p, cons
                                 const void *g, void *out, cudaStream_t stream);
 
 size_t prefill_workspace_bytes(const kda_config_t &cfg, int64_t total_chunks, int64_t total_T, int N);
+// f and w_fb non-null: z is not read; it is formed in the prefill as W_fb f (BF16 I/O only)
 cudaError_t launch_prefill(const State &st, const kda_layer_params &p, const int32_t *slots,
                            const int32_t *cu_seqlens, int N, int64_t total_T, int64_t total_chunks,
                            const void *q, const void *k, const void *v, const void *z, const void *b,
-                           const void *g, void *out, void *ws, cudaStream_t stream);
+                           const void *g, void *out, void *ws, cudaStream_t stream, const void *f = nullptr,
+                           const void *w_fb = nullptr);
 
 // Error text and config checks shared by every entry point (kda_api.cu).
 kda_status record_error(kda_status s, const char *msg);

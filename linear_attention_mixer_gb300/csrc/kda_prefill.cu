@@ -515,9 +515,10 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                const T *__restrict__ z, const T *__restrict__ bl,
                unsigned char *__restrict__ chunks, int32_t *__restrict__ err,
-               float gmin, float l2_eps, float q_scale, int n_items, int box_rows,
+               float gmin, float l2_eps, float q_scale, int n_items, int box_rows, int f_rows, int fused,
                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z)
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
+               const __grid_constant__ CUtensorMap tm_f, const __grid_constant__ CUtensorMap tm_fb)
 {
     extern __shared__ __align__(1024) float smf[];
     float *Yq = smf;                                  // [64][132] q^
@@ -526,8 +527,9 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     float *GL = Yv + kC * kYS;                        // [64][132] gk, then G = cumulative log decay
     unsigned char *Y = reinterpret_cast<unsigned char *>(GL + kC * kYS);
     float *sbeta = reinterpret_cast<float *>(Y + kPtY);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sbeta + kC);  // [0] inputs, [1..2] A/P buffers, [3] solve
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 4);
+    // [0] z operands (fused), [1..2] A/P buffers, [3] solve, [4] z product (fused)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbeta + kC);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 5);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t D = (size_t)H * kD;
@@ -551,6 +553,19 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         while (it < n_items && !item_ok(it)) it += (int)gridDim.x;
         return it;
     };
+    // With the gate projection fused (fused != 0) an item's z = W_fb,h f is one tcgen05 product at
+    // the item's start, in place of the z rows: the head's W_fb rows (128 x 128) arrive in the
+    // gate array (only the gate threads write it, after the product) and the chunk's f rows
+    // (64 x 128) past the q, k, v rows of the staging region, both as 128-byte-swizzled TMA boxes
+    // with the item's other inputs; the product (lane = channel, column = row) lands in TMEM
+    // columns 160..223, where the gate threads read it in FP32.
+    unsigned char *sFb = reinterpret_cast<unsigned char *>(GL);        // [2 k halves][128 rows][128 B]
+    unsigned char *sF = Y + 54272;                                      // [2 k halves][64 rows][128 B]
+    constexpr uint32_t kZCol = 160;
+    static_assert(2 * kD * 128 <= kC * kYS * 4 && 54272 >= 3 * (kC + 6) * kD * 2 && 54272 % 1024 == 0 &&
+                  54272 + 2 * kC * 128 <= kPtY && (4 * kC * kYS * 4 - kC * kYS * 4) % 1024 == 0,
+                  "z operands fit and are 1024-byte aligned");
+
     // 0. (one thread) an item's inputs, counted on bars[0]: one 2-D box of box_rows rows (x = the
     //    head's 128 channels) per stream, from 3 rows before the chunk, or, for a sequence's
     //    first chunk (and for z), from its first row, with the 3 history rows then taken from
@@ -560,13 +575,21 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         const int ci = it / H, hi = it - ci * H;
         const ChunkEntry ei = table[ci];
         const bool first = ei.pos0 == 0;
-        mbar_arrive_expect_tx(bars, (uint32_t)((4 * box_rows + (first ? 9 : 0)) * kD * sizeof(T)));
+        mbar_arrive_expect_tx(bars, (uint32_t)(((fused ? 3 : 4) * box_rows + (first ? 9 : 0)) * kD * sizeof(T)) +
+                                        (fused ? (uint32_t)(2 * (kD + f_rows) * 128) : 0u));
         const int hx = hi * kD;
         const int ylo = first ? ei.t0 : ei.t0 - 3, jlo = first ? 3 : 0;
         tma_load_2d(raw + (size_t)(0 * kRows + jlo) * kD, &tm_q, hx, ylo, bars);
         tma_load_2d(raw + (size_t)(1 * kRows + jlo) * kD, &tm_k, hx, ylo, bars);
         tma_load_2d(raw + (size_t)(2 * kRows + jlo) * kD, &tm_v, hx, ylo, bars);
-        tma_load_2d(raw + (size_t)(3 * kRows + 3) * kD, &tm_z, hx, ei.t0, bars);
+        if (fused) {  // the z operands instead of the z rows
+            tma_load_2d(sFb, &tm_fb, 0, hi * kD, bars);
+            tma_load_2d(sFb + kD * 128, &tm_fb, 64, hi * kD, bars);
+            tma_load_2d(sF, &tm_f, 0, ei.t0, bars);
+            tma_load_2d(sF + kC * 128, &tm_f, 64, ei.t0, bars);
+        } else {
+            tma_load_2d(raw + (size_t)(3 * kRows + 3) * kD, &tm_z, hx, ei.t0, bars);
+        }
         if (first) {
             const T *tl0 = tail_all + (size_t)slots[ei.seq] * 3 * (kK - 1) * D + (size_t)hi * kD;
             for (int x = 0; x < 3; ++x)
@@ -577,10 +600,17 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
 
     if (warp == 0) tc::tmem_alloc(tslot, 512);
     int it = next_item((int)blockIdx.x);
+    bool staged = false;    // (thread 32) z operand copies in flight, completing phase staged_ph
+    uint32_t staged_ph = 0;
+    bool zmma_out = false;  // (thread 32) a z product in flight, completing phase zmma_ph
+    uint32_t zmma_ph = 0;
     if (tid == 32) {
-        for (int i = 0; i < 4; ++i) mbar_init(bars + i, 1);
+        for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
         fence_mbar_init();
-        if (it < n_items) stage(it);
+        if (it < n_items) {
+            stage(it);
+            staged = true;
+        }
     }
     tc::fence_before_sync();
     __syncthreads();  // barrier init and TMEM base visible
@@ -622,7 +652,6 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
     };
     bool good = true;
-    bool staged = false;  // (thread 32) the next item's copies are in flight
     bool aborted = false;
     unsigned char *blk_prev = nullptr;  // the previous item's block: its W and U' are still in TMEM
     uint32_t done = 0;    // items processed: the phase parity of bars[0] and bars[3]
@@ -639,19 +668,44 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             tma_prefetch_2d(&tm_q, h2 * kD, y2);
             tma_prefetch_2d(&tm_k, h2 * kD, y2);
             tma_prefetch_2d(&tm_v, h2 * kD, y2);
-            tma_prefetch_2d(&tm_z, h2 * kD, e2.t0);
+            if (fused) {
+                tma_prefetch_2d(&tm_f, 0, e2.t0);
+                tma_prefetch_2d(&tm_f, 64, e2.t0);
+                tma_prefetch_2d(&tm_fb, 0, h2 * kD);
+                tma_prefetch_2d(&tm_fb, 64, h2 * kD);
+            } else {
+                tma_prefetch_2d(&tm_z, h2 * kD, e2.t0);
+            }
         }
         const int t0 = table[chunk].t0;
         unsigned short braw = 0;
         if (tid < kC && tid < n) braw = ld_nc_u16(bl + (size_t)(t0 + tid) * H + h);
-        // this thread's per-channel parameters, loaded while the staging copies are in flight
+        // this thread's per-channel parameters
         const int pc = tid & (kD - 1), px = tid >> 7;  // channel, stream (q, k, v, or the gate)
         const float4 p_w = px < 3 ? __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)px * D + (size_t)h * kD + pc) * kK))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         const float p_dt = __ldg(dt_bias + (size_t)h * kD + pc);
         const float p_eA = expf(__ldg(A_log + h));
-        good &= mbar_wait_bounded(bars, done & 1u, kTcWaitLimit);
-        staged = false;
+        {
+            const bool ok = mbar_wait_bounded(bars, done & 1u, kTcWaitLimit);
+            good &= ok;
+            if (ok && tid == 32) staged = false;
+        }
+        if (fused && tid == 32 && good) {  // z = W_fb,h f for this item's rows (8 K steps of 16)
+            {
+                tc::fence_after_sync();
+                const uint32_t idz = tc::idesc_bf16(128, kC);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t ko = (uint32_t)(kk & 3) * 32;
+                    tc::mma_bf16(tb + kZCol, tc::sw128_desc(smem_u32(sFb + (kk >> 2) * kD * 128) + ko),
+                                 tc::sw128_desc(smem_u32(sF + (kk >> 2) * kC * 128) + ko), idz, kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(bars + 4);
+                zmma_out = true;
+                zmma_ph = done & 1u;
+            }
+        }
         if (tid < kC) sbeta[tid] = tid < n ? sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
 
         // 1. conv + SiLU (sliding window in registers) for stream px < 3, 2. the gates for px == 3;
@@ -680,19 +734,34 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             }
         } else {
             // the gate thread of channel pc also carries G_r = sum_{t<=r} gk_t down the rows (gk = 0,
-            // no decay, past the chunk, so G stays at G_last there)
+            // no decay, past the chunk, so G stays at G_last there); z from TMEM (fused) or the
+            // staged rows
+            if (fused) {
+                good &= mbar_wait_bounded(bars + 4, done & 1u, kTcWaitLimit);
+                tc::fence_after_sync();
+            }
             const T *col = raw + ((size_t)3 * kRows + 3) * kD + pc;
             float acc = 0.f;
 #pragma unroll 1
-            for (int r0 = 0; r0 < kC; r0 += 8) {
-                float zz[8];
+            for (int hb = 0; hb < 2; ++hb) {  // 32 rows at a time
+                float zz[32];
+                if (fused) {
+                    uint32_t zr[32];
+                    tc::tmem_ld32_nowait(tb + ((uint32_t)(32 * (warp & 3)) << 16) + kZCol + 32 * hb, zr);
+                    tc::tmem_wait_ld();
 #pragma unroll
-                for (int u = 0; u < 8; ++u) zz[u] = IO<T>::ld(col + (r0 + u) * kD);
+                    for (int j = 0; j < 32; ++j) zz[j] = __uint_as_float(zr[j]);
+                } else {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[u] + p_dt), 80.f)));
-                    acc += r0 + u < n ? gmin * sg : 0.f;
-                    GL[(r0 + u) * kYS + pc] = acc;
+                    for (int j = 0; j < 32; ++j) zz[j] = IO<T>::ld(col + (32 * hb + j) * kD);
+                }
+                // (fused: the product has completed, so the array that held W_fb takes G)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int r = 32 * hb + j;
+                    const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[j] + p_dt), 80.f)));
+                    acc += r < n ? gmin * sg : 0.f;
+                    GL[r * kYS + pc] = acc;
                 }
             }
         }
@@ -1008,6 +1077,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             tc::fence_smem_to_async();
             stage(nxt);
             staged = true;
+            staged_ph = (done + 1) & 1u;
         }
         blk_prev = blk;
         tc::fence_before_sync();
@@ -1020,8 +1090,10 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
         it = nxt;
     }
-    // after an abort the next item's copies may still be in flight: wait for them (bounded)
-    if (staged) mbar_wait_bounded(bars, (done + 1) & 1u, kTcWaitLimit);
+    // after an abort a z operand copy or product may still be in flight: wait for it (bounded)
+    if (staged) mbar_wait_bounded(bars, staged_ph, kTcWaitLimit);
+    if (zmma_out && !aborted) zmma_out = false;
+    if (zmma_out) mbar_wait_bounded(bars + 4, zmma_ph, kTcWaitLimit);
     if (!aborted && blk_prev) write_wu(blk_prev, warp >> 2, 4);  // the last item's W and U'
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
@@ -1605,11 +1677,36 @@ cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int6
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tensor map of a packed [rows][cols] BF16 matrix for 2-D boxes of 64 columns x box_rows rows
+// with 128-byte swizzle (MMA operands).
+cudaError_t encode_sw128_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows)
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            fn = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <typename T>
 cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32_t *slots,
                          const int32_t *cu, int N, int64_t total_T, int64_t total_chunks,
                          const void *q, const void *k, const void *v, const void *z, const void *b,
-                         const void *g, void *out, void *ws, cudaStream_t stream)
+                         const void *g, void *out, void *ws, cudaStream_t stream, const void *f,
+                         const void *w_fb)
 {
     // BF16 I/O runs the tensor-core state pass; FP32 I/O keeps every contraction in FP32.
     constexpr bool kTC = sizeof(T) == 2;
@@ -1632,12 +1729,24 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
             // boxes of 67 rows (3 history rows + a chunk); never taller than the tensor
             const int box_rows = (int)(total_T < kC + 3 ? total_T : kC + 3);
             const int64_t Dm = (int64_t)H * kD;
-            CUtensorMap tmq, tmk, tmv, tmz;
+            CUtensorMap tmq, tmk, tmv, tmz, tmf, tmfb;
+            const bool fused = f != nullptr;
+            const int f_rows = (int)(total_T < kC ? total_T : kC);
             if ((e = encode_rows_map(&tmq, q, total_T, Dm, box_rows)) != cudaSuccess ||
                 (e = encode_rows_map(&tmk, k, total_T, Dm, box_rows)) != cudaSuccess ||
-                (e = encode_rows_map(&tmv, v, total_T, Dm, box_rows)) != cudaSuccess ||
-                (e = encode_rows_map(&tmz, z, total_T, Dm, box_rows)) != cudaSuccess)
+                (e = encode_rows_map(&tmv, v, total_T, Dm, box_rows)) != cudaSuccess)
                 return e;
+            if (fused) {
+                // z is formed in prep from f = W_fa x ([T][d]) and the head's rows of W_fb ([H d][d])
+                if ((e = encode_sw128_map(&tmf, f, total_T, kD, f_rows)) != cudaSuccess ||
+                    (e = encode_sw128_map(&tmfb, w_fb, Dm, kD, kD)) != cudaSuccess)
+                    return e;
+                memcpy(&tmz, &tmq, sizeof(tmz));
+            } else {
+                if ((e = encode_rows_map(&tmz, z, total_T, Dm, box_rows)) != cudaSuccess) return e;
+                memcpy(&tmf, &tmq, sizeof(tmf));
+                memcpy(&tmfb, &tmq, sizeof(tmfb));
+            }
             e = raise_smem_once(st, kSmemPrepTc, prep_tc_kernel<T>, kPrepTcSmem);
             if (e != cudaSuccess) return e;
             // persistent: one CTA per SM strides over the (chunk, head) items
@@ -1645,7 +1754,8 @@ cudaError_t launch_typed(const State &st, const kda_layer_params &p, const int32
             prep_tc_kernel<T><<<(unsigned)(n_items < sms ? n_items : sms), 512, kPrepTcSmem, stream>>>(
                 p.conv_w, p.dt_bias, p.A_log, (const T *)st.tail, slots, H, st.max_slots, table,
                 (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, chunks, st.err,
-                c.gate_lower_bound, c.l2_eps, c.q_scale, n_items, box_rows, tmq, tmk, tmv, tmz);
+                c.gate_lower_bound, c.l2_eps, c.q_scale, n_items, box_rows, f_rows, fused ? 1 : 0, tmq, tmk, tmv,
+                tmz, tmf, tmfb);
         } else {
             const int prep_smem = kPrepSmemFloats * (int)sizeof(float);
             e = raise_smem_once(st, kSmemPrepF32, prep_kernel<T>, prep_smem);
@@ -1705,13 +1815,15 @@ size_t prefill_workspace_bytes(const kda_config_t &cfg, int64_t total_chunks, in
 cudaError_t launch_prefill(const State &st, const kda_layer_params &p, const int32_t *slots,
                            const int32_t *cu_seqlens, int N, int64_t total_T, int64_t total_chunks,
                            const void *q, const void *k, const void *v, const void *z, const void *b,
-                           const void *g, void *out, void *ws, cudaStream_t stream)
+                           const void *g, void *out, void *ws, cudaStream_t stream, const void *f,
+                           const void *w_fb)
 {
     if (st.cfg.io_dtype == KDA_BF16)
         return launch_typed<__nv_bfloat16>(st, p, slots, cu_seqlens, N, total_T, total_chunks, q, k, v, z, b,
-                                           g, out, ws, stream);
+                                           g, out, ws, stream, f, w_fb);
+    if (f) return cudaErrorInvalidValue;  // the fused gate projection runs on the tensor-core path
     return launch_typed<float>(st, p, slots, cu_seqlens, N, total_T, total_chunks, q, k, v, z, b, g, out, ws,
-                               stream);
+                               stream, nullptr, nullptr);
 }
 
 }  // namespace kda

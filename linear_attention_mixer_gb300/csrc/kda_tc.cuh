@@ -60,6 +60,20 @@ __device__ __forceinline__ uint64_t kmajor_desc_pad(const void *tile, int kk, in
     return smem_desc(smem_u32(tile) + (uint32_t)kk * 2u * kPadLBO, (uint32_t)kPadLBO, (uint32_t)(Kd / 8) * kPadLBO);
 }
 
+// K-major descriptor of a 128-byte-swizzled tile (rows of 128 bytes as TMA lands them with
+// 128-byte swizzle, 8-row groups 1024 bytes apart, the tile 1024-byte aligned); a K step of 16
+// moves the start by 32 bytes.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;             // leading byte offset (unused by swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset: 8-row groups
+    d |= (uint64_t)1 << 46;             // descriptor version for this architecture
+    d |= (uint64_t)2 << 61;             // layout: 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor: kind::f16, BF16 x BF16 -> FP32, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
 {

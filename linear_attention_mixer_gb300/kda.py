@@ -81,6 +81,10 @@ SIGNATURES = [
     ("kda_gate_proj_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(kda_config_t), _I32, ctypes.c_int64]),
     ("kda_gate_proj", _I32, [ctypes.POINTER(kda_config_t), _I32, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP,
                              _VP, ctypes.c_size_t, _VP]),
+    ("kda_gate_proj_in", _I32, [ctypes.POINTER(kda_config_t), _I32, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP,
+                                ctypes.c_size_t, _VP]),
+    ("kda_prefill_gate_fused", _I32, [ctypes.POINTER(kda_config_t), ctypes.POINTER(kda_layer_params), _VP, _VP, _VP,
+                                      _PI32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("kda_linear_workspace_bytes", ctypes.c_size_t, [_I32, _I32, _I32]),
     ("kda_linear", _I32, [_I32, _I32, _I32, _VP, _VP, _VP, _VP, _I32, _VP, ctypes.c_size_t, _VP]),
     ("kda_photo_store_create", _I32, [_I32, ctypes.c_char_p, ctypes.POINTER(_VP)]),
@@ -308,6 +312,45 @@ def kda_gate_proj(cfg: kda_config_t, x, w_fa, w_fb, w_b, z, b, workspace: torch.
     _check(lib().kda_gate_proj(ctypes.byref(cfg), hidden, T, _dev(x, bf, "x"), _dev(w_fa, bf, "w_fa"),
                                _dev(w_fb, bf, "w_fb"), _dev(w_b, bf, "w_b"), _dev(z, bf, "z"), _dev(b, bf, "b"),
                                ws, workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kda_gate_proj_in(cfg: kda_config_t, x, w_fa, w_b, f, b, workspace: torch.Tensor, stream=None) -> None:
+    """f = W_fa x [T, d] and b = W_b x [T, H] (BF16), the inputs of kda_prefill_gate_fused."""
+    H, d = cfg.num_heads, cfg.head_dim
+    if x.dim() != 2:
+        raise ValueError("x must be [T, hidden]")
+    T, hidden = int(x.shape[0]), int(x.shape[1])
+    for name, t, shape in (("w_fa", w_fa, (d, hidden)), ("w_b", w_b, (H, hidden)), ("f", f, (T, d)), ("b", b, (T, H))):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {list(shape)}, got {list(t.shape)}")
+    bf = torch.bfloat16
+    _check(lib().kda_gate_proj_in(ctypes.byref(cfg), hidden, T, _dev(x, bf, "x"), _dev(w_fa, bf, "w_fa"),
+                                  _dev(w_b, bf, "w_b"), _dev(f, bf, "f"), _dev(b, bf, "b"),
+                                  _dev(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
+
+
+def kda_prefill_gate_fused(cfg: kda_config_t, params: kda_layer_params, st, slots: torch.Tensor,
+                           cu_seqlens: torch.Tensor, cu_seqlens_host, q, k, v, f, w_fb, b, g, out, stream=None) -> None:
+    """kda_prefill with z = W_fb f formed inside (f = W_fa x [T, d], w_fb [H d, d]; BF16)."""
+    bf = torch.bfloat16
+    N = int(slots.numel())
+    cu_h, cu_p = _host_i32(cu_seqlens_host)
+    if len(cu_h) != N + 1 or cu_seqlens.numel() != N + 1:
+        raise ValueError("cu_seqlens must hold N + 1 entries")
+    T = int(cu_h[-1]) if N > 0 else 0
+    H, d = cfg.num_heads, cfg.head_dim
+    D = H * d
+    for name, t, width in (("q", q, D), ("k", k, D), ("v", v, D), ("f", f, d), ("g", g, D), ("b", b, H),
+                           ("out", out, D)):
+        if t.numel() != T * width:
+            raise ValueError(f"{name} must hold {T} x {width} elements, got {tuple(t.shape)}")
+    if tuple(w_fb.shape) != (D, d):
+        raise ValueError(f"w_fb must be [{D}, {d}]")
+    _check(lib().kda_prefill_gate_fused(ctypes.byref(cfg), ctypes.byref(params), st, _dev(slots, torch.int32, "slots"),
+                                        _dev(cu_seqlens, torch.int32, "cu_seqlens"), cu_p, N, _dev(q, bf, "q"),
+                                        _dev(k, bf, "k"), _dev(v, bf, "v"), _dev(f, bf, "f"), _dev(w_fb, bf, "w_fb"),
+                                        _dev(b, bf, "b"), _dev(g, bf, "g"), _dev(out, bf, "out"), _stream(stream)))
 
 
 def kda_linear_workspace_bytes(M: int, N: int, K: int) -> int:

@@ -165,3 +165,77 @@ def test_gate_proj_feeds_the_mixer_fp32(oracle_mod):
     err = rel_err(got, np.concatenate(refs))
     print(f"gate_proj -> prefill, FP32, {T} tokens: rel err {err:.2e}")
     assert err <= TOL_F32
+
+
+@pytest.mark.parametrize("H,hidden,lens", [(4, 256, [70, 33, 130]), (96, 1024, [300, 129])])
+def test_gate_projection_fused_into_prefill_bf16(oracle_mod, H, hidden, lens):
+    """x -> kda_gate_proj_in (f = W_fa x, b = W_b x) -> kda_prefill_gate_fused (z = W_fb f formed
+    inside the prefill, never written) against the oracle's projection and recurrence, next to
+    the separate path x -> kda_gate_proj -> kda_prefill; outputs and final states within the BF16
+    bound, and b equal bit for bit between the two projection calls."""
+    from tests.kda_testutil import TOL_BF16, dev_params, download_state, to_np
+    d = 128
+    T = sum(lens)
+    N = len(lens)
+    cfg = K.kda_config(H, d, K.KDA_BF16)
+    gp = KI.make_gate_proj(T, hidden, H, d, seed=23)
+    p = KI.make_params(H, d, 4, seed=23)
+    tok = KI.make_tokens(T, H, d, seed=23, bf16=True)
+    bf = torch.bfloat16
+    dv = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda().to(bf).contiguous()
+    x, w_fa, w_fb, w_b = (dv(gp[n]) for n in ("x", "w_fa", "w_fb", "w_b"))
+    ws = torch.empty(K.kda_gate_proj_workspace_bytes(cfg, hidden, T), dtype=torch.uint8, device="cuda")
+    z = torch.empty(T, H * d, dtype=bf, device="cuda")
+    b1 = torch.empty(T, H, dtype=bf, device="cuda")
+    f = torch.empty(T, d, dtype=bf, device="cuda")
+    b2 = torch.empty(T, H, dtype=bf, device="cuda")
+    K.kda_gate_proj(cfg, x, w_fa, w_fb, w_b, z, b1, ws)
+    K.kda_gate_proj_in(cfg, x, w_fa, w_b, f, b2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(b1, b2)
+    q, k, v, g = (dv(tok[n]) for n in ("q", "k", "v", "g"))
+    cu_h = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cu = torch.tensor(cu_h, device="cuda")
+    slots = torch.arange(N, dtype=torch.int32, device="cuda")
+    params = dev_params(p)
+    res = {}
+    for mode in ("separate", "fused"):
+        st = K.kda_state_alloc(cfg, N)
+        try:
+            out = torch.empty(T, H * d, dtype=bf, device="cuda")
+            if mode == "fused":
+                K.kda_prefill_gate_fused(cfg, params, st, slots, cu, cu_h, q, k, v, f, w_fb, b2, g, out)
+            else:
+                K.kda_prefill(cfg, params, st, slots, cu, cu_h, q, k, v, z, b1, g, out)
+            res[mode] = (to_np(out), download_state(cfg, st, list(range(N)))[0])
+            assert K.kda_state_poll_error(st) == 0
+        finally:
+            K.kda_state_free(st)
+    z_o, b_o = gate_proj(gp["x"], gp["w_fa"], gp["w_fb"], gp["w_b"])
+    oc = oracle_mod.OracleCfg(H=H, d=d)
+    refs, Ss = [], []
+    for i in range(N):
+        s0, s1 = cu_h[i], cu_h[i + 1]
+        seq = {n: tok[n][s0:s1] for n in ("q", "k", "v", "g")}
+        seq["z"], seq["b"] = z_o[s0:s1].astype(np.float32), b_o[s0:s1].astype(np.float32)
+        S, tail = oracle_mod.new_state(oc)
+        refs.append(oracle_mod.sequence(oc, p, S, tail, seq))
+        Ss.append(S)
+    ref = np.concatenate(refs)
+    for mode, (got, Sg) in res.items():
+        e, es = rel_err(got, ref), rel_err(Sg, np.stack(Ss))
+        print(f"gate projection + prefill ({mode}), H={H}, {T} tokens: out {e:.2e} state {es:.2e}")
+        assert e <= TOL_BF16 and es <= TOL_BF16
+    # FP32 I/O has no fused path (the C entry point refuses it before enqueuing anything)
+    import ctypes
+    from linear_attention_mixer_gb300 import kda as KM
+    cfg32 = K.kda_config(H, d, K.KDA_F32)
+    st = K.kda_state_alloc(cfg32, N)
+    try:
+        P = lambda t: ctypes.c_void_p(t.data_ptr())
+        rc = K.lib().kda_prefill_gate_fused(ctypes.byref(cfg32), ctypes.byref(params), st, P(slots), P(cu),
+                                             KM._host_i32(cu_h)[1], N, P(q), P(k), P(v), P(f), P(w_fb), P(b2), P(g),
+                                             P(q), ctypes.c_void_p(None))
+        assert rc == K.KDA_ERR_INVALID and "BF16" in K.kda_last_error()
+    finally:
+        K.kda_state_free(st)
