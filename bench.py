@@ -658,6 +658,65 @@ def _time_layer_stack(K, args, cfg, gen, dev, stream, reps=5):
                           f"{reps} steps"}
 
 
+def _time_gate_prefill(K, args, cfg, params, gen, dev, stream, reps=10):
+    """From the hidden state to the mixer output for one sequence of T tokens (hidden 7168, 96
+    heads): kda_gate_proj then kda_prefill (z written and read back), against kda_gate_proj_in
+    then kda_prefill_gate_fused (z formed inside the prefill). L2 flushed before each call."""
+    import torch
+    T = args.prefill_tokens
+    bf = torch.bfloat16
+    x = torch.randn(T, HIDDEN, generator=gen, device=dev).to(bf)
+    fa = (torch.randn(DH, HIDDEN, generator=gen, device=dev) * HIDDEN ** -0.5).to(bf)
+    fb = (torch.randn(D, DH, generator=gen, device=dev) * DH ** -0.5).to(bf)
+    bp = (torch.randn(H, HIDDEN, generator=gen, device=dev) * HIDDEN ** -0.5).to(bf)
+    px = _inputs(T, gen, dev, bf)
+    z = torch.empty(T, D, dtype=bf, device=dev)
+    f = torch.empty(T, DH, dtype=bf, device=dev)
+    b = torch.empty(T, H, dtype=bf, device=dev)
+    out = torch.empty(T, D, dtype=bf, device=dev)
+    ws = torch.empty(K.kda_gate_proj_workspace_bytes(cfg, HIDDEN, T), dtype=torch.uint8, device=dev)
+    st = K.kda_state_alloc(cfg, 1)
+    slots = torch.zeros(1, dtype=torch.int32, device=dev)
+    cu_h = [0, T]
+    cu = torch.tensor(cu_h, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def separate():
+        K.kda_gate_proj(cfg, x, fa, fb, bp, z, b, ws, stream)
+        K.kda_prefill(cfg, params, st, slots, cu, cu_h, px["q"], px["k"], px["v"], z, b, px["g"], out, stream)
+
+    def fused():
+        K.kda_gate_proj_in(cfg, x, fa, bp, f, b, ws, stream)
+        K.kda_prefill_gate_fused(cfg, params, st, slots, cu, cu_h, px["q"], px["k"], px["v"], f, fb, b, px["g"],
+                                 out, stream)
+
+    res = {}
+    for name, fn in (("separate", separate), ("fused", fused)):
+        for _ in range(3):
+            K.kda_state_reset(st, [0], stream)
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for i in range(reps):
+            K.kda_state_reset(st, [0], stream)
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        res[name] = statistics.median(a.elapsed_time(c) for a, c in ev)
+    assert K.kda_state_poll_error(st) == 0 and int(ws[:4].view(torch.int32).item()) == 0
+    K.kda_state_free(st)
+    del x, px, z, f, out, ws, flush
+    torch.cuda.empty_cache()
+    return {"workload": f"hidden state -> mixer output, 1 sequence T={T}, hidden {HIDDEN}, 96 heads x 128, BF16 I/O "
+                        "(L2 flushed before each call)",
+            "separate_ms": res["separate"], "fused_ms": res["fused"],
+            "separate_calls": "kda_gate_proj + kda_prefill (z written, 24 KB per token, and read back)",
+            "fused_calls": "kda_gate_proj_in + kda_prefill_gate_fused (z = W_fb f formed in the prefill)",
+            "fused_vs_separate": res["separate"] / res["fused"]}
+
+
 def _time_varlen(K, args, cfg, params, gen, dev, stream):
     """Varlen workload: 16 sequences ~U[512, 16384] (seeded lengths), prefill all, snapshot /
     reset / restore sequences 0-7, then 128 batched decode steps; tokens/s of both phases."""
@@ -858,6 +917,7 @@ def run_kda(args):
             line["gpu_launches"] = 3 * args.prefill_reps
     if args.only in ("all", "gate_proj"):
         line["gate_proj"] = _time_gate_proj(K, args, gen, dev, stream)
+        line["gate_prefill"] = _time_gate_prefill(K, args, cfg, params, gen, dev, stream)
         if args.only == "gate_proj":
             line["value"] = line["gate_proj"]["value"]
             line["ms_per_step"] = line["gate_proj"]["ms"]
