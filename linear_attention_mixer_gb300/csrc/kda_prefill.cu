@@ -938,8 +938,37 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 }
             }
         }
-        {   // every warp (warps 0..7 after their read-back) builds a share of the B operand
-            for (int u = tid; u < 256 * (kC / 8); u += 512) {
+        // 6a. The diagonal blocks TD of T = (I + A)^-1, T_RR = (I + A_RR)^-1, by forward substitution
+        //     (threads 0..63, one column each) as soon as the A rows are in M (warps 0, 1, 4 and 5
+        //     read A back: a named barrier over those four), while the other warps write the zero
+        //     blocks of the T tile above the diagonal (columns c >= 16 (r / 16 + 1)) and build the B
+        //     operand.
+        if (warp == 0 || warp == 1 || warp == 4 || warp == 5) named_bar_sync(3, 128);
+        if (tid < kC) {
+            const int R = tid >> 4, j = tid & (kBlk - 1), nR = kBlk * R;
+            float x[kBlk];
+#pragma unroll
+            for (int r = 0; r < kBlk; ++r) {
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < r; ++i) {
+                    if (i & 1) s1 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s1);
+                    else s0 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s0);
+                }
+                x[r] = r == j ? 1.f : (r < j ? 0.f : s0 + s1);
+            }
+            // stored after the loop, so that no shared store sits between the loads of the rows
+#pragma unroll
+            for (int r = 0; r < kBlk; ++r) TD[(nR + r) * kTD + j] = x[r];
+        } else if (tid < 256) {
+            const int u = tid - kC;  // 192 groups of 8 columns, hi and lo parts
+            const int r = u < 96 ? u / 6 : (u < 160 ? kBlk + (u - 96) / 4 : 2 * kBlk + (u - 160) / 2);
+            const int g = u < 96 ? 2 + u % 6 : (u < 160 ? 4 + (u - 96) % 4 : 6 + (u - 160) % 2);
+            st16(tT + tc::kmajor_off(r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
+            st16(tT + tc::kmajor_off(kC + r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
+        }
+        if (tid >= kC) {   // warps 2..15 (after their read-back or zero blocks) build the B operand
+            for (int u = tid - kC; u < 256 * (kC / 8); u += 512 - kC) {
                 const int nn = u & 255, i0 = 8 * (u >> 8);
                 float o[8];
                 if (nn < kD) {
@@ -961,11 +990,9 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             tc::fence_after_sync();
             if (blk_prev) write_wu(blk_prev, (warp >> 2) - 2, 2);
         } else {
-            // 6. T = (I + A)^-1 as BF16 hi and lo parts in the T tile, by blocks of 16 and a two-level
-            //    merge, by warps 0..7 (a 256-thread named barrier between phases). Phase 0: the diagonal
-            //    blocks TD, T_RR = (I + A_RR)^-1, by forward substitution (threads 0..63, one column
-            //    each) while threads 64..255 write the zero blocks above the diagonal (columns
-            //    c >= 16 (r / 16 + 1)) to the tile. With X = rows/columns 0..31 and Y = 32..63,
+            // 6b. T = (I + A)^-1 as BF16 hi and lo parts in the T tile, by blocks of 16 and a two-level
+            //    merge, by warps 0..7 (a 256-thread named barrier between phases), from the diagonal
+            //    blocks TD of 6a. With X = rows/columns 0..31 and Y = 32..63,
             //    T_YX = -T_YY A_YX T_XX, and inside each half T_10 = -T_11 A_10 T_00,
             //    T_32 = -T_33 A_32 T_22. Three phases:
             //      1. Y1_p = A_(2p+1)(2p) T_(2p)(2p) (p = 0, 1), Z0 = A_Y0 T_00, Z1 = A_Y1 T_11;
@@ -977,31 +1004,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             //    the 8 lanes of a quarter warp share their rows and take consecutive column tiles.
             float *T32 = Yv, *Y1 = GL, *Y2 = GL + 2 * kBlk * kBlk;  // T32: [16][kMS], Y1: [2][16][16], Y2: [32][kY2]
             constexpr int kY2 = 36;
-            // phase 0
-            if (tid < kC) {
-                const int R = tid >> 4, j = tid & (kBlk - 1), nR = kBlk * R;
-                float x[kBlk];
-#pragma unroll
-                for (int r = 0; r < kBlk; ++r) {
-                    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                    for (int i = 0; i < r; ++i) {
-                        if (i & 1) s1 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s1);
-                        else s0 = fmaf(-Mm[(nR + r) * kMS + nR + i], x[i], s0);
-                    }
-                    x[r] = r == j ? 1.f : (r < j ? 0.f : s0 + s1);
-                }
-                // stored after the loop, so that no shared store sits between the loads of the rows
-#pragma unroll
-                for (int r = 0; r < kBlk; ++r) TD[(nR + r) * kTD + j] = x[r];
-            } else {
-                const int u = tid - kC;  // 192 groups of 8 columns, hi and lo parts
-                const int r = u < 96 ? u / 6 : (u < 160 ? kBlk + (u - 96) / 4 : 2 * kBlk + (u - 160) / 2);
-                const int g = u < 96 ? 2 + u % 6 : (u < 160 ? 4 + (u - 96) % 4 : 6 + (u - 160) % 2);
-                st16(tT + tc::kmajor_off(r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
-                st16(tT + tc::kmajor_off(kC + r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
-            }
-            named_bar_sync(1, 256);
+            // (phase 0, the diagonal blocks, ran before the barrier)
             // phase 1 (threads 0..191)
             if (tid < 64) {
                 const int p = tid >> 5, rp = (tid >> 2) & 7, ct = tid & 3, o = 2 * kBlk * p;
