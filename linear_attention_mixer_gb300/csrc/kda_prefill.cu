@@ -61,8 +61,9 @@ constexpr int kTcChunkBytes = 131584;
 constexpr int kStageABytes = kOffTB;   // tile A + gamma
 constexpr int kStageBBytes = kOffUp - kOffTB;
 static_assert(kStageBBytes == 49152 && kOffUp + kC * kD * 4 == kTcChunkBytes, "chunk block layout");
-// state_tc_kernel shared memory: S^T hi | S^T lo | U^T hi | U^T lo | stage A | stage B | g/out rows | sums | barriers
-constexpr int kSmST = 0, kSmUT = 65536, kSmA = 98304, kSmB = kSmA + kStageABytes, kSmGY = kSmB + kStageBBytes;
+// state_tc_kernel shared memory: stage A | stage B | g/out rows | sums | barriers (the A
+// operands are in tensor memory)
+constexpr int kSmA = 0, kSmB = kSmA + kStageABytes, kSmGY = kSmB + kStageBBytes;
 constexpr int kSmRed = kSmGY + kC * kD * 2, kSmBar = kSmRed + 4 * kC * 4;
 constexpr int kStateTcSmem = kSmBar + 12 * 8 + 16;
 static_assert(kSmB % 128 == 0 && kSmGY % 128 == 0, "TMA and bulk destinations");
@@ -1240,27 +1241,34 @@ state_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__res
 }
 
 // ---------------------------------------------------------------- state pass on tensor cores
-// One CTA per (sequence, head), warp-specialised, 416 threads. TMEM lane v holds value index v:
-//   D1 = S^T W^T     [v][r]  TMEM columns   0.. 63
-//   D2 = S^T QG^T    [v][r]  TMEM columns  64..127, then += U^T P^T  -> O^T
-//   D3 = S^T         [v][k]  TMEM columns 128..255, the FP32 state (scaled by the chunk's decay
-//                            before MMA2, += U^T KD)
-// S^T and U^T are kept in shared memory as BF16 high and low parts (A operands), and each
-// product that carries the state is formed as hi*hi + lo*hi + hi*lo:
-//   MMA1: [D1 | D2] = S_hi^T [W_hi | QG]^T, D1 += S_lo^T W_hi^T + S_hi^T W_lo^T
-//   MMA2: [D2 | D3] += U_hi^T [P_hi | KDT_hi] + U_lo^T [P_hi | KDT_hi] + U_hi^T [P_lo | KDT_lo]
+// One CTA per (sequence, head), warp-specialised, 416 threads. All A operands live in tensor
+// memory (512 columns; lane v = value index v):
+//   D1  = S^T W^T       [v][r]  columns   0.. 63  (S_hi W_hi + S_lo W_hi)
+//   D2  = S^T QG^T      [v][r]  columns  64..127, then += U^T P^T  -> O^T
+//   D1b = S_hi^T W_lo^T [v][r]  columns 128..191
+//   S^T hi / lo parts   [v][k]  columns 192..255 / 256..319 (BF16 pairs, K = 128)
+//   D3  = S^T           [v][k]  columns 320..447, the FP32 state (scaled by the chunk's decay
+//                               before MMA2, += U^T KD)
+//   U^T hi / lo parts   [v][r]  columns 448..479 / 480..511 (BF16 pairs, K = 64)
+// The products that carry the state, and the output's U term (whose terms cancel when the
+// keys are strongly correlated), are formed as hi*hi + lo*hi + hi*lo (about 16 bits of
+// mantissa); the output's S term takes one BF16 pass:
+//   MMA1: [D1 | D2 | D1b] = S_hi^T [W_hi | QG | W_lo]^T (N = 192), D1 += S_lo^T W_hi^T
+//   MMA2: D3 += U_hi^T KDT_hi + U_lo^T KDT_hi + U_hi^T KDT_lo (committed: the state may be
+//         read), then D2 += U_hi^T P_hi + U_lo^T P_hi + U_hi^T P_lo
 // Roles (each hand-off is an mbarrier; every wait is bounded):
-//   warps 0-7  (state): per chunk, U^T = U' - D1 -> hi/lo (after MMA1), then after MMA2 the
-//              S^T operand refresh from D3 and the next chunk's decay put on D3. Warps w and
-//              w + 4 share lane quarter w % 4 and split the columns in halves.
+//   warps 0-7  (state): per chunk, U^T = U' - D1 - D1b as hi/lo parts (after MMA1), then after
+//              the state products of MMA2 the S^T parts from D3 and the next chunk's decay put
+//              on D3. Warps w and w + 4 share lane quarter w % 4 and split the columns in halves.
 //   warp 8     (issuer, one lane): MMA1 once S^T is ready and D2 has been read out, MMA2 once
 //              U^T is ready; the chunk-block copies (stage A after MMA1, stage B after MMA2),
 //              the gate-row boxes and the L2 prefetches.
 //   warps 9-12 (epilogue): O^T from D2 right after MMA2 (so MMA1 of the next chunk may start),
 //              then the gated RMSNorm and the output box, under the next chunk's products.
-// The serial chain per chunk is MMA1 -> U -> MMA2 -> refresh; the epilogue and the copies
-// run beside it.
+// The serial chain per chunk is MMA1 -> U -> MMA2 (state part) -> refresh; the output product,
+// the epilogue and the copies run beside it.
 constexpr int kStThreads = 416;
+constexpr uint32_t kTD1 = 0, kTD2 = 64, kTD1b = 128, kTSh = 192, kTSl = 256, kTD3 = 320, kTUh = 448, kTUl = 480;
 
 // AND of pred over the `count` threads of named barrier `id` (also a barrier), so that every
 // thread of a group takes the same branch after a bounded wait.
@@ -1277,6 +1285,26 @@ __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred)
         : "memory");
     return r != 0;
 }
+
+// 32 FP32 values of this thread's lane -> BF16 high parts (nearest) and low parts (x - high,
+// nearest), two per 32-bit word (value 2c in the low half of word c), stored to 16 + 16
+// tensor-memory columns starting at t_hi and t_lo (no wait).
+__device__ __forceinline__ void tmem_put_split32(uint32_t t_hi, uint32_t t_lo, const float *x)
+{
+    uint32_t h[16], l[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(x[2 * c], x[2 * c + 1]);
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(&p);
+        h[c] = u;
+        const __nv_bfloat162 q = __floats2bfloat162_rn(x[2 * c] - __uint_as_float(u << 16),
+                                                       x[2 * c + 1] - __uint_as_float(u & 0xFFFF0000u));
+        l[c] = *reinterpret_cast<const uint32_t *>(&q);
+    }
+    tc::tmem_st16u_nowait(t_hi, h);
+    tc::tmem_st16u_nowait(t_lo, l);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kStThreads, 1)
 state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__restrict__ err,
@@ -1290,17 +1318,15 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     static_assert(sizeof(T) == 2, "the tensor-core path reads BF16 gate logits");
     extern __shared__ __align__(1024) float smf[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(smf);
-    unsigned char *sSTh = sm + kSmST, *sSTl = sSTh + 32768;   // S^T [v][k] BF16, K = 128
-    unsigned char *sUTh = sm + kSmUT, *sUTl = sUTh + 16384;   // U^T [v][r] BF16, K = 64
     unsigned char *sA = sm + kSmA, *sB = sm + kSmB;
     const float *sgam = reinterpret_cast<const float *>(sA + kOffGam);
     __nv_bfloat16 *sGY = reinterpret_cast<__nv_bfloat16 *>(sm + kSmGY);  // gate rows, then output rows
     // [64 tokens][4 value quarters] partial sums of squares, added in a fixed order (so that the
     // outputs do not depend on the order the warps finish in)
     float *red = reinterpret_cast<float *>(sm + kSmRed);
-    // [0] stage A landed, [1] stage B landed, [2] MMA1 done, [3] MMA2 done, [4] gate rows landed,
-    // [5] U^T ready (8 warps), [6] S^T ready (8 warps), [7] D2 read out (4 warps), [8] output box
-    // read out of the gate/output buffer (1 thread)
+    // [0] stage A landed, [1] stage B landed, [2] MMA1 done, [3] state products of MMA2 done,
+    // [4] gate rows landed, [5] U^T ready (8 warps), [6] S^T ready (8 warps), [7] D2 read out
+    // (4 warps), [8] output box read out of the gate/output buffer (1 thread), [9] MMA2 done
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kSmBar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 12);
 
@@ -1317,13 +1343,14 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     float *Sg = S_all + ((size_t)slot * H + h) * kD * kD;
     auto block_of = [&](int ci) { return chunks + ((size_t)h * total_chunks + ci) * kTcChunkBytes; };
 
-    if (w == 0) tc::tmem_alloc(tslot, 256);
+    if (w == 0) tc::tmem_alloc(tslot, 512);
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
         mbar_init(&bar[5], 8);
         mbar_init(&bar[6], 8);
         mbar_init(&bar[7], 4);
         mbar_init(&bar[8], 1);
+        mbar_init(&bar[9], 1);
         fence_mbar_init();
     }
     tc::fence_before_sync();
@@ -1336,37 +1363,25 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         // ------------------------------------------------------------ state warps
         const int qtr = w & 3, grp = w >> 2;
         const int vi = 32 * qtr + lane;
-        const uint32_t lanes = (uint32_t)(32 * qtr) << 16;
-        const uint32_t tD1 = tb + lanes, tD3 = tb + lanes + 128;
+        const uint32_t tl = tb + ((uint32_t)(32 * qtr) << 16);   // this warp's lane quarter
         const int k0 = 64 * grp, r0 = 32 * grp;
-        auto put16_split = [](unsigned char *th, unsigned char *tl, int row, int kc, const float *x, int Kd) {
-            uint4 hi, lo;
-            split8(x, hi, lo);
-            st16(th + tc::kmajor_off(row, kc, Kd), hi);
-            st16(tl + tc::kmajor_off(row, kc, Kd), lo);
-            split8(x + 8, hi, lo);
-            st16(th + tc::kmajor_off(row, kc + 8, Kd), hi);
-            st16(tl + tc::kmajor_off(row, kc + 8, Kd), lo);
-        };
         float vals[32];
-        // initial state: S[k][v] -> D3 row v (FP32) and the BF16 operand parts of row v
+        // initial state: S[k][v] -> the S^T parts of row v and D3 row v (FP32, with the first
+        // chunk's decay; stage A brings its gamma)
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
             const int kb = k0 + 32 * half;
 #pragma unroll
             for (int j = 0; j < 32; ++j) vals[j] = Sg[(size_t)(kb + j) * kD + vi];
-            put16_split(sSTh, sSTl, vi, kb, vals, kD);
-            put16_split(sSTh, sSTl, vi, kb + 16, vals + 16, kD);
-            if (n_chunks > 0) {  // the first chunk's decay (stage A brings its gamma)
+            tmem_put_split32(tl + kTSh + kb / 2, tl + kTSl + kb / 2, vals);
+            if (n_chunks > 0) {
                 if (half == 0) good &= mbar_wait_bounded(&bar[0], 0, kTcWaitLimit);
-                const float *gam = sgam + kb;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) vals[j] *= gam[j];
+                for (int j = 0; j < 32; ++j) vals[j] *= sgam[kb + j];
             }
-            tc::tmem_st32(tD3 + kb, vals);
+            tc::tmem_st32(tl + kTD3 + kb, vals);
         }
         tc::tmem_wait_st();
-        tc::fence_smem_to_async();
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[6]);  // S^T of the first chunk is ready
@@ -1383,59 +1398,59 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             if (!(good = mbar_wait_bounded(&bar[2], par, kTcWaitLimit))) break;
             tc::fence_after_sync();
             {   // U^T = U'^T - (W S)^T on this thread's tokens, as BF16 high and low parts
-                uint32_t raw[32];
-                tc::tmem_ld32_nowait(tD1 + r0, raw);
+                uint32_t a[32];
+                tc::tmem_ld32_nowait(tl + kTD1 + r0, a);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) vals[j] = up[j] - __uint_as_float(raw[j]);
-                put16_split(sUTh, sUTl, vi, r0, vals, kC);
-                put16_split(sUTh, sUTl, vi, r0 + 16, vals + 16, kC);
+                for (int j = 0; j < 32; ++j) vals[j] = up[j] - __uint_as_float(a[j]);
+                tc::tmem_ld32_nowait(tl + kTD1b + r0, a);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) vals[j] -= __uint_as_float(a[j]);
+                tmem_put_split32(tl + kTUh + r0 / 2, tl + kTUl + r0 / 2, vals);
             }
-            tc::fence_smem_to_async();
+            tc::tmem_wait_st();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[5]);
             if (!(good = mbar_wait_bounded(&bar[3], par, kTcWaitLimit))) break;
             tc::fence_after_sync();
-            // refresh the S^T operand parts from the updated FP32 state and put the next chunk's
-            // decay on D3 (its gamma arrives with stage A of the next chunk)
-            const bool has_next = it + 1 < n_chunks;
-            if (has_next && !(good = mbar_wait_bounded(&bar[0], (uint32_t)((it + 1) & 1), kTcWaitLimit))) break;
-            {
-                uint32_t raw[32];
+            // the S^T parts from the updated FP32 state, and the next chunk's decay put on D3
+            // (its gamma arrives with stage A of the next chunk, and is read before S^T is handed
+            // over: stage A is refilled once the next MMA1 has run); after the last chunk, the
+            // final state back to HBM, S[k][v] from D3 row v
+            const bool last = it + 1 == n_chunks;
+            if (!last && !(good = mbar_wait_bounded(&bar[0], (uint32_t)((it + 1) & 1), kTcWaitLimit))) break;
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    tc::tmem_ld32_nowait(tD3 + k0 + 32 * half, raw);
-                    tc::tmem_wait_ld();
+            for (int half = 0; half < 2; ++half) {
+                const int kb = k0 + 32 * half;
+                uint32_t raw[32];
+                tc::tmem_ld32_nowait(tl + kTD3 + kb, raw);
+                tc::tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
-                    if (has_next) {
-                        put16_split(sSTh, sSTl, vi, k0 + 32 * half, vals, kD);
-                        put16_split(sSTh, sSTl, vi, k0 + 32 * half + 16, vals + 16, kD);
-                        const float *gam = sgam + k0 + 32 * half;
+                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
+                if (last) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) vals[j] *= gam[j];
-                        tc::tmem_st32(tD3 + k0 + 32 * half, vals);
-                    } else {  // the final state back to HBM: S[k][v] from D3 row v
+                    for (int j = 0; j < 32; ++j) Sg[(size_t)(kb + j) * kD + vi] = vals[j];
+                } else {
+                    tmem_put_split32(tl + kTSh + kb / 2, tl + kTSl + kb / 2, vals);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) Sg[(size_t)(k0 + 32 * half + j) * kD + vi] = vals[j];
-                    }
+                    for (int j = 0; j < 32; ++j) vals[j] *= sgam[kb + j];
+                    tc::tmem_st32(tl + kTD3 + kb, vals);
                 }
-                tc::tmem_wait_st();
             }
-            if (has_next) {
-                tc::fence_smem_to_async();
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[6]);
-            }
+            if (last) break;
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[6]);
         }
         if (!good) atomicExch(err, KDA_ERR_TIMEOUT);
         // new conv history (the last K-1 raw inputs of the sequence)
         if (good && n_chunks > 0 && tid < kD) {
             const int start = table[c_first].t0;
             const int len = table[c_last - 1].t0 + table[c_last - 1].n - start;
-            T *tl = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD + tid;
+            T *tlh = tail_all + (size_t)slot * 3 * (kK - 1) * D + (size_t)h * kD + tid;
             const T *src[3] = {q, k, v};
 #pragma unroll
             for (int x = 0; x < 3; ++x) {
@@ -1443,8 +1458,8 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 for (int j = 0; j < 3; ++j) {
                     const int pos = len - 3 + j;
                     const T val = pos >= 0 ? src[x][(size_t)(start + pos) * D + (size_t)h * kD + tid]
-                                           : tl[(size_t)(x * 3 + (pos + 3)) * D];
-                    tl[(size_t)(x * 3 + j) * D] = val;
+                                           : tlh[(size_t)(x * 3 + (pos + 3)) * D];
+                    tlh[(size_t)(x * 3 + j) * D] = val;
                 }
             }
         }
@@ -1466,17 +1481,18 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             };
             constexpr uint32_t id64 = tc::idesc_bf16(128, 64), id128 = tc::idesc_bf16(128, 128);
             constexpr uint32_t id192 = tc::idesc_bf16(128, 192);
-            const uint64_t dSh = tc::kmajor_desc(sSTh, 0, kD), dSl = tc::kmajor_desc(sSTl, 0, kD);
-            const uint64_t dA = tc::kmajor_desc(sA, 0, kD), dAlo = tc::kmajor_desc(sA + 2 * kC * kD * 2, 0, kD);
-            const uint64_t dUh = tc::kmajor_desc(sUTh, 0, kC), dUl = tc::kmajor_desc(sUTl, 0, kC);
-            const uint64_t dB = tc::kmajor_desc(sB, 0, kC), dBlo = tc::kmajor_desc(sB + 3 * kC * kC * 2, 0, kC);
+            const uint64_t dA = tc::kmajor_desc(sA, 0, kD);                               // W_hi | QG | W_lo
+            const uint64_t dP = tc::kmajor_desc(sB, 0, kC);                               // P_hi
+            const uint64_t dPl = tc::kmajor_desc(sB + tc::kmajor_off(3 * kC, 0, kC), 0, kC);  // P_lo
+            const uint64_t dKh = tc::kmajor_desc(sB + tc::kmajor_off(kC, 0, kC), 0, kC);      // KDT_hi
+            const uint64_t dKl = tc::kmajor_desc(sB + tc::kmajor_off(4 * kC, 0, kC), 0, kC);  // KDT_lo
             issue_a(c_first);
             issue_b(c_first);
             if (n_chunks > 1) prefetch_block(c_first + 1);
             if (n_chunks > 2) prefetch_block(c_first + 2);
             tma_prefetch_2d(&tm_g, h * kD, table[c_first].t0);
             // copies and products in flight when a wait gives up
-            int a_out = 1, b_out = 1, g_out = 0, m1_out = 0, m2_out = 0;
+            int a_out = 1, b_out = 1, m1_out = 0, m2_out = 0;
             for (int it = 0; it < n_chunks && good; ++it) {
                 const int ci = c_first + it;
                 const uint32_t par = (uint32_t)(it & 1);
@@ -1489,11 +1505,9 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 a_out = 0;
                 tc::fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tb, dSh + 16u * kk, dA + 16u * kk, id128, kk > 0);
+                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16_ta(tb + kTD1, tb + kTSh + 8 * kk, dA + 16u * kk, id192, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tb, dSl + 16u * kk, dA + 16u * kk, id64, 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tb, dSh + 16u * kk, dAlo + 16u * kk, id64, 1);
+                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16_ta(tb + kTD1, tb + kTSl + 8 * kk, dA + 16u * kk, id64, 1);
                 tc::mma_commit(&bar[2]);
                 m1_out = 1;
                 if (!(good = mbar_wait_bounded(&bar[2], par, kTcWaitLimit))) break;
@@ -1503,20 +1517,27 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                     issue_a(ci + 1);
                     a_out = 1;
                 }
-                // MMA2: U^T ready, stage B landed
+                // MMA2: U^T ready, stage B landed; the state products first
                 good = mbar_wait_bounded(&bar[5], par, kTcWaitLimit) && mbar_wait_bounded(&bar[1], par, kTcWaitLimit);
                 if (!good) break;
                 b_out = 0;
                 tc::fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tb + 64, dUh + 16u * kk, dB + 16u * kk, id192, 1);
+                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tb + kTD3, tb + kTUh + 8 * kk, dKh + 16u * kk, id128, 1);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tb + 64, dUl + 16u * kk, dB + 16u * kk, id192, 1);
+                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tb + kTD3, tb + kTUl + 8 * kk, dKh + 16u * kk, id128, 1);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tb + 64, dUh + 16u * kk, dBlo + 16u * kk, id192, 1);
+                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tb + kTD3, tb + kTUh + 8 * kk, dKl + 16u * kk, id128, 1);
                 tc::mma_commit(&bar[3]);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tb + kTD2, tb + kTUh + 8 * kk, dP + 16u * kk, id64, 1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tb + kTD2, tb + kTUl + 8 * kk, dP + 16u * kk, id64, 1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tb + kTD2, tb + kTUh + 8 * kk, dPl + 16u * kk, id64, 1);
+                tc::mma_commit(&bar[9]);
                 m2_out = 1;
-                if (!(good = mbar_wait_bounded(&bar[3], par, kTcWaitLimit))) break;
+                if (!(good = mbar_wait_bounded(&bar[9], par, kTcWaitLimit))) break;
                 m2_out = 0;
                 if (it + 1 < n_chunks) {
                     issue_b(ci + 1);
@@ -1526,7 +1547,6 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 if (!(good = mbar_wait_bounded(&bar[8], par, kTcWaitLimit))) break;
                 mbar_arrive_expect_tx(&bar[4], (uint32_t)(box_rows * kD * sizeof(T)));
                 tma_load_2d(sGY, &tm_g, h * kD, table[ci].t0, &bar[4]);
-                g_out = 1;
             }
             if (!good) {
                 atomicExch(err, KDA_ERR_TIMEOUT);
@@ -1535,8 +1555,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 if (a_out) mbar_wait_bounded(&bar[0], 0, kTcWaitLimit);
                 if (b_out) mbar_wait_bounded(&bar[1], 0, kTcWaitLimit);
                 if (m1_out) mbar_wait_bounded(&bar[2], 0, kTcWaitLimit);
-                if (m2_out) mbar_wait_bounded(&bar[3], 0, kTcWaitLimit);
-                (void)g_out;
+                if (m2_out) mbar_wait_bounded(&bar[9], 0, kTcWaitLimit);
             }
         }
         __syncwarp();
@@ -1554,7 +1573,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             const int ci = c_first + it;
             const uint32_t par = (uint32_t)(it & 1);
             const ChunkEntry e = table[ci];
-            if (!bar_and(2, 128, mbar_wait_bounded(&bar[3], par, kTcWaitLimit))) { good = false; break; }
+            if (!bar_and(2, 128, mbar_wait_bounded(&bar[9], par, kTcWaitLimit))) { good = false; break; }
             tc::fence_after_sync();
             float o[64];
             {
@@ -1631,7 +1650,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (w == 0) tc::tmem_dealloc(tb, 256);
+    if (w == 0) tc::tmem_dealloc(tb, 512);
 }
 
 // ---------------------------------------------------------------- epilogue

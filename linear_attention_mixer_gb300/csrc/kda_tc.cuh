@@ -96,6 +96,20 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A * B^T with A read from tensor memory: row m of A in lane m, its K values
+// two BF16 per 32-bit column (element 2c in the low half of column c), so one K step of 16
+// is 8 columns starting at a_tmem. B is a shared-memory descriptor as in mma_bf16.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on the mbarrier when every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
@@ -189,6 +203,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v)
 }
 
 // TMEM address of (lane, column) relative to an allocation base.
+// 16 consecutive 32-bit columns of this thread's lane, raw words, no wait.
+__device__ __forceinline__ void tmem_st16u_nowait(uint32_t taddr, const uint32_t *v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int lane, int col)
 {
     return base + ((uint32_t)lane << 16) + (uint32_t)col;
