@@ -64,7 +64,7 @@ static_assert(kStageBBytes == 49152 && kOffUp + kC * kD * 4 == kTcChunkBytes, "c
 // state_tc_kernel shared memory: stage A | stage B | g/out rows | sums | barriers (the A
 // operands are in tensor memory)
 constexpr int kSmA = 0, kSmB = kSmA + kStageABytes, kSmGY = kSmB + kStageBBytes;
-constexpr int kSmRed = kSmGY + kC * kD * 2, kSmBar = kSmRed + 4 * kC * 4;
+constexpr int kSmRed = kSmGY + kC * kD * 2, kSmGam = kSmRed + 4 * kC * 4, kSmBar = kSmGam + 2 * kD * 4;
 constexpr int kStateTcSmem = kSmBar + 12 * 8 + 16;
 static_assert(kSmB % 128 == 0 && kSmGY % 128 == 0, "TMA and bulk destinations");
 static_assert(kStateTcSmem <= 232448, "state_tc_kernel shared memory");
@@ -1270,6 +1270,29 @@ state_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__res
 constexpr int kStThreads = 416;
 constexpr uint32_t kTD1 = 0, kTD2 = 64, kTD1b = 128, kTSh = 192, kTSl = 256, kTD3 = 320, kTUh = 448, kTUl = 480;
 
+// Two FP32 operations in one instruction (each half rounded as the scalar operation would be).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<const uint64_t *>(&a)),
+        "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<const uint64_t *>(&a)),
+        "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(*reinterpret_cast<const uint64_t *>(&a)),
+        "l"(*reinterpret_cast<const uint64_t *>(&b)), "l"(*reinterpret_cast<const uint64_t *>(&c)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
 // AND of pred over the `count` threads of named barrier `id` (also a barrier), so that every
 // thread of a group takes the same branch after a bounded wait.
 __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred)
@@ -1319,7 +1342,9 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
     extern __shared__ __align__(1024) float smf[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(smf);
     unsigned char *sA = sm + kSmA, *sB = sm + kSmB;
-    const float *sgam = reinterpret_cast<const float *>(sA + kOffGam);
+    // exp(G_last) of chunk it in slot it % 2 (its own copy, so that stage A can be refilled
+    // before the decay has been put on the state)
+    const float *sgam2 = reinterpret_cast<const float *>(sm + kSmGam);
     __nv_bfloat16 *sGY = reinterpret_cast<__nv_bfloat16 *>(sm + kSmGY);  // gate rows, then output rows
     // [64 tokens][4 value quarters] partial sums of squares, added in a fixed order (so that the
     // outputs do not depend on the order the warps finish in)
@@ -1377,7 +1402,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             if (n_chunks > 0) {
                 if (half == 0) good &= mbar_wait_bounded(&bar[0], 0, kTcWaitLimit);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) vals[j] *= sgam[kb + j];
+                for (int j = 0; j < 32; ++j) vals[j] *= sgam2[kb + j];
             }
             tc::tmem_st32(tl + kTD3 + kb, vals);
         }
@@ -1415,35 +1440,47 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             if (lane == 0) mbar_arrive(&bar[5]);
             if (!(good = mbar_wait_bounded(&bar[3], par, kTcWaitLimit))) break;
             tc::fence_after_sync();
-            // the S^T parts from the updated FP32 state, and the next chunk's decay put on D3
-            // (its gamma arrives with stage A of the next chunk, and is read before S^T is handed
-            // over: stage A is refilled once the next MMA1 has run); after the last chunk, the
-            // final state back to HBM, S[k][v] from D3 row v
+            // the S^T parts from the updated FP32 state, handed over first; then the next chunk's
+            // decay put on D3 (MMA2 of the next chunk follows this warp's U^T hand-off, after its
+            // wait on these stores); after the last chunk, the final state back to HBM
             const bool last = it + 1 == n_chunks;
-            if (!last && !(good = mbar_wait_bounded(&bar[0], (uint32_t)((it + 1) & 1), kTcWaitLimit))) break;
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                const int kb = k0 + 32 * half;
+            float v0[32], v1[32];
+            {
                 uint32_t raw[32];
-                tc::tmem_ld32_nowait(tl + kTD3 + kb, raw);
+                tc::tmem_ld32_nowait(tl + kTD3 + k0, raw);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
-                if (last) {
+                for (int j = 0; j < 32; ++j) v0[j] = __uint_as_float(raw[j]);
+                tc::tmem_ld32_nowait(tl + kTD3 + k0 + 32, raw);
+                tc::tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) Sg[(size_t)(kb + j) * kD + vi] = vals[j];
-                } else {
-                    tmem_put_split32(tl + kTSh + kb / 2, tl + kTSl + kb / 2, vals);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) vals[j] *= sgam[kb + j];
-                    tc::tmem_st32(tl + kTD3 + kb, vals);
-                }
+                for (int j = 0; j < 32; ++j) v1[j] = __uint_as_float(raw[j]);
             }
-            if (last) break;
+            if (last) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) Sg[(size_t)(k0 + j) * kD + vi] = v0[j];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) Sg[(size_t)(k0 + 32 + j) * kD + vi] = v1[j];
+                break;
+            }
+            tmem_put_split32(tl + kTSh + k0 / 2, tl + kTSl + k0 / 2, v0);
+            tmem_put_split32(tl + kTSh + k0 / 2 + 16, tl + kTSl + k0 / 2 + 16, v1);
+            // the next chunk's stage A (and its gamma) has landed: waited on before the hand-off,
+            // since the issuer may refill stage A once the next MMA1 has run
+            if (!(good = mbar_wait_bounded(&bar[0], (uint32_t)((it + 1) & 1), kTcWaitLimit))) break;
             tc::tmem_wait_st();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[6]);
+            {
+                const float *gam = sgam2 + ((it + 1) & 1) * kD + k0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v0[j] *= gam[j];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v1[j] *= gam[32 + j];
+                tc::tmem_st32(tl + kTD3 + k0, v0);
+                tc::tmem_st32(tl + kTD3 + k0 + 32, v1);
+            }
         }
         if (!good) atomicExch(err, KDA_ERR_TIMEOUT);
         // new conv history (the last K-1 raw inputs of the sequence)
@@ -1468,7 +1505,8 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
         if (lane == 0 && n_chunks > 0) {
             auto issue_a = [&](int ci) {
                 mbar_arrive_expect_tx(&bar[0], kStageABytes);
-                bulk_g2s(sA, block_of(ci) + kOffTA, kStageABytes, &bar[0]);
+                bulk_g2s(sA, block_of(ci) + kOffTA, kOffGam - kOffTA, &bar[0]);
+                bulk_g2s(sm + kSmGam + ((ci - c_first) & 1) * kD * 4, block_of(ci) + kOffGam, kD * 4, &bar[0]);
             };
             auto issue_b = [&](int ci) {
                 mbar_arrive_expect_tx(&bar[1], kStageBBytes);
@@ -1588,23 +1626,31 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[7]);  // D2 is free for the next chunk's MMA1
             // sums of squares over this warp's 32 v for each token: a reduce-scatter butterfly per
-            // 32 tokens (31 shuffles) leaves the sum of token 32 hf + lane in lane `lane`
+            // 32 tokens (31 shuffles) leaves the sum of token 32 hf + lane in lane `lane`; values
+            // 2j and 2j + 1 travel as a pair while they move together (offsets 16 .. 2)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                float sq[32];
+                float2 sq[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) sq[j] = o[32 * hf + j] * o[32 * hf + j];
+                for (int j = 0; j < 16; ++j) {
+                    const float2 x = make_float2(o[32 * hf + 2 * j], o[32 * hf + 2 * j + 1]);
+                    sq[j] = mul2(x, x);
+                }
 #pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) {
+                for (int off = 16; off >= 2; off >>= 1) {
                     const bool upper = (lane & off) != 0;
 #pragma unroll
-                    for (int j = 0; j < off; ++j) {
-                        const float keep = upper ? sq[j + off] : sq[j];
-                        const float send = upper ? sq[j] : sq[j + off];
-                        sq[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    for (int j = 0; j < off / 2; ++j) {
+                        const float2 keep = upper ? sq[j + off / 2] : sq[j];
+                        const float2 send = upper ? sq[j] : sq[j + off / 2];
+                        const float2 recv = make_float2(__shfl_xor_sync(0xffffffffu, send.x, off),
+                                                        __shfl_xor_sync(0xffffffffu, send.y, off));
+                        sq[j] = add2(keep, recv);
                     }
                 }
-                red[(32 * hf + lane) * 4 + qe] = sq[0];
+                const bool upper = (lane & 1) != 0;
+                const float keep = upper ? sq[0].y : sq[0].x, send = upper ? sq[0].x : sq[0].y;
+                red[(32 * hf + lane) * 4 + qe] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
             }
             // (the AND is also the barrier after every warp's sums are in red)
             if (!bar_and(2, 128, mbar_wait_bounded(&bar[4], par, kTcWaitLimit))) { good = false; break; }
@@ -1616,14 +1662,20 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 rinv_l[hf] = rsqrt_ftz(((pl.x + pl.y) + (pl.z + pl.w)) * (1.0f / kD) + rms_eps);
             }
             __nv_bfloat16 y[64];
+            const float2 half2 = make_float2(0.5f, 0.5f), nw2 = make_float2(nw, nw);
 #pragma unroll
-            for (int r = 0; r < 64; ++r) {
-                const float rinv = __shfl_sync(0xFFFFFFFFu, rinv_l[r >> 5], r & 31);
-                const float gv = __bfloat162float(sGY[r * kD + vi]);
+            for (int r = 0; r < 64; r += 2) {  // tokens r and r + 1 as a pair
+                const float2 rinv = make_float2(__shfl_sync(0xFFFFFFFFu, rinv_l[r >> 5], r & 31),
+                                                __shfl_sync(0xFFFFFFFFu, rinv_l[r >> 5], (r + 1) & 31));
+                const float2 gv = make_float2(__bfloat162float(sGY[r * kD + vi]), __bfloat162float(sGY[(r + 1) * kD + vi]));
                 // sigmoid(g) = (1 + tanh(g/2)) / 2; the hardware tanh's error is below the BF16
                 // rounding of the output it multiplies
-                const float sg = fmaf(0.5f, tanh_approx(0.5f * gv), 0.5f);
-                y[r] = __float2bfloat16_rn(sg * nw * (o[r] * rinv));
+                const float2 hg = mul2(half2, gv);
+                const float2 sg = fma2(half2, make_float2(tanh_approx(hg.x), tanh_approx(hg.y)), half2);
+                const float2 yy = mul2(mul2(sg, nw2), mul2(make_float2(o[r], o[r + 1]), rinv));
+                const __nv_bfloat162 yb = __floats2bfloat162_rn(yy.x, yy.y);
+                y[r] = yb.x;
+                y[r + 1] = yb.y;
             }
             if (e.n == kC) {  // each thread overwrites only the gate values it has read
 #pragma unroll
