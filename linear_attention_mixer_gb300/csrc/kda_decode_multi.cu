@@ -34,14 +34,16 @@ struct MultiStage {
 constexpr uint32_t kMultiWaitLimit = 1u << 26;
 
 // NST stage buffers per CTA. NST = 1 fits two CTAs (two units) on an SM, so that one unit's
-// serial token chain overlaps the other's; NST = 2 keeps one CTA per SM and prefetches its
-// next unit instead.
-template <typename T, int NST>
+// serial token chain overlaps the other's, and requests the next unit's copy as soon as the
+// prologue has read the stage (the copy then lands under the token chain); NST = 2 keeps one
+// CTA per SM and prefetches its next unit a whole unit ahead. n, the tokens per sequence, is a
+// template parameter so that the prologue's token loop unrolls.
+template <typename T, int NST, int n>
 __global__ void __launch_bounds__(256, 3 - NST)
 decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
                     const float *__restrict__ A_log, const float *__restrict__ norm_w,
                     float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__restrict__ err,
-                    const int32_t *__restrict__ slots, int B, int n, int H, int max_slots,
+                    const int32_t *__restrict__ slots, int B, int H, int max_slots,
                     const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                     const T *__restrict__ z, const T *__restrict__ bl, const T *__restrict__ g,
                     T *__restrict__ out, float gmin, float l2_eps, float rms_eps, float q_scale)
@@ -100,7 +102,6 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
     for (int u = u_begin; u < u_end; ++u, ++it) {
         const int stage = NST == 2 ? (it & 1) : 0;
         if (NST == 2 && tid == 0 && u + 1 < u_end) issue(stage ^ 1, u + 1);  // the other stage is free
-        if (NST == 1 && tid == 0 && it > 0) issue(0, u);  // the previous unit ended with a barrier
         const int h = u / B, r = u - (u / B) * B;
         const int slot = slots[r];
         const bool bad = slot < 0 || slot >= max_slots;
@@ -120,6 +121,7 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
         if (bad) {
             if (tid == 0) atomicExch(err, kErrBadSlot);
             __syncthreads();
+            if (NST == 1 && tid == 0 && u + 1 < u_end) issue(0, u + 1);
             continue;
         }
         const unsigned char *st = smem + stage * L::kBytes;
@@ -142,38 +144,62 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
                 return j >= 0 ? IO<T>::ld(in + (x * KDA_DECODE_MAX_TOKENS + j) * kD + i)
                               : IO<T>::ld(tl + (x * 3 + (j + 3)) * kD + i);
             };
-            for (int t = tg; t < n; t += 2) {
-                float y[3];
+            // the new history (the last three raw inputs) leaves now, so that the stage is free
+            // once the prologue is done
+            if (tid < kD) {
+                T *tg_out = tail_all + (size_t)slot * 9 * D + (size_t)h * kD + tid;
 #pragma unroll
                 for (int x = 0; x < 3; ++x)
-                    y[x] = silu_ftz(fmaf(wt[x].x, raw(x, t - 3), fmaf(wt[x].y, raw(x, t - 2),
-                                  fmaf(wt[x].z, raw(x, t - 1), wt[x].w * raw(x, t)))));
-                sh_q[t * kD + i] = y[0];
-                sh_k[t * kD + i] = y[1];
-                sh_v[t * kD + i] = y[2];
-                sh_a[t * kD + i] = exp_ftz(gmin * sigmoid_ftz(eA * (IO<T>::ld(in + (3 * KDA_DECODE_MAX_TOKENS + t) * kD + i) + dti)));
-                sh_gw[t * kD + i] = sigmoid_ftz(IO<T>::ld(in + (4 * KDA_DECODE_MAX_TOKENS + t) * kD + i)) * nwi;
-                const float a0 = warp_sum(y[0] * y[0]), a1 = warp_sum(y[1] * y[1]), a2 = warp_sum(y[0] * y[1]);
-                if (l == 0) { part[t * 12 + (w & 3)] = a0; part[t * 12 + 4 + (w & 3)] = a1; part[t * 12 + 8 + (w & 3)] = a2; }
+#pragma unroll
+                    for (int j = 0; j < 3; ++j) {
+                        const int tok = n - 3 + j;
+                        tg_out[(size_t)(x * 3 + j) * D] = tok >= 0 ? in[(x * KDA_DECODE_MAX_TOKENS + tok) * kD + tid]
+                                                                   : tl[(x * 3 + (tok + 3)) * kD + tid];
+                    }
+            }
+#pragma unroll
+            for (int jt = 0; jt < (n + 1) / 2; ++jt) {
+                const int t = tg + 2 * jt;
+                if (t < n) {  // uniform per warp
+                    float y[3];
+#pragma unroll
+                    for (int x = 0; x < 3; ++x)
+                        y[x] = silu_ftz(fmaf(wt[x].x, raw(x, t - 3), fmaf(wt[x].y, raw(x, t - 2),
+                                      fmaf(wt[x].z, raw(x, t - 1), wt[x].w * raw(x, t)))));
+                    sh_q[t * kD + i] = y[0];
+                    sh_k[t * kD + i] = y[1];
+                    sh_v[t * kD + i] = y[2];
+                    sh_a[t * kD + i] = exp_ftz(gmin * sigmoid_ftz(eA * (IO<T>::ld(in + (3 * KDA_DECODE_MAX_TOKENS + t) * kD + i) + dti)));
+                    sh_gw[t * kD + i] = sigmoid_ftz(IO<T>::ld(in + (4 * KDA_DECODE_MAX_TOKENS + t) * kD + i)) * nwi;
+                    const float a0 = warp_sum(y[0] * y[0]), a1 = warp_sum(y[1] * y[1]), a2 = warp_sum(y[0] * y[1]);
+                    if (l == 0) { part[t * 12 + (w & 3)] = a0; part[t * 12 + 4 + (w & 3)] = a1; part[t * 12 + 8 + (w & 3)] = a2; }
+                }
             }
             __syncthreads();
-            for (int t = tg; t < n; t += 2) {
-                const float *pt = part + t * 12;
-                const float rq = q_scale * rsqrt_ftz((pt[0] + pt[1] + pt[2] + pt[3]) + l2_eps);
-                const float rk = rsqrt_ftz((pt[4] + pt[5] + pt[6] + pt[7]) + l2_eps);
-                const float kn = sh_k[t * kD + i] * rk, qn = sh_q[t * kD + i] * rq, a = sh_a[t * kD + i];
-                sh_k[t * kD + i] = kn;
-                if constexpr (NST == 2) {
-                    sh_ak[t * kD + i] = a * kn;
-                    sh_aq[t * kD + i] = a * qn;
-                } else {
-                    sh_q[t * kD + i] = qn;
+#pragma unroll
+            for (int jt = 0; jt < (n + 1) / 2; ++jt) {
+                const int t = tg + 2 * jt;
+                if (t < n) {
+                    const float *pt = part + t * 12;
+                    const float rq = q_scale * rsqrt_ftz((pt[0] + pt[1] + pt[2] + pt[3]) + l2_eps);
+                    const float rk = rsqrt_ftz((pt[4] + pt[5] + pt[6] + pt[7]) + l2_eps);
+                    const float kn = sh_k[t * kD + i] * rk, qn = sh_q[t * kD + i] * rq, a = sh_a[t * kD + i];
+                    sh_k[t * kD + i] = kn;
+                    if constexpr (NST == 2) {
+                        sh_ak[t * kD + i] = a * kn;
+                        sh_aq[t * kD + i] = a * qn;
+                    } else {
+                        sh_q[t * kD + i] = qn;
+                    }
                 }
             }
             __syncthreads();
         }
+        // the stage has been read (state, inputs and history): the next unit's copy may land in it
+        if (NST == 1 && tid == 0 && u + 1 < u_end) issue(0, u + 1);
 
         // the tokens in order
+#pragma unroll 1
         for (int t = 0; t < n; ++t) {
             const size_t row = (size_t)r * n + t;
             const float *pt = part + t * 12;
@@ -185,22 +211,11 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
                                            sh_k + t * kD, sh_v + t * kD, sh_gw + t * kD, sbeta[t], kq, red, su, so,
                                            out + row * D + (size_t)h * kD, rms_eps, w, l);
         }
-        // the state after the run, and the new history (the last three raw inputs)
+        // the state after the run
         float4 *S4 = reinterpret_cast<float4 *>(S_all + ((size_t)slot * H + h) * kD * kD);
 #pragma unroll
         for (int m = 0; m < 16; ++m) st_stream(S4 + (16 * w + m) * 32 + l, s[m]);
-        if (tid < kD) {
-            T *tg_out = tail_all + (size_t)slot * 9 * D + (size_t)h * kD + tid;
-#pragma unroll
-            for (int x = 0; x < 3; ++x)
-#pragma unroll
-                for (int j = 0; j < 3; ++j) {
-                    const int tok = n - 3 + j;
-                    tg_out[(size_t)(x * 3 + j) * D] = tok >= 0 ? in[(x * KDA_DECODE_MAX_TOKENS + tok) * kD + tid]
-                                                               : tl[(x * 3 + (tok + 3)) * kD + tid];
-                }
-        }
-        __syncthreads();  // the stage, the prologue arrays and the partials are free
+        __syncthreads();  // the prologue arrays and the partials are free (and, NST = 2, the stage)
     }
     if (timed_out) {
         if (tid == 0) {
@@ -214,8 +229,8 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
     }
 }
 
-template <typename T, int NST>
-cudaError_t launch_multi_typed(const State &st, const kda_layer_params &p, const int32_t *slots, int B, int n,
+template <typename T, int NST, int n>
+cudaError_t launch_multi_typed(const State &st, const kda_layer_params &p, const int32_t *slots, int B,
                                const void *q, const void *k, const void *v, const void *z, const void *b,
                                const void *g, void *out, cudaStream_t stream)
 {
@@ -224,16 +239,15 @@ cudaError_t launch_multi_typed(const State &st, const kda_layer_params &p, const
     const int H = c.num_heads;
     const size_t smem = NST * (size_t)L::kBytes + (NST == 2 ? 7 : 5) * KDA_DECODE_MAX_TOKENS * kD * 4 + 2 * kD * 4 +
                         kRedFloats * 4 + KDA_DECODE_MAX_TOKENS * 13 * 4 + 2 * 8;
-    cudaError_t e = raise_smem_once(st, sizeof(T) == 2 ? kSmemMultiBf16 : kSmemMultiF32,
-                                    decode_multi_kernel<T, NST>, smem);
+    cudaError_t e = raise_smem_once(st, smem_bit_multi(sizeof(T) == 4, n), decode_multi_kernel<T, NST, n>, smem);
     if (e != cudaSuccess) return e;
     int sms = 0;
     if ((e = state_sms(st, &sms)) != cudaSuccess) return e;
     const int n_units = B * H;
     const int ctas = (3 - NST) * sms;  // CTAs resident at once
     const int grid = n_units < ctas ? n_units : ctas;
-    decode_multi_kernel<T, NST><<<grid, 256, smem, stream>>>(
-        p.conv_w, p.dt_bias, p.A_log, p.norm_w, st.S, (T *)st.tail, st.err, slots, B, n, H, st.max_slots,
+    decode_multi_kernel<T, NST, n><<<grid, 256, smem, stream>>>(
+        p.conv_w, p.dt_bias, p.A_log, p.norm_w, st.S, (T *)st.tail, st.err, slots, B, H, st.max_slots,
         (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, (const T *)g, (T *)out,
         c.gate_lower_bound, c.l2_eps, c.rms_eps, c.q_scale);
     return cudaGetLastError();
@@ -245,9 +259,23 @@ cudaError_t launch_decode_multi(const State &st, const kda_layer_params &p, cons
                                 const void *q, const void *k, const void *v, const void *z, const void *b,
                                 const void *g, void *out, cudaStream_t stream)
 {
-    if (st.cfg.io_dtype == KDA_BF16)
-        return launch_multi_typed<__nv_bfloat16, 1>(st, p, slots, B, n, q, k, v, z, b, g, out, stream);
-    return launch_multi_typed<float, 2>(st, p, slots, B, n, q, k, v, z, b, g, out, stream);
+#define KDA_MULTI_CASE(N)                                                                                   \
+    case N:                                                                                                 \
+        return st.cfg.io_dtype == KDA_BF16                                                                  \
+                   ? launch_multi_typed<__nv_bfloat16, 1, N>(st, p, slots, B, q, k, v, z, b, g, out, stream) \
+                   : launch_multi_typed<float, 2, N>(st, p, slots, B, q, k, v, z, b, g, out, stream);
+    switch (n) {
+        KDA_MULTI_CASE(1)
+        KDA_MULTI_CASE(2)
+        KDA_MULTI_CASE(3)
+        KDA_MULTI_CASE(4)
+        KDA_MULTI_CASE(5)
+        KDA_MULTI_CASE(6)
+        KDA_MULTI_CASE(7)
+        KDA_MULTI_CASE(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef KDA_MULTI_CASE
 }
 
 }  // namespace kda

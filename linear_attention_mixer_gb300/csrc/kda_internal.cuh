@@ -35,9 +35,11 @@ struct State {
 };
 
 enum : uint32_t {
-    kSmemDecodeBf16 = 1u << 0, kSmemDecodeF32 = 1u << 1, kSmemMultiBf16 = 1u << 2, kSmemMultiF32 = 1u << 3,
-    kSmemPrepTc = 1u << 4, kSmemPrepF32 = 1u << 5, kSmemStateTc = 1u << 6, kSmemStateF32 = 1u << 7,
+    kSmemDecodeBf16 = 1u << 0, kSmemDecodeF32 = 1u << 1, kSmemPrepTc = 1u << 4, kSmemPrepF32 = 1u << 5,
+    kSmemStateTc = 1u << 6, kSmemStateF32 = 1u << 7,
 };
+// the multi-token decode has one kernel per (I/O type, tokens per call n = 1 .. 8): bits 8 .. 23
+constexpr uint32_t smem_bit_multi(bool f32, int n) { return 1u << (8 + 2 * (n - 1) + (f32 ? 1 : 0)); }
 
 // Raise `kernel`'s dynamic shared-memory limit to `bytes` once per state.
 template <typename Fn>
