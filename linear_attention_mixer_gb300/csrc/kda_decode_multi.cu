@@ -10,10 +10,10 @@
 // u = beta (v - (Diag(a) S)^T k), the readout o = S'^T q and the gated RMSNorm);
 // the conv history slides through the run in registers.
 //
-// One CTA per SM walks a contiguous range of units (head-major); the state, the
-// n input rows of each of q,k,v,z,g and the history of the next unit arrive by
-// bulk copies into the other of two shared-memory stages while the current unit
-// is computed. The per-token state step is the single-token decode's
+// One CTA per SM walks a contiguous range of units (head-major); the state (one bulk
+// copy), the n input rows of each of q,k,v,z,g (one 2-D TMA box per stream: the rows of
+// one sequence are consecutive) and the history (one box of its 9 rows) of the next unit
+// arrive in a shared-memory stage while the current unit is computed. The per-token state step is the single-token decode's
 // (kda_decode_common.cuh): warp w owns state rows 16w .. 16w+15, lane l columns 4l..4l+3.
 #include "kda_decode_common.cuh"
 #include "kda_internal.cuh"
@@ -46,7 +46,10 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
                     const int32_t *__restrict__ slots, int B, int H, int max_slots,
                     const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                     const T *__restrict__ z, const T *__restrict__ bl, const T *__restrict__ g,
-                    T *__restrict__ out, float gmin, float l2_eps, float rms_eps, float q_scale)
+                    T *__restrict__ out, float gmin, float l2_eps, float rms_eps, float q_scale,
+                    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
+                    const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_tail)
 {
     using L = MultiStage<T>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -68,7 +71,7 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
     const int u_end = min(n_units, u_begin + per);
     if (u_begin >= u_end) return;
     const size_t D = (size_t)H * kD;
-    const T *src5[5] = {q, k, v, z, g};
+    const CUtensorMap *tm5[5] = {&tm_q, &tm_k, &tm_v, &tm_z, &tm_g};
 
     if (tid == 0) {
         for (int i = 0; i < NST; ++i) mbar_init(&bar[i], 1);
@@ -87,13 +90,9 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
         }
         mbar_arrive_expect_tx(&bar[stage], (uint32_t)(L::kS + (5 * n + 9) * L::kRow));
         bulk_g2s_hint(st, S_all + ((size_t)slot * H + h) * kD * kD, L::kS, &bar[stage], pol);
-        for (int x = 0; x < 5; ++x)
-            for (int t = 0; t < n; ++t)
-                bulk_g2s(st + L::kS + (x * KDA_DECODE_MAX_TOKENS + t) * L::kRow,
-                         src5[x] + ((size_t)r * n + t) * D + (size_t)h * kD, L::kRow, &bar[stage]);
-        for (int e = 0; e < 9; ++e)
-            bulk_g2s(st + L::kS + L::kIn + e * L::kRow, tail_all + ((size_t)slot * 9 + e) * D + (size_t)h * kD,
-                     L::kRow, &bar[stage]);
+        for (int x = 0; x < 5; ++x)  // rows r n .. r n + n - 1, channels of head h
+            tma_load_2d(st + L::kS + x * KDA_DECODE_MAX_TOKENS * L::kRow, tm5[x], h * kD, r * n, &bar[stage]);
+        tma_load_2d(st + L::kS + L::kIn, &tm_tail, h * kD, slot * 9, &bar[stage]);
     };
 
     if (tid == 0) issue(0, u_begin);
@@ -243,13 +242,22 @@ cudaError_t launch_multi_typed(const State &st, const kda_layer_params &p, const
     if (e != cudaSuccess) return e;
     int sms = 0;
     if ((e = state_sms(st, &sms)) != cudaSuccess) return e;
+    // one map per input stream ([B n][H d] rows, boxes of n rows x one head) and one for the
+    // conv history ([slots 9][H d] rows, boxes of 9 rows x one head)
+    const int64_t D = (int64_t)H * kD;
+    CUtensorMap tm[6];
+    const void *src[5] = {q, k, v, z, g};
+    for (int x = 0; x < 5; ++x)
+        if ((e = encode_rows_box(&tm[x], src[x], (int)sizeof(T), (int64_t)B * n, D, kD, n)) != cudaSuccess) return e;
+    if ((e = encode_rows_box(&tm[5], st.tail, (int)sizeof(T), (int64_t)st.max_slots * 9, D, kD, 9)) != cudaSuccess)
+        return e;
     const int n_units = B * H;
     const int ctas = (3 - NST) * sms;  // CTAs resident at once
     const int grid = n_units < ctas ? n_units : ctas;
     decode_multi_kernel<T, NST, n><<<grid, 256, smem, stream>>>(
         p.conv_w, p.dt_bias, p.A_log, p.norm_w, st.S, (T *)st.tail, st.err, slots, B, H, st.max_slots,
         (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)b, (const T *)g, (T *)out,
-        c.gate_lower_bound, c.l2_eps, c.rms_eps, c.q_scale);
+        c.gate_lower_bound, c.l2_eps, c.rms_eps, c.q_scale, tm[0], tm[1], tm[2], tm[3], tm[4], tm[5]);
     return cudaGetLastError();
 }
 

@@ -2,6 +2,8 @@
 // Not part of the public ABI (that is include/kda.h).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -59,6 +61,41 @@ inline cudaError_t state_sms(const State &st, int *sms)
         return cudaSuccess;
     }
     return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, st.device);
+}
+
+// cuTensorMapEncodeTiled, looked up once from the driver through the runtime (the library does
+// not link the driver library itself); null when the driver offers none.
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            fn = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }();
+    return encode;
+}
+
+// Tensor map of a row-major [rows][cols] matrix of BF16 (elem_bytes 2) or FP32 (4) values, for
+// 2-D boxes of box_cols x box_rows with no swizzle. The base must be 16-byte aligned and a row
+// a multiple of 16 bytes.
+inline cudaError_t encode_rows_box(CUtensorMap *m, const void *base, int elem_bytes, int64_t rows, int64_t cols,
+                                   int box_cols, int box_rows)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * (cuuint64_t)elem_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r =
+        encode(m, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 // ---------------------------------------------------------------- IO types

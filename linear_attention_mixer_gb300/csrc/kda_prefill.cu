@@ -1270,29 +1270,6 @@ state_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__res
 constexpr int kStThreads = 416;
 constexpr uint32_t kTD1 = 0, kTD2 = 64, kTD1b = 128, kTSh = 192, kTSl = 256, kTD3 = 320, kTUh = 448, kTUl = 480;
 
-// Two FP32 operations in one instruction (each half rounded as the scalar operation would be).
-__device__ __forceinline__ float2 mul2(float2 a, float2 b)
-{
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<const uint64_t *>(&a)),
-        "l"(*reinterpret_cast<const uint64_t *>(&b)));
-    return *reinterpret_cast<const float2 *>(&d);
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b)
-{
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<const uint64_t *>(&a)),
-        "l"(*reinterpret_cast<const uint64_t *>(&b)));
-    return *reinterpret_cast<const float2 *>(&d);
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
-{
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(*reinterpret_cast<const uint64_t *>(&a)),
-        "l"(*reinterpret_cast<const uint64_t *>(&b)), "l"(*reinterpret_cast<const uint64_t *>(&c)));
-    return *reinterpret_cast<const float2 *>(&d);
-}
-
 // AND of pred over the `count` threads of named barrier `id` (also a barrier), so that every
 // thread of a group takes the same branch after a bounded wait.
 __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred)
@@ -1634,7 +1611,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const float2 x = make_float2(o[32 * hf + 2 * j], o[32 * hf + 2 * j + 1]);
-                    sq[j] = mul2(x, x);
+                    sq[j] = f2_mul(x, x);
                 }
 #pragma unroll
                 for (int off = 16; off >= 2; off >>= 1) {
@@ -1645,7 +1622,7 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                         const float2 send = upper ? sq[j] : sq[j + off / 2];
                         const float2 recv = make_float2(__shfl_xor_sync(0xffffffffu, send.x, off),
                                                         __shfl_xor_sync(0xffffffffu, send.y, off));
-                        sq[j] = add2(keep, recv);
+                        sq[j] = f2_add(keep, recv);
                     }
                 }
                 const bool upper = (lane & 1) != 0;
@@ -1670,9 +1647,9 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 const float2 gv = make_float2(__bfloat162float(sGY[r * kD + vi]), __bfloat162float(sGY[(r + 1) * kD + vi]));
                 // sigmoid(g) = (1 + tanh(g/2)) / 2; the hardware tanh's error is below the BF16
                 // rounding of the output it multiplies
-                const float2 hg = mul2(half2, gv);
-                const float2 sg = fma2(half2, make_float2(tanh_approx(hg.x), tanh_approx(hg.y)), half2);
-                const float2 yy = mul2(mul2(sg, nw2), mul2(make_float2(o[r], o[r + 1]), rinv));
+                const float2 hg = f2_mul(half2, gv);
+                const float2 sg = f2_fma(half2, make_float2(tanh_approx(hg.x), tanh_approx(hg.y)), half2);
+                const float2 yy = f2_mul(f2_mul(sg, nw2), f2_mul(make_float2(o[r], o[r + 1]), rinv));
                 const __nv_bfloat162 yb = __floats2bfloat162_rn(yy.x, yy.y);
                 y[r] = yb.x;
                 y[r + 1] = yb.y;

@@ -183,4 +183,28 @@ __device__ __forceinline__ float tanh_approx(float x)
     return y;
 }
 
+// Two FP32 operations in one instruction; each half is rounded exactly as the scalar
+// operation (round to nearest) would be.
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<const uint64_t *>(&a)),
+        "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<const uint64_t *>(&a)),
+        "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(*reinterpret_cast<const uint64_t *>(&a)),
+        "l"(*reinterpret_cast<const uint64_t *>(&b)), "l"(*reinterpret_cast<const uint64_t *>(&c)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
 }  // namespace kda
