@@ -585,7 +585,7 @@ def _time_layer_stack(K, args, cfg, gen, dev, stream, reps=5):
     per_layer = (4 * D * HIDDEN + DH * HIDDEN + D * DH + H * HIDDEN + HIDDEN * D) * 2 + \
         Bd * (H * DH * DH * 4 + 3 * (KCONV - 1) * D * 2)
     free, _ = torch.cuda.mem_get_info(dev)
-    n_layers = int(max(1, min(KDA_LAYERS, (free - (8 << 30)) // per_layer)))
+    n_layers = int(max(1, min(args.stack_layers, (free - (8 << 30)) // per_layer)))
     layers, states = [], []
     try:
         for _ in range(n_layers):
@@ -974,6 +974,8 @@ def main(argv=None):
                     help="time one part only (small profiling runs); the JSON line keeps its keys")
     ap.add_argument("--batch", type=int, default=B_DEC, help="decode batch (profiling runs)")
     ap.add_argument("--prefill-tokens", type=int, default=T_PRE, help="prefill length (profiling runs)")
+    ap.add_argument("--stack-layers", type=int, default=KDA_LAYERS,
+                    help="KDA layers in the layer-stack leg (profiling runs; the model has 69)")
     args = ap.parse_args(argv)
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         return _self_launch(args.gpus, argv)
