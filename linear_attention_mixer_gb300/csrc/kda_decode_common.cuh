@@ -49,28 +49,6 @@ __device__ __forceinline__ void dc_partials(const float4 (&s)[16], const float *
     }
 }
 
-// 1'. the same sums with the coefficients formed from a, k^ and q^ on the fly (the same
-//     products as stored ak = a k^, aq = a q^)
-__device__ __forceinline__ void dc_partials_akq(const float4 (&s)[16], const float *a, const float *k,
-                                                const float *q, int w, float4 &p, float4 &rr)
-{
-    p = make_float4(0.f, 0.f, 0.f, 0.f);
-    rr = p;
-    const float4 *a4 = reinterpret_cast<const float4 *>(a + 16 * w);
-    const float4 *k4 = reinterpret_cast<const float4 *>(k + 16 * w);
-    const float4 *q4 = reinterpret_cast<const float4 *>(q + 16 * w);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float4 av = a4[j], kv = k4[j], qv = q4[j];
-        const float4 x = make_float4(av.x * kv.x, av.y * kv.y, av.z * kv.z, av.w * kv.w);
-        const float4 y = make_float4(av.x * qv.x, av.y * qv.y, av.z * qv.z, av.w * qv.w);
-        p = dc_fma4(x.x, s[4 * j + 0], p);  rr = dc_fma4(y.x, s[4 * j + 0], rr);
-        p = dc_fma4(x.y, s[4 * j + 1], p);  rr = dc_fma4(y.y, s[4 * j + 1], rr);
-        p = dc_fma4(x.z, s[4 * j + 2], p);  rr = dc_fma4(y.z, s[4 * j + 2], rr);
-        p = dc_fma4(x.w, s[4 * j + 3], p);  rr = dc_fma4(y.w, s[4 * j + 3], rr);
-    }
-}
-
 // 2. (per column, once its 8 row-group partials are added in group order) u and o
 __device__ __forceinline__ float dc_u(float beta, float v, float p_sum) { return beta * (v - p_sum); }
 __device__ __forceinline__ float dc_o(float kq, float u, float r_sum) { return fmaf(kq, u, r_sum); }
@@ -113,8 +91,7 @@ __device__ __forceinline__ void dc_norm_store(float4 oo, const float *gw, T *out
 // ak[i] = a_i k^_i, aq[i] = a_i q^_i, a[i], k[i] (k^), v[c], gw[c]: shared-memory vectors of 128
 // red: kRedFloats floats (warp partials of p and of r, see kRedR), su, so: [128] floats (u and o).
 // kq = k^ . q^. out_row: this unit's 128 output values. Contains two __syncthreads.
-// With kFly, ak and aq are not read: the coefficients come from a, k and aq, which then holds q^.
-template <typename T, bool kFly = false>
+template <typename T>
 __device__ __forceinline__ void decode_token_step(float4 (&s)[16], const float *ak, const float *aq,
                                                   const float *a, const float *k, const float *v,
                                                   const float *gw, float beta, float kq, float *red, float *su,
@@ -122,8 +99,7 @@ __device__ __forceinline__ void decode_token_step(float4 (&s)[16], const float *
 {
     // 1. partial column sums over this warp's 16 rows
     float4 p, rr;
-    if constexpr (kFly) dc_partials_akq(s, a, k, aq, w, p, rr);
-    else dc_partials(s, ak, aq, w, p, rr);
+    dc_partials(s, ak, aq, w, p, rr);
     reinterpret_cast<float4 *>(red)[w * 32 + l] = p;
     reinterpret_cast<float4 *>(red + kRedR)[w * 32 + l] = rr;
     __syncthreads();

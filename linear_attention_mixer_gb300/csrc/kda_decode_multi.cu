@@ -56,13 +56,14 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
     constexpr int kNT = KDA_DECODE_MAX_TOKENS;
     float *sh_k = reinterpret_cast<float *>(smem + NST * L::kBytes);  // [token][d] k^ of every token
     float *sh_q = sh_k + kNT * kD, *sh_a = sh_q + kNT * kD, *sh_v = sh_a + kNT * kD, *sh_gw = sh_v + kNT * kD;
-    // NST = 2: alpha k^ and alpha q^ per row; NST = 1 forms them on the fly and sh_q holds q^
-    float *sh_ak = sh_gw + kNT * kD, *sh_aq = sh_ak + kNT * kD;
-    float *su = (NST == 2 ? sh_aq + kNT * kD : sh_gw + kNT * kD), *so = su + kD;  // [d] u, o of the current token
+    // alpha k^ per row; alpha q^ per row is sh_q (q^ itself is not needed past the prologue)
+    float *sh_ak = sh_gw + kNT * kD, *sh_aq = sh_q;
+    float *su = sh_ak + kNT * kD, *so = su + kD;  // [d] u, o of the current token
     float *red = so + kD;                          // warp partials of p and r (kRedFloats)
     float *part = red + kRedFloats;                // [token][3][4] quarter sums of squares
     float *sbeta = part + kNT * 12;                                  // [token] beta
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sbeta + kNT);       // [2]
+    float *skq = sbeta + kNT;                                        // [token] k^ . q^
+    uint64_t *bar = reinterpret_cast<uint64_t *>(skq + kNT);         // [2]
 
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
     const int n_units = B * H;
@@ -175,6 +176,13 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
                 }
             }
             __syncthreads();
+            if (tid < n) {  // k^ . q^ of token tid, from the quarter sums
+                const float *pt = part + tid * 12;
+                const float sqq = pt[0] + pt[1] + pt[2] + pt[3];
+                const float skk = pt[4] + pt[5] + pt[6] + pt[7];
+                const float sqk = pt[8] + pt[9] + pt[10] + pt[11];
+                skq[tid] = sqk * (q_scale * rsqrt_ftz(sqq + l2_eps)) * (rsqrt_ftz(skk + l2_eps));
+            }
 #pragma unroll
             for (int jt = 0; jt < (n + 1) / 2; ++jt) {
                 const int t = tg + 2 * jt;
@@ -184,12 +192,8 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
                     const float rk = rsqrt_ftz((pt[4] + pt[5] + pt[6] + pt[7]) + l2_eps);
                     const float kn = sh_k[t * kD + i] * rk, qn = sh_q[t * kD + i] * rq, a = sh_a[t * kD + i];
                     sh_k[t * kD + i] = kn;
-                    if constexpr (NST == 2) {
-                        sh_ak[t * kD + i] = a * kn;
-                        sh_aq[t * kD + i] = a * qn;
-                    } else {
-                        sh_q[t * kD + i] = qn;
-                    }
+                    sh_ak[t * kD + i] = a * kn;
+                    sh_aq[t * kD + i] = a * qn;  // over q^ (sh_aq is sh_q): this thread's own element
                 }
             }
             __syncthreads();
@@ -201,14 +205,9 @@ decode_multi_kernel(const float *__restrict__ conv_w, const float *__restrict__ 
 #pragma unroll 1
         for (int t = 0; t < n; ++t) {
             const size_t row = (size_t)r * n + t;
-            const float *pt = part + t * 12;
-            const float sqq = pt[0] + pt[1] + pt[2] + pt[3];
-            const float skk = pt[4] + pt[5] + pt[6] + pt[7];
-            const float sqk = pt[8] + pt[9] + pt[10] + pt[11];
-            const float kq = sqk * (q_scale * rsqrt_ftz(sqq + l2_eps)) * (rsqrt_ftz(skk + l2_eps));
-            decode_token_step<T, NST == 1>(s, sh_ak + t * kD, (NST == 2 ? sh_aq : sh_q) + t * kD, sh_a + t * kD,
-                                           sh_k + t * kD, sh_v + t * kD, sh_gw + t * kD, sbeta[t], kq, red, su, so,
-                                           out + row * D + (size_t)h * kD, rms_eps, w, l);
+            decode_token_step<T>(s, sh_ak + t * kD, sh_aq + t * kD, sh_a + t * kD, sh_k + t * kD, sh_v + t * kD,
+                                 sh_gw + t * kD, sbeta[t], skq[t], red, su, so, out + row * D + (size_t)h * kD,
+                                 rms_eps, w, l);
         }
         // the state after the run
         float4 *S4 = reinterpret_cast<float4 *>(S_all + ((size_t)slot * H + h) * kD * kD);
@@ -236,8 +235,8 @@ cudaError_t launch_multi_typed(const State &st, const kda_layer_params &p, const
     using L = MultiStage<T>;
     const kda_config_t &c = st.cfg;
     const int H = c.num_heads;
-    const size_t smem = NST * (size_t)L::kBytes + (NST == 2 ? 7 : 5) * KDA_DECODE_MAX_TOKENS * kD * 4 + 2 * kD * 4 +
-                        kRedFloats * 4 + KDA_DECODE_MAX_TOKENS * 13 * 4 + 2 * 8;
+    const size_t smem = NST * (size_t)L::kBytes + 6 * KDA_DECODE_MAX_TOKENS * kD * 4 + 2 * kD * 4 + kRedFloats * 4 +
+                        KDA_DECODE_MAX_TOKENS * 14 * 4 + 2 * 8;
     cudaError_t e = raise_smem_once(st, smem_bit_multi(sizeof(T) == 4, n), decode_multi_kernel<T, NST, n>, smem);
     if (e != cudaSuccess) return e;
     int sms = 0;
