@@ -41,9 +41,26 @@ DEC_BYTES_PER_UNIT = 2 * DH * DH * 4 + 5 * DH * 2 + 2 + DH * 2 + 2 * 3 * (KCONV 
 PRE_FLOP_PER_TOKEN_HEAD = 2 * (3 * DH * DH + 5 * CHUNK * DH)
 # algorithmic bytes per token of prefill with BF16 I/O: q,k,v,z,g,b in, out
 PRE_BYTES_PER_TOKEN = (5 * D + H + D) * 2
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch at B=256,
-# from one ncu capture of the decode kernel as it stands; None once that kernel changes.
-DEC_TRAFFIC_B256 = 1_699_824_128 + 1_611_796_992
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch at B=256, from
+# one ncu capture of the decode kernel built from the sources below, whose SHA-256 (over the
+# files in this order) is recorded with it. The line reports null when the sources differ, and
+# a CPU test fails until the capture is taken again.
+DEC_TRAFFIC_B256 = 1_699_825_664 + 1_612_125_184
+DEC_TRAFFIC_SOURCES = ("linear_attention_mixer_gb300/csrc/kda_decode.cu",
+                       "linear_attention_mixer_gb300/csrc/kda_decode_common.cuh",
+                       "linear_attention_mixer_gb300/csrc/kda_ptx.cuh",
+                       "linear_attention_mixer_gb300/csrc/kda_internal.cuh")
+DEC_TRAFFIC_SRC_SHA256 = "3f0ea532124da2c4f17d78e6a3791603693172d9a59f7042cc0e85c46bfc1bbc"
+
+
+def decode_sources_sha256() -> str:
+    """SHA-256 of the decode kernel's source files, in DEC_TRAFFIC_SOURCES order."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in DEC_TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def _peaks():
@@ -857,7 +874,8 @@ def run_kda(args):
             "ms_per_step": total_ms_max / args.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": DEC_TRAFFIC_B256 if Bd == B_DEC else None,
+                         "traffic": (DEC_TRAFFIC_B256 if Bd == B_DEC and decode_sources_sha256() == DEC_TRAFFIC_SRC_SHA256
+                                     else None),
                          "kernel": "decode_persistent_kernel<bf16,3>", "bytes_per_launch": dec_bytes,
                          "launch_ms": r["launch_ms"], "peak_note": src},
             "e2e": {"value": Bd * r["e2e_steps"] * ws / (e2e_ms_max / 1e3), "unit": "tokens/s",

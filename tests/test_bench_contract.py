@@ -27,3 +27,14 @@ def test_reference_arm_prints_one_contract_line():
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_decode_traffic_figure_matches_the_kernel_sources():
+    """bench.py's roofline.traffic for decode B=256 is one ncu capture of the decode kernel; it
+    stands only for the sources it was taken on. When they change, take the capture again (ncu
+    dram__bytes_read.sum and dram__bytes_write.sum of one B=256 decode launch) and record the
+    new bytes and the new source hash in bench.py."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.decode_sources_sha256() == bench.DEC_TRAFFIC_SRC_SHA256, (
+        "the decode kernel's sources changed since its DRAM traffic was captured")

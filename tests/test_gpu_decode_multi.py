@@ -43,8 +43,10 @@ def _run_single(cfg, params, st, slots_np, tok, bf16, n):
     return np.stack(outs, axis=1)  # [B][n][D]
 
 
-@pytest.mark.parametrize("bf16,H,B,n", [(False, 2, 3, 1), (False, 2, 3, 8), (False, 2, 2, 5),
-                                        (True, 96, 3, 4), (True, 96, 2, 8)])
+# every n has its own kernel (the token count is a template parameter): each one runs, in both
+# I/O types, at small sizes, and the workload's geometry at n = 4 and 8
+@pytest.mark.parametrize("bf16,H,B,n", [(False, 2, 3, n) for n in range(1, 9)] + [(True, 4, 3, n) for n in range(1, 9)]
+                         + [(False, 2, 2, 5), (True, 96, 3, 4), (True, 96, 2, 8)])
 def test_decode_tokens_matches_oracle_and_single_calls(oracle_mod, bf16, H, B, n):
     d, seed = 128, 70 + n + H
     p = KI.make_params(H, d, 4, seed)
@@ -161,3 +163,49 @@ def test_bad_slot_then_good_units_in_one_cta():
         assert np.array_equal(Sa, Sb) and np.array_equal(ta, tb)
     finally:
         K.kda_state_free(st)
+
+
+def test_decode_tokens_b256_n8_full_size(oracle_mod):
+    """The bench's workload: 256 sequences x 8 tokens in one call, 96 heads x 128, BF16 I/O, FP32
+    states (~1.6 GB) from the generator, slots a permutation inside a larger state. All units are
+    checked bit for bit against 8 single-token calls on a copy of the state; sampled (sequence,
+    head) units against the oracle, one by one."""
+    c = KI.CONFIGS["decode_b256"]
+    H, d, B, n = c["H"], c["d"], c["B"], 8
+    n_slots = 2 * B
+    rng = np.random.default_rng(c["seed"] + 8)
+    perm = rng.permutation(n_slots).astype(np.int32)
+    multi_slots, single_slots = perm[:B], perm[B:]
+    p = KI.make_params(H, d, 4, c["seed"])
+    tok = KI.make_tokens(B * n, H, d, c["seed"] + 8, bf16=True)  # row r, token t at r * n + t
+    S0 = KI.make_state(B, H, d, c["seed"], std=0.05)
+    T0 = KI.make_tail(B, H, d, 4, c["seed"], bf16=True)
+    cfg = K.kda_config(H, d, K.KDA_BF16)
+    params = dev_params(p)
+    st = K.kda_state_alloc(cfg, n_slots)
+    try:
+        upload_state(cfg, st, multi_slots.tolist(), S0, T0)
+        upload_state(cfg, st, single_slots.tolist(), S0, T0)
+        got = _run_multi(cfg, params, st, multi_slots.tolist(), tok, True, n)     # [B][n][D]
+        one = _run_single(cfg, params, st, single_slots.tolist(), tok, True, n)
+        Sm, tm = download_state(cfg, st, multi_slots.tolist())
+        Ss, ts = download_state(cfg, st, single_slots.tolist())
+        assert K.kda_state_poll_error(st) == 0
+    finally:
+        K.kda_state_free(st)
+    assert np.array_equal(got, one) and np.array_equal(Sm, Ss) and np.array_equal(tm, ts)
+    oc = oracle_mod.OracleCfg(H=H, d=d)
+    units = [(int(r), int(h)) for r, h in zip(rng.integers(0, B, 24), rng.integers(0, H, 24))]
+    units += [(0, 0), (B - 1, H - 1)]
+    errs, serrs = [], []
+    for r, h in units:
+        S_h = S0[r, h].astype(np.float64)
+        tl = T0[r].astype(np.float64)
+        ref = oracle_mod.unit(oc, h, p, S_h, tl, tok, rows=list(range(r * n, (r + 1) * n)))  # [n, d]
+        g = got[r][:, h * d:(h + 1) * d]
+        errs.append(np.abs(g - ref).max() / max(np.abs(ref).max(), 1e-30))
+        serrs.append(rel_err(Sm[r, h], S_h))
+        assert np.array_equal(tm[r][:, :, h * d:(h + 1) * d], tl[:, :, h * d:(h + 1) * d].astype(np.float32))
+    print(f"decode_tokens B=256 n=8 bf16 ({len(units)} sampled units): out {max(errs):.2e} state {max(serrs):.2e}; "
+          f"all units bit-exact against single-token calls")
+    assert max(errs) <= TOL_BF16 and max(serrs) <= TOL_F32
