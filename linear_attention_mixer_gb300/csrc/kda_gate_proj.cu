@@ -587,15 +587,7 @@ kda_status gp_fail(kda_status s, const char *fmt, ...)
 cudaError_t encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
                       uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz)
 {
-    static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            fn = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }();
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};

@@ -336,25 +336,11 @@ ln_reduce_kernel(const float *__restrict__ part, const __nv_bfloat16 *__restrict
         make_uint4(ln_pack(acc[0], acc[1]), ln_pack(acc[2], acc[3]), ln_pack(acc[4], acc[5]), ln_pack(acc[6], acc[7]));
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 ln_encoder()
-{
-    static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            fn = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }();
-    return encode;
-}
-
 // rank-3 map: dims {d0, d1, d2}, byte strides of dims 1 and 2, box {b0, b1, 1}, 128-byte swizzle
 cudaError_t ln_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                    uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1)
 {
-    const PFN_cuTensorMapEncodeTiled_v12000 encode = ln_encoder();
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const cuuint64_t dims[3] = {d0, d1, d2};
     const cuuint64_t strides[2] = {s1, s2};
@@ -370,7 +356,7 @@ cudaError_t ln_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uin
 // box {b0, b1}, 128-byte swizzle
 cudaError_t ln_map2(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t s1, uint32_t b0, uint32_t b1)
 {
-    const PFN_cuTensorMapEncodeTiled_v12000 encode = ln_encoder();
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {d0, d1};
     const cuuint64_t strides[1] = {s1};

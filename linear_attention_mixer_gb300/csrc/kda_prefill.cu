@@ -1704,19 +1704,10 @@ epilogue_kernel(const float *__restrict__ obuf, const float *__restrict__ norm_w
 }
 
 // Tensor map of a packed [rows][D] BF16 input for 2-D box copies of box_rows rows x 128
-// channels (one head). The encoder comes from the driver through the runtime, so the
-// library does not link the driver library itself.
+// channels (one head).
 cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t D, int box_rows)
 {
-    static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            fn = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }();
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
@@ -1732,15 +1723,7 @@ cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int6
 // with 128-byte swizzle (MMA operands).
 cudaError_t encode_sw128_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows)
 {
-    static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            fn = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }();
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
