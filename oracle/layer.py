@@ -42,3 +42,21 @@ def layer_decode(cfg: O.OracleCfg, params, w: dict, S_all, tail_all, slots, x) -
     tok = {n: np.ascontiguousarray(a, dtype=np.float32) for n, a in tok.items()}
     mixed = O.decode_batch(cfg, params, S_all, tail_all, slots, tok)
     return linear(mixed, w["w_o"], r=x)
+
+
+def layer_prefill(cfg: O.OracleCfg, params, w: dict, S_all, tail_all, slots, cu_seqlens, x) -> np.ndarray:
+    """Packed variable-length prefill of x [T][hidden]: sequence i is rows cu_seqlens[i] ..
+    cu_seqlens[i + 1] - 1, on slot slots[i] of S_all and tail_all (which advance in place), its
+    mixer run token by token by the sequential oracle. Returns x' [T][hidden]."""
+    D = cfg.H * cfg.d
+    qkvg = linear(x, w["w_qkvg"])
+    z, b = gate_proj(x, w["w_fa"], w["w_fb"], w["w_b"])
+    cols = {"q": qkvg[:, 0:D], "k": qkvg[:, D:2 * D], "v": qkvg[:, 2 * D:3 * D], "g": qkvg[:, 3 * D:4 * D],
+            "z": z, "b": b}
+    mixed = np.zeros((np.asarray(x).shape[0], D))
+    for i, slot in enumerate(slots):
+        a, e = int(cu_seqlens[i]), int(cu_seqlens[i + 1])
+        tok = {n: np.ascontiguousarray(arr[a:e], dtype=np.float32) for n, arr in cols.items()}
+        mixed[a:e] = O.sequence(cfg, params, S_all[slot], tail_all[slot], tok)
+    return linear(mixed, w["w_o"], r=x)
+

@@ -117,3 +117,50 @@ def test_layer_decode_matches_oracle(oracle_mod):
         x = outs[s].astype(np.float64)  # the next step continues from the GPU's own output
     print(f"layer decode state: {rel_err(Sg, S_all):.2e}")
     assert rel_err(Sg, S_all) <= TOL_BF16
+
+
+def test_layer_prefill_matches_oracle(oracle_mod):
+    """A whole layer's packed prefill (hidden 256, 2 heads): sequences of 70 and 33 tokens
+    (full chunks and ragged tails) from filled states, x' = x + W_o mixer(...), against the
+    layer oracle's prefill, and the final states."""
+    from linear_attention_mixer_gb300.layer import KdaLayerRunner, KdaLayerWeights
+    H, d, hidden = 2, 128, 256
+    D = H * d
+    lens = [70, 33]
+    cu_h = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu_h[-1])
+    rng = np.random.default_rng(83)
+    p = KI.make_params(H, d, 4, 83)
+    wn = {"w_qkvg": _bf(rng.standard_normal((4 * D, hidden)) * hidden ** -0.5),
+          "w_fa": _bf(rng.standard_normal((d, hidden)) * hidden ** -0.5),
+          "w_fb": _bf(rng.standard_normal((D, d)) * d ** -0.5),
+          "w_b": _bf(rng.standard_normal((H, hidden)) * hidden ** -0.5),
+          "w_o": _bf(rng.standard_normal((hidden, D)) * D ** -0.5)}
+    dev = lambda a: torch.from_numpy(a).cuda().to(torch.bfloat16).contiguous()
+    lw = KdaLayerWeights(dev(wn["w_qkvg"]), dev(wn["w_fa"]), dev(wn["w_fb"]), dev(wn["w_b"]), dev(wn["w_o"]),
+                         dev_params(p))
+    cfg = K.kda_config(H, d, K.KDA_BF16)
+    S0 = KI.make_state(2, H, d, 83)
+    T0 = KI.make_tail(2, H, d, 4, 83, bf16=True)
+    slots_np = np.array([1, 0], dtype=np.int32)
+    x = _bf(rng.standard_normal((T, hidden)))
+    st = K.kda_state_alloc(cfg, 2)
+    runner = KdaLayerRunner(cfg, hidden, T, "cuda")
+    try:
+        from tests.kda_testutil import upload_state
+        upload_state(cfg, st, [0, 1], S0, T0)
+        y = torch.empty(T, hidden, dtype=torch.bfloat16, device="cuda")
+        runner.prefill(lw, st, torch.tensor(slots_np, device="cuda"), torch.tensor(cu_h, device="cuda"), cu_h, dev(x),
+                       y)
+        got = to_np(y)
+        Sg, tg = download_state(cfg, st, [0, 1])
+        assert K.kda_state_poll_error(st) == 0
+    finally:
+        K.kda_state_free(st)
+    oc = oracle_mod.OracleCfg(H=H, d=d)
+    S_all, tail_all = S0.astype(np.float64), T0.astype(np.float64)
+    ref = OL.layer_prefill(oc, p, wn, S_all, tail_all, slots_np, cu_h, x.astype(np.float64))
+    e, es = rel_err(got, ref), rel_err(Sg, S_all)
+    print(f"layer prefill, 2 sequences ({lens[0]} + {lens[1]} tokens): out {e:.2e} state {es:.2e}")
+    assert e <= TOL_BF16 and es <= TOL_BF16
+

@@ -1,7 +1,7 @@
 """Pins of the layer oracle (oracle/layer.py): the dense product against brute-force loops,
-and a whole layer's first token from a zero state against the page's formula written out
-with numpy (so a swapped projection, a missing residual or W_o applied before the mixer
-fails)."""
+a whole layer's first token from a zero state against the page's formula written out with
+numpy (so a swapped projection, a missing residual or W_o applied before the mixer fails),
+and the prefill form against token-by-token decode steps."""
 import math
 
 import numpy as np
@@ -56,3 +56,33 @@ def test_layer_first_token_closed_form(oracle_mod):
         np.testing.assert_allclose(got[r], x[r] + 5 * mixed, rtol=1e-6, atol=1e-7)
     # the slots advanced: row 0 wrote slot 1, row 1 slot 0, both away from zero
     assert np.abs(S[0]).max() > 0 and np.abs(S[1]).max() > 0
+
+
+def test_layer_prefill_equals_token_by_token_decode(oracle_mod):
+    """The prefill form of the layer oracle over T tokens of two sequences equals T decode steps
+    of the layer oracle (pinned above by its closed form) fed the same rows in order."""
+    from oracle import layer as OL
+    H, d, hidden = 2, 8, 24
+    D = H * d
+    rng = np.random.default_rng(5)
+    p = KI.make_params(H, d, 4, 5)
+    w = {"w_qkvg": rng.standard_normal((4 * D, hidden)) * 0.3, "w_fa": rng.standard_normal((d, hidden)) * 0.3,
+         "w_fb": rng.standard_normal((D, d)) * 0.3, "w_b": rng.standard_normal((H, hidden)) * 0.3,
+         "w_o": rng.standard_normal((hidden, D)) * 0.3}
+    oc = oracle_mod.OracleCfg(H=H, d=d)
+    lens = [5, 3]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    x = rng.standard_normal((cu[-1], hidden))
+    slots = [1, 0]
+    S0 = rng.standard_normal((2, H, d, d)) * 0.1
+    T0 = rng.standard_normal((2, 3, 3, D))
+    S_p, T_p = S0.copy(), T0.copy()
+    got = OL.layer_prefill(oc, p, w, S_p, T_p, slots, cu, x)
+    S_d, T_d = S0.copy(), T0.copy()
+    ref = np.zeros_like(got)
+    for i, slot in enumerate(slots):
+        for t in range(cu[i], cu[i + 1]):
+            ref[t] = OL.layer_decode(oc, p, w, S_d, T_d, np.array([slot]), x[t:t + 1])[0]
+    assert np.abs(got - ref).max() <= 1e-9 * max(1.0, np.abs(ref).max())
+    assert np.abs(S_p - S_d).max() <= 1e-9 * np.abs(S_d).max() and np.array_equal(T_p, T_d)
+
