@@ -239,3 +239,43 @@ def test_gate_projection_fused_into_prefill_bf16(oracle_mod, H, hidden, lens):
         assert rc == K.KDA_ERR_INVALID and "BF16" in K.kda_last_error()
     finally:
         K.kda_state_free(st)
+
+
+def test_gate_projection_fused_prefill_t8192_full_size(oracle_mod):
+    """The hidden state of one 8192-token sequence (hidden 7168, 96 heads x 128, BF16) through
+    kda_gate_proj_in and kda_prefill_gate_fused, against the FP64 projection oracle followed by
+    the sequential oracle over all 8192 tokens; the final state too."""
+    from tests.kda_testutil import dev_params, download_state
+    c = KI.CONFIGS["prefill_8192"]
+    H, d, T, hidden = c["H"], c["d"], c["T"], 7168
+    cfg = K.kda_config(H, d, K.KDA_BF16)
+    gp = KI.make_gate_proj(T, hidden, H, d, seed=31)
+    p = KI.make_params(H, d, 4, 31)
+    tok = KI.make_tokens(T, H, d, seed=31, bf16=True)
+    bf = torch.bfloat16
+    dv = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda().to(bf).contiguous()
+    f = torch.empty(T, d, dtype=bf, device="cuda")
+    b = torch.empty(T, H, dtype=bf, device="cuda")
+    ws = torch.empty(K.kda_gate_proj_workspace_bytes(cfg, hidden, T), dtype=torch.uint8, device="cuda")
+    K.kda_gate_proj_in(cfg, dv(gp["x"]), dv(gp["w_fa"]), dv(gp["w_b"]), f, b, ws)
+    st = K.kda_state_alloc(cfg, 1)
+    try:
+        cu_h = np.array([0, T], dtype=np.int32)
+        out = torch.empty(T, H * d, dtype=bf, device="cuda")
+        K.kda_prefill_gate_fused(cfg, dev_params(p), st, torch.zeros(1, dtype=torch.int32, device="cuda"),
+                                 torch.tensor(cu_h, device="cuda"), cu_h, dv(tok["q"]), dv(tok["k"]), dv(tok["v"]), f,
+                                 dv(gp["w_fb"]), b, dv(tok["g"]), out)
+        got = out.float().cpu().numpy()
+        Sg, _ = download_state(cfg, st, [0])
+        assert K.kda_state_poll_error(st) == 0
+    finally:
+        K.kda_state_free(st)
+    z_o, b_o = gate_proj(gp["x"], gp["w_fa"], gp["w_fb"], gp["w_b"])
+    seq = {n: tok[n] for n in ("q", "k", "v", "g")}
+    seq["z"], seq["b"] = z_o.astype(np.float32), b_o.astype(np.float32)
+    oc = oracle_mod.OracleCfg(H=H, d=d)
+    S, tail = oracle_mod.new_state(oc)
+    ref = oracle_mod.sequence(oc, p, S, tail, seq)
+    e, es = rel_err(got, ref), rel_err(Sg[0], S)
+    print(f"gate projection fused into the prefill, T=8192, hidden 7168: out {e:.2e} final state {es:.2e}")
+    assert e <= TOL_BF16 and es <= TOL_BF16 and np.isfinite(got).all()
