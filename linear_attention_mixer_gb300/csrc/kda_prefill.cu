@@ -1489,10 +1489,8 @@ state_tc_kernel(float *__restrict__ S_all, T *__restrict__ tail_all, int32_t *__
                 mbar_arrive_expect_tx(&bar[1], kStageBBytes);
                 bulk_g2s(sB, block_of(ci) + kOffTB, kStageBBytes, &bar[1]);
             };
-            auto prefetch_block = [&](int ci) {  // into L2 ahead of its copies, 16 KB per request
-                const unsigned char *src = block_of(ci);
-                for (int off = 0; off < kTcChunkBytes; off += 16384)
-                    prefetch_l2_bulk(src + off, (uint32_t)min(16384, kTcChunkBytes - off));
+            auto prefetch_block = [&](int ci) {  // into L2 ahead of its copies, one request
+                prefetch_l2_bulk(block_of(ci), (uint32_t)kTcChunkBytes);
             };
             constexpr uint32_t id64 = tc::idesc_bf16(128, 64), id128 = tc::idesc_bf16(128, 128);
             constexpr uint32_t id192 = tc::idesc_bf16(128, 192);
