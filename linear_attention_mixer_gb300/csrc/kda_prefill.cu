@@ -92,19 +92,6 @@ WsLayout ws_layout(int H, int64_t total_chunks, int64_t total_T, int N, bool tc)
     return L;
 }
 
-// 16 values -> BF16 at (row, k0 .. k0+15) of a K-major interleaved tile with Kd columns (k0 % 16 == 0)
-__device__ __forceinline__ void store_row_bf16(unsigned char *tile, int row, int k0, const float *v16, int Kd)
-{
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const __nv_bfloat162 p2 = __floats2bfloat162_rn(v16[2 * i], v16[2 * i + 1]);
-        w[i] = *reinterpret_cast<const uint32_t *>(&p2);
-    }
-    *reinterpret_cast<uint4 *>(tile + tc::kmajor_off(row, k0, Kd)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4 *>(tile + tc::kmajor_off(row, k0 + 8, Kd)) = make_uint4(w[4], w[5], w[6], w[7]);
-}
-
 // ---------------------------------------------------------------- chunk table
 // One thread builds the chunk list. The device copy of cu_seqlens is checked
 // against what the host sized the launch for (N + 1 entries, starting at 0,
