@@ -494,6 +494,39 @@ __device__ __forceinline__ void mma_split3(uint32_t d, uint64_t a_hi, uint64_t a
     for (int kk = 0; kk < ksteps; ++kk) tc::mma_bf16(d, a_hi + 16u * kk, b_lo + 16u * kk, idesc, 1u);
 }
 
+// conv + SiLU of two adjacent channels over 32 output rows: col points at the staged raw row
+// of the first output's oldest tap (staged row j holds position j - 3), w0 and w1 are the two
+// channels' taps (oldest first), dst at the first output row (row pitch kYS). Rows at or past
+// n_valid are written as zero (only checked when kFull is false).
+template <bool kFull>
+__device__ __forceinline__ void conv_silu_pair32(const __nv_bfloat16 *col, float4 w0, float4 w1, float *dst,
+                                                 int n_valid)
+{
+    auto ld2 = [&](int j) { return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(col + j * kD)); };
+    float2 h0 = ld2(0), h1 = ld2(1), h2 = ld2(2);
+#pragma unroll 1
+    for (int r0 = 0; r0 < 32; r0 += 8) {
+        float2 cv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float2 xin = ld2(r0 + u + 3);
+            cv[u].x = fmaf(w0.x, h0.x, fmaf(w0.y, h1.x, fmaf(w0.z, h2.x, w0.w * xin.x)));
+            cv[u].y = fmaf(w1.x, h0.y, fmaf(w1.y, h1.y, fmaf(w1.z, h2.y, w1.w * xin.y)));
+            h0 = h1; h1 = h2; h2 = xin;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            // sigmoid(x) = (1 + tanh(x/2)) / 2: one SFU operation instead of two; the hardware
+            // tanh's error (about 2^-11 relative) is far below BF16's rounding
+            const float sx = fmaf(0.5f, tanh_approx(0.5f * cv[u].x), 0.5f);
+            const float sy = fmaf(0.5f, tanh_approx(0.5f * cv[u].y), 0.5f);
+            float2 y = make_float2(cv[u].x * sx, cv[u].y * sy);
+            if (!kFull && r0 + u >= n_valid) y = make_float2(0.f, 0.f);
+            *reinterpret_cast<float2 *>(dst + (r0 + u) * kYS) = y;
+        }
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(512, 1)
 prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bias,
@@ -670,8 +703,14 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         if (tid < kC && tid < n) braw = ld_nc_u16(bl + (size_t)(t0 + tid) * H + h);
         // this thread's per-channel parameters
         const int pc = tid & (kD - 1), px = tid >> 7;  // channel, stream (q, k, v, or the gate)
-        const float4 p_w = px < 3 ? __ldg(reinterpret_cast<const float4 *>(conv_w + ((size_t)px * D + (size_t)h * kD + pc) * kK))
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        // (conv threads, px < 3: channels 2 cp, 2 cp + 1 of stream px, output rows 32 rh .. +31)
+        const int cp = tid & 63, rh = (tid >> 6) & 1;
+        float4 p_w0 = make_float4(0.f, 0.f, 0.f, 0.f), p_w1 = p_w0;
+        if (px < 3) {
+            const float4 *wb = reinterpret_cast<const float4 *>(conv_w + ((size_t)px * D + (size_t)h * kD + 2 * cp) * kK);
+            p_w0 = __ldg(wb);
+            p_w1 = __ldg(wb + 1);
+        }
         const float p_dt = __ldg(dt_bias + (size_t)h * kD + pc);
         const float p_eA = expf(__ldg(A_log + h));
         {
@@ -696,30 +735,15 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
         if (tid < kC) sbeta[tid] = tid < n ? sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
 
-        // 1. conv + SiLU (sliding window in registers) for stream px < 3, 2. the gates for px == 3;
-        //    thread (channel pc, stream px) walks all 64 rows, 8 at a time. The gate's exponent is
-        //    capped at 80 (the sigmoid is then below 2e-35).
+        // 1. conv + SiLU (sliding window in registers) for stream px < 3, two channels and 32 rows a
+        //    thread, 2. the gates for px == 3, one channel and all 64 rows a thread. The gate's
+        //    exponent is capped at 80 (the sigmoid is then below 2e-35).
         if (px < 3) {
-            float *dst = Yq + px * (kC * kYS);  // Yq, Yk, Yv are consecutive: the stores stay shared
-            const T *col = raw + (size_t)px * kRows * kD + pc;
-            float h0 = IO<T>::ld(col), h1 = IO<T>::ld(col + kD), h2 = IO<T>::ld(col + 2 * kD);
-#pragma unroll 1
-            for (int r0 = 0; r0 < kC; r0 += 8) {
-                float cv[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float xin = IO<T>::ld(col + (r0 + u + 3) * kD);
-                    cv[u] = fmaf(p_w.x, h0, fmaf(p_w.y, h1, fmaf(p_w.z, h2, p_w.w * xin)));
-                    h0 = h1; h1 = h2; h2 = xin;
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    // sigmoid(x) = (1 + tanh(x/2)) / 2: one SFU operation instead of two; the
-                    // hardware tanh's error (about 2^-11 relative) is far below BF16's rounding
-                    const float sg = fmaf(0.5f, tanh_approx(0.5f * cv[u]), 0.5f);
-                    dst[(r0 + u) * kYS + pc] = r0 + u < n ? cv[u] * sg : 0.f;
-                }
-            }
+            // Yq, Yk, Yv are consecutive: the stores stay shared
+            float *dst = Yq + px * (kC * kYS) + (32 * rh) * kYS + 2 * cp;
+            const __nv_bfloat16 *col = reinterpret_cast<const __nv_bfloat16 *>(raw) + (size_t)(px * kRows + 32 * rh) * kD + 2 * cp;
+            if (n == kC) conv_silu_pair32<true>(col, p_w0, p_w1, dst, kC);
+            else conv_silu_pair32<false>(col, p_w0, p_w1, dst, n - 32 * rh);
         } else {
             // the gate thread of channel pc also carries G_r = sum_{t<=r} gk_t down the rows (gk = 0,
             // no decay, past the chunk, so G stays at G_last there); z from TMEM (fused) or the
