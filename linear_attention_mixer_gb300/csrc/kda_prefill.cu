@@ -768,12 +768,21 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                     for (int j = 0; j < 32; ++j) zz[j] = IO<T>::ld(col + (32 * hb + j) * kD);
                 }
                 // (fused: the product has completed, so the array that held W_fb takes G)
+                if (n == kC) {  // a full chunk: no row mask
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int r = 32 * hb + j;
-                    const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[j] + p_dt), 80.f)));
-                    acc += r < n ? gmin * sg : 0.f;
-                    GL[r * kYS + pc] = acc;
+                    for (int j = 0; j < 32; ++j) {
+                        const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[j] + p_dt), 80.f)));
+                        acc += gmin * sg;
+                        GL[(32 * hb + j) * kYS + pc] = acc;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int r = 32 * hb + j;
+                        const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[j] + p_dt), 80.f)));
+                        acc += r < n ? gmin * sg : 0.f;
+                        GL[r * kYS + pc] = acc;
+                    }
                 }
             }
         }
@@ -982,14 +991,15 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         if (tid >= kC) {   // warps 2..15 (after their read-back or zero blocks) build the B operand
             for (int u = tid - kC; u < 256 * (kC / 8); u += 512 - kC) {
                 const int nn = u & 255, i0 = 8 * (u >> 8);
-                float o[8];
+                float o[8], bt[8];
+                ld8f(sbeta + i0, bt);
                 if (nn < kD) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        o[j] = sbeta[i0 + j] * (Yk[(i0 + j) * kYS + nn] * exp_ftz(GL[(i0 + j) * kYS + nn]));
+                        o[j] = bt[j] * (Yk[(i0 + j) * kYS + nn] * exp_ftz(GL[(i0 + j) * kYS + nn]));
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) o[j] = sbeta[i0 + j] * Yv[(i0 + j) * kYS + nn - kD];
+                    for (int j = 0; j < 8; ++j) o[j] = bt[j] * Yv[(i0 + j) * kYS + nn - kD];
                 }
                 uint4 hi, lo;
                 split8(o, hi, lo);
