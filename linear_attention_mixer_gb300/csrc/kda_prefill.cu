@@ -494,6 +494,16 @@ __device__ __forceinline__ void mma_split3(uint32_t d, uint64_t a_hi, uint64_t a
     for (int kk = 0; kk < ksteps; ++kk) tc::mma_bf16(d, a_hi + 16u * kk, b_lo + 16u * kk, idesc, 1u);
 }
 
+// 2^x by the special-function unit (about 2 ulp); results below the smallest normal number flush
+// to zero. prep_tc keeps the cumulative log decay in base 2 (G log2(e)), so that each of its
+// exponentials of G, or of a difference of G values, is this one instruction.
+__device__ __forceinline__ float ex2_ftz(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // conv + SiLU of two adjacent channels over 32 output rows: col points at the staged raw row
 // of the first output's oldest tap (staged row j holds position j - 3), w0 and w1 are the two
 // channels' taps (oldest first), dst at the first output row (row pitch kYS). Rows at or past
@@ -545,7 +555,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
     float *Yq = smf;                                  // [64][132] q^
     float *Yk = Yq + kC * kYS;                        // [64][132] k^
     float *Yv = Yk + kC * kYS;                        // [64][132] v
-    float *GL = Yv + kC * kYS;                        // [64][132] gk, then G = cumulative log decay
+    float *GL = Yv + kC * kYS;                        // [64][132] G log2(e), G the cumulative log decay
     unsigned char *Y = reinterpret_cast<unsigned char *>(GL + kC * kYS);
     float *sbeta = reinterpret_cast<float *>(Y + kPtY);
     // [0] z operands (fused), [1..2] A/P buffers, [3] solve, [4] z product (fused)
@@ -713,6 +723,9 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
         const float p_dt = __ldg(dt_bias + (size_t)h * kD + pc);
         const float p_eA = expf(__ldg(A_log + h));
+        // the gate in base 2: exp(-eA (z + dt)) = 2^(p_eA2 (z + dt)) (the cap 115 ~ 80 log2(e):
+        // the sigmoid is then below 2e-35), and G log2(e) accumulates gk log2(e) = gmin2 sg
+        const float p_eA2 = -p_eA * 1.4426950408889634f, gmin2 = gmin * 1.4426950408889634f;
         {
             const bool ok = mbar_wait_bounded(bars, done & 1u, kTcWaitLimit);
             good &= ok;
@@ -771,16 +784,16 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 if (n == kC) {  // a full chunk: no row mask
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[j] + p_dt), 80.f)));
-                        acc += gmin * sg;
+                        const float sg = rcp_ftz(1.0f + ex2_ftz(fminf(p_eA2 * (zz[j] + p_dt), 115.f)));
+                        acc += gmin2 * sg;
                         GL[(32 * hb + j) * kYS + pc] = acc;
                     }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int r = 32 * hb + j;
-                        const float sg = rcp_ftz(1.0f + exp_ftz(fminf(-p_eA * (zz[j] + p_dt), 80.f)));
-                        acc += r < n ? gmin * sg : 0.f;
+                        const float sg = rcp_ftz(1.0f + ex2_ftz(fminf(p_eA2 * (zz[j] + p_dt), 115.f)));
+                        acc += r < n ? gmin2 * sg : 0.f;
                         GL[r * kYS + pc] = acc;
                     }
                 }
@@ -846,7 +859,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 ld8f(GL + kBlk * b * kYS + c0, gn);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float f = exp_ftz(gr[j] - gn[j]);
+                    const float f = ex2_ftz(gr[j] - gn[j]);
                     kl[j] = kv[j] * f;
                     ql[j] = qv[j] * f;
                 }
@@ -861,7 +874,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                     if (R != b) ld8f(GL + kBlk * R * kYS + c0, gn);
                     float kx[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) kx[j] = kv[j] * exp_ftz(gn[j] - gr[j]);
+                    for (int j = 0; j < 8; ++j) kx[j] = kv[j] * ex2_ftz(gn[j] - gr[j]);
                     split8(kx, hi, lo);
                     const int row = 8 * R * (R + 1) + r;
                     st16(tRh + tc::kmajor_off(row, cl, kD / 2), hi);
@@ -885,7 +898,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                     ld8f(Yq + r * kYS + c0, qv);
                     ld8f(GL + r * kYS + c0, gr);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) o[j] = qv[j] * exp_ftz(gr[j]);
+                    for (int j = 0; j < 8; ++j) o[j] = qv[j] * ex2_ftz(gr[j]);
                     st16(blk + kOffTA + tc::kmajor_off(kC + r, c0, kD), pack8_bf16(o));
                 }
             } else {
@@ -896,14 +909,14 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int r = 8 * rb + j;
-                        o[j] = Yk[r * kYS + c] * exp_ftz(gl - GL[r * kYS + c]);
+                        o[j] = Yk[r * kYS + c] * ex2_ftz(gl - GL[r * kYS + c]);
                     }
                     uint4 hi, lo;
                     split8(o, hi, lo);
                     st16(blk + kOffTB + tc::kmajor_off(kC + c, 8 * rb, kC), hi);
                     st16(blk + kOffTB + tc::kmajor_off(4 * kC + c, 8 * rb, kC), lo);
                 }
-                if (tid < kD) reinterpret_cast<float *>(blk + kOffGam)[tid] = exp_ftz(GL[(kC - 1) * kYS + tid]);
+                if (tid < kD) reinterpret_cast<float *>(blk + kOffGam)[tid] = ex2_ftz(GL[(kC - 1) * kYS + tid]);
             }
         }
         good &= mbar_wait_bounded(bars + 1, 1u, kTcWaitLimit);  // second completion: half 1
@@ -996,7 +1009,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 if (nn < kD) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        o[j] = bt[j] * (Yk[(i0 + j) * kYS + nn] * exp_ftz(GL[(i0 + j) * kYS + nn]));
+                        o[j] = bt[j] * (Yk[(i0 + j) * kYS + nn] * ex2_ftz(GL[(i0 + j) * kYS + nn]));
                 } else {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) o[j] = bt[j] * Yv[(i0 + j) * kYS + nn - kD];
@@ -1097,13 +1110,6 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         }
         good = __all_sync(0xFFFFFFFFu, good && mbar_wait_bounded(bars + 3, done & 1u, kTcWaitLimit));  // warp-uniform
         tc::fence_after_sync();
-        // the operand tiles are consumed: the next item's inputs may land in the reused region
-        if (tid == 32 && good && nxt < n_items) {
-            tc::fence_smem_to_async();
-            stage(nxt);
-            staged = true;
-            staged_ph = (done + 1) & 1u;
-        }
         blk_prev = blk;
         tc::fence_before_sync();
         const bool bad = __syncthreads_or(!good);
@@ -1112,6 +1118,14 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             if (tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
             aborted = true;
             break;
+        }
+        // the operand tiles are consumed: the next item's inputs may land in the reused region
+        // (issued past the barrier, so that no other thread waits for the copies' issue)
+        if (tid == 32 && nxt < n_items) {
+            tc::fence_smem_to_async();
+            stage(nxt);
+            staged = true;
+            staged_ph = (done + 1) & 1u;
         }
         it = nxt;
     }
