@@ -682,6 +682,34 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             for (int t = 0; t < 16; ++t) Up[(col + t) * kD] = uv[t];
         }
     };
+    // 8b. an item's P (inclusive mask) from the A/P accumulator (lanes 64..127, the q rows) to its
+    //     chunk block as BF16 hi and lo parts, by the write-out warps on lane quarters 2 and 3:
+    //     warp w reads block R = 2 (w % 2) + (w / 4) % 2's segment, used by lanes 16 ((w / 4) % 2) .. +15
+    auto write_p = [&](unsigned char *b) {
+        const int qd = warp & 3, half = (warp >> 2) & 1, R = 2 * (qd & 1) + half, oR = 8 * R * (R + 1);
+        uint32_t a0[32], a1[32];
+        const uint32_t ta = tb + ((uint32_t)(32 * qd) << 16) + oR;
+        tc::tmem_ld32_nowait(ta, a0);
+        tc::tmem_ld32_nowait(ta + 32, a1);
+        tc::tmem_wait_ld();
+        if ((lane >> 4) == half) {
+            const int r = 32 * (qd - 2) + lane;
+#pragma unroll
+            for (int g8 = 0; g8 < kC / 8; ++g8) {
+                float o[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int i = 8 * g8 + t;
+                    const float pv = __uint_as_float(i < 32 ? a0[i] : a1[i - 32]);
+                    o[t] = i <= r ? pv : 0.f;
+                }
+                uint4 hi, lo;
+                split8(o, hi, lo);
+                st16(b + kOffTB + tc::kmajor_off(r, 8 * g8, kC), hi);
+                st16(b + kOffTB + tc::kmajor_off(3 * kC + r, 8 * g8, kC), lo);
+            }
+        }
+    };
     bool good = true;
     bool aborted = false;
     unsigned char *blk_prev = nullptr;  // the previous item's block: its W and U' are still in TMEM
@@ -930,17 +958,18 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         //    rows, hi parts in the q^ array (free now), lo parts in the region.
         float *Mm = reinterpret_cast<float *>(Y + kPtM), *TD = reinterpret_cast<float *>(Y + kPtD);
         unsigned char *tBh = reinterpret_cast<unsigned char *>(Yq), *tBl = Y + kPtBl, *tT = Y + kPtT;
-        if (warp < 8) {
-            // lane quarter qd holds left rows 32 qd .. +31 (k rows for qd < 2, q rows after);
-            // this warp reads block R's segment, used by lanes 16 half .. +15
+        if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {
+            // lane quarter qd < 2 holds the k rows 32 qd .. +31; this warp reads block R's
+            // segment, used by lanes 16 half .. +15 (P, on lane quarters 2 and 3, is written out
+            // later by the write-out warps, step 8)
             const int qd = warp & 3, half = warp >> 2, R = 2 * (qd & 1) + half, oR = 8 * R * (R + 1);
             uint32_t a0[32], a1[32];
             const uint32_t ta = tb + ((uint32_t)(32 * qd) << 16) + oR;
             tc::tmem_ld32_nowait(ta, a0);
             tc::tmem_ld32_nowait(ta + 32, a1);
             tc::tmem_wait_ld();
-            // columns past the segment belong to other blocks; the masks (i < r, i <= r) drop them
-            if ((lane >> 4) == half && qd < 2) {
+            // columns past the segment belong to other blocks; the mask (i < r) drops them
+            if ((lane >> 4) == half) {
                 const int r = 32 * qd + lane;
                 const float bt = sbeta[r];
 #pragma unroll
@@ -953,22 +982,6 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                         o[t] = i < r ? bt * a : 0.f;
                     }
                     reinterpret_cast<float4 *>(Mm + r * kMS)[i4] = make_float4(o[0], o[1], o[2], o[3]);
-                }
-            } else if ((lane >> 4) == half) {
-                const int r = 32 * (qd - 2) + lane;
-#pragma unroll
-                for (int g8 = 0; g8 < kC / 8; ++g8) {
-                    float o[8];
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        const int i = 8 * g8 + t;
-                        const float pv = __uint_as_float(i < 32 ? a0[i] : a1[i - 32]);
-                        o[t] = i <= r ? pv : 0.f;
-                    }
-                    uint4 hi, lo;
-                    split8(o, hi, lo);
-                    st16(blk + kOffTB + tc::kmajor_off(r, 8 * g8, kC), hi);
-                    st16(blk + kOffTB + tc::kmajor_off(3 * kC + r, 8 * g8, kC), lo);
                 }
             }
         }
@@ -1024,6 +1037,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         if (warp >= 8) {
             tc::fence_after_sync();
             if (blk_prev) write_wu(blk_prev, (warp >> 2) - 2, 2);
+            if ((warp & 3) >= 2) write_p(blk);  // this item's P
         } else {
             // 6b. T = (I + A)^-1 as BF16 hi and lo parts in the T tile, by blocks of 16 and a two-level
             //    merge, by warps 0..7 (a 256-thread named barrier between phases), from the diagonal
