@@ -919,7 +919,25 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                            kD / 2 / 16, half != 0);
                 tc::mma_commit(bars + 1);
             }
-            if (half == 0) {
+            {
+                // (K o exp(G_last - G))^T hi and lo: items u in [u0, u1) (channel c, rows 8 rb .. +7)
+                auto kdt = [&](int u0, int u1) {
+                    for (int u = u0 + tid; u < u1; u += 512) {
+                        const int c = u & (kD - 1), rb = u >> 7;
+                        const float gl = GL[(kC - 1) * kYS + c];
+                        float o[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int r = 8 * rb + j;
+                            o[j] = Yk[r * kYS + c] * ex2_ftz(gl - GL[r * kYS + c]);
+                        }
+                        uint4 hi, lo;
+                        split8(o, hi, lo);
+                        st16(blk + kOffTB + tc::kmajor_off(kC + c, 8 * rb, kC), hi);
+                        st16(blk + kOffTB + tc::kmajor_off(4 * kC + c, 8 * rb, kC), lo);
+                    }
+                };
+                if (half == 0) {
                 for (int u = tid; u < kC * (kD / 8); u += 512) {
                     const int r = (u & 7) | ((u >> 7) << 3), c0 = 8 * ((u >> 3) & 15);
                     float qv[8], gr[8], o[8];
@@ -929,22 +947,11 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                     for (int j = 0; j < 8; ++j) o[j] = qv[j] * ex2_ftz(gr[j]);
                     st16(blk + kOffTA + tc::kmajor_off(kC + r, c0, kD), pack8_bf16(o));
                 }
-            } else {
-                for (int u = tid; u < kD * (kC / 8); u += 512) {  // channel c, rows 8 rb .. +7
-                    const int c = u & (kD - 1), rb = u >> 7;
-                    const float gl = GL[(kC - 1) * kYS + c];
-                    float o[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int r = 8 * rb + j;
-                        o[j] = Yk[r * kYS + c] * ex2_ftz(gl - GL[r * kYS + c]);
-                    }
-                    uint4 hi, lo;
-                    split8(o, hi, lo);
-                    st16(blk + kOffTB + tc::kmajor_off(kC + c, 8 * rb, kC), hi);
-                    st16(blk + kOffTB + tc::kmajor_off(4 * kC + c, 8 * rb, kC), lo);
+                    kdt(0, 512);
+                } else {
+                    kdt(512, 1024);
+                    if (tid < kD) reinterpret_cast<float *>(blk + kOffGam)[tid] = ex2_ftz(GL[(kC - 1) * kYS + tid]);
                 }
-                if (tid < kD) reinterpret_cast<float *>(blk + kOffGam)[tid] = ex2_ftz(GL[(kC - 1) * kYS + tid]);
             }
         }
         good &= mbar_wait_bounded(bars + 1, 1u, kTcWaitLimit);  // second completion: half 1
