@@ -959,10 +959,10 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         if (__syncthreads_or(!good) && tid == 0) atomicExch(err, KDA_ERR_TIMEOUT);
         tc::fence_after_sync();
 
-        // 5. warps 0..7 read A and P back: A (beta and the strict mask applied) to the FP32 matrix
-        //    M, P (inclusive mask) straight to the chunk block. Then all warps build the solve
-        //    operands: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the 64 chunk
-        //    rows, hi parts in the q^ array (free now), lo parts in the region.
+        // 5. warps 0, 1, 4 and 5 read A back (beta and the strict mask applied) to the FP32 matrix M
+        //    (P stays in TMEM until the write-out warps take it, step 8b). Then warps 2..15 build the
+        //    solve operands: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the 64
+        //    chunk rows, hi parts in the q^ array (free now), lo parts in the region.
         float *Mm = reinterpret_cast<float *>(Y + kPtM), *TD = reinterpret_cast<float *>(Y + kPtD);
         unsigned char *tBh = reinterpret_cast<unsigned char *>(Yq), *tBl = Y + kPtBl, *tT = Y + kPtT;
         if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {
@@ -1021,7 +1021,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             st16(tT + tc::kmajor_off(r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
             st16(tT + tc::kmajor_off(kC + r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
         }
-        if (tid >= kC) {   // warps 2..15 (after their read-back or zero blocks) build the B operand
+        if (tid >= kC) {   // warps 2..15 (4 and 5 after their read-back, 2 and 3 after the zero blocks) build B
             for (int u = tid - kC; u < 256 * (kC / 8); u += 512 - kC) {
                 const int nn = u & 255, i0 = 8 * (u >> 8);
                 float o[8], bt[8];
