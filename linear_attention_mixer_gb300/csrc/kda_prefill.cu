@@ -1021,8 +1021,8 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             st16(tT + tc::kmajor_off(r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
             st16(tT + tc::kmajor_off(kC + r, 8 * g, kC), make_uint4(0u, 0u, 0u, 0u));
         }
-        if (tid >= kC) {   // warps 2..15 (4 and 5 after their read-back, 2 and 3 after the zero blocks) build B
-            for (int u = tid - kC; u < 256 * (kC / 8); u += 512 - kC) {
+        if (tid >= kC && (warp < 4 || warp >= 6)) {  // warps 2, 3 (after the zero blocks) and 6..15 build B
+            for (int u = warp < 4 ? tid - kC : tid - 2 * kC; u < 256 * (kC / 8); u += 512 - 2 * kC) {
                 const int nn = u & 255, i0 = 8 * (u >> 8);
                 float o[8], bt[8];
                 ld8f(sbeta + i0, bt);
