@@ -913,7 +913,9 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
             tc::fence_before_sync();
             __syncthreads();
             tc::fence_after_sync();
-            if (tid == 0) {
+            // (issued by a thread of warp 12, whose rows have the fewest right segments, so that the
+            // issue time does not lengthen the most loaded warps' shadow work)
+            if (tid == 384) {
                 mma_split3(tb, tc::kmajor_desc(tLh, 0, kD / 2), tc::kmajor_desc(tLl, 0, kD / 2),
                            tc::kmajor_desc(tRh, 0, kD / 2), tc::kmajor_desc(tRl, 0, kD / 2), tc::idesc_bf16(128, kApN),
                            kD / 2 / 16, half != 0);
