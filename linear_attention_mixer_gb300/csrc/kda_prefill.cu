@@ -962,15 +962,15 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         tc::fence_after_sync();
 
         // 5. warps 0, 1, 4 and 5 read A back (beta and the strict mask applied) to the FP32 matrix M
-        //    (P stays in TMEM until the write-out warps take it, step 8b). Then warps 2..15 build the
-        //    solve operands: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T, K = the 64
-        //    chunk rows, hi parts in the q^ array (free now), lo parts in the region.
+        //    (P stays in TMEM until the write-out warps take it, step 8b). Then warps 2, 3 and 6..15
+        //    build the solve operands: rows 0..127 (beta K o exp(G))^T, rows 128..255 (beta V)^T,
+        //    K = the 64 chunk rows, hi parts in the q^ array (free now), lo parts in the region.
         float *Mm = reinterpret_cast<float *>(Y + kPtM), *TD = reinterpret_cast<float *>(Y + kPtD);
         unsigned char *tBh = reinterpret_cast<unsigned char *>(Yq), *tBl = Y + kPtBl, *tT = Y + kPtT;
         if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {
             // lane quarter qd < 2 holds the k rows 32 qd .. +31; this warp reads block R's
             // segment, used by lanes 16 half .. +15 (P, on lane quarters 2 and 3, is written out
-            // later by the write-out warps, step 8)
+            // later by the write-out warps, step 8b)
             const int qd = warp & 3, half = warp >> 2, R = 2 * (qd & 1) + half, oR = 8 * R * (R + 1);
             uint32_t a0[32], a1[32];
             const uint32_t ta = tb + ((uint32_t)(32 * qd) << 16) + oR;
