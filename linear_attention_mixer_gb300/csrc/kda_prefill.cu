@@ -898,13 +898,28 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
                 split8(ql, hi, lo);
                 st16(tLh + tc::kmajor_off(kC + r, cl, kD / 2), hi);
                 st16(tLl + tc::kmajor_off(kC + r, cl, kD / 2), lo);
-                for (int R = b; R < kC / kBlk; ++R) {  // warp-uniform: a warp's 8 rows share a block
+                // block 0's rows have four segments and block 3's one: block 0's last segment (R = 3)
+                // is built by the block-3 threads, each for the block-0 row 48 rows above its own
+                const int R_end = b == 0 ? kC / kBlk - 1 : kC / kBlk;
+                for (int R = b; R < R_end; ++R) {  // warp-uniform: a warp's 8 rows share a block
                     if (R != b) ld8f(GL + kBlk * R * kYS + c0, gn);
                     float kx[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) kx[j] = kv[j] * ex2_ftz(gn[j] - gr[j]);
                     split8(kx, hi, lo);
                     const int row = 8 * R * (R + 1) + r;
+                    st16(tRh + tc::kmajor_off(row, cl, kD / 2), hi);
+                    st16(tRl + tc::kmajor_off(row, cl, kD / 2), lo);
+                }
+                if (b == kC / kBlk - 1) {  // gn holds G_48 here
+                    const int r0 = r - kBlk * (kC / kBlk - 1);
+                    float k0[8], g0[8], kx[8];
+                    ld8f(Yk + r0 * kYS + c0, k0);
+                    ld8f(GL + r0 * kYS + c0, g0);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) kx[j] = k0[j] * ex2_ftz(gn[j] - g0[j]);
+                    split8(kx, hi, lo);
+                    const int row = 8 * (kC / kBlk - 1) * (kC / kBlk) + r0;
                     st16(tRh + tc::kmajor_off(row, cl, kD / 2), hi);
                     st16(tRl + tc::kmajor_off(row, cl, kD / 2), lo);
                 }
