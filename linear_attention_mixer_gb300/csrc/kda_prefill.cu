@@ -1060,7 +1060,7 @@ prep_tc_kernel(const float *__restrict__ conv_w, const float *__restrict__ dt_bi
         __syncthreads();
         if (warp >= 8) {
             tc::fence_after_sync();
-            __nanosleep(400);  // let the merge's first shared-memory loads go ahead of the write-out's stores
+            __nanosleep(300);  // let the merge's first shared-memory loads go ahead of the write-out's stores
             if (blk_prev) write_wu(blk_prev, (warp >> 2) - 2, 2);
             if ((warp & 3) >= 2) write_p(blk);  // this item's P
         } else {
